@@ -1,0 +1,381 @@
+"""Benchmark: causal-adjusted attention forward TFLOP/s on one GB300 (per rank).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+One step is one pass of the whole hot path (``ra_ring_sim_fwd`` for the workload's ring
+size: attention steps, causal tile skipping and the in-kernel LSE merge) over one
+batch of seeded synthetic inputs resident in HBM.  Each timed step is bracketed by CUDA
+events on the launching stream; between steps a 256 MiB buffer (larger than the 129 MB
+L2) is rewritten to flush L2.  ``value`` = FLOPs of all steps of all ranks / the slowest
+rank's summed step time.  Under torchrun every rank runs an independent replica (no data
+exchange), so scaling is weak.
+
+``--impl reference`` times the oracle (plain fp64 C, all host cores) on a bounded sample
+of the same workload and prints the same JSON shape with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+DEFAULT_WORKLOAD = "dense_causal_b2h32n4k"
+METRIC = "attention fwd TFLOP/s (causal-adjusted) and % of GB300 dense BF16 peak"
+PROFILE_JSON = os.path.join(ROOT, "profiles", "attn_tc_dense_causal_b2h32n4k.json")
+KERNEL_SRC = os.path.join(ROOT, "exact_long_context_gb300", "csrc", "attn_tc.cu")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p.get("bf16_tflops", 1900.0), p.get("hbm_gbs", 6800.0), "measured"
+    return 1900.0, 6800.0, "fallback"
+
+
+def kernel_hash():
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic():
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary, if
+    that summary was taken on the current kernel source; else None."""
+    try:
+        with open(PROFILE_JSON) as f:
+            prof = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if prof.get("kernel_src_sha256_16") != kernel_hash():
+        return None
+    return prof.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons, sampled during the timed region."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines: list[tuple[float, str]] = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.dev)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append((ts, parts))
+        inside = [p for ts, p in rows if self.t0 is not None and self.t0 - 0.15 <= ts <= self.t1 + 0.15]
+        use = inside if inside else rows[-3:]
+        if not use:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+
+        sm = [num(p[2]) for p in use]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in use:
+            for name, val in zip(names, p[6:10]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(num(p[3]) for p in use),
+                "reasons": sorted(reasons), "samples": len(use),
+                "power_w_max": max(num(p[4]) for p in use)}
+
+
+def run_ours(args, w, ws, rank, local):
+    from exact_long_context_gb300 import ra, synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    q, k, v = synth.workload_inputs(w, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=dev)
+    need = ra.ring_sim_workspace_bytes(q, w.ring_size)
+    wsbuf = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ra.ring_sim_fwd(q, k, v, w.ring_size, w.layout, causal=w.causal, scale=w.scale, o=o,
+                        lse=lse, workspace=wsbuf if need else None, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    ra.check(stream)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = ra.launch_count()
+    clocks.mark("t0")
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    clocks.mark("t1")
+    if ws > 1:
+        torch.distributed.barrier()
+    launches = ra.launch_count() - launches0
+    ra.check(stream)
+    clk = clocks.stop()
+    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = float(sum(times))
+    if ws > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    flops = w.flops()
+    value = flops * args.steps * ws / (total_ms * 1e-3) / 1e12
+    launches_per_step = launches / args.steps
+
+    # end to end through the public call: pinned host inputs -> device -> host result
+    e2e = None
+    if args.e2e_steps > 0:
+        hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            ra.ring_sim_fwd(dq, dk, dv, w.ring_size, w.layout, causal=w.causal, scale=w.scale,
+                            o=o, lse=lse, workspace=wsbuf if need else None, stream=stream)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        etot = 0.0
+        for _ in range(args.e2e_steps):
+            flush.zero_()
+            es.record(stream)
+            e2e_step()
+            ee.record(stream)
+            ee.synchronize()
+            etot += es.elapsed_time(ee)
+        ra.check(stream)
+        if ws > 1:
+            t = torch.tensor([etot], dtype=torch.float64, device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            etot = float(t.item())
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+        e2e = {"value": round(flops * args.e2e_steps * ws / (etot * 1e-3) / 1e12, 2),
+               "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(etot / args.e2e_steps, 4)}
+
+    peak_tf, _, peak_kind = peaks()
+    # dominant kernel: the attention launches (all launches of a step are attention
+    # launches; per-launch FLOPs = step FLOPs / launches per step)
+    per_launch_flops = flops / max(1.0, launches_per_step)
+    per_launch_ms = ms_per_step / max(1.0, launches_per_step)
+    achieved = per_launch_flops / (per_launch_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf,
+                "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4),
+                "traffic": profiled_traffic(), "peak_kind": peak_kind}
+    return {
+        "value": round(value, 2), "ms_per_step": round(ms_per_step, 5), "e2e": e2e,
+        "roofline": roofline, "clocks": clk, "gpu_launches": launches,
+        "wall_s_timed_region": round(wall, 4),
+        "tokens_per_s": round(w.B * w.N * args.steps * ws / (total_ms * 1e-3), 1),
+    }
+
+
+def oracle_rate_sample(w, budget_s, seed=0):
+    """Time the oracle on rows sampled from the workload; returns (flops, seconds, rows, threads)."""
+    import oracle
+    from exact_long_context_gb300 import synth
+
+    q, k, v = synth.workload_inputs(w, device="cpu")
+
+    def enc(t):
+        t = t.contiguous()
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).numpy().view(np.uint16)
+        return t.numpy()
+
+    qn, kn, vn = enc(q), enc(k), enc(v)
+    threads = oracle.default_threads()
+    rng = np.random.default_rng(seed)
+
+    def rows_for(n):
+        b = rng.integers(0, w.B, n)
+        h = rng.integers(0, w.Hq, n)
+        i = rng.integers(0, w.N, n)
+        return np.stack([b, h, i], 1).astype(np.int64)
+
+    def flops_of(rows):
+        vis = (rows[:, 2] + 1) if w.causal else np.full(len(rows), w.N)
+        return float(np.sum(vis)) * 4.0 * w.D
+
+    # calibrate on a small batch, then size the timed sample to the budget
+    cal = rows_for(max(threads, 8))
+    t0 = time.perf_counter()
+    oracle.attention(qn, kn, vn, w.causal, w.scale, rows=cal, nthreads=threads)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    per_row = dt / len(cal)
+    n = int(max(threads, min(200000, budget_s / per_row)))
+    rows = rows_for(n)
+    t0 = time.perf_counter()
+    oracle.attention(qn, kn, vn, w.causal, w.scale, rows=rows, nthreads=threads)
+    sec = time.perf_counter() - t0
+    return flops_of(rows), sec, len(rows), threads
+
+
+def run_reference(args, w, ws, rank):
+    """The oracle as it stands, on the host cores, a bounded sample per step."""
+    if rank != 0:
+        return None
+    per_step = max(0.05, min(2.0, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_rate_sample(w, per_step, seed=1)
+    tf = tsec = 0.0
+    nrows = 0
+    threads = 1
+    for i in range(args.steps):
+        f, s, n, threads = oracle_rate_sample(w, per_step, seed=100 + i)
+        tf += f
+        tsec += s
+        nrows += n
+    value = tf / tsec / 1e12
+    sample = (f"{nrows} uniformly random query rows of {w.name} over {args.steps} steps "
+              f"(fp64 oracle, causal-adjusted FLOPs of the rows' visible keys)")
+    return {"value": round(value, 6), "ms_per_step": round(tsec / args.steps * 1e3, 3),
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    from exact_long_context_gb300 import synth
+
+    w = synth.WORKLOADS[args.workload]
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.distributed.init_process_group("nccl" if args.impl == "ours" else "gloo")
+
+    config = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "D": w.D,
+              "causal": w.causal, "ring_size": w.ring_size, "layout": w.layout,
+              "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{ws}"}
+    line = {"metric": METRIC, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
+            "data": "synthetic (seeded N(0,1), rounded to bf16)", "config": config}
+
+    if args.impl == "reference":
+        res = run_reference(args, w, ws, rank)
+        if ws > 1:
+            torch.distributed.barrier()
+        if res is None:
+            return
+        line.update(res)
+        line["impl"] = "reference"
+        print(json.dumps(line), flush=True)
+        return
+
+    res = run_ours(args, w, ws, rank, local)
+    if rank == 0:
+        line.update(res)
+        line["pct_of_peak"] = round(100 * res["roofline"]["frac"], 2)
+        f, sec, nrows, threads = oracle_rate_sample(w, args.cpu_budget_s)
+        line["cpu_baseline"] = {
+            "value": round(f / sec / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{nrows} uniformly random query rows of {w.name} (fp64 oracle, "
+                      f"{sec:.1f} s wall)"}
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,737 @@
+// attn_tc.cu - exact attention on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// One CTA owns a block of 256 query rows of one (batch, head) - two 128-row halves -
+// and streams the key/value tiles of its ring-step segment through shared memory.
+//
+//   warp 0        TMA producer: Q halves once, then K_t, V_t tiles into a ring of slots
+//   warp 1        MMA issuer (one lane) and tensor-memory owner:
+//                   S_h = Q_h K_t^T      (tcgen05.mma, A and B from shared memory)
+//                   O_h += P_h V_t       (tcgen05.mma, A = P from tensor memory)
+//   warps 4-7     softmax of half 0, one thread per query row
+//   warps 8-11    softmax of half 1
+//
+// Tensor memory (512 columns x 128 lanes x 32 bit): S_0 | S_1 | O_0 | O_1.  The bf16
+// P_h overwrites the first 64 columns of S_h once the softmax threads hold S_h in
+// registers; the next S_h is issued after the P_h V MMA, and tcgen05 MMAs of one
+// thread run in issue order.
+//
+// The arithmetic per query row is the online softmax of "Ring Attention explained"
+// (guijiagi.com), section "在线 Softmax 算法" - running max, running sum, rescaled
+// unnormalised output - in log2 units (scale * log2 e folded into one FFMA before
+// exp2), with the normalisation deferred to the end ("第12章 FlashAttention原理与实现",
+// FlashAttention-2 paragraph).  The running max is only moved when a tile's max
+// exceeds it by more than 2^8; the final O / l and LSE are the same quantities for
+// any reference value, and this skips most rescales of O.
+//
+// Causality is decided per 128x128 tile on global positions: tiles entirely after
+// the half's last row are never issued, tiles that straddle the diagonal or a key
+// range end are masked element-wise (key j visible to row i iff j <= i: the block
+// classes of the `ring_attention_causal_step` listing of "Ring Attention 论文解析").
+//
+// Epilogue (per row): O / l and LSE = ln sum exp, then, by segment flags, a direct
+// write, or the log-sum-exp merge of the Twinkle page's `update_out_and_lse` into the
+// float32 running output - so a ring step's partial never goes to HBM unnormalised.
+//
+// Every mbarrier wait is bounded (globaltimer).  On a timeout the CTA records
+// DERR_TIMEOUT in the device error word, every role stops, waits (bounded) for its
+// own copies and MMAs in flight, and the tensor memory is released before exit.
+#include <cuda.h>
+
+#include "ra_internal.cuh"
+
+namespace ra {
+namespace tc {
+
+constexpr int BM = 128;  // query rows per half (MMA M)
+constexpr int BN = 128;  // keys per tile
+constexpr int kThreads = 384;
+constexpr float kRescaleThreshold = 8.0f;      // log2 units
+constexpr int64_t kDrainLimitNs = 1000000000;  // bound on waiting for own async work
+
+template <int HD>
+struct Cfg {
+    static constexpr int SLABS = HD / 64;          // 128-byte column slabs per tile row
+    static constexpr int TILE_BYTES = 128 * HD * 2;  // one Q half or one K/V tile (bf16)
+    static constexpr int SLAB_BYTES = 128 * 128;     // 128 rows x 128 bytes
+    static constexpr int NSLOT = (HD == 128) ? 4 : 8;
+    static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + HD;
+    static constexpr uint32_t TM_COLS = 512;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM_BYTES = 1024 + (2 + NSLOT) * TILE_BYTES + BAR_BYTES;
+};
+
+struct Bars {
+    uint64_t q_full;
+    uint64_t full[8];
+    uint64_t empty[8];
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t o_full[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int32_t abort;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of parity `parity` of `bar` to complete.  Returns false if the
+// CTA is aborting (this wait exceeded `limit_ns`, or another role gave up first).
+__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int32_t *abort,
+                                        int64_t limit_ns, int *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if ((int64_t)(globaltimer() - t0) > limit_ns) {
+            record_error(err, DERR_TIMEOUT);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+// Bounded wait used only while winding down (own copies / MMAs in flight).
+__device__ __noinline__ void wait_phase_drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if ((int64_t)(globaltimer() - t0) > kDrainLimitNs) return;
+    }
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     dst_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 layout: start address,
+// leading and stride byte offsets in 16-byte units, descriptor version 1 at bit 46,
+// swizzle mode 2 = 128B at bits 61-63).  Tiles are 1024-byte aligned, so the
+// base-offset field stays 0.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor for kind::f16: f32 accumulator (bits 4-5 = 1), A and B bf16
+// (bits 7-9 and 10-12 = 1), B major-ness at bit 16 (1 = MN-major), N >> 3 at bits
+// 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+#define RA_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
+                 "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+#define RA_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), \
+                 "r"(r[i + 4]), "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
+
+// 32 consecutive 32-bit columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : RA_R8(0), RA_R8(8), RA_R8(16), RA_R8(24)
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        RA_W8(0), RA_W8(8), RA_W8(16), RA_W8(24)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// ---------------------------------------------------------------- tile bookkeeping
+
+struct KTiles {
+    int k0[2], k1[2];
+    int nt0, ntot;
+    __device__ __forceinline__ int start(int t) const {
+        return t < nt0 ? k0[0] + BN * t : k0[1] + BN * (t - nt0);
+    }
+    __device__ __forceinline__ int range_end(int t) const { return t < nt0 ? k1[0] : k1[1]; }
+    // Number of leading tiles whose first key is <= last_row (the tiles some row
+    // <= last_row can see under causality).
+    __device__ __forceinline__ int visible_prefix(int last_row) const {
+        int c = 0;
+        if (last_row >= k0[0]) c += min(nt0, (last_row - k0[0]) / BN + 1);
+        if (ntot > nt0 && last_row >= k0[1]) c += min(ntot - nt0, (last_row - k0[1]) / BN + 1);
+        return c;
+    }
+};
+
+// ---------------------------------------------------------------- the kernel
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ StepParams P) {
+    using C = Cfg<HD>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *base_ptr = smem_raw + (base - raw);
+    const uint32_t sQ = base;
+    const uint32_t sKV = base + 2 * C::TILE_BYTES;
+    Bars *bars = reinterpret_cast<Bars *>(base_ptr + (2 + C::NSLOT) * C::TILE_BYTES);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ---- work decode (uniform over the CTA)
+    const int bh = blockIdx.x;
+    const int b = bh / P.Hq, h = bh - (bh / P.Hq) * P.Hq;
+    const int hk = h / (P.Hq / P.Hkv);
+    int si, lb;
+    decode_work(P, blockIdx.y, si, lb);
+    if (lb < 0) return;
+    const Seg &S = P.seg[si];
+    const int qrow0 = S.q0 + lb * 2 * BM;
+    KTiles kt;
+    kt.k0[0] = S.k0[0];
+    kt.k1[0] = S.k1[0];
+    kt.k0[1] = S.k0[1];
+    kt.k1[1] = S.k1[1];
+    kt.nt0 = (S.k1[0] > S.k0[0]) ? (S.k1[0] - S.k0[0] + BN - 1) / BN : 0;
+    kt.ntot = kt.nt0 + ((S.k1[1] > S.k0[1]) ? (S.k1[1] - S.k0[1] + BN - 1) / BN : 0);
+    int nh[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const int r0 = qrow0 + hh * BM;
+        if (r0 >= S.q1) {
+            nh[hh] = 0;
+        } else if (!P.causal) {
+            nh[hh] = kt.ntot;
+        } else {
+            nh[hh] = kt.visible_prefix(min(r0 + BM, S.q1) - 1);
+        }
+    }
+    const int nmax = max(nh[0], nh[1]);
+    if (nmax == 0) return;
+
+    const uint32_t b_q = smem_u32(&bars->q_full);
+    const uint32_t b_drain = smem_u32(&bars->drain);
+    volatile int32_t *abort_flag = &bars->abort;
+
+    // ---- set-up
+    if (threadIdx.x == 0) {
+        bars->abort = 0;
+        mbar_init(b_q, 1);
+#pragma unroll
+        for (int s = 0; s < C::NSLOT; ++s) {
+            mbar_init(smem_u32(&bars->full[s]), 1);
+            mbar_init(smem_u32(&bars->empty[s]), 1);
+        }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            mbar_init(smem_u32(&bars->s_full[hh]), 1);
+            mbar_init(smem_u32(&bars->p_full[hh]), 128);
+            mbar_init(smem_u32(&bars->o_full[hh]), 1);
+        }
+        mbar_init(b_drain, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) tmem_alloc(smem_u32(&bars->tmem_base), C::TM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == 0) {
+        // ================= TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_expect_tx(b_q, 2 * C::TILE_BYTES);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int c = 0; c < C::SLABS; ++c)
+                    tma_load_4d(sQ + hh * C::TILE_BYTES + c * C::SLAB_BYTES, &tm_q, b_q, c * 64,
+                                qrow0 + hh * BM, h, b);
+            int slot = 0;
+            uint32_t ph = 0;
+            uint32_t issued = 0, last_ph = 0;  // per-slot bit sets
+            bool ok = true;
+            for (int t = 0; t < nmax && ok; ++t) {
+                const int ks = kt.start(t);
+#pragma unroll 1
+                for (int which = 0; which < 2; ++which) {
+                    const uint32_t b_empty = smem_u32(&bars->empty[slot]);
+                    const uint32_t b_full = smem_u32(&bars->full[slot]);
+                    if (!wait_phase(b_empty, ph ^ 1u, abort_flag, P.wait_limit_ns, P.err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(b_full, C::TILE_BYTES);
+                    const CUtensorMap *m = which ? &tm_v : &tm_k;
+#pragma unroll
+                    for (int c = 0; c < C::SLABS; ++c)
+                        tma_load_4d(sKV + slot * C::TILE_BYTES + c * C::SLAB_BYTES, m, b_full,
+                                    c * 64, ks, hk, b);
+                    issued |= 1u << slot;
+                    last_ph = (last_ph & ~(1u << slot)) | (ph << slot);
+                    if (++slot == C::NSLOT) {
+                        slot = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {  // wind down: let every copy this thread issued land
+                wait_phase_drain(b_q, 0);
+                for (int s = 0; s < C::NSLOT; ++s)
+                    if (issued & (1u << s))
+                        wait_phase_drain(smem_u32(&bars->full[s]), (last_ph >> s) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false);
+            constexpr uint32_t IDESC_PV = idesc_bf16(BM, HD, true);
+            auto issue_qk = [&](int hh, int kslot) {
+                const uint32_t d = tmem + (hh ? C::TM_S1 : C::TM_S0);
+                const uint32_t qa = sQ + hh * C::TILE_BYTES;
+                const uint32_t kb = sKV + kslot * C::TILE_BYTES;
+#pragma unroll
+                for (int k = 0; k < HD / 16; ++k) {
+                    const uint32_t off = (k >> 2) * C::SLAB_BYTES + (k & 3) * 32;
+                    mma_ss(d, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                           IDESC_QK, k > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int hh, int vslot, bool acc_in) {
+                const uint32_t d = tmem + (hh ? C::TM_O1 : C::TM_O0);
+                const uint32_t p = tmem + (hh ? C::TM_S1 : C::TM_S0);
+                const uint32_t vb = sKV + vslot * C::TILE_BYTES;
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k) {
+                    mma_ts(d, p + k * 8, sdesc_sw128(vb + k * 16 * 128, C::SLAB_BYTES, 1024),
+                           IDESC_PV, (acc_in || k > 0) ? 1u : 0u);
+                }
+            };
+            bool ok = wait_phase(b_q, 0, abort_flag, P.wait_limit_ns, P.err);
+            int slot = 0;
+            uint32_t ph = 0;
+            if (ok) {
+                tc_fence_after();
+                ok = wait_phase(smem_u32(&bars->full[slot]), ph, abort_flag, P.wait_limit_ns, P.err);
+            }
+            if (ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+                    if (nh[hh] > 0) {
+                        issue_qk(hh, slot);
+                        mma_commit(smem_u32(&bars->s_full[hh]));
+                    }
+                mma_commit(smem_u32(&bars->empty[slot]));
+                if (++slot == C::NSLOT) {
+                    slot = 0;
+                    ph ^= 1u;
+                }
+            }
+            for (int t = 0; ok && t < nmax; ++t) {
+                const int vslot = slot;
+                ok = wait_phase(smem_u32(&bars->full[vslot]), ph, abort_flag, P.wait_limit_ns,
+                                P.err);
+                if (!ok) break;
+                if (++slot == C::NSLOT) {
+                    slot = 0;
+                    ph ^= 1u;
+                }
+                const bool has_next = t + 1 < nmax;
+                const int kslot = slot;
+                if (has_next) {
+                    ok = wait_phase(smem_u32(&bars->full[kslot]), ph, abort_flag, P.wait_limit_ns,
+                                    P.err);
+                    if (!ok) break;
+                    if (++slot == C::NSLOT) {
+                        slot = 0;
+                        ph ^= 1u;
+                    }
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (t < nh[hh]) {
+                        ok = wait_phase(smem_u32(&bars->p_full[hh]), (uint32_t)(t & 1), abort_flag,
+                                        P.wait_limit_ns, P.err);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv(hh, vslot, t > 0);
+                        if (t + 1 < nh[hh]) {
+                            issue_qk(hh, kslot);
+                            mma_commit(smem_u32(&bars->s_full[hh]));
+                        } else {
+                            mma_commit(smem_u32(&bars->o_full[hh]));
+                        }
+                    }
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&bars->empty[vslot]));
+                if (has_next) mma_commit(smem_u32(&bars->empty[kslot]));
+            }
+            // every MMA this thread issued completes before tensor memory is released
+            mma_commit(b_drain);
+            wait_phase_drain(b_drain, 0);
+        }
+    } else if (warp >= 4) {
+        // ================= softmax (+ O rescale and epilogue) of one half
+        const int hh = (warp - 4) >> 2;
+        const int quarter = warp & 3;
+        const int row_g = qrow0 + hh * BM + quarter * 32 + lane;
+        const int n = nh[hh];
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tS = tmem + (hh ? C::TM_S1 : C::TM_S0) + lane_off;
+        const uint32_t tO = tmem + (hh ? C::TM_O1 : C::TM_O0) + lane_off;
+        const uint32_t b_s = smem_u32(&bars->s_full[hh]);
+        const uint32_t b_p = smem_u32(&bars->p_full[hh]);
+        const float sl2 = P.scale_log2;
+        const int first_row = qrow0 + hh * BM;
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int t = 0; t < n; ++t) {
+            ok = wait_phase(b_s, (uint32_t)(t & 1), abort_flag, P.wait_limit_ns, P.err);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t r[4][32];
+            tmem_ld32(tS + 0, r[0]);
+            tmem_ld32(tS + 32, r[1]);
+            tmem_ld32(tS + 64, r[2]);
+            tmem_ld32(tS + 96, r[3]);
+            tmem_ld_wait();
+            const int ks = kt.start(t);
+            const int ke = kt.range_end(t);
+            const bool need_mask =
+                (ks + BN > ke) || (P.causal && (min(ks + BN, ke) - 1 > first_row));
+            if (need_mask) {
+                const int lim = (P.causal ? min(ke, row_g + 1) : ke) - ks;
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (c >= lim) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+            }
+            float mx = __uint_as_float(r[0][0]);
+#pragma unroll
+            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(r[c >> 5][c & 31]));
+            const float m_tile = mx * sl2;
+            float alpha = 1.f;
+            bool resc = false;
+            if (t == 0) {
+                m_ref = m_tile;
+            } else if (m_tile > m_ref + kRescaleThreshold) {
+                alpha = ex2(m_ref - m_tile);
+                m_ref = m_tile;
+                resc = true;
+            }
+            const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            float rs = 0.f;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int c = j * 64 + 2 * i;
+                    const float p0 = ex2(fmaf(__uint_as_float(r[c >> 5][c & 31]), sl2, neg_m));
+                    const float p1 =
+                        ex2(fmaf(__uint_as_float(r[(c + 1) >> 5][(c + 1) & 31]), sl2, neg_m));
+                    rs += p0 + p1;
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(tS + j * 32, pk);
+            }
+            l = l * alpha + rs;
+            if (t > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+                for (int c = 0; c < HD / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c * 32, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(tO + c * 32, o);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(b_p);
+        }
+        if (ok && n > 0) {
+            ok = wait_phase(smem_u32(&bars->o_full[hh]), 0, abort_flag, P.wait_limit_ns, P.err);
+            if (ok) {
+                tc_fence_after();
+                const bool valid = row_g < S.q1;
+                const bool have = l > 0.f;
+                const float lse_b = have ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+                const float inv = have ? 1.f / l : 0.f;
+                const int64_t lrow = ((int64_t)b * P.Hq + h) * P.N + row_g;
+                const bool first = (S.flags & SEG_FIRST) != 0;
+                const bool final_ = (S.flags & SEG_FINAL) != 0;
+                MergeW w;
+                w.wa = 0.f;
+                w.wb = 1.f;
+                w.L = lse_b;
+                if (valid && !first) w = merge_weights(P.lse[lrow], lse_b);
+                const float wb = w.wb * inv;
+                __nv_bfloat16 *orow =
+                    static_cast<__nv_bfloat16 *>(P.o) + (int64_t)b * P.so[0] +
+                    (int64_t)h * P.so[1] + (int64_t)row_g * P.so[2];
+                float *arow = P.oacc ? P.oacc + lrow * HD : nullptr;
+#pragma unroll 1
+                for (int c = 0; c < HD / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c * 32, o);
+                    tmem_ld_wait();
+                    if (!valid) continue;
+                    float x[32];
+                    if (!first && w.wa != 0.f) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 a = *reinterpret_cast<const float4 *>(arow + c * 32 + i);
+                            x[i] = w.wa * a.x;
+                            x[i + 1] = w.wa * a.y;
+                            x[i + 2] = w.wa * a.z;
+                            x[i + 3] = w.wa * a.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) x[i] = 0.f;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[i] = fmaf(wb, __uint_as_float(o[i]), x[i]);
+                    if (final_) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 8) {
+                            uint4 u;
+                            u.x = pack_bf16x2(x[i], x[i + 1]);
+                            u.y = pack_bf16x2(x[i + 2], x[i + 3]);
+                            u.z = pack_bf16x2(x[i + 4], x[i + 5]);
+                            u.w = pack_bf16x2(x[i + 6], x[i + 7]);
+                            *reinterpret_cast<uint4 *>(orow + c * 32 + i) = u;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4 *>(arow + c * 32 + i) =
+                                make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+                    }
+                }
+                if (valid) P.lse[lrow] = first ? lse_b : w.L;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
+}
+
+// One block, one thread: a bounded wait on a barrier nothing completes.
+__global__ void wait_selftest_kernel(int64_t limit_ns, int *err) {
+    __shared__ uint64_t bar;
+    __shared__ int32_t abort;
+    if (threadIdx.x != 0) return;
+    abort = 0;
+    mbar_init(smem_u32(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    wait_phase(smem_u32(&bar), 0, &abort, limit_ns, err);
+}
+
+}  // namespace tc
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// [B, H, N, D] bf16 with element strides s[0..2] (D contiguous) as a 4-D tiled map
+// (dims D, N, H, B), box 64 x 128 rows, 128-byte swizzle.
+static bool encode_map(CUtensorMap *map, const void *ptr, int64_t B, int64_t H, int64_t N,
+                       int64_t D, const int64_t *s) {
+    EncodeTiledFn fn = get_encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)s[2] * 2, (cuuint64_t)s[1] * 2, (cuuint64_t)s[0] * 2};
+    cuuint32_t box[4] = {64, 128, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int HD>
+static cudaError_t launch_tc_hd(const StepParams &P, int blocks_y, cudaStream_t stream) {
+    using C = tc::Cfg<HD>;
+    static int configured_mask = 0;  // per device ordinal bit (devices < 32)
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!(configured_mask & (1 << (dev & 31)))) {
+        cudaError_t e = cudaFuncSetAttribute(tc::attn_tc_kernel<HD>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured_mask |= 1 << (dev & 31);
+    }
+    CUtensorMap mq, mk, mv;
+    if (!encode_map(&mq, P.q, P.B, P.Hq, P.N, P.D, P.sq) ||
+        !encode_map(&mk, P.k, P.B, P.Hkv, P.N, P.D, P.sk) ||
+        !encode_map(&mv, P.v, P.B, P.Hkv, P.N, P.D, P.sv))
+        return cudaErrorInvalidValue;
+    dim3 grid(P.B * P.Hq, blocks_y);
+    tc::attn_tc_kernel<HD><<<grid, tc::kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, P);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attn_tc(const StepParams &P, int blocks_y, cudaStream_t stream) {
+    if (blocks_y <= 0 || P.B * P.Hq <= 0) return cudaSuccess;
+    if (P.D == 128) return launch_tc_hd<128>(P, blocks_y, stream);
+    if (P.D == 64) return launch_tc_hd<64>(P, blocks_y, stream);
+    return cudaErrorInvalidValue;
+}
+
+int attn_tc_rows_per_block() { return 2 * tc::BM; }
+
+cudaError_t launch_wait_selftest(int64_t limit_ns, int *err, cudaStream_t stream) {
+    tc::wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns, err);
+    return cudaGetLastError();
+}
+
+}  // namespace ra

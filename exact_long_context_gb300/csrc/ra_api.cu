@@ -1,0 +1,450 @@
+// ra_api.cu - the C ABI of libra: argument checks, the ring schedule, kernel dispatch,
+// the device error word.
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "ra_internal.cuh"
+
+namespace ra {
+cudaError_t launch_attn_simt(const StepParams &P, int blocks_y, cudaStream_t stream);
+cudaError_t launch_attn_tc(const StepParams &P, int blocks_y, cudaStream_t stream);
+int attn_tc_rows_per_block();
+cudaError_t launch_wait_selftest(int64_t limit_ns, int *err, cudaStream_t stream);
+
+cudaError_t launch_lse_merge(const MergeParams &P, int num_sms, cudaStream_t stream);
+}  // namespace ra
+
+using namespace ra;
+
+// ---------------------------------------------------------------- error state
+
+static thread_local std::string t_last_error;
+static thread_local int64_t t_launches = 0;
+
+static ra_status fail(ra_status s, const std::string &msg) {
+    t_last_error = msg;
+    return s;
+}
+
+static ra_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(RA_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+__device__ int g_device_error;
+
+static const int kMaxDev = 64;
+static std::mutex g_mu;
+static int *g_err_ptr[kMaxDev];
+static int g_num_sms[kMaxDev];
+static int64_t g_wait_limit_ns = 2000000000LL;
+
+struct DevInfo {
+    int dev;
+    int *err;
+    int sms;
+    bool tc_ok;
+};
+
+static bool device_info(DevInfo &d, std::string &msg) {
+    if (cudaGetDevice(&d.dev) != cudaSuccess || d.dev < 0 || d.dev >= kMaxDev) {
+        msg = "no current CUDA device";
+        cudaGetLastError();
+        return false;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[d.dev]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_device_error);
+        if (e != cudaSuccess) {
+            msg = std::string("cudaGetSymbolAddress(error word): ") + cudaGetErrorString(e);
+            return false;
+        }
+        int sms = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d.dev);
+        g_num_sms[d.dev] = sms > 0 ? sms : 1;
+        g_err_ptr[d.dev] = static_cast<int *>(p);
+    }
+    d.err = g_err_ptr[d.dev];
+    d.sms = g_num_sms[d.dev];
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, d.dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, d.dev);
+    d.tc_ok = (major == 10 && minor == 3);
+    return true;
+}
+
+// ---------------------------------------------------------------- argument checks
+
+static bool is_dtype(int32_t d) { return d == RA_F32 || d == RA_BF16; }
+static int esize(int32_t d) { return d == RA_F32 ? 4 : 2; }
+
+static ra_status check_tensor(const ra_tensor *t, const char *name) {
+    if (!t) return fail(RA_ERR_INVALID_ARG, std::string(name) + " is NULL");
+    if (!is_dtype(t->dtype)) return fail(RA_ERR_INVALID_ARG, std::string(name) + ": bad dtype");
+    for (int i = 0; i < 4; ++i)
+        if (t->shape[i] < 0) return fail(RA_ERR_INVALID_ARG, std::string(name) + ": negative shape");
+    const int64_t numel = t->shape[0] * t->shape[1] * t->shape[2] * t->shape[3];
+    if (numel > 0) {
+        if (!t->data) return fail(RA_ERR_INVALID_ARG, std::string(name) + ": data is NULL");
+        if (t->stride[3] != 1)
+            return fail(RA_ERR_INVALID_ARG, std::string(name) + ": stride[3] must be 1");
+        for (int i = 0; i < 3; ++i)
+            if (t->stride[i] < 0)
+                return fail(RA_ERR_INVALID_ARG, std::string(name) + ": negative stride");
+        if (reinterpret_cast<uintptr_t>(t->data) % esize(t->dtype))
+            return fail(RA_ERR_INVALID_ARG, std::string(name) + ": misaligned data pointer");
+    }
+    return RA_OK;
+}
+
+static bool aligned16(const ra_tensor *t) {
+    const int64_t per16 = 16 / esize(t->dtype);
+    return reinterpret_cast<uintptr_t>(t->data) % 16 == 0 && t->stride[0] % per16 == 0 &&
+           t->stride[1] % per16 == 0 && t->stride[2] % per16 == 0;
+}
+
+struct Problem {
+    int64_t B, Hq, Hkv, N, D;
+    int32_t dtype;
+};
+
+static ra_status check_qkvo(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v,
+                            const ra_tensor *o, const float *lse, Problem &pb) {
+    ra_status s;
+    if ((s = check_tensor(q, "q")) || (s = check_tensor(k, "k")) || (s = check_tensor(v, "v")) ||
+        (s = check_tensor(o, "o")))
+        return s;
+    pb.B = q->shape[0];
+    pb.Hq = q->shape[1];
+    pb.N = q->shape[2];
+    pb.D = q->shape[3];
+    pb.Hkv = k->shape[1];
+    pb.dtype = q->dtype;
+    if (k->dtype != q->dtype || v->dtype != q->dtype || o->dtype != q->dtype)
+        return fail(RA_ERR_INVALID_ARG, "q, k, v, o must share one dtype");
+    for (int i = 0; i < 4; ++i) {
+        if (k->shape[i] != v->shape[i]) return fail(RA_ERR_INVALID_ARG, "k and v shapes differ");
+        if (o->shape[i] != q->shape[i]) return fail(RA_ERR_INVALID_ARG, "o shape differs from q");
+    }
+    if (k->shape[0] != pb.B || k->shape[2] != pb.N || k->shape[3] != pb.D)
+        return fail(RA_ERR_INVALID_ARG, "k/v must be [B, Hkv, N, D] with q's B, N, D");
+    const int64_t rows = pb.B * pb.Hq * pb.N;
+    if (rows == 0) return RA_OK;
+    if (pb.Hkv < 1 || pb.Hq % pb.Hkv != 0)
+        return fail(RA_ERR_INVALID_ARG, "Hq must be a positive multiple of Hkv");
+    if (pb.D < 1) return fail(RA_ERR_INVALID_ARG, "D must be >= 1");
+    if (!lse) return fail(RA_ERR_INVALID_ARG, "lse is NULL");
+    if (pb.D > 128) return fail(RA_ERR_UNSUPPORTED, "head size D > 128 is not supported");
+    if (pb.N > (int64_t)1 << 30 || pb.B * pb.Hq > 65535LL * 32768LL)
+        return fail(RA_ERR_UNSUPPORTED, "problem too large for one launch grid");
+    return RA_OK;
+}
+
+// ---------------------------------------------------------------- ring schedule
+
+struct Range {
+    int64_t a, b;
+};
+
+static std::vector<Range> rank_ranges(int64_t N, int R, int layout, int r) {
+    if (layout == RA_LAYOUT_CONTIG) {
+        const int64_t c = N / R;
+        return {{r * c, (r + 1) * c}};
+    }
+    const int64_t h = N / (2 * (int64_t)R);
+    return {{r * h, (r + 1) * h}, {(2 * (int64_t)R - 1 - r) * h, (2 * (int64_t)R - r) * h}};
+}
+
+// Segments of one step before flags: for every rank r, each of its query chunks
+// against the chunks of rank (r - step) mod R that some row of the chunk can see.
+static void step_segments(int64_t N, int R, int layout, int causal, int step,
+                          std::vector<Seg> &out) {
+    out.clear();
+    for (int r = 0; r < R; ++r) {
+        const int j = ((r - step) % R + R) % R;
+        const std::vector<Range> kv = rank_ranges(N, R, layout, j);
+        for (const Range &qr : rank_ranges(N, R, layout, r)) {
+            if (qr.b <= qr.a) continue;
+            Seg s;
+            memset(&s, 0, sizeof s);
+            s.q0 = (int32_t)qr.a;
+            s.q1 = (int32_t)qr.b;
+            int nk = 0;
+            for (const Range &kr : kv) {
+                if (kr.b <= kr.a) continue;
+                if (causal && kr.a > qr.b - 1) continue;  // every key after every row
+                s.k0[nk] = (int32_t)kr.a;
+                s.k1[nk] = (int32_t)kr.b;
+                ++nk;
+            }
+            if (nk == 0) continue;
+            if (nk == 1) s.k0[1] = s.k1[1] = s.k1[0];
+            s.rank = r;
+            out.push_back(s);
+        }
+    }
+}
+
+static bool chunk_touched(int64_t N, int R, int layout, int causal, int step, int r, int64_t q0,
+                          int64_t q1) {
+    const int j = ((r - step) % R + R) % R;
+    for (const Range &kr : rank_ranges(N, R, layout, j)) {
+        if (kr.b <= kr.a) continue;
+        if (causal && kr.a > q1 - 1) continue;
+        return true;
+    }
+    (void)q0;
+    return false;
+}
+
+static void plan_step(int64_t N, int R, int layout, int causal, int step, std::vector<Seg> &segs) {
+    step_segments(N, R, layout, causal, step, segs);
+    for (Seg &s : segs) {
+        bool earlier = false, later = false;
+        for (int t = 0; t < step && !earlier; ++t)
+            earlier = chunk_touched(N, R, layout, causal, t, s.rank, s.q0, s.q1);
+        for (int t = step + 1; t < R && !later; ++t)
+            later = chunk_touched(N, R, layout, causal, t, s.rank, s.q0, s.q1);
+        s.flags = (earlier ? 0 : SEG_FIRST) | (later ? 0 : SEG_FINAL);
+    }
+    // heaviest segments first (more keys), so they lead every dispatch round
+    std::stable_sort(segs.begin(), segs.end(), [](const Seg &x, const Seg &y) {
+        const int64_t cx = (int64_t)(x.k1[0] - x.k0[0]) + (x.k1[1] - x.k0[1]);
+        const int64_t cy = (int64_t)(y.k1[0] - y.k0[0]) + (y.k1[1] - y.k0[1]);
+        return cx > cy;
+    });
+}
+
+static ra_status check_ring(int64_t N, int R, int layout) {
+    if (R < 1) return fail(RA_ERR_INVALID_ARG, "ring_size must be >= 1");
+    if (layout != RA_LAYOUT_CONTIG && layout != RA_LAYOUT_ZIGZAG)
+        return fail(RA_ERR_INVALID_ARG, "unknown layout");
+    if (layout == RA_LAYOUT_CONTIG && N % R != 0)
+        return fail(RA_ERR_INVALID_ARG, "contiguous layout needs N % ring_size == 0");
+    if (layout == RA_LAYOUT_ZIGZAG && N % (2 * (int64_t)R) != 0)
+        return fail(RA_ERR_INVALID_ARG, "zigzag layout needs N % (2 ring_size) == 0");
+    return RA_OK;
+}
+
+// ---------------------------------------------------------------- dispatch
+
+static void fill_common(StepParams &P, const ra_tensor *q, const ra_tensor *k, const ra_tensor *v,
+                        const ra_tensor *o, float *lse, const Problem &pb, int causal,
+                        float scale, const DevInfo &di) {
+    memset(&P, 0, sizeof P);
+    P.q = q->data;
+    P.k = k->data;
+    P.v = v->data;
+    P.o = o->data;
+    for (int i = 0; i < 3; ++i) {
+        P.sq[i] = q->stride[i];
+        P.sk[i] = k->stride[i];
+        P.sv[i] = v->stride[i];
+        P.so[i] = o->stride[i];
+    }
+    P.lse = lse;
+    P.B = (int32_t)pb.B;
+    P.Hq = (int32_t)pb.Hq;
+    P.Hkv = (int32_t)pb.Hkv;
+    P.N = (int32_t)pb.N;
+    P.D = (int32_t)pb.D;
+    P.in_bf16 = pb.dtype == RA_BF16;
+    P.causal = causal ? 1 : 0;
+    const float sc = scale > 0.f ? scale : (float)(1.0 / sqrt((double)pb.D));
+    P.scale_log2 = sc * kLog2e;
+    P.wait_limit_ns = g_wait_limit_ns;
+    P.err = di.err;
+}
+
+static bool use_tensor_cores(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v,
+                             const ra_tensor *o, const Problem &pb, const DevInfo &di) {
+    return di.tc_ok && pb.dtype == RA_BF16 && (pb.D == 64 || pb.D == 128) && aligned16(q) &&
+           aligned16(k) && aligned16(v) && aligned16(o);
+}
+
+// Launch the segments of one step (split into launches of <= kMaxSeg segments; all
+// segments of a step have equal query length).
+static ra_status run_step(StepParams &P, const std::vector<Seg> &segs, bool tc,
+                          cudaStream_t stream) {
+    const int rows_per_block = tc ? attn_tc_rows_per_block() : 16;
+    for (size_t first = 0; first < segs.size(); first += kMaxSeg) {
+        const size_t n = std::min(segs.size() - first, (size_t)kMaxSeg);
+        int64_t qlen = 0;
+        for (size_t i = 0; i < n; ++i) {
+            P.seg[i] = segs[first + i];
+            qlen = std::max<int64_t>(qlen, segs[first + i].q1 - segs[first + i].q0);
+        }
+        P.nseg = (int32_t)n;
+        P.rows_per_block = rows_per_block;
+        P.blocks_per_seg = (int32_t)((qlen + rows_per_block - 1) / rows_per_block);
+        const int64_t blocks_y = (int64_t)P.nseg * P.blocks_per_seg;
+        if (blocks_y > 65535) return fail(RA_ERR_UNSUPPORTED, "too many work blocks in one step");
+        cudaError_t e = tc ? launch_attn_tc(P, (int)blocks_y, stream)
+                           : launch_attn_simt(P, (int)blocks_y, stream);
+        if (e != cudaSuccess) return cuda_fail(e, tc ? "attention (tensor-core) launch"
+                                                     : "attention (CUDA-core) launch");
+        ++t_launches;
+    }
+    return RA_OK;
+}
+
+extern "C" {
+
+ra_status ra_attn_fwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v, ra_tensor *o,
+                      float *lse, int causal, float scale, void *stream) {
+    return ra_ring_sim_fwd(q, k, v, o, lse, 1, RA_LAYOUT_CONTIG, causal, scale, nullptr, stream);
+}
+
+size_t ra_ring_sim_workspace_bytes(const ra_tensor *q, int ring_size) {
+    if (!q || ring_size < 1) return 0;
+    for (int i = 0; i < 4; ++i)
+        if (q->shape[i] < 0) return 0;
+    if (ring_size == 1) return 0;
+    return (size_t)(q->shape[0] * q->shape[1] * q->shape[2] * q->shape[3]) * sizeof(float);
+}
+
+ra_status ra_ring_sim_fwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v,
+                          ra_tensor *o, float *lse, int ring_size, ra_layout layout, int causal,
+                          float scale, void *workspace, void *stream) {
+    Problem pb;
+    ra_status s = check_qkvo(q, k, v, o, lse, pb);
+    if (s) return s;
+    if (isnan(scale)) return fail(RA_ERR_INVALID_ARG, "scale is NaN");
+    if ((s = check_ring(pb.N, ring_size, layout))) return s;
+    if (pb.B * pb.Hq * pb.N == 0) return RA_OK;
+    if (ring_size > 1) {
+        if (!workspace) return fail(RA_ERR_INVALID_ARG, "workspace is NULL (ring_size > 1)");
+        if (reinterpret_cast<uintptr_t>(workspace) % 16)
+            return fail(RA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    }
+    DevInfo di;
+    std::string msg;
+    if (!device_info(di, msg)) return fail(RA_ERR_CUDA, msg);
+    StepParams *P = new StepParams;
+    fill_common(*P, q, k, v, o, lse, pb, causal, scale, di);
+    P->oacc = ring_size > 1 ? static_cast<float *>(workspace) : nullptr;
+    const bool tc = use_tensor_cores(q, k, v, o, pb, di);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    std::vector<Seg> segs;
+    for (int step = 0; step < ring_size; ++step) {
+        plan_step(pb.N, ring_size, layout, causal, step, segs);
+        if (segs.empty()) continue;
+        s = run_step(*P, segs, tc, st);
+        if (s) break;
+    }
+    delete P;
+    return s;
+}
+
+int64_t ra_ring_sim_plan(int64_t N, int ring_size, ra_layout layout, int causal, int step,
+                         int64_t *segments, int64_t cap) {
+    if (N < 0 || N > ((int64_t)1 << 30) || step < 0 || step >= ring_size) return -1;
+    if (check_ring(N, ring_size, layout) != RA_OK) return -1;
+    std::vector<Seg> segs;
+    plan_step(N, ring_size, layout, causal, step, segs);
+    for (int64_t i = 0; i < (int64_t)segs.size() && i < cap && segments; ++i) {
+        const Seg &x = segs[i];
+        int64_t *o = segments + 8 * i;
+        o[0] = x.q0;
+        o[1] = x.q1;
+        o[2] = x.k0[0];
+        o[3] = x.k1[0];
+        o[4] = x.k0[1];
+        o[5] = x.k1[1];
+        o[6] = x.flags;
+        o[7] = x.rank;
+    }
+    return (int64_t)segs.size();
+}
+
+ra_status ra_lse_merge(ra_tensor *o_acc, float *lse_acc, const ra_tensor *o_blk,
+                       const float *lse_blk, void *stream) {
+    ra_status s;
+    if ((s = check_tensor(o_acc, "o_acc")) || (s = check_tensor(o_blk, "o_blk"))) return s;
+    if (o_acc->dtype != RA_F32) return fail(RA_ERR_INVALID_ARG, "o_acc must be float32");
+    for (int i = 0; i < 4; ++i)
+        if (o_acc->shape[i] != o_blk->shape[i])
+            return fail(RA_ERR_INVALID_ARG, "o_acc and o_blk shapes differ");
+    const int64_t rows = o_acc->shape[0] * o_acc->shape[1] * o_acc->shape[2];
+    if (rows == 0 || o_acc->shape[3] == 0) return RA_OK;
+    if (!lse_acc || !lse_blk) return fail(RA_ERR_INVALID_ARG, "lse pointer is NULL");
+    DevInfo di;
+    std::string msg;
+    if (!device_info(di, msg)) return fail(RA_ERR_CUDA, msg);
+    MergeParams P;
+    memset(&P, 0, sizeof P);
+    P.oacc = static_cast<float *>(o_acc->data);
+    P.lse_acc = lse_acc;
+    P.oblk = o_blk->data;
+    P.lse_blk = lse_blk;
+    for (int i = 0; i < 3; ++i) {
+        P.sa[i] = o_acc->stride[i];
+        P.sb[i] = o_blk->stride[i];
+    }
+    P.blk_bf16 = o_blk->dtype == RA_BF16;
+    P.H = (int32_t)o_acc->shape[1];
+    P.N = (int32_t)o_acc->shape[2];
+    P.D = (int32_t)o_acc->shape[3];
+    P.rows = rows;
+    const int64_t bvec = P.blk_bf16 ? 4 : 4;  // elements per vector access
+    const uintptr_t balign = P.blk_bf16 ? 8 : 16;
+    P.vec = (P.D % 4 == 0) && reinterpret_cast<uintptr_t>(P.oacc) % 16 == 0 &&
+            reinterpret_cast<uintptr_t>(P.oblk) % balign == 0 && P.sa[0] % 4 == 0 &&
+            P.sa[1] % 4 == 0 && P.sa[2] % 4 == 0 && P.sb[0] % bvec == 0 && P.sb[1] % bvec == 0 &&
+            P.sb[2] % bvec == 0;
+    cudaError_t e = launch_lse_merge(P, di.sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "lse_merge launch");
+    ++t_launches;
+    return RA_OK;
+}
+
+ra_status ra_check_device_error(void *stream) {
+    DevInfo di;
+    std::string msg;
+    if (!device_info(di, msg)) return fail(RA_ERR_CUDA, msg);
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    int word = 0;
+    e = cudaMemcpy(&word, di.err, sizeof word, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+    if (word != 0) {
+        const int zero = 0;
+        e = cudaMemcpy(di.err, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+        if (word == DERR_TIMEOUT)
+            return fail(RA_ERR_TIMEOUT, "a device pipeline wait exceeded its time limit");
+        return fail(RA_ERR_CUDA, "device error word " + std::to_string(word));
+    }
+    return RA_OK;
+}
+
+void ra_debug_set_wait_limit_ns(int64_t ns) { g_wait_limit_ns = ns < 0 ? 2000000000LL : ns; }
+
+ra_status ra_debug_wait_selftest(int64_t limit_ns, void *stream) {
+    if (limit_ns < 0 || limit_ns > 10000000000LL)
+        return fail(RA_ERR_INVALID_ARG, "limit_ns must be in [0, 1e10]");
+    DevInfo di;
+    std::string msg;
+    if (!device_info(di, msg)) return fail(RA_ERR_CUDA, msg);
+    cudaError_t e = launch_wait_selftest(limit_ns, di.err, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "wait self-test launch");
+    ++t_launches;
+    return RA_OK;
+}
+
+const char *ra_last_error(void) { return t_last_error.c_str(); }
+
+int64_t ra_launch_count(int reset) {
+    const int64_t n = t_launches;
+    if (reset) t_launches = 0;
+    return n;
+}
+
+int ra_version(void) { return 100; }
+
+}  // extern "C"

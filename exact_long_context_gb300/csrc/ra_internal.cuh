@@ -1,0 +1,112 @@
+// ra_internal.cuh - launch parameters and device helpers shared by the attention kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ra.h"
+
+namespace ra {
+
+// One query chunk of one simulated rank against the key/value block it holds in a
+// ring step.  Key ranges are disjoint and in increasing position; the second may be
+// empty (k0[1] == k1[1]).
+struct Seg {
+    int32_t q0, q1;
+    int32_t k0[2], k1[2];
+    int32_t flags;
+    int32_t rank;
+};
+
+enum : int32_t { SEG_FIRST = 1, SEG_FINAL = 2 };
+
+constexpr int kMaxSeg = 128;
+
+// Everything one step launch needs.  Every segment of a launch has the same number
+// of query rows, so a work block decodes to (segment, local block) arithmetically.
+struct StepParams {
+    const void *q, *k, *v;
+    int64_t sq[3], sk[3], sv[3];  // strides (elements) of dims B, H, N
+    void *o;
+    int64_t so[3];
+    float *lse;   // [B, Hq, N] contiguous; also the running LSE across steps
+    float *oacc;  // [B, Hq, N, D] contiguous float32 running output (steps > 1)
+    int32_t B, Hq, Hkv, N, D;
+    int32_t in_bf16;   // q, k, v, o are bf16 (else float32)
+    int32_t causal;
+    float scale_log2;  // softmax scale * log2(e)
+    int32_t nseg;
+    int32_t blocks_per_seg;  // work blocks per segment
+    int32_t rows_per_block;  // query rows per work block
+    int64_t wait_limit_ns;
+    int *err;  // device error word
+    Seg seg[kMaxSeg];
+};
+
+// Standalone LSE merge of a block partial into a running partial (see lse_merge.cu).
+struct MergeParams {
+    float *oacc;
+    int64_t sa[3];
+    float *lse_acc;
+    const void *oblk;
+    int64_t sb[3];
+    const float *lse_blk;
+    int32_t blk_bf16;
+    int32_t H, N, D;
+    int32_t vec;  // rows are 16-byte aligned (8 for bf16) and D % 4 == 0
+    int64_t rows;
+};
+
+// Device error codes (first one wins).
+enum : int { DERR_TIMEOUT = 1 };
+
+__device__ __forceinline__ void record_error(int *err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// Decode blockIdx.y into (segment, local block).  Work blocks are numbered round-robin
+// over segments; the local block counts down, so the last (under causality the
+// heaviest) blocks of every segment are dispatched first.
+__device__ __forceinline__ void decode_work(const StepParams &P, int w, int &si, int &lb) {
+    const int round = w / P.nseg;
+    si = w - round * P.nseg;
+    lb = P.blocks_per_seg - 1 - round;
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Per-row epilogue weights for folding a block partial with LSE `b` into the running
+// partial with LSE `a` (natural logs): L = ln(e^a + e^b), w_a = e^(a-L), w_b = e^(b-L).
+struct MergeW {
+    float wa, wb, L;
+};
+
+__device__ __forceinline__ MergeW merge_weights(float a, float b) {
+    MergeW m;
+    if (a == -INFINITY) {
+        m.wa = 0.f;
+        m.wb = (b == -INFINITY) ? 0.f : 1.f;
+        m.L = b;
+        return m;
+    }
+    if (b == -INFINITY) {
+        m.wa = 1.f;
+        m.wb = 0.f;
+        m.L = a;
+        return m;
+    }
+    const float mx = fmaxf(a, b);
+    const float L = mx + log1pf(expf(-fabsf(a - b)));
+    m.wa = expf(a - L);
+    m.wb = expf(b - L);
+    m.L = L;
+    return m;
+}
+
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+}  // namespace ra

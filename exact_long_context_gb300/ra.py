@@ -1,0 +1,196 @@
+"""ctypes binding of libra.so: torch tensors in, C-ABI calls out.
+
+Argument marshalling only - every step of the computation runs in the library's CUDA
+kernels.  The library must be built (``python -m exact_long_context_gb300.build``);
+if it is missing, or a tensor is not on a CUDA device, the call raises.  There is
+no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libra.so")
+
+RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_TIMEOUT = range(5)
+RA_F32, RA_BF16 = 0, 1
+LAYOUTS = {"contig": 0, "zigzag": 1}
+SEG_FIRST, SEG_FINAL = 1, 2
+
+
+class RaError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"ra status {status}: {msg}")
+        self.status = status
+
+
+class RaTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is not built: run python -m exact_long_context_gb300.build")
+            L = ctypes.CDLL(LIB_PATH)
+            P, T = ctypes.c_void_p, ctypes.POINTER(RaTensor)
+            i64, c_int, c_float = ctypes.c_int64, ctypes.c_int, ctypes.c_float
+            L.ra_attn_fwd.argtypes = [T, T, T, T, P, c_int, c_float, P]
+            L.ra_lse_merge.argtypes = [T, P, T, P, P]
+            L.ra_ring_sim_workspace_bytes.argtypes = [T, c_int]
+            L.ra_ring_sim_workspace_bytes.restype = ctypes.c_size_t
+            L.ra_ring_sim_fwd.argtypes = [T, T, T, T, P, c_int, c_int, c_int, c_float, P, P]
+            L.ra_ring_sim_plan.argtypes = [i64, c_int, c_int, c_int, c_int, P, i64]
+            L.ra_ring_sim_plan.restype = i64
+            L.ra_check_device_error.argtypes = [P]
+            L.ra_debug_set_wait_limit_ns.argtypes = [i64]
+            L.ra_debug_set_wait_limit_ns.restype = None
+            L.ra_debug_wait_selftest.argtypes = [i64, P]
+            L.ra_last_error.restype = ctypes.c_char_p
+            L.ra_launch_count.argtypes = [c_int]
+            L.ra_launch_count.restype = i64
+            for name in ("ra_attn_fwd", "ra_lse_merge", "ra_ring_sim_fwd", "ra_check_device_error",
+                         "ra_debug_wait_selftest"):
+                getattr(L, name).restype = c_int
+            _lib = L
+        return _lib
+
+
+def _check(status: int):
+    if status != RA_OK:
+        raise RaError(status, lib().ra_last_error().decode())
+
+
+def _desc(t: torch.Tensor | None, name: str) -> RaTensor:
+    d = RaTensor()
+    if t is None:
+        return d
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be 4-D [B, H, N, D]")
+    if t.dtype == torch.float32:
+        d.dtype = RA_F32
+    elif t.dtype == torch.bfloat16:
+        d.dtype = RA_BF16
+    else:
+        raise TypeError(f"{name}: dtype {t.dtype} (want float32 or bfloat16)")
+    if t.numel() and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    d.data = t.data_ptr() if t.numel() else None
+    for i in range(4):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    if t.shape[3] <= 1:
+        d.stride[3] = 1  # the stride of a size-1 dimension carries no information
+    return d
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None or t.numel() == 0 else t.data_ptr()
+
+
+def _outputs(q, o, lse):
+    B, Hq, N, _ = q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, Hq, N):
+        raise ValueError("lse must be a contiguous float32 [B, Hq, N] tensor")
+    return o, lse
+
+
+def attn_fwd(q, k, v, causal=False, scale=None, o=None, lse=None, stream=None):
+    """Exact attention: returns (o, lse).  q [B,Hq,N,D]; k, v [B,Hkv,N,D]."""
+    o, lse = _outputs(q, o, lse)
+    dq, dk, dv, do = _desc(q, "q"), _desc(k, "k"), _desc(v, "v"), _desc(o, "o")
+    _check(lib().ra_attn_fwd(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), ctypes.byref(do),
+                             _ptr(lse), int(bool(causal)), float(scale or 0.0), _stream(stream)))
+    return o, lse
+
+
+def lse_merge(o_acc, lse_acc, o_blk, lse_blk, stream=None):
+    """Fold (o_blk, lse_blk) into (o_acc, lse_acc) in place."""
+    da, db = _desc(o_acc, "o_acc"), _desc(o_blk, "o_blk")
+    for name, t in (("lse_acc", lse_acc), ("lse_blk", lse_blk)):
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous float32")
+    _check(lib().ra_lse_merge(ctypes.byref(da), _ptr(lse_acc), ctypes.byref(db), _ptr(lse_blk),
+                              _stream(stream)))
+    return o_acc, lse_acc
+
+
+def ring_sim_workspace_bytes(q, ring_size: int) -> int:
+    return int(lib().ra_ring_sim_workspace_bytes(ctypes.byref(_desc(q, "q")), int(ring_size)))
+
+
+def ring_sim_fwd(q, k, v, ring_size: int, layout="contig", causal=False, scale=None, o=None,
+                 lse=None, workspace=None, stream=None):
+    """Ring attention over ``ring_size`` simulated ranks on one GPU: returns (o, lse)."""
+    o, lse = _outputs(q, o, lse)
+    need = ring_sim_workspace_bytes(q, ring_size)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if workspace is not None and workspace.numel() < need:
+        raise ValueError(f"workspace needs {need} bytes")
+    dq, dk, dv, do = _desc(q, "q"), _desc(k, "k"), _desc(v, "v"), _desc(o, "o")
+    _check(lib().ra_ring_sim_fwd(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv),
+                                 ctypes.byref(do), _ptr(lse), int(ring_size), LAYOUTS[layout],
+                                 int(bool(causal)), float(scale or 0.0), _ptr(workspace),
+                                 _stream(stream)))
+    return o, lse
+
+
+def ring_sim_plan(N: int, ring_size: int, layout="contig", causal=False, step=0):
+    """Host-only schedule of one step: list of dicts (q0, q1, k ranges, flags, rank)."""
+    L = lib()
+    n = L.ra_ring_sim_plan(int(N), int(ring_size), LAYOUTS[layout], int(bool(causal)), int(step),
+                           None, 0)
+    if n < 0:
+        raise ValueError("bad ring plan arguments")
+    buf = (ctypes.c_int64 * (8 * max(n, 1)))()
+    L.ra_ring_sim_plan(int(N), int(ring_size), LAYOUTS[layout], int(bool(causal)), int(step),
+                       ctypes.cast(buf, ctypes.c_void_p), n)
+    out = []
+    for i in range(n):
+        q0, q1, ka0, ka1, kb0, kb1, flags, rank = buf[8 * i:8 * i + 8]
+        ranges = [(ka0, ka1)] + ([(kb0, kb1)] if kb1 > kb0 else [])
+        out.append({"q": (q0, q1), "kv": ranges, "flags": flags, "rank": rank})
+    return out
+
+
+def check(stream=None):
+    """Synchronise and raise if a kernel recorded a device-side error (e.g. a wait timeout)."""
+    _check(lib().ra_check_device_error(_stream(stream)))
+
+
+def set_wait_limit_ns(ns: int):
+    lib().ra_debug_set_wait_limit_ns(int(ns))
+
+
+def wait_selftest(limit_ns: int, stream=None):
+    _check(lib().ra_debug_wait_selftest(int(limit_ns), _stream(stream)))
+
+
+def launch_count(reset=False) -> int:
+    return int(lib().ra_launch_count(1 if reset else 0))
+
+
+def version() -> int:
+    return int(lib().ra_version())

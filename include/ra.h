@@ -1,0 +1,186 @@
+/*
+ * ra.h - exact blockwise attention, log-sum-exp merge and a one-GPU ring simulation.
+ *
+ * C ABI of libra.so (CUDA, sm_103a).  Plain pointers and sizes; no C++ or torch types.
+ *
+ * Tensors
+ *   ra_tensor describes a 4-D strided array [B, H, N, D] in device memory:
+ *   data (device pointer), dtype, shape[4] = {B, H, N, D} and stride[4] in ELEMENTS.
+ *   stride[3] must be 1 (rows of D contiguous).  The caller owns every buffer.
+ *   q is [B, Hq, N, D]; k and v are [B, Hkv, N, D] with Hq % Hkv == 0; query head h
+ *   reads key/value head h / (Hq / Hkv) (consecutive query heads share a KV head).
+ *   o has q's shape and dtype.  lse is a contiguous float32 [B, Hq, N] array.
+ *
+ * Scale
+ *   scale <= 0 selects 1/sqrt(D), the default of the pages' attention definition.
+ *
+ * Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ * Argument errors are reported synchronously as a status; the message of the last
+ * non-OK status of the calling thread is ra_last_error().  Device-side failures
+ * (a pipeline wait that exceeded its time limit) are recorded in a device error word
+ * that ra_check_device_error() reads.
+ *
+ * Paths (all on the GPU; there is no CPU path):
+ *   bf16, D in {64, 128}, 16-byte aligned base and row strides: tcgen05 tensor-core
+ *     kernel (TMA-fed shared-memory pipeline, S and O accumulated in tensor memory).
+ *   anything else with D <= 128 (float32 inputs, other head sizes, unaligned strides):
+ *     a CUDA-core kernel computing in float32.
+ *   D > 128: RA_ERR_UNSUPPORTED.
+ */
+#ifndef RA_H
+#define RA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RA_OK = 0,
+    RA_ERR_INVALID_ARG = 1, /* null pointer, bad shape/stride/dtype/size rule */
+    RA_ERR_UNSUPPORTED = 2, /* well-formed but outside what the library implements */
+    RA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+    RA_ERR_TIMEOUT = 4      /* a device-side pipeline wait exceeded its limit */
+} ra_status;
+
+typedef enum { RA_F32 = 0, RA_BF16 = 1 } ra_dtype;
+
+typedef enum { RA_LAYOUT_CONTIG = 0, RA_LAYOUT_ZIGZAG = 1 } ra_layout;
+
+typedef struct {
+    void *data;        /* device pointer */
+    int32_t dtype;     /* ra_dtype */
+    int32_t reserved;  /* must be 0 */
+    int64_t shape[4];  /* B, H, N, D */
+    int64_t stride[4]; /* in elements; stride[3] == 1 */
+} ra_tensor;
+
+/*
+ * ra_attn_fwd - exact attention of one sequence block, O = softmax(scale Q K^T) V,
+ * and the per-row natural-log LSE = ln sum_j exp(scale q_i . k_j).
+ *
+ * Defined by the standard attention formula of "Ring Attention explained"
+ * (guijiagi.com), section "朴素 Attention 的显存墙", computed blockwise with the
+ * online softmax of its section "在线 Softmax 算法" and the deferred normalisation of
+ * "第12章 FlashAttention原理与实现" (FlashAttention-2 paragraph).  With causal != 0,
+ * key j is visible to query i iff j <= i ("因果掩码处理": the diagonal block is
+ * lower-triangular).  Any N >= 0 (ragged tails are masked); N == 0, B == 0 or
+ * H == 0 is a no-op.
+ *
+ *   q, k, v  inputs as described above (read only)
+ *   o        output [B, Hq, N, D], same dtype as q (written)
+ *   lse      output float32 [B, Hq, N], contiguous (written)
+ *   causal   0 or 1
+ *   scale    softmax scale; <= 0 means 1/sqrt(D)
+ *   stream   cudaStream_t
+ * Errors: RA_ERR_INVALID_ARG (null pointers, shape or dtype mismatch, stride[3] != 1,
+ *   NaN scale), RA_ERR_UNSUPPORTED (D > 128), RA_ERR_CUDA (launch failure).
+ */
+ra_status ra_attn_fwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v, ra_tensor *o,
+                      float *lse, int causal, float scale, void *stream);
+
+/*
+ * ra_lse_merge - fold a block partial into a running partial, row by row:
+ *   L       = ln(e^a + e^b)           with a = lse_acc[row], b = lse_blk[row]
+ *   o_acc  <- e^(a-L) o_acc + e^(b-L) o_blk
+ *   lse_acc <- L
+ * This is `update_out_and_lse` of "序列并行与 Ring Attention：超长上下文训练技术解析"
+ * (section "前向传播：ZigZag Ring FlashAttention"), evaluated in the max-shifted form
+ * (same value; no overflow).  The identity partial is (o = 0, lse = -inf): a side with
+ * lse = -inf contributes nothing, and two identities give the identity.
+ *
+ *   o_acc    [B, H, N, D] float32 (read and written)
+ *   lse_acc  float32 [B, H, N] contiguous (read and written)
+ *   o_blk    [B, H, N, D] float32 or bf16 (read)
+ *   lse_blk  float32 [B, H, N] contiguous (read)
+ * Errors: RA_ERR_INVALID_ARG (null pointers, shape mismatch, o_acc not float32,
+ *   stride[3] != 1), RA_ERR_CUDA.
+ */
+ra_status ra_lse_merge(ra_tensor *o_acc, float *lse_acc, const ra_tensor *o_blk,
+                       const float *lse_blk, void *stream);
+
+/*
+ * ra_ring_sim_workspace_bytes - device workspace that ra_ring_sim_fwd needs for the
+ * float32 running output: B*Hq*N*D*4 bytes when ring_size > 1, else 0.  Returns 0 on
+ * bad arguments.
+ */
+size_t ra_ring_sim_workspace_bytes(const ra_tensor *q, int ring_size);
+
+/*
+ * ra_ring_sim_fwd - ring attention over ring_size simulated ranks on one GPU.
+ *
+ * The sequence is split among the ranks ("Ring Attention" glossary page,
+ * ultralytics.com, section on how ring attention works):
+ *   RA_LAYOUT_CONTIG  rank r holds rows [r c, (r+1) c), c = N / ring_size
+ *   RA_LAYOUT_ZIGZAG  2*ring_size chunks; rank r holds chunk r and chunk 2R-1-r
+ *                     ("序列并行与 Ring Attention", section "2. ZigZag Ring Attention")
+ * At step s rank r holds the key/value block of rank (r - s) mod R; the step's
+ * partial for each rank's query rows (causality on global positions, so later
+ * blocks are skipped and the diagonal block masked) is merged into a float32 running
+ * result by the LSE merge above, inside the attention kernel's epilogue.  Each step
+ * is one kernel launch covering every simulated rank.  The result equals
+ * ra_attn_fwd on the whole sequence (up to rounding); inputs and outputs are in
+ * natural sequence order; ring_size == 1 is ra_attn_fwd.
+ *
+ *   ring_size  >= 1; contig needs N % ring_size == 0, zigzag N % (2 ring_size) == 0
+ *   layout     ra_layout
+ *   workspace  device buffer of ra_ring_sim_workspace_bytes() bytes (may be NULL when
+ *              that is 0); contents on entry are ignored; owned by the caller
+ * Errors: as ra_attn_fwd, plus RA_ERR_INVALID_ARG for a bad ring size / layout /
+ *   divisibility or a missing workspace.
+ */
+ra_status ra_ring_sim_fwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v,
+                          ra_tensor *o, float *lse, int ring_size, ra_layout layout, int causal,
+                          float scale, void *workspace, void *stream);
+
+/*
+ * ra_ring_sim_plan - host-only description of the ring schedule (no GPU work).
+ * For step `step`, writes up to `cap` segments; each segment is 8 int64 values:
+ *   q0, q1          query rows [q0, q1) of one chunk of one simulated rank
+ *   k0a, k1a        first key range [k0a, k1a)
+ *   k0b, k1b        second key range (k0b == k1b when absent)
+ *   flags           bit 0: first partial of these rows, bit 1: last partial
+ *   rank            the simulated rank
+ * Returns the number of segments of that step (which may exceed cap), or -1 on bad
+ * arguments.
+ */
+int64_t ra_ring_sim_plan(int64_t N, int ring_size, ra_layout layout, int causal, int step,
+                         int64_t *segments, int64_t cap);
+
+/*
+ * ra_check_device_error - synchronise `stream`, then read and clear the device error
+ * word of the current device.  RA_ERR_TIMEOUT if a kernel recorded a wait timeout,
+ * RA_ERR_CUDA if the synchronisation failed, else RA_OK.
+ */
+ra_status ra_check_device_error(void *stream);
+
+/*
+ * ra_debug_set_wait_limit_ns - time limit of the kernels' pipeline waits on the
+ * current device (default 2e9 ns).  A wait that exceeds it records RA_ERR_TIMEOUT and
+ * the kernel winds down cleanly.  Values < 0 restore the default.  Diagnostic hook.
+ */
+void ra_debug_set_wait_limit_ns(int64_t ns);
+
+/*
+ * ra_debug_wait_selftest - launch one block that waits, bounded by `limit_ns`, on a
+ * shared-memory barrier that nothing completes, then records RA_ERR_TIMEOUT in the
+ * device error word.  Exercises the timeout path without touching any pipeline.
+ */
+ra_status ra_debug_wait_selftest(int64_t limit_ns, void *stream);
+
+/* Message of the calling thread's last non-OK status ("" if none). */
+const char *ra_last_error(void);
+
+/* Number of kernel launches issued by the calling thread since the last reset. */
+int64_t ra_launch_count(int reset);
+
+/* Library version, 100 * major + minor. */
+int ra_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RA_H */

@@ -1,0 +1,74 @@
+"""Shared test helpers: moving tensors to the oracle, sampling rows, tolerances."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+# GPU-vs-oracle tolerances: bf16 inputs: max-abs on O <= 2e-2, LSE |d| <= 1e-3 max(1, |lse|);
+# float32 inputs (CUDA-core path): max-abs <= 1e-5 on both.
+BF16_O_TOL = 2e-2
+BF16_LSE_REL = 1e-3
+F32_TOL = 1e-5
+
+
+def to_oracle(t: torch.Tensor) -> np.ndarray:
+    """CPU numpy copy in the oracle's input encoding (bf16 -> uint16 bit patterns)."""
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.float32:
+        return t.numpy()
+    raise TypeError(t.dtype)
+
+
+def oracle_full(q, k, v, causal, scale=None, kv_lo=0, kv_hi=None):
+    return oracle.attention(to_oracle(q), to_oracle(k), to_oracle(v), causal, scale, kv_lo, kv_hi)
+
+
+def sample_rows(B, Hq, N, chunk=None, n_random=16, seed=0, heads=None):
+    """(b, h, i) triples: rows 0, 1, N-1, every chunk's first and last row, random rows."""
+    rng = np.random.default_rng(seed)
+    base = {0, min(1, N - 1), N - 1}
+    if chunk:
+        for c0 in range(0, N, chunk):
+            base.add(c0)
+            base.add(min(N, c0 + chunk) - 1)
+    rows = []
+    heads = heads if heads is not None else [(b, h) for b in range(B) for h in range(Hq)]
+    for b, h in heads:
+        extra = rng.integers(0, N, size=n_random) if n_random else []
+        for i in sorted(base | {int(x) for x in extra}):
+            rows.append((b, h, i))
+    return np.array(rows, dtype=np.int64)
+
+
+def gather_rows(o: torch.Tensor, lse: torch.Tensor, rows: np.ndarray):
+    idx = torch.as_tensor(rows, device=o.device)
+    og = o[idx[:, 0], idx[:, 1], idx[:, 2]].float().cpu().numpy().astype(np.float64)
+    lg = lse[idx[:, 0], idx[:, 1], idx[:, 2]].cpu().numpy().astype(np.float64)
+    return og, lg
+
+
+def errors(o_gpu, lse_gpu, o_ref, lse_ref):
+    o_gpu = np.asarray(o_gpu, np.float64)
+    lse_gpu = np.asarray(lse_gpu, np.float64)
+    assert np.all(np.isfinite(o_gpu)), "non-finite output"
+    assert np.all(np.isfinite(lse_gpu)), "non-finite LSE"
+    o_err = float(np.max(np.abs(o_gpu - o_ref))) if o_gpu.size else 0.0
+    d = np.abs(lse_gpu - lse_ref)
+    lse_rel = float(np.max(d / np.maximum(1.0, np.abs(lse_ref)))) if d.size else 0.0
+    lse_abs = float(np.max(d)) if d.size else 0.0
+    return o_err, lse_rel, lse_abs
+
+
+def assert_close(o_gpu, lse_gpu, o_ref, lse_ref, dtype, what=""):
+    o_err, lse_rel, lse_abs = errors(o_gpu, lse_gpu, o_ref, lse_ref)
+    if dtype == torch.bfloat16:
+        assert o_err <= BF16_O_TOL, f"{what}: O max-abs {o_err:.3e} > {BF16_O_TOL}"
+        assert lse_rel <= BF16_LSE_REL, f"{what}: LSE rel {lse_rel:.3e} > {BF16_LSE_REL}"
+    else:
+        assert o_err <= F32_TOL, f"{what}: O max-abs {o_err:.3e} > {F32_TOL}"
+        assert lse_abs <= F32_TOL, f"{what}: LSE abs {lse_abs:.3e} > {F32_TOL}"
+    return o_err, lse_rel

@@ -1,0 +1,190 @@
+"""Host-side checks of libra.so that need no GPU: exports, argument validation, ring plan."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from oracle import ring as oring
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ra():
+    from exact_long_context_gb300 import build
+    build.build()
+    from exact_long_context_gb300 import ra as ra_mod
+    return ra_mod
+
+
+def header_symbols():
+    txt = open(os.path.join(ROOT, "include", "ra.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(ra_[a-z0-9_]+)\s*\(", txt)))
+
+
+def test_library_exports_every_declared_symbol(ra):
+    names = header_symbols()
+    assert {"ra_attn_fwd", "ra_lse_merge", "ra_ring_sim_fwd", "ra_ring_sim_workspace_bytes"} <= set(names)
+    L = ctypes.CDLL(ra.LIB_PATH)
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, f"declared but not exported: {missing}"
+    assert ra.version() == 100
+
+
+def _t(shape, dtype=1, data=0x10000, stride=None):
+    d = ra_mod().RaTensor()
+    d.data = data
+    d.dtype = dtype
+    if stride is None:
+        stride = [shape[1] * shape[2] * shape[3], shape[2] * shape[3], shape[3], 1]
+    for i in range(4):
+        d.shape[i] = shape[i]
+        d.stride[i] = stride[i]
+    return d
+
+
+def ra_mod():
+    from exact_long_context_gb300 import ra as ra_m
+    return ra_m
+
+
+def _call(ra, q, k, v, o, lse=0x20000, causal=1, scale=0.0, R=1, layout=0, ws=None):
+    L = ra.lib()
+    P = ctypes.byref
+    return L.ra_ring_sim_fwd(P(q) if q is not None else None, P(k), P(v), P(o), lse, R, layout,
+                             causal, scale, ws, None)
+
+
+def test_argument_errors_are_reported_without_touching_a_gpu(ra):
+    S = (1, 4, 256, 128)
+    KV = (1, 2, 256, 128)
+    IA, UN = ra.RA_ERR_INVALID_ARG, ra.RA_ERR_UNSUPPORTED
+    assert _call(ra, None, _t(KV), _t(KV), _t(S)) == IA
+    assert _call(ra, _t(S), _t(KV), _t((1, 2, 255, 128)), _t(S)) == IA  # k/v differ
+    assert _call(ra, _t(S), _t((1, 3, 256, 128)), _t((1, 3, 256, 128)), _t(S)) == IA  # Hq % Hkv
+    assert _call(ra, _t(S), _t(KV), _t(KV), _t((1, 4, 256, 64))) == IA  # o shape
+    assert _call(ra, _t(S), _t(KV), _t(KV), _t(S, dtype=0)) == IA  # mixed dtype
+    assert _call(ra, _t(S, stride=[0, 0, 128, 2]), _t(KV), _t(KV), _t(S)) == IA  # stride[3]
+    assert _call(ra, _t(S, data=0), _t(KV), _t(KV), _t(S)) == IA  # null data
+    assert _call(ra, _t(S, data=0x10001), _t(KV), _t(KV), _t(S)) == IA  # misaligned bf16
+    assert _call(ra, _t(S), _t(KV), _t(KV), _t(S), lse=None) == IA
+    assert _call(ra, _t(S), _t(KV), _t(KV), _t(S), scale=math.nan) == IA
+    assert _call(ra, _t(S), _t(KV), _t(KV), _t(S), R=0) == IA
+    assert _call(ra, _t(S), _t(KV), _t(KV), _t(S), R=3) == IA  # 256 % 3
+    assert _call(ra, _t(S), _t(KV), _t(KV), _t(S), R=3, layout=1) == IA
+    assert _call(ra, _t(S), _t(KV), _t(KV), _t(S), R=256, layout=1) == IA  # 256 % 512
+    assert _call(ra, _t(S), _t(KV), _t(KV), _t(S), R=4, layout=7) == IA
+    assert _call(ra, _t(S), _t(KV), _t(KV), _t(S), R=4, ws=None) == IA  # workspace missing
+    big = (1, 4, 256, 192)
+    assert _call(ra, _t(big), _t((1, 2, 256, 192)), _t((1, 2, 256, 192)), _t(big)) == UN
+    assert "D > 128" in ra.lib().ra_last_error().decode()
+    bad = _t(S)
+    bad.dtype = 9
+    assert _call(ra, bad, _t(KV), _t(KV), _t(S)) == IA
+
+
+def test_workspace_size(ra):
+    q = _t((2, 8, 1024, 128))
+    L = ra.lib()
+    assert L.ra_ring_sim_workspace_bytes(ctypes.byref(q), 1) == 0
+    assert L.ra_ring_sim_workspace_bytes(ctypes.byref(q), 4) == 2 * 8 * 1024 * 128 * 4
+    assert L.ra_ring_sim_workspace_bytes(ctypes.byref(q), 0) == 0
+
+
+def test_merge_argument_errors(ra):
+    L = ra.lib()
+    a = _t((1, 2, 8, 16), dtype=0)
+    b = _t((1, 2, 8, 16), dtype=1)
+    wrong = _t((1, 2, 9, 16), dtype=1)
+    assert L.ra_lse_merge(ctypes.byref(a), 0x20000, ctypes.byref(wrong), 0x30000, None) == ra.RA_ERR_INVALID_ARG
+    assert L.ra_lse_merge(ctypes.byref(b), 0x20000, ctypes.byref(b), 0x30000, None) == ra.RA_ERR_INVALID_ARG
+    assert L.ra_lse_merge(ctypes.byref(a), None, ctypes.byref(b), 0x30000, None) == ra.RA_ERR_INVALID_ARG
+
+
+def _covered(plan_steps, N, causal):
+    """For every query row, the multiset of keys it is scheduled to see over all steps."""
+    seen = {}
+    for segs in plan_steps:
+        for s in segs:
+            for i in range(*s["q"]):
+                for a, b in s["kv"]:
+                    hi = min(b, i + 1) if causal else b
+                    if hi > a:
+                        seen.setdefault(i, []).append((a, hi))
+    return seen
+
+
+@pytest.mark.parametrize("layout", ["contig", "zigzag"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 8])
+def test_plan_covers_every_visible_key_once(ra, layout, causal, R):
+    N = 2 * R * 6
+    steps = [ra.ring_sim_plan(N, R, layout, causal, s) for s in range(R)]
+    seen = _covered(steps, N, causal)
+    for i in range(N):
+        keys = sorted(k for a, b in seen.get(i, []) for k in range(a, b))
+        want = list(range(0, i + 1)) if causal else list(range(N))
+        assert keys == want, (i, keys[:10])
+    # first/last flags: every query chunk has exactly one FIRST and one FINAL segment
+    firsts, finals = {}, {}
+    for segs in steps:
+        for s in segs:
+            firsts[s["q"]] = firsts.get(s["q"], 0) + (s["flags"] & ra.SEG_FIRST > 0)
+            finals[s["q"]] = finals.get(s["q"], 0) + (s["flags"] & ra.SEG_FINAL > 0)
+    assert set(firsts.values()) == {1} and set(finals.values()) == {1}
+    # the rank partition matches the oracle's restatement
+    for s in steps[0]:
+        assert s["q"] in [tuple(x) for x in oring.rank_ranges(N, R, layout)[s["rank"]]]
+
+
+@pytest.mark.parametrize("R", [2, 3, 4, 8])
+def test_plan_reproduces_the_zigzag_step_cases(ra, R):
+    N = 2 * R * 4
+    h = N // (2 * R)
+    for s in range(R):
+        by_rank = {}
+        for seg in ra.ring_sim_plan(N, R, "zigzag", True, s):
+            by_rank.setdefault(seg["rank"], []).append(seg)
+        for r in range(R):
+            case = oring.zigzag_step_case(r, s, R)
+            segs = sorted(by_rank.get(r, []), key=lambda x: x["q"])
+            src = oring.kv_source(r, s, R)
+            front = (src * h, (src + 1) * h)
+            back = ((2 * R - 1 - src) * h, (2 * R - src) * h)
+            if case == "local":
+                assert [x["q"] for x in segs] == [(r * h, (r + 1) * h), ((2 * R - 1 - r) * h, (2 * R - r) * h)]
+            elif case == "front_kv":
+                assert len(segs) == 2 and all(x["kv"] == [front] for x in segs)
+            else:
+                assert len(segs) == 1 and segs[0]["q"] == ((2 * R - 1 - r) * h, (2 * R - r) * h)
+                assert segs[0]["kv"] == [front, back]
+
+
+def test_plan_contig_causal_block_classes(ra, golden_dir):
+    """Contiguous causal ring: rank r sees rank j's block iff j <= r (the page's three classes)."""
+    rows = []
+    for line in open(os.path.join(golden_dir, "causal_block_classes.txt")):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            qb, kb, cls = line.split()
+            rows.append((int(qb), int(kb), cls))
+    R, c = 8, 16
+    N = R * c
+    for qb, kb, cls in rows:
+        s = (qb - kb) % R  # the step at which rank qb holds block kb
+        segs = [x for x in ra.ring_sim_plan(N, R, "contig", True, s) if x["rank"] == qb]
+        if cls == "skip":
+            assert segs == []
+        else:
+            assert len(segs) == 1 and segs[0]["kv"] == [(kb * c, (kb + 1) * c)]
+            assert (kb == qb) == (cls == "diagonal")
+
+
+def test_plan_rejects_bad_arguments(ra):
+    with pytest.raises(ValueError):
+        ra.ring_sim_plan(100, 3, "contig", True, 0)
+    with pytest.raises(ValueError):
+        ra.ring_sim_plan(96, 3, "zigzag", True, 3)
