@@ -448,3 +448,168 @@ int64_t ra_launch_count(int reset) {
 int ra_version(void) { return 100; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- allocation-free ring run
+//
+// Some callers cannot let this library allocate device memory: a framework whose own
+// memory pool owns the device, a latency-critical loop where cudaMalloc/cudaFree would
+// synchronise the device, or a host application that hands a plugin only its input and
+// output buffers.  ra_ring_sim_fwd_noalloc serves them: the float32 running output that
+// ra_ring_sim_fwd keeps in a caller-provided workspace lives instead in the fixed array
+// below, and the call allocates nothing (no cudaMalloc/cudaFree, no host heap on success).
+//
+// The array is part of this module: every GPU that loads the library holds it until the
+// process exits.  Host code must not pass the array's name to a kernel (in host code it
+// is only a stand-in for the device symbol); the kernels get its device address, looked
+// up once per device with that device current.
+
+namespace {
+
+constexpr int64_t kNoAllocScratchFloats = (int64_t)8 << 20;  // 8 Mi floats = 32 MiB
+constexpr int kNoAllocMaxRing = kMaxSeg / 2;                  // one launch per ring step
+constexpr int kNoAllocMaxSeg = 2 * kNoAllocMaxRing;
+
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
+
+static float *g_noalloc_ptr[kMaxDev];
+
+// Set-up, once per device, with that device current: the scratch array's device address.
+static bool noalloc_scratch(int dev, float **out, std::string &msg) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) {
+            msg = std::string("cudaGetSymbolAddress(scratch): ") + cudaGetErrorString(e);
+            return false;
+        }
+        g_noalloc_ptr[dev] = static_cast<float *>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return true;
+}
+
+// Row ranges of rank r without a container: returns how many (1 or 2).
+static int noalloc_ranges(int64_t N, int R, int layout, int r, Range out[2]) {
+    if (layout == RA_LAYOUT_CONTIG) {
+        const int64_t c = N / R;
+        out[0] = {r * c, (r + 1) * c};
+        return 1;
+    }
+    const int64_t h = N / (2 * (int64_t)R);
+    out[0] = {r * h, (r + 1) * h};
+    out[1] = {(2 * (int64_t)R - 1 - r) * h, (2 * (int64_t)R - r) * h};
+    return 2;
+}
+
+static bool noalloc_touched(int64_t N, int R, int layout, int causal, int step, int r,
+                            int64_t q1) {
+    Range kv[2];
+    const int j = ((r - step) % R + R) % R;
+    const int nk = noalloc_ranges(N, R, layout, j, kv);
+    for (int i = 0; i < nk; ++i) {
+        if (kv[i].b <= kv[i].a) continue;
+        if (causal && kv[i].a > q1 - 1) continue;
+        return true;
+    }
+    return false;
+}
+
+// The same schedule as plan_step (same segments, flags and order) into a fixed array.
+static int noalloc_plan(int64_t N, int R, int layout, int causal, int step, Seg *segs) {
+    int n = 0;
+    for (int r = 0; r < R; ++r) {
+        Range qr[2], kv[2];
+        const int j = ((r - step) % R + R) % R;
+        const int nq = noalloc_ranges(N, R, layout, r, qr);
+        const int nkv = noalloc_ranges(N, R, layout, j, kv);
+        for (int qi = 0; qi < nq; ++qi) {
+            if (qr[qi].b <= qr[qi].a) continue;
+            Seg s;
+            memset(&s, 0, sizeof s);
+            s.q0 = (int32_t)qr[qi].a;
+            s.q1 = (int32_t)qr[qi].b;
+            int nk = 0;
+            for (int ki = 0; ki < nkv; ++ki) {
+                if (kv[ki].b <= kv[ki].a) continue;
+                if (causal && kv[ki].a > qr[qi].b - 1) continue;
+                s.k0[nk] = (int32_t)kv[ki].a;
+                s.k1[nk] = (int32_t)kv[ki].b;
+                ++nk;
+            }
+            if (nk == 0) continue;
+            if (nk == 1) s.k0[1] = s.k1[1] = s.k1[0];
+            s.rank = r;
+            bool earlier = false, later = false;
+            for (int t = 0; t < step && !earlier; ++t)
+                earlier = noalloc_touched(N, R, layout, causal, t, r, s.q1);
+            for (int t = step + 1; t < R && !later; ++t)
+                later = noalloc_touched(N, R, layout, causal, t, r, s.q1);
+            s.flags = (earlier ? 0 : SEG_FIRST) | (later ? 0 : SEG_FINAL);
+            // stable insertion by descending key count (the order plan_step produces)
+            const int64_t c = (int64_t)(s.k1[0] - s.k0[0]) + (s.k1[1] - s.k0[1]);
+            int at = n;
+            while (at > 0) {
+                const Seg &p = segs[at - 1];
+                const int64_t cp = (int64_t)(p.k1[0] - p.k0[0]) + (p.k1[1] - p.k0[1]);
+                if (cp >= c) break;
+                segs[at] = segs[at - 1];
+                --at;
+            }
+            segs[at] = s;
+            ++n;
+        }
+    }
+    return n;
+}
+
+}  // namespace
+
+extern "C" ra_status ra_ring_sim_fwd_noalloc(const ra_tensor *q, const ra_tensor *k,
+                                             const ra_tensor *v, ra_tensor *o, float *lse,
+                                             int ring_size, ra_layout layout, int causal,
+                                             float scale, void *stream) {
+    Problem pb;
+    ra_status s = check_qkvo(q, k, v, o, lse, pb);
+    if (s) return s;
+    if (isnan(scale)) return fail(RA_ERR_INVALID_ARG, "scale is NaN");
+    if ((s = check_ring(pb.N, ring_size, layout))) return s;
+    if (ring_size > kNoAllocMaxRing)
+        return fail(RA_ERR_UNSUPPORTED, "ra_ring_sim_fwd_noalloc: ring_size above 64");
+    if (pb.B * pb.Hq * pb.N == 0) return RA_OK;
+    if (ring_size > 1 && pb.B * pb.Hq * pb.N * pb.D > kNoAllocScratchFloats)
+        return fail(RA_ERR_UNSUPPORTED,
+                    "ra_ring_sim_fwd_noalloc: B*Hq*N*D exceeds its fixed scratch of 8Mi floats "
+                    "(32 MiB); use ra_ring_sim_fwd with a caller-provided workspace");
+    DevInfo di;
+    std::string msg;
+    if (!device_info(di, msg)) return fail(RA_ERR_CUDA, msg);
+    float *scratch = nullptr;
+    if (ring_size > 1 && !noalloc_scratch(di.dev, &scratch, msg)) return fail(RA_ERR_CUDA, msg);
+    StepParams P;
+    fill_common(P, q, k, v, o, lse, pb, causal, scale, di);
+    P.oacc = scratch;
+    const bool tc = use_tensor_cores(q, k, v, o, pb, di);
+    const int rows_per_block = tc ? attn_tc_rows_per_block() : 16;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Seg segs[kNoAllocMaxSeg];
+    for (int step = 0; step < ring_size; ++step) {
+        const int n = noalloc_plan(pb.N, ring_size, layout, causal, step, segs);
+        if (n == 0) continue;
+        int64_t qlen = 0;
+        for (int i = 0; i < n; ++i) {
+            P.seg[i] = segs[i];
+            qlen = std::max<int64_t>(qlen, segs[i].q1 - segs[i].q0);
+        }
+        P.nseg = n;
+        P.rows_per_block = rows_per_block;
+        P.blocks_per_seg = (int32_t)((qlen + rows_per_block - 1) / rows_per_block);
+        const int64_t blocks_y = (int64_t)P.nseg * P.blocks_per_seg;
+        if (blocks_y > 65535) return fail(RA_ERR_UNSUPPORTED, "too many work blocks in one step");
+        cudaError_t e = tc ? launch_attn_tc(P, (int)blocks_y, st)
+                           : launch_attn_simt(P, (int)blocks_y, st);
+        if (e != cudaSuccess) return cuda_fail(e, "attention launch (no-alloc)");
+        ++t_launches;
+    }
+    return RA_OK;
+}

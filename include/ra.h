@@ -150,6 +150,30 @@ int64_t ra_ring_sim_plan(int64_t N, int ring_size, ra_layout layout, int causal,
                          int64_t *segments, int64_t cap);
 
 /*
+ * ra_ring_sim_fwd_noalloc - ra_ring_sim_fwd for callers that cannot have device memory
+ * allocated on their behalf: a framework whose memory pool owns the device, a
+ * latency-critical loop where cudaMalloc/cudaFree would synchronise the device, or a
+ * host application that gives a plugin only its input and output buffers.  The pages
+ * have no counterpart; this is a property of the library, not of the method.
+ *
+ * Same arguments, result and errors as ra_ring_sim_fwd, without the workspace: the
+ * float32 running output lives in a fixed device array inside the library, 8 Mi floats
+ * (32 MiB), which every GPU that loads the library holds until the process exits.
+ *   - B*Hq*N*D must be <= 8388608 when ring_size > 1, and ring_size <= 64; larger
+ *     problems get RA_ERR_UNSUPPORTED (use ra_ring_sim_fwd with a workspace).
+ *   - The call allocates nothing: no cudaMalloc/cudaFree, no host heap on success.
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - Every call shares the array and it keeps the last call's contents.  Nothing in
+ *     it needs clearing: each row's first partial is written, never merged.  Calls
+ *     that overlap on the GPU (different streams, or different host threads) race on
+ *     it: serialise them.
+ */
+ra_status ra_ring_sim_fwd_noalloc(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v,
+                                  ra_tensor *o, float *lse, int ring_size, ra_layout layout,
+                                  int causal, float scale, void *stream);
+
+/*
  * ra_check_device_error - synchronise `stream`, then read and clear the device error
  * word of the current device.  RA_ERR_TIMEOUT if a kernel recorded a wait timeout,
  * RA_ERR_CUDA if the synchronisation failed, else RA_OK.
