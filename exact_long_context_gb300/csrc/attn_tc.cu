@@ -112,7 +112,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Wait for the phase of parity `parity` of `bar` to complete.  Returns false if the
 // CTA is aborting (this wait exceeded `limit_ns`, or another role gave up first).
-__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int32_t *abort,
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int32_t *abort,
                                         int64_t limit_ns, int *err) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
@@ -130,7 +130,7 @@ __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile 
 }
 
 // Bounded wait used only while winding down (own copies / MMAs in flight).
-__device__ __noinline__ void wait_phase_drain(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ void wait_phase_drain(uint32_t bar, uint32_t parity) {
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(bar, parity)) {
         if ((int64_t)(globaltimer() - t0) > kDrainLimitNs) return;
@@ -255,6 +255,51 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Register split between warpgroups (launch: 168 per thread x 384 threads = 64512).
+// Warpgroup 0 (TMA + MMA warps) gives back to 72, the two softmax warpgroups take 216:
+// 72 * 128 + 216 * 256 = 64512.  (setmaxnreg needs the waits inlined: no calls.)
+constexpr uint32_t kRegsControl = 72;
+constexpr uint32_t kRegsSoftmax = 216;
+static_assert(kRegsControl * 128 + kRegsSoftmax * 256 <= 168 * 384, "register split");
+
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Two fp32 lanes in one 64-bit register (low = first) for the paired f32x2 ops.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -356,7 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp == 0) {
+    if (warp < 4) {
+      regs_dec<kRegsControl>();
+      if (warp == 0) {
         // ================= TMA producer
         if (lane == 0) {
             prefetch_tmap(&tm_q);
@@ -404,12 +451,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         wait_phase_drain(smem_u32(&bars->full[s]), (last_ph >> s) & 1u);
             }
         }
-    } else if (warp == 1) {
+      } else if (warp == 1) {
         // ================= MMA issuer
         if (lane == 0) {
             constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false);
             constexpr uint32_t IDESC_PV = idesc_bf16(BM, HD, true);
-            auto issue_qk = [&](int hh, int kslot) {
+            auto issue_qk = [=](int hh, int kslot) {
                 const uint32_t d = tmem + (hh ? C::TM_S1 : C::TM_S0);
                 const uint32_t qa = sQ + hh * C::TILE_BYTES;
                 const uint32_t kb = sKV + kslot * C::TILE_BYTES;
@@ -420,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            IDESC_QK, k > 0 ? 1u : 0u);
                 }
             };
-            auto issue_pv = [&](int hh, int vslot, bool acc_in) {
+            auto issue_pv = [=](int hh, int vslot, bool acc_in) {
                 const uint32_t d = tmem + (hh ? C::TM_O1 : C::TM_O0);
                 const uint32_t p = tmem + (hh ? C::TM_S1 : C::TM_S0);
                 const uint32_t vb = sKV + vslot * C::TILE_BYTES;
@@ -496,12 +543,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(b_drain);
             wait_phase_drain(b_drain, 0);
         }
-    } else if (warp >= 4) {
+      }
+    } else {
+        regs_inc<kRegsSoftmax>();
         // ================= softmax (+ O rescale and epilogue) of one half
         const int hh = (warp - 4) >> 2;
         const int quarter = warp & 3;
         const int row_g = qrow0 + hh * BM + quarter * 32 + lane;
-        const int n = nh[hh];
+        const int n = hh ? nh[1] : nh[0];
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem + (hh ? C::TM_S1 : C::TM_S0) + lane_off;
         const uint32_t tO = tmem + (hh ? C::TM_O1 : C::TM_O0) + lane_off;
@@ -531,9 +580,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 128; ++c)
                     if (c >= lim) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
             }
-            float mx = __uint_as_float(r[0][0]);
+            // row max: four independent chains of 3-input max (depth 16, not 127)
+            float mc[4];
 #pragma unroll
-            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(r[c >> 5][c & 31]));
+            for (int j = 0; j < 4; ++j) mc[j] = __uint_as_float(r[j][0]);
+#pragma unroll
+            for (int i = 1; i < 31; i += 2)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    mc[j] = fmax3(mc[j], __uint_as_float(r[j][i]), __uint_as_float(r[j][i + 1]));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) mc[j] = fmaxf(mc[j], __uint_as_float(r[j][31]));
+            const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
             const float m_tile = mx * sl2;
             float alpha = 1.f;
             bool resc = false;
@@ -545,20 +603,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 resc = true;
             }
             const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
-            float rs = 0.f;
+            // p = 2^(s * scale * log2e - m): paired FFMA, one ex2 per element, bf16 pack,
+            // four paired partial sums; the first 64 keys go to tensor memory while the
+            // rest are computed
+            const uint64_t sl2x2 = pack_f32x2(sl2, sl2);
+            const uint64_t negm2 = pack_f32x2(neg_m, neg_m);
+            uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int c = j * 64 + 2 * i;
-                    const float p0 = ex2(fmaf(__uint_as_float(r[c >> 5][c & 31]), sl2, neg_m));
-                    const float p1 =
-                        ex2(fmaf(__uint_as_float(r[(c + 1) >> 5][(c + 1) & 31]), sl2, neg_m));
-                    rs += p0 + p1;
+                    const uint64_t x = ffma2(pack_f32x2(__uint_as_float(r[c >> 5][c & 31]),
+                                                        __uint_as_float(r[c >> 5][(c & 31) + 1])),
+                                             sl2x2, negm2);
+                    float x0, x1;
+                    unpack_f32x2(x, x0, x1);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    acc2[i & 3] = fadd2(acc2[i & 3], pack_f32x2(p0, p1));
                     pk[i] = pack_bf16x2(p0, p1);
                 }
                 tmem_st32(tS + j * 32, pk);
+            }
+            float rs;
+            {
+                const uint64_t a = fadd2(fadd2(acc2[0], acc2[1]), fadd2(acc2[2], acc2[3]));
+                float a0, a1;
+                unpack_f32x2(a, a0, a1);
+                rs = a0 + a1;
             }
             l = l * alpha + rs;
             if (t > 0 && __any_sync(0xffffffffu, resc)) {
