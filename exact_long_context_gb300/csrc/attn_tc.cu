@@ -36,6 +36,9 @@
 // DERR_TIMEOUT in the device error word, every role stops, waits (bounded) for its
 // own copies and MMAs in flight, and the tensor memory is released before exit.
 #include <cuda.h>
+#include <string.h>
+
+#include <algorithm>
 
 #include "ra_internal.cuh"
 
@@ -61,7 +64,8 @@ struct Cfg {
 };
 
 struct Bars {
-    uint64_t q_full;
+    uint64_t q_full[2];
+    uint64_t q_empty[2];
     uint64_t full[8];
     uint64_t empty[8];
     uint64_t s_full[2];
@@ -233,6 +237,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "r"(taddr));
 }
 
+// 16 consecutive 32-bit columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : RA_R8(0), RA_R8(8)
+        : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -256,10 +269,10 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // Register split between warpgroups (launch: 168 per thread x 384 threads = 64512).
-// Warpgroup 0 (TMA + MMA warps) gives back to 72, the two softmax warpgroups take 216:
-// 72 * 128 + 216 * 256 = 64512.  (setmaxnreg needs the waits inlined: no calls.)
-constexpr uint32_t kRegsControl = 72;
-constexpr uint32_t kRegsSoftmax = 216;
+// Warpgroup 0 (TMA + MMA warps) gives back to 88, the two softmax warpgroups take 208:
+// 88 * 128 + 208 * 256 = 64512.  (setmaxnreg needs the waits inlined: no calls.)
+constexpr uint32_t kRegsControl = 88;
+constexpr uint32_t kRegsSoftmax = 208;
 static_assert(kRegsControl * 128 + kRegsSoftmax * 256 <= 168 * 384, "register split");
 
 template <uint32_t N>
@@ -325,7 +338,71 @@ struct KTiles {
     }
 };
 
+// ---------------------------------------------------------------- work items
+
+// One work item: 256 query rows (two 128-row halves) of one (batch, head) against the
+// key tiles of one segment.  Every role decodes the same items in the same order.
+struct Item {
+    int b, h, hk;
+    int qrow0, q1;
+    int flags;
+    int nh[2];  // key tiles each half iterates (a prefix of the segment's tiles)
+    int nmax;
+    KTiles kt;
+};
+
+// Item L of a launch: L = w * (B*Hq) + bh, so the heaviest work blocks of every head
+// come first.  A persistent CTA takes one item per round of gridDim.x items, in snake
+// order (forward in even rounds, backward in odd ones) so that the heavy and light
+// ends of the cost-sorted list even out across CTAs.
+__device__ __forceinline__ int snake_item(int k) {
+    const int G = gridDim.x;
+    return k * G + ((k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
+}
+
+__device__ __forceinline__ void decode_item(const StepParams &P, int L, Item &it) {
+    const int BH = P.B * P.Hq;
+    const int w = L / BH;
+    const int bh = L - w * BH;
+    it.b = bh / P.Hq;
+    it.h = bh - it.b * P.Hq;
+    it.hk = it.h / (P.Hq / P.Hkv);
+    int si, lb;
+    decode_work(P, w, si, lb);
+    it.nmax = 0;
+    it.nh[0] = it.nh[1] = 0;
+    if (lb < 0) return;
+    const Seg &S = P.seg[si];
+    it.qrow0 = S.q0 + lb * 2 * BM;
+    it.q1 = S.q1;
+    it.flags = S.flags;
+    it.kt.k0[0] = S.k0[0];
+    it.kt.k1[0] = S.k1[0];
+    it.kt.k0[1] = S.k0[1];
+    it.kt.k1[1] = S.k1[1];
+    it.kt.nt0 = (S.k1[0] > S.k0[0]) ? (S.k1[0] - S.k0[0] + BN - 1) / BN : 0;
+    it.kt.ntot = it.kt.nt0 + ((S.k1[1] > S.k0[1]) ? (S.k1[1] - S.k0[1] + BN - 1) / BN : 0);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const int r0 = it.qrow0 + hh * BM;
+        if (r0 >= S.q1)
+            it.nh[hh] = 0;
+        else if (!P.causal)
+            it.nh[hh] = it.kt.ntot;
+        else
+            it.nh[hh] = it.kt.visible_prefix(min(r0 + BM, S.q1) - 1);
+    }
+    it.nmax = max(it.nh[0], it.nh[1]);
+}
+
 // ---------------------------------------------------------------- the kernel
+//
+// Persistent: one CTA per SM walks its work items.  Barrier phases run on across items
+// (every wait uses a running count), so the next item's Q/K/V loads and first Q K^T
+// overlap the current item's last P V products and epilogue.  Q_h is reloaded once
+// the MMA thread has issued the item's last Q_h K^T (q_empty[h]); the softmax
+// warpgroup of half h finishes its epilogue (reads O_h) before it signals the next
+// item's first P_h, and only then is O_h overwritten.
 
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -341,46 +418,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     Bars *bars = reinterpret_cast<Bars *>(base_ptr + (2 + C::NSLOT) * C::TILE_BYTES);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = P.total_items;
+    if ((int)blockIdx.x >= total) return;
 
-    // ---- work decode (uniform over the CTA)
-    const int bh = blockIdx.x;
-    const int b = bh / P.Hq, h = bh - (bh / P.Hq) * P.Hq;
-    const int hk = h / (P.Hq / P.Hkv);
-    int si, lb;
-    decode_work(P, blockIdx.y, si, lb);
-    if (lb < 0) return;
-    const Seg &S = P.seg[si];
-    const int qrow0 = S.q0 + lb * 2 * BM;
-    KTiles kt;
-    kt.k0[0] = S.k0[0];
-    kt.k1[0] = S.k1[0];
-    kt.k0[1] = S.k0[1];
-    kt.k1[1] = S.k1[1];
-    kt.nt0 = (S.k1[0] > S.k0[0]) ? (S.k1[0] - S.k0[0] + BN - 1) / BN : 0;
-    kt.ntot = kt.nt0 + ((S.k1[1] > S.k0[1]) ? (S.k1[1] - S.k0[1] + BN - 1) / BN : 0);
-    int nh[2];
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        const int r0 = qrow0 + hh * BM;
-        if (r0 >= S.q1) {
-            nh[hh] = 0;
-        } else if (!P.causal) {
-            nh[hh] = kt.ntot;
-        } else {
-            nh[hh] = kt.visible_prefix(min(r0 + BM, S.q1) - 1);
-        }
-    }
-    const int nmax = max(nh[0], nh[1]);
-    if (nmax == 0) return;
-
-    const uint32_t b_q = smem_u32(&bars->q_full);
     const uint32_t b_drain = smem_u32(&bars->drain);
     volatile int32_t *abort_flag = &bars->abort;
 
-    // ---- set-up
+    // ---- set-up (once per CTA)
     if (threadIdx.x == 0) {
         bars->abort = 0;
-        mbar_init(b_q, 1);
 #pragma unroll
         for (int s = 0; s < C::NSLOT; ++s) {
             mbar_init(smem_u32(&bars->full[s]), 1);
@@ -388,8 +434,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
+            mbar_init(smem_u32(&bars->q_full[hh]), 1);
+            mbar_init(smem_u32(&bars->q_empty[hh]), 1);
             mbar_init(smem_u32(&bars->s_full[hh]), 1);
-            mbar_init(smem_u32(&bars->p_full[hh]), 128);
+            mbar_init(smem_u32(&bars->p_full[hh]), 4);  // one elected lane per softmax warp
             mbar_init(smem_u32(&bars->o_full[hh]), 1);
         }
         mbar_init(b_drain, 1);
@@ -400,6 +448,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    // The next ring step's kernel may start on SMs this grid frees; it only waits for
+    // this grid before its epilogue touches the running result (griddepcontrol.wait).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp < 4) {
       regs_dec<kRegsControl>();
@@ -409,21 +460,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            mbar_expect_tx(b_q, 2 * C::TILE_BYTES);
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                for (int c = 0; c < C::SLABS; ++c)
-                    tma_load_4d(sQ + hh * C::TILE_BYTES + c * C::SLAB_BYTES, &tm_q, b_q, c * 64,
-                                qrow0 + hh * BM, h, b);
             int slot = 0;
             uint32_t ph = 0;
             uint32_t issued = 0, last_ph = 0;  // per-slot bit sets
+            uint32_t qcnt[2] = {0u, 0u};       // Q_h loads issued
             bool ok = true;
-            for (int t = 0; t < nmax && ok; ++t) {
-                const int ks = kt.start(t);
-#pragma unroll 1
-                for (int which = 0; which < 2; ++which) {
+            for (int k = 0; k * (int)gridDim.x < total && ok; ++k) {
+                const int L = snake_item(k);
+                if (L >= total) continue;
+                Item it;
+                decode_item(P, L, it);
+                if (it.nmax == 0) continue;
+                // K_0 first (it only needs a free slot), then Q (which waits until the
+                // previous item has issued its last Q K^T), then V_0, K_1, V_1, ...
+                for (int seq = 0; seq < 2 * it.nmax && ok; ++seq) {
+                    const int t = seq >> 1;
+                    const int which = seq & 1;  // 0 = K_t, 1 = V_t
                     const uint32_t b_empty = smem_u32(&bars->empty[slot]);
                     const uint32_t b_full = smem_u32(&bars->full[slot]);
                     if (!wait_phase(b_empty, ph ^ 1u, abort_flag, P.wait_limit_ns, P.err)) {
@@ -432,23 +484,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     mbar_expect_tx(b_full, C::TILE_BYTES);
                     const CUtensorMap *m = which ? &tm_v : &tm_k;
+                    const int ks = it.kt.start(t);
 #pragma unroll
                     for (int c = 0; c < C::SLABS; ++c)
                         tma_load_4d(sKV + slot * C::TILE_BYTES + c * C::SLAB_BYTES, m, b_full,
-                                    c * 64, ks, hk, b);
+                                    c * 64, ks, it.hk, it.b);
                     issued |= 1u << slot;
                     last_ph = (last_ph & ~(1u << slot)) | (ph << slot);
                     if (++slot == C::NSLOT) {
                         slot = 0;
                         ph ^= 1u;
                     }
+                    if (seq == 0) {
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            if (it.nh[hh] == 0 || !ok) continue;
+                            const uint32_t qf = smem_u32(&bars->q_full[hh]);
+                            if (!wait_phase(smem_u32(&bars->q_empty[hh]), (qcnt[hh] & 1u) ^ 1u,
+                                            abort_flag, P.wait_limit_ns, P.err)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_expect_tx(qf, C::TILE_BYTES);
+#pragma unroll
+                            for (int c = 0; c < C::SLABS; ++c)
+                                tma_load_4d(sQ + hh * C::TILE_BYTES + c * C::SLAB_BYTES, &tm_q, qf,
+                                            c * 64, it.qrow0 + hh * BM, it.h, it.b);
+                            ++qcnt[hh];
+                        }
+                    }
                 }
             }
             if (!ok) {  // wind down: let every copy this thread issued land
-                wait_phase_drain(b_q, 0);
-                for (int s = 0; s < C::NSLOT; ++s)
-                    if (issued & (1u << s))
-                        wait_phase_drain(smem_u32(&bars->full[s]), (last_ph >> s) & 1u);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+                    if (qcnt[hh]) wait_phase_drain(smem_u32(&bars->q_full[hh]), (qcnt[hh] - 1u) & 1u);
+                for (int s2 = 0; s2 < C::NSLOT; ++s2)
+                    if (issued & (1u << s2))
+                        wait_phase_drain(smem_u32(&bars->full[s2]), (last_ph >> s2) & 1u);
             }
         }
       } else if (warp == 1) {
@@ -477,67 +550,87 @@ __global__ void __launch_bounds__(kThreads, 1)
                            IDESC_PV, (acc_in || k > 0) ? 1u : 0u);
                 }
             };
-            bool ok = wait_phase(b_q, 0, abort_flag, P.wait_limit_ns, P.err);
             int slot = 0;
             uint32_t ph = 0;
-            if (ok) {
-                tc_fence_after();
+            uint32_t qcnt[2] = {0u, 0u};  // Q_h loads consumed
+            uint32_t pcnt[2] = {0u, 0u};  // P_h tiles consumed
+            bool ok = true;
+            for (int k = 0; k * (int)gridDim.x < total && ok; ++k) {
+                const int L = snake_item(k);
+                if (L >= total) continue;
+                Item it;
+                decode_item(P, L, it);
+                if (it.nmax == 0) continue;
+                const int n0 = it.nh[0], n1 = it.nh[1];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    if ((hh ? n1 : n0) == 0 || !ok) continue;
+                    ok = wait_phase(smem_u32(&bars->q_full[hh]), qcnt[hh] & 1u, abort_flag,
+                                    P.wait_limit_ns, P.err);
+                    ++qcnt[hh];
+                }
+                if (!ok) break;
                 ok = wait_phase(smem_u32(&bars->full[slot]), ph, abort_flag, P.wait_limit_ns, P.err);
-            }
-            if (ok) {
+                if (!ok) break;
                 tc_fence_after();
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-                    if (nh[hh] > 0) {
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int nhh = hh ? n1 : n0;
+                    if (nhh > 0) {
                         issue_qk(hh, slot);
                         mma_commit(smem_u32(&bars->s_full[hh]));
+                        if (nhh == 1) mma_commit(smem_u32(&bars->q_empty[hh]));
                     }
+                }
                 mma_commit(smem_u32(&bars->empty[slot]));
                 if (++slot == C::NSLOT) {
                     slot = 0;
                     ph ^= 1u;
                 }
-            }
-            for (int t = 0; ok && t < nmax; ++t) {
-                const int vslot = slot;
-                ok = wait_phase(smem_u32(&bars->full[vslot]), ph, abort_flag, P.wait_limit_ns,
-                                P.err);
-                if (!ok) break;
-                if (++slot == C::NSLOT) {
-                    slot = 0;
-                    ph ^= 1u;
-                }
-                const bool has_next = t + 1 < nmax;
-                const int kslot = slot;
-                if (has_next) {
-                    ok = wait_phase(smem_u32(&bars->full[kslot]), ph, abort_flag, P.wait_limit_ns,
+                for (int t = 0; ok && t < it.nmax; ++t) {
+                    const int vslot = slot;
+                    ok = wait_phase(smem_u32(&bars->full[vslot]), ph, abort_flag, P.wait_limit_ns,
                                     P.err);
                     if (!ok) break;
                     if (++slot == C::NSLOT) {
                         slot = 0;
                         ph ^= 1u;
                     }
-                }
-                tc_fence_after();
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    if (t < nh[hh]) {
-                        ok = wait_phase(smem_u32(&bars->p_full[hh]), (uint32_t)(t & 1), abort_flag,
+                    const bool has_next = t + 1 < it.nmax;
+                    const int kslot = slot;
+                    if (has_next) {
+                        ok = wait_phase(smem_u32(&bars->full[kslot]), ph, abort_flag,
                                         P.wait_limit_ns, P.err);
                         if (!ok) break;
-                        tc_fence_after();
-                        issue_pv(hh, vslot, t > 0);
-                        if (t + 1 < nh[hh]) {
-                            issue_qk(hh, kslot);
-                            mma_commit(smem_u32(&bars->s_full[hh]));
-                        } else {
-                            mma_commit(smem_u32(&bars->o_full[hh]));
+                        if (++slot == C::NSLOT) {
+                            slot = 0;
+                            ph ^= 1u;
                         }
                     }
+                    tc_fence_after();
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int nhh = hh ? n1 : n0;
+                        if (t < nhh) {
+                            ok = wait_phase(smem_u32(&bars->p_full[hh]), pcnt[hh] & 1u, abort_flag,
+                                            P.wait_limit_ns, P.err);
+                            ++pcnt[hh];
+                            if (!ok) break;
+                            tc_fence_after();
+                            issue_pv(hh, vslot, t > 0);
+                            if (t + 1 < nhh) {
+                                issue_qk(hh, kslot);
+                                mma_commit(smem_u32(&bars->s_full[hh]));
+                                if (t + 2 == nhh) mma_commit(smem_u32(&bars->q_empty[hh]));
+                            } else {
+                                mma_commit(smem_u32(&bars->o_full[hh]));
+                            }
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(smem_u32(&bars->empty[vslot]));
+                    if (has_next) mma_commit(smem_u32(&bars->empty[kslot]));
                 }
-                if (!ok) break;
-                mma_commit(smem_u32(&bars->empty[vslot]));
-                if (has_next) mma_commit(smem_u32(&bars->empty[kslot]));
             }
             // every MMA this thread issued completes before tensor memory is released
             mma_commit(b_drain);
@@ -549,168 +642,198 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================= softmax (+ O rescale and epilogue) of one half
         const int hh = (warp - 4) >> 2;
         const int quarter = warp & 3;
-        const int row_g = qrow0 + hh * BM + quarter * 32 + lane;
-        const int n = hh ? nh[1] : nh[0];
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem + (hh ? C::TM_S1 : C::TM_S0) + lane_off;
         const uint32_t tO = tmem + (hh ? C::TM_O1 : C::TM_O0) + lane_off;
         const uint32_t b_s = smem_u32(&bars->s_full[hh]);
         const uint32_t b_p = smem_u32(&bars->p_full[hh]);
+        const uint32_t b_o = smem_u32(&bars->o_full[hh]);
         const float sl2 = P.scale_log2;
-        const int first_row = qrow0 + hh * BM;
-        float m_ref = -INFINITY, l = 0.f;
+        uint32_t scnt = 0, ocnt = 0;  // S_h tiles and O_h results seen
         bool ok = true;
-        for (int t = 0; t < n; ++t) {
-            ok = wait_phase(b_s, (uint32_t)(t & 1), abort_flag, P.wait_limit_ns, P.err);
+        for (int k = 0; k * (int)gridDim.x < total && ok; ++k) {
+                const int L = snake_item(k);
+                if (L >= total) continue;
+            Item it;
+            decode_item(P, L, it);
+            const int n = hh ? it.nh[1] : it.nh[0];
+            if (it.nmax == 0 || n == 0) continue;
+            const int first_row = it.qrow0 + hh * BM;
+            const int row_g = first_row + quarter * 32 + lane;
+            if (P.oacc && !(it.flags & SEG_FIRST) && row_g < it.q1) {
+                // the running row is read by this item's epilogue: stage it in L2 now
+                const float *pre = P.oacc + (((int64_t)it.b * P.Hq + it.h) * P.N + row_g) * HD;
+#pragma unroll
+                for (int i = 0; i < HD * 4 / 128; ++i)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(pre + i * 32));
+            }
+            float m_ref = -INFINITY, l = 0.f;
+            for (int t = 0; t < n; ++t) {
+                ok = wait_phase(b_s, scnt & 1u, abort_flag, P.wait_limit_ns, P.err);
+                ++scnt;
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t r[4][32];
+                tmem_ld32(tS + 0, r[0]);
+                tmem_ld32(tS + 32, r[1]);
+                tmem_ld32(tS + 64, r[2]);
+                tmem_ld32(tS + 96, r[3]);
+                tmem_ld_wait();
+                const int ks = it.kt.start(t);
+                const int ke = it.kt.range_end(t);
+                const bool need_mask =
+                    (ks + BN > ke) || (P.causal && (min(ks + BN, ke) - 1 > first_row));
+                if (need_mask) {
+                    const int lim = (P.causal ? min(ke, row_g + 1) : ke) - ks;
+#pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (c >= lim) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+                }
+                // row max: eight independent chains of 3-input max
+                float mc[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int c0 = j * 16;
+                    float m = fmax3(__uint_as_float(r[c0 >> 5][c0 & 31]),
+                                    __uint_as_float(r[c0 >> 5][(c0 & 31) + 1]),
+                                    __uint_as_float(r[c0 >> 5][(c0 & 31) + 2]));
+#pragma unroll
+                    for (int i = 3; i < 15; i += 2)
+                        m = fmax3(m, __uint_as_float(r[c0 >> 5][(c0 & 31) + i]),
+                                  __uint_as_float(r[c0 >> 5][(c0 & 31) + i + 1]));
+                    mc[j] = fmaxf(m, __uint_as_float(r[c0 >> 5][(c0 & 31) + 15]));
+                }
+                const float mx = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]),
+                                       fmaxf(mc[6], mc[7]));
+                const float m_tile = mx * sl2;
+                float alpha = 1.f;
+                bool resc = false;
+                if (t == 0) {
+                    m_ref = m_tile;
+                } else if (m_tile > m_ref + kRescaleThreshold) {
+                    alpha = ex2(m_ref - m_tile);
+                    m_ref = m_tile;
+                    resc = true;
+                }
+                const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+                // p = 2^(s * scale * log2e - m): paired FFMA, one ex2 per element, bf16
+                // pack, four paired partial sums; the first 64 keys go to tensor memory
+                // while the rest are computed
+                const uint64_t sl2x2 = pack_f32x2(sl2, sl2);
+                const uint64_t negm2 = pack_f32x2(neg_m, neg_m);
+                uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int c = j * 64 + 2 * i;
+                        const uint64_t x =
+                            ffma2(pack_f32x2(__uint_as_float(r[c >> 5][c & 31]),
+                                             __uint_as_float(r[c >> 5][(c & 31) + 1])),
+                                  sl2x2, negm2);
+                        float x0, x1;
+                        unpack_f32x2(x, x0, x1);
+                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        acc2[i & 3] = fadd2(acc2[i & 3], pack_f32x2(p0, p1));
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st32(tS + j * 32, pk);
+                }
+                float rs;
+                {
+                    const uint64_t a = fadd2(fadd2(acc2[0], acc2[1]), fadd2(acc2[2], acc2[3]));
+                    float a0, a1;
+                    unpack_f32x2(a, a0, a1);
+                    rs = a0 + a1;
+                }
+                l = l * alpha + rs;
+                if (t > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+                    for (int c = 0; c < HD / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(tO + c * 32, o);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_p);
+            }
+            if (!ok) break;
+            // ---- epilogue: O / l, LSE, then write or LSE-merge into the running result.
+            // (The running row was staged in L2 at the start of the item.)
+            // the previous ring step wrote the running result (o_acc, lse) and, for its
+            // last rows, O: wait for that grid before reading or writing them
+            if (P.chained) asm volatile("griddepcontrol.wait;" ::: "memory");
+            const bool first = (it.flags & SEG_FIRST) != 0;
+            const bool final_ = (it.flags & SEG_FINAL) != 0;
+            const int64_t lrow = ((int64_t)it.b * P.Hq + it.h) * P.N + row_g;
+            const bool valid = row_g < it.q1;
+            const bool merge = valid && !first;
+            float *arow = P.oacc ? P.oacc + lrow * HD : nullptr;
+            const float lse_a = merge ? P.lse[lrow] : -INFINITY;
+            ok = wait_phase(b_o, ocnt & 1u, abort_flag, P.wait_limit_ns, P.err);
+            ++ocnt;
             if (!ok) break;
             tc_fence_after();
-            uint32_t r[4][32];
-            tmem_ld32(tS + 0, r[0]);
-            tmem_ld32(tS + 32, r[1]);
-            tmem_ld32(tS + 64, r[2]);
-            tmem_ld32(tS + 96, r[3]);
-            tmem_ld_wait();
-            const int ks = kt.start(t);
-            const int ke = kt.range_end(t);
-            const bool need_mask =
-                (ks + BN > ke) || (P.causal && (min(ks + BN, ke) - 1 > first_row));
-            if (need_mask) {
-                const int lim = (P.causal ? min(ke, row_g + 1) : ke) - ks;
-#pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (c >= lim) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
-            }
-            // row max: four independent chains of 3-input max (depth 16, not 127)
-            float mc[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) mc[j] = __uint_as_float(r[j][0]);
-#pragma unroll
-            for (int i = 1; i < 31; i += 2)
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    mc[j] = fmax3(mc[j], __uint_as_float(r[j][i]), __uint_as_float(r[j][i + 1]));
-#pragma unroll
-            for (int j = 0; j < 4; ++j) mc[j] = fmaxf(mc[j], __uint_as_float(r[j][31]));
-            const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
-            const float m_tile = mx * sl2;
-            float alpha = 1.f;
-            bool resc = false;
-            if (t == 0) {
-                m_ref = m_tile;
-            } else if (m_tile > m_ref + kRescaleThreshold) {
-                alpha = ex2(m_ref - m_tile);
-                m_ref = m_tile;
-                resc = true;
-            }
-            const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
-            // p = 2^(s * scale * log2e - m): paired FFMA, one ex2 per element, bf16 pack,
-            // four paired partial sums; the first 64 keys go to tensor memory while the
-            // rest are computed
-            const uint64_t sl2x2 = pack_f32x2(sl2, sl2);
-            const uint64_t negm2 = pack_f32x2(neg_m, neg_m);
-            uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int c = j * 64 + 2 * i;
-                    const uint64_t x = ffma2(pack_f32x2(__uint_as_float(r[c >> 5][c & 31]),
-                                                        __uint_as_float(r[c >> 5][(c & 31) + 1])),
-                                             sl2x2, negm2);
-                    float x0, x1;
-                    unpack_f32x2(x, x0, x1);
-                    const float p0 = ex2(x0), p1 = ex2(x1);
-                    acc2[i & 3] = fadd2(acc2[i & 3], pack_f32x2(p0, p1));
-                    pk[i] = pack_bf16x2(p0, p1);
-                }
-                tmem_st32(tS + j * 32, pk);
-            }
-            float rs;
-            {
-                const uint64_t a = fadd2(fadd2(acc2[0], acc2[1]), fadd2(acc2[2], acc2[3]));
-                float a0, a1;
-                unpack_f32x2(a, a0, a1);
-                rs = a0 + a1;
-            }
-            l = l * alpha + rs;
-            if (t > 0 && __any_sync(0xffffffffu, resc)) {
+            const bool have = l > 0.f;
+            const float lse_b = have ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+            const float inv = have ? 1.f / l : 0.f;
+            MergeW w;
+            w.wa = 0.f;
+            w.wb = 1.f;
+            w.L = lse_b;
+            if (merge) w = merge_weights(lse_a, lse_b);
+            const bool use_prev = merge && w.wa != 0.f;
+            const float wb = w.wb * inv;
+            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(P.o) + (int64_t)it.b * P.so[0] +
+                                  (int64_t)it.h * P.so[1] + (int64_t)row_g * P.so[2];
 #pragma unroll 1
-                for (int c = 0; c < HD / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + c * 32, o);
-                    tmem_ld_wait();
+            for (int c = 0; c < HD / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tO + c * 32, o);
+                float x[32];
+                if (use_prev) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(tO + c * 32, o);
+                    for (int i = 0; i < 32; i += 4) {
+                        const float4 a = __ldcs(reinterpret_cast<const float4 *>(arow + c * 32 + i));
+                        x[i] = w.wa * a.x;
+                        x[i + 1] = w.wa * a.y;
+                        x[i + 2] = w.wa * a.z;
+                        x[i + 3] = w.wa * a.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[i] = 0.f;
+                }
+                tmem_ld_wait();
+                if (!valid) continue;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[i] = fmaf(wb, __uint_as_float(o[i]), x[i]);
+                if (final_) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        uint4 u;
+                        u.x = pack_bf16x2(x[i], x[i + 1]);
+                        u.y = pack_bf16x2(x[i + 2], x[i + 3]);
+                        u.z = pack_bf16x2(x[i + 4], x[i + 5]);
+                        u.w = pack_bf16x2(x[i + 6], x[i + 7]);
+                        *reinterpret_cast<uint4 *>(orow + c * 32 + i) = u;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        __stcg(reinterpret_cast<float4 *>(arow + c * 32 + i),
+                               make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]));
                 }
             }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(b_p);
-        }
-        if (ok && n > 0) {
-            ok = wait_phase(smem_u32(&bars->o_full[hh]), 0, abort_flag, P.wait_limit_ns, P.err);
-            if (ok) {
-                tc_fence_after();
-                const bool valid = row_g < S.q1;
-                const bool have = l > 0.f;
-                const float lse_b = have ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
-                const float inv = have ? 1.f / l : 0.f;
-                const int64_t lrow = ((int64_t)b * P.Hq + h) * P.N + row_g;
-                const bool first = (S.flags & SEG_FIRST) != 0;
-                const bool final_ = (S.flags & SEG_FINAL) != 0;
-                MergeW w;
-                w.wa = 0.f;
-                w.wb = 1.f;
-                w.L = lse_b;
-                if (valid && !first) w = merge_weights(P.lse[lrow], lse_b);
-                const float wb = w.wb * inv;
-                __nv_bfloat16 *orow =
-                    static_cast<__nv_bfloat16 *>(P.o) + (int64_t)b * P.so[0] +
-                    (int64_t)h * P.so[1] + (int64_t)row_g * P.so[2];
-                float *arow = P.oacc ? P.oacc + lrow * HD : nullptr;
-#pragma unroll 1
-                for (int c = 0; c < HD / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + c * 32, o);
-                    tmem_ld_wait();
-                    if (!valid) continue;
-                    float x[32];
-                    if (!first && w.wa != 0.f) {
-#pragma unroll
-                        for (int i = 0; i < 32; i += 4) {
-                            const float4 a = *reinterpret_cast<const float4 *>(arow + c * 32 + i);
-                            x[i] = w.wa * a.x;
-                            x[i + 1] = w.wa * a.y;
-                            x[i + 2] = w.wa * a.z;
-                            x[i + 3] = w.wa * a.w;
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) x[i] = 0.f;
-                    }
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) x[i] = fmaf(wb, __uint_as_float(o[i]), x[i]);
-                    if (final_) {
-#pragma unroll
-                        for (int i = 0; i < 32; i += 8) {
-                            uint4 u;
-                            u.x = pack_bf16x2(x[i], x[i + 1]);
-                            u.y = pack_bf16x2(x[i + 2], x[i + 3]);
-                            u.z = pack_bf16x2(x[i + 4], x[i + 5]);
-                            u.w = pack_bf16x2(x[i + 6], x[i + 7]);
-                            *reinterpret_cast<uint4 *>(orow + c * 32 + i) = u;
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4 *>(arow + c * 32 + i) =
-                                make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
-                    }
-                }
-                if (valid) P.lse[lrow] = first ? lse_b : w.L;
-            }
+            if (valid) P.lse[lrow] = first ? lse_b : w.L;
         }
     }
 
@@ -771,7 +894,8 @@ static bool encode_map(CUtensorMap *map, const void *ptr, int64_t B, int64_t H, 
 }
 
 template <int HD>
-static cudaError_t launch_tc_hd(const StepParams &P, int blocks_y, cudaStream_t stream) {
+static cudaError_t launch_tc_hd(const StepParams &P, int blocks_y, int num_sms,
+                                cudaStream_t stream) {
     using C = tc::Cfg<HD>;
     static int configured_mask = 0;  // per device ordinal bit (devices < 32)
     int dev = 0;
@@ -788,15 +912,31 @@ static cudaError_t launch_tc_hd(const StepParams &P, int blocks_y, cudaStream_t 
         !encode_map(&mk, P.k, P.B, P.Hkv, P.N, P.D, P.sk) ||
         !encode_map(&mv, P.v, P.B, P.Hkv, P.N, P.D, P.sv))
         return cudaErrorInvalidValue;
-    dim3 grid(P.B * P.Hq, blocks_y);
-    tc::attn_tc_kernel<HD><<<grid, tc::kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, P);
-    return cudaGetLastError();
+    const int64_t total = (int64_t)P.B * P.Hq * blocks_y;
+    if (total > 0x7fffffff) return cudaErrorInvalidValue;
+    StepParams Q = P;
+    Q.total_items = (int32_t)total;
+    const int grid = (int)std::min<int64_t>(total, (int64_t)num_sms);
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(tc::kThreads);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (P.chained) {  // only ever chained to the previous step of the same ring run
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel<HD>, mq, mk, mv, Q);
 }
 
-cudaError_t launch_attn_tc(const StepParams &P, int blocks_y, cudaStream_t stream) {
+cudaError_t launch_attn_tc(const StepParams &P, int blocks_y, int num_sms, cudaStream_t stream) {
     if (blocks_y <= 0 || P.B * P.Hq <= 0) return cudaSuccess;
-    if (P.D == 128) return launch_tc_hd<128>(P, blocks_y, stream);
-    if (P.D == 64) return launch_tc_hd<64>(P, blocks_y, stream);
+    if (P.D == 128) return launch_tc_hd<128>(P, blocks_y, num_sms, stream);
+    if (P.D == 64) return launch_tc_hd<64>(P, blocks_y, num_sms, stream);
     return cudaErrorInvalidValue;
 }
 

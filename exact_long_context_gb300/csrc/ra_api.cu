@@ -12,7 +12,7 @@
 
 namespace ra {
 cudaError_t launch_attn_simt(const StepParams &P, int blocks_y, cudaStream_t stream);
-cudaError_t launch_attn_tc(const StepParams &P, int blocks_y, cudaStream_t stream);
+cudaError_t launch_attn_tc(const StepParams &P, int blocks_y, int num_sms, cudaStream_t stream);
 int attn_tc_rows_per_block();
 cudaError_t launch_wait_selftest(int64_t limit_ns, int *err, cudaStream_t stream);
 
@@ -269,7 +269,7 @@ static bool use_tensor_cores(const ra_tensor *q, const ra_tensor *k, const ra_te
 
 // Launch the segments of one step (split into launches of <= kMaxSeg segments; all
 // segments of a step have equal query length).
-static ra_status run_step(StepParams &P, const std::vector<Seg> &segs, bool tc,
+static ra_status run_step(StepParams &P, const std::vector<Seg> &segs, bool tc, int num_sms,
                           cudaStream_t stream) {
     const int rows_per_block = tc ? attn_tc_rows_per_block() : 16;
     for (size_t first = 0; first < segs.size(); first += kMaxSeg) {
@@ -284,8 +284,9 @@ static ra_status run_step(StepParams &P, const std::vector<Seg> &segs, bool tc,
         P.blocks_per_seg = (int32_t)((qlen + rows_per_block - 1) / rows_per_block);
         const int64_t blocks_y = (int64_t)P.nseg * P.blocks_per_seg;
         if (blocks_y > 65535) return fail(RA_ERR_UNSUPPORTED, "too many work blocks in one step");
-        cudaError_t e = tc ? launch_attn_tc(P, (int)blocks_y, stream)
+        cudaError_t e = tc ? launch_attn_tc(P, (int)blocks_y, num_sms, stream)
                            : launch_attn_simt(P, (int)blocks_y, stream);
+        P.chained = 1;  // later launches of this run may overlap this one's tail
         if (e != cudaSuccess) return cuda_fail(e, tc ? "attention (tensor-core) launch"
                                                      : "attention (CUDA-core) launch");
         ++t_launches;
@@ -334,7 +335,7 @@ ra_status ra_ring_sim_fwd(const ra_tensor *q, const ra_tensor *k, const ra_tenso
     for (int step = 0; step < ring_size; ++step) {
         plan_step(pb.N, ring_size, layout, causal, step, segs);
         if (segs.empty()) continue;
-        s = run_step(*P, segs, tc, st);
+        s = run_step(*P, segs, tc, di.sms, st);
         if (s) break;
     }
     delete P;
@@ -606,7 +607,7 @@ extern "C" ra_status ra_ring_sim_fwd_noalloc(const ra_tensor *q, const ra_tensor
         P.blocks_per_seg = (int32_t)((qlen + rows_per_block - 1) / rows_per_block);
         const int64_t blocks_y = (int64_t)P.nseg * P.blocks_per_seg;
         if (blocks_y > 65535) return fail(RA_ERR_UNSUPPORTED, "too many work blocks in one step");
-        cudaError_t e = tc ? launch_attn_tc(P, (int)blocks_y, st)
+        cudaError_t e = tc ? launch_attn_tc(P, (int)blocks_y, di.sms, st)
                            : launch_attn_simt(P, (int)blocks_y, st);
         if (e != cudaSuccess) return cuda_fail(e, "attention launch (no-alloc)");
         ++t_launches;

@@ -39,6 +39,8 @@ struct StepParams {
     int32_t nseg;
     int32_t blocks_per_seg;  // work blocks per segment
     int32_t rows_per_block;  // query rows per work block
+    int32_t total_items;     // persistent kernels: work items in this launch
+    int32_t chained;         // launched as a dependent of the previous ring step's kernel
     int64_t wait_limit_ns;
     int *err;  // device error word
     Seg seg[kMaxSeg];
