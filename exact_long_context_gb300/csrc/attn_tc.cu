@@ -56,7 +56,8 @@ struct Cfg {
     static constexpr int SLABS = HD / 64;          // 128-byte column slabs per tile row
     static constexpr int TILE_BYTES = 128 * HD * 2;  // one Q half or one K/V tile (bf16)
     static constexpr int SLAB_BYTES = 128 * 128;     // 128 rows x 128 bytes
-    static constexpr int NSLOT = (HD == 128) ? 4 : 8;
+    static constexpr int NSLOT = (HD == 128) ? 4 : 8;  // tile buffers
+    static constexpr int NSTAGE = NSLOT / 2;            // a stage = (V_t, K_t+1) buffer pair
     static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + HD;
     static constexpr uint32_t TM_COLS = 512;
     static constexpr int BAR_BYTES = 256;
@@ -428,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         bars->abort = 0;
 #pragma unroll
-        for (int s = 0; s < C::NSLOT; ++s) {
+        for (int s = 0; s < C::NSTAGE; ++s) {
             mbar_init(smem_u32(&bars->full[s]), 1);
             mbar_init(smem_u32(&bars->empty[s]), 1);
         }
@@ -471,31 +472,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 Item it;
                 decode_item(P, L, it);
                 if (it.nmax == 0) continue;
-                // K_0 first (it only needs a free slot), then Q (which waits until the
-                // previous item has issued its last Q K^T), then V_0, K_1, V_1, ...
-                for (int seq = 0; seq < 2 * it.nmax && ok; ++seq) {
-                    const int t = seq >> 1;
-                    const int which = seq & 1;  // 0 = K_t, 1 = V_t
+                // Stages of an item: (K_0), then (V_t, K_t+1) for t = 0..n-1 (the last one
+                // V only).  Stage (K_0) first - it only needs a free buffer pair - then Q,
+                // which waits until the previous item has issued its last Q K^T.
+                for (int st = -1; st < it.nmax && ok; ++st) {
                     const uint32_t b_empty = smem_u32(&bars->empty[slot]);
                     const uint32_t b_full = smem_u32(&bars->full[slot]);
                     if (!wait_phase(b_empty, ph ^ 1u, abort_flag, P.wait_limit_ns, P.err)) {
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(b_full, C::TILE_BYTES);
-                    const CUtensorMap *m = which ? &tm_v : &tm_k;
-                    const int ks = it.kt.start(t);
+                    const bool has_v = st >= 0;
+                    const bool has_k = st + 1 < it.nmax;
+                    mbar_expect_tx(b_full, (has_v + has_k) * C::TILE_BYTES);
+                    const uint32_t vbuf = sKV + (2 * slot) * C::TILE_BYTES;
+                    const uint32_t kbuf = sKV + (2 * slot + 1) * C::TILE_BYTES;
+                    if (has_v) {
+                        const int vs = it.kt.start(st);
 #pragma unroll
-                    for (int c = 0; c < C::SLABS; ++c)
-                        tma_load_4d(sKV + slot * C::TILE_BYTES + c * C::SLAB_BYTES, m, b_full,
-                                    c * 64, ks, it.hk, it.b);
+                        for (int c = 0; c < C::SLABS; ++c)
+                            tma_load_4d(vbuf + c * C::SLAB_BYTES, &tm_v, b_full, c * 64, vs, it.hk,
+                                        it.b);
+                    }
+                    if (has_k) {
+                        const int ks = it.kt.start(st + 1);
+#pragma unroll
+                        for (int c = 0; c < C::SLABS; ++c)
+                            tma_load_4d(kbuf + c * C::SLAB_BYTES, &tm_k, b_full, c * 64, ks, it.hk,
+                                        it.b);
+                    }
                     issued |= 1u << slot;
                     last_ph = (last_ph & ~(1u << slot)) | (ph << slot);
-                    if (++slot == C::NSLOT) {
+                    if (++slot == C::NSTAGE) {
                         slot = 0;
                         ph ^= 1u;
                     }
-                    if (seq == 0) {
+                    if (st == -1) {
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh) {
                             if (it.nh[hh] == 0 || !ok) continue;
@@ -519,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh)
                     if (qcnt[hh]) wait_phase_drain(smem_u32(&bars->q_full[hh]), (qcnt[hh] - 1u) & 1u);
-                for (int s2 = 0; s2 < C::NSLOT; ++s2)
+                for (int s2 = 0; s2 < C::NSTAGE; ++s2)
                     if (issued & (1u << s2))
                         wait_phase_drain(smem_u32(&bars->full[s2]), (last_ph >> s2) & 1u);
             }
@@ -529,10 +541,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false);
             constexpr uint32_t IDESC_PV = idesc_bf16(BM, HD, true);
-            auto issue_qk = [=](int hh, int kslot) {
+            auto issue_qk = [=](int hh, uint32_t kb) {
                 const uint32_t d = tmem + (hh ? C::TM_S1 : C::TM_S0);
                 const uint32_t qa = sQ + hh * C::TILE_BYTES;
-                const uint32_t kb = sKV + kslot * C::TILE_BYTES;
 #pragma unroll
                 for (int k = 0; k < HD / 16; ++k) {
                     const uint32_t off = (k >> 2) * C::SLAB_BYTES + (k & 3) * 32;
@@ -540,10 +551,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                            IDESC_QK, k > 0 ? 1u : 0u);
                 }
             };
-            auto issue_pv = [=](int hh, int vslot, bool acc_in) {
+            auto issue_pv = [=](int hh, uint32_t vb, bool acc_in) {
                 const uint32_t d = tmem + (hh ? C::TM_O1 : C::TM_O0);
                 const uint32_t p = tmem + (hh ? C::TM_S1 : C::TM_S0);
-                const uint32_t vb = sKV + vslot * C::TILE_BYTES;
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k) {
                     mma_ts(d, p + k * 8, sdesc_sw128(vb + k * 16 * 128, C::SLAB_BYTES, 1024),
@@ -570,6 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++qcnt[hh];
                 }
                 if (!ok) break;
+                // stage (K_0): the first Q K^T of both halves
                 ok = wait_phase(smem_u32(&bars->full[slot]), ph, abort_flag, P.wait_limit_ns, P.err);
                 if (!ok) break;
                 tc_fence_after();
@@ -577,37 +588,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int hh = 0; hh < 2; ++hh) {
                     const int nhh = hh ? n1 : n0;
                     if (nhh > 0) {
-                        issue_qk(hh, slot);
+                        issue_qk(hh, sKV + (2 * slot + 1) * C::TILE_BYTES);
                         mma_commit(smem_u32(&bars->s_full[hh]));
                         if (nhh == 1) mma_commit(smem_u32(&bars->q_empty[hh]));
                     }
                 }
                 mma_commit(smem_u32(&bars->empty[slot]));
-                if (++slot == C::NSLOT) {
+                if (++slot == C::NSTAGE) {
                     slot = 0;
                     ph ^= 1u;
                 }
+                // stage (V_t, K_t+1): P_h V_t and the next Q_h K^T of each half
                 for (int t = 0; ok && t < it.nmax; ++t) {
-                    const int vslot = slot;
-                    ok = wait_phase(smem_u32(&bars->full[vslot]), ph, abort_flag, P.wait_limit_ns,
+                    ok = wait_phase(smem_u32(&bars->full[slot]), ph, abort_flag, P.wait_limit_ns,
                                     P.err);
                     if (!ok) break;
-                    if (++slot == C::NSLOT) {
-                        slot = 0;
-                        ph ^= 1u;
-                    }
-                    const bool has_next = t + 1 < it.nmax;
-                    const int kslot = slot;
-                    if (has_next) {
-                        ok = wait_phase(smem_u32(&bars->full[kslot]), ph, abort_flag,
-                                        P.wait_limit_ns, P.err);
-                        if (!ok) break;
-                        if (++slot == C::NSLOT) {
-                            slot = 0;
-                            ph ^= 1u;
-                        }
-                    }
                     tc_fence_after();
+                    const uint32_t vb = sKV + (2 * slot) * C::TILE_BYTES;
+                    const uint32_t kb = sKV + (2 * slot + 1) * C::TILE_BYTES;
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         const int nhh = hh ? n1 : n0;
@@ -617,9 +615,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ++pcnt[hh];
                             if (!ok) break;
                             tc_fence_after();
-                            issue_pv(hh, vslot, t > 0);
+                            issue_pv(hh, vb, t > 0);
                             if (t + 1 < nhh) {
-                                issue_qk(hh, kslot);
+                                issue_qk(hh, kb);
                                 mma_commit(smem_u32(&bars->s_full[hh]));
                                 if (t + 2 == nhh) mma_commit(smem_u32(&bars->q_empty[hh]));
                             } else {
@@ -628,8 +626,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     if (!ok) break;
-                    mma_commit(smem_u32(&bars->empty[vslot]));
-                    if (has_next) mma_commit(smem_u32(&bars->empty[kslot]));
+                    mma_commit(smem_u32(&bars->empty[slot]));
+                    if (++slot == C::NSTAGE) {
+                        slot = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
             // every MMA this thread issued completes before tensor memory is released
