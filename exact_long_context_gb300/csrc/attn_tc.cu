@@ -75,6 +75,7 @@ struct Bars {
     uint64_t drain;
     uint32_t tmem_base;
     int32_t abort;
+    uint32_t p_count[2];  // P_h tiles published by the softmax warps (4 per tile)
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
@@ -132,6 +133,33 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
             return false;
         }
     }
+}
+
+// Wait until the shared counter reaches `target` (acquire); same bounds as wait_phase.
+__device__ __forceinline__ bool wait_count(const uint32_t *ctr, uint32_t target,
+                                           volatile int32_t *abort, int64_t limit_ns, int *err) {
+    const uint32_t a = smem_u32(ctr);
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    if ((int32_t)(v - target) >= 0) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i) {
+            asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+            if ((int32_t)(v - target) >= 0) return true;
+        }
+        if (*abort) return false;
+        if ((int64_t)(globaltimer() - t0) > limit_ns) {
+            record_error(err, DERR_TIMEOUT);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void count_release_add(uint32_t *ctr) {
+    asm volatile("red.release.cta.shared::cta.add.u32 [%0], 1;" ::"r"(smem_u32(ctr)) : "memory");
 }
 
 // Bounded wait used only while winding down (own copies / MMAs in flight).
@@ -442,6 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&bars->o_full[hh]), 1);
         }
         mbar_init(b_drain, 1);
+        bars->p_count[0] = bars->p_count[1] = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) tmem_alloc(smem_u32(&bars->tmem_base), C::TM_COLS);
@@ -610,9 +639,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int hh = 0; hh < 2; ++hh) {
                         const int nhh = hh ? n1 : n0;
                         if (t < nhh) {
-                            ok = wait_phase(smem_u32(&bars->p_full[hh]), pcnt[hh] & 1u, abort_flag,
-                                            P.wait_limit_ns, P.err);
                             ++pcnt[hh];
+                            ok = wait_count(&bars->p_count[hh], 4u * pcnt[hh], abort_flag,
+                                            P.wait_limit_ns, P.err);
                             if (!ok) break;
                             tc_fence_after();
                             issue_pv(hh, vb, t > 0);
@@ -647,7 +676,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS = tmem + (hh ? C::TM_S1 : C::TM_S0) + lane_off;
         const uint32_t tO = tmem + (hh ? C::TM_O1 : C::TM_O0) + lane_off;
         const uint32_t b_s = smem_u32(&bars->s_full[hh]);
-        const uint32_t b_p = smem_u32(&bars->p_full[hh]);
         const uint32_t b_o = smem_u32(&bars->o_full[hh]);
         const float sl2 = P.scale_log2;
         uint32_t scnt = 0, ocnt = 0;  // S_h tiles and O_h results seen
@@ -764,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(b_p);
+                if (lane == 0) count_release_add(&bars->p_count[hh]);
             }
             if (!ok) break;
             // ---- epilogue: O / l, LSE, then write or LSE-merge into the running result.
