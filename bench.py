@@ -156,9 +156,16 @@ def run_ours(args, w, ws, rank, local):
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    varlen = isinstance(w, synth.VarlenWorkload)
+    cu = w.cu_seqlens() if varlen else None
+
     def step():
-        ra.ring_sim_fwd(q, k, v, w.ring_size, w.layout, causal=w.causal, scale=w.scale, o=o,
-                        lse=lse, workspace=wsbuf if need else None, stream=stream)
+        if varlen:
+            ra.attn_varlen_fwd(q, k, v, cu, causal=w.causal, scale=w.scale, o=o, lse=lse,
+                               stream=stream)
+        else:
+            ra.ring_sim_fwd(q, k, v, w.ring_size, w.layout, causal=w.causal, scale=w.scale, o=o,
+                            lse=lse, workspace=wsbuf if need else None, stream=stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -212,8 +219,12 @@ def run_ours(args, w, ws, rank, local):
             dq.copy_(hq, non_blocking=True)
             dk.copy_(hk, non_blocking=True)
             dv.copy_(hv, non_blocking=True)
-            ra.ring_sim_fwd(dq, dk, dv, w.ring_size, w.layout, causal=w.causal, scale=w.scale,
-                            o=o, lse=lse, workspace=wsbuf if need else None, stream=stream)
+            if varlen:
+                ra.attn_varlen_fwd(dq, dk, dv, cu, causal=w.causal, scale=w.scale, o=o, lse=lse,
+                                   stream=stream)
+            else:
+                ra.ring_sim_fwd(dq, dk, dv, w.ring_size, w.layout, causal=w.causal, scale=w.scale,
+                                o=o, lse=lse, workspace=wsbuf if need else None, stream=stream)
             ho.copy_(o, non_blocking=True)
             hl.copy_(lse, non_blocking=True)
 
@@ -280,22 +291,38 @@ def oracle_rate_sample(w, budget_s, seed=0):
         i = rng.integers(0, w.N, n)
         return np.stack([b, h, i], 1).astype(np.int64)
 
-    def flops_of(rows):
-        vis = (rows[:, 2] + 1) if w.causal else np.full(len(rows), w.N)
-        return float(np.sum(vis)) * 4.0 * w.D
+    varlen = isinstance(w, synth.VarlenWorkload)
+    cu = w.cu_seqlens() if varlen else None
+
+    def run(rows):
+        """Oracle over the rows; returns their causal-adjusted FLOPs."""
+        if not varlen:
+            oracle.attention(qn, kn, vn, w.causal, w.scale, rows=rows, nthreads=threads)
+            vis = (rows[:, 2] + 1) if w.causal else np.full(len(rows), w.N)
+            return float(np.sum(vis)) * 4.0 * w.D
+        seq = np.searchsorted(np.array(cu), rows[:, 2], side="right") - 1
+        flops = 0.0
+        for s_ in np.unique(seq):
+            sel = rows[seq == s_]
+            a, b = cu[s_], cu[s_ + 1]
+            oracle.attention(qn, kn, vn, w.causal, w.scale, kv_lo=a, kv_hi=b, rows=sel,
+                             nthreads=threads)
+            vis = (sel[:, 2] - a + 1) if w.causal else np.full(len(sel), b - a)
+            flops += float(np.sum(vis)) * 4.0 * w.D
+        return flops
 
     # calibrate on a small batch, then size the timed sample to the budget
     cal = rows_for(max(threads, 8))
     t0 = time.perf_counter()
-    oracle.attention(qn, kn, vn, w.causal, w.scale, rows=cal, nthreads=threads)
+    run(cal)
     dt = max(time.perf_counter() - t0, 1e-4)
     per_row = dt / len(cal)
     n = int(max(threads, min(200000, budget_s / per_row)))
     rows = rows_for(n)
     t0 = time.perf_counter()
-    oracle.attention(qn, kn, vn, w.causal, w.scale, rows=rows, nthreads=threads)
+    f = run(rows)
     sec = time.perf_counter() - t0
-    return flops_of(rows), sec, len(rows), threads
+    return f, sec, len(rows), threads
 
 
 def run_reference(args, w, ws, rank):
@@ -337,13 +364,14 @@ def main():
 
     from exact_long_context_gb300 import synth
 
-    w = synth.WORKLOADS[args.workload]
+    w = synth.WORKLOADS.get(args.workload) or synth.VARLEN_WORKLOADS[args.workload]
     ws, rank, local = dist_env()
     if ws > 1:
         torch.distributed.init_process_group("nccl" if args.impl == "ours" else "gloo")
 
     config = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "D": w.D,
               "causal": w.causal, "ring_size": w.ring_size, "layout": w.layout,
+              **({"sequences": len(w.lengths())} if isinstance(w, synth.VarlenWorkload) else {}),
               "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{ws}"}
     line = {"metric": METRIC, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",

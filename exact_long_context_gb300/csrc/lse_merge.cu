@@ -5,6 +5,8 @@
 //   L = max(a,b) + ln(1 + e^-|a-b|),  o <- e^(a-L) o_acc + e^(b-L) o_blk,  lse <- L.
 // HBM-bound: one warp per row, lanes own contiguous 16-byte pieces of the row so every
 // load and store is coalesced; a grid-stride loop over rows on a grid sized to the SMs.
+#include <algorithm>
+
 #include "ra_internal.cuh"
 
 namespace ra {
@@ -67,6 +69,41 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const __grid_constant__ 
         __syncwarp();
         if (lane == 0) P.lse_acc[row] = w.L;
     }
+}
+
+// Rows [r0, r1) of every (b, h): O = 0 and LSE = -inf, the identity partial of a row
+// that sees no key (padding rows of a packed batch).
+__global__ void __launch_bounds__(256) fill_identity_kernel(void *o, int o_bf16, int64_t s0, int64_t s1,
+                                                            int64_t s2, float *lse, int H, int N, int D,
+                                                            int r0, int r1) {
+    const int64_t rows = (int64_t)(r1 - r0);
+    const int64_t total = (int64_t)gridDim.y * H * rows;  // gridDim.y = B
+    const int b = blockIdx.y;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (int64_t)H * rows * D;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int d = (int)(i % D);
+        const int64_t hr = i / D;
+        const int h = (int)(hr / rows);
+        const int n = r0 + (int)(hr - (int64_t)h * rows);
+        const int64_t off = (int64_t)b * s0 + (int64_t)h * s1 + (int64_t)n * s2 + d;
+        if (o_bf16)
+            static_cast<uint16_t *>(o)[off] = 0;
+        else
+            static_cast<float *>(o)[off] = 0.f;
+        if (d == 0) lse[((int64_t)b * H + h) * N + n] = -INFINITY;
+    }
+    (void)total;
+}
+
+cudaError_t launch_fill_identity(void *o, int o_bf16, const int64_t *so, float *lse, int B, int H,
+                                 int N, int D, int r0, int r1, int num_sms, cudaStream_t stream) {
+    if (r1 <= r0 || B <= 0 || H <= 0 || D <= 0) return cudaSuccess;
+    const int64_t work = (int64_t)H * (r1 - r0) * D;
+    int gx = (int)std::min<int64_t>((work + 255) / 256, (int64_t)num_sms * 8);
+    if (gx < 1) gx = 1;
+    fill_identity_kernel<<<dim3(gx, B), 256, 0, stream>>>(o, o_bf16, so[0], so[1], so[2], lse, H, N, D,
+                                                          r0, r1);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_lse_merge(const MergeParams &P, int num_sms, cudaStream_t stream) {

@@ -17,6 +17,8 @@ int attn_tc_rows_per_block();
 cudaError_t launch_wait_selftest(int64_t limit_ns, int *err, cudaStream_t stream);
 
 cudaError_t launch_lse_merge(const MergeParams &P, int num_sms, cudaStream_t stream);
+cudaError_t launch_fill_identity(void *o, int o_bf16, const int64_t *so, float *lse, int B, int H,
+                                 int N, int D, int r0, int r1, int num_sms, cudaStream_t stream);
 }  // namespace ra
 
 using namespace ra;
@@ -361,6 +363,99 @@ int64_t ra_ring_sim_plan(int64_t N, int ring_size, ra_layout layout, int causal,
         o[7] = x.rank;
     }
     return (int64_t)segs.size();
+}
+
+ra_status ra_attn_varlen_fwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v,
+                             ra_tensor *o, float *lse, const int32_t *cu_seqlens, int num_seqs,
+                             int causal, float scale, void *stream) {
+    Problem pb;
+    ra_status s = check_qkvo(q, k, v, o, lse, pb);
+    if (s) return s;
+    if (isnan(scale)) return fail(RA_ERR_INVALID_ARG, "scale is NaN");
+    if (pb.B > 1) return fail(RA_ERR_INVALID_ARG, "packed batches are [1, H, total, D] (B must be 1)");
+    if (num_seqs < 0 || (num_seqs > 0 && !cu_seqlens))
+        return fail(RA_ERR_INVALID_ARG, "cu_seqlens is NULL or num_seqs < 0");
+    for (int i = 0; i < num_seqs; ++i) {
+        if (cu_seqlens[i] < 0 || cu_seqlens[i + 1] < cu_seqlens[i])
+            return fail(RA_ERR_INVALID_ARG, "cu_seqlens must be non-negative and non-decreasing");
+    }
+    if (num_seqs > 0 && cu_seqlens[num_seqs] > pb.N)
+        return fail(RA_ERR_INVALID_ARG, "cu_seqlens[num_seqs] exceeds the packed length");
+    if (pb.B * pb.Hq * pb.N == 0) return RA_OK;
+    DevInfo di;
+    std::string msg;
+    if (!device_info(di, msg)) return fail(RA_ERR_CUDA, msg);
+    StepParams *P = new StepParams;
+    fill_common(*P, q, k, v, o, lse, pb, causal, scale, di);
+    const bool tc = use_tensor_cores(q, k, v, o, pb, di);
+    const int rows_per_block = tc ? attn_tc_rows_per_block() : 16;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // one segment per non-empty sequence: its rows against its own keys only
+    std::vector<Seg> segs;
+    for (int i = 0; i < num_seqs; ++i) {
+        const int32_t a0 = cu_seqlens[i], a1 = cu_seqlens[i + 1];
+        if (a1 <= a0) continue;
+        Seg g;
+        memset(&g, 0, sizeof g);
+        g.q0 = a0;
+        g.q1 = a1;
+        g.k0[0] = a0;
+        g.k1[0] = a1;
+        g.k0[1] = g.k1[1] = a1;
+        g.flags = SEG_FIRST | SEG_FINAL;
+        g.rank = i;
+        segs.push_back(g);
+    }
+    std::stable_sort(segs.begin(), segs.end(),
+                     [](const Seg &x, const Seg &y) { return x.q1 - x.q0 > y.q1 - y.q0; });
+    s = RA_OK;
+    for (size_t first = 0; first < segs.size() && !s; first += kMaxSeg) {
+        const size_t n = std::min(segs.size() - first, (size_t)kMaxSeg);
+        int64_t blocks = 0;
+        for (size_t i = 0; i < n; ++i) {
+            P->seg[i] = segs[first + i];
+            P->seg[i].blk0 = (int32_t)blocks;
+            blocks += (P->seg[i].q1 - P->seg[i].q0 + rows_per_block - 1) / rows_per_block;
+        }
+        P->nseg = (int32_t)n;
+        P->var_blocks = 1;
+        P->rows_per_block = rows_per_block;
+        P->blocks_per_seg = 0;
+        if (blocks > 65535) {
+            s = fail(RA_ERR_UNSUPPORTED, "too many work blocks in one launch");
+            break;
+        }
+        cudaError_t e = tc ? launch_attn_tc(*P, (int)blocks, di.sms, st)
+                           : launch_attn_simt(*P, (int)blocks, st);
+        if (e != cudaSuccess) {
+            s = cuda_fail(e, "varlen attention launch");
+            break;
+        }
+        ++t_launches;
+    }
+    // rows outside every sequence (padding): the identity partial, O = 0 and LSE = -inf
+    int64_t covered = 0;
+    std::vector<std::pair<int64_t, int64_t>> gaps;
+    {
+        std::vector<std::pair<int64_t, int64_t>> spans;
+        for (int i = 0; i < num_seqs; ++i)
+            if (cu_seqlens[i + 1] > cu_seqlens[i]) spans.push_back({cu_seqlens[i], cu_seqlens[i + 1]});
+        std::sort(spans.begin(), spans.end());
+        for (auto &sp : spans) {
+            if (sp.first > covered) gaps.push_back({covered, sp.first});
+            covered = std::max(covered, sp.second);
+        }
+        if (covered < pb.N) gaps.push_back({covered, pb.N});
+    }
+    for (size_t i = 0; i < gaps.size() && !s; ++i) {
+        cudaError_t e = launch_fill_identity(o->data, pb.dtype == RA_BF16, o->stride, lse, (int)pb.B,
+                                             (int)pb.Hq, (int)pb.N, (int)pb.D, (int)gaps[i].first,
+                                             (int)gaps[i].second, di.sms, st);
+        if (e != cudaSuccess) s = cuda_fail(e, "padding fill launch");
+        else ++t_launches;
+    }
+    delete P;
+    return s;
 }
 
 ra_status ra_lse_merge(ra_tensor *o_acc, float *lse_acc, const ra_tensor *o_blk,

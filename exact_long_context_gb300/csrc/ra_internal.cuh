@@ -17,6 +17,8 @@ struct Seg {
     int32_t k0[2], k1[2];
     int32_t flags;
     int32_t rank;
+    int32_t blk0;  // first work block of this segment (variable-length launches)
+    int32_t pad_;
 };
 
 enum : int32_t { SEG_FIRST = 1, SEG_FINAL = 2 };
@@ -41,6 +43,7 @@ struct StepParams {
     int32_t rows_per_block;  // query rows per work block
     int32_t total_items;     // persistent kernels: work items in this launch
     int32_t chained;         // launched as a dependent of the previous ring step's kernel
+    int32_t var_blocks;      // segments have different lengths: decode through Seg::blk0
     int64_t wait_limit_ns;
     int *err;  // device error word
     Seg seg[kMaxSeg];
@@ -67,13 +70,30 @@ __device__ __forceinline__ void record_error(int *err, int code) {
     if (err) atomicCAS(err, 0, code);
 }
 
-// Decode blockIdx.y into (segment, local block).  Work blocks are numbered round-robin
-// over segments; the local block counts down, so the last (under causality the
-// heaviest) blocks of every segment are dispatched first.
+// Decode a work-block index into (segment, local block).
+// Equal-length segments: blocks are numbered round-robin over segments.
+// Variable-length segments (sorted longest first by the host): segment si owns blocks
+// [blk0, blk0 + its block count).
+// Either way the local block counts down, so the last (under causality the heaviest)
+// blocks of a segment are dispatched first.
 __device__ __forceinline__ void decode_work(const StepParams &P, int w, int &si, int &lb) {
-    const int round = w / P.nseg;
-    si = w - round * P.nseg;
-    lb = P.blocks_per_seg - 1 - round;
+    if (!P.var_blocks) {
+        const int round = w / P.nseg;
+        si = w - round * P.nseg;
+        lb = P.blocks_per_seg - 1 - round;
+        return;
+    }
+    int lo = 0, hi = P.nseg - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (P.seg[mid].blk0 <= w)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    si = lo;
+    const int nb = (P.seg[si].q1 - P.seg[si].q0 + P.rows_per_block - 1) / P.rows_per_block;
+    lb = nb - 1 - (w - P.seg[si].blk0);
 }
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) {

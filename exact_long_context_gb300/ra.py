@@ -51,6 +51,8 @@ def lib() -> ctypes.CDLL:
             L.ra_ring_sim_workspace_bytes.argtypes = [T, c_int]
             L.ra_ring_sim_workspace_bytes.restype = ctypes.c_size_t
             L.ra_ring_sim_fwd.argtypes = [T, T, T, T, P, c_int, c_int, c_int, c_float, P, P]
+            L.ra_attn_varlen_fwd.argtypes = [T, T, T, T, P, P, c_int, c_int, c_float, P]
+            L.ra_attn_varlen_fwd.restype = c_int
             L.ra_ring_sim_plan.argtypes = [i64, c_int, c_int, c_int, c_int, P, i64]
             L.ra_ring_sim_plan.restype = i64
             L.ra_check_device_error.argtypes = [P]
@@ -122,6 +124,19 @@ def attn_fwd(q, k, v, causal=False, scale=None, o=None, lse=None, stream=None):
     dq, dk, dv, do = _desc(q, "q"), _desc(k, "k"), _desc(v, "v"), _desc(o, "o")
     _check(lib().ra_attn_fwd(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), ctypes.byref(do),
                              _ptr(lse), int(bool(causal)), float(scale or 0.0), _stream(stream)))
+    return o, lse
+
+
+def attn_varlen_fwd(q, k, v, cu_seqlens, causal=False, scale=None, o=None, lse=None, stream=None):
+    """Packed variable-length attention: q [1,Hq,total,D], k/v [1,Hkv,total,D];
+    ``cu_seqlens`` host offsets (sequence i = rows [cu[i], cu[i+1])).  Returns (o, lse)."""
+    o, lse = _outputs(q, o, lse)
+    cu = (ctypes.c_int32 * len(cu_seqlens))(*[int(x) for x in cu_seqlens])
+    dq, dk, dv, do = _desc(q, "q"), _desc(k, "k"), _desc(v, "v"), _desc(o, "o")
+    _check(lib().ra_attn_varlen_fwd(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv),
+                                    ctypes.byref(do), _ptr(lse), ctypes.cast(cu, ctypes.c_void_p),
+                                    len(cu_seqlens) - 1, int(bool(causal)), float(scale or 0.0),
+                                    _stream(stream)))
     return o, lse
 
 

@@ -55,6 +55,64 @@ WORKLOADS = {
 WORKLOAD_ORDER = list(WORKLOADS)
 
 
+@dataclass(frozen=True)
+class VarlenWorkload:
+    """A packed batch of variable-length sequences (cu_seqlens).
+
+    Sequence lengths are drawn log-uniformly in [min_len, max_len] with numpy's
+    default_rng(seed) until ``total`` tokens are filled (the last one is cut to fit).
+    """
+    name: str
+    Hq: int
+    Hkv: int
+    D: int
+    dtype: torch.dtype
+    causal: bool
+    total: int
+    min_len: int
+    max_len: int
+    seed: int
+    B: int = 1
+    ring_size: int = 1
+    layout: str = "packed"
+
+    @property
+    def N(self) -> int:
+        return self.total
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    def lengths(self):
+        import numpy as np
+
+        rng = np.random.default_rng(self.seed)
+        out, used = [], 0
+        while used < self.total:
+            n = int(round(math.exp(rng.uniform(math.log(self.min_len), math.log(self.max_len)))))
+            n = min(n, self.total - used)
+            out.append(n)
+            used += n
+        return out
+
+    def cu_seqlens(self):
+        cu = [0]
+        for n in self.lengths():
+            cu.append(cu[-1] + n)
+        return cu
+
+    def flops(self) -> float:
+        f = sum(4.0 * self.Hq * n * n * self.D for n in self.lengths())
+        return f / 2 if self.causal else f
+
+
+VARLEN_WORKLOADS = {
+    "varlen_causal_h32kv8_128k": VarlenWorkload("varlen_causal_h32kv8_128k", 32, 8, 128,
+                                                torch.bfloat16, True, 131072, 256, 16384, 6),
+}
+
+
 def _fill(shape, gen, device, dtype):
     B, H, N, D = shape
     out = torch.empty(shape, dtype=dtype, device=device)
@@ -83,8 +141,10 @@ def worked_example_qkv():
             v.reshape(1, 1, 32, 16).contiguous())
 
 
-def workload_inputs(w: Workload, device="cpu"):
+def workload_inputs(w, device="cpu"):
     if w.name == "tiny_ring4_fp32":
         q, k, v = worked_example_qkv()
         return q.to(device), k.to(device), v.to(device)
+    if isinstance(w, VarlenWorkload):
+        return make_qkv(1, w.Hq, w.Hkv, w.total, w.D, w.dtype, w.seed, device)
     return make_qkv(w.B, w.Hq, w.Hkv, w.N, w.D, w.dtype, w.seed, device)

@@ -136,6 +136,27 @@ ra_status ra_ring_sim_fwd(const ra_tensor *q, const ra_tensor *k, const ra_tenso
                           float scale, void *workspace, void *stream);
 
 /*
+ * ra_attn_varlen_fwd - exact attention over a packed batch of variable-length sequences.
+ *
+ * Sequence i occupies rows [cu_seqlens[i], cu_seqlens[i+1]) of the packed axis; a row
+ * attends only to keys of its own sequence (causal within it when causal != 0), the
+ * block-diagonal mask of packed batches ("序列并行与 Ring Attention：超长上下文训练技术解析":
+ * varlen FlashAttention over `cu_seqlens`, padding excluded by the attention mask;
+ * "第12章 FlashAttention原理与实现": `flash_attn_varlen_func` for samples of different
+ * lengths).  Rows outside every sequence (padding) get the identity, O = 0 and
+ * LSE = -inf.
+ *
+ *   q, k, v    [1, Hq, total, D] / [1, Hkv, total, D] (B must be 1)
+ *   o, lse     outputs as in ra_attn_fwd
+ *   cu_seqlens HOST array of num_seqs + 1 non-decreasing offsets, cu_seqlens[num_seqs]
+ *              <= total (read during the call only; empty sequences are allowed)
+ * Errors: as ra_attn_fwd, plus RA_ERR_INVALID_ARG for B != 1 or bad cu_seqlens.
+ */
+ra_status ra_attn_varlen_fwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v,
+                             ra_tensor *o, float *lse, const int32_t *cu_seqlens, int num_seqs,
+                             int causal, float scale, void *stream);
+
+/*
  * ra_ring_sim_plan - host-only description of the ring schedule (no GPU work).
  * For step `step`, writes up to `cap` segments; each segment is 8 int64 values:
  *   q0, q1          query rows [q0, q1) of one chunk of one simulated rank

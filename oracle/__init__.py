@@ -7,6 +7,7 @@ library never calls it and shares no code with it.
 Contents
 - :func:`attention`     - softmax(scale * Q K^T) V and the per-row natural-log LSE,
                           row by row in C (``oracle.c``), two passes per row.
+- :func:`attention_varlen` - the same per sequence of a packed batch (``cu_seqlens``).
 - :mod:`oracle.merge`   - the log-sum-exp merge of two partial results.
 - :mod:`oracle.ring`    - an fp64 restatement of the ring of KV-block passes
                           (contiguous / zigzag partitions), used only for invariants.
@@ -141,3 +142,31 @@ def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
     out = rounded.astype(np.uint16)
     out[nan] = 0x7FC0
     return out
+
+
+def attention_varlen(q, k, v, cu_seqlens, causal: bool, scale: float | None = None,
+                     nthreads: int | None = None, plant: int = 0):
+    """Exact attention over a packed batch: sequence i = rows [cu[i], cu[i+1]) of the
+    packed axis of q [1,Hq,T,D], k/v [1,Hkv,T,D]; a row sees only keys of its own sequence
+    (and j <= i when causal).  Rows outside every sequence: o = 0, lse = -inf.
+
+    Each sequence is the plain definition over its own rows and keys: the key window
+    of :func:`attention` restricted to the sequence.
+    """
+    q = np.ascontiguousarray(q)
+    B, Hq, T, D = q.shape
+    if B != 1:
+        raise ValueError("packed batches have B == 1")
+    o = np.zeros((B, Hq, T, D), np.float64)
+    lse = np.full((B, Hq, T), -np.inf)
+    cu = [int(x) for x in cu_seqlens]
+    for i in range(len(cu) - 1):
+        a, b = cu[i], cu[i + 1]
+        if b <= a:
+            continue
+        rows = np.array([(0, h, r) for h in range(Hq) for r in range(a, b)], dtype=np.int64)
+        oi, li = attention(q, k, v, causal, scale, kv_lo=a, kv_hi=b, rows=rows,
+                           nthreads=nthreads, plant=plant)
+        o[0, rows[:, 1], rows[:, 2]] = oi
+        lse[0, rows[:, 1], rows[:, 2]] = li
+    return o, lse

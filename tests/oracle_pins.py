@@ -323,3 +323,47 @@ def pin_zigzag_map(golden_dir):
 
 ALL_PINS = ["pin_brute_force", "pin_worked_example", "pin_closed_forms", "pin_invariants",
             "pin_merge", "pin_ring"]
+
+
+def pin_varlen(plant=0):
+    """Packed batch == block-diagonal brute force, and == each sequence run on its own."""
+    rng = np.random.default_rng(17)
+    cu = [3, 3, 10, 11, 30, 52]  # leading padding, an empty sequence, trailing padding
+    T = 57
+    Hq, Hkv, D = 4, 2, 8
+    q = rng.standard_normal((1, Hq, T, D))
+    k = rng.standard_normal((1, Hkv, T, D))
+    v = rng.standard_normal((1, Hkv, T, D))
+    scale = 0.41
+    for causal in (False, True):
+        o, l = oracle.attention_varlen(q, k, v, cu, causal, scale, plant=plant)
+        # brute force with a block-diagonal mask
+        G = Hq // Hkv
+        kx = np.repeat(k, G, axis=1)
+        vx = np.repeat(v, G, axis=1)
+        S = scale * np.einsum("bhid,bhjd->bhij", q, kx)
+        seq = np.full(T, -1)
+        for i in range(len(cu) - 1):
+            seq[cu[i]:cu[i + 1]] = i
+        vis = (seq[:, None] == seq[None, :]) & (seq[:, None] >= 0)
+        if causal:
+            vis &= np.tril(np.ones((T, T), bool))
+        Pm = np.where(vis, np.exp(S), 0.0)
+        Z = Pm.sum(-1)
+        with np.errstate(invalid="ignore", divide="ignore"):
+            ob = np.where(Z[..., None] > 0, (Pm @ vx) / Z[..., None], 0.0)
+            lb = np.where(Z > 0, np.log(Z), -np.inf)
+        _close(o, ob, what=f"varlen brute causal={causal}")
+        _close(l, lb, what=f"varlen brute LSE causal={causal}")
+        # each sequence alone (sliced arrays, no window)
+        for i in range(len(cu) - 1):
+            a, b = cu[i], cu[i + 1]
+            if b <= a:
+                continue
+            oi, li = oracle.attention(q[:, :, a:b], k[:, :, a:b], v[:, :, a:b], causal, scale,
+                                      plant=plant)
+            _close(o[:, :, a:b], oi, what=f"varlen seq {i} alone")
+            _close(l[:, :, a:b], li, what=f"varlen seq {i} alone LSE")
+
+
+ALL_PINS.append("pin_varlen")

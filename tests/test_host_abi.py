@@ -188,3 +188,22 @@ def test_plan_rejects_bad_arguments(ra):
         ra.ring_sim_plan(100, 3, "contig", True, 0)
     with pytest.raises(ValueError):
         ra.ring_sim_plan(96, 3, "zigzag", True, 3)
+
+
+def test_varlen_argument_errors(ra):
+    L = ra.lib()
+    S = (1, 2, 100, 128)
+    IA = ra.RA_ERR_INVALID_ARG
+
+    def call(cu, n, shape=S):
+        arr = (ctypes.c_int32 * max(1, len(cu)))(*cu)
+        return L.ra_attn_varlen_fwd(ctypes.byref(_t(shape)), ctypes.byref(_t(shape)),
+                                    ctypes.byref(_t(shape)), ctypes.byref(_t(shape)), 0x20000,
+                                    ctypes.cast(arr, ctypes.c_void_p), n, 1, 0.0, None)
+    assert call([0, 50, 40], 2) == IA      # decreasing
+    assert call([0, 50, 101], 2) == IA     # beyond the packed length
+    assert call([-1, 50], 1) == IA         # negative
+    assert call([0, 50], -1) == IA
+    assert call([0, 50], 1, shape=(2, 2, 100, 128)) == IA  # B must be 1
+    assert L.ra_attn_varlen_fwd(ctypes.byref(_t(S)), ctypes.byref(_t(S)), ctypes.byref(_t(S)),
+                                ctypes.byref(_t(S)), 0x20000, None, 3, 1, 0.0, None) == IA

@@ -89,3 +89,7 @@ def test_merge_identity_both_forms():
         mo, ml = f(*ident, o, l)
         assert np.array_equal(ml, l)
         assert np.array_equal(mo[0], o[0])
+
+
+def test_varlen_block_diagonal():
+    P.pin_varlen()
