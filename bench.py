@@ -35,7 +35,6 @@ import torch  # noqa: E402
 
 DEFAULT_WORKLOAD = "dense_causal_b2h32n4k"
 METRIC = "attention fwd TFLOP/s (causal-adjusted) and % of GB300 dense BF16 peak"
-PROFILE_JSON = os.path.join(ROOT, "profiles", "attn_tc_dense_causal_b2h32n4k.json")
 KERNEL_SRC = os.path.join(ROOT, "exact_long_context_gb300", "csrc", "attn_tc.cu")
 
 
@@ -60,15 +59,16 @@ def kernel_hash():
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def profiled_traffic():
-    """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary, if
-    that summary was taken on the current kernel source; else None."""
+def profiled_traffic(workload: str):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary of this
+    workload, if that summary was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"attn_tc_{workload}.json")
     try:
-        with open(PROFILE_JSON) as f:
+        with open(path) as f:
             prof = json.load(f)
     except (OSError, ValueError):
         return None
-    if prof.get("kernel_src_sha256_16") != kernel_hash():
+    if prof.get("workload") != workload or prof.get("kernel_src_sha256_16") != kernel_hash():
         return None
     return prof.get("dram_bytes_per_launch")
 
@@ -259,7 +259,7 @@ def run_ours(args, w, ws, rank, local):
     achieved = per_launch_flops / (per_launch_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4),
-                "traffic": profiled_traffic(), "peak_kind": peak_kind}
+                "traffic": profiled_traffic(w.name), "peak_kind": peak_kind}
     return {
         "value": round(value, 2), "ms_per_step": round(ms_per_step, 5), "e2e": e2e,
         "roofline": roofline, "clocks": clk, "gpu_launches": launches,
