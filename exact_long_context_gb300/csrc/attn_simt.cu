@@ -71,10 +71,14 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(const __grid_constant__ 
     const int64_t kbase = (int64_t)b * P.sk[0] + (int64_t)hk * P.sk[1];
     const int64_t vbase = (int64_t)b * P.sv[0] + (int64_t)hk * P.sv[1];
 
+    // segment indices map to sequence positions through the rank interleave
+    const int64_t qs = (int64_t)P.rs * P.sq[2], ks_ = (int64_t)P.rs * P.sk[2], vs_ = (int64_t)P.rs * P.sv[2];
+    const int64_t qoff = (int64_t)S.q_rank * P.sq[2];
+    const int64_t koff = (int64_t)S.kv_rank * P.sk[2], voff = (int64_t)S.kv_rank * P.sv[2];
     for (int idx = tid; idx < kSimtRows * D; idx += blockDim.x) {
         const int r = idx / D, d = idx - (idx / D) * D;
         const int row = qa + r;
-        sQ[r][d] = row < qb ? ld_elem<BF16>(P.q, qbase + (int64_t)row * P.sq[2] + d) : 0.f;
+        sQ[r][d] = row < qb ? ld_elem<BF16>(P.q, qbase + qoff + (int64_t)row * qs + d) : 0.f;
     }
 
     float m[4], l[4], acc[4][4];
@@ -88,15 +92,15 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(const __grid_constant__ 
 
     for (int r = 0; r < 2; ++r) {
         const int ka = S.k0[r], kb = S.k1[r];
-        const int kend = P.causal ? min(kb, qb) : kb;  // row qb-1 sees keys <= qb-1
+        const int kend = P.causal ? min(kb, qb - S.diag) : kb;  // row qb-1 sees keys <= qb-1-diag
         for (int t0 = ka; t0 < kend; t0 += kSimtKT) {
             __syncthreads();
             for (int idx = tid; idx < kSimtKT * D; idx += blockDim.x) {
                 const int j = idx / D, d = idx - (idx / D) * D;
                 const int key = t0 + j;
                 const bool in = key < kb;
-                sK[j][d] = in ? ld_elem<BF16>(P.k, kbase + (int64_t)key * P.sk[2] + d) : 0.f;
-                sV[j][d] = in ? ld_elem<BF16>(P.v, vbase + (int64_t)key * P.sv[2] + d) : 0.f;
+                sK[j][d] = in ? ld_elem<BF16>(P.k, kbase + koff + (int64_t)key * ks_ + d) : 0.f;
+                sV[j][d] = in ? ld_elem<BF16>(P.v, vbase + voff + (int64_t)key * vs_ + d) : 0.f;
             }
             __syncthreads();
 #pragma unroll
@@ -106,7 +110,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(const __grid_constant__ 
                 const int key = t0 + lane;
                 float s = 0.f;
                 for (int d = 0; d < D; ++d) s = fmaf(sQ[lr][d], sK[lane][d], s);
-                const bool vis = key < kb && row < qb && (!P.causal || key <= row);
+                const bool vis = key < kb && row < qb && (!P.causal || key + S.diag <= row);
                 const float x = vis ? s * P.scale_log2 : -INFINITY;
                 const float mnew = fmaxf(m[rr], warp_max(x));
                 const float muse = (mnew == -INFINITY) ? 0.f : mnew;
@@ -133,11 +137,12 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(const __grid_constant__ 
     for (int rr = 0; rr < 4; ++rr) {
         const int row = qa + warp * 4 + rr;
         if (row >= qb) continue;
+        const int pos = row * P.rs + S.q_rank;  // position in the sequence
         const bool have = l[rr] > 0.f;
         const float lse_b = have ? (m[rr] + log2f(l[rr])) * kLn2 : -INFINITY;
         const float inv = have ? 1.f / l[rr] : 0.f;
-        const int64_t lrow = ((int64_t)b * P.Hq + h) * P.N + row;
-        const int64_t orow = (int64_t)b * P.so[0] + (int64_t)h * P.so[1] + (int64_t)row * P.so[2];
+        const int64_t lrow = ((int64_t)b * P.Hq + h) * P.N + pos;
+        const int64_t orow = (int64_t)b * P.so[0] + (int64_t)h * P.so[1] + (int64_t)pos * P.so[2];
         float *accrow = P.oacc ? P.oacc + lrow * D : nullptr;
         if (S.flags & SEG_FIRST) {
             for (int c = 0; c < 4; ++c) {

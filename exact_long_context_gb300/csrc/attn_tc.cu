@@ -170,12 +170,15 @@ __device__ __forceinline__ void wait_phase_drain(uint32_t bar, uint32_t parity) 
     }
 }
 
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                            int c0, int c1, int c2, int c3) {
+// Tiled TMA load from a 5-D map (d, rank, index, head, batch); c0 is a multiple of 64
+// elements (128 bytes), so every copy starts 16-byte aligned.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3, int c4) {
     asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "r"(c4)
         : "memory");
 }
 
@@ -373,6 +376,7 @@ struct KTiles {
 // key tiles of one segment.  Every role decodes the same items in the same order.
 struct Item {
     int b, h, hk;
+    int q_rank, kv_rank, diag;
     int qrow0, q1;
     int flags;
     int nh[2];  // key tiles each half iterates (a prefix of the segment's tiles)
@@ -404,6 +408,9 @@ __device__ __forceinline__ void decode_item(const StepParams &P, int L, Item &it
     const Seg &S = P.seg[si];
     it.qrow0 = S.q0 + lb * 2 * BM;
     it.q1 = S.q1;
+    it.q_rank = S.q_rank;
+    it.kv_rank = S.kv_rank;
+    it.diag = S.diag;
     it.flags = S.flags;
     it.kt.k0[0] = S.k0[0];
     it.kt.k1[0] = S.k1[0];
@@ -419,7 +426,7 @@ __device__ __forceinline__ void decode_item(const StepParams &P, int L, Item &it
         else if (!P.causal)
             it.nh[hh] = it.kt.ntot;
         else
-            it.nh[hh] = it.kt.visible_prefix(min(r0 + BM, S.q1) - 1);
+            it.nh[hh] = it.kt.visible_prefix(min(r0 + BM, S.q1) - 1 - S.diag);
     }
     it.nmax = max(it.nh[0], it.nh[1]);
 }
@@ -520,15 +527,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int vs = it.kt.start(st);
 #pragma unroll
                         for (int c = 0; c < C::SLABS; ++c)
-                            tma_load_4d(vbuf + c * C::SLAB_BYTES, &tm_v, b_full, c * 64, vs, it.hk,
-                                        it.b);
+                            tma_load_5d(vbuf + c * C::SLAB_BYTES, &tm_v, b_full, c * 64,
+                                        it.kv_rank, vs, it.hk, it.b);
                     }
                     if (has_k) {
                         const int ks = it.kt.start(st + 1);
 #pragma unroll
                         for (int c = 0; c < C::SLABS; ++c)
-                            tma_load_4d(kbuf + c * C::SLAB_BYTES, &tm_k, b_full, c * 64, ks, it.hk,
-                                        it.b);
+                            tma_load_5d(kbuf + c * C::SLAB_BYTES, &tm_k, b_full, c * 64,
+                                        it.kv_rank, ks, it.hk, it.b);
                     }
                     issued |= 1u << slot;
                     last_ph = (last_ph & ~(1u << slot)) | (ph << slot);
@@ -549,8 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mbar_expect_tx(qf, C::TILE_BYTES);
 #pragma unroll
                             for (int c = 0; c < C::SLABS; ++c)
-                                tma_load_4d(sQ + hh * C::TILE_BYTES + c * C::SLAB_BYTES, &tm_q, qf,
-                                            c * 64, it.qrow0 + hh * BM, it.h, it.b);
+                                tma_load_5d(sQ + hh * C::TILE_BYTES + c * C::SLAB_BYTES, &tm_q, qf,
+                                            c * 64, it.q_rank, it.qrow0 + hh * BM, it.h, it.b);
                             ++qcnt[hh];
                         }
                     }
@@ -688,10 +695,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n = hh ? it.nh[1] : it.nh[0];
             if (it.nmax == 0 || n == 0) continue;
             const int first_row = it.qrow0 + hh * BM;
-            const int row_g = first_row + quarter * 32 + lane;
+            const int row_g = first_row + quarter * 32 + lane;     // index in the segment
+            const int pos = row_g * P.rs + it.q_rank;               // position in the sequence
             if (P.oacc && !(it.flags & SEG_FIRST) && row_g < it.q1) {
                 // the running row is read by this item's epilogue: stage it in L2 now
-                const float *pre = P.oacc + (((int64_t)it.b * P.Hq + it.h) * P.N + row_g) * HD;
+                const float *pre = P.oacc + (((int64_t)it.b * P.Hq + it.h) * P.N + pos) * HD;
 #pragma unroll
                 for (int i = 0; i < HD * 4 / 128; ++i)
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(pre + i * 32));
@@ -711,9 +719,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ks = it.kt.start(t);
                 const int ke = it.kt.range_end(t);
                 const bool need_mask =
-                    (ks + BN > ke) || (P.causal && (min(ks + BN, ke) - 1 > first_row));
+                    (ks + BN > ke) || (P.causal && (min(ks + BN, ke) - 1 + it.diag > first_row));
                 if (need_mask) {
-                    const int lim = (P.causal ? min(ke, row_g + 1) : ke) - ks;
+                    const int lim = (P.causal ? min(ke, row_g + 1 - it.diag) : ke) - ks;
 #pragma unroll
                     for (int c = 0; c < 128; ++c)
                         if (c >= lim) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
@@ -802,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (P.chained) asm volatile("griddepcontrol.wait;" ::: "memory");
             const bool first = (it.flags & SEG_FIRST) != 0;
             const bool final_ = (it.flags & SEG_FINAL) != 0;
-            const int64_t lrow = ((int64_t)it.b * P.Hq + it.h) * P.N + row_g;
+            const int64_t lrow = ((int64_t)it.b * P.Hq + it.h) * P.N + pos;
             const bool valid = row_g < it.q1;
             const bool merge = valid && !first;
             float *arow = P.oacc ? P.oacc + lrow * HD : nullptr;
@@ -822,7 +830,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool use_prev = merge && w.wa != 0.f;
             const float wb = w.wb * inv;
             __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(P.o) + (int64_t)it.b * P.so[0] +
-                                  (int64_t)it.h * P.so[1] + (int64_t)row_g * P.so[2];
+                                  (int64_t)it.h * P.so[1] + (int64_t)pos * P.so[2];
 #pragma unroll 1
             for (int c = 0; c < HD / 32; ++c) {
                 uint32_t o[32];
@@ -907,17 +915,21 @@ static EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-// [B, H, N, D] bf16 with element strides s[0..2] (D contiguous) as a 4-D tiled map
-// (dims D, N, H, B), box 64 x 128 rows, 128-byte swizzle.
+// [B, H, N, D] bf16 with element strides s[0..2] (D contiguous), the sequence axis
+// split as N = (N / rs) x rs (position = index * rs + rank), as a 5-D tiled map with
+// dims (D, rank, index, H, B); box 64 x 1 x 128 rows, 128-byte swizzle.  rs = 1 is the
+// plain layout.
 static bool encode_map(CUtensorMap *map, const void *ptr, int64_t B, int64_t H, int64_t N,
-                       int64_t D, const int64_t *s) {
+                       int64_t D, const int64_t *s, int64_t rs) {
     EncodeTiledFn fn = get_encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
-    cuuint64_t strides[3] = {(cuuint64_t)s[2] * 2, (cuuint64_t)s[1] * 2, (cuuint64_t)s[0] * 2};
-    cuuint32_t box[4] = {64, 128, 1, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box,
+    if (!fn || rs < 1 || N % rs) return false;
+    cuuint64_t dims[5] = {(cuuint64_t)D, (cuuint64_t)rs, (cuuint64_t)(N / rs), (cuuint64_t)H,
+                          (cuuint64_t)B};
+    cuuint64_t strides[4] = {(cuuint64_t)s[2] * 2, (cuuint64_t)(s[2] * rs) * 2,
+                             (cuuint64_t)s[1] * 2, (cuuint64_t)s[0] * 2};
+    cuuint32_t box[5] = {64, 1, 128, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(ptr), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -937,9 +949,9 @@ static cudaError_t launch_tc_hd(const StepParams &P, int blocks_y, int num_sms,
         configured_mask |= 1 << (dev & 31);
     }
     CUtensorMap mq, mk, mv;
-    if (!encode_map(&mq, P.q, P.B, P.Hq, P.N, P.D, P.sq) ||
-        !encode_map(&mk, P.k, P.B, P.Hkv, P.N, P.D, P.sk) ||
-        !encode_map(&mv, P.v, P.B, P.Hkv, P.N, P.D, P.sv))
+    if (!encode_map(&mq, P.q, P.B, P.Hq, P.N, P.D, P.sq, P.rs) ||
+        !encode_map(&mk, P.k, P.B, P.Hkv, P.N, P.D, P.sk, P.rs) ||
+        !encode_map(&mv, P.v, P.B, P.Hkv, P.N, P.D, P.sv, P.rs))
         return cudaErrorInvalidValue;
     const int64_t total = (int64_t)P.B * P.Hq * blocks_y;
     if (total > 0x7fffffff) return cudaErrorInvalidValue;

@@ -164,9 +164,32 @@ static std::vector<Range> rank_ranges(int64_t N, int R, int layout, int r) {
 
 // Segments of one step before flags: for every rank r, each of its query chunks
 // against the chunks of rank (r - step) mod R that some row of the chunk can see.
+// Striped layout: rank r holds positions r, r + R, r + 2R, ...; its segment is indices
+// [0, N/R) of the interleave against the same indices of rank j, with key index j'
+// visible to row index i iff j' + [j > r] <= i under causality.
 static void step_segments(int64_t N, int R, int layout, int causal, int step,
                           std::vector<Seg> &out) {
     out.clear();
+    if (layout == RA_LAYOUT_STRIPED) {
+        const int64_t c = N / R;
+        for (int r = 0; r < R; ++r) {
+            const int j = ((r - step) % R + R) % R;
+            Seg s;
+            memset(&s, 0, sizeof s);
+            s.q0 = 0;
+            s.q1 = (int32_t)c;
+            s.k0[0] = 0;
+            s.k1[0] = (int32_t)c;
+            s.k0[1] = s.k1[1] = (int32_t)c;
+            s.rank = r;
+            s.q_rank = r;
+            s.kv_rank = j;
+            s.diag = (causal && j > r) ? 1 : 0;
+            if (c == 0 || (causal && s.diag > c - 1)) continue;  // no row sees a key
+            out.push_back(s);
+        }
+        return;
+    }
     for (int r = 0; r < R; ++r) {
         const int j = ((r - step) % R + R) % R;
         const std::vector<Range> kv = rank_ranges(N, R, layout, j);
@@ -195,6 +218,10 @@ static void step_segments(int64_t N, int R, int layout, int causal, int step,
 static bool chunk_touched(int64_t N, int R, int layout, int causal, int step, int r, int64_t q0,
                           int64_t q1) {
     const int j = ((r - step) % R + R) % R;
+    if (layout == RA_LAYOUT_STRIPED) {
+        const int64_t c = N / R;
+        return c > 0 && !(causal && j > r && c < 2);
+    }
     for (const Range &kr : rank_ranges(N, R, layout, j)) {
         if (kr.b <= kr.a) continue;
         if (causal && kr.a > q1 - 1) continue;
@@ -224,10 +251,10 @@ static void plan_step(int64_t N, int R, int layout, int causal, int step, std::v
 
 static ra_status check_ring(int64_t N, int R, int layout) {
     if (R < 1) return fail(RA_ERR_INVALID_ARG, "ring_size must be >= 1");
-    if (layout != RA_LAYOUT_CONTIG && layout != RA_LAYOUT_ZIGZAG)
+    if (layout != RA_LAYOUT_CONTIG && layout != RA_LAYOUT_ZIGZAG && layout != RA_LAYOUT_STRIPED)
         return fail(RA_ERR_INVALID_ARG, "unknown layout");
-    if (layout == RA_LAYOUT_CONTIG && N % R != 0)
-        return fail(RA_ERR_INVALID_ARG, "contiguous layout needs N % ring_size == 0");
+    if ((layout == RA_LAYOUT_CONTIG || layout == RA_LAYOUT_STRIPED) && N % R != 0)
+        return fail(RA_ERR_INVALID_ARG, "contiguous and striped layouts need N % ring_size == 0");
     if (layout == RA_LAYOUT_ZIGZAG && N % (2 * (int64_t)R) != 0)
         return fail(RA_ERR_INVALID_ARG, "zigzag layout needs N % (2 ring_size) == 0");
     return RA_OK;
@@ -261,6 +288,7 @@ static void fill_common(StepParams &P, const ra_tensor *q, const ra_tensor *k, c
     P.scale_log2 = sc * kLog2e;
     P.wait_limit_ns = g_wait_limit_ns;
     P.err = di.err;
+    P.rs = 1;
 }
 
 static bool use_tensor_cores(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v,
@@ -331,6 +359,7 @@ ra_status ra_ring_sim_fwd(const ra_tensor *q, const ra_tensor *k, const ra_tenso
     StepParams *P = new StepParams;
     fill_common(*P, q, k, v, o, lse, pb, causal, scale, di);
     P->oacc = ring_size > 1 ? static_cast<float *>(workspace) : nullptr;
+    P->rs = (layout == RA_LAYOUT_STRIPED) ? ring_size : 1;
     const bool tc = use_tensor_cores(q, k, v, o, pb, di);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     std::vector<Seg> segs;
@@ -352,7 +381,7 @@ int64_t ra_ring_sim_plan(int64_t N, int ring_size, ra_layout layout, int causal,
     plan_step(N, ring_size, layout, causal, step, segs);
     for (int64_t i = 0; i < (int64_t)segs.size() && i < cap && segments; ++i) {
         const Seg &x = segs[i];
-        int64_t *o = segments + 8 * i;
+        int64_t *o = segments + 12 * i;
         o[0] = x.q0;
         o[1] = x.q1;
         o[2] = x.k0[0];
@@ -361,6 +390,10 @@ int64_t ra_ring_sim_plan(int64_t N, int ring_size, ra_layout layout, int causal,
         o[5] = x.k1[1];
         o[6] = x.flags;
         o[7] = x.rank;
+        o[8] = x.q_rank;
+        o[9] = x.kv_rank;
+        o[10] = x.diag;
+        o[11] = (layout == RA_LAYOUT_STRIPED) ? ring_size : 1;
     }
     return (int64_t)segs.size();
 }
@@ -672,6 +705,8 @@ extern "C" ra_status ra_ring_sim_fwd_noalloc(const ra_tensor *q, const ra_tensor
     if ((s = check_ring(pb.N, ring_size, layout))) return s;
     if (ring_size > kNoAllocMaxRing)
         return fail(RA_ERR_UNSUPPORTED, "ra_ring_sim_fwd_noalloc: ring_size above 64");
+    if (layout == RA_LAYOUT_STRIPED)
+        return fail(RA_ERR_UNSUPPORTED, "ra_ring_sim_fwd_noalloc: contiguous or zigzag layout only");
     if (pb.B * pb.Hq * pb.N == 0) return RA_OK;
     if (ring_size > 1 && pb.B * pb.Hq * pb.N * pb.D > kNoAllocScratchFloats)
         return fail(RA_ERR_UNSUPPORTED,

@@ -10,15 +10,21 @@
 namespace ra {
 
 // One query chunk of one simulated rank against the key/value block it holds in a
-// ring step.  Key ranges are disjoint and in increasing position; the second may be
-// empty (k0[1] == k1[1]).
+// ring step.  Rows and keys are indices along the sequence axis as seen through a rank
+// interleave of stride StepParams::rs: index i of the query chunk is sequence position
+// i * rs + q_rank, index j of a key range is position j * rs + kv_rank (rs = 1 and
+// ranks 0 for contiguous and zigzag layouts, rs = R for the striped layout).  Key ranges
+// are disjoint and increasing; the second may be empty (k0[1] == k1[1]).  Under
+// causality key index j is visible to row index i iff j + diag <= i (diag = 1 when the
+// key rank follows the query rank in the interleave, else 0).
 struct Seg {
     int32_t q0, q1;
     int32_t k0[2], k1[2];
     int32_t flags;
     int32_t rank;
     int32_t blk0;  // first work block of this segment (variable-length launches)
-    int32_t pad_;
+    int32_t q_rank, kv_rank;
+    int32_t diag;
 };
 
 enum : int32_t { SEG_FIRST = 1, SEG_FINAL = 2 };
@@ -44,6 +50,7 @@ struct StepParams {
     int32_t total_items;     // persistent kernels: work items in this launch
     int32_t chained;         // launched as a dependent of the previous ring step's kernel
     int32_t var_blocks;      // segments have different lengths: decode through Seg::blk0
+    int32_t rs;              // rank interleave stride of the sequence axis (1 unless striped)
     int64_t wait_limit_ns;
     int *err;  // device error word
     Seg seg[kMaxSeg];

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libra.so")
 
 RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_TIMEOUT = range(5)
 RA_F32, RA_BF16 = 0, 1
-LAYOUTS = {"contig": 0, "zigzag": 1}
+LAYOUTS = {"contig": 0, "zigzag": 1, "striped": 2}
 SEG_FIRST, SEG_FINAL = 1, 2
 
 
@@ -179,14 +179,15 @@ def ring_sim_plan(N: int, ring_size: int, layout="contig", causal=False, step=0)
                            None, 0)
     if n < 0:
         raise ValueError("bad ring plan arguments")
-    buf = (ctypes.c_int64 * (8 * max(n, 1)))()
+    buf = (ctypes.c_int64 * (12 * max(n, 1)))()
     L.ra_ring_sim_plan(int(N), int(ring_size), LAYOUTS[layout], int(bool(causal)), int(step),
                        ctypes.cast(buf, ctypes.c_void_p), n)
     out = []
     for i in range(n):
-        q0, q1, ka0, ka1, kb0, kb1, flags, rank = buf[8 * i:8 * i + 8]
+        q0, q1, ka0, ka1, kb0, kb1, flags, rank, q_rank, kv_rank, diag, rs = buf[12 * i:12 * i + 12]
         ranges = [(ka0, ka1)] + ([(kb0, kb1)] if kb1 > kb0 else [])
-        out.append({"q": (q0, q1), "kv": ranges, "flags": flags, "rank": rank})
+        out.append({"q": (q0, q1), "kv": ranges, "flags": flags, "rank": rank, "q_rank": q_rank,
+                    "kv_rank": kv_rank, "diag": diag, "rs": rs})
     return out
 
 

@@ -47,6 +47,8 @@ WORKLOADS = {
                                       torch.bfloat16, True, 1, "contig", 2),
     "ring8_zigzag_h8n32k": Workload("ring8_zigzag_h8n32k", 1, 8, 8, 32768, 128, torch.bfloat16,
                                     True, 8, "zigzag", 3),
+    "ring8_striped_h8n32k": Workload("ring8_striped_h8n32k", 1, 8, 8, 32768, 128, torch.bfloat16,
+                                     True, 8, "striped", 3),
     "gqa_ring16_zigzag_h32kv8n128k": Workload("gqa_ring16_zigzag_h32kv8n128k", 1, 32, 8, 131072,
                                               128, torch.bfloat16, True, 16, "zigzag", 4),
     "ring64_zigzag_h8kv2n1m": Workload("ring64_zigzag_h8kv2n1m", 1, 8, 2, 1048576, 128,

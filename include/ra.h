@@ -47,7 +47,7 @@ typedef enum {
 
 typedef enum { RA_F32 = 0, RA_BF16 = 1 } ra_dtype;
 
-typedef enum { RA_LAYOUT_CONTIG = 0, RA_LAYOUT_ZIGZAG = 1 } ra_layout;
+typedef enum { RA_LAYOUT_CONTIG = 0, RA_LAYOUT_ZIGZAG = 1, RA_LAYOUT_STRIPED = 2 } ra_layout;
 
 typedef struct {
     void *data;        /* device pointer */
@@ -116,6 +116,9 @@ size_t ra_ring_sim_workspace_bytes(const ra_tensor *q, int ring_size);
  *   RA_LAYOUT_CONTIG  rank r holds rows [r c, (r+1) c), c = N / ring_size
  *   RA_LAYOUT_ZIGZAG  2*ring_size chunks; rank r holds chunk r and chunk 2R-1-r
  *                     ("序列并行与 Ring Attention", section "2. ZigZag Ring Attention")
+ *   RA_LAYOUT_STRIPED rank r holds positions r, r + R, r + 2R, ... (tokens spread evenly
+ *                     over the ranks: Striped Attention, named on the glossary page for
+ *                     balancing causal work)
  * At step s rank r holds the key/value block of rank (r - s) mod R; the step's
  * partial for each rank's query rows (causality on global positions, so later
  * blocks are skipped and the diagonal block masked) is merged into a float32 running
@@ -124,7 +127,8 @@ size_t ra_ring_sim_workspace_bytes(const ra_tensor *q, int ring_size);
  * ra_attn_fwd on the whole sequence (up to rounding); inputs and outputs are in
  * natural sequence order; ring_size == 1 is ra_attn_fwd.
  *
- *   ring_size  >= 1; contig needs N % ring_size == 0, zigzag N % (2 ring_size) == 0
+ *   ring_size  >= 1; contig and striped need N % ring_size == 0, zigzag
+ *              N % (2 ring_size) == 0
  *   layout     ra_layout
  *   workspace  device buffer of ra_ring_sim_workspace_bytes() bytes (may be NULL when
  *              that is 0); contents on entry are ignored; owned by the caller
@@ -158,12 +162,17 @@ ra_status ra_attn_varlen_fwd(const ra_tensor *q, const ra_tensor *k, const ra_te
 
 /*
  * ra_ring_sim_plan - host-only description of the ring schedule (no GPU work).
- * For step `step`, writes up to `cap` segments; each segment is 8 int64 values:
- *   q0, q1          query rows [q0, q1) of one chunk of one simulated rank
- *   k0a, k1a        first key range [k0a, k1a)
- *   k0b, k1b        second key range (k0b == k1b when absent)
+ * For step `step`, writes up to `cap` segments; each segment is 12 int64 values:
+ *   q0, q1          query indices [q0, q1) of one chunk of one simulated rank
+ *   k0a, k1a        first key index range [k0a, k1a)
+ *   k0b, k1b        second key index range (k0b == k1b when absent)
  *   flags           bit 0: first partial of these rows, bit 1: last partial
  *   rank            the simulated rank
+ *   q_rank, kv_rank, diag, rs
+ *                   index i of the query chunk is sequence position i*rs + q_rank and
+ *                   key index j is position j*rs + kv_rank; under causality key j is
+ *                   visible to row i iff j + diag <= i (rs = ring_size for the striped
+ *                   layout, else 1 with ranks and diag 0)
  * Returns the number of segments of that step (which may exceed cap), or -1 on bad
  * arguments.
  */

@@ -11,6 +11,8 @@ Partitions
 - zigzag: the sequence is cut into 2R chunks of N / (2R) rows; rank r holds chunk r
   and chunk 2R-1-r ("序列并行与 Ring Attention：超长上下文训练技术解析",
   section "2. ZigZag Ring Attention").
+- striped: rank r holds positions r, r + R, r + 2R, ... (tokens spread evenly over the
+  devices: Striped Attention, named on the glossary page).
 
 Ring schedule: at step s, rank r holds the keys/values of rank (r - s) mod R (the
 worked example of the glossary page; the `ring_attention_forward` listing of
@@ -30,6 +32,7 @@ from .merge import merge_sigmoid
 
 CONTIG = "contig"
 ZIGZAG = "zigzag"
+STRIPED = "striped"
 
 
 def rank_ranges(N: int, R: int, layout: str):
@@ -45,6 +48,15 @@ def rank_ranges(N: int, R: int, layout: str):
         h = N // (2 * R)
         return [[(r * h, (r + 1) * h), ((2 * R - 1 - r) * h, (2 * R - r) * h)] for r in range(R)]
     raise ValueError(layout)
+
+
+def rank_positions(N: int, R: int, layout: str):
+    """Sequence positions held by each rank (increasing)."""
+    if layout == STRIPED:
+        if N % R:
+            raise ValueError("striped layout needs N % R == 0")
+        return [np.arange(r, N, R) for r in range(R)]
+    return [_positions(rr) for rr in rank_ranges(N, R, layout)]
 
 
 def kv_source(r: int, s: int, R: int) -> int:
@@ -91,18 +103,18 @@ def ring_forward(q, k, v, R: int, layout: str, causal: bool, scale: float | None
     G = Hq // Hkv
     if scale is None:
         scale = 1.0 / np.sqrt(D)
-    ranges = rank_ranges(N, R, layout)
+    positions = rank_positions(N, R, layout)
     o_all = np.zeros((B, Hq, N, D))
     lse_all = np.full((B, Hq, N), -np.inf)
     for b in range(B):
         for h in range(Hq):
             hk = h // G
             for r in range(R):
-                qpos = _positions(ranges[r])
+                qpos = positions[r]
                 out = np.zeros((len(qpos), D))
                 lse = np.full(len(qpos), -np.inf)
                 for s in range(R):
-                    kpos = _positions(ranges[kv_source(r, s, R)])
+                    kpos = positions[kv_source(r, s, R)]
                     bo, bl = step_partial(q[b, h], k[b, hk], v[b, hk], qpos, kpos, causal, scale)
                     out, lse = merge_sigmoid(out, lse, bo, bl)
                 o_all[b, h, qpos] = out

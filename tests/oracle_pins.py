@@ -270,6 +270,9 @@ def pin_ring(plant=0):
         (1, 2, 1, 40, 8, 5, "zigzag", False),
         (1, 1, 1, 16, 4, 1, "zigzag", True),
         (1, 2, 1, 64, 8, 8, "zigzag", True),
+        (1, 2, 1, 36, 8, 4, "striped", True),
+        (1, 4, 2, 40, 8, 8, "striped", True),
+        (1, 2, 2, 30, 8, 3, "striped", False),
     ]:
         q = rng.standard_normal((B, Hq, N, D))
         k = rng.standard_normal((B, Hkv, N, D))

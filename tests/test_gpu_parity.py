@@ -154,6 +154,12 @@ RING_SMALL = [
     (1, 2, 1, 256, 32, 4, "zigzag", True, torch.bfloat16),   # CUDA-core path
     (1, 2, 1, 96, 16, 4, "zigzag", True, torch.float32),
     (1, 1, 1, 64, 16, 8, "contig", False, torch.float32),
+    (1, 2, 1, 2048, 128, 4, "striped", True, torch.bfloat16),
+    (1, 4, 2, 1024, 128, 8, "striped", True, torch.bfloat16),
+    (1, 2, 2, 768, 64, 3, "striped", True, torch.bfloat16),
+    (1, 2, 1, 1000, 128, 5, "striped", False, torch.bfloat16),   # 200 rows per rank: ragged
+    (1, 2, 1, 96, 16, 4, "striped", True, torch.float32),
+    (1, 2, 1, 256, 32, 8, "striped", True, torch.bfloat16),       # CUDA-core path
 ]
 
 
@@ -168,13 +174,14 @@ def test_ring_sim_small(ra, case):
 
 
 def test_ring_invariants_gpu(ra):
-    """R = 1 vs R = 4 contig vs R = 4 zigzag on the GPU: same result within rounding."""
+    """R = 1 vs R = 4 contig / zigzag / striped on the GPU: same result within rounding."""
     q, k, v = synth.make_qkv(1, 4, 2, 4096, 128, torch.bfloat16, seed=9, device="cuda")
     o1, l1 = ra.attn_fwd(q, k, v, causal=True)
     oc, lc = ra.ring_sim_fwd(q, k, v, 4, "contig", causal=True)
     oz, lz = ra.ring_sim_fwd(q, k, v, 4, "zigzag", causal=True)
+    os_, ls = ra.ring_sim_fwd(q, k, v, 4, "striped", causal=True)
     ra.check()
-    for o, l, name in ((oc, lc, "contig"), (oz, lz, "zigzag")):
+    for o, l, name in ((oc, lc, "contig"), (oz, lz, "zigzag"), (os_, ls, "striped")):
         assert (o.float() - o1.float()).abs().max().item() <= 2e-2, name
         assert ((l - l1).abs() / l1.abs().clamp(min=1)).max().item() <= 1e-3, name
 

@@ -105,19 +105,21 @@ def test_merge_argument_errors(ra):
 
 
 def _covered(plan_steps, N, causal):
-    """For every query row, the multiset of keys it is scheduled to see over all steps."""
+    """For every query position, the list of key positions it is scheduled to see."""
     seen = {}
     for segs in plan_steps:
         for s in segs:
+            rs, qr, kr, dg = s["rs"], s["q_rank"], s["kv_rank"], s["diag"]
             for i in range(*s["q"]):
                 for a, b in s["kv"]:
-                    hi = min(b, i + 1) if causal else b
-                    if hi > a:
-                        seen.setdefault(i, []).append((a, hi))
+                    for j in range(a, b):
+                        if causal and j + dg > i:
+                            continue
+                        seen.setdefault(i * rs + qr, []).append(j * rs + kr)
     return seen
 
 
-@pytest.mark.parametrize("layout", ["contig", "zigzag"])
+@pytest.mark.parametrize("layout", ["contig", "zigzag", "striped"])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("R", [1, 2, 3, 4, 8])
 def test_plan_covers_every_visible_key_once(ra, layout, causal, R):
@@ -125,19 +127,22 @@ def test_plan_covers_every_visible_key_once(ra, layout, causal, R):
     steps = [ra.ring_sim_plan(N, R, layout, causal, s) for s in range(R)]
     seen = _covered(steps, N, causal)
     for i in range(N):
-        keys = sorted(k for a, b in seen.get(i, []) for k in range(a, b))
+        keys = sorted(seen.get(i, []))
         want = list(range(0, i + 1)) if causal else list(range(N))
         assert keys == want, (i, keys[:10])
     # first/last flags: every query chunk has exactly one FIRST and one FINAL segment
     firsts, finals = {}, {}
     for segs in steps:
         for s in segs:
-            firsts[s["q"]] = firsts.get(s["q"], 0) + (s["flags"] & ra.SEG_FIRST > 0)
-            finals[s["q"]] = finals.get(s["q"], 0) + (s["flags"] & ra.SEG_FINAL > 0)
+            key = (s["rank"], s["q"])
+            firsts[key] = firsts.get(key, 0) + (s["flags"] & ra.SEG_FIRST > 0)
+            finals[key] = finals.get(key, 0) + (s["flags"] & ra.SEG_FINAL > 0)
     assert set(firsts.values()) == {1} and set(finals.values()) == {1}
     # the rank partition matches the oracle's restatement
+    held = oring.rank_positions(N, R, layout)
     for s in steps[0]:
-        assert s["q"] in [tuple(x) for x in oring.rank_ranges(N, R, layout)[s["rank"]]]
+        pos = [i * s["rs"] + s["q_rank"] for i in range(*s["q"])]
+        assert set(pos) <= set(held[s["rank"]].tolist())
 
 
 @pytest.mark.parametrize("R", [2, 3, 4, 8])
@@ -181,6 +186,16 @@ def test_plan_contig_causal_block_classes(ra, golden_dir):
         else:
             assert len(segs) == 1 and segs[0]["kv"] == [(kb * c, (kb + 1) * c)]
             assert (kb == qb) == (cls == "diagonal")
+
+
+def test_plan_striped_is_balanced(ra):
+    """Striped ranks see (almost) the same number of causal pairs at every step."""
+    R, N = 8, 8 * 64
+    for s_ in range(R):
+        segs = ra.ring_sim_plan(N, R, "striped", True, s_)
+        assert len(segs) == R
+        for g in segs:
+            assert g["rs"] == R and g["diag"] == (1 if g["kv_rank"] > g["q_rank"] else 0)
 
 
 def test_plan_rejects_bad_arguments(ra):
