@@ -17,6 +17,7 @@ int attn_tc_rows_per_block();
 cudaError_t launch_wait_selftest(int64_t limit_ns, int *err, cudaStream_t stream);
 
 cudaError_t launch_lse_merge(const MergeParams &P, int num_sms, cudaStream_t stream);
+cudaError_t launch_attn_bwd_simt(const BwdParams &P, int num_sms, cudaStream_t stream);
 cudaError_t launch_fill_identity(void *o, int o_bf16, const int64_t *so, float *lse, int B, int H,
                                  int N, int D, int r0, int r1, int num_sms, cudaStream_t stream);
 }  // namespace ra
@@ -489,6 +490,76 @@ ra_status ra_attn_varlen_fwd(const ra_tensor *q, const ra_tensor *k, const ra_te
     }
     delete P;
     return s;
+}
+
+size_t ra_attn_bwd_workspace_bytes(const ra_tensor *q) {
+    if (!q) return 0;
+    for (int i = 0; i < 4; ++i)
+        if (q->shape[i] < 0) return 0;
+    return (size_t)(q->shape[0] * q->shape[1] * q->shape[2]) * sizeof(float);
+}
+
+ra_status ra_attn_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v, const ra_tensor *o,
+                      const float *lse, const ra_tensor *dout, ra_tensor *dq, ra_tensor *dk,
+                      ra_tensor *dv, int causal, float scale, void *workspace, void *stream) {
+    Problem pb;
+    ra_status s = check_qkvo(q, k, v, o, lse, pb);
+    if (s) return s;
+    if ((s = check_tensor(dout, "dout")) || (s = check_tensor(dq, "dq")) ||
+        (s = check_tensor(dk, "dk")) || (s = check_tensor(dv, "dv")))
+        return s;
+    for (int i = 0; i < 4; ++i) {
+        if (dout->shape[i] != q->shape[i] || dq->shape[i] != q->shape[i])
+            return fail(RA_ERR_INVALID_ARG, "dout and dq must have q's shape");
+        if (dk->shape[i] != k->shape[i] || dv->shape[i] != k->shape[i])
+            return fail(RA_ERR_INVALID_ARG, "dk and dv must have k's shape");
+    }
+    if (dout->dtype != pb.dtype || dq->dtype != pb.dtype || dk->dtype != pb.dtype ||
+        dv->dtype != pb.dtype)
+        return fail(RA_ERR_INVALID_ARG, "gradients must share q's dtype");
+    if (isnan(scale)) return fail(RA_ERR_INVALID_ARG, "scale is NaN");
+    if (pb.B * pb.Hq * pb.N == 0) return RA_OK;
+    if (!workspace) return fail(RA_ERR_INVALID_ARG, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(workspace) % 16)
+        return fail(RA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    DevInfo di;
+    std::string msg;
+    if (!device_info(di, msg)) return fail(RA_ERR_CUDA, msg);
+    BwdParams P;
+    memset(&P, 0, sizeof P);
+    P.q = q->data;
+    P.k = k->data;
+    P.v = v->data;
+    P.o = o->data;
+    P.dout = dout->data;
+    P.dq = dq->data;
+    P.dk = dk->data;
+    P.dv = dv->data;
+    for (int i = 0; i < 3; ++i) {
+        P.sq[i] = q->stride[i];
+        P.sk[i] = k->stride[i];
+        P.sv[i] = v->stride[i];
+        P.so[i] = o->stride[i];
+        P.sdo[i] = dout->stride[i];
+        P.sdq[i] = dq->stride[i];
+        P.sdk[i] = dk->stride[i];
+        P.sdv[i] = dv->stride[i];
+    }
+    P.lse = lse;
+    P.dvec = static_cast<float *>(workspace);
+    P.B = (int32_t)pb.B;
+    P.Hq = (int32_t)pb.Hq;
+    P.Hkv = (int32_t)pb.Hkv;
+    P.N = (int32_t)pb.N;
+    P.D = (int32_t)pb.D;
+    P.bf16 = pb.dtype == RA_BF16;
+    P.causal = causal ? 1 : 0;
+    P.scale = scale > 0.f ? scale : (float)(1.0 / sqrt((double)pb.D));
+    P.scale_log2 = P.scale * kLog2e;
+    cudaError_t e = launch_attn_bwd_simt(P, di.sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    t_launches += 3;
+    return RA_OK;
 }
 
 ra_status ra_lse_merge(ra_tensor *o_acc, float *lse_acc, const ra_tensor *o_blk,

@@ -70,6 +70,19 @@ struct MergeParams {
     int64_t rows;
 };
 
+// Gradients of attention (see attn_bwd_simt.cu).
+struct BwdParams {
+    const void *q, *k, *v, *o, *dout;
+    void *dq, *dk, *dv;
+    int64_t sq[3], sk[3], sv[3], so[3], sdo[3], sdq[3], sdk[3], sdv[3];
+    const float *lse;  // [B, Hq, N]
+    float *dvec;       // [B, Hq, N] rowsum(dO * O)
+    int32_t B, Hq, Hkv, N, D;
+    int32_t bf16;
+    int32_t causal;
+    float scale, scale_log2;
+};
+
 // Device error codes (first one wins).
 enum : int { DERR_TIMEOUT = 1 };
 

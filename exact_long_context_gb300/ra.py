@@ -53,6 +53,10 @@ def lib() -> ctypes.CDLL:
             L.ra_ring_sim_fwd.argtypes = [T, T, T, T, P, c_int, c_int, c_int, c_float, P, P]
             L.ra_attn_varlen_fwd.argtypes = [T, T, T, T, P, P, c_int, c_int, c_float, P]
             L.ra_attn_varlen_fwd.restype = c_int
+            L.ra_attn_bwd_workspace_bytes.argtypes = [T]
+            L.ra_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+            L.ra_attn_bwd.argtypes = [T, T, T, T, P, T, T, T, T, c_int, c_float, P, P]
+            L.ra_attn_bwd.restype = c_int
             L.ra_ring_sim_plan.argtypes = [i64, c_int, c_int, c_int, c_int, P, i64]
             L.ra_ring_sim_plan.restype = i64
             L.ra_check_device_error.argtypes = [P]
@@ -138,6 +142,28 @@ def attn_varlen_fwd(q, k, v, cu_seqlens, causal=False, scale=None, o=None, lse=N
                                     len(cu_seqlens) - 1, int(bool(causal)), float(scale or 0.0),
                                     _stream(stream)))
     return o, lse
+
+
+def attn_bwd(q, k, v, o, lse, dout, causal=False, scale=None, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of attn_fwd for the loss sum(dout * o)."""
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    dqd = _desc(q, "q")
+    need = int(lib().ra_attn_bwd_workspace_bytes(ctypes.byref(dqd)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32")
+    descs = [_desc(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"))]
+    dd = _desc(dout, "dout")
+    gq, gk, gv = _desc(dq, "dq"), _desc(dk, "dk"), _desc(dv, "dv")
+    _check(lib().ra_attn_bwd(*(ctypes.byref(x) for x in descs), _ptr(lse), ctypes.byref(dd),
+                             ctypes.byref(gq), ctypes.byref(gk), ctypes.byref(gv),
+                             int(bool(causal)), float(scale or 0.0), _ptr(workspace),
+                             _stream(stream)))
+    return dq, dk, dv
 
 
 def lse_merge(o_acc, lse_acc, o_blk, lse_blk, stream=None):

@@ -161,6 +161,26 @@ ra_status ra_attn_varlen_fwd(const ra_tensor *q, const ra_tensor *k, const ra_te
                              int causal, float scale, void *stream);
 
 /*
+ * ra_attn_bwd - gradients of ra_attn_fwd for the loss L = sum(dout * O).
+ *
+ * Recomputes P = exp(scale Q K^T - LSE) from the forward's LSE and follows the backward
+ * of the `ring_attention_backward` listing of "Ring Attention 论文解析" over the whole key
+ * axis: D = rowsum(dout * O), dV = P^T dout, dS = P * (dout V^T - D),
+ * dQ = scale dS K, dK = scale dS^T Q (grouped query heads summed into their KV head).
+ *
+ *   q, k, v, o, lse  the forward's inputs and outputs (o and lse as ra_attn_fwd wrote them)
+ *   dout             [B, Hq, N, D] gradient of O (q's dtype)
+ *   dq               [B, Hq, N, D] (written); dk, dv [B, Hkv, N, D] (written)
+ *   workspace        device buffer of ra_attn_bwd_workspace_bytes() bytes, 16-byte aligned
+ * Errors: as ra_attn_fwd, plus RA_ERR_INVALID_ARG for gradient shape/dtype mismatches or a
+ *   missing workspace.
+ */
+size_t ra_attn_bwd_workspace_bytes(const ra_tensor *q);
+ra_status ra_attn_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v, const ra_tensor *o,
+                      const float *lse, const ra_tensor *dout, ra_tensor *dq, ra_tensor *dk,
+                      ra_tensor *dv, int causal, float scale, void *workspace, void *stream);
+
+/*
  * ra_ring_sim_plan - host-only description of the ring schedule (no GPU work).
  * For step `step`, writes up to `cap` segments; each segment is 12 int64 values:
  *   q0, q1          query indices [q0, q1) of one chunk of one simulated rank

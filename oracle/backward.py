@@ -1,0 +1,65 @@
+"""Gradients of exact attention, fp64.  TEST INFRASTRUCTURE ONLY.
+
+For the loss L = sum(dO * O) with O = softmax(scale Q K^T (+ mask)) V, the gradients are
+written out as in the `ring_attention_backward` listing of "Ring Attention 论文解析：
+在分布式环境中实现无限上下文窗口训练" (there per ring step; here for the whole key axis,
+which is the sum of those per-block terms):
+
+    D_i   = sum_t dO[i,t] O[i,t]
+    P_ij  = exp(s_ij - LSE_i)                (s_ij = scale q_i . k_j, visible pairs only)
+    dV_j  = sum_i P_ij dO_i
+    dP_ij = dO_i . v_j
+    dS_ij = P_ij (dP_ij - D_i)
+    dQ_i  = scale sum_j dS_ij k_j
+    dK_j  = scale sum_i dS_ij q_i
+
+With grouped KV heads (query head h reads KV head h // G) dK and dV of a KV head are
+the sums over its G query heads.  O and LSE are computed here from the definition, so
+the result is the exact gradient of the exact attention.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _f64(a):
+    a = np.asarray(a)
+    if a.dtype == np.uint16:  # bfloat16 bit patterns
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def attention_bwd(q, k, v, do, causal: bool, scale: float | None = None):
+    """Returns (dq [B,Hq,N,D], dk [B,Hkv,N,D], dv [B,Hkv,N,D], o, lse) in fp64."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, Hq, N, D = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    vis = np.tril(np.ones((N, N), bool)) if causal else np.ones((N, N), bool)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    o = np.zeros_like(q)
+    lse = np.full((B, Hq, N), -np.inf)
+    for b in range(B):
+        for h in range(Hq):
+            hk = h // G
+            s = scale * (q[b, h] @ k[b, hk].T)
+            s = np.where(vis, s, -np.inf)
+            m = s.max(axis=1, keepdims=True)
+            e = np.where(vis, np.exp(s - m), 0.0)
+            z = e.sum(axis=1, keepdims=True)
+            lse_bh = (m + np.log(z))[:, 0]
+            o_bh = (e / z) @ v[b, hk]
+            p = np.where(vis, np.exp(s - lse_bh[:, None]), 0.0)
+            d_i = np.sum(do[b, h] * o_bh, axis=1)
+            dv[b, hk] += p.T @ do[b, h]
+            dp = do[b, h] @ v[b, hk].T
+            ds = p * (dp - d_i[:, None])
+            dq[b, h] = scale * (ds @ k[b, hk])
+            dk[b, hk] += scale * (ds.T @ q[b, h])
+            o[b, h] = o_bh
+            lse[b, h] = lse_bh
+    return dq, dk, dv, o, lse

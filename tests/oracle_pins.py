@@ -370,3 +370,60 @@ def pin_varlen(plant=0):
 
 
 ALL_PINS.append("pin_varlen")
+
+
+def pin_backward():
+    """The gradient oracle against torch autograd (fp64) and central finite differences."""
+    import torch
+
+    from oracle import backward as ob
+
+    rng = np.random.default_rng(23)
+    for (B, Hq, Hkv, N, D, causal) in [(1, 2, 1, 9, 4, True), (2, 4, 2, 13, 8, False),
+                                        (1, 3, 3, 7, 5, True)]:
+        q = rng.standard_normal((B, Hq, N, D))
+        k = rng.standard_normal((B, Hkv, N, D))
+        v = rng.standard_normal((B, Hkv, N, D))
+        do = rng.standard_normal((B, Hq, N, D))
+        scale = 0.6 / np.sqrt(D)
+        dq, dk, dv, o, lse = ob.attention_bwd(q, k, v, do, causal, scale)
+        # the forward it differentiates is the oracle's forward
+        of, lf = oracle.attention(q, k, v, causal, scale)
+        _close(o, of, what="backward oracle forward O")
+        _close(lse, lf, what="backward oracle forward LSE")
+        # autograd on an independent torch formulation
+        tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+        G = Hq // Hkv
+        s = scale * torch.einsum("bhid,bhjd->bhij", tq, tk.repeat_interleave(G, dim=1))
+        if causal:
+            s = s.masked_fill(~torch.tril(torch.ones(N, N, dtype=torch.bool)), float("-inf"))
+        out = torch.softmax(s, dim=-1) @ tv.repeat_interleave(G, dim=1)
+        (out * torch.tensor(do)).sum().backward()
+        _close(dq, tq.grad.numpy(), tol=1e-11, what="dq vs autograd")
+        _close(dk, tk.grad.numpy(), tol=1e-11, what="dk vs autograd")
+        _close(dv, tv.grad.numpy(), tol=1e-11, what="dv vs autograd")
+    # central finite differences of L = sum(dO * O) on a tiny case
+    B, Hq, Hkv, N, D = 1, 2, 1, 5, 3
+    q = rng.standard_normal((B, Hq, N, D))
+    k = rng.standard_normal((B, Hkv, N, D))
+    v = rng.standard_normal((B, Hkv, N, D))
+    do = rng.standard_normal((B, Hq, N, D))
+    dq, dk, dv, _, _ = ob.attention_bwd(q, k, v, do, True, 0.5)
+
+    def loss(qq, kk, vv):
+        o_, _ = oracle.attention(qq, kk, vv, True, 0.5)
+        return float(np.sum(do * o_))
+
+    eps = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            xp = x.copy(); xp[idx] += eps
+            xm = x.copy(); xm[idx] -= eps
+            args_p = [q, k, v]; args_m = [q, k, v]
+            pos = "qkv".index(name)
+            args_p[pos] = xp; args_m[pos] = xm
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+        _close(g, num, tol=1e-7, what=f"d{name} vs finite differences")

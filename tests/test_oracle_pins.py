@@ -93,3 +93,7 @@ def test_merge_identity_both_forms():
 
 def test_varlen_block_diagonal():
     P.pin_varlen()
+
+
+def test_backward_oracle():
+    P.pin_backward()
