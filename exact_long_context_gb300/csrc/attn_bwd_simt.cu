@@ -234,6 +234,17 @@ __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(const __grid_constant_
     }
 }
 
+cudaError_t launch_bwd_rowdot(const BwdParams &P, int num_sms, cudaStream_t stream) {
+    if (P.B <= 0 || P.Hq <= 0 || P.N <= 0) return cudaSuccess;
+    const int64_t rows = (int64_t)P.B * P.Hq * P.N;
+    const int g0 = (int)std::min<int64_t>((rows + 7) / 8, (int64_t)num_sms * 16);
+    if (P.bf16)
+        bwd_rowdot_kernel<true><<<g0, 256, 0, stream>>>(P);
+    else
+        bwd_rowdot_kernel<false><<<g0, 256, 0, stream>>>(P);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_attn_bwd_simt(const BwdParams &P, int num_sms, cudaStream_t stream) {
     if (P.B <= 0 || P.Hq <= 0 || P.N <= 0) return cudaSuccess;
     const int64_t rows = (int64_t)P.B * P.Hq * P.N;

@@ -18,6 +18,9 @@ cudaError_t launch_wait_selftest(int64_t limit_ns, int *err, cudaStream_t stream
 
 cudaError_t launch_lse_merge(const MergeParams &P, int num_sms, cudaStream_t stream);
 cudaError_t launch_attn_bwd_simt(const BwdParams &P, int num_sms, cudaStream_t stream);
+cudaError_t launch_bwd_rowdot(const BwdParams &P, int num_sms, cudaStream_t stream);
+cudaError_t launch_attn_bwd_tc(const BwdParams &P, int num_sms, int64_t wait_ns, int *err,
+                               cudaStream_t stream);
 cudaError_t launch_fill_identity(void *o, int o_bf16, const int64_t *so, float *lse, int B, int H,
                                  int N, int D, int r0, int r1, int num_sms, cudaStream_t stream);
 }  // namespace ra
@@ -556,7 +559,17 @@ ra_status ra_attn_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v
     P.causal = causal ? 1 : 0;
     P.scale = scale > 0.f ? scale : (float)(1.0 / sqrt((double)pb.D));
     P.scale_log2 = P.scale * kLog2e;
-    cudaError_t e = launch_attn_bwd_simt(P, di.sms, static_cast<cudaStream_t>(stream));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool tc = di.tc_ok && pb.dtype == RA_BF16 && (pb.D == 64 || pb.D == 128) && aligned16(q) &&
+                    aligned16(k) && aligned16(v) && aligned16(dout) && aligned16(dq) &&
+                    aligned16(dk) && aligned16(dv);
+    cudaError_t e;
+    if (tc) {
+        e = launch_bwd_rowdot(P, di.sms, st);
+        if (e == cudaSuccess) e = launch_attn_bwd_tc(P, di.sms, g_wait_limit_ns, di.err, st);
+    } else {
+        e = launch_attn_bwd_simt(P, di.sms, st);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     t_launches += 3;
     return RA_OK;

@@ -34,7 +34,10 @@ CASES = [
     (1, 2, 2, 128, 128, True, torch.bfloat16),
     (1, 4, 1, 200, 128, True, torch.bfloat16),
     (2, 2, 2, 96, 64, False, torch.bfloat16),
-    (1, 2, 1, 50, 32, True, torch.bfloat16),
+    (1, 2, 1, 50, 32, True, torch.bfloat16),     # CUDA-core path (D = 32)
+    (1, 4, 2, 1000, 128, True, torch.bfloat16),  # tensor cores: ragged tail, GQA
+    (1, 2, 2, 512, 64, True, torch.bfloat16),
+    (2, 2, 1, 384, 128, False, torch.bfloat16),
 ]
 
 
@@ -55,6 +58,29 @@ def test_backward_matches_oracle(ra, case):
         err = np.max(np.abs(got - ref)) / max(1.0, np.max(np.abs(ref)))
         assert err <= TOL[dtype], f"{name}: scaled max-abs error {err:.3e}"
         print(case, name, f"{err:.2e}")
+
+
+def test_backward_tensor_cores_match_cuda_cores(ra):
+    """Same values through the tensor-core kernels (aligned) and the CUDA-core kernels
+    (rows of 136 elements viewed as 128: strides not 16-byte multiples)."""
+    B, Hq, Hkv, N, D = 1, 4, 2, 700, 128
+    g = torch.Generator(device="cuda").manual_seed(4)
+    raw = torch.randn(4, B, Hq, N, 136, generator=g, device="cuda").to(torch.bfloat16)
+    q_u, do_u = raw[0][..., :D], raw[3][..., :D]
+    k_u, v_u = raw[1][:, :Hkv, :, :D], raw[2][:, :Hkv, :, :D]
+    q, k, v, do = (t.contiguous() for t in (q_u, k_u, v_u, do_u))
+    o, lse = ra.attn_fwd(q, k, v, causal=True)
+    a = ra.attn_bwd(q, k, v, o, lse, do, causal=True)
+    o_u = torch.empty(B, Hq, N, 136, dtype=torch.bfloat16, device="cuda")[..., :D]
+    o_u.copy_(o)
+    bq = torch.empty_like(raw[0])[..., :D]
+    bk = torch.empty(B, Hkv, N, 136, dtype=torch.bfloat16, device="cuda")[..., :D]
+    bv = torch.empty(B, Hkv, N, 136, dtype=torch.bfloat16, device="cuda")[..., :D]
+    c = ra.attn_bwd(q_u, k_u, v_u, o_u, lse, do_u, causal=True, dq=bq, dk=bk, dv=bv)
+    ra.check()
+    for x, y, name in zip(a, c, ("dq", "dk", "dv")):
+        err = (x.float() - y.float()).abs().max().item() / max(1.0, y.float().abs().max().item())
+        assert err <= 2e-2, (name, err)
 
 
 def test_backward_empty_and_errors(ra):
