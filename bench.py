@@ -158,8 +158,23 @@ def run_ours(args, w, ws, rank, local):
 
     varlen = isinstance(w, synth.VarlenWorkload)
     cu = w.cu_seqlens() if varlen else None
+    bwd = args.pass_ == "bwd"
+    if bwd:
+        if varlen or w.ring_size != 1:
+            raise SystemExit("--pass bwd times the single-pass backward (ring_size 1 workloads)")
+        ra.ring_sim_fwd(q, k, v, 1, w.layout, causal=w.causal, scale=w.scale, o=o, lse=lse,
+                        stream=stream)
+        g = torch.Generator(device=dev)
+        g.manual_seed(w.seed + 1000)
+        dout = torch.randn(q.shape, generator=g, device=dev).to(q.dtype)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        bws = torch.empty(max(16, w.B * w.Hq * w.N * 4), dtype=torch.uint8, device=dev)
 
     def step():
+        if bwd:
+            ra.attn_bwd(q, k, v, o, lse, dout, causal=w.causal, scale=w.scale, dq=dq, dk=dk, dv=dv,
+                        workspace=bws, stream=stream)
+            return
         if varlen:
             ra.attn_varlen_fwd(q, k, v, cu, causal=w.causal, scale=w.scale, o=o, lse=lse,
                                stream=stream)
@@ -203,13 +218,14 @@ def run_ours(args, w, ws, rank, local):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
-    flops = w.flops()
+    # backward: the conventional 2.5x of the forward (five products of the forward's size)
+    flops = w.flops() * (2.5 if bwd else 1.0)
     value = flops * args.steps * ws / (total_ms * 1e-3) / 1e12
     launches_per_step = launches / args.steps
 
     # end to end through the public call: pinned host inputs -> device -> host result
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and not bwd:
         hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
         ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
         hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
@@ -359,6 +375,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="time the forward (default) or the backward of ring_size-1 workloads")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -373,7 +391,8 @@ def main():
               "causal": w.causal, "ring_size": w.ring_size, "layout": w.layout,
               **({"sequences": len(w.lengths())} if isinstance(w, synth.VarlenWorkload) else {}),
               "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{ws}"}
-    line = {"metric": METRIC, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+    metric = METRIC if args.pass_ == "fwd" else METRIC.replace("attention fwd", "attention bwd")
+    line = {"metric": metric, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
             "data": "synthetic (seeded N(0,1), rounded to bf16)", "config": config}
@@ -393,6 +412,13 @@ def main():
     if rank == 0:
         line.update(res)
         line["pct_of_peak"] = round(100 * res["roofline"]["frac"], 2)
+        if args.pass_ == "bwd":
+            line["cpu_baseline"] = None  # the oracle's timed leg is the forward
+            print(json.dumps(line), flush=True)
+            if ws > 1:
+                torch.distributed.barrier()
+                torch.distributed.destroy_process_group()
+            return
         f, sec, nrows, threads = oracle_rate_sample(w, args.cpu_budget_s)
         line["cpu_baseline"] = {
             "value": round(f / sec / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
