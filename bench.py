@@ -45,6 +45,21 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float) -> float:
+    """The largest value of x over all ranks (identity without a process group)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(x)
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Units processed by all ranks per second of the slowest rank's timed region."""
+    return units_per_rank_step * steps * world / (max_ms * 1e-3)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -212,15 +227,11 @@ def run_ours(args, w, ws, rank, local):
     ra.check(stream)
     clk = clocks.stop()
     times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = float(sum(times))
-    if ws > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(sum(times)))
     ms_per_step = total_ms / args.steps
     # backward: the conventional 2.5x of the forward (five products of the forward's size)
     flops = w.flops() * (2.5 if bwd else 1.0)
-    value = flops * args.steps * ws / (total_ms * 1e-3) / 1e12
+    value = whole_job_rate(flops, args.steps, ws, total_ms) / 1e12
     launches_per_step = launches / args.steps
 
     # end to end through the public call: pinned host inputs -> device -> host result
@@ -257,10 +268,7 @@ def run_ours(args, w, ws, rank, local):
             ee.synchronize()
             etot += es.elapsed_time(ee)
         ra.check(stream)
-        if ws > 1:
-            t = torch.tensor([etot], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            etot = float(t.item())
+        etot = max_over_ranks(etot)
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
         d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
         e2e = {"value": round(flops * args.e2e_steps * ws / (etot * 1e-3) / 1e12, 2),
@@ -282,6 +290,65 @@ def run_ours(args, w, ws, rank, local):
         "wall_s_timed_region": round(wall, 4),
         "tokens_per_s": round(w.B * w.N * args.steps * ws / (total_ms * 1e-3), 1),
     }
+
+
+def run_hbm_pass(args, w, ws, rank, local):
+    """HBM-bound calls: the standalone LSE merge on the workload's whole running output
+    (fp32 o_acc [B,Hq,N,D], bf16 o_blk, 1292 algorithmic bytes per row at D = 128) or the
+    Ulysses exchange of the workload's Q (read + write of every element)."""
+    from exact_long_context_gb300 import ra
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed + 7)
+    stream = torch.cuda.current_stream(dev)
+    if args.pass_ == "merge":
+        shape = (w.B, w.Hq, w.N, w.D)
+        o_acc = torch.randn(shape, generator=g, device=dev)
+        o_blk = torch.randn(shape, generator=g, device=dev).to(torch.bfloat16)
+        lse_acc = torch.randn(shape[:3], generator=g, device=dev)
+        lse_blk = torch.randn(shape[:3], generator=g, device=dev)
+        rows = w.B * w.Hq * w.N
+        nbytes = rows * (w.D * 4 * 2 + w.D * 2 + 4 * 3)
+
+        def step():
+            ra.lse_merge(o_acc, lse_acc, o_blk, lse_blk, stream=stream)
+    else:
+        sp = max(1, min(8, w.Hq))
+        while w.Hq % sp or w.N % sp:
+            sp -= 1
+        x = torch.randn((sp, w.N // sp, w.Hq, w.D), generator=g, device=dev).to(w.dtype)
+        y = torch.empty((sp, w.N, w.Hq // sp, w.D), dtype=w.dtype, device=dev)
+        nbytes = 2 * x.numel() * x.element_size()
+
+        def step():
+            ra.ulysses_all_to_all(x, sp, to_heads=True, out=y, stream=stream)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        step()
+    ra.check(stream)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    launches0 = ra.launch_count()
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    launches = ra.launch_count() - launches0
+    ra.check(stream)
+    total_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)))
+    gbs = whole_job_rate(nbytes, args.steps, ws, total_ms) / 1e9
+    _, hbm, kind = peaks()
+    per_rank = gbs / ws
+    return {"value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(total_ms / args.steps, 5),
+            "gpu_launches": launches, "higher_is_better": True,
+            "roofline": {"bound": "hbm", "achieved": round(per_rank, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(per_rank / hbm, 4), "traffic": None, "peak_kind": kind},
+            "bytes_per_step": nbytes}
 
 
 def oracle_rate_sample(w, budget_s, seed=0):
@@ -375,8 +442,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
-    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
-                    help="time the forward (default) or the backward of ring_size-1 workloads")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "merge", "ulysses"], default="fwd",
+                    help="fwd (default): the hot path; bwd: the backward of ring_size-1 workloads; "
+                         "merge / ulysses: the HBM-bound LSE merge / Ulysses exchange")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -391,7 +459,9 @@ def main():
               "causal": w.causal, "ring_size": w.ring_size, "layout": w.layout,
               **({"sequences": len(w.lengths())} if isinstance(w, synth.VarlenWorkload) else {}),
               "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{ws}"}
-    metric = METRIC if args.pass_ == "fwd" else METRIC.replace("attention fwd", "attention bwd")
+    metric = {"fwd": METRIC, "bwd": METRIC.replace("attention fwd", "attention bwd"),
+              "merge": "lse_merge GB/s (algorithmic bytes) and % of measured HBM bandwidth",
+              "ulysses": "Ulysses all-to-all GB/s and % of measured HBM bandwidth"}[args.pass_]
     line = {"metric": metric, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
@@ -408,6 +478,17 @@ def main():
         print(json.dumps(line), flush=True)
         return
 
+    if args.pass_ in ("merge", "ulysses"):
+        res = run_hbm_pass(args, w, ws, rank, local)
+        if rank == 0:
+            line.update(res)
+            line["unit"] = "GB/s"
+            line["dtype"] = "f32+bf16" if args.pass_ == "merge" else line["dtype"]
+            print(json.dumps(line), flush=True)
+        if ws > 1:
+            torch.distributed.barrier()
+            torch.distributed.destroy_process_group()
+        return
     res = run_ours(args, w, ws, rank, local)
     if rank == 0:
         line.update(res)

@@ -19,6 +19,7 @@ cudaError_t launch_wait_selftest(int64_t limit_ns, int *err, cudaStream_t stream
 cudaError_t launch_lse_merge(const MergeParams &P, int num_sms, cudaStream_t stream);
 cudaError_t launch_attn_bwd_simt(const BwdParams &P, int num_sms, cudaStream_t stream);
 cudaError_t launch_bwd_rowdot(const BwdParams &P, int num_sms, cudaStream_t stream);
+cudaError_t launch_ulysses(const UlyssesParams &P, int num_sms, cudaStream_t stream);
 cudaError_t launch_attn_bwd_tc(const BwdParams &P, int num_sms, int64_t wait_ns, int *err,
                                cudaStream_t stream);
 cudaError_t launch_fill_identity(void *o, int o_bf16, const int64_t *so, float *lse, int B, int H,
@@ -572,6 +573,47 @@ ra_status ra_attn_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v
     }
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     t_launches += 3;
+    return RA_OK;
+}
+
+ra_status ra_ulysses_all_to_all(const ra_tensor *in, ra_tensor *out, int sp, int to_heads,
+                                void *stream) {
+    ra_status s;
+    if ((s = check_tensor(in, "in")) || (s = check_tensor(out, "out"))) return s;
+    if (in->dtype != out->dtype) return fail(RA_ERR_INVALID_ARG, "in and out must share a dtype");
+    if (sp < 1) return fail(RA_ERR_INVALID_ARG, "sp must be >= 1");
+    const ra_tensor *seq = to_heads ? in : out;
+    const ra_tensor *head = to_heads ? out : in;
+    const int64_t S = seq->shape[1] * sp, H = seq->shape[2], D = seq->shape[3];
+    if (seq->shape[0] != sp || head->shape[0] != sp || head->shape[1] != S ||
+        head->shape[2] * sp != H || head->shape[3] != D || H % sp != 0)
+        return fail(RA_ERR_INVALID_ARG,
+                    "expected sequence shards [sp, S/sp, H, D] and head shards [sp, S, H/sp, D]");
+    if (S * H * D == 0) return RA_OK;
+    if (S > INT32_MAX || H > INT32_MAX || D > INT32_MAX)
+        return fail(RA_ERR_UNSUPPORTED, "dimension too large");
+    DevInfo di;
+    std::string msg;
+    if (!device_info(di, msg)) return fail(RA_ERR_CUDA, msg);
+    UlyssesParams P;
+    memset(&P, 0, sizeof P);
+    P.in = in->data;
+    P.out = out->data;
+    for (int i = 0; i < 4; ++i) {
+        P.si[i] = in->stride[i];
+        P.so[i] = out->stride[i];
+    }
+    P.sp = sp;
+    P.S = (int32_t)S;
+    P.H = (int32_t)H;
+    P.D = (int32_t)D;
+    P.esize = esize(in->dtype);
+    P.to_heads = to_heads ? 1 : 0;
+    const int64_t per16 = 16 / P.esize;
+    P.vec = (D % per16 == 0) && aligned16(in) && aligned16(out);
+    cudaError_t e = launch_ulysses(P, di.sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ulysses launch");
+    ++t_launches;
     return RA_OK;
 }
 

@@ -83,6 +83,17 @@ struct BwdParams {
     float scale, scale_log2;
 };
 
+// Ulysses all-to-all as a layout transform (see ulysses.cu).
+struct UlyssesParams {
+    const void *in;
+    void *out;
+    int64_t si[4], so[4];  // element strides of in / out (dims 0..3)
+    int32_t sp, S, H, D;   // full sequence S, all heads H
+    int32_t esize;         // 2 or 4 bytes
+    int32_t to_heads;      // 1: seq shards -> head shards, 0: inverse
+    int32_t vec;           // rows are 16-byte aligned and D * esize % 16 == 0
+};
+
 // Device error codes (first one wins).
 enum : int { DERR_TIMEOUT = 1 };
 

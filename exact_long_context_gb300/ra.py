@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
             L.ra_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
             L.ra_attn_bwd.argtypes = [T, T, T, T, P, T, T, T, T, c_int, c_float, P, P]
             L.ra_attn_bwd.restype = c_int
+            L.ra_ulysses_all_to_all.argtypes = [T, T, c_int, c_int, P]
+            L.ra_ulysses_all_to_all.restype = c_int
             L.ra_ring_sim_plan.argtypes = [i64, c_int, c_int, c_int, c_int, P, i64]
             L.ra_ring_sim_plan.restype = i64
             L.ra_check_device_error.argtypes = [P]
@@ -164,6 +166,20 @@ def attn_bwd(q, k, v, o, lse, dout, causal=False, scale=None, dq=None, dk=None, 
                              int(bool(causal)), float(scale or 0.0), _ptr(workspace),
                              _stream(stream)))
     return dq, dk, dv
+
+
+def ulysses_all_to_all(x, sp: int, to_heads: bool, out=None, stream=None):
+    """Sequence shards [sp, S/sp, H, D] <-> head shards [sp, S, H/sp, D] (exact copy)."""
+    if out is None:
+        if to_heads:
+            _, ss, H, D = x.shape
+            out = torch.empty((sp, ss * sp, H // sp, D), dtype=x.dtype, device=x.device)
+        else:
+            _, S, hs, D = x.shape
+            out = torch.empty((sp, S // sp, hs * sp, D), dtype=x.dtype, device=x.device)
+    _check(lib().ra_ulysses_all_to_all(ctypes.byref(_desc(x, "in")), ctypes.byref(_desc(out, "out")),
+                                       int(sp), int(bool(to_heads)), _stream(stream)))
+    return out
 
 
 def lse_merge(o_acc, lse_acc, o_blk, lse_blk, stream=None):

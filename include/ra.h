@@ -181,6 +181,22 @@ ra_status ra_attn_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v
                       ra_tensor *dv, int causal, float scale, void *workspace, void *stream);
 
 /*
+ * ra_ulysses_all_to_all - the Ulysses sequence <-> head exchange of sp ranks, restated as a
+ * layout transform of one GPU's memory ("序列并行与 Ring Attention：超长上下文训练技术解析",
+ * section "1. Ulysses (All-to-All)": scatter the head axis, gather the sequence axis).
+ *
+ *   to_heads != 0: in  = sequence shards [sp, S/sp, H, D] (rank r holds positions
+ *                        [r S/sp, (r+1) S/sp), all heads)
+ *                  out = head shards     [sp, S, H/sp, D] (rank r holds heads
+ *                        [r H/sp, (r+1) H/sp), whole sequence)
+ *   to_heads == 0: the inverse (in = head shards, out = sequence shards).
+ * Element strides are free (dim 3 contiguous); H % sp == 0.  The copy is exact.
+ * Errors: RA_ERR_INVALID_ARG for mismatched shapes or dtypes, RA_ERR_CUDA.
+ */
+ra_status ra_ulysses_all_to_all(const ra_tensor *in, ra_tensor *out, int sp, int to_heads,
+                                void *stream);
+
+/*
  * ra_ring_sim_plan - host-only description of the ring schedule (no GPU work).
  * For step `step`, writes up to `cap` segments; each segment is 12 int64 values:
  *   q0, q1          query indices [q0, q1) of one chunk of one simulated rank

@@ -427,3 +427,31 @@ def pin_backward():
             args_p[pos] = xp; args_m[pos] = xm
             num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * eps)
         _close(g, num, tol=1e-7, what=f"d{name} vs finite differences")
+
+
+def pin_ulysses():
+    """The all-to-all restatement: round trip, element formula, labelled example."""
+    from oracle import ulysses as ou
+
+    rng = np.random.default_rng(31)
+    for sp, S, H, D in [(1, 8, 4, 3), (2, 8, 4, 3), (4, 12, 8, 2), (8, 16, 8, 5)]:
+        x = rng.standard_normal((sp, S // sp, H, D))
+        y = ou.seq_to_heads(x, sp)
+        assert y.shape == (sp, S, H // sp, D)
+        assert np.array_equal(ou.heads_to_seq(y, sp), x), "round trip"
+        ss, hs = S // sp, H // sp
+        for _ in range(50):
+            r, s, j = rng.integers(sp), rng.integers(S), rng.integers(hs)
+            assert np.array_equal(y[r, s, j], x[s // ss, s % ss, r * hs + j])
+    # labelled: value = 1000 * position + head; rank r must hold the whole sequence of
+    # its heads, positions in order
+    sp, S, H = 4, 8, 8
+    lab = np.zeros((sp, S // sp, H, 1))
+    for r in range(sp):
+        for i in range(S // sp):
+            for h in range(H):
+                lab[r, i, h, 0] = 1000 * (r * (S // sp) + i) + h
+    y = ou.seq_to_heads(lab, sp)
+    for r in range(sp):
+        want = np.array([[1000 * p + h for h in range(r * 2, r * 2 + 2)] for p in range(S)])
+        assert np.array_equal(y[r, :, :, 0], want)

@@ -1,0 +1,52 @@
+"""bench.py's multi-rank logic on CPU: two gloo ranks, max-over-ranks timing and the
+whole-job rate (each rank an independent replica, so the rate sums over ranks)."""
+import os
+import socket
+
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, out):
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    ws, r, local = bench.dist_env()
+    local_ms = 100.0 + 50.0 * rank  # rank 1 is the slower one
+    mx = bench.max_over_ranks(local_ms)
+    rate = bench.whole_job_rate(2.0e12, 10, ws, mx)
+    out[rank] = (ws, r, local, mx, rate)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_slowest_rank():
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_rank, args=(2, port, out), nprocs=2, join=True)
+        res = dict(out)
+    assert res[0][:3] == (2, 0, 0) and res[1][:3] == (2, 1, 1)
+    for rank in (0, 1):
+        assert res[rank][3] == 150.0
+        assert abs(res[rank][4] - 2.0e12 * 10 * 2 / 0.150) < 1e-3 * res[rank][4]
+
+
+def test_single_process_is_identity():
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+
+    assert bench.max_over_ranks(3.5) == 3.5
+    assert bench.whole_job_rate(1.0, 4, 1, 2.0) == 2000.0

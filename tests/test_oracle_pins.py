@@ -97,3 +97,7 @@ def test_varlen_block_diagonal():
 
 def test_backward_oracle():
     P.pin_backward()
+
+
+def test_ulysses_oracle():
+    P.pin_ulysses()
