@@ -5,6 +5,8 @@
 //   L = max(a,b) + ln(1 + e^-|a-b|),  o <- e^(a-L) o_acc + e^(b-L) o_blk,  lse <- L.
 // HBM-bound: one warp per row, lanes own contiguous 16-byte pieces of the row so every
 // load and store is coalesced; a grid-stride loop over rows on a grid sized to the SMs.
+// For D <= 128 the row's loads are issued before the weights are computed, so a row
+// costs one memory latency instead of two.
 #include <algorithm>
 
 #include "ra_internal.cuh"
@@ -21,11 +23,50 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const __grid_constant__ 
         const int64_t n = row % P.N;
         const int64_t bh = row / P.N;
         const int64_t h = bh % P.H, b = bh / P.H;
+        float *acc = P.oacc + b * P.sa[0] + h * P.sa[1] + n * P.sa[2];
+        const int64_t boff = b * P.sb[0] + h * P.sb[1] + n * P.sb[2];
+        if (vec && P.D <= 128) {
+            // every load is issued before the weights are known (one memory latency per
+            // row); the values of an identity side are discarded by select, never used
+            const int d = lane * 4;
+            const bool in = d < P.D;
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
+            if (in) {
+                x = __ldcs(reinterpret_cast<const float4 *>(acc + d));
+                if constexpr (BF16) {
+                    const uint2 u = __ldcs(reinterpret_cast<const uint2 *>(
+                        static_cast<const uint16_t *>(P.oblk) + boff + d));
+                    y0 = __uint_as_float(u.x << 16);
+                    y1 = __uint_as_float(u.x & 0xffff0000u);
+                    y2 = __uint_as_float(u.y << 16);
+                    y3 = __uint_as_float(u.y & 0xffff0000u);
+                } else {
+                    const float4 f = __ldcs(reinterpret_cast<const float4 *>(
+                        static_cast<const float *>(P.oblk) + boff + d));
+                    y0 = f.x;
+                    y1 = f.y;
+                    y2 = f.z;
+                    y3 = f.w;
+                }
+            }
+            const MergeW w = merge_weights(P.lse_acc[row], P.lse_blk[row]);
+            if (w.wa == 0.f) x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (w.wb == 0.f) y0 = y1 = y2 = y3 = 0.f;
+            if (in) {
+                x.x = w.wa * x.x + w.wb * y0;
+                x.y = w.wa * x.y + w.wb * y1;
+                x.z = w.wa * x.z + w.wb * y2;
+                x.w = w.wa * x.w + w.wb * y3;
+                __stcs(reinterpret_cast<float4 *>(acc + d), x);
+            }
+            __syncwarp();
+            if (lane == 0) P.lse_acc[row] = w.L;
+            continue;
+        }
         const float a = P.lse_acc[row];
         const float bl = P.lse_blk[row];
         const MergeW w = merge_weights(a, bl);
-        float *acc = P.oacc + b * P.sa[0] + h * P.sa[1] + n * P.sa[2];
-        const int64_t boff = b * P.sb[0] + h * P.sb[1] + n * P.sb[2];
         if (vec) {
             for (int d = lane * 4; d < P.D; d += 128) {
                 float4 x = (w.wa != 0.f) ? *reinterpret_cast<const float4 *>(acc + d)
