@@ -63,3 +63,57 @@ def attention_bwd(q, k, v, do, causal: bool, scale: float | None = None):
             o[b, h] = o_bh
             lse[b, h] = lse_bh
     return dq, dk, dv, o, lse
+
+
+def ring_backward(q, k, v, do, R: int, layout: str, causal: bool, scale: float | None = None,
+                  steps: bool = False):
+    """Gradients on the ring schedule of R simulated ranks.  fp64.
+
+    The `ring_attention_backward` listing of "Ring Attention 论文解析" keeps dQ on the
+    query's rank and, at step s, computes rank r's block gradients against the
+    key/value block it holds, that of rank j = (r - s) mod R, with the forward's
+    saved LSE and D = rowsum(dO * O); the block's dK / dV go back to rank j, which sums
+    them.  The forward's causal rule on global positions applies to every block (the
+    listing shows no mask; the gradient of the causal forward needs it).  O and LSE are
+    the ring forward's.
+
+    Returns (dq, dk, dv), and with ``steps=True`` also a list over steps of each step's
+    (dq, dk, dv) contributions (full-size arrays, zero where the step adds nothing).
+    """
+    from .ring import kv_source, rank_positions, ring_forward
+
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, Hq, N, D = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    o, lse = ring_forward(q, k, v, R, layout, causal, scale)
+    dvec = np.sum(do * o, axis=-1)
+    positions = rank_positions(N, R, layout)
+    per_step = []
+    for s in range(R):
+        dq_s = np.zeros_like(q)
+        dk_s = np.zeros_like(k)
+        dv_s = np.zeros_like(v)
+        for r in range(R):
+            j = kv_source(r, s, R)
+            qpos, kpos = positions[r], positions[j]
+            vis = (kpos[None, :] <= qpos[:, None]) if causal else np.ones((len(qpos), len(kpos)), bool)
+            for b in range(B):
+                for h in range(Hq):
+                    hk = h // G
+                    sc = scale * (q[b, h, qpos] @ k[b, hk, kpos].T)
+                    p = np.where(vis, np.exp(np.where(vis, sc, 0.0) - lse[b, h, qpos][:, None]), 0.0)
+                    dp = do[b, h, qpos] @ v[b, hk, kpos].T
+                    ds = p * (dp - dvec[b, h, qpos][:, None])
+                    dq_s[b, h, qpos] += scale * (ds @ k[b, hk, kpos])
+                    dk_s[b, hk, kpos] += scale * (ds.T @ q[b, h, qpos])
+                    dv_s[b, hk, kpos] += p.T @ do[b, h, qpos]
+        per_step.append((dq_s, dk_s, dv_s))
+    dq = sum(x[0] for x in per_step)
+    dk = sum(x[1] for x in per_step)
+    dv = sum(x[2] for x in per_step)
+    if steps:
+        return dq, dk, dv, per_step
+    return dq, dk, dv

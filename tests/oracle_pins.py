@@ -429,6 +429,90 @@ def pin_backward():
         _close(g, num, tol=1e-7, what=f"d{name} vs finite differences")
 
 
+def pin_ring_backward():
+    """The ring-scheduled gradients against the whole-sequence gradients and, step by
+    step, against torch autograd taken with respect to the score matrix.
+
+    - Summed over the R steps they equal ``attention_bwd`` (itself pinned to autograd
+      and finite differences) for every layout, ring size, mask and head grouping.
+    - Step s of rank r is the gradient through the scores of r's rows against the keys
+      of rank (r - s) mod R only: dS and P of the full problem come from autograd on
+      S = scale Q K^T (so the D = rowsum(dO * O) term is not retyped here), and the
+      step's dQ / dK / dV are their products restricted to that block.
+    - Zigzag steps follow the Twinkle page's three cases: for s > r the front query
+      chunk of rank r adds nothing; for 0 < s <= r the back key chunk of the held
+      block receives nothing.
+    """
+    import torch
+
+    from oracle import backward as ob
+
+    rng = np.random.default_rng(29)
+    B, Hq, Hkv, D = 1, 4, 2, 8
+    G = Hq // Hkv
+    for (N, R, layout, causal) in [(24, 3, oring.CONTIG, True), (24, 3, oring.ZIGZAG, True),
+                                   (24, 4, oring.STRIPED, True), (24, 2, oring.ZIGZAG, False),
+                                   (20, 5, oring.STRIPED, False), (16, 1, oring.CONTIG, True),
+                                   (32, 4, oring.ZIGZAG, True)]:
+        q = rng.standard_normal((B, Hq, N, D))
+        k = rng.standard_normal((B, Hkv, N, D))
+        v = rng.standard_normal((B, Hkv, N, D))
+        do = rng.standard_normal((B, Hq, N, D))
+        scale = 0.7 / np.sqrt(D)
+        dq, dk, dv, steps = ob.ring_backward(q, k, v, do, R, layout, causal, scale, steps=True)
+        fq, fk, fv, _, _ = ob.attention_bwd(q, k, v, do, causal, scale)
+        what = f"{layout} R={R} causal={causal}"
+        _close(dq, fq, what="ring dq " + what)
+        _close(dk, fk, what="ring dk " + what)
+        _close(dv, fv, what="ring dv " + what)
+        assert len(steps) == R
+        # autograd with respect to the scaled scores
+        tq, tk = torch.tensor(q), torch.tensor(k).repeat_interleave(G, dim=1)
+        S = (scale * torch.einsum("bhid,bhjd->bhij", tq, tk)).detach().requires_grad_(True)
+        Sm = S
+        if causal:
+            Sm = S.masked_fill(~torch.tril(torch.ones(N, N, dtype=torch.bool)), float("-inf"))
+        Pt = torch.softmax(Sm, dim=-1)
+        (Pt @ torch.tensor(v).repeat_interleave(G, dim=1) * torch.tensor(do)).sum().backward()
+        dS = S.grad.numpy()
+        Pf = Pt.detach().numpy()
+        if layout == oring.STRIPED:
+            pos = [np.arange(r, N, R) for r in range(R)]
+        elif layout == oring.CONTIG:
+            c = N // R
+            pos = [np.arange(r * c, (r + 1) * c) for r in range(R)]
+        else:
+            h2 = N // (2 * R)
+            pos = [np.concatenate([np.arange(r * h2, (r + 1) * h2),
+                                   np.arange((2 * R - 1 - r) * h2, (2 * R - r) * h2)]) for r in range(R)]
+        for s_, (sq, sk, sv) in enumerate(steps):
+            eq = np.zeros_like(q)
+            ek = np.zeros_like(k)
+            ev = np.zeros_like(v)
+            for r in range(R):
+                j = (r - s_) % R  # the block rank r holds at step s (glossary worked example)
+                qp, kp = pos[r], pos[j]
+                for h in range(Hq):
+                    blk = dS[0, h][np.ix_(qp, kp)]
+                    pb = Pf[0, h][np.ix_(qp, kp)]
+                    eq[0, h, qp] += scale * blk @ k[0, h // G, kp]
+                    ek[0, h // G, kp] += scale * blk.T @ q[0, h, qp]
+                    ev[0, h // G, kp] += pb.T @ do[0, h, qp]
+            _close(sq, eq, tol=1e-11, what=f"step {s_} dq " + what)
+            _close(sk, ek, tol=1e-11, what=f"step {s_} dk " + what)
+            _close(sv, ev, tol=1e-11, what=f"step {s_} dv " + what)
+            if layout == oring.ZIGZAG and causal:
+                h2 = N // (2 * R)
+                for r in range(R):
+                    j = (r - s_) % R
+                    case = oring.zigzag_step_case(r, s_, R)
+                    if case == "back_q":
+                        assert not np.any(sq[:, :, r * h2:(r + 1) * h2]), what
+                    if case == "front_kv":
+                        back = slice((2 * R - 1 - j) * h2, (2 * R - j) * h2)
+                        assert not np.any(sk[:, :, back]) or R == 1, what
+
+
 def pin_ulysses():
     """The all-to-all restatement: round trip, element formula, labelled example."""
     from oracle import ulysses as ou

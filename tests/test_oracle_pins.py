@@ -31,6 +31,10 @@ def test_ring_restatement_equals_single_pass():
     P.pin_ring()
 
 
+def test_ring_backward_steps():
+    P.pin_ring_backward()
+
+
 def test_zigzag_map_and_step_cases(golden_dir):
     P.pin_zigzag_map(golden_dir)
 
