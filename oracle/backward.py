@@ -117,3 +117,64 @@ def ring_backward(q, k, v, do, R: int, layout: str, causal: bool, scale: float |
     if steps:
         return dq, dk, dv, per_step
     return dq, dk, dv
+
+
+def gradient_rows(q, k, v, do, causal: bool, scale: float | None = None, q_rows=None, kv_rows=None,
+                  nthreads: int | None = None):
+    """Selected rows of the gradients, each from its definition, for problems too large
+    for :func:`attention_bwd`.
+
+    q_rows: (b, h, i) triples -> dq rows [n, D]; kv_rows: (b, hk, j) triples -> dk and dv
+    rows [m, D].  The forward rows a gradient row needs (row i itself for dQ_i; every
+    row of the G query heads that sees key j for dK_j, dV_j) come from the attention
+    oracle; then, per the formulas above, with D_i = dO_i . O_i:
+        dQ_i = scale sum_j P_ij (dO_i . v_j - D_i) k_j
+        dK_j = scale sum_i P_ij (dO_i . v_j - D_i) q_i,   dV_j = sum_i P_ij dO_i.
+    Returns (dq_rows, dk_rows, dv_rows) (None for an empty selection).
+    """
+    from . import attention
+
+    qf, kf, vf, dof = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, Hq, N, D = qf.shape
+    Hkv = kf.shape[1]
+    G = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    q_rows = np.zeros((0, 3), np.int64) if q_rows is None else np.asarray(q_rows, np.int64).reshape(-1, 3)
+    kv_rows = np.zeros((0, 3), np.int64) if kv_rows is None else np.asarray(kv_rows, np.int64).reshape(-1, 3)
+    need = set(map(tuple, q_rows.tolist()))
+    for b, hk, j in kv_rows.tolist():
+        lo = j if causal else 0
+        for h in range(hk * G, (hk + 1) * G):
+            need.update((b, h, i) for i in range(lo, N))
+    need = sorted(need)
+    fwd = {}
+    if need:
+        o_r, l_r = attention(q, k, v, causal, scale, rows=np.array(need, np.int64), nthreads=nthreads)
+        for n_, key in enumerate(need):
+            fwd[key] = (o_r[n_], l_r[n_])
+    dq_out = None
+    if len(q_rows):
+        dq_out = np.zeros((len(q_rows), D))
+        for n_, (b, h, i) in enumerate(q_rows.tolist()):
+            hk = h // G
+            o_i, lse_i = fwd[(b, h, i)]
+            hi = i + 1 if causal else N
+            p = np.exp(scale * (kf[b, hk, :hi] @ qf[b, h, i]) - lse_i)
+            ds = p * (vf[b, hk, :hi] @ dof[b, h, i] - dof[b, h, i] @ o_i)
+            dq_out[n_] = scale * (ds @ kf[b, hk, :hi])
+    dk_out = dv_out = None
+    if len(kv_rows):
+        dk_out = np.zeros((len(kv_rows), D))
+        dv_out = np.zeros((len(kv_rows), D))
+        for n_, (b, hk, j) in enumerate(kv_rows.tolist()):
+            lo = j if causal else 0
+            for h in range(hk * G, (hk + 1) * G):
+                idx = range(lo, N)
+                o_i = np.array([fwd[(b, h, i)][0] for i in idx]).reshape(-1, D)
+                lse_i = np.array([fwd[(b, h, i)][1] for i in idx])
+                p = np.exp(scale * (qf[b, h, lo:] @ kf[b, hk, j]) - lse_i)
+                ds = p * (dof[b, h, lo:] @ vf[b, hk, j] - np.sum(dof[b, h, lo:] * o_i, axis=1))
+                dk_out[n_] += scale * (ds @ qf[b, h, lo:])
+                dv_out[n_] += p @ dof[b, h, lo:]
+    return dq_out, dk_out, dv_out

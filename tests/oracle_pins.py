@@ -513,6 +513,26 @@ def pin_ring_backward():
                         assert not np.any(sk[:, :, back]) or R == 1, what
 
 
+def pin_gradient_rows():
+    """Gradient rows computed one by one equal the rows of the whole-problem gradients."""
+    from oracle import backward as ob
+
+    rng = np.random.default_rng(31)
+    for causal, (B, Hq, Hkv, N, D) in [(True, (2, 4, 2, 37, 8)), (False, (1, 3, 1, 29, 5)),
+                                       (True, (1, 2, 2, 1, 4))]:
+        q = rng.standard_normal((B, Hq, N, D))
+        k = rng.standard_normal((B, Hkv, N, D))
+        v = rng.standard_normal((B, Hkv, N, D))
+        do = rng.standard_normal((B, Hq, N, D))
+        fq, fk, fv, _, _ = ob.attention_bwd(q, k, v, do, causal, 0.45)
+        qr = np.array([(b, h, i) for b in range(B) for h in range(Hq) for i in {0, N // 2, N - 1}])
+        kr = np.array([(b, h, j) for b in range(B) for h in range(Hkv) for j in {0, N // 3, N - 1}])
+        gq, gk, gv = ob.gradient_rows(q, k, v, do, causal, 0.45, qr, kr)
+        _close(gq, fq[qr[:, 0], qr[:, 1], qr[:, 2]], what="dq rows")
+        _close(gk, fk[kr[:, 0], kr[:, 1], kr[:, 2]], what="dk rows")
+        _close(gv, fv[kr[:, 0], kr[:, 1], kr[:, 2]], what="dv rows")
+
+
 def pin_ulysses():
     """The all-to-all restatement: round trip, element formula, labelled example."""
     from oracle import ulysses as ou

@@ -35,6 +35,10 @@ def test_ring_backward_steps():
     P.pin_ring_backward()
 
 
+def test_gradient_rows_match_whole_gradients():
+    P.pin_gradient_rows()
+
+
 def test_zigzag_map_and_step_cases(golden_dir):
     P.pin_zigzag_map(golden_dir)
 
