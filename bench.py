@@ -175,20 +175,21 @@ def run_ours(args, w, ws, rank, local):
     cu = w.cu_seqlens() if varlen else None
     bwd = args.pass_ == "bwd"
     if bwd:
-        if varlen or w.ring_size != 1:
-            raise SystemExit("--pass bwd times the single-pass backward (ring_size 1 workloads)")
-        ra.ring_sim_fwd(q, k, v, 1, w.layout, causal=w.causal, scale=w.scale, o=o, lse=lse,
-                        stream=stream)
+        if varlen:
+            raise SystemExit("--pass bwd times the ring (or single-pass) backward, not packed batches")
+        ra.ring_sim_fwd(q, k, v, w.ring_size, w.layout, causal=w.causal, scale=w.scale, o=o, lse=lse,
+                        workspace=wsbuf if need else None, stream=stream)
         g = torch.Generator(device=dev)
         g.manual_seed(w.seed + 1000)
         dout = torch.randn(q.shape, generator=g, device=dev).to(q.dtype)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        bws = torch.empty(max(16, w.B * w.Hq * w.N * 4), dtype=torch.uint8, device=dev)
+        bws = torch.empty(max(16, ra.ring_sim_bwd_workspace_bytes(q, k, w.ring_size)), dtype=torch.uint8,
+                          device=dev)
 
     def step():
         if bwd:
-            ra.attn_bwd(q, k, v, o, lse, dout, causal=w.causal, scale=w.scale, dq=dq, dk=dk, dv=dv,
-                        workspace=bws, stream=stream)
+            ra.ring_sim_bwd(q, k, v, o, lse, dout, w.ring_size, w.layout, causal=w.causal, scale=w.scale,
+                            dq=dq, dk=dk, dv=dv, workspace=bws, stream=stream)
             return
         if varlen:
             ra.attn_varlen_fwd(q, k, v, cu, causal=w.causal, scale=w.scale, o=o, lse=lse,
@@ -443,7 +444,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "merge", "ulysses"], default="fwd",
-                    help="fwd (default): the hot path; bwd: the backward of ring_size-1 workloads; "
+                    help="fwd (default): the hot path; bwd: its backward (ring schedule when ring_size > 1); "
                          "merge / ulysses: the HBM-bound LSE merge / Ulysses exchange")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

@@ -4,12 +4,14 @@
 // `ring_attention_backward` listing of "Ring Attention 论文解析"), as two persistent
 // kernels with one writer per output element (no atomics):
 //
-//   dQ kernel   one CTA item = 128 query rows of one (b, h); for each visible key tile:
+//   dQ kernel   one CTA item = 128 query rows of one segment and one (b, h); for each
+//               visible key tile of the segment's streamed ranges:
 //                 S  = Q K^T,  dP = dO V^T          (tcgen05, A and B from shared memory)
 //                 dS = P * (dP - D),  P = exp(S * scale - LSE)   (one thread per row)
 //                 dQ += dS K                        (tcgen05, A = dS from tensor memory)
-//   dK/dV kernel one CTA item = 128 keys of one (b, KV head); for each visible query tile
-//                of every query head that reads the KV head:
+//   dK/dV kernel one CTA item = 128 keys of one segment and one (b, KV head); for each
+//                visible query tile of the streamed ranges, for every query head that
+//                reads the KV head:
 //                 S^T = K Q^T,  dP^T = V dO^T
 //                 P^T, dS^T                         (one thread per key)
 //                 dV += P^T dO,  dK += dS^T Q       (A from tensor memory)
@@ -21,6 +23,10 @@
 // columns of the fp32 S / dP they came from once those are in registers; the MMA
 // thread issues the next S / dP of a half after the products that read it (tcgen05 MMAs
 // of a thread run in order).  Every wait is bounded like the forward kernel's.
+//
+// A launch covers the segments of one ring step (struct BSeg): the whole-sequence
+// backward is one segment.  On a ring, the gradient of a range that earlier or later
+// steps also write is carried between steps in fp32 running buffers (store_grad_chunk).
 #include "tc_common.cuh"
 
 namespace ra {
@@ -57,31 +63,86 @@ struct BBars {
 };
 static_assert(sizeof(BBars) <= 256, "barrier block");
 
-// dQ item L: query tile of one (b, h), the heaviest (most key tiles under causality) first.
-__device__ __forceinline__ void decode_q(const BwdParams &P, int nq, int L, int &b, int &h, int &hk,
-                                         int &qi, int &n) {
+// dQ item L: query tile qi of one segment and one (b, h), the last tiles (most keys
+// under causality) first.  Rows [r_lo, r_hi) of the segment's fixed range; streamed key
+// tiles: n0 from the first range, then n - n0 from the second.
+struct QItem {
+    int b, h, hk, si, r_lo, r_hi, n0, n;
+};
+__device__ __forceinline__ void decode_q(const BwdParams &P, int tps, int L, QItem &it) {
     const int BH = P.B * P.Hq;
-    const int w = L / BH;
-    const int bh = L - w * BH;
-    b = bh / P.Hq;
-    h = bh - b * P.Hq;
-    hk = h / (P.Hq / P.Hkv);
-    qi = nq - 1 - w;
-    n = P.causal ? min(qi + 1, nq) : nq;
+    const int per = P.nseg * BH;
+    const int w = L / per;
+    const int rem = L - w * per;
+    it.si = rem / BH;
+    const int bh = rem - it.si * BH;
+    it.b = bh / P.Hq;
+    it.h = bh - it.b * P.Hq;
+    it.hk = it.h / (P.Hq / P.Hkv);
+    const BSeg &S = P.seg[it.si];
+    it.r_lo = S.f0 + (tps - 1 - w) * kT;
+    it.r_hi = min(it.r_lo + kT, S.f1);
+    it.n = 0;
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        const int a = S.s0[p];
+        const int e = P.causal ? min(S.s1[p], it.r_hi - S.diag) : S.s1[p];
+        const int np = e > a ? (e - a + kT - 1) / kT : 0;
+        if (p == 0) it.n0 = np;
+        it.n += np;
+    }
 }
 
-// dK/dV item L: keys [kj*128, +128) of (b, hk), the heaviest (most query tiles) first; it
-// visits query tiles q_first .. nq-1 of each of the G query heads, n = G (nq - q_first).
-__device__ __forceinline__ void decode_kv(const BwdParams &P, int nq, int L, int &b, int &hk,
-                                          int &kj, int &q_first, int &n) {
+// Streamed key tile t of a dQ item: first key index and the end of its range.
+__device__ __forceinline__ void q_tile(const BSeg &S, const QItem &it, int t, int &k0, int &klim) {
+    const int p = t < it.n0 ? 0 : 1;
+    k0 = p ? S.s0[1] + (t - it.n0) * kT : S.s0[0] + t * kT;
+    klim = p ? S.s1[1] : S.s1[0];
+}
+
+// dK/dV item L: key tile kj of one segment and one (b, KV head), the first tiles (most
+// query tiles under causality) first; it visits the visible query tiles of both streamed
+// ranges for each of the G query heads: n = G * per.
+struct KItem {
+    int b, hk, si, c_lo, c_hi, t0[2], n0, per, n;
+};
+__device__ __forceinline__ void decode_kv(const BwdParams &P, int L, KItem &it) {
     const int BHk = P.B * P.Hkv;
-    const int w = L / BHk;
-    const int bhk = L - w * BHk;
-    b = bhk / P.Hkv;
-    hk = bhk - b * P.Hkv;
-    kj = w;
-    q_first = P.causal ? kj : 0;
-    n = (P.Hq / P.Hkv) * (nq - q_first);
+    const int per_all = P.nseg * BHk;
+    const int w = L / per_all;
+    const int rem = L - w * per_all;
+    it.si = rem / BHk;
+    const int bhk = rem - it.si * BHk;
+    it.b = bhk / P.Hkv;
+    it.hk = bhk - it.b * P.Hkv;
+    const BSeg &S = P.seg[it.si];
+    it.c_lo = S.f0 + w * kT;
+    it.c_hi = min(it.c_lo + kT, S.f1);
+    it.per = 0;
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        const int a = P.causal ? max(S.s0[p], it.c_lo + S.diag) : S.s0[p];
+        int np = 0, t0 = 0;
+        if (a < S.s1[p]) {
+            t0 = (a - S.s0[p]) / kT;
+            np = (S.s1[p] - S.s0[p] + kT - 1) / kT - t0;
+        }
+        it.t0[p] = t0;
+        if (p == 0) it.n0 = np;
+        it.per += np;
+    }
+    it.n = (P.Hq / P.Hkv) * it.per;
+}
+
+// Streamed query tile t of a dK/dV item: first query index, the end of its range, head.
+__device__ __forceinline__ void kv_tile(const BSeg &S, const KItem &it, int G, int t, int &q0, int &qlim,
+                                        int &g) {
+    g = t / it.per;
+    const int tt = t - g * it.per;
+    const int p = tt < it.n0 ? 0 : 1;
+    q0 = p ? S.s0[1] + (it.t0[1] + tt - it.n0) * kT : S.s0[0] + (it.t0[0] + tt) * kT;
+    qlim = p ? S.s1[1] : S.s1[0];
+    (void)G;
 }
 
 __device__ __forceinline__ int snake(int k) {
@@ -117,13 +178,15 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
-// Producer: per item the fixed pair (fa, fb) at rows f_row of (fh, b), then `n` streamed
-// pairs (sa, sb) from rows_of(t) of heads_of(t).  Shared by both kernels.
+// Producer: per item the fixed pair (fa, fb) at index f_row of rank f_rank of (fh, b), then
+// `n` streamed pairs (sa, sb) at the index and head coords(t) gives, of rank s_rank.
+// Shared by both kernels.
 template <int HD, typename StreamCoords>
 __device__ __forceinline__ bool produce_item(BBars *bars, uint32_t fix0, uint32_t st0, int &slot, uint32_t &ph,
                                              uint32_t &fcnt, uint32_t &issued, uint32_t &last_ph,
-                                             const CUtensorMap *fa, const CUtensorMap *fb, int f_row, int fh,
-                                             const CUtensorMap *sa, const CUtensorMap *sb, int n, int b,
+                                             const CUtensorMap *fa, const CUtensorMap *fb, int f_row, int f_rank,
+                                             int fh, const CUtensorMap *sa, const CUtensorMap *sb, int s_rank,
+                                             int n, int b,
                                              StreamCoords coords, volatile int32_t *abort_flag,
                                              int64_t limit, int *err) {
     using C = BCfg<HD>;
@@ -132,8 +195,8 @@ __device__ __forceinline__ bool produce_item(BBars *bars, uint32_t fix0, uint32_
         const uint32_t bf = smem_u32(&bars->fix_full);
         mbar_expect_tx(bf, 2 * C::TILE_BYTES);
         for (int c = 0; c < C::SLABS; ++c) {
-            tma_load_5d(fix0 + c * C::SLAB_BYTES, fa, bf, c * 64, 0, f_row, fh, b);
-            tma_load_5d(fix0 + C::TILE_BYTES + c * C::SLAB_BYTES, fb, bf, c * 64, 0, f_row, fh, b);
+            tma_load_5d(fix0 + c * C::SLAB_BYTES, fa, bf, c * 64, f_rank, f_row, fh, b);
+            tma_load_5d(fix0 + C::TILE_BYTES + c * C::SLAB_BYTES, fb, bf, c * 64, f_rank, f_row, fh, b);
         }
         ++fcnt;
     }
@@ -145,8 +208,8 @@ __device__ __forceinline__ bool produce_item(BBars *bars, uint32_t fix0, uint32_
         mbar_expect_tx(bf, 2 * C::TILE_BYTES);
         const uint32_t a0 = st0 + (2 * slot) * C::TILE_BYTES;
         for (int c = 0; c < C::SLABS; ++c) {
-            tma_load_5d(a0 + c * C::SLAB_BYTES, sa, bf, c * 64, 0, row, head, b);
-            tma_load_5d(a0 + C::TILE_BYTES + c * C::SLAB_BYTES, sb, bf, c * 64, 0, row, head, b);
+            tma_load_5d(a0 + c * C::SLAB_BYTES, sa, bf, c * 64, s_rank, row, head, b);
+            tma_load_5d(a0 + C::TILE_BYTES + c * C::SLAB_BYTES, sb, bf, c * 64, s_rank, row, head, b);
         }
         issued |= 1u << slot;
         last_ph = (last_ph & ~(1u << slot)) | (ph << slot);
@@ -188,6 +251,41 @@ __device__ __forceinline__ void issue_acc(uint32_t tmem, uint32_t acc_col, uint3
                (accumulate || kk > 0) ? 1u : 0u);
 }
 
+// 32 columns of one gradient row: mul * the step's value, plus the running value of earlier
+// steps unless the range is new this step; bf16 to the gradient on the range's last step,
+// else fp32 to the running buffer.
+__device__ __forceinline__ void store_grad_chunk(__nv_bfloat16 *dst, float *acc, const uint32_t (&o)[32],
+                                                 float mul, int flags) {
+    float x[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) x[e] = mul * __uint_as_float(o[e]);
+    if (!(flags & SEG_FIRST)) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+            const float4 a = __ldcs(reinterpret_cast<const float4 *>(acc + e));
+            x[e] += a.x;
+            x[e + 1] += a.y;
+            x[e + 2] += a.z;
+            x[e + 3] += a.w;
+        }
+    }
+    if (flags & SEG_FINAL) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+            uint4 v4;
+            v4.x = pack_bf16x2(x[e], x[e + 1]);
+            v4.y = pack_bf16x2(x[e + 2], x[e + 3]);
+            v4.z = pack_bf16x2(x[e + 4], x[e + 5]);
+            v4.w = pack_bf16x2(x[e + 6], x[e + 7]);
+            *reinterpret_cast<uint4 *>(dst + e) = v4;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+            __stcs(reinterpret_cast<float4 *>(acc + e), make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]));
+    }
+}
+
 // ---------------------------------------------------------------- dQ kernel
 
 template <int HD>
@@ -206,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if ((int)blockIdx.x >= total) return;
     volatile int32_t *abort_flag = &bars->abort;
-    const int nq = (P.N + kT - 1) / kT;
+    const int tps = (P.flen + kT - 1) / kT;
     const float sl2 = P.scale_log2;
 
     if (threadIdx.x == 0) bwd_init(bars, C::NST);
@@ -228,14 +326,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k * (int)gridDim.x < total && ok; ++k) {
                 const int L = snake(k);
                 if (L >= total) continue;
-                int b, h, hk, qi, n;
-                decode_q(P, nq, L, b, h, hk, qi, n);
-                auto coords = [=](int t, int &row, int &head) {
-                    row = t * kT;
+                QItem it;
+                decode_q(P, tps, L, it);
+                if (it.n == 0) continue;
+                const BSeg &S = P.seg[it.si];
+                const int hk = it.hk;
+                auto coords = [=, &S](int t, int &row, int &head) {
+                    int klim;
+                    q_tile(S, it, t, row, klim);
                     head = hk;
                 };
-                ok = produce_item<HD>(bars, sQ, sSt, slot, ph, fcnt, issued, last_ph, &tm_q, &tm_do, qi * kT, h,
-                                      &tm_k, &tm_v, n, b, coords, abort_flag, limit, err);
+                ok = produce_item<HD>(bars, sQ, sSt, slot, ph, fcnt, issued, last_ph, &tm_q, &tm_do, it.r_lo,
+                                      S.f_rank, it.h, &tm_k, &tm_v, S.s_rank, it.n, it.b, coords, abort_flag,
+                                      limit, err);
             }
             if (!ok) {
                 if (fcnt) wait_phase_drain(smem_u32(&bars->fix_full), (fcnt - 1u) & 1u);
@@ -251,8 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k * (int)gridDim.x < total && ok; ++k) {
                 const int L = snake(k);
                 if (L >= total) continue;
-                int b, h, hk, qi, n;
-                decode_q(P, nq, L, b, h, hk, qi, n);
+                QItem it;
+                decode_q(P, tps, L, it);
+                const int n = it.n;
+                if (n == 0) continue;
                 ok = wait_phase(smem_u32(&bars->fix_full), fcnt & 1u, abort_flag, limit, err);
                 ++fcnt;
                 if (!ok) break;
@@ -311,21 +416,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k * (int)gridDim.x < total && ok; ++k) {
             const int L = snake(k);
             if (L >= total) continue;
-            int b, h, hk, qi, n;
-            decode_q(P, nq, L, b, h, hk, qi, n);
-            const int row = qi * kT + quarter * 32 + lane;
-            const bool valid = row < P.N;
-            const int64_t lrow = ((int64_t)b * P.Hq + h) * P.N + row;
+            QItem it;
+            decode_q(P, tps, L, it);
+            const BSeg &S = P.seg[it.si];
+            const int n = it.n, diag = S.diag;
+            const int row = it.r_lo + quarter * 32 + lane;  // index in the fixed range
+            const bool valid = row < it.r_hi;
+            const int64_t pos = (int64_t)row * P.rs + S.f_rank;
+            const int64_t lrow = ((int64_t)it.b * P.Hq + it.h) * P.N + pos;
             const float lse_l2 = valid ? P.lse[lrow] * kLog2e : 0.f;
             const float d_r = valid ? P.dvec[lrow] : 0.f;
+            float *accp = P.acc_q + lrow * HD;
+            if (valid && !(S.flags & SEG_FIRST))
+                for (int i = 0; i < HD * 4; i += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(
+                                                          reinterpret_cast<const char *>(accp) + i));
             for (int t = 0; t < n && ok; ++t) {
+                int kt0, klim;
+                q_tile(S, it, t, kt0, klim);
                 for (int u = 0; u < 2; ++u) {
                     ok = wait_phase(smem_u32(&bars->s_full[u]), sc[u] & 1u, abort_flag, limit, err);
                     ++sc[u];
                     if (!ok) break;
                     tc_fence_after();
-                    const int k0 = t * kT + u * kSub;  // first key of this half
-                    const bool mask = (k0 + kSub > P.N) || (P.causal && k0 + kSub - 1 > qi * kT) || !valid;
+                    const int k0 = kt0 + u * kSub;  // first key of this half
+                    const bool mask = (k0 + kSub > klim) || (P.causal && k0 + kSub - 1 + diag > row) || !valid;
                     uint32_t pk[2][16];
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
@@ -339,8 +453,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             float p1 = ex2(fmaf(__uint_as_float(s[e + 1]), sl2, -lse_l2));
                             if (mask) {
                                 const int key = k0 + c * 32 + e;
-                                p0 = (valid && key < P.N && (!P.causal || key <= row)) ? p0 : 0.f;
-                                p1 = (valid && key + 1 < P.N && (!P.causal || key + 1 <= row)) ? p1 : 0.f;
+                                p0 = (valid && key < klim && (!P.causal || key + diag <= row)) ? p0 : 0.f;
+                                p1 = (valid && key + 1 < klim && (!P.causal || key + 1 + diag <= row)) ? p1 : 0.f;
                             }
                             pk[c][e / 2] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - d_r),
                                                        p1 * (__uint_as_float(dp[e + 1]) - d_r));
@@ -356,26 +470,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!ok) break;
-            ok = wait_phase(smem_u32(&bars->o_full), ocnt & 1u, abort_flag, limit, err);
-            ++ocnt;
-            if (!ok) break;
-            tc_fence_after();
-            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(P.dq) + (int64_t)b * P.sdq[0] +
-                                  (int64_t)h * P.sdq[1] + (int64_t)row * P.sdq[2];
+            if (n > 0) {
+                ok = wait_phase(smem_u32(&bars->o_full), ocnt & 1u, abort_flag, limit, err);
+                ++ocnt;
+                if (!ok) break;
+                tc_fence_after();
+            }
+            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(P.dq) + (int64_t)it.b * P.sdq[0] +
+                                  (int64_t)it.h * P.sdq[1] + pos * P.sdq[2];
             for (int c = 0; c < HD / 32; ++c) {
                 uint32_t o[32];
-                tmem_ld32(tmem + C::TM_A0 + lane_off + c * 32, o);
-                tmem_ld_wait();
-                if (!valid) continue;
+                if (n > 0) {
+                    tmem_ld32(tmem + C::TM_A0 + lane_off + c * 32, o);
+                    tmem_ld_wait();
+                } else {
 #pragma unroll
-                for (int e = 0; e < 32; e += 8) {
-                    uint4 v4;
-                    v4.x = pack_bf16x2(P.scale * __uint_as_float(o[e]), P.scale * __uint_as_float(o[e + 1]));
-                    v4.y = pack_bf16x2(P.scale * __uint_as_float(o[e + 2]), P.scale * __uint_as_float(o[e + 3]));
-                    v4.z = pack_bf16x2(P.scale * __uint_as_float(o[e + 4]), P.scale * __uint_as_float(o[e + 5]));
-                    v4.w = pack_bf16x2(P.scale * __uint_as_float(o[e + 6]), P.scale * __uint_as_float(o[e + 7]));
-                    *reinterpret_cast<uint4 *>(orow + c * 32 + e) = v4;
+                    for (int e = 0; e < 32; ++e) o[e] = 0u;
                 }
+                if (!valid) continue;
+                store_grad_chunk(orow + c * 32, accp + c * 32, o, P.scale, S.flags);
             }
         }
     }
@@ -406,7 +519,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if ((int)blockIdx.x >= total) return;
     volatile int32_t *abort_flag = &bars->abort;
     const int G = P.Hq / P.Hkv;
-    const int nq = (P.N + kT - 1) / kT;
     const float sl2 = P.scale_log2;
 
     if (threadIdx.x == 0) bwd_init(bars, C::NST);
@@ -428,16 +540,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k * (int)gridDim.x < total && ok; ++k) {
                 const int L = snake(k);
                 if (L >= total) continue;
-                int b, hk, kj, q_first, n;
-                decode_kv(P, nq, L, b, hk, kj, q_first, n);
-                const int per = nq - q_first;
-                auto coords = [=](int t, int &row, int &head) {
-                    const int g = t / per;
-                    row = (q_first + (t - g * per)) * kT;
+                KItem it;
+                decode_kv(P, L, it);
+                if (it.n == 0) continue;
+                const BSeg &S = P.seg[it.si];
+                const int hk = it.hk;
+                auto coords = [=, &S](int t, int &row, int &head) {
+                    int qlim, g;
+                    kv_tile(S, it, G, t, row, qlim, g);
                     head = hk * G + g;
                 };
-                ok = produce_item<HD>(bars, sK, sSt, slot, ph, fcnt, issued, last_ph, &tm_k, &tm_v, kj * kT, hk,
-                                      &tm_q, &tm_do, n, b, coords, abort_flag, limit, err);
+                ok = produce_item<HD>(bars, sK, sSt, slot, ph, fcnt, issued, last_ph, &tm_k, &tm_v, it.c_lo,
+                                      S.f_rank, hk, &tm_q, &tm_do, S.s_rank, it.n, it.b, coords, abort_flag,
+                                      limit, err);
             }
             if (!ok) {
                 if (fcnt) wait_phase_drain(smem_u32(&bars->fix_full), (fcnt - 1u) & 1u);
@@ -453,8 +568,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k * (int)gridDim.x < total && ok; ++k) {
                 const int L = snake(k);
                 if (L >= total) continue;
-                int b, hk, kj, q_first, n;
-                decode_kv(P, nq, L, b, hk, kj, q_first, n);
+                KItem it;
+                decode_kv(P, L, it);
+                const int n = it.n;
+                if (n == 0) continue;
                 ok = wait_phase(smem_u32(&bars->fix_full), fcnt & 1u, abort_flag, limit, err);
                 ++fcnt;
                 if (!ok) break;
@@ -516,21 +633,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k * (int)gridDim.x < total && ok; ++k) {
             const int L = snake(k);
             if (L >= total) continue;
-            int b, hk, kj, q_first, n;
-            decode_kv(P, nq, L, b, hk, kj, q_first, n);
-            const int key = kj * kT + quarter * 32 + lane;
-            const int per = nq - q_first;
+            KItem it;
+            decode_kv(P, L, it);
+            const BSeg &S = P.seg[it.si];
+            const int n = it.n, diag = S.diag;
+            const int key = it.c_lo + quarter * 32 + lane;  // index in the fixed range
+            const bool kvalid = key < it.c_hi;
+            const int64_t kpos = (int64_t)key * P.rs + S.f_rank;
+            const int64_t arow = (((int64_t)it.b * P.Hkv + it.hk) * P.N + kpos) * HD;
+            if (kvalid && !(S.flags & SEG_FIRST))
+                for (int i = 0; i < HD * 4; i += 128) {
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(P.acc_k + arow) + i));
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(P.acc_v + arow) + i));
+                }
             for (int t = 0; t < n && ok; ++t) {
-                const int g = t / per;
-                const int q0 = (q_first + (t - g * per)) * kT;
-                const int h = hk * G + g;
+                int q0, qlim, g;
+                kv_tile(S, it, G, t, q0, qlim, g);
+                const int h = it.hk * G + g;
                 __syncwarp();  // every lane is done with the previous tile's values
 #pragma unroll
                 for (int r = 0; r < kT / 32; ++r) {
                     const int qme = q0 + r * 32 + lane;
-                    const int64_t li = ((int64_t)b * P.Hq + h) * P.N + qme;
-                    lb[r * 32 + lane] = qme < P.N ? P.lse[li] * kLog2e : 0.f;
-                    db[r * 32 + lane] = qme < P.N ? P.dvec[li] : 0.f;
+                    const int64_t li = ((int64_t)it.b * P.Hq + h) * P.N + (int64_t)qme * P.rs + S.s_rank;
+                    lb[r * 32 + lane] = qme < qlim ? P.lse[li] * kLog2e : 0.f;
+                    db[r * 32 + lane] = qme < qlim ? P.dvec[li] : 0.f;
                 }
                 __syncwarp();
                 for (int u = 0; u < 2; ++u) {
@@ -539,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     tc_fence_after();
                     const int qa = q0 + u * kSub;  // first query of this half
-                    const bool mask = (qa + kSub > P.N) || (P.causal && kj * kT + kT - 1 > qa);
+                    const bool mask = (qa + kSub > qlim) || (P.causal && it.c_hi - 1 + diag > qa);
                     uint32_t pp[2][16], pd[2][16];
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
@@ -554,8 +680,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             float p1 = ex2(fmaf(__uint_as_float(s[e + 1]), sl2, -lb[qo + 1]));
                             if (mask) {
                                 const int qq = q0 + qo;
-                                p0 = (qq < P.N && (!P.causal || key <= qq)) ? p0 : 0.f;
-                                p1 = (qq + 1 < P.N && (!P.causal || key <= qq + 1)) ? p1 : 0.f;
+                                p0 = (qq < qlim && (!P.causal || key + diag <= qq)) ? p0 : 0.f;
+                                p1 = (qq + 1 < qlim && (!P.causal || key + diag <= qq + 1)) ? p1 : 0.f;
                             }
                             pp[c][e / 2] = pack_bf16x2(p0, p1);
                             pd[c][e / 2] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - db[qo]),
@@ -573,33 +699,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!ok) break;
-            ok = wait_phase(smem_u32(&bars->o_full), ocnt & 1u, abort_flag, limit, err);
-            ++ocnt;
-            if (!ok) break;
-            tc_fence_after();
-            const bool valid = key < P.N;
-            __nv_bfloat16 *vrow = static_cast<__nv_bfloat16 *>(P.dv) + (int64_t)b * P.sdv[0] +
-                                  (int64_t)hk * P.sdv[1] + (int64_t)key * P.sdv[2];
-            __nv_bfloat16 *krow = static_cast<__nv_bfloat16 *>(P.dk) + (int64_t)b * P.sdk[0] +
-                                  (int64_t)hk * P.sdk[1] + (int64_t)key * P.sdk[2];
+            if (n > 0) {
+                ok = wait_phase(smem_u32(&bars->o_full), ocnt & 1u, abort_flag, limit, err);
+                ++ocnt;
+                if (!ok) break;
+                tc_fence_after();
+            }
+            __nv_bfloat16 *vrow = static_cast<__nv_bfloat16 *>(P.dv) + (int64_t)it.b * P.sdv[0] +
+                                  (int64_t)it.hk * P.sdv[1] + kpos * P.sdv[2];
+            __nv_bfloat16 *krow = static_cast<__nv_bfloat16 *>(P.dk) + (int64_t)it.b * P.sdk[0] +
+                                  (int64_t)it.hk * P.sdk[1] + kpos * P.sdk[2];
             for (int which = 0; which < 2; ++which) {
                 const float mul = which ? P.scale : 1.f;
                 __nv_bfloat16 *dst = which ? krow : vrow;
+                float *acc = (which ? P.acc_k : P.acc_v) + arow;
                 const uint32_t col = which ? C::TM_A1 : C::TM_A0;
                 for (int c = 0; c < HD / 32; ++c) {
                     uint32_t o[32];
-                    tmem_ld32(tmem + col + lane_off + c * 32, o);
-                    tmem_ld_wait();
-                    if (!valid) continue;
+                    if (n > 0) {
+                        tmem_ld32(tmem + col + lane_off + c * 32, o);
+                        tmem_ld_wait();
+                    } else {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        uint4 v4;
-                        v4.x = pack_bf16x2(mul * __uint_as_float(o[e]), mul * __uint_as_float(o[e + 1]));
-                        v4.y = pack_bf16x2(mul * __uint_as_float(o[e + 2]), mul * __uint_as_float(o[e + 3]));
-                        v4.z = pack_bf16x2(mul * __uint_as_float(o[e + 4]), mul * __uint_as_float(o[e + 5]));
-                        v4.w = pack_bf16x2(mul * __uint_as_float(o[e + 6]), mul * __uint_as_float(o[e + 7]));
-                        *reinterpret_cast<uint4 *>(dst + c * 32 + e) = v4;
+                        for (int e = 0; e < 32; ++e) o[e] = 0u;
                     }
+                    if (!kvalid) continue;
+                    store_grad_chunk(dst + c * 32, acc + c * 32, o, mul, S.flags);
                 }
             }
         }
@@ -613,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace tcb
 
 template <int HD>
-static cudaError_t launch_bwd_tc_hd(const BwdParams &P, int num_sms, int64_t wait_ns, int *err,
+static cudaError_t launch_bwd_tc_hd(const BwdParams &P, int parts, int num_sms, int64_t wait_ns, int *err,
                                     cudaStream_t stream) {
     using C = tcb::BCfg<HD>;
     static int configured_mask = 0;
@@ -629,28 +754,33 @@ static cudaError_t launch_bwd_tc_hd(const BwdParams &P, int num_sms, int64_t wai
         configured_mask |= 1 << (dev & 31);
     }
     CUtensorMap mq, mk, mv, mdo;
-    if (!encode_map(&mq, P.q, P.B, P.Hq, P.N, P.D, P.sq, 1) ||
-        !encode_map(&mk, P.k, P.B, P.Hkv, P.N, P.D, P.sk, 1) ||
-        !encode_map(&mv, P.v, P.B, P.Hkv, P.N, P.D, P.sv, 1) ||
-        !encode_map(&mdo, P.dout, P.B, P.Hq, P.N, P.D, P.sdo, 1))
+    if (!encode_map(&mq, P.q, P.B, P.Hq, P.N, P.D, P.sq, P.rs) ||
+        !encode_map(&mk, P.k, P.B, P.Hkv, P.N, P.D, P.sk, P.rs) ||
+        !encode_map(&mv, P.v, P.B, P.Hkv, P.N, P.D, P.sv, P.rs) ||
+        !encode_map(&mdo, P.dout, P.B, P.Hq, P.N, P.D, P.sdo, P.rs))
         return cudaErrorInvalidValue;
-    const int nt = (P.N + tcb::kT - 1) / tcb::kT;
-    const int64_t tq = (int64_t)P.B * P.Hq * nt, tkv = (int64_t)P.B * P.Hkv * nt;
+    const int nt = (P.flen + tcb::kT - 1) / tcb::kT;
+    const int64_t tq = (int64_t)P.B * P.Hq * P.nseg * nt, tkv = (int64_t)P.B * P.Hkv * P.nseg * nt;
     if (tq > 0x7fffffff || tkv > 0x7fffffff) return cudaErrorInvalidValue;
-    tcb::bwd_dq_tc_kernel<HD><<<(int)std::min<int64_t>(tq, num_sms), tcb::kThreads, C::SMEM_BYTES, stream>>>(
-        mq, mk, mv, mdo, P, (int)tq, wait_ns, err);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    tcb::bwd_dkdv_tc_kernel<HD><<<(int)std::min<int64_t>(tkv, num_sms), tcb::kThreads, C::SMEM_BYTES, stream>>>(
-        mq, mk, mv, mdo, P, (int)tkv, wait_ns, err);
+    if (parts & 1) {
+        tcb::bwd_dq_tc_kernel<HD><<<(int)std::min<int64_t>(tq, num_sms), tcb::kThreads, C::SMEM_BYTES, stream>>>(
+            mq, mk, mv, mdo, P, (int)tq, wait_ns, err);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (parts & 2)
+        tcb::bwd_dkdv_tc_kernel<HD><<<(int)std::min<int64_t>(tkv, num_sms), tcb::kThreads, C::SMEM_BYTES,
+                                      stream>>>(mq, mk, mv, mdo, P, (int)tkv, wait_ns, err);
     return cudaGetLastError();
 }
 
-cudaError_t launch_attn_bwd_tc(const BwdParams &P, int num_sms, int64_t wait_ns, int *err,
+// The dQ kernel (parts & 1) and the dK/dV kernel (parts & 2) over the segments in P (the
+// D vector is computed before).
+cudaError_t launch_attn_bwd_tc(const BwdParams &P, int parts, int num_sms, int64_t wait_ns, int *err,
                                cudaStream_t stream) {
-    if (P.B <= 0 || P.Hq <= 0 || P.N <= 0) return cudaSuccess;
-    if (P.D == 128) return launch_bwd_tc_hd<128>(P, num_sms, wait_ns, err, stream);
-    if (P.D == 64) return launch_bwd_tc_hd<64>(P, num_sms, wait_ns, err, stream);
+    if (P.B <= 0 || P.Hq <= 0 || P.nseg <= 0 || P.flen <= 0) return cudaSuccess;
+    if (P.D == 128) return launch_bwd_tc_hd<128>(P, parts, num_sms, wait_ns, err, stream);
+    if (P.D == 64) return launch_bwd_tc_hd<64>(P, parts, num_sms, wait_ns, err, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -17,10 +17,10 @@ int attn_tc_rows_per_block();
 cudaError_t launch_wait_selftest(int64_t limit_ns, int *err, cudaStream_t stream);
 
 cudaError_t launch_lse_merge(const MergeParams &P, int num_sms, cudaStream_t stream);
-cudaError_t launch_attn_bwd_simt(const BwdParams &P, int num_sms, cudaStream_t stream);
+cudaError_t launch_attn_bwd_simt(const BwdParams &P, int parts, cudaStream_t stream);
 cudaError_t launch_bwd_rowdot(const BwdParams &P, int num_sms, cudaStream_t stream);
 cudaError_t launch_ulysses(const UlyssesParams &P, int num_sms, cudaStream_t stream);
-cudaError_t launch_attn_bwd_tc(const BwdParams &P, int num_sms, int64_t wait_ns, int *err,
+cudaError_t launch_attn_bwd_tc(const BwdParams &P, int parts, int num_sms, int64_t wait_ns, int *err,
                                cudaStream_t stream);
 cudaError_t launch_fill_identity(void *o, int o_bf16, const int64_t *so, float *lse, int B, int H,
                                  int N, int D, int r0, int r1, int num_sms, cudaStream_t stream);
@@ -265,6 +265,131 @@ static ra_status check_ring(int64_t N, int R, int layout) {
     return RA_OK;
 }
 
+// ---------------------------------------------------------------- ring backward schedule
+
+// One block of a backward ring step: rank r's query chunk qr against chunk kr of the rank
+// j = (r - step) mod R whose keys and values r holds at that step.
+struct BPair {
+    int r, j;
+    Range qr, kr;
+    int diag;
+};
+
+// The blocks of one step with at least one visible (row, key) pair: the same visibility
+// as the forward's step (causal on global positions; the striped interleave's offset).
+static void bwd_pairs(int64_t N, int R, int layout, int causal, int step, std::vector<BPair> &out) {
+    out.clear();
+    for (int r = 0; r < R; ++r) {
+        const int j = ((r - step) % R + R) % R;
+        if (layout == RA_LAYOUT_STRIPED) {
+            const int64_t c = N / R;
+            const int diag = (causal && j > r) ? 1 : 0;
+            if (c == 0 || (causal && diag > c - 1)) continue;
+            out.push_back({r, j, {0, c}, {0, c}, diag});
+            continue;
+        }
+        for (const Range &qr : rank_ranges(N, R, layout, r))
+            for (const Range &kr : rank_ranges(N, R, layout, j)) {
+                if (qr.b <= qr.a || kr.b <= kr.a) continue;
+                if (causal && kr.a > qr.b - 1) continue;  // every key after every row
+                out.push_back({r, j, qr, kr, 0});
+            }
+    }
+}
+
+// A step's blocks grouped by fixed range: by query chunk for the dQ kernels (the chunk
+// stays on its rank), by key chunk for the dK/dV kernels (the chunk's gradients go back
+// to its rank).  `owner` receives the rank that owns each segment's fixed range.
+static void bwd_group(const std::vector<BPair> &pairs, bool dq, bool striped, std::vector<BSeg> &segs,
+                      std::vector<int> &owner) {
+    segs.clear();
+    owner.clear();
+    for (const BPair &p : pairs) {
+        const int frank = dq ? p.r : p.j, srank = dq ? p.j : p.r;
+        const Range &f = dq ? p.qr : p.kr;
+        const Range &sr = dq ? p.kr : p.qr;
+        size_t i = 0;
+        while (i < segs.size() && !(owner[i] == frank && segs[i].f0 == f.a)) ++i;
+        if (i == segs.size()) {
+            BSeg g;
+            memset(&g, 0, sizeof g);
+            g.f0 = (int32_t)f.a;
+            g.f1 = (int32_t)f.b;
+            g.s0[0] = (int32_t)sr.a;
+            g.s1[0] = (int32_t)sr.b;
+            g.s0[1] = g.s1[1] = (int32_t)sr.b;
+            g.f_rank = striped ? frank : 0;
+            g.s_rank = striped ? srank : 0;
+            g.diag = p.diag;
+            segs.push_back(g);
+            owner.push_back(frank);
+        } else {  // a second chunk of the partner rank (zigzag): ranges kept in order
+            BSeg &g = segs[i];
+            if (sr.a < g.s0[0]) {
+                g.s0[1] = g.s0[0];
+                g.s1[1] = g.s1[0];
+                g.s0[0] = (int32_t)sr.a;
+                g.s1[0] = (int32_t)sr.b;
+            } else {
+                g.s0[1] = (int32_t)sr.a;
+                g.s1[1] = (int32_t)sr.b;
+            }
+        }
+    }
+}
+
+static int64_t bseg_work(const BSeg &g) {
+    return (int64_t)(g.s1[0] - g.s0[0]) + (g.s1[1] - g.s0[1]);
+}
+
+// The first and last step that writes each fixed range, per kind (0: dQ, 1: dK/dV),
+// indexed by owner rank * 2 + chunk slot; then one step's segments with their flags,
+// heaviest first.
+struct BwdPlan {
+    int64_t N;
+    int R, layout, causal;
+    std::vector<int> first[2], last[2];
+
+    int slot(int own, int32_t f0) const {
+        if (layout != RA_LAYOUT_ZIGZAG) return own * 2;
+        return own * 2 + ((int64_t)f0 < (int64_t)(own + 1) * (N / (2 * (int64_t)R)) ? 0 : 1);
+    }
+
+    BwdPlan(int64_t n, int r, int lay, int c) : N(n), R(r), layout(lay), causal(c) {
+        std::vector<BPair> pairs;
+        std::vector<BSeg> segs;
+        std::vector<int> owner;
+        for (int kind = 0; kind < 2; ++kind) {
+            first[kind].assign(2 * (size_t)R, -1);
+            last[kind].assign(2 * (size_t)R, -1);
+        }
+        for (int step = 0; step < R; ++step) {
+            bwd_pairs(N, R, layout, causal, step, pairs);
+            for (int kind = 0; kind < 2; ++kind) {
+                bwd_group(pairs, kind == 0, layout == RA_LAYOUT_STRIPED, segs, owner);
+                for (size_t i = 0; i < segs.size(); ++i) {
+                    const int sl = slot(owner[i], segs[i].f0);
+                    if (first[kind][sl] < 0) first[kind][sl] = step;
+                    last[kind][sl] = step;
+                }
+            }
+        }
+    }
+
+    void step(int st, int kind, std::vector<BSeg> &segs) const {
+        std::vector<BPair> pairs;
+        std::vector<int> owner;
+        bwd_pairs(N, R, layout, causal, st, pairs);
+        bwd_group(pairs, kind == 0, layout == RA_LAYOUT_STRIPED, segs, owner);
+        for (size_t i = 0; i < segs.size(); ++i) {
+            const int sl = slot(owner[i], segs[i].f0);
+            segs[i].flags = (first[kind][sl] == st ? SEG_FIRST : 0) | (last[kind][sl] == st ? SEG_FINAL : 0);
+        }
+        std::stable_sort(segs.begin(), segs.end(),
+                         [](const BSeg &x, const BSeg &y) { return bseg_work(x) > bseg_work(y); });
+    }
+};
+
 // ---------------------------------------------------------------- dispatch
 
 static void fill_common(StepParams &P, const ra_tensor *q, const ra_tensor *k, const ra_tensor *v,
@@ -403,6 +528,21 @@ int64_t ra_ring_sim_plan(int64_t N, int ring_size, ra_layout layout, int causal,
     return (int64_t)segs.size();
 }
 
+int64_t ra_ring_sim_bwd_plan(int64_t N, int ring_size, ra_layout layout, int causal, int step, int kind,
+                             int64_t *out, int64_t cap) {
+    if (N < 0 || N > ((int64_t)1 << 30) || step < 0 || step >= ring_size || kind < 0 || kind > 1) return -1;
+    if (check_ring(N, ring_size, layout) != RA_OK) return -1;
+    const BwdPlan plan(N, ring_size, layout, causal);
+    std::vector<BSeg> segs;
+    plan.step(step, kind, segs);
+    for (size_t i = 0; i < segs.size() && (int64_t)i < cap && out; ++i) {
+        const BSeg &g = segs[i];
+        const int64_t v[10] = {g.f0, g.f1, g.s0[0], g.s1[0], g.s0[1], g.s1[1], g.f_rank, g.s_rank, g.diag, g.flags};
+        for (int t = 0; t < 10; ++t) out[i * 10 + t] = v[t];
+    }
+    return (int64_t)segs.size();
+}
+
 ra_status ra_attn_varlen_fwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v,
                              ra_tensor *o, float *lse, const int32_t *cu_seqlens, int num_seqs,
                              int causal, float scale, void *stream) {
@@ -503,9 +643,22 @@ size_t ra_attn_bwd_workspace_bytes(const ra_tensor *q) {
     return (size_t)(q->shape[0] * q->shape[1] * q->shape[2]) * sizeof(float);
 }
 
-ra_status ra_attn_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v, const ra_tensor *o,
-                      const float *lse, const ra_tensor *dout, ra_tensor *dq, ra_tensor *dk,
-                      ra_tensor *dv, int causal, float scale, void *workspace, void *stream) {
+size_t ra_ring_sim_bwd_workspace_bytes(const ra_tensor *q, const ra_tensor *k, int ring_size) {
+    if (!q || !k || ring_size < 1) return 0;
+    for (int i = 0; i < 4; ++i)
+        if (q->shape[i] < 0 || k->shape[i] < 0) return 0;
+    const size_t rows = (size_t)(q->shape[0] * q->shape[1] * q->shape[2]);
+    if (ring_size == 1) return rows * sizeof(float);
+    const size_t dv_bytes = (rows * sizeof(float) + 255) & ~(size_t)255;
+    const size_t nq = rows * (size_t)q->shape[3];
+    const size_t nk = (size_t)(k->shape[0] * k->shape[1] * k->shape[2] * k->shape[3]);
+    return dv_bytes + (nq + 2 * nk) * sizeof(float);
+}
+
+ra_status ra_ring_sim_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v, const ra_tensor *o,
+                          const float *lse, const ra_tensor *dout, ra_tensor *dq, ra_tensor *dk, ra_tensor *dv,
+                          int ring_size, ra_layout layout, int causal, float scale, void *workspace,
+                          void *stream) {
     Problem pb;
     ra_status s = check_qkvo(q, k, v, o, lse, pb);
     if (s) return s;
@@ -522,6 +675,7 @@ ra_status ra_attn_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v
         dv->dtype != pb.dtype)
         return fail(RA_ERR_INVALID_ARG, "gradients must share q's dtype");
     if (isnan(scale)) return fail(RA_ERR_INVALID_ARG, "scale is NaN");
+    if ((s = check_ring(pb.N, ring_size, layout))) return s;
     if (pb.B * pb.Hq * pb.N == 0) return RA_OK;
     if (!workspace) return fail(RA_ERR_INVALID_ARG, "workspace is NULL");
     if (reinterpret_cast<uintptr_t>(workspace) % 16)
@@ -529,7 +683,8 @@ ra_status ra_attn_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v
     DevInfo di;
     std::string msg;
     if (!device_info(di, msg)) return fail(RA_ERR_CUDA, msg);
-    BwdParams P;
+    BwdParams *Pp = new BwdParams;
+    BwdParams &P = *Pp;
     memset(&P, 0, sizeof P);
     P.q = q->data;
     P.k = k->data;
@@ -551,6 +706,13 @@ ra_status ra_attn_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v
     }
     P.lse = lse;
     P.dvec = static_cast<float *>(workspace);
+    if (ring_size > 1) {
+        const size_t rows = (size_t)(pb.B * pb.Hq * pb.N);
+        char *w = static_cast<char *>(workspace) + ((rows * sizeof(float) + 255) & ~(size_t)255);
+        P.acc_q = reinterpret_cast<float *>(w);
+        P.acc_k = P.acc_q + rows * pb.D;
+        P.acc_v = P.acc_k + (size_t)(pb.B * pb.Hkv * pb.N * pb.D);
+    }
     P.B = (int32_t)pb.B;
     P.Hq = (int32_t)pb.Hq;
     P.Hkv = (int32_t)pb.Hkv;
@@ -560,20 +722,46 @@ ra_status ra_attn_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v
     P.causal = causal ? 1 : 0;
     P.scale = scale > 0.f ? scale : (float)(1.0 / sqrt((double)pb.D));
     P.scale_log2 = P.scale * kLog2e;
+    const bool striped = layout == RA_LAYOUT_STRIPED;
+    P.rs = striped ? ring_size : 1;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool tc = di.tc_ok && pb.dtype == RA_BF16 && (pb.D == 64 || pb.D == 128) && aligned16(q) &&
                     aligned16(k) && aligned16(v) && aligned16(dout) && aligned16(dq) &&
                     aligned16(dk) && aligned16(dv);
-    cudaError_t e;
-    if (tc) {
-        e = launch_bwd_rowdot(P, di.sms, st);
-        if (e == cudaSuccess) e = launch_attn_bwd_tc(P, di.sms, g_wait_limit_ns, di.err, st);
-    } else {
-        e = launch_attn_bwd_simt(P, di.sms, st);
+    ra_status result = RA_OK;
+    cudaError_t e = launch_bwd_rowdot(P, di.sms, st);
+    if (e != cudaSuccess) result = cuda_fail(e, "backward D launch");
+    else ++t_launches;
+    const BwdPlan plan(pb.N, ring_size, layout, causal);
+    std::vector<BSeg> segs;
+    for (int step = 0; step < ring_size && result == RA_OK; ++step) {
+        for (int kind = 0; kind < 2 && result == RA_OK; ++kind) {
+            plan.step(step, kind, segs);
+            for (size_t f = 0; f < segs.size() && result == RA_OK; f += kMaxBSeg) {
+                const size_t n = std::min(segs.size() - f, (size_t)kMaxBSeg);
+                P.nseg = (int32_t)n;
+                P.flen = 0;
+                for (size_t i = 0; i < n; ++i) {
+                    P.seg[i] = segs[f + i];
+                    P.flen = std::max<int32_t>(P.flen, segs[f + i].f1 - segs[f + i].f0);
+                }
+                const int parts = kind == 0 ? 1 : 2;
+                e = tc ? launch_attn_bwd_tc(P, parts, di.sms, g_wait_limit_ns, di.err, st)
+                       : launch_attn_bwd_simt(P, parts, st);
+                if (e != cudaSuccess) result = cuda_fail(e, "backward launch");
+                else ++t_launches;
+            }
+        }
     }
-    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
-    t_launches += 3;
-    return RA_OK;
+    delete Pp;
+    return result;
+}
+
+ra_status ra_attn_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v, const ra_tensor *o,
+                      const float *lse, const ra_tensor *dout, ra_tensor *dq, ra_tensor *dk,
+                      ra_tensor *dv, int causal, float scale, void *workspace, void *stream) {
+    return ra_ring_sim_bwd(q, k, v, o, lse, dout, dq, dk, dv, 1, RA_LAYOUT_CONTIG, causal, scale, workspace,
+                           stream);
 }
 
 ra_status ra_ulysses_all_to_all(const ra_tensor *in, ra_tensor *out, int sp, int to_heads,

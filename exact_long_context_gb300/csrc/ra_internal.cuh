@@ -71,16 +71,37 @@ struct MergeParams {
 };
 
 // Gradients of attention (see attn_bwd_simt.cu).
+// One unit of backward work in a ring step: a fixed range (query rows for the dQ kernels,
+// keys for the dK/dV kernels) of one rank against up to two streamed ranges of the
+// partner rank, in the layout's index space (absolute positions for the contiguous and
+// zigzag layouts; indices within a rank's interleave for the striped layout, where the
+// position of index i of rank r is i * rs + r).  Under causality key c is visible to
+// row i iff c + diag <= i.
+struct BSeg {
+    int32_t f0, f1;
+    int32_t s0[2], s1[2];  // s0[1] == s1[1] when the second range is unused
+    int32_t f_rank, s_rank;
+    int32_t diag;
+    int32_t flags;  // SEG_FIRST: no earlier step wrote the fixed range; SEG_FINAL: no later step will
+};
+constexpr int kMaxBSeg = 128;
+
 struct BwdParams {
     const void *q, *k, *v, *o, *dout;
     void *dq, *dk, *dv;
     int64_t sq[3], sk[3], sv[3], so[3], sdo[3], sdq[3], sdk[3], sdv[3];
     const float *lse;  // [B, Hq, N]
     float *dvec;       // [B, Hq, N] rowsum(dO * O)
+    float *acc_q;      // [B, Hq, N, D] fp32 running dQ between ring steps (final units)
+    float *acc_k, *acc_v;  // [B, Hkv, N, D] fp32 running dK, dV
     int32_t B, Hq, Hkv, N, D;
     int32_t bf16;
     int32_t causal;
     float scale, scale_log2;
+    int32_t rs;    // rank interleave of the striped layout (1 otherwise)
+    int32_t flen;  // length of every segment's fixed range
+    int32_t nseg;
+    BSeg seg[kMaxBSeg];
 };
 
 // Ulysses all-to-all as a layout transform (see ulysses.cu).

@@ -57,10 +57,16 @@ def lib() -> ctypes.CDLL:
             L.ra_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
             L.ra_attn_bwd.argtypes = [T, T, T, T, P, T, T, T, T, c_int, c_float, P, P]
             L.ra_attn_bwd.restype = c_int
+            L.ra_ring_sim_bwd_workspace_bytes.argtypes = [T, T, c_int]
+            L.ra_ring_sim_bwd_workspace_bytes.restype = ctypes.c_size_t
+            L.ra_ring_sim_bwd.argtypes = [T, T, T, T, P, T, T, T, T, c_int, c_int, c_int, c_float, P, P]
+            L.ra_ring_sim_bwd.restype = c_int
             L.ra_ulysses_all_to_all.argtypes = [T, T, c_int, c_int, P]
             L.ra_ulysses_all_to_all.restype = c_int
             L.ra_ring_sim_plan.argtypes = [i64, c_int, c_int, c_int, c_int, P, i64]
             L.ra_ring_sim_plan.restype = i64
+            L.ra_ring_sim_bwd_plan.argtypes = [i64, c_int, c_int, c_int, c_int, c_int, P, i64]
+            L.ra_ring_sim_bwd_plan.restype = i64
             L.ra_check_device_error.argtypes = [P]
             L.ra_debug_set_wait_limit_ns.argtypes = [i64]
             L.ra_debug_set_wait_limit_ns.restype = None
@@ -166,6 +172,48 @@ def attn_bwd(q, k, v, o, lse, dout, causal=False, scale=None, dq=None, dk=None, 
                              int(bool(causal)), float(scale or 0.0), _ptr(workspace),
                              _stream(stream)))
     return dq, dk, dv
+
+
+def ring_sim_bwd_workspace_bytes(q, k, ring_size: int) -> int:
+    """Bytes of device workspace ring_sim_bwd needs."""
+    dqd, dkd = _desc(q, "q"), _desc(k, "k")
+    return int(lib().ra_ring_sim_bwd_workspace_bytes(ctypes.byref(dqd), ctypes.byref(dkd), int(ring_size)))
+
+
+def ring_sim_bwd(q, k, v, o, lse, dout, ring_size: int, layout: str = "zigzag", causal=True, scale=None,
+                 dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of ring_sim_fwd on the ring schedule, for the loss sum(dout * o)."""
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = ring_sim_bwd_workspace_bytes(q, k, ring_size)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    elif workspace.numel() < need:
+        raise ValueError(f"workspace needs {need} bytes")
+    if lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32")
+    descs = [_desc(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"))]
+    dd = _desc(dout, "dout")
+    gq, gk, gv = _desc(dq, "dq"), _desc(dk, "dk"), _desc(dv, "dv")
+    _check(lib().ra_ring_sim_bwd(*(ctypes.byref(x) for x in descs), _ptr(lse), ctypes.byref(dd),
+                                 ctypes.byref(gq), ctypes.byref(gk), ctypes.byref(gv), int(ring_size),
+                                 LAYOUTS[layout], int(bool(causal)), float(scale or 0.0), _ptr(workspace),
+                                 _stream(stream)))
+    return dq, dk, dv
+
+
+def ring_sim_bwd_plan(N: int, ring_size: int, layout="zigzag", causal=True, step=0, kind=0):
+    """Host-only schedule of one backward step: list of dicts, kind 0 = dQ, 1 = dK/dV."""
+    L = lib()
+    args = (int(N), int(ring_size), LAYOUTS[layout], int(bool(causal)), int(step), int(kind))
+    n = L.ra_ring_sim_bwd_plan(*args, None, 0)
+    if n < 0:
+        raise ValueError("bad ring plan arguments")
+    buf = (ctypes.c_int64 * (10 * max(n, 1)))()
+    L.ra_ring_sim_bwd_plan(*args, buf, n)
+    keys = ("f0", "f1", "s0a", "s1a", "s0b", "s1b", "f_rank", "s_rank", "diag", "flags")
+    return [dict(zip(keys, buf[10 * i:10 * i + 10])) for i in range(n)]
 
 
 def ulysses_all_to_all(x, sp: int, to_heads: bool, out=None, stream=None):

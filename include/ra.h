@@ -181,6 +181,35 @@ ra_status ra_attn_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v
                       ra_tensor *dv, int causal, float scale, void *workspace, void *stream);
 
 /*
+ * ra_ring_sim_bwd - gradients of ra_ring_sim_fwd on the ring schedule of ring_size
+ * simulated ranks, on one GPU.
+ *
+ * The `ring_attention_backward` listing of "Ring Attention 论文解析": at step s rank r
+ * holds the key/value block of rank (r - s) mod R (the forward's rotation), recomputes
+ * P = exp(scale Q K^T - LSE) of its queries against that block with the forward's LSE and
+ * D = rowsum(dout * O), adds dS K to its own dQ, and returns the block's dK = scale dS^T Q
+ * and dV = P^T dout to the block's rank, which sums them over the steps.  Each step
+ * applies the forward's causal rule (skipped, diagonal or full blocks; the striped
+ * interleave's offset).  One launch of the dQ kernel and one of the dK/dV kernel per step
+ * cover every rank; gradients that several steps write are carried between steps in fp32
+ * in the workspace.  The sum over steps is the gradient of the whole sequence, so
+ * ring_size = 1 (any layout) is ra_attn_bwd.
+ *
+ *   q, k, v, o, lse  the forward's inputs and outputs (natural sequence order)
+ *   dout             [B, Hq, N, D] gradient of O (q's dtype)
+ *   dq               [B, Hq, N, D] (written); dk, dv [B, Hkv, N, D] (written)
+ *   ring_size, layout  as ra_ring_sim_fwd (N divisible as it requires)
+ *   workspace        device buffer of ra_ring_sim_bwd_workspace_bytes(q, k, ring_size)
+ *                    bytes, 16-byte aligned, owned by the caller, overwritten
+ * Errors: as ra_attn_bwd, plus the ring-size/layout checks of ra_ring_sim_fwd.
+ */
+size_t ra_ring_sim_bwd_workspace_bytes(const ra_tensor *q, const ra_tensor *k, int ring_size);
+ra_status ra_ring_sim_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v, const ra_tensor *o,
+                          const float *lse, const ra_tensor *dout, ra_tensor *dq, ra_tensor *dk, ra_tensor *dv,
+                          int ring_size, ra_layout layout, int causal, float scale, void *workspace,
+                          void *stream);
+
+/*
  * ra_ulysses_all_to_all - the Ulysses sequence <-> head exchange of sp ranks, restated as a
  * layout transform of one GPU's memory ("序列并行与 Ring Attention：超长上下文训练技术解析",
  * section "1. Ulysses (All-to-All)": scatter the head axis, gather the sequence axis).
@@ -214,6 +243,25 @@ ra_status ra_ulysses_all_to_all(const ra_tensor *in, ra_tensor *out, int sp, int
  */
 int64_t ra_ring_sim_plan(int64_t N, int ring_size, ra_layout layout, int causal, int step,
                          int64_t *segments, int64_t cap);
+
+/*
+ * ra_ring_sim_bwd_plan - host-only description of one step of ra_ring_sim_bwd (no GPU
+ * work).  kind 0: the segments of the dQ kernel (fixed range = a query chunk, streamed
+ * ranges = the key chunks of the block it holds); kind 1: the segments of the dK/dV
+ * kernel (fixed range = a key chunk, streamed ranges = the query chunks of the rank that
+ * holds it at this step).  Each segment is 10 int64 values:
+ *   f0, f1          fixed index range
+ *   s0a, s1a        first streamed index range
+ *   s0b, s1b        second streamed index range (s0b == s1b when absent)
+ *   f_rank, s_rank  striped layout: ranks of the fixed and streamed ranges (0 otherwise;
+ *                   index i of rank r is sequence position i * ring_size + r)
+ *   diag            under causality key c is visible to row i iff c + diag <= i
+ *   flags           bit 0: no earlier step writes the fixed range's gradient,
+ *                   bit 1: no later step does
+ * Returns the number of segments (which may exceed cap), or -1 on bad arguments.
+ */
+int64_t ra_ring_sim_bwd_plan(int64_t N, int ring_size, ra_layout layout, int causal, int step, int kind,
+                             int64_t *out, int64_t cap);
 
 /*
  * ra_ring_sim_fwd_noalloc - ra_ring_sim_fwd for callers that cannot have device memory

@@ -1,0 +1,153 @@
+"""Ring-scheduled gradients through the C ABI (ra_ring_sim_bwd) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+from exact_long_context_gb300 import synth
+from helpers import to_oracle
+from oracle import backward as ob
+
+pytestmark = pytest.mark.gpu
+
+# max-abs error / max(1, max |reference|), as for ra_attn_bwd: float32 arithmetic with fp32
+# inputs; with bf16 inputs/outputs the rounding of O (inside D = rowsum(dO * O)), of P and
+# dS before the tensor-core products and of the stored gradients (2^-9 relative).
+TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
+
+
+@pytest.fixture(scope="module")
+def ra():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from exact_long_context_gb300 import build
+    build.build()
+    from exact_long_context_gb300 import ra as ra_mod
+    return ra_mod
+
+
+def _inputs(B, Hq, Hkv, N, D, dtype, seed):
+    q, k, v = synth.make_qkv(B, Hq, Hkv, N, D, dtype, seed=seed, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(seed + 1)
+    dout = torch.randn(B, Hq, N, D, generator=g, device="cuda").to(dtype)
+    return q, k, v, dout
+
+
+def _scaled_err(got, ref):
+    got = got.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got))
+    return float(np.max(np.abs(got - ref)) / max(1.0, np.max(np.abs(ref))))
+
+
+CASES = [
+    # B, Hq, Hkv, N, D, R, layout, causal, dtype
+    (1, 2, 1, 64, 16, 4, "zigzag", True, torch.float32),      # worked-example sized chunks of 8
+    (1, 2, 2, 48, 16, 3, "striped", True, torch.float32),
+    (1, 2, 1, 60, 32, 3, "contig", False, torch.float32),
+    (1, 4, 2, 1024, 128, 4, "zigzag", True, torch.bfloat16),  # chunks of one tile
+    (1, 4, 2, 768, 128, 4, "zigzag", True, torch.bfloat16),   # chunks of 96 rows: under a tile
+    (1, 2, 2, 640, 128, 2, "contig", True, torch.bfloat16),   # 320-row blocks: ragged tiles
+    (1, 4, 1, 600, 128, 3, "striped", True, torch.bfloat16),  # interleave of 200
+    (1, 2, 2, 516, 128, 4, "striped", True, torch.bfloat16),  # 129 per rank: key tiles no row sees
+    (2, 2, 2, 512, 64, 2, "zigzag", False, torch.bfloat16),
+    (1, 2, 2, 480, 64, 5, "striped", False, torch.bfloat16),
+    (1, 2, 1, 96, 32, 2, "zigzag", True, torch.bfloat16),     # CUDA-core path (D = 32)
+    (1, 2, 2, 2048, 128, 8, "zigzag", True, torch.bfloat16),
+]
+
+
+def _id(c):
+    return f"B{c[0]}H{c[1]}-{c[2]}N{c[3]}D{c[4]}R{c[5]}{c[6]}{'c' if c[7] else 'n'}{str(c[8])[6:]}"
+
+
+@pytest.mark.parametrize("case", CASES, ids=_id)
+def test_ring_backward_matches_oracle(ra, case):
+    B, Hq, Hkv, N, D, R, layout, causal, dtype = case
+    q, k, v, dout = _inputs(B, Hq, Hkv, N, D, dtype, seed=N * 3 + R)
+    o, lse = ra.ring_sim_fwd(q, k, v, R, layout, causal)
+    dq, dk, dv = ra.ring_sim_bwd(q, k, v, o, lse, dout, R, layout, causal)
+    ra.check()
+    args = [to_oracle(t) for t in (q, k, v, dout)]
+    if N <= 256:
+        rq, rk, rv = ob.ring_backward(*args, R, layout, causal)
+    else:
+        rq, rk, rv, _, _ = ob.attention_bwd(*args, causal)
+    for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        err = _scaled_err(got, ref)
+        assert err <= TOL[dtype], f"{name}: scaled max-abs error {err:.3e}"
+
+
+@pytest.mark.parametrize("dtype,D", [(torch.bfloat16, 128), (torch.float32, 64)])
+@pytest.mark.parametrize("layout", ["contig", "zigzag", "striped"])
+def test_ring_size_one_is_attn_bwd(ra, dtype, D, layout):
+    """One simulated rank is the whole-sequence backward, bit for bit (same kernels, one
+    segment)."""
+    q, k, v, dout = _inputs(1, 4, 2, 384, D, dtype, seed=5)
+    o, lse = ra.attn_fwd(q, k, v, causal=True)
+    a = ra.attn_bwd(q, k, v, o, lse, dout, causal=True)
+    b = ra.ring_sim_bwd(q, k, v, o, lse, dout, 1, layout, True)
+    ra.check()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_ring_backward_tensor_cores_match_cuda_cores(ra):
+    """The tensor-core kernels (aligned rows) and the CUDA-core kernels (rows whose
+    strides are not 16-byte multiples) give the same ring gradients."""
+    B, Hq, Hkv, N, D, R = 1, 4, 2, 1024, 128, 4
+    q, k, v, dout = _inputs(B, Hq, Hkv, N, D, torch.bfloat16, seed=9)
+    o, lse = ra.ring_sim_fwd(q, k, v, R, "zigzag", True)
+    a = ra.ring_sim_bwd(q, k, v, o, lse, dout, R, "zigzag", True)
+
+    def unaligned(t):
+        buf = torch.empty(*t.shape[:3], 136, dtype=t.dtype, device=t.device)[..., :D]
+        buf.copy_(t)
+        return buf
+
+    qu, ku, vu, ou, du = (unaligned(t) for t in (q, k, v, o, dout))
+    b = ra.ring_sim_bwd(qu, ku, vu, ou, lse, du, R, "zigzag", True,
+                        dq=unaligned(q), dk=unaligned(k), dv=unaligned(v))
+    ra.check()
+    for x, y in zip(a, b):
+        err = (x.float() - y.float()).abs().max().item() / max(1.0, y.float().abs().max().item())
+        assert err <= 1e-2
+
+
+def test_ring_backward_full_size_sampled(ra):
+    """The 8-rank zigzag ring over 32768 positions (8 heads, head_dim 128, bf16):
+    sampled dQ rows and dK/dV rows against the oracle one by one, the ring against the
+    single pass, and sum_j dV_j = sum_i dO_i (each row of P sums to one)."""
+    w = synth.WORKLOADS["ring8_zigzag_h8n32k"]
+    q, k, v = synth.workload_inputs(w, device="cuda")
+    B, Hq, N, D = q.shape
+    Hkv = k.shape[1]
+    g = torch.Generator(device="cuda").manual_seed(77)
+    dout = torch.randn(B, Hq, N, D, generator=g, device="cuda").to(torch.bfloat16)
+    R, layout = w.ring_size, w.layout
+    o, lse = ra.ring_sim_fwd(q, k, v, R, layout, True)
+    dq, dk, dv = ra.ring_sim_bwd(q, k, v, o, lse, dout, R, layout, True)
+    ra.check()
+    rng = np.random.default_rng(8)
+    # query rows anywhere; key rows in the last two chunks (the rows that see them are few
+    # enough for the oracle), which include keys whose gradients two ring steps write
+    chunk = N // (2 * R)
+    q_rows = np.array([(0, int(h), int(i)) for h, i in zip(rng.integers(0, Hq, 12), rng.integers(0, N, 12))]
+                      + [(0, 0, 0), (0, Hq - 1, N - 1), (0, 3, chunk), (0, 5, chunk - 1)])
+    kj = [N - 1, N - chunk, N - chunk - 1, N - 2 * chunk + 3]
+    kv_rows = np.array([(0, 0, j) for j in kj])
+    args = [to_oracle(t) for t in (q, k, v, dout)]
+    rq, rk, rv = ob.gradient_rows(*args, True, None, q_rows, kv_rows)
+    for name, got, rows, ref in (("dq", dq, q_rows, rq), ("dk", dk, kv_rows, rk), ("dv", dv, kv_rows, rv)):
+        sel = got[rows[:, 0], rows[:, 1], rows[:, 2]].float().cpu().numpy().astype(np.float64)
+        err = float(np.max(np.abs(sel - ref)) / max(1.0, np.max(np.abs(ref))))
+        assert err <= TOL[torch.bfloat16], f"{name}: sampled scaled error {err:.3e}"
+    # the ring against the single pass on the same forward outputs
+    sq, sk, sv = ra.attn_bwd(q, k, v, o, lse, dout, causal=True)
+    for x, y in ((dq, sq), (dk, sk), (dv, sv)):
+        err = (x.float() - y.float()).abs().max().item() / max(1.0, y.float().abs().max().item())
+        assert err <= TOL[torch.bfloat16]
+    # sum over keys of dV = sum over rows of dO, per KV head (G query heads each)
+    G = Hq // Hkv
+    lhs = dv.double().sum(dim=2)
+    rhs = dout.double().view(B, Hkv, G, N, D).sum(dim=(2, 3))
+    bound = 2.0 ** -8 * (dv.double().abs().sum(dim=2) + dout.double().abs().view(B, Hkv, G, N, D).sum(dim=(2, 3)))
+    assert torch.all((lhs - rhs).abs() <= bound)

@@ -222,3 +222,59 @@ def test_varlen_argument_errors(ra):
     assert call([0, 50], 1, shape=(2, 2, 100, 128)) == IA  # B must be 1
     assert L.ra_attn_varlen_fwd(ctypes.byref(_t(S)), ctypes.byref(_t(S)), ctypes.byref(_t(S)),
                                 ctypes.byref(_t(S)), 0x20000, None, 3, 1, 0.0, None) == IA
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("layout", ["contig", "zigzag", "striped"])
+def test_backward_plan_covers_every_visible_pair_once(ra, layout, causal, R):
+    """Over the ring steps, the dQ segments (kind 0) visit every visible (row, key) pair
+    exactly once, and so do the dK/dV segments (kind 1); each fixed range has exactly one
+    FIRST and one FINAL segment, on its first and last step; at step s the partner of a
+    range of rank r (dQ) is rank (r - s) mod R, of a key range of rank j (dK/dV) rank
+    (j + s) mod R."""
+    N = 2 * R * 6
+    held = oring.rank_positions(N, R, layout)
+    rank_of = {}
+    for r, pos in enumerate(held):
+        for p in pos.tolist():
+            rank_of[p] = r
+    rs = R if layout == "striped" else 1
+
+    def positions(a, b, rank):
+        return [i * rs + rank for i in range(a, b)]
+
+    for kind in (0, 1):
+        seen = {}
+        first, last, nfirst, nfinal = {}, {}, {}, {}
+        for s in range(R):
+            for g in ra.ring_sim_bwd_plan(N, R, layout, causal, s, kind):
+                fixed = positions(g["f0"], g["f1"], g["f_rank"])
+                streamed = positions(g["s0a"], g["s1a"], g["s_rank"]) + positions(g["s0b"], g["s1b"], g["s_rank"])
+                fr = {rank_of[p] for p in fixed}
+                sr = {rank_of[p] for p in streamed}
+                assert len(fr) == 1 and len(sr) == 1
+                fr, sr = fr.pop(), sr.pop()
+                assert sr == ((fr - s) % R if kind == 0 else (fr + s) % R)
+                for a in fixed:
+                    for b in streamed:
+                        row, key = (a, b) if kind == 0 else (b, a)
+                        vis = (not causal) or key <= row
+                        # the kernels' index rule (key index + diag <= row index) is the
+                        # position rule
+                        assert vis == ((not causal) or key // rs + g["diag"] <= row // rs)
+                        if vis:
+                            seen[(row, key)] = seen.get((row, key), 0) + 1
+                rid = (fr, g["f0"])
+                first.setdefault(rid, s)
+                last[rid] = s
+                nfirst[rid] = nfirst.get(rid, 0) + (g["flags"] & 1)
+                nfinal[rid] = nfinal.get(rid, 0) + ((g["flags"] >> 1) & 1)
+                assert bool(g["flags"] & 1) == (first[rid] == s)
+        want = {(i, j) for i in range(N) for j in range(N) if (not causal or j <= i)}
+        assert set(seen) == want and set(seen.values()) == {1}, kind
+        assert set(nfirst.values()) == {1} and set(nfinal.values()) == {1}
+        for s in range(R):
+            for g in ra.ring_sim_bwd_plan(N, R, layout, causal, s, kind):
+                rid = ({rank_of[p] for p in positions(g["f0"], g["f1"], g["f_rank"])}.pop(), g["f0"])
+                assert bool(g["flags"] & 2) == (last[rid] == s)
