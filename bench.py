@@ -284,7 +284,7 @@ def run_ours(args, w, ws, rank, local):
     achieved = per_launch_flops / (per_launch_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4),
-                "traffic": profiled_traffic(w.name), "peak_kind": peak_kind}
+                "traffic": None if bwd else profiled_traffic(w.name), "peak_kind": peak_kind}
     return {
         "value": round(value, 2), "ms_per_step": round(ms_per_step, 5), "e2e": e2e,
         "roofline": roofline, "clocks": clk, "gpu_launches": launches,

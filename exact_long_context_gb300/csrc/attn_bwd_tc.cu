@@ -16,8 +16,10 @@
 //                 P^T, dS^T                         (one thread per key)
 //                 dV += P^T dO,  dK += dS^T Q       (A from tensor memory)
 //
-// Warp roles: warp 0 TMA producer, warp 1 MMA issuer and tensor-memory owner, warps 4-7
-// the element-wise work and the epilogue.  The streamed tile is handled as two 64-wide
+// Warp roles: warp 0 TMA producer, warp 1 MMA issuer and tensor-memory owner, warps 4-11
+// the element-wise work and the epilogue: two warps per tensor-memory lane quarter, each
+// owning 32 of a sub-tile's 64 columns (one warp per scheduler left the exponentials and
+// the tensor-memory round trips exposed).  The streamed tile is handled as two 64-wide
 // halves with their own S / dP buffers, so the tensor core computes one half's S / dP
 // while the element-wise warps work on the other.  The bf16 P / dS overwrite the
 // columns of the fp32 S / dP they came from once those are in registers; the MMA
@@ -36,11 +38,16 @@ using namespace ra::tc;
 
 constexpr int kT = 128;   // rows per tile (queries or keys)
 constexpr int kSub = 64;  // a tile's streamed dimension is processed as two 64-wide halves
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
+constexpr int kEwWarps = 8;
+constexpr uint32_t kNegInfBits = 0xff800000u;  // -inf as fp32 bits  // warps 4-11: two groups of four, one per 32-column half of a sub-tile
 
 // Tensor memory: for sub-tile u in {0, 1}, S_u at 128u (64 fp32 columns) and dP_u at
-// 128u + 64; the bf16 P_u / dS_u (32 columns) overwrite the leading columns of S_u / dP_u.
-// Accumulators at 256 (dQ or dV) and 256 + HD (dK).
+// 128u + 64.  Element-wise group g in {0, 1} reads columns [32g, 32g + 32) of S_u / dP_u
+// and writes its 32 bf16 values (16 columns) of P_u / dS_u to columns 16 + 16g of them:
+// inside what the group itself read, and clear of the other group's columns, so P_u and
+// dS_u are 32 contiguous columns at 128u + 16 and 128u + 80.  Accumulators at 256 (dQ or
+// dV) and 256 + HD (dK).
 template <int HD>
 struct BCfg {
     static constexpr int SLABS = HD / 64;
@@ -50,7 +57,7 @@ struct BCfg {
     static constexpr uint32_t TM_A0 = 256, TM_A1 = 256 + HD;
     static constexpr uint32_t TM_COLS = 512;
     static constexpr int BAR_OFF = (2 + 2 * NST) * TILE_BYTES;
-    static constexpr int SMEM_BYTES = 1024 + BAR_OFF + 256 + 4096;
+    static constexpr int SMEM_BYTES = 1024 + BAR_OFF + 256 + kEwWarps * 2 * 64 * 4;
 };
 
 struct BBars {
@@ -63,34 +70,46 @@ struct BBars {
 };
 static_assert(sizeof(BBars) <= 256, "barrier block");
 
-// dQ item L: query tile qi of one segment and one (b, h), the last tiles (most keys
-// under causality) first.  Rows [r_lo, r_hi) of the segment's fixed range; streamed key
-// tiles: n0 from the first range, then n - n0 from the second.
+// Work items are pairs of tiles of one segment and one head: tile p and tile tps-1-p of
+// the segment's fixed range.  Under causality the two costs add up to the same total,
+// so every item of a segment costs the same; items are numbered segment (heaviest
+// first, as the host orders them), then head, then pair, so the CTAs that run at the
+// same time share the streamed tiles of a few heads in L2.  `sub` selects the pair's
+// first (0) or second (1) tile; false when the pair has a single (middle) tile.
+__device__ __forceinline__ int tile_pairs(int tps) { return (tps + 1) >> 1; }
+
+// dQ sub-item: query tile of one segment and one (b, h).  Rows [r_lo, r_hi) of the
+// segment's fixed range; streamed key tiles: n0 from the first range, then n - n0 from
+// the second.
 struct QItem {
     int b, h, hk, si, r_lo, r_hi, n0, n;
 };
-__device__ __forceinline__ void decode_q(const BwdParams &P, int tps, int L, QItem &it) {
+__device__ __forceinline__ bool decode_q(const BwdParams &P, int tps, int L, int sub, QItem &it) {
     const int BH = P.B * P.Hq;
-    const int per = P.nseg * BH;
-    const int w = L / per;
-    const int rem = L - w * per;
-    it.si = rem / BH;
-    const int bh = rem - it.si * BH;
+    const int np = tile_pairs(tps);
+    const int per_seg = BH * np;
+    it.si = L / per_seg;
+    const int rem = L - it.si * per_seg;
+    const int bh = rem / np;
+    const int pp = rem - bh * np;
+    const int qi = sub ? pp : tps - 1 - pp;  // the later (heavier) query tile first
+    if (sub && qi == tps - 1 - pp) return false;
     it.b = bh / P.Hq;
     it.h = bh - it.b * P.Hq;
     it.hk = it.h / (P.Hq / P.Hkv);
     const BSeg &S = P.seg[it.si];
-    it.r_lo = S.f0 + (tps - 1 - w) * kT;
+    it.r_lo = S.f0 + qi * kT;
     it.r_hi = min(it.r_lo + kT, S.f1);
     it.n = 0;
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
         const int a = S.s0[p];
         const int e = P.causal ? min(S.s1[p], it.r_hi - S.diag) : S.s1[p];
-        const int np = e > a ? (e - a + kT - 1) / kT : 0;
-        if (p == 0) it.n0 = np;
-        it.n += np;
+        const int np_ = e > a ? (e - a + kT - 1) / kT : 0;
+        if (p == 0) it.n0 = np_;
+        it.n += np_;
     }
+    return true;
 }
 
 // Streamed key tile t of a dQ item: first key index and the end of its range.
@@ -100,38 +119,42 @@ __device__ __forceinline__ void q_tile(const BSeg &S, const QItem &it, int t, in
     klim = p ? S.s1[1] : S.s1[0];
 }
 
-// dK/dV item L: key tile kj of one segment and one (b, KV head), the first tiles (most
-// query tiles under causality) first; it visits the visible query tiles of both streamed
-// ranges for each of the G query heads: n = G * per.
+// dK/dV sub-item: key tile of one segment and one (b, KV head), the earlier (heavier)
+// tile of the pair first; it visits the visible query tiles of both streamed ranges for
+// each of the G query heads: n = G * per.
 struct KItem {
     int b, hk, si, c_lo, c_hi, t0[2], n0, per, n;
 };
-__device__ __forceinline__ void decode_kv(const BwdParams &P, int L, KItem &it) {
+__device__ __forceinline__ bool decode_kv(const BwdParams &P, int tps, int L, int sub, KItem &it) {
     const int BHk = P.B * P.Hkv;
-    const int per_all = P.nseg * BHk;
-    const int w = L / per_all;
-    const int rem = L - w * per_all;
-    it.si = rem / BHk;
-    const int bhk = rem - it.si * BHk;
+    const int np = tile_pairs(tps);
+    const int per_seg = BHk * np;
+    it.si = L / per_seg;
+    const int rem = L - it.si * per_seg;
+    const int bhk = rem / np;
+    const int pp = rem - bhk * np;
+    const int kj = sub ? tps - 1 - pp : pp;
+    if (sub && kj == pp) return false;
     it.b = bhk / P.Hkv;
     it.hk = bhk - it.b * P.Hkv;
     const BSeg &S = P.seg[it.si];
-    it.c_lo = S.f0 + w * kT;
+    it.c_lo = S.f0 + kj * kT;
     it.c_hi = min(it.c_lo + kT, S.f1);
     it.per = 0;
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
         const int a = P.causal ? max(S.s0[p], it.c_lo + S.diag) : S.s0[p];
-        int np = 0, t0 = 0;
+        int np_ = 0, t0 = 0;
         if (a < S.s1[p]) {
             t0 = (a - S.s0[p]) / kT;
-            np = (S.s1[p] - S.s0[p] + kT - 1) / kT - t0;
+            np_ = (S.s1[p] - S.s0[p] + kT - 1) / kT - t0;
         }
         it.t0[p] = t0;
-        if (p == 0) it.n0 = np;
-        it.per += np;
+        if (p == 0) it.n0 = np_;
+        it.per += np_;
     }
     it.n = (P.Hq / P.Hkv) * it.per;
+    return true;
 }
 
 // Streamed query tile t of a dK/dV item: first query index, the end of its range, head.
@@ -323,11 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             int slot = 0;
             uint32_t ph = 0, fcnt = 0, issued = 0, last_ph = 0;
             bool ok = true;
-            for (int k = 0; k * (int)gridDim.x < total && ok; ++k) {
-                const int L = snake(k);
+            for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, tile of the pair)
+                const int L = snake(k2 >> 1);
                 if (L >= total) continue;
                 QItem it;
-                decode_q(P, tps, L, it);
+                if (!decode_q(P, tps, L, k2 & 1, it)) continue;
                 if (it.n == 0) continue;
                 const BSeg &S = P.seg[it.si];
                 const int hk = it.hk;
@@ -351,11 +374,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             int slot = 0;
             uint32_t ph = 0, fcnt = 0, pc[2] = {0u, 0u};
             bool ok = true;
-            for (int k = 0; k * (int)gridDim.x < total && ok; ++k) {
-                const int L = snake(k);
+            for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, tile of the pair)
+                const int L = snake(k2 >> 1);
                 if (L >= total) continue;
                 QItem it;
-                decode_q(P, tps, L, it);
+                if (!decode_q(P, tps, L, k2 & 1, it)) continue;
                 const int n = it.n;
                 if (n == 0) continue;
                 ok = wait_phase(smem_u32(&bars->fix_full), fcnt & 1u, abort_flag, limit, err);
@@ -382,10 +405,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     for (int u = 0; u < 2 && ok; ++u) {
                         ++pc[u];
-                        ok = wait_count(&bars->p_count[u], 4u * pc[u], abort_flag, limit, err);
+                        ok = wait_count(&bars->p_count[u], (uint32_t)kEwWarps * pc[u], abort_flag, limit, err);
                         if (!ok) break;
                         tc_fence_after();
-                        issue_acc<HD>(tmem, C::TM_A0, 128 * u + 64, kb, u, t > 0 || u > 0);  // dQ += dS_u K_u
+                        issue_acc<HD>(tmem, C::TM_A0, 128 * u + 80, kb, u, t > 0 || u > 0);  // dQ += dS_u K_u
                         if (t + 1 < n) {
                             if (u == 0) {
                                 ok = wait_phase(smem_u32(&bars->full[nslot]), nph, abort_flag, limit, err);
@@ -410,14 +433,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= 4) {
         const int quarter = warp & 3;
+        const int grp = (warp - 4) >> 2;  // which 32 columns of a sub-tile this warp owns
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         uint32_t sc[2] = {0u, 0u}, ocnt = 0;
         bool ok = true;
-        for (int k = 0; k * (int)gridDim.x < total && ok; ++k) {
-            const int L = snake(k);
+        for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, tile of the pair)
+            const int L = snake(k2 >> 1);
             if (L >= total) continue;
             QItem it;
-            decode_q(P, tps, L, it);
+            if (!decode_q(P, tps, L, k2 & 1, it)) continue;
             const BSeg &S = P.seg[it.si];
             const int n = it.n, diag = S.diag;
             const int row = it.r_lo + quarter * 32 + lane;  // index in the fixed range
@@ -427,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float lse_l2 = valid ? P.lse[lrow] * kLog2e : 0.f;
             const float d_r = valid ? P.dvec[lrow] : 0.f;
             float *accp = P.acc_q + lrow * HD;
-            if (valid && !(S.flags & SEG_FIRST))
+            if (valid && grp == 0 && !(S.flags & SEG_FIRST))
                 for (int i = 0; i < HD * 4; i += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(
                                                           reinterpret_cast<const char *>(accp) + i));
             for (int t = 0; t < n && ok; ++t) {
@@ -438,31 +462,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++sc[u];
                     if (!ok) break;
                     tc_fence_after();
-                    const int k0 = kt0 + u * kSub;  // first key of this half
-                    const bool mask = (k0 + kSub > klim) || (P.causal && k0 + kSub - 1 + diag > row) || !valid;
-                    uint32_t pk[2][16];
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
+                    const int k0 = kt0 + u * kSub + grp * 32;  // first key of this warp's columns
+                    const bool mask = (k0 + 32 > klim) || (P.causal && k0 + 31 + diag > row) || !valid;
+                    uint32_t pk[16];
+                    {
                         uint32_t s[32], dp[32];
-                        tmem_ld32(tmem + 128 * u + lane_off + c * 32, s);
-                        tmem_ld32(tmem + 128 * u + 64 + lane_off + c * 32, dp);
+                        tmem_ld32(tmem + 128 * u + lane_off + grp * 32, s);
+                        tmem_ld32(tmem + 128 * u + 64 + lane_off + grp * 32, dp);
                         tmem_ld_wait();
+                        // invisible scores become -inf (P = 0, dS = 0) in a pass of their own,
+                        // so the loop below has no branch and its iterations interleave
+                        if (mask) {
+                            const int lim = !valid ? 0 : (P.causal ? min(klim, row + 1 - diag) : klim) - k0;
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) s[e] = e < lim ? s[e] : kNegInfBits;
+                        }
 #pragma unroll
                         for (int e = 0; e < 32; e += 2) {
-                            float p0 = ex2(fmaf(__uint_as_float(s[e]), sl2, -lse_l2));
-                            float p1 = ex2(fmaf(__uint_as_float(s[e + 1]), sl2, -lse_l2));
-                            if (mask) {
-                                const int key = k0 + c * 32 + e;
-                                p0 = (valid && key < klim && (!P.causal || key + diag <= row)) ? p0 : 0.f;
-                                p1 = (valid && key + 1 < klim && (!P.causal || key + 1 + diag <= row)) ? p1 : 0.f;
-                            }
-                            pk[c][e / 2] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - d_r),
-                                                       p1 * (__uint_as_float(dp[e + 1]) - d_r));
+                            const float p0 = ex2(fmaf(__uint_as_float(s[e]), sl2, -lse_l2));
+                            const float p1 = ex2(fmaf(__uint_as_float(s[e + 1]), sl2, -lse_l2));
+                            pk[e / 2] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - d_r),
+                                                    p1 * (__uint_as_float(dp[e + 1]) - d_r));
                         }
                     }
-                    // dS_u over the (already loaded) leading dP_u columns
-                    tmem_st16(tmem + 128 * u + 64 + lane_off, pk[0]);
-                    tmem_st16(tmem + 128 * u + 64 + 16 + lane_off, pk[1]);
+                    // this warp's half of dS_u, inside the dP_u columns it has read
+                    tmem_st16(tmem + 128 * u + 80 + 16 * grp + lane_off, pk);
                     tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();
@@ -478,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(P.dq) + (int64_t)it.b * P.sdq[0] +
                                   (int64_t)it.h * P.sdq[1] + pos * P.sdq[2];
-            for (int c = 0; c < HD / 32; ++c) {
+            for (int c = grp * (HD / 64); c < (grp + 1) * (HD / 64); ++c) {  // this group's columns
                 uint32_t o[32];
                 if (n > 0) {
                     tmem_ld32(tmem + C::TM_A0 + lane_off + c * 32, o);
@@ -514,11 +538,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sSt = base + 2 * C::TILE_BYTES;  // stages of (Q, dO)
     BBars *bars = reinterpret_cast<BBars *>(base_ptr + C::BAR_OFF);
     // per element-wise warp: the current query tile's LSE (log2 units) and D values
-    float *s_stage = reinterpret_cast<float *>(base_ptr + C::BAR_OFF + 256);  // [4 warps][2][128]
+    float *s_stage = reinterpret_cast<float *>(base_ptr + C::BAR_OFF + 256);  // [8 warps][2][64]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if ((int)blockIdx.x >= total) return;
     volatile int32_t *abort_flag = &bars->abort;
     const int G = P.Hq / P.Hkv;
+    const int tps = (P.flen + kT - 1) / kT;
     const float sl2 = P.scale_log2;
 
     if (threadIdx.x == 0) bwd_init(bars, C::NST);
@@ -537,11 +562,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             int slot = 0;
             uint32_t ph = 0, fcnt = 0, issued = 0, last_ph = 0;
             bool ok = true;
-            for (int k = 0; k * (int)gridDim.x < total && ok; ++k) {
-                const int L = snake(k);
+            for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, tile of the pair)
+                const int L = snake(k2 >> 1);
                 if (L >= total) continue;
                 KItem it;
-                decode_kv(P, L, it);
+                if (!decode_kv(P, tps, L, k2 & 1, it)) continue;
                 if (it.n == 0) continue;
                 const BSeg &S = P.seg[it.si];
                 const int hk = it.hk;
@@ -565,11 +590,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             int slot = 0;
             uint32_t ph = 0, fcnt = 0, pc[2] = {0u, 0u};
             bool ok = true;
-            for (int k = 0; k * (int)gridDim.x < total && ok; ++k) {
-                const int L = snake(k);
+            for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, tile of the pair)
+                const int L = snake(k2 >> 1);
                 if (L >= total) continue;
                 KItem it;
-                decode_kv(P, L, it);
+                if (!decode_kv(P, tps, L, k2 & 1, it)) continue;
                 const int n = it.n;
                 if (n == 0) continue;
                 ok = wait_phase(smem_u32(&bars->fix_full), fcnt & 1u, abort_flag, limit, err);
@@ -595,12 +620,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     for (int u = 0; u < 2 && ok; ++u) {
                         ++pc[u];
-                        ok = wait_count(&bars->p_count[u], 4u * pc[u], abort_flag, limit, err);
+                        ok = wait_count(&bars->p_count[u], (uint32_t)kEwWarps * pc[u], abort_flag, limit, err);
                         if (!ok) break;
                         tc_fence_after();
                         const bool accum = t > 0 || u > 0;
-                        issue_acc<HD>(tmem, C::TM_A0, 128 * u, qb + C::TILE_BYTES, u, accum);  // dV += P^T_u dO_u
-                        issue_acc<HD>(tmem, C::TM_A1, 128 * u + 64, qb, u, accum);             // dK += dS^T_u Q_u
+                        issue_acc<HD>(tmem, C::TM_A0, 128 * u + 16, qb + C::TILE_BYTES, u, accum);  // dV += P^T_u dO_u
+                        issue_acc<HD>(tmem, C::TM_A1, 128 * u + 80, qb, u, accum);                  // dK += dS^T_u Q_u
                         if (t + 1 < n) {
                             if (u == 0) {
                                 ok = wait_phase(smem_u32(&bars->full[nslot]), nph, abort_flag, limit, err);
@@ -625,23 +650,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= 4) {
         const int quarter = warp & 3;
+        const int grp = (warp - 4) >> 2;  // which 32 columns of a sub-tile this warp owns
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        float *lb = s_stage + quarter * 2 * kT;  // this warp's copy, so no cross-warp barrier
-        float *db = lb + kT;
+        float *lb = s_stage + (warp - 4) * 2 * 64;  // this warp's columns only: no cross-warp barrier
+        float *db = lb + 64;
         uint32_t sc[2] = {0u, 0u}, ocnt = 0;
         bool ok = true;
-        for (int k = 0; k * (int)gridDim.x < total && ok; ++k) {
-            const int L = snake(k);
+        for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, tile of the pair)
+            const int L = snake(k2 >> 1);
             if (L >= total) continue;
             KItem it;
-            decode_kv(P, L, it);
+            if (!decode_kv(P, tps, L, k2 & 1, it)) continue;
             const BSeg &S = P.seg[it.si];
             const int n = it.n, diag = S.diag;
             const int key = it.c_lo + quarter * 32 + lane;  // index in the fixed range
             const bool kvalid = key < it.c_hi;
             const int64_t kpos = (int64_t)key * P.rs + S.f_rank;
             const int64_t arow = (((int64_t)it.b * P.Hkv + it.hk) * P.N + kpos) * HD;
-            if (kvalid && !(S.flags & SEG_FIRST))
+            if (kvalid && grp == 0 && !(S.flags & SEG_FIRST))
                 for (int i = 0; i < HD * 4; i += 128) {
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(P.acc_k + arow) + i));
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(P.acc_v + arow) + i));
@@ -652,8 +678,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int h = it.hk * G + g;
                 __syncwarp();  // every lane is done with the previous tile's values
 #pragma unroll
-                for (int r = 0; r < kT / 32; ++r) {
-                    const int qme = q0 + r * 32 + lane;
+                for (int r = 0; r < 2; ++r) {  // the queries of this warp's columns of both halves
+                    const int qme = q0 + r * kSub + grp * 32 + lane;
                     const int64_t li = ((int64_t)it.b * P.Hq + h) * P.N + (int64_t)qme * P.rs + S.s_rank;
                     lb[r * 32 + lane] = qme < qlim ? P.lse[li] * kLog2e : 0.f;
                     db[r * 32 + lane] = qme < qlim ? P.dvec[li] : 0.f;
@@ -664,34 +690,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++sc[u];
                     if (!ok) break;
                     tc_fence_after();
-                    const int qa = q0 + u * kSub;  // first query of this half
-                    const bool mask = (qa + kSub > qlim) || (P.causal && it.c_hi - 1 + diag > qa);
-                    uint32_t pp[2][16], pd[2][16];
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
+                    const int qa = q0 + u * kSub + grp * 32;  // first query of this warp's columns
+                    const bool mask = (qa + 32 > qlim) || (P.causal && it.c_hi - 1 + diag > qa);
+                    uint32_t pp[16], pd[16];
+                    {
                         uint32_t s[32], dp[32];
-                        tmem_ld32(tmem + 128 * u + lane_off + c * 32, s);
-                        tmem_ld32(tmem + 128 * u + 64 + lane_off + c * 32, dp);
+                        tmem_ld32(tmem + 128 * u + lane_off + grp * 32, s);
+                        tmem_ld32(tmem + 128 * u + 64 + lane_off + grp * 32, dp);
                         tmem_ld_wait();
+                        const float *lu = lb + u * 32, *du = db + u * 32;
+                        // invisible scores become -inf (P = 0, dS = 0) in a pass of their own,
+                        // so the loop below has no branch and its iterations interleave
+                        if (mask) {
+                            const int lo = P.causal ? key + diag - qa : 0;  // first visible offset
+                            const int hi = qlim - qa;                       // end of the range
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) s[e] = (e >= lo && e < hi) ? s[e] : kNegInfBits;
+                        }
 #pragma unroll
                         for (int e = 0; e < 32; e += 2) {
-                            const int qo = u * kSub + c * 32 + e;  // offset in the tile
-                            float p0 = ex2(fmaf(__uint_as_float(s[e]), sl2, -lb[qo]));
-                            float p1 = ex2(fmaf(__uint_as_float(s[e + 1]), sl2, -lb[qo + 1]));
-                            if (mask) {
-                                const int qq = q0 + qo;
-                                p0 = (qq < qlim && (!P.causal || key + diag <= qq)) ? p0 : 0.f;
-                                p1 = (qq + 1 < qlim && (!P.causal || key + diag <= qq + 1)) ? p1 : 0.f;
-                            }
-                            pp[c][e / 2] = pack_bf16x2(p0, p1);
-                            pd[c][e / 2] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - db[qo]),
-                                                       p1 * (__uint_as_float(dp[e + 1]) - db[qo + 1]));
+                            const float p0 = ex2(fmaf(__uint_as_float(s[e]), sl2, -lu[e]));
+                            const float p1 = ex2(fmaf(__uint_as_float(s[e + 1]), sl2, -lu[e + 1]));
+                            pp[e / 2] = pack_bf16x2(p0, p1);
+                            pd[e / 2] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - du[e]),
+                                                    p1 * (__uint_as_float(dp[e + 1]) - du[e + 1]));
                         }
                     }
-                    tmem_st16(tmem + 128 * u + lane_off, pp[0]);
-                    tmem_st16(tmem + 128 * u + 16 + lane_off, pp[1]);
-                    tmem_st16(tmem + 128 * u + 64 + lane_off, pd[0]);
-                    tmem_st16(tmem + 128 * u + 64 + 16 + lane_off, pd[1]);
+                    // this warp's halves of P_u and dS_u, inside the columns it has read
+                    tmem_st16(tmem + 128 * u + 16 + 16 * grp + lane_off, pp);
+                    tmem_st16(tmem + 128 * u + 80 + 16 * grp + lane_off, pd);
                     tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();
@@ -714,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __nv_bfloat16 *dst = which ? krow : vrow;
                 float *acc = (which ? P.acc_k : P.acc_v) + arow;
                 const uint32_t col = which ? C::TM_A1 : C::TM_A0;
-                for (int c = 0; c < HD / 32; ++c) {
+                for (int c = grp * (HD / 64); c < (grp + 1) * (HD / 64); ++c) {  // this group's columns
                     uint32_t o[32];
                     if (n > 0) {
                         tmem_ld32(tmem + col + lane_off + c * 32, o);
@@ -759,8 +786,8 @@ static cudaError_t launch_bwd_tc_hd(const BwdParams &P, int parts, int num_sms, 
         !encode_map(&mv, P.v, P.B, P.Hkv, P.N, P.D, P.sv, P.rs) ||
         !encode_map(&mdo, P.dout, P.B, P.Hq, P.N, P.D, P.sdo, P.rs))
         return cudaErrorInvalidValue;
-    const int nt = (P.flen + tcb::kT - 1) / tcb::kT;
-    const int64_t tq = (int64_t)P.B * P.Hq * P.nseg * nt, tkv = (int64_t)P.B * P.Hkv * P.nseg * nt;
+    const int np = ((P.flen + tcb::kT - 1) / tcb::kT + 1) / 2;  // tile pairs per segment and head
+    const int64_t tq = (int64_t)P.B * P.Hq * P.nseg * np, tkv = (int64_t)P.B * P.Hkv * P.nseg * np;
     if (tq > 0x7fffffff || tkv > 0x7fffffff) return cudaErrorInvalidValue;
     if (parts & 1) {
         tcb::bwd_dq_tc_kernel<HD><<<(int)std::min<int64_t>(tq, num_sms), tcb::kThreads, C::SMEM_BYTES, stream>>>(
