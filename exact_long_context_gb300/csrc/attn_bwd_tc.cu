@@ -36,33 +36,43 @@ namespace tcb {
 
 using namespace ra::tc;
 
-constexpr int kT = 128;   // rows per tile (queries or keys)
-constexpr int kSub = 64;  // a tile's streamed dimension is processed as two 64-wide halves
+constexpr int kT = 128;  // rows per tile (queries or keys); S / dP products are 128 x 128
 constexpr int kThreads = 384;
-constexpr int kEwWarps = 8;
-constexpr uint32_t kNegInfBits = 0xff800000u;  // -inf as fp32 bits  // warps 4-11: two groups of four, one per 32-column half of a sub-tile
+constexpr int kEwWarps = 8;  // warps 4-11: two groups of four, each owning 64 of a tile's 128 columns
+constexpr uint32_t kNegInfBits = 0xff800000u;  // -inf as fp32 bits
 
-// Tensor memory: for sub-tile u in {0, 1}, S_u at 128u (64 fp32 columns) and dP_u at
-// 128u + 64.  Element-wise group g in {0, 1} reads columns [32g, 32g + 32) of S_u / dP_u
-// and writes its 32 bf16 values (16 columns) of P_u / dS_u to columns 16 + 16g of them:
-// inside what the group itself read, and clear of the other group's columns, so P_u and
-// dS_u are 32 contiguous columns at 128u + 16 and 128u + 80.  Accumulators at 256 (dQ or
-// dV) and 256 + HD (dK).
+// Tensor memory (512 columns).  dQ kernel: three 128-column slots that hold the S and dP
+// of consecutive tiles in rotation (tile g: S in slot s_slot(g), dP in slot d_slot(g);
+// the next tile's S goes to the free slot and its dP to the slot of this tile's S once
+// that has been read), dQ accumulator at 384.  dK/dV kernel: S^T at 0, dP^T at 128, dV
+// at 256, dK at 256 + HD.  The bf16 P / dS a tile produces (64 packed columns) overwrite
+// columns 32..95 of the fp32 S / dP they came from: element-wise group g reads columns
+// [64g, 64g + 64) and writes its 32 packed columns at 32 + 32g, inside what it has read
+// and clear of the other group's columns (the order of its two 32-column chunks keeps a
+// chunk from being overwritten before it is read).
 template <int HD>
 struct BCfg {
     static constexpr int SLABS = HD / 64;
     static constexpr int TILE_BYTES = kT * HD * 2;
     static constexpr int SLAB_BYTES = 128 * 128;
-    static constexpr int NST = (HD == 128) ? 2 : 4;  // stages of two tiles
-    static constexpr uint32_t TM_A0 = 256, TM_A1 = 256 + HD;
+    static constexpr int NST = (HD == 128) ? 2 : 4;  // dK/dV kernel: stages of two tiles (Q, dO)
+    // dQ kernel: separate rings of K tiles and V tiles (V is free after the dP product,
+    // K only after the dQ product, so K gets the deeper ring)
+    static constexpr int KST = (HD == 128) ? 3 : 4;
+    static constexpr int VST = (HD == 128) ? 2 : 4;
+    static constexpr uint32_t TM_A0 = 256, TM_A1 = 256 + HD;  // dK/dV kernel: dV, dK
+    static constexpr uint32_t TM_DQ = 384;                    // dQ kernel: dQ
     static constexpr uint32_t TM_COLS = 512;
     static constexpr int BAR_OFF = (2 + 2 * NST) * TILE_BYTES;
     static constexpr int SMEM_BYTES = 1024 + BAR_OFF + 256 + kEwWarps * 2 * 64 * 4;
+    static constexpr int BAR_OFF_DQ = (2 + KST + VST) * TILE_BYTES;
+    static constexpr int SMEM_BYTES_DQ = 1024 + BAR_OFF_DQ + 256;
 };
 
 struct BBars {
     uint64_t fix_full, fix_empty;  // the item's fixed pair (Q, dO) or (K, V)
-    uint64_t full[4], empty[4];    // streamed pairs
+    uint64_t full[4], empty[4];    // streamed pairs (dK/dV kernel) or K tiles (dQ kernel)
+    uint64_t fullv[4], emptyv[4];  // V tiles (dQ kernel)
     uint64_t s_full[2], o_full, drain;
     uint32_t tmem_base;
     int32_t abort;
@@ -183,6 +193,8 @@ __device__ __forceinline__ void bwd_init(BBars *bars, int nst) {
     for (int s = 0; s < nst; ++s) {
         mbar_init(smem_u32(&bars->full[s]), 1);
         mbar_init(smem_u32(&bars->empty[s]), 1);
+        mbar_init(smem_u32(&bars->fullv[s]), 1);
+        mbar_init(smem_u32(&bars->emptyv[s]), 1);
     }
     mbar_init(smem_u32(&bars->s_full[0]), 1);
     mbar_init(smem_u32(&bars->s_full[1]), 1);
@@ -244,34 +256,103 @@ __device__ __forceinline__ bool produce_item(BBars *bars, uint32_t fix0, uint32_
     return true;
 }
 
-// MMA issue for S_u = A B_u^T and dP_u = A' B'_u^T (N = 64 of the streamed tile's rows,
-// K = HD): the fixed pair (fa, fb) against half u of the streamed pair (sa, sb).
-template <int HD>
-__device__ __forceinline__ void issue_sdp(uint32_t tmem, int u, uint32_t fa, uint32_t fb, uint32_t sa,
-                                          uint32_t sb) {
+// A ring of single-tile buffers: slot, phase, and for a bounded drain on abort the slots
+// with loads in flight and their phases.
+struct Ring {
+    int slot;
+    uint32_t ph, issued, last_ph;
+    template <int DEPTH>
+    __device__ __forceinline__ void advance() {
+        if (++slot == DEPTH) {
+            slot = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
+// Producer of the dQ kernel: per item the fixed pair (Q, dO), then for each streamed tile
+// its K into the K ring and its V into the V ring.
+template <int HD, typename StreamCoords>
+__device__ __forceinline__ bool produce_item_kv(BBars *bars, uint32_t fix0, uint32_t k0, uint32_t v0, Ring &kr,
+                                                Ring &vr, uint32_t &fcnt, const CUtensorMap *fa,
+                                                const CUtensorMap *fb, int f_row, int f_rank, int fh,
+                                                const CUtensorMap *tk, const CUtensorMap *tv, int s_rank, int n,
+                                                int b, StreamCoords coords, volatile int32_t *abort_flag,
+                                                int64_t limit, int *err) {
     using C = BCfg<HD>;
-    constexpr uint32_t ID = idesc_bf16(kT, kSub, false);
-    const uint32_t half = u * kSub * 128;  // rows 64u.. of each 128-byte-wide slab
+    if (!wait_phase(smem_u32(&bars->fix_empty), (fcnt & 1u) ^ 1u, abort_flag, limit, err)) return false;
+    {
+        const uint32_t bf = smem_u32(&bars->fix_full);
+        mbar_expect_tx(bf, 2 * C::TILE_BYTES);
+        for (int c = 0; c < C::SLABS; ++c) {
+            tma_load_5d(fix0 + c * C::SLAB_BYTES, fa, bf, c * 64, f_rank, f_row, fh, b);
+            tma_load_5d(fix0 + C::TILE_BYTES + c * C::SLAB_BYTES, fb, bf, c * 64, f_rank, f_row, fh, b);
+        }
+        ++fcnt;
+    }
+    for (int t = 0; t < n; ++t) {
+        int row, head;
+        coords(t, row, head);
+        for (int which = 0; which < 2; ++which) {
+            Ring &r = which ? vr : kr;
+            uint64_t *emp = which ? bars->emptyv : bars->empty;
+            uint64_t *ful = which ? bars->fullv : bars->full;
+            if (!wait_phase(smem_u32(&emp[r.slot]), r.ph ^ 1u, abort_flag, limit, err)) return false;
+            const uint32_t bf = smem_u32(&ful[r.slot]);
+            mbar_expect_tx(bf, C::TILE_BYTES);
+            const uint32_t dst = (which ? v0 : k0) + r.slot * C::TILE_BYTES;
+            for (int c = 0; c < C::SLABS; ++c)
+                tma_load_5d(dst + c * C::SLAB_BYTES, which ? tv : tk, bf, c * 64, s_rank, row, head, b);
+            r.issued |= 1u << r.slot;
+            r.last_ph = (r.last_ph & ~(1u << r.slot)) | (r.ph << r.slot);
+            if (which)
+                r.advance<C::VST>();
+            else
+                r.advance<C::KST>();
+        }
+    }
+    return true;
+}
+
+// D = A B^T over K = HD into the 128 x 128 fp32 tile at tensor-memory column tcol: A and
+// B are 128-row tiles in shared memory, K-major (SWIZZLE_128B slabs of 64 columns).
+template <int HD>
+__device__ __forceinline__ void issue_nt(uint32_t tcol, uint32_t a, uint32_t b) {
+    using C = BCfg<HD>;
+    constexpr uint32_t ID = idesc_bf16(kT, kT, false);
+#pragma unroll
     for (int kk = 0; kk < HD / 16; ++kk) {
         const uint32_t off = (kk >> 2) * C::SLAB_BYTES + (kk & 3) * 32;
-        mma_ss(tmem + 128 * u, sdesc_sw128(fa + off, 16, 1024), sdesc_sw128(sa + half + off, 16, 1024), ID,
-               kk > 0);
-        mma_ss(tmem + 128 * u + 64, sdesc_sw128(fb + off, 16, 1024),
-               sdesc_sw128(sb + half + off, 16, 1024), ID, kk > 0);
+        mma_ss(tcol, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(b + off, 16, 1024), ID, kk > 0);
     }
 }
 
-// acc += X_u B_u where X_u (bf16, 128 x 64) sits in tensor memory at column xcol and B_u
-// is rows 64u.. of a streamed tile read as an MN-major operand (K = 64, N = HD).
+// acc += X B over K = 128: X (bf16, 128 x 128) in tensor memory at column xcol (64 packed
+// columns), B a 128-row tile in shared memory read as an MN-major operand (N = HD).
 template <int HD>
-__device__ __forceinline__ void issue_acc(uint32_t tmem, uint32_t acc_col, uint32_t xcol, uint32_t bsrc, int u,
-                                          bool accumulate) {
+__device__ __forceinline__ void issue_tn(uint32_t acc, uint32_t xcol, uint32_t bsrc, bool accumulate) {
     using C = BCfg<HD>;
     constexpr uint32_t ID = idesc_bf16(kT, HD, true);
-    for (int kk = 0; kk < kSub / 16; ++kk)
-        mma_ts(tmem + acc_col, tmem + xcol + kk * 8,
-               sdesc_sw128(bsrc + u * kSub * 128 + kk * 16 * 128, C::SLAB_BYTES, 1024), ID,
+#pragma unroll
+    for (int kk = 0; kk < kT / 16; ++kk)
+        mma_ts(acc, xcol + kk * 8, sdesc_sw128(bsrc + kk * 16 * 128, C::SLAB_BYTES, 1024), ID,
                (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// Tensor-memory slots of tile g in the dQ kernel's rotation.
+__device__ __forceinline__ uint32_t s_slot(uint32_t g) {
+    const uint32_t r = g % 3u;
+    return r == 0 ? 0u : (r == 1 ? 256u : 128u);
+}
+__device__ __forceinline__ uint32_t d_slot(uint32_t g) {
+    const uint32_t r = g % 3u;
+    return r == 0 ? 128u : (r == 1 ? 0u : 256u);
+}
+
+// Invisible entries of 32 scores become -inf (P = 0, dS = 0): e < lo or e >= hi.
+__device__ __forceinline__ void mask32(uint32_t (&v)[32], int lo, int hi) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = (e >= lo && e < hi) ? v[e] : kNegInfBits;
 }
 
 // 32 columns of one gradient row: mul * the step's value, plus the running value of earlier
@@ -311,6 +392,26 @@ __device__ __forceinline__ void store_grad_chunk(__nv_bfloat16 *dst, float *acc,
 
 // ---------------------------------------------------------------- dQ kernel
 
+// Element-wise work of one tile in the dQ kernel for this warp's 64 columns: P from the
+// S registers (already masked), then dS = P (dP - D) chunk by chunk into the dP slot.
+// FIRST is the chunk (0: columns 0-31 of the group, 1: 32-63) processed first.
+template <int FIRST>
+__device__ __forceinline__ void dq_tile_ew(uint32_t (&sv)[64], uint32_t tD, int grp, float d_r) {
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+        const int c = cc == 0 ? FIRST : 1 - FIRST;
+        uint32_t dp[32];
+        tmem_ld32(tD + grp * 64 + c * 32, dp);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+            pk[e / 2] = pack_bf16x2(__uint_as_float(sv[c * 32 + e]) * (__uint_as_float(dp[e]) - d_r),
+                                    __uint_as_float(sv[c * 32 + e + 1]) * (__uint_as_float(dp[e + 1]) - d_r));
+        tmem_st16(tD + 32 + 32 * grp + 16 * c, pk);
+    }
+}
+
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -322,15 +423,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *base_ptr = smem_raw + (base - raw);
     const uint32_t sQ = base, sDo = base + C::TILE_BYTES;
-    const uint32_t sSt = base + 2 * C::TILE_BYTES;  // stages of (K, V)
-    BBars *bars = reinterpret_cast<BBars *>(base_ptr + C::BAR_OFF);
+    const uint32_t sK = base + 2 * C::TILE_BYTES;               // ring of K tiles
+    const uint32_t sV = base + (2 + C::KST) * C::TILE_BYTES;    // ring of V tiles
+    BBars *bars = reinterpret_cast<BBars *>(base_ptr + C::BAR_OFF_DQ);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if ((int)blockIdx.x >= total) return;
     volatile int32_t *abort_flag = &bars->abort;
     const int tps = (P.flen + kT - 1) / kT;
     const float sl2 = P.scale_log2;
 
-    if (threadIdx.x == 0) bwd_init(bars, C::NST);
+    if (threadIdx.x == 0) bwd_init(bars, 4);
     if (warp == 1) tmem_alloc(smem_u32(&bars->tmem_base), C::TM_COLS);
     tc_fence_before();
     __syncthreads();
@@ -343,8 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_do);
-            int slot = 0;
-            uint32_t ph = 0, fcnt = 0, issued = 0, last_ph = 0;
+            Ring kr = {0, 0u, 0u, 0u}, vr = {0, 0u, 0u, 0u};
+            uint32_t fcnt = 0;
             bool ok = true;
             for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, tile of the pair)
                 const int L = snake(k2 >> 1);
@@ -359,22 +461,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                     q_tile(S, it, t, row, klim);
                     head = hk;
                 };
-                ok = produce_item<HD>(bars, sQ, sSt, slot, ph, fcnt, issued, last_ph, &tm_q, &tm_do, it.r_lo,
-                                      S.f_rank, it.h, &tm_k, &tm_v, S.s_rank, it.n, it.b, coords, abort_flag,
-                                      limit, err);
+                ok = produce_item_kv<HD>(bars, sQ, sK, sV, kr, vr, fcnt, &tm_q, &tm_do, it.r_lo, S.f_rank, it.h,
+                                         &tm_k, &tm_v, S.s_rank, it.n, it.b, coords, abort_flag, limit, err);
             }
             if (!ok) {
                 if (fcnt) wait_phase_drain(smem_u32(&bars->fix_full), (fcnt - 1u) & 1u);
-                for (int s2 = 0; s2 < C::NST; ++s2)
-                    if (issued & (1u << s2)) wait_phase_drain(smem_u32(&bars->full[s2]), (last_ph >> s2) & 1u);
+                for (int s2 = 0; s2 < C::KST; ++s2)
+                    if (kr.issued & (1u << s2)) wait_phase_drain(smem_u32(&bars->full[s2]), (kr.last_ph >> s2) & 1u);
+                for (int s2 = 0; s2 < C::VST; ++s2)
+                    if (vr.issued & (1u << s2))
+                        wait_phase_drain(smem_u32(&bars->fullv[s2]), (vr.last_ph >> s2) & 1u);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            int slot = 0;
-            uint32_t ph = 0, fcnt = 0, pc[2] = {0u, 0u};
+            Ring kr = {0, 0u, 0u, 0u}, vr = {0, 0u, 0u, 0u};
+            uint32_t fcnt = 0, g = 0;
             bool ok = true;
-            for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, tile of the pair)
+            // the dQ product of the previous tile, issued once its dS is in tensor memory
+            bool pend = false, pend_acc = false, pend_last = false;
+            int pend_slot = 0;
+            uint32_t pend_g = 0;
+            auto flush = [&]() -> bool {
+                if (!wait_count(&bars->p_count[1], (uint32_t)kEwWarps * (pend_g + 1u), abort_flag, limit, err))
+                    return false;
+                tc_fence_after();
+                issue_tn<HD>(tmem + C::TM_DQ, tmem + d_slot(pend_g) + 32, sK + pend_slot * C::TILE_BYTES,
+                             pend_acc);  // dQ += dS K
+                mma_commit(smem_u32(&bars->empty[pend_slot]));  // the K tile is free
+                if (pend_last) mma_commit(smem_u32(&bars->o_full));
+                pend = false;
+                return true;
+            };
+            for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {
                 const int L = snake(k2 >> 1);
                 if (L >= total) continue;
                 QItem it;
@@ -383,59 +502,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (n == 0) continue;
                 ok = wait_phase(smem_u32(&bars->fix_full), fcnt & 1u, abort_flag, limit, err);
                 ++fcnt;
-                if (!ok) break;
-                // S / dP of both halves of key tile 0
-                ok = wait_phase(smem_u32(&bars->full[slot]), ph, abort_flag, limit, err);
-                if (!ok) break;
-                tc_fence_after();
-                for (int u = 0; u < 2; ++u) {
-                    const uint32_t kb = sSt + (2 * slot) * C::TILE_BYTES;
-                    issue_sdp<HD>(tmem, u, sQ, sDo, kb, kb + C::TILE_BYTES);
-                    mma_commit(smem_u32(&bars->s_full[u]));
-                }
-                if (n == 1) mma_commit(smem_u32(&bars->fix_empty));
-                for (int t = 0; ok && t < n; ++t) {
-                    const int cur = slot;
-                    const uint32_t kb = sSt + (2 * cur) * C::TILE_BYTES;
-                    int nslot = slot + 1;
-                    uint32_t nph = ph;
-                    if (nslot == C::NST) {
-                        nslot = 0;
-                        nph ^= 1u;
-                    }
-                    for (int u = 0; u < 2 && ok; ++u) {
-                        ++pc[u];
-                        ok = wait_count(&bars->p_count[u], (uint32_t)kEwWarps * pc[u], abort_flag, limit, err);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_acc<HD>(tmem, C::TM_A0, 128 * u + 80, kb, u, t > 0 || u > 0);  // dQ += dS_u K_u
-                        if (t + 1 < n) {
-                            if (u == 0) {
-                                ok = wait_phase(smem_u32(&bars->full[nslot]), nph, abort_flag, limit, err);
-                                if (!ok) break;
-                                tc_fence_after();
-                            }
-                            const uint32_t nb = sSt + (2 * nslot) * C::TILE_BYTES;
-                            issue_sdp<HD>(tmem, u, sQ, sDo, nb, nb + C::TILE_BYTES);
-                            mma_commit(smem_u32(&bars->s_full[u]));
-                            if (u == 1 && t + 2 == n) mma_commit(smem_u32(&bars->fix_empty));
-                        }
-                    }
+                for (int t = 0; ok && t < n; ++t, ++g) {
+                    ok = wait_phase(smem_u32(&bars->full[kr.slot]), kr.ph, abort_flag, limit, err);
                     if (!ok) break;
-                    mma_commit(smem_u32(&bars->empty[cur]));
-                    if (t == n - 1) mma_commit(smem_u32(&bars->o_full));
-                    slot = nslot;
-                    ph = nph;
+                    tc_fence_after();
+                    issue_nt<HD>(tmem + s_slot(g), sQ, sK + kr.slot * C::TILE_BYTES);  // S = Q K^T
+                    if (g > 0) {  // this tile's dP goes where the previous tile's S was read from
+                        ok = wait_count(&bars->p_count[0], (uint32_t)kEwWarps * g, abort_flag, limit, err);
+                        if (!ok) break;
+                    }
+                    ok = wait_phase(smem_u32(&bars->fullv[vr.slot]), vr.ph, abort_flag, limit, err);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_nt<HD>(tmem + d_slot(g), sDo, sV + vr.slot * C::TILE_BYTES);  // dP = dO V^T
+                    mma_commit(smem_u32(&bars->s_full[0]));
+                    mma_commit(smem_u32(&bars->emptyv[vr.slot]));  // the V tile is free
+                    vr.advance<C::VST>();
+                    if (t == n - 1) mma_commit(smem_u32(&bars->fix_empty));
+                    if (pend && !(ok = flush())) break;
+                    pend = true;
+                    pend_acc = t > 0;
+                    pend_last = t == n - 1;
+                    pend_slot = kr.slot;
+                    pend_g = g;
+                    kr.advance<C::KST>();
                 }
             }
+            if (ok && pend) ok = flush();
             mma_commit(smem_u32(&bars->drain));
             wait_phase_drain(smem_u32(&bars->drain), 0);
         }
     } else if (warp >= 4) {
         const int quarter = warp & 3;
-        const int grp = (warp - 4) >> 2;  // which 32 columns of a sub-tile this warp owns
+        const int grp = (warp - 4) >> 2;  // which 64 columns of a tile this warp owns
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        uint32_t sc[2] = {0u, 0u}, ocnt = 0;
+        uint32_t g = 0, icnt = 0;
         bool ok = true;
         for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, tile of the pair)
             const int L = snake(k2 >> 1);
@@ -454,49 +555,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (valid && grp == 0 && !(S.flags & SEG_FIRST))
                 for (int i = 0; i < HD * 4; i += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(
                                                           reinterpret_cast<const char *>(accp) + i));
-            for (int t = 0; t < n && ok; ++t) {
+            for (int t = 0; t < n && ok; ++t, ++g) {
                 int kt0, klim;
                 q_tile(S, it, t, kt0, klim);
-                for (int u = 0; u < 2; ++u) {
-                    ok = wait_phase(smem_u32(&bars->s_full[u]), sc[u] & 1u, abort_flag, limit, err);
-                    ++sc[u];
-                    if (!ok) break;
-                    tc_fence_after();
-                    const int k0 = kt0 + u * kSub + grp * 32;  // first key of this warp's columns
-                    const bool mask = (k0 + 32 > klim) || (P.causal && k0 + 31 + diag > row) || !valid;
-                    uint32_t pk[16];
-                    {
-                        uint32_t s[32], dp[32];
-                        tmem_ld32(tmem + 128 * u + lane_off + grp * 32, s);
-                        tmem_ld32(tmem + 128 * u + 64 + lane_off + grp * 32, dp);
-                        tmem_ld_wait();
-                        // invisible scores become -inf (P = 0, dS = 0) in a pass of their own,
-                        // so the loop below has no branch and its iterations interleave
-                        if (mask) {
-                            const int lim = !valid ? 0 : (P.causal ? min(klim, row + 1 - diag) : klim) - k0;
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) s[e] = e < lim ? s[e] : kNegInfBits;
-                        }
-#pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            const float p0 = ex2(fmaf(__uint_as_float(s[e]), sl2, -lse_l2));
-                            const float p1 = ex2(fmaf(__uint_as_float(s[e + 1]), sl2, -lse_l2));
-                            pk[e / 2] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - d_r),
-                                                    p1 * (__uint_as_float(dp[e + 1]) - d_r));
-                        }
-                    }
-                    // this warp's half of dS_u, inside the dP_u columns it has read
-                    tmem_st16(tmem + 128 * u + 80 + 16 * grp + lane_off, pk);
-                    tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) count_release_add(&bars->p_count[u]);
+                ok = wait_phase(smem_u32(&bars->s_full[0]), g & 1u, abort_flag, limit, err);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t tS = tmem + s_slot(g) + lane_off, tD = tmem + d_slot(g) + lane_off;
+                uint32_t sv[64];
+                tmem_ld32(tS + grp * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+                tmem_ld32(tS + grp * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+                tmem_ld_wait();
+                // S is in registers: its slot may take the next tile's dP
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) count_release_add(&bars->p_count[0]);
+                const int k0 = kt0 + grp * 64;  // first key of this warp's columns
+                if ((k0 + 64 > klim) || (P.causal && k0 + 63 + diag > row) || !valid) {
+                    const int hi = !valid ? 0 : (P.causal ? min(klim, row + 1 - diag) : klim) - k0;
+                    mask32(*reinterpret_cast<uint32_t(*)[32]>(&sv[0]), 0, hi);
+                    mask32(*reinterpret_cast<uint32_t(*)[32]>(&sv[32]), 0, hi - 32);
                 }
+#pragma unroll
+                for (int e = 0; e < 64; e += 2) {
+                    const uint64_t x = ffma2(pack_f32x2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                             pack_f32x2(sl2, sl2), pack_f32x2(-lse_l2, -lse_l2));
+                    float x0, x1;
+                    unpack_f32x2(x, x0, x1);
+                    sv[e] = __float_as_uint(ex2(x0));
+                    sv[e + 1] = __float_as_uint(ex2(x1));
+                }
+                if (grp == 0)
+                    dq_tile_ew<1>(sv, tD, 0, d_r);
+                else
+                    dq_tile_ew<0>(sv, tD, 1, d_r);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) count_release_add(&bars->p_count[1]);
             }
             if (!ok) break;
             if (n > 0) {
-                ok = wait_phase(smem_u32(&bars->o_full), ocnt & 1u, abort_flag, limit, err);
-                ++ocnt;
+                ok = wait_phase(smem_u32(&bars->o_full), icnt & 1u, abort_flag, limit, err);
+                ++icnt;
                 if (!ok) break;
                 tc_fence_after();
             }
@@ -505,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = grp * (HD / 64); c < (grp + 1) * (HD / 64); ++c) {  // this group's columns
                 uint32_t o[32];
                 if (n > 0) {
-                    tmem_ld32(tmem + C::TM_A0 + lane_off + c * 32, o);
+                    tmem_ld32(tmem + C::TM_DQ + lane_off + c * 32, o);
                     tmem_ld_wait();
                 } else {
 #pragma unroll
@@ -524,6 +625,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- dK / dV kernel
 
+// Pack 64 fp32 values (this warp's columns) to bf16 into the 32 packed columns at
+// 32 + 32 * grp of the slot at t, the chunk FIRST first (see the tensor-memory layout).
+template <int FIRST>
+__device__ __forceinline__ void pack_store64(const uint32_t (&v)[64], uint32_t t, int grp) {
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+        const int c = cc == 0 ? FIRST : 1 - FIRST;
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+            pk[e / 2] = pack_bf16x2(__uint_as_float(v[c * 32 + e]), __uint_as_float(v[c * 32 + e + 1]));
+        tmem_st16(t + 32 + 32 * grp + 16 * c, pk);
+    }
+}
+
+// dS = P (dP - D) for this warp's 64 columns, chunk by chunk from the dP slot at tD, into
+// the packed columns of that slot, the chunk FIRST first.
+template <int FIRST>
+__device__ __forceinline__ void ds_tile_ew(const uint32_t (&pv)[64], uint32_t tD, int grp, const float *du) {
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+        const int c = cc == 0 ? FIRST : 1 - FIRST;
+        uint32_t dp[32];
+        tmem_ld32(tD + grp * 64 + c * 32, dp);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+            pk[e / 2] = pack_bf16x2(__uint_as_float(pv[c * 32 + e]) * (__uint_as_float(dp[e]) - du[c * 32 + e]),
+                                    __uint_as_float(pv[c * 32 + e + 1]) *
+                                        (__uint_as_float(dp[e + 1]) - du[c * 32 + e + 1]));
+        tmem_st16(tD + 32 + 32 * grp + 16 * c, pk);
+    }
+}
+
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -537,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sK = base, sV = base + C::TILE_BYTES;
     const uint32_t sSt = base + 2 * C::TILE_BYTES;  // stages of (Q, dO)
     BBars *bars = reinterpret_cast<BBars *>(base_ptr + C::BAR_OFF);
-    // per element-wise warp: the current query tile's LSE (log2 units) and D values
+    // per element-wise warp: the current query tile's LSE (log2 units) and D values of its columns
     float *s_stage = reinterpret_cast<float *>(base_ptr + C::BAR_OFF + 256);  // [8 warps][2][64]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if ((int)blockIdx.x >= total) return;
@@ -588,9 +724,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             int slot = 0;
-            uint32_t ph = 0, fcnt = 0, pc[2] = {0u, 0u};
+            uint32_t ph = 0, fcnt = 0, g = 0;
             bool ok = true;
-            for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, tile of the pair)
+            for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {
                 const int L = snake(k2 >> 1);
                 if (L >= total) continue;
                 KItem it;
@@ -599,50 +735,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (n == 0) continue;
                 ok = wait_phase(smem_u32(&bars->fix_full), fcnt & 1u, abort_flag, limit, err);
                 ++fcnt;
-                if (!ok) break;
-                ok = wait_phase(smem_u32(&bars->full[slot]), ph, abort_flag, limit, err);
-                if (!ok) break;
-                tc_fence_after();
-                for (int u = 0; u < 2; ++u) {
-                    const uint32_t qb = sSt + (2 * slot) * C::TILE_BYTES;
-                    issue_sdp<HD>(tmem, u, sK, sV, qb, qb + C::TILE_BYTES);  // S^T_u, dP^T_u
-                    mma_commit(smem_u32(&bars->s_full[u]));
-                }
-                if (n == 1) mma_commit(smem_u32(&bars->fix_empty));
-                for (int t = 0; ok && t < n; ++t) {
-                    const int cur = slot;
-                    const uint32_t qb = sSt + (2 * cur) * C::TILE_BYTES;
-                    int nslot = slot + 1;
-                    uint32_t nph = ph;
-                    if (nslot == C::NST) {
-                        nslot = 0;
-                        nph ^= 1u;
-                    }
-                    for (int u = 0; u < 2 && ok; ++u) {
-                        ++pc[u];
-                        ok = wait_count(&bars->p_count[u], (uint32_t)kEwWarps * pc[u], abort_flag, limit, err);
-                        if (!ok) break;
-                        tc_fence_after();
-                        const bool accum = t > 0 || u > 0;
-                        issue_acc<HD>(tmem, C::TM_A0, 128 * u + 16, qb + C::TILE_BYTES, u, accum);  // dV += P^T_u dO_u
-                        issue_acc<HD>(tmem, C::TM_A1, 128 * u + 80, qb, u, accum);                  // dK += dS^T_u Q_u
-                        if (t + 1 < n) {
-                            if (u == 0) {
-                                ok = wait_phase(smem_u32(&bars->full[nslot]), nph, abort_flag, limit, err);
-                                if (!ok) break;
-                                tc_fence_after();
-                            }
-                            const uint32_t nb = sSt + (2 * nslot) * C::TILE_BYTES;
-                            issue_sdp<HD>(tmem, u, sK, sV, nb, nb + C::TILE_BYTES);
-                            mma_commit(smem_u32(&bars->s_full[u]));
-                            if (u == 1 && t + 2 == n) mma_commit(smem_u32(&bars->fix_empty));
-                        }
-                    }
+                for (int t = 0; ok && t < n; ++t, ++g) {
+                    ok = wait_phase(smem_u32(&bars->full[slot]), ph, abort_flag, limit, err);
                     if (!ok) break;
-                    mma_commit(smem_u32(&bars->empty[cur]));
+                    tc_fence_after();
+                    const uint32_t qb = sSt + (2 * slot) * C::TILE_BYTES;
+                    // S^T and dP^T overwrite the previous tile's P^T and dS^T, which the dV
+                    // and dK products issued before have read (they run in order)
+                    issue_nt<HD>(tmem + 0, sK, qb);  // S^T = K Q^T
+                    mma_commit(smem_u32(&bars->s_full[0]));
+                    issue_nt<HD>(tmem + 128, sV, qb + C::TILE_BYTES);  // dP^T = V dO^T
+                    mma_commit(smem_u32(&bars->s_full[1]));
+                    if (t == n - 1) mma_commit(smem_u32(&bars->fix_empty));
+                    ok = wait_count(&bars->p_count[0], (uint32_t)kEwWarps * (g + 1u), abort_flag, limit, err);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_tn<HD>(tmem + C::TM_A0, tmem + 0 + 32, qb + C::TILE_BYTES, t > 0);  // dV += P^T dO
+                    ok = wait_count(&bars->p_count[1], (uint32_t)kEwWarps * (g + 1u), abort_flag, limit, err);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_tn<HD>(tmem + C::TM_A1, tmem + 128 + 32, qb, t > 0);  // dK += dS^T Q
+                    mma_commit(smem_u32(&bars->empty[slot]));
                     if (t == n - 1) mma_commit(smem_u32(&bars->o_full));
-                    slot = nslot;
-                    ph = nph;
+                    if (++slot == C::NST) {
+                        slot = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
             mma_commit(smem_u32(&bars->drain));
@@ -650,11 +768,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= 4) {
         const int quarter = warp & 3;
-        const int grp = (warp - 4) >> 2;  // which 32 columns of a sub-tile this warp owns
+        const int grp = (warp - 4) >> 2;  // which 64 columns of a tile this warp owns
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         float *lb = s_stage + (warp - 4) * 2 * 64;  // this warp's columns only: no cross-warp barrier
         float *db = lb + 64;
-        uint32_t sc[2] = {0u, 0u}, ocnt = 0;
+        uint32_t g = 0, icnt = 0;
         bool ok = true;
         for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, tile of the pair)
             const int L = snake(k2 >> 1);
@@ -672,63 +790,67 @@ __global__ void __launch_bounds__(kThreads, 1)
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(P.acc_k + arow) + i));
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(P.acc_v + arow) + i));
                 }
-            for (int t = 0; t < n && ok; ++t) {
-                int q0, qlim, g;
-                kv_tile(S, it, G, t, q0, qlim, g);
-                const int h = it.hk * G + g;
+            for (int t = 0; t < n && ok; ++t, ++g) {
+                int q0, qlim, gh;
+                kv_tile(S, it, G, t, q0, qlim, gh);
+                const int h = it.hk * G + gh;
+                const int qa = q0 + grp * 64;  // first query of this warp's columns
                 __syncwarp();  // every lane is done with the previous tile's values
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {  // the queries of this warp's columns of both halves
-                    const int qme = q0 + r * kSub + grp * 32 + lane;
+                for (int r = 0; r < 2; ++r) {
+                    const int qme = qa + r * 32 + lane;
                     const int64_t li = ((int64_t)it.b * P.Hq + h) * P.N + (int64_t)qme * P.rs + S.s_rank;
                     lb[r * 32 + lane] = qme < qlim ? P.lse[li] * kLog2e : 0.f;
                     db[r * 32 + lane] = qme < qlim ? P.dvec[li] : 0.f;
                 }
                 __syncwarp();
-                for (int u = 0; u < 2; ++u) {
-                    ok = wait_phase(smem_u32(&bars->s_full[u]), sc[u] & 1u, abort_flag, limit, err);
-                    ++sc[u];
-                    if (!ok) break;
-                    tc_fence_after();
-                    const int qa = q0 + u * kSub + grp * 32;  // first query of this warp's columns
-                    const bool mask = (qa + 32 > qlim) || (P.causal && it.c_hi - 1 + diag > qa);
-                    uint32_t pp[16], pd[16];
-                    {
-                        uint32_t s[32], dp[32];
-                        tmem_ld32(tmem + 128 * u + lane_off + grp * 32, s);
-                        tmem_ld32(tmem + 128 * u + 64 + lane_off + grp * 32, dp);
-                        tmem_ld_wait();
-                        const float *lu = lb + u * 32, *du = db + u * 32;
-                        // invisible scores become -inf (P = 0, dS = 0) in a pass of their own,
-                        // so the loop below has no branch and its iterations interleave
-                        if (mask) {
-                            const int lo = P.causal ? key + diag - qa : 0;  // first visible offset
-                            const int hi = qlim - qa;                       // end of the range
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) s[e] = (e >= lo && e < hi) ? s[e] : kNegInfBits;
-                        }
-#pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            const float p0 = ex2(fmaf(__uint_as_float(s[e]), sl2, -lu[e]));
-                            const float p1 = ex2(fmaf(__uint_as_float(s[e + 1]), sl2, -lu[e + 1]));
-                            pp[e / 2] = pack_bf16x2(p0, p1);
-                            pd[e / 2] = pack_bf16x2(p0 * (__uint_as_float(dp[e]) - du[e]),
-                                                    p1 * (__uint_as_float(dp[e + 1]) - du[e + 1]));
-                        }
-                    }
-                    // this warp's halves of P_u and dS_u, inside the columns it has read
-                    tmem_st16(tmem + 128 * u + 16 + 16 * grp + lane_off, pp);
-                    tmem_st16(tmem + 128 * u + 80 + 16 * grp + lane_off, pd);
-                    tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) count_release_add(&bars->p_count[u]);
+                ok = wait_phase(smem_u32(&bars->s_full[0]), g & 1u, abort_flag, limit, err);
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t pv[64];
+                tmem_ld32(tmem + lane_off + grp * 64, *reinterpret_cast<uint32_t(*)[32]>(&pv[0]));
+                tmem_ld32(tmem + lane_off + grp * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&pv[32]));
+                tmem_ld_wait();
+                if ((qa + 64 > qlim) || (P.causal && it.c_hi - 1 + diag > qa)) {
+                    const int lo = P.causal ? key + diag - qa : 0;  // first visible column
+                    const int hi = qlim - qa;
+                    mask32(*reinterpret_cast<uint32_t(*)[32]>(&pv[0]), lo, hi);
+                    mask32(*reinterpret_cast<uint32_t(*)[32]>(&pv[32]), lo - 32, hi - 32);
                 }
+#pragma unroll
+                for (int e = 0; e < 64; e += 2) {
+                    const uint64_t x = ffma2(pack_f32x2(__uint_as_float(pv[e]), __uint_as_float(pv[e + 1])),
+                                             pack_f32x2(sl2, sl2), pack_f32x2(-lb[e], -lb[e + 1]));
+                    float x0, x1;
+                    unpack_f32x2(x, x0, x1);
+                    pv[e] = __float_as_uint(ex2(x0));
+                    pv[e + 1] = __float_as_uint(ex2(x1));
+                }
+                const uint32_t tSl = tmem + lane_off, tDl = tmem + 128 + lane_off;
+                if (grp == 0)
+                    pack_store64<1>(pv, tSl, 0);
+                else
+                    pack_store64<0>(pv, tSl, 1);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) count_release_add(&bars->p_count[0]);  // P^T is in tensor memory
+                ok = wait_phase(smem_u32(&bars->s_full[1]), g & 1u, abort_flag, limit, err);
+                if (!ok) break;
+                tc_fence_after();
+                if (grp == 0)
+                    ds_tile_ew<1>(pv, tDl, 0, db);
+                else
+                    ds_tile_ew<0>(pv, tDl, 1, db);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) count_release_add(&bars->p_count[1]);  // dS^T is in tensor memory
             }
             if (!ok) break;
             if (n > 0) {
-                ok = wait_phase(smem_u32(&bars->o_full), ocnt & 1u, abort_flag, limit, err);
-                ++ocnt;
+                ok = wait_phase(smem_u32(&bars->o_full), icnt & 1u, abort_flag, limit, err);
+                ++icnt;
                 if (!ok) break;
                 tc_fence_after();
             }
@@ -773,7 +895,7 @@ static cudaError_t launch_bwd_tc_hd(const BwdParams &P, int parts, int num_sms, 
     cudaGetDevice(&dev);
     if (!(configured_mask & (1 << (dev & 31)))) {
         cudaError_t e = cudaFuncSetAttribute(tcb::bwd_dq_tc_kernel<HD>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES_DQ);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(tcb::bwd_dkdv_tc_kernel<HD>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -790,7 +912,8 @@ static cudaError_t launch_bwd_tc_hd(const BwdParams &P, int parts, int num_sms, 
     const int64_t tq = (int64_t)P.B * P.Hq * P.nseg * np, tkv = (int64_t)P.B * P.Hkv * P.nseg * np;
     if (tq > 0x7fffffff || tkv > 0x7fffffff) return cudaErrorInvalidValue;
     if (parts & 1) {
-        tcb::bwd_dq_tc_kernel<HD><<<(int)std::min<int64_t>(tq, num_sms), tcb::kThreads, C::SMEM_BYTES, stream>>>(
+        tcb::bwd_dq_tc_kernel<HD><<<(int)std::min<int64_t>(tq, num_sms), tcb::kThreads, C::SMEM_BYTES_DQ,
+                                    stream>>>(
             mq, mk, mv, mdo, P, (int)tq, wait_ns, err);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
