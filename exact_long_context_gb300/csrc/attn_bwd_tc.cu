@@ -735,32 +735,63 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (n == 0) continue;
                 ok = wait_phase(smem_u32(&bars->fix_full), fcnt & 1u, abort_flag, limit, err);
                 ++fcnt;
-                for (int t = 0; ok && t < n; ++t, ++g) {
-                    ok = wait_phase(smem_u32(&bars->full[slot]), ph, abort_flag, limit, err);
-                    if (!ok) break;
+                if (!ok) break;
+                // Order of the products, tile t: ... dV(t), S^T(t+1), dK(t), dP^T(t+1), dV(t+1) ...
+                // S^T(t+1) overwrites P^T(t), read by dV(t) before it; dP^T(t+1) overwrites
+                // dS^T(t), read by dK(t) before it (tcgen05 MMAs of a thread run in order).
+                // So the next tile's S^T is computed while the element-wise warps work on
+                // this tile's dS^T, and its dP^T while they work on its P^T.
+                auto load_wait = [&]() -> bool {
+                    if (!wait_phase(smem_u32(&bars->full[slot]), ph, abort_flag, limit, err)) return false;
                     tc_fence_after();
+                    return true;
+                };
+                int nslot = slot;
+                uint32_t nph = ph;
+                auto next_stage = [&]() {
+                    if (++nslot == C::NST) {
+                        nslot = 0;
+                        nph ^= 1u;
+                    }
+                };
+                if (!(ok = load_wait())) break;
+                issue_nt<HD>(tmem + 0, sK, sSt + (2 * slot) * C::TILE_BYTES);  // S^T(0) = K Q^T
+                mma_commit(smem_u32(&bars->s_full[0]));
+                issue_nt<HD>(tmem + 128, sV, sSt + (2 * slot) * C::TILE_BYTES + C::TILE_BYTES);  // dP^T(0)
+                mma_commit(smem_u32(&bars->s_full[1]));
+                if (n == 1) mma_commit(smem_u32(&bars->fix_empty));
+                for (int t = 0; ok && t < n; ++t, ++g) {
                     const uint32_t qb = sSt + (2 * slot) * C::TILE_BYTES;
-                    // S^T and dP^T overwrite the previous tile's P^T and dS^T, which the dV
-                    // and dK products issued before have read (they run in order)
-                    issue_nt<HD>(tmem + 0, sK, qb);  // S^T = K Q^T
-                    mma_commit(smem_u32(&bars->s_full[0]));
-                    issue_nt<HD>(tmem + 128, sV, qb + C::TILE_BYTES);  // dP^T = V dO^T
-                    mma_commit(smem_u32(&bars->s_full[1]));
-                    if (t == n - 1) mma_commit(smem_u32(&bars->fix_empty));
                     ok = wait_count(&bars->p_count[0], (uint32_t)kEwWarps * (g + 1u), abort_flag, limit, err);
                     if (!ok) break;
                     tc_fence_after();
                     issue_tn<HD>(tmem + C::TM_A0, tmem + 0 + 32, qb + C::TILE_BYTES, t > 0);  // dV += P^T dO
+                    nslot = slot;
+                    nph = ph;
+                    next_stage();
+                    const uint32_t nb = sSt + (2 * nslot) * C::TILE_BYTES;
+                    if (t + 1 < n) {
+                        if (!wait_phase(smem_u32(&bars->full[nslot]), nph, abort_flag, limit, err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_nt<HD>(tmem + 0, sK, nb);  // S^T(t+1)
+                        mma_commit(smem_u32(&bars->s_full[0]));
+                    }
                     ok = wait_count(&bars->p_count[1], (uint32_t)kEwWarps * (g + 1u), abort_flag, limit, err);
                     if (!ok) break;
                     tc_fence_after();
                     issue_tn<HD>(tmem + C::TM_A1, tmem + 128 + 32, qb, t > 0);  // dK += dS^T Q
                     mma_commit(smem_u32(&bars->empty[slot]));
                     if (t == n - 1) mma_commit(smem_u32(&bars->o_full));
-                    if (++slot == C::NST) {
-                        slot = 0;
-                        ph ^= 1u;
+                    if (t + 1 < n) {
+                        issue_nt<HD>(tmem + 128, sV, nb + C::TILE_BYTES);  // dP^T(t+1)
+                        mma_commit(smem_u32(&bars->s_full[1]));
+                        if (t + 2 == n) mma_commit(smem_u32(&bars->fix_empty));
                     }
+                    slot = nslot;
+                    ph = nph;
                 }
             }
             mma_commit(smem_u32(&bars->drain));
@@ -790,20 +821,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(P.acc_k + arow) + i));
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(P.acc_v + arow) + i));
                 }
-            for (int t = 0; t < n && ok; ++t, ++g) {
+            // LSE (log2 units) and D of this lane's two queries of tile t; the next tile's
+            // are loaded while this one is processed, so their latency is hidden
+            auto fetch = [&](int t, float (&l)[2], float (&d)[2]) {
                 int q0, qlim, gh;
                 kv_tile(S, it, G, t, q0, qlim, gh);
                 const int h = it.hk * G + gh;
-                const int qa = q0 + grp * 64;  // first query of this warp's columns
-                __syncwarp();  // every lane is done with the previous tile's values
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const int qme = qa + r * 32 + lane;
+                    const int qme = q0 + grp * 64 + r * 32 + lane;
                     const int64_t li = ((int64_t)it.b * P.Hq + h) * P.N + (int64_t)qme * P.rs + S.s_rank;
-                    lb[r * 32 + lane] = qme < qlim ? P.lse[li] * kLog2e : 0.f;
-                    db[r * 32 + lane] = qme < qlim ? P.dvec[li] : 0.f;
+                    l[r] = qme < qlim ? P.lse[li] * kLog2e : 0.f;
+                    d[r] = qme < qlim ? P.dvec[li] : 0.f;
                 }
+            };
+            float nl[2] = {0.f, 0.f}, nd[2] = {0.f, 0.f};
+            if (n > 0) fetch(0, nl, nd);
+            for (int t = 0; t < n && ok; ++t, ++g) {
+                int q0, qlim, gh;
+                kv_tile(S, it, G, t, q0, qlim, gh);
+                const int qa = q0 + grp * 64;  // first query of this warp's columns
+                __syncwarp();  // every lane is done with the previous tile's values
+                lb[lane] = nl[0];
+                lb[32 + lane] = nl[1];
+                db[lane] = nd[0];
+                db[32 + lane] = nd[1];
                 __syncwarp();
+                if (t + 1 < n) fetch(t + 1, nl, nd);
                 ok = wait_phase(smem_u32(&bars->s_full[0]), g & 1u, abort_flag, limit, err);
                 if (!ok) break;
                 tc_fence_after();
