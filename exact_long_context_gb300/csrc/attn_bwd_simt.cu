@@ -58,6 +58,41 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const __grid_constant__
     }
 }
 
+// The same for bf16 rows of 16-byte multiples with 16-byte aligned starts: each lane
+// reads 8 elements of O and of dO per load; a warp covers 256 elements of a row per
+// pass (two rows of D = 128, four of D = 64), so every lane has work and the loads stay
+// coalesced.  HBM-bound: 4 D bytes read per row.
+__global__ void __launch_bounds__(256) bwd_rowdot_vec_kernel(const __grid_constant__ BwdParams P) {
+    const int lane = threadIdx.x & 31;
+    const int per_row = P.D / 8;                 // lanes per row (8 or 16)
+    const int rows_per_warp = 32 / per_row;      // 4 or 2
+    const int sub = lane / per_row, l = lane - sub * per_row;
+    const int64_t rows = (int64_t)P.B * P.Hq * P.N;
+    const int64_t wstride = (int64_t)gridDim.x * 8 * rows_per_warp;
+    for (int64_t row0 = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * rows_per_warp; row0 < rows;
+         row0 += wstride) {
+        const int64_t row = row0 + sub;
+        float acc = 0.f;
+        if (row < rows) {
+            const int64_t n = row % P.N, bh = row / P.N;
+            const int64_t h = bh % P.Hq, b = bh / P.Hq;
+            const uint4 x = __ldcs(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(P.o) + b * P.so[0] +
+                                                                 h * P.so[1] + n * P.so[2]) + l);
+            const uint4 y = __ldcs(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(P.dout) +
+                                                                 b * P.sdo[0] + h * P.sdo[1] + n * P.sdo[2]) + l);
+            const uint32_t xa[4] = {x.x, x.y, x.z, x.w}, ya[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc = fmaf(__uint_as_float(xa[i] << 16), __uint_as_float(ya[i] << 16), acc);
+                acc = fmaf(__uint_as_float(xa[i] & 0xffff0000u), __uint_as_float(ya[i] & 0xffff0000u), acc);
+            }
+        }
+        // reduce within each row's group of lanes
+        for (int o = per_row >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (l == 0 && row < rows) P.dvec[row] = acc;
+    }
+}
+
 // A gradient element of a ring step: the step's value plus the running value of earlier
 // steps (unless the range is new this step), written to the gradient on the range's last
 // step and to the fp32 running buffer otherwise.
@@ -266,6 +301,15 @@ __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(const __grid_constant_
 cudaError_t launch_bwd_rowdot(const BwdParams &P, int num_sms, cudaStream_t stream) {
     if (P.B <= 0 || P.Hq <= 0 || P.N <= 0) return cudaSuccess;
     const int64_t rows = (int64_t)P.B * P.Hq * P.N;
+    const bool vec = P.bf16 && (P.D == 64 || P.D == 128) && P.so[0] % 8 == 0 && P.so[1] % 8 == 0 &&
+                     P.so[2] % 8 == 0 && P.sdo[0] % 8 == 0 && P.sdo[1] % 8 == 0 && P.sdo[2] % 8 == 0 &&
+                     reinterpret_cast<uintptr_t>(P.o) % 16 == 0 && reinterpret_cast<uintptr_t>(P.dout) % 16 == 0;
+    if (vec) {
+        const int64_t warps = (rows + (256 / P.D) * 8 - 1) / ((256 / P.D) * 8) * 8;  // warps needed
+        const int g = (int)std::min<int64_t>((warps + 7) / 8, (int64_t)num_sms * 16);
+        bwd_rowdot_vec_kernel<<<g, 256, 0, stream>>>(P);
+        return cudaGetLastError();
+    }
     const int g0 = (int)std::min<int64_t>((rows + 7) / 8, (int64_t)num_sms * 16);
     if (P.bf16)
         bwd_rowdot_kernel<true><<<g0, 256, 0, stream>>>(P);
