@@ -320,10 +320,11 @@ template <int HD>
 __device__ __forceinline__ void issue_nt(uint32_t tcol, uint32_t a, uint32_t b) {
     using C = BCfg<HD>;
     constexpr uint32_t ID = idesc_bf16(kT, kT, false);
+    const SDesc ad = sdesc_split(a, 16, 1024), bd = sdesc_split(b, 16, 1024);
 #pragma unroll
     for (int kk = 0; kk < HD / 16; ++kk) {
         const uint32_t off = (kk >> 2) * C::SLAB_BYTES + (kk & 3) * 32;
-        mma_ss(tcol, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(b + off, 16, 1024), ID, kk > 0);
+        mma_ss(tcol, ad.at(off), bd.at(off), ID, kk > 0);
     }
 }
 
@@ -333,10 +334,10 @@ template <int HD>
 __device__ __forceinline__ void issue_tn(uint32_t acc, uint32_t xcol, uint32_t bsrc, bool accumulate) {
     using C = BCfg<HD>;
     constexpr uint32_t ID = idesc_bf16(kT, HD, true);
+    const SDesc bd = sdesc_split(bsrc, C::SLAB_BYTES, 1024);
 #pragma unroll
     for (int kk = 0; kk < kT / 16; ++kk)
-        mma_ts(acc, xcol + kk * 8, sdesc_sw128(bsrc + kk * 16 * 128, C::SLAB_BYTES, 1024), ID,
-               (accumulate || kk > 0) ? 1u : 0u);
+        mma_ts(acc, xcol + kk * 8, bd.at(kk * 16 * 128), ID, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // Tensor-memory slots of tile g in the dQ kernel's rotation.

@@ -321,24 +321,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false);
             constexpr uint32_t IDESC_PV = idesc_bf16(BM, HD, true);
+            // descriptors of the two Q halves, built once; K and V ones once per stage
+            const SDesc qd0 = sdesc_split(sQ, 16, 1024), qd1 = sdesc_split(sQ + C::TILE_BYTES, 16, 1024);
             auto issue_qk = [=](int hh, uint32_t kb) {
                 const uint32_t d = tmem + (hh ? C::TM_S1 : C::TM_S0);
-                const uint32_t qa = sQ + hh * C::TILE_BYTES;
+                const SDesc qd = hh ? qd1 : qd0;
+                const SDesc kd = sdesc_split(kb, 16, 1024);
 #pragma unroll
                 for (int k = 0; k < HD / 16; ++k) {
                     const uint32_t off = (k >> 2) * C::SLAB_BYTES + (k & 3) * 32;
-                    mma_ss(d, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                           IDESC_QK, k > 0 ? 1u : 0u);
+                    mma_ss(d, qd.at(off), kd.at(off), IDESC_QK, k > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [=](int hh, uint32_t vb, bool acc_in) {
                 const uint32_t d = tmem + (hh ? C::TM_O1 : C::TM_O0);
                 const uint32_t p = tmem + (hh ? C::TM_S1 : C::TM_S0);
+                const SDesc vd = sdesc_split(vb, C::SLAB_BYTES, 1024);
 #pragma unroll
-                for (int k = 0; k < BN / 16; ++k) {
-                    mma_ts(d, p + k * 8, sdesc_sw128(vb + k * 16 * 128, C::SLAB_BYTES, 1024),
-                           IDESC_PV, (acc_in || k > 0) ? 1u : 0u);
-                }
+                for (int k = 0; k < BN / 16; ++k)
+                    mma_ts(d, p + k * 8, vd.at(k * 16 * 128), IDESC_PV, (acc_in || k > 0) ? 1u : 0u);
             };
             int slot = 0;
             uint32_t ph = 0;

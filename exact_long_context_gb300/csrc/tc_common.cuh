@@ -156,6 +156,21 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
+// A shared-memory descriptor kept as two words, built once per operand tile: the start
+// address (address >> 4) is bits 0-13 of the low word, and shared memory lies below
+// 256 KB, so stepping to another K slice of the tile is an add to the low word that never
+// carries out of the field.  Keeps the MMA issuer to a few instructions per tcgen05.mma.
+struct SDesc {
+    uint32_t lo, hi;
+    __device__ __forceinline__ uint64_t at(uint32_t byte_off) const {
+        return ((uint64_t)hi << 32) | (uint64_t)(lo + (byte_off >> 4));
+    }
+};
+__device__ __forceinline__ SDesc sdesc_split(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    const uint64_t d = sdesc_sw128(saddr, lbo, sbo);
+    return {(uint32_t)d, (uint32_t)(d >> 32)};
+}
+
 // Instruction descriptor for kind::f16: f32 accumulator (bits 4-5 = 1), A and B bf16
 // (bits 7-9 and 10-12 = 1), B major-ness at bit 16 (1 = MN-major), N >> 3 at bits
 // 17-22, M >> 4 at bits 24-28.
