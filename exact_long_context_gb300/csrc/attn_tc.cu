@@ -137,18 +137,38 @@ __device__ __forceinline__ int snake_item(int k) {
     return k * G + ((k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
 }
 
-__device__ __forceinline__ void decode_item(const StepParams &P, int L, Item &it) {
+// Work item L, part `sub`.  With P.pair_items (segments of equal length): an item is a
+// pair of 256-row blocks of one segment and one head, block p and block nb-1-p, so under
+// causality every item of a segment costs the same; items are numbered segment
+// (heaviest first, as the host orders them), then head, then pair, so the CTAs that run
+// at the same time share the K/V tiles of a few heads in L2.  `sub` 0 is the later
+// block, 1 the earlier one (false when the pair has a single middle block).  Otherwise
+// an item is one block, as decode_work numbers them (heaviest first) with the heads
+// innermost, which balances best when there are few items per CTA; `sub` 1 is empty.
+__device__ __forceinline__ bool decode_item(const StepParams &P, int L, int sub, Item &it) {
     const int BH = P.B * P.Hq;
-    const int w = L / BH;
-    const int bh = L - w * BH;
+    int si, lb, bh;
+    if (!P.pair_items) {
+        if (sub) return false;
+        const int w = L / BH;
+        bh = L - w * BH;
+        decode_work(P, w, si, lb);
+    } else {
+        const int np = (P.blocks_per_seg + 1) >> 1;
+        const int per_seg = BH * np;
+        si = L / per_seg;
+        const int rem = L - si * per_seg;
+        bh = rem / np;
+        const int pp = rem - bh * np;
+        lb = sub ? pp : P.blocks_per_seg - 1 - pp;
+        if (sub && lb == P.blocks_per_seg - 1 - pp) return false;
+    }
     it.b = bh / P.Hq;
     it.h = bh - it.b * P.Hq;
     it.hk = it.h / (P.Hq / P.Hkv);
-    int si, lb;
-    decode_work(P, w, si, lb);
     it.nmax = 0;
     it.nh[0] = it.nh[1] = 0;
-    if (lb < 0) return;
+    if (lb < 0) return true;
     const Seg &S = P.seg[si];
     it.qrow0 = S.q0 + lb * 2 * BM;
     it.q1 = S.q1;
@@ -173,6 +193,7 @@ __device__ __forceinline__ void decode_item(const StepParams &P, int L, Item &it
             it.nh[hh] = it.kt.visible_prefix(min(r0 + BM, S.q1) - 1 - S.diag);
     }
     it.nmax = max(it.nh[0], it.nh[1]);
+    return true;
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -246,11 +267,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t issued = 0, last_ph = 0;  // per-slot bit sets
             uint32_t qcnt[2] = {0u, 0u};       // Q_h loads issued
             bool ok = true;
-            for (int k = 0; k * (int)gridDim.x < total && ok; ++k) {
-                const int L = snake_item(k);
+            for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, part)
+                const int L = snake_item(k2 >> 1);
                 if (L >= total) continue;
                 Item it;
-                decode_item(P, L, it);
+                if (!decode_item(P, L, k2 & 1, it)) continue;
                 if (it.nmax == 0) continue;
                 // Stages of an item: (K_0), then (V_t, K_t+1) for t = 0..n-1 (the last one
                 // V only).  Stage (K_0) first - it only needs a free buffer pair - then Q,
@@ -346,11 +367,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t qcnt[2] = {0u, 0u};  // Q_h loads consumed
             uint32_t pcnt[2] = {0u, 0u};  // P_h tiles consumed
             bool ok = true;
-            for (int k = 0; k * (int)gridDim.x < total && ok; ++k) {
-                const int L = snake_item(k);
+            for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, part)
+                const int L = snake_item(k2 >> 1);
                 if (L >= total) continue;
                 Item it;
-                decode_item(P, L, it);
+                if (!decode_item(P, L, k2 & 1, it)) continue;
                 if (it.nmax == 0) continue;
                 const int n0 = it.nh[0], n1 = it.nh[1];
 #pragma unroll
@@ -432,11 +453,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sl2 = P.scale_log2;
         uint32_t scnt = 0, ocnt = 0;  // S_h tiles and O_h results seen
         bool ok = true;
-        for (int k = 0; k * (int)gridDim.x < total && ok; ++k) {
-                const int L = snake_item(k);
-                if (L >= total) continue;
+        for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, part)
+            const int L = snake_item(k2 >> 1);
+            if (L >= total) continue;
             Item it;
-            decode_item(P, L, it);
+            if (!decode_item(P, L, k2 & 1, it)) continue;
             const int n = hh ? it.nh[1] : it.nh[0];
             if (it.nmax == 0 || n == 0) continue;
             const int first_row = it.qrow0 + hh * BM;
@@ -659,10 +680,22 @@ static cudaError_t launch_tc_hd(const StepParams &P, int blocks_y, int num_sms,
         !encode_map(&mk, P.k, P.B, P.Hkv, P.N, P.D, P.sk, P.rs) ||
         !encode_map(&mv, P.v, P.B, P.Hkv, P.N, P.D, P.sv, P.rs))
         return cudaErrorInvalidValue;
-    const int64_t total = (int64_t)P.B * P.Hq * blocks_y;
+    // Items: pairs of blocks for a ring step (its tail overlaps the next step's launch)
+    // or when the pairs fill their rounds over the persistent grid to 93 %; single
+    // blocks (heaviest first) otherwise, and for packed batches.
+    const int64_t singles = (int64_t)P.B * P.Hq * blocks_y;
+    const int64_t pairs = (int64_t)P.B * P.Hq * P.nseg * ((P.blocks_per_seg + 1) / 2);
+    bool use_pairs = false;
+    if (!P.var_blocks && pairs > 0) {
+        const int64_t g = std::min<int64_t>(pairs, num_sms);
+        const int64_t rounds = (pairs + g - 1) / g;
+        use_pairs = P.prefer_pairs || (double)pairs >= 0.93 * (double)(rounds * g);
+    }
+    const int64_t total = use_pairs ? pairs : singles;
     if (total > 0x7fffffff) return cudaErrorInvalidValue;
     StepParams Q = P;
     Q.total_items = (int32_t)total;
+    Q.pair_items = use_pairs ? 1 : 0;
     const int grid = (int)std::min<int64_t>(total, (int64_t)num_sms);
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);

@@ -490,6 +490,7 @@ ra_status ra_ring_sim_fwd(const ra_tensor *q, const ra_tensor *k, const ra_tenso
     fill_common(*P, q, k, v, o, lse, pb, causal, scale, di);
     P->oacc = ring_size > 1 ? static_cast<float *>(workspace) : nullptr;
     P->rs = (layout == RA_LAYOUT_STRIPED) ? ring_size : 1;
+    P->prefer_pairs = ring_size > 1 ? 1 : 0;
     const bool tc = use_tensor_cores(q, k, v, o, pb, di);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     std::vector<Seg> segs;
@@ -1034,6 +1035,7 @@ extern "C" ra_status ra_ring_sim_fwd_noalloc(const ra_tensor *q, const ra_tensor
     StepParams P;
     fill_common(P, q, k, v, o, lse, pb, causal, scale, di);
     P.oacc = scratch;
+    P.prefer_pairs = ring_size > 1 ? 1 : 0;
     const bool tc = use_tensor_cores(q, k, v, o, pb, di);
     const int rows_per_block = tc ? attn_tc_rows_per_block() : 16;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

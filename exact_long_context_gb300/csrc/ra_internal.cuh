@@ -50,6 +50,8 @@ struct StepParams {
     int32_t total_items;     // persistent kernels: work items in this launch
     int32_t chained;         // launched as a dependent of the previous ring step's kernel
     int32_t var_blocks;      // segments have different lengths: decode through Seg::blk0
+    int32_t pair_items;      // tensor-core kernel: items are pairs of blocks (set at launch)
+    int32_t prefer_pairs;    // host: a ring step (tails overlap the next step's launch)
     int32_t rs;              // rank interleave stride of the sequence axis (1 unless striped)
     int64_t wait_limit_ns;
     int *err;  // device error word
