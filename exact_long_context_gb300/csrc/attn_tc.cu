@@ -123,10 +123,115 @@ struct Item {
     int q_rank, kv_rank, diag;
     int qrow0, q1;
     int flags;
-    int nh[2];  // key tiles each half iterates (a prefix of the segment's tiles)
-    int nmax;
-    KTiles kt;
+    int rank;   // the query chunk's rank (fused ring: the key ranges of every step follow from it)
+    int nh[2];  // key tiles each half takes part in
+    int nmax;   // key tiles of the item (T)
+    int T0;     // tiles of the first step (the only one with a diagonal range)
+    int skip0;  // the one tile half 0 sits out (the last of the first step), or -1
+    KTiles kt;  // the first step's key ranges
+    // Half 1 (the later rows) takes part in every tile; half 0 in every tile but the last
+    // of the first step when that tile starts past its last row.
+    __device__ __forceinline__ bool part(int hh, int t) const {
+        return hh ? nh[1] > 0 : (nh[0] > 0 && t != skip0);
+    }
+    __device__ __forceinline__ int last(int hh) const { return (!hh && skip0 == nmax - 1) ? nmax - 2 : nmax - 1; }
 };
+
+// Fused ring (contiguous or zigzag layout): the key ranges rank r's query chunk ending at
+// q1 sees at step s, those of rank (r - s) mod R, with the forward's causal rule (a range
+// starting after the chunk's last row is skipped).  Only step 0, the rank's own block, can
+// hold a diagonal range, and it is that step's last.
+__device__ __forceinline__ int ring_ranges(const StepParams &P, int r, int q1, int s, int &a0, int &b0,
+                                           int &a1, int &b1) {
+    const int R = P.ring_R;
+    const int j = ((r - s) % R + R) % R;
+    int ca0, cb0, ca1 = 0, cb1 = 0, nc;
+    if (P.ring_layout == 0) {
+        const int c = P.N / R;
+        ca0 = j * c;
+        cb0 = ca0 + c;
+        nc = 1;
+    } else {
+        const int h = P.N / (2 * R);
+        ca0 = j * h;
+        cb0 = ca0 + h;
+        ca1 = (2 * R - 1 - j) * h;
+        cb1 = ca1 + h;
+        nc = 2;
+    }
+    int n = 0;
+    a0 = b0 = a1 = b1 = 0;
+    for (int i = 0; i < nc; ++i) {
+        const int ca = i ? ca1 : ca0, cb = i ? cb1 : cb0;
+        if (cb <= ca || (P.causal && ca > q1 - 1)) continue;
+        if (n == 0) {
+            a0 = ca;
+            b0 = cb;
+        } else {
+            a1 = ca;
+            b1 = cb;
+        }
+        ++n;
+    }
+    return n;
+}
+
+// Walks an item's key tiles in order: the first T0 tiles of step 0's ranges (the tiles
+// some row of the item sees: the diagonal range is cut at the causal prefix), then every
+// tile of step 1's ranges, of step 2's, ...
+struct TileCursor {
+    int s, ri, nr, ti, nti;
+    int left0;  // tiles of step 0 still to come
+    int a0, b0, a1, b1;
+    __device__ __forceinline__ int start() const { return (ri ? a1 : a0) + ti * BN; }
+    __device__ __forceinline__ int end() const { return ri ? b1 : b0; }
+};
+__device__ __forceinline__ int ntiles(int a, int b) { return b > a ? (b - a + BN - 1) / BN : 0; }
+__device__ __forceinline__ void cursor_seek(const StepParams &P, const Item &it, TileCursor &c) {
+    const int steps = P.ring_fused ? P.ring_R : 1;
+    for (; c.s < steps; ++c.s) {
+        if (c.s == 0) {
+            c.a0 = it.kt.k0[0];
+            c.b0 = it.kt.k1[0];
+            c.a1 = it.kt.k0[1];
+            c.b1 = it.kt.k1[1];
+            c.nr = (c.b0 > c.a0) + (c.b1 > c.a1);
+            if (c.b0 <= c.a0) {
+                c.a0 = c.a1;
+                c.b0 = c.b1;
+            }
+        } else {
+            c.nr = ring_ranges(P, it.rank, it.q1, c.s, c.a0, c.b0, c.a1, c.b1);
+        }
+        if (c.nr > 0) {
+            c.ri = 0;
+            c.ti = 0;
+            c.nti = ntiles(c.a0, c.b0);
+            return;
+        }
+    }
+}
+__device__ __forceinline__ void cursor_begin(const StepParams &P, const Item &it, TileCursor &c) {
+    c.s = 0;
+    c.left0 = it.T0;
+    cursor_seek(P, it, c);
+}
+__device__ __forceinline__ void cursor_next(const StepParams &P, const Item &it, TileCursor &c) {
+    if (c.s == 0 && --c.left0 <= 0) {  // past step 0's visible prefix
+        c.s = 1;
+        cursor_seek(P, it, c);
+        return;
+    }
+    if (++c.ti < c.nti) return;
+    if (c.ri + 1 < c.nr) {
+        c.ri = 1;
+        c.ti = 0;
+        c.nti = ntiles(c.a1, c.b1);
+        return;
+    }
+    ++c.s;
+    cursor_seek(P, it, c);
+}
 
 // Item L of a launch: L = w * (B*Hq) + bh, so the heaviest work blocks of every head
 // come first.  A persistent CTA takes one item per round of gridDim.x items, in snake
@@ -168,20 +273,32 @@ __device__ __forceinline__ bool decode_item(const StepParams &P, int L, int sub,
     it.hk = it.h / (P.Hq / P.Hkv);
     it.nmax = 0;
     it.nh[0] = it.nh[1] = 0;
+    it.T0 = 0;
+    it.skip0 = -1;
     if (lb < 0) return true;
     const Seg &S = P.seg[si];
+    it.rank = S.rank;
     it.qrow0 = S.q0 + lb * 2 * BM;
     it.q1 = S.q1;
     it.q_rank = S.q_rank;
     it.kv_rank = S.kv_rank;
     it.diag = S.diag;
     it.flags = S.flags;
-    it.kt.k0[0] = S.k0[0];
-    it.kt.k1[0] = S.k1[0];
-    it.kt.k0[1] = S.k0[1];
-    it.kt.k1[1] = S.k1[1];
-    it.kt.nt0 = (S.k1[0] > S.k0[0]) ? (S.k1[0] - S.k0[0] + BN - 1) / BN : 0;
-    it.kt.ntot = it.kt.nt0 + ((S.k1[1] > S.k0[1]) ? (S.k1[1] - S.k0[1] + BN - 1) / BN : 0);
+    if (P.ring_fused) {  // step 0's ranges: the rank's own block
+        int a0, b0, a1, b1;
+        const int nr = ring_ranges(P, S.rank, S.q1, 0, a0, b0, a1, b1);
+        it.kt.k0[0] = a0;
+        it.kt.k1[0] = b0;
+        it.kt.k0[1] = nr > 1 ? a1 : b0;
+        it.kt.k1[1] = nr > 1 ? b1 : b0;
+    } else {
+        it.kt.k0[0] = S.k0[0];
+        it.kt.k1[0] = S.k1[0];
+        it.kt.k0[1] = S.k0[1];
+        it.kt.k1[1] = S.k1[1];
+    }
+    it.kt.nt0 = ntiles(it.kt.k0[0], it.kt.k1[0]);
+    it.kt.ntot = it.kt.nt0 + ntiles(it.kt.k0[1], it.kt.k1[1]);
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
         const int r0 = it.qrow0 + hh * BM;
@@ -192,7 +309,22 @@ __device__ __forceinline__ bool decode_item(const StepParams &P, int L, int sub,
         else
             it.nh[hh] = it.kt.visible_prefix(min(r0 + BM, S.q1) - 1 - S.diag);
     }
-    it.nmax = max(it.nh[0], it.nh[1]);
+    // the first step: each half a prefix of its tiles; the later steps (fused ring): every
+    // tile for both halves (their ranges lie wholly before or wholly after the chunk)
+    it.T0 = max(it.nh[0], it.nh[1]);
+    // half 1 sees every first-step tile (its rows come later); half 0 at most one fewer
+    it.skip0 = (it.nh[0] > 0 && it.nh[0] < it.T0) ? it.T0 - 1 : -1;
+    int later = 0;
+    if (P.ring_fused && it.T0 > 0)
+        for (int s = 1; s < P.ring_R; ++s) {
+            int a0, b0, a1, b1;
+            const int nr = ring_ranges(P, S.rank, S.q1, s, a0, b0, a1, b1);
+            later += (nr > 0 ? ntiles(a0, b0) : 0) + (nr > 1 ? ntiles(a1, b1) : 0);
+        }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+        if (it.nh[hh] > 0) it.nh[hh] += later;
+    it.nmax = it.T0 + later;
     return true;
 }
 
@@ -205,7 +337,9 @@ __device__ __forceinline__ bool decode_item(const StepParams &P, int L, int sub,
 // warpgroup of half h finishes its epilogue (reads O_h) before it signals the next
 // item's first P_h, and only then is O_h overwritten.
 
-template <int HD>
+// FUSED: the launch walks every step of a ring (P.ring_fused): key tiles come from a
+// cursor over the steps' ranges; otherwise from the item's segment ranges directly.
+template <int HD, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ StepParams P) {
@@ -276,6 +410,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Stages of an item: (K_0), then (V_t, K_t+1) for t = 0..n-1 (the last one
                 // V only).  Stage (K_0) first - it only needs a free buffer pair - then Q,
                 // which waits until the previous item has issued its last Q K^T.
+                TileCursor cur;
+                if constexpr (FUSED) cursor_begin(P, it, cur);
+                int vstart = 0;  // V_t is the tile K_t came from
                 for (int st = -1; st < it.nmax && ok; ++st) {
                     const uint32_t b_empty = smem_u32(&bars->empty[slot]);
                     const uint32_t b_full = smem_u32(&bars->full[slot]);
@@ -289,14 +426,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t vbuf = sKV + (2 * slot) * C::TILE_BYTES;
                     const uint32_t kbuf = sKV + (2 * slot + 1) * C::TILE_BYTES;
                     if (has_v) {
-                        const int vs = it.kt.start(st);
+                        const int vs = FUSED ? vstart : it.kt.start(st);
 #pragma unroll
                         for (int c = 0; c < C::SLABS; ++c)
                             tma_load_5d(vbuf + c * C::SLAB_BYTES, &tm_v, b_full, c * 64,
                                         it.kv_rank, vs, it.hk, it.b);
                     }
                     if (has_k) {
-                        const int ks = it.kt.start(st + 1);
+                        const int ks = FUSED ? cur.start() : it.kt.start(st + 1);
+                        if constexpr (FUSED) {
+                            vstart = ks;
+                            cursor_next(P, it, cur);
+                        }
 #pragma unroll
                         for (int c = 0; c < C::SLABS; ++c)
                             tma_load_5d(kbuf + c * C::SLAB_BYTES, &tm_k, b_full, c * 64,
@@ -373,10 +514,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 Item it;
                 if (!decode_item(P, L, k2 & 1, it)) continue;
                 if (it.nmax == 0) continue;
-                const int n0 = it.nh[0], n1 = it.nh[1];
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    if ((hh ? n1 : n0) == 0 || !ok) continue;
+                    if (it.nh[hh] == 0 || !ok) continue;
                     ok = wait_phase(smem_u32(&bars->q_full[hh]), qcnt[hh] & 1u, abort_flag,
                                     P.wait_limit_ns, P.err);
                     ++qcnt[hh];
@@ -388,11 +528,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    const int nhh = hh ? n1 : n0;
-                    if (nhh > 0) {
+                    if (it.part(hh, 0)) {
                         issue_qk(hh, sKV + (2 * slot + 1) * C::TILE_BYTES);
                         mma_commit(smem_u32(&bars->s_full[hh]));
-                        if (nhh == 1) mma_commit(smem_u32(&bars->q_empty[hh]));
+                        if (it.last(hh) == 0) mma_commit(smem_u32(&bars->q_empty[hh]));
                     }
                 }
                 mma_commit(smem_u32(&bars->empty[slot]));
@@ -400,7 +539,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     slot = 0;
                     ph ^= 1u;
                 }
-                // stage (V_t, K_t+1): P_h V_t and the next Q_h K^T of each half
+                // stage (V_t, K_t+1): P_h V_t and the next Q_h K^T of each half (a half
+                // issues the next Q K^T of a tile it takes part in even when it sat this
+                // tile out: its last P was read by the P V issued before)
+                bool started[2] = {false, false};
                 for (int t = 0; ok && t < it.nmax; ++t) {
                     ok = wait_phase(smem_u32(&bars->full[slot]), ph, abort_flag, P.wait_limit_ns,
                                     P.err);
@@ -410,21 +552,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t kb = sKV + (2 * slot + 1) * C::TILE_BYTES;
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
-                        const int nhh = hh ? n1 : n0;
-                        if (t < nhh) {
+                        if (it.part(hh, t)) {
                             ++pcnt[hh];
                             ok = wait_count(&bars->p_count[hh], 4u * pcnt[hh], abort_flag,
                                             P.wait_limit_ns, P.err);
                             if (!ok) break;
                             tc_fence_after();
-                            issue_pv(hh, vb, t > 0);
-                            if (t + 1 < nhh) {
-                                issue_qk(hh, kb);
-                                mma_commit(smem_u32(&bars->s_full[hh]));
-                                if (t + 2 == nhh) mma_commit(smem_u32(&bars->q_empty[hh]));
-                            } else {
-                                mma_commit(smem_u32(&bars->o_full[hh]));
-                            }
+                            issue_pv(hh, vb, started[hh]);
+                            started[hh] = true;
+                            if (t == it.last(hh)) mma_commit(smem_u32(&bars->o_full[hh]));
+                        }
+                        if (t + 1 < it.nmax && it.part(hh, t + 1)) {
+                            issue_qk(hh, kb);
+                            mma_commit(smem_u32(&bars->s_full[hh]));
+                            if (t + 1 == it.last(hh)) mma_commit(smem_u32(&bars->q_empty[hh]));
                         }
                     }
                     if (!ok) break;
@@ -471,7 +612,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(pre + i * 32));
             }
             float m_ref = -INFINITY, l = 0.f;
-            for (int t = 0; t < n; ++t) {
+            TileCursor cur;
+            if constexpr (FUSED) cursor_begin(P, it, cur);
+            bool first_tile = true;
+            for (int t = 0; t < it.nmax; ++t) {
+                const int ks = FUSED ? cur.start() : it.kt.start(t);
+                const int ke = FUSED ? cur.end() : it.kt.range_end(t);
+                if constexpr (FUSED) cursor_next(P, it, cur);
+                if (!it.part(hh, t)) continue;
                 ok = wait_phase(b_s, scnt & 1u, abort_flag, P.wait_limit_ns, P.err);
                 ++scnt;
                 if (!ok) break;
@@ -482,8 +630,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(tS + 64, r[2]);
                 tmem_ld32(tS + 96, r[3]);
                 tmem_ld_wait();
-                const int ks = it.kt.start(t);
-                const int ke = it.kt.range_end(t);
                 const bool need_mask =
                     (ks + BN > ke) || (P.causal && (min(ks + BN, ke) - 1 + it.diag > first_row));
                 if (need_mask) {
@@ -511,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float m_tile = mx * sl2;
                 float alpha = 1.f;
                 bool resc = false;
-                if (t == 0) {
+                if (first_tile) {
                     m_ref = m_tile;
                 } else if (m_tile > m_ref + kRescaleThreshold) {
                     alpha = ex2(m_ref - m_tile);
@@ -551,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rs = a0 + a1;
                 }
                 l = l * alpha + rs;
-                if (t > 0 && __any_sync(0xffffffffu, resc)) {
+                if (!first_tile && __any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
                     for (int c = 0; c < HD / 32; ++c) {
                         uint32_t o[32];
@@ -567,6 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) count_release_add(&bars->p_count[hh]);
+                first_tile = false;
             }
             if (!ok) break;
             // ---- epilogue: O / l, LSE, then write or LSE-merge into the running result.
@@ -669,9 +816,12 @@ static cudaError_t launch_tc_hd(const StepParams &P, int blocks_y, int num_sms,
     int dev = 0;
     cudaGetDevice(&dev);
     if (!(configured_mask & (1 << (dev & 31)))) {
-        cudaError_t e = cudaFuncSetAttribute(tc::attn_tc_kernel<HD>,
+        cudaError_t e = cudaFuncSetAttribute(tc::attn_tc_kernel<HD, false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(tc::attn_tc_kernel<HD, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured_mask |= 1 << (dev & 31);
     }
@@ -710,7 +860,8 @@ static cudaError_t launch_tc_hd(const StepParams &P, int blocks_y, int num_sms,
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel<HD>, mq, mk, mv, Q);
+    if (P.ring_fused) return cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel<HD, true>, mq, mk, mv, Q);
+    return cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel<HD, false>, mq, mk, mv, Q);
 }
 
 cudaError_t launch_attn_tc(const StepParams &P, int blocks_y, int num_sms, cudaStream_t stream) {

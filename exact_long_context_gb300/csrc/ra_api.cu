@@ -390,6 +390,43 @@ struct BwdPlan {
     }
 };
 
+// The fused ring launch (tensor cores, contiguous or zigzag layout): one segment per query
+// chunk, tagged with its rank; the kernel walks the chunk's key ranges of steps 0..R-1 in
+// ring order (those of rank (r - s) mod R) and keeps the running result on chip, so each
+// row is written once (SEG_FIRST | SEG_FINAL).  Heaviest chunks (most visible keys over
+// all steps) first.  False when it does not apply (striped layout, or more chunks than a
+// launch holds).
+static bool fused_ring_segments(int64_t N, int R, int layout, int causal, std::vector<Seg> &out) {
+    out.clear();
+    if (layout == RA_LAYOUT_STRIPED) return false;
+    const int chunks = layout == RA_LAYOUT_ZIGZAG ? 2 * R : R;
+    if (chunks > kMaxSeg || N > INT32_MAX) return false;
+    std::vector<std::pair<int64_t, Seg>> work;
+    for (int r = 0; r < R; ++r)
+        for (const Range &qr : rank_ranges(N, R, layout, r)) {
+            if (qr.b <= qr.a) continue;
+            Seg g;
+            memset(&g, 0, sizeof g);
+            g.q0 = (int32_t)qr.a;
+            g.q1 = (int32_t)qr.b;
+            g.rank = r;
+            g.flags = SEG_FIRST | SEG_FINAL;
+            int64_t keys = 0;
+            for (int s = 0; s < R; ++s) {
+                const int j = ((r - s) % R + R) % R;
+                for (const Range &kr : rank_ranges(N, R, layout, j)) {
+                    if (kr.b <= kr.a || (causal && kr.a > qr.b - 1)) continue;
+                    keys += kr.b - kr.a;
+                }
+            }
+            work.push_back({keys, g});
+        }
+    std::stable_sort(work.begin(), work.end(),
+                     [](const std::pair<int64_t, Seg> &x, const std::pair<int64_t, Seg> &y) { return x.first > y.first; });
+    for (const auto &w : work) out.push_back(w.second);
+    return !out.empty();
+}
+
 // ---------------------------------------------------------------- dispatch
 
 static void fill_common(StepParams &P, const ra_tensor *q, const ra_tensor *k, const ra_tensor *v,
@@ -490,15 +527,26 @@ ra_status ra_ring_sim_fwd(const ra_tensor *q, const ra_tensor *k, const ra_tenso
     fill_common(*P, q, k, v, o, lse, pb, causal, scale, di);
     P->oacc = ring_size > 1 ? static_cast<float *>(workspace) : nullptr;
     P->rs = (layout == RA_LAYOUT_STRIPED) ? ring_size : 1;
-    P->prefer_pairs = ring_size > 1 ? 1 : 0;
+    // per-step ring launches overlap their tails with the next step's launch, so they
+    // take tile-pair items; striped rings measured better with single blocks
+    P->prefer_pairs = (ring_size > 1 && layout != RA_LAYOUT_STRIPED) ? 1 : 0;
     const bool tc = use_tensor_cores(q, k, v, o, pb, di);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     std::vector<Seg> segs;
-    for (int step = 0; step < ring_size; ++step) {
-        plan_step(pb.N, ring_size, layout, causal, step, segs);
-        if (segs.empty()) continue;
+    if (tc && ring_size > 1 && fused_ring_segments(pb.N, ring_size, layout, causal, segs)) {
+        // one launch walks every step: each query chunk's running result stays on chip
+        P->ring_fused = 1;
+        P->ring_R = ring_size;
+        P->ring_layout = layout == RA_LAYOUT_ZIGZAG ? 1 : 0;
+        P->prefer_pairs = 0;
         s = run_step(*P, segs, tc, di.sms, st);
-        if (s) break;
+    } else {
+        for (int step = 0; step < ring_size; ++step) {
+            plan_step(pb.N, ring_size, layout, causal, step, segs);
+            if (segs.empty()) continue;
+            s = run_step(*P, segs, tc, di.sms, st);
+            if (s) break;
+        }
     }
     delete P;
     return s;

@@ -133,12 +133,21 @@ def test_empty_and_degenerate(ra):
 
 
 def test_launch_counts_are_native(ra):
-    before = ra.launch_count()
+    """One launch for the single pass and for a tensor-core zigzag or contiguous ring (all
+    steps in one launch); one per step for the striped ring and the CUDA-core path."""
     q, k, v = synth.make_qkv(1, 2, 1, 256, 128, torch.bfloat16, seed=3, device="cuda")
+    before = ra.launch_count()
     ra.attn_fwd(q, k, v, causal=True)
     ra.ring_sim_fwd(q, k, v, 2, "zigzag", causal=True)
+    ra.ring_sim_fwd(q, k, v, 4, "contig", causal=True)
     ra.check()
-    assert ra.launch_count() - before == 1 + 2
+    assert ra.launch_count() - before == 1 + 1 + 1
+    before = ra.launch_count()
+    ra.ring_sim_fwd(q, k, v, 2, "striped", causal=True)
+    qf, kf, vf = (t.float() for t in (q, k, v))
+    ra.ring_sim_fwd(qf, kf, vf, 2, "zigzag", causal=True)
+    ra.check()
+    assert ra.launch_count() - before == 2 + 2
 
 
 # ---------------------------------------------------------------- ring simulation
@@ -158,6 +167,11 @@ RING_SMALL = [
     (1, 4, 2, 1024, 128, 8, "striped", True, torch.bfloat16),
     (1, 2, 2, 768, 64, 3, "striped", True, torch.bfloat16),
     (1, 2, 1, 1000, 128, 5, "striped", False, torch.bfloat16),   # 200 rows per rank: ragged
+    # several 256-row blocks per chunk: the fused ring walks a diagonal prefix, then the
+    # later steps' ranges
+    (1, 2, 1, 4096, 128, 4, "contig", True, torch.bfloat16),
+    (1, 2, 2, 4096, 128, 2, "zigzag", True, torch.bfloat16),
+    (1, 2, 1, 3072, 64, 3, "zigzag", False, torch.bfloat16),
     (1, 2, 1, 96, 16, 4, "striped", True, torch.float32),
     (1, 2, 1, 256, 32, 8, "striped", True, torch.bfloat16),       # CUDA-core path
 ]
