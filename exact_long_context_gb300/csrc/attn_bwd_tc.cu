@@ -29,6 +29,8 @@
 // A launch covers the segments of one ring step (struct BSeg): the whole-sequence
 // backward is one segment.  On a ring, the gradient of a range that earlier or later
 // steps also write is carried between steps in fp32 running buffers (store_grad_chunk).
+#include <climits>
+
 #include "tc_common.cuh"
 
 namespace ra {
@@ -88,11 +90,125 @@ static_assert(sizeof(BBars) <= 256, "barrier block");
 // first (0) or second (1) tile; false when the pair has a single (middle) tile.
 __device__ __forceinline__ int tile_pairs(int tps) { return (tps + 1) >> 1; }
 
+// Fused ring (contiguous or zigzag layout): the streamed ranges of step s for a fixed
+// range [f0, f1) of rank `rank`.  dQ (kind 0): the key chunks of rank (rank - s) mod R
+// that some row of the range sees; dK/dV (kind 1): the query chunks of rank
+// (rank + s) mod R that see some key of the range (the rank holding this block at step s).
+// Ranges are in increasing position; returns their number (0..2).
+__device__ __forceinline__ int ring_ranges_bwd(const BwdParams &P, int kind, int rank, int f0, int f1, int s,
+                                               int &a0, int &b0, int &a1, int &b1) {
+    const int R = P.ring_R;
+    const int j = kind ? (rank + s) % R : ((rank - s) % R + R) % R;
+    int ca0, cb0, ca1 = 0, cb1 = 0, nc;
+    if (P.ring_layout == 0) {
+        const int c = P.N / R;
+        ca0 = j * c;
+        cb0 = ca0 + c;
+        nc = 1;
+    } else {
+        const int hc = P.N / (2 * R);
+        ca0 = j * hc;
+        cb0 = ca0 + hc;
+        ca1 = (2 * R - 1 - j) * hc;
+        cb1 = ca1 + hc;
+        nc = 2;
+    }
+    int n = 0;
+    a0 = b0 = a1 = b1 = 0;
+    for (int i = 0; i < nc; ++i) {
+        const int ca = i ? ca1 : ca0, cb = i ? cb1 : cb0;
+        if (cb <= ca) continue;
+        if (P.causal && (kind ? f0 > cb - 1 : ca > f1 - 1)) continue;
+        if (n == 0) {
+            a0 = ca;
+            b0 = cb;
+        } else {
+            a1 = ca;
+            b1 = cb;
+        }
+        ++n;
+    }
+    return n;
+}
+
+// Walks the streamed tiles of the later steps (s = 1 .. R-1) of a fused ring item: every
+// tile of each range from its first visible one (`vis0` is the first streamed index some
+// fixed row pairs with: for dK/dV the query tiles before the range's first visible row
+// are skipped; dQ ranges of later steps are wholly visible).
+struct BCursor {
+    int s, ri, nr, ti, nti;
+    int a0, b0, a1, b1, sk0, sk1;
+    __device__ __forceinline__ int start() const { return ri ? a1 + (sk1 + ti) * kT : a0 + (sk0 + ti) * kT; }
+    __device__ __forceinline__ int end() const { return ri ? b1 : b0; }
+};
+__device__ __forceinline__ int skip_tiles(int a, int b, int vis0) {
+    return vis0 > a ? (min(vis0, b) - a) / kT : 0;
+}
+__device__ __forceinline__ int vis_tiles(int a, int b, int vis0) {
+    const int lo = max(a, vis0);
+    return lo < b ? (b - a + kT - 1) / kT - skip_tiles(a, b, vis0) : 0;
+}
+__device__ __forceinline__ void bcur_seek(const BwdParams &P, int kind, int rank, int f0, int f1, int vis0,
+                                          BCursor &c) {
+    for (; c.s < P.ring_R; ++c.s) {
+        c.nr = ring_ranges_bwd(P, kind, rank, f0, f1, c.s, c.a0, c.b0, c.a1, c.b1);
+        c.sk0 = skip_tiles(c.a0, c.b0, vis0);
+        c.sk1 = skip_tiles(c.a1, c.b1, vis0);
+        const int n0 = c.nr > 0 ? vis_tiles(c.a0, c.b0, vis0) : 0;
+        const int n1 = c.nr > 1 ? vis_tiles(c.a1, c.b1, vis0) : 0;
+        if (n0 > 0) {
+            c.ri = 0;
+            c.ti = 0;
+            c.nti = n0;
+            return;
+        }
+        if (n1 > 0) {
+            c.ri = 1;
+            c.ti = 0;
+            c.nti = n1;
+            return;
+        }
+    }
+}
+__device__ __forceinline__ void bcur_begin(const BwdParams &P, int kind, int rank, int f0, int f1, int vis0,
+                                           BCursor &c) {
+    c.s = 1;
+    bcur_seek(P, kind, rank, f0, f1, vis0, c);
+}
+__device__ __forceinline__ void bcur_next(const BwdParams &P, int kind, int rank, int f0, int f1, int vis0,
+                                          BCursor &c) {
+    if (++c.ti < c.nti) return;
+    if (c.ri == 0 && c.nr > 1) {
+        const int n1 = vis_tiles(c.a1, c.b1, vis0);
+        if (n1 > 0) {
+            c.ri = 1;
+            c.ti = 0;
+            c.nti = n1;
+            return;
+        }
+    }
+    ++c.s;
+    bcur_seek(P, kind, rank, f0, f1, vis0, c);
+}
+// Streamed tiles of the later steps of a fused item.
+__device__ __forceinline__ int later_tiles(const BwdParams &P, int kind, int rank, int f0, int f1, int vis0) {
+    int n = 0;
+    for (int s = 1; s < P.ring_R; ++s) {
+        int a0, b0, a1, b1;
+        const int nr = ring_ranges_bwd(P, kind, rank, f0, f1, s, a0, b0, a1, b1);
+        if (nr > 0) n += vis_tiles(a0, b0, vis0);
+        if (nr > 1) n += vis_tiles(a1, b1, vis0);
+    }
+    return n;
+}
+
 // dQ sub-item: query tile of one segment and one (b, h).  Rows [r_lo, r_hi) of the
-// segment's fixed range; streamed key tiles: n0 from the first range, then n - n0 from
-// the second.
+// segment's fixed range; streamed key tiles: n0 from the first range, then n1 - n0 from
+// the second (the first step's ranges sa/sb; for a fused ring, the later steps' tiles
+// follow, n in all).
 struct QItem {
-    int b, h, hk, si, r_lo, r_hi, n0, n;
+    int b, h, hk, si, r_lo, r_hi, n0, n1, n;
+    int sa0, sb0, sa1, sb1;
 };
 __device__ __forceinline__ bool decode_q(const BwdParams &P, int tps, int L, int sub, QItem &it) {
     const int BH = P.B * P.Hq;
@@ -110,30 +226,45 @@ __device__ __forceinline__ bool decode_q(const BwdParams &P, int tps, int L, int
     const BSeg &S = P.seg[it.si];
     it.r_lo = S.f0 + qi * kT;
     it.r_hi = min(it.r_lo + kT, S.f1);
-    it.n = 0;
+    if (P.ring_fused) {
+        const int nr = ring_ranges_bwd(P, 0, S.rank, S.f0, S.f1, 0, it.sa0, it.sb0, it.sa1, it.sb1);
+        if (nr < 2) it.sa1 = it.sb1 = it.sb0;
+    } else {
+        it.sa0 = S.s0[0];
+        it.sb0 = S.s1[0];
+        it.sa1 = S.s0[1];
+        it.sb1 = S.s1[1];
+    }
+    it.n1 = 0;
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
-        const int a = S.s0[p];
-        const int e = P.causal ? min(S.s1[p], it.r_hi - S.diag) : S.s1[p];
+        const int a = p ? it.sa1 : it.sa0;
+        const int b = p ? it.sb1 : it.sb0;
+        const int e = P.causal ? min(b, it.r_hi - S.diag) : b;
         const int np_ = e > a ? (e - a + kT - 1) / kT : 0;
         if (p == 0) it.n0 = np_;
-        it.n += np_;
+        it.n1 += np_;
     }
+    it.n = it.n1;
+    if (P.ring_fused && it.n1 > 0) it.n += later_tiles(P, 0, S.rank, S.f0, S.f1, 0);
     return true;
 }
 
-// Streamed key tile t of a dQ item: first key index and the end of its range.
+// Streamed key tile t (t < n1: the first step) of a dQ item: first key index and the end
+// of its range.
 __device__ __forceinline__ void q_tile(const BSeg &S, const QItem &it, int t, int &k0, int &klim) {
     const int p = t < it.n0 ? 0 : 1;
-    k0 = p ? S.s0[1] + (t - it.n0) * kT : S.s0[0] + t * kT;
-    klim = p ? S.s1[1] : S.s1[0];
+    k0 = p ? it.sa1 + (t - it.n0) * kT : it.sa0 + t * kT;
+    klim = p ? it.sb1 : it.sb0;
+    (void)S;
 }
 
 // dK/dV sub-item: key tile of one segment and one (b, KV head), the earlier (heavier)
 // tile of the pair first; it visits the visible query tiles of both streamed ranges for
 // each of the G query heads: n = G * per.
 struct KItem {
-    int b, hk, si, c_lo, c_hi, t0[2], n0, per, n;
+    int b, hk, si, c_lo, c_hi, t0[2], n0, per0, per, n;
+    int sa0, sb0, sa1, sb1;  // the first step's query ranges
 };
 __device__ __forceinline__ bool decode_kv(const BwdParams &P, int tps, int L, int sub, KItem &it) {
     const int BHk = P.B * P.Hkv;
@@ -150,33 +281,87 @@ __device__ __forceinline__ bool decode_kv(const BwdParams &P, int tps, int L, in
     const BSeg &S = P.seg[it.si];
     it.c_lo = S.f0 + kj * kT;
     it.c_hi = min(it.c_lo + kT, S.f1);
-    it.per = 0;
+    if (P.ring_fused) {
+        const int nr = ring_ranges_bwd(P, 1, S.rank, S.f0, S.f1, 0, it.sa0, it.sb0, it.sa1, it.sb1);
+        if (nr < 2) it.sa1 = it.sb1 = it.sb0;
+    } else {
+        it.sa0 = S.s0[0];
+        it.sb0 = S.s1[0];
+        it.sa1 = S.s0[1];
+        it.sb1 = S.s1[1];
+    }
+    it.per0 = 0;
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
-        const int a = P.causal ? max(S.s0[p], it.c_lo + S.diag) : S.s0[p];
+        const int sa = p ? it.sa1 : it.sa0, sb = p ? it.sb1 : it.sb0;
+        const int a = P.causal ? max(sa, it.c_lo + S.diag) : sa;
         int np_ = 0, t0 = 0;
-        if (a < S.s1[p]) {
-            t0 = (a - S.s0[p]) / kT;
-            np_ = (S.s1[p] - S.s0[p] + kT - 1) / kT - t0;
+        if (a < sb) {
+            t0 = (a - sa) / kT;
+            np_ = (sb - sa + kT - 1) / kT - t0;
         }
-        it.t0[p] = t0;
-        if (p == 0) it.n0 = np_;
-        it.per += np_;
+        if (p == 0) {
+            it.t0[0] = t0;
+            it.n0 = np_;
+        } else {
+            it.t0[1] = t0;
+        }
+        it.per0 += np_;
     }
+    it.per = it.per0;
+    if (P.ring_fused && it.per0 > 0)
+        it.per += later_tiles(P, 1, S.rank, S.f0, S.f1, P.causal ? it.c_lo : INT_MIN);
     it.n = (P.Hq / P.Hkv) * it.per;
     return true;
 }
 
-// Streamed query tile t of a dK/dV item: first query index, the end of its range, head.
-__device__ __forceinline__ void kv_tile(const BSeg &S, const KItem &it, int G, int t, int &q0, int &qlim,
-                                        int &g) {
-    g = t / it.per;
-    const int tt = t - g * it.per;
+// Streamed query tile tt (tt < per0: the first step) of a dK/dV item: first query index
+// and the end of its range.
+__device__ __forceinline__ void kv_tile0(const KItem &it, int tt, int &q0, int &qlim) {
     const int p = tt < it.n0 ? 0 : 1;
-    q0 = p ? S.s0[1] + (it.t0[1] + tt - it.n0) * kT : S.s0[0] + (it.t0[0] + tt) * kT;
-    qlim = p ? S.s1[1] : S.s1[0];
-    (void)G;
+    q0 = p ? it.sa1 + (it.t0[1] + tt - it.n0) * kT : it.sa0 + (it.t0[0] + tt) * kT;
+    qlim = p ? it.sb1 : it.sb0;
 }
+
+// Sequential walks over an item's streamed tiles (the producer and the element-wise warps
+// take them in order): the first step's from the item's ranges, a fused ring's later
+// steps from a cursor.
+struct QWalk {
+    BCursor c;
+    int t = 0;
+    template <bool FUSED>
+    __device__ __forceinline__ void next(const BwdParams &P, const BSeg &S, const QItem &it, int &k0, int &klim) {
+        if (!FUSED || t < it.n1) {
+            q_tile(S, it, t, k0, klim);
+        } else {
+            if (t == it.n1) bcur_begin(P, 0, S.rank, S.f0, S.f1, 0, c);
+            k0 = c.start();
+            klim = c.end();
+            bcur_next(P, 0, S.rank, S.f0, S.f1, 0, c);
+        }
+        ++t;
+    }
+};
+struct KWalk {
+    BCursor c;
+    int t = 0;
+    template <bool FUSED>
+    __device__ __forceinline__ void next(const BwdParams &P, const BSeg &S, const KItem &it, int &q0, int &qlim,
+                                         int &g) {
+        g = t / it.per;
+        const int tt = t - g * it.per;
+        if (!FUSED || tt < it.per0) {
+            kv_tile0(it, tt, q0, qlim);
+        } else {
+            const int vis0 = P.causal ? it.c_lo : INT_MIN;
+            if (tt == it.per0) bcur_begin(P, 1, S.rank, S.f0, S.f1, vis0, c);
+            q0 = c.start();
+            qlim = c.end();
+            bcur_next(P, 1, S.rank, S.f0, S.f1, vis0, c);
+        }
+        ++t;
+    }
+};
 
 __device__ __forceinline__ int snake(int k) {
     const int G = gridDim.x;
@@ -413,7 +598,7 @@ __device__ __forceinline__ void dq_tile_ew(uint32_t (&sv)[64], uint32_t tD, int 
     }
 }
 
-template <int HD>
+template <int HD, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -457,10 +642,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (it.n == 0) continue;
                 const BSeg &S = P.seg[it.si];
                 const int hk = it.hk;
-                auto coords = [=, &S](int t, int &row, int &head) {
+                QWalk walk;
+                auto coords = [&](int t, int &row, int &head) {
                     int klim;
-                    q_tile(S, it, t, row, klim);
+                    walk.next<FUSED>(P, S, it, row, klim);
                     head = hk;
+                    (void)t;
                 };
                 ok = produce_item_kv<HD>(bars, sQ, sK, sV, kr, vr, fcnt, &tm_q, &tm_do, it.r_lo, S.f_rank, it.h,
                                          &tm_k, &tm_v, S.s_rank, it.n, it.b, coords, abort_flag, limit, err);
@@ -556,9 +743,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (valid && grp == 0 && !(S.flags & SEG_FIRST))
                 for (int i = 0; i < HD * 4; i += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(
                                                           reinterpret_cast<const char *>(accp) + i));
+            QWalk walk;
             for (int t = 0; t < n && ok; ++t, ++g) {
                 int kt0, klim;
-                q_tile(S, it, t, kt0, klim);
+                walk.next<FUSED>(P, S, it, kt0, klim);
                 ok = wait_phase(smem_u32(&bars->s_full[0]), g & 1u, abort_flag, limit, err);
                 if (!ok) break;
                 tc_fence_after();
@@ -661,7 +849,7 @@ __device__ __forceinline__ void ds_tile_ew(const uint32_t (&pv)[64], uint32_t tD
     }
 }
 
-template <int HD>
+template <int HD, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -707,10 +895,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (it.n == 0) continue;
                 const BSeg &S = P.seg[it.si];
                 const int hk = it.hk;
-                auto coords = [=, &S](int t, int &row, int &head) {
+                KWalk walk;
+                auto coords = [&](int t, int &row, int &head) {
                     int qlim, g;
-                    kv_tile(S, it, G, t, row, qlim, g);
+                    walk.next<FUSED>(P, S, it, row, qlim, g);
                     head = hk * G + g;
+                    (void)t;
                 };
                 ok = produce_item<HD>(bars, sK, sSt, slot, ph, fcnt, issued, last_ph, &tm_k, &tm_v, it.c_lo,
                                       S.f_rank, hk, &tm_q, &tm_do, S.s_rank, it.n, it.b, coords, abort_flag,
@@ -824,9 +1014,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             // LSE (log2 units) and D of this lane's two queries of tile t; the next tile's
             // are loaded while this one is processed, so their latency is hidden
+            // the walk runs one tile ahead: fetch() takes tile t+1's coordinates and values
+            // while tile t is processed, and hands the coordinates on
+            KWalk walk;
+            int nq0 = 0, nqlim = 0, ngh = 0;
             auto fetch = [&](int t, float (&l)[2], float (&d)[2]) {
                 int q0, qlim, gh;
-                kv_tile(S, it, G, t, q0, qlim, gh);
+                walk.next<FUSED>(P, S, it, q0, qlim, gh);
+                nq0 = q0;
+                nqlim = qlim;
+                ngh = gh;
+                (void)t;
                 const int h = it.hk * G + gh;
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
@@ -839,8 +1037,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float nl[2] = {0.f, 0.f}, nd[2] = {0.f, 0.f};
             if (n > 0) fetch(0, nl, nd);
             for (int t = 0; t < n && ok; ++t, ++g) {
-                int q0, qlim, gh;
-                kv_tile(S, it, G, t, q0, qlim, gh);
+                const int q0 = nq0, qlim = nqlim;
+                (void)ngh;
                 const int qa = q0 + grp * 64;  // first query of this warp's columns
                 __syncwarp();  // every lane is done with the previous tile's values
                 lb[lane] = nl[0];
@@ -939,10 +1137,16 @@ static cudaError_t launch_bwd_tc_hd(const BwdParams &P, int parts, int num_sms, 
     int dev = 0;
     cudaGetDevice(&dev);
     if (!(configured_mask & (1 << (dev & 31)))) {
-        cudaError_t e = cudaFuncSetAttribute(tcb::bwd_dq_tc_kernel<HD>,
+        cudaError_t e = cudaFuncSetAttribute(tcb::bwd_dq_tc_kernel<HD, false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES_DQ);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(tcb::bwd_dkdv_tc_kernel<HD>,
+            e = cudaFuncSetAttribute(tcb::bwd_dq_tc_kernel<HD, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES_DQ);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(tcb::bwd_dkdv_tc_kernel<HD, false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(tcb::bwd_dkdv_tc_kernel<HD, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured_mask |= 1 << (dev & 31);
@@ -956,16 +1160,25 @@ static cudaError_t launch_bwd_tc_hd(const BwdParams &P, int parts, int num_sms, 
     const int np = ((P.flen + tcb::kT - 1) / tcb::kT + 1) / 2;  // tile pairs per segment and head
     const int64_t tq = (int64_t)P.B * P.Hq * P.nseg * np, tkv = (int64_t)P.B * P.Hkv * P.nseg * np;
     if (tq > 0x7fffffff || tkv > 0x7fffffff) return cudaErrorInvalidValue;
+    const int gq = (int)std::min<int64_t>(tq, num_sms), gkv = (int)std::min<int64_t>(tkv, num_sms);
     if (parts & 1) {
-        tcb::bwd_dq_tc_kernel<HD><<<(int)std::min<int64_t>(tq, num_sms), tcb::kThreads, C::SMEM_BYTES_DQ,
-                                    stream>>>(
-            mq, mk, mv, mdo, P, (int)tq, wait_ns, err);
+        if (P.ring_fused)
+            tcb::bwd_dq_tc_kernel<HD, true><<<gq, tcb::kThreads, C::SMEM_BYTES_DQ, stream>>>(mq, mk, mv, mdo, P, (int)tq,
+                                                                                          wait_ns, err);
+        else
+            tcb::bwd_dq_tc_kernel<HD, false><<<gq, tcb::kThreads, C::SMEM_BYTES_DQ, stream>>>(mq, mk, mv, mdo, P,
+                                                                                           (int)tq, wait_ns, err);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    if (parts & 2)
-        tcb::bwd_dkdv_tc_kernel<HD><<<(int)std::min<int64_t>(tkv, num_sms), tcb::kThreads, C::SMEM_BYTES,
-                                      stream>>>(mq, mk, mv, mdo, P, (int)tkv, wait_ns, err);
+    if (parts & 2) {
+        if (P.ring_fused)
+            tcb::bwd_dkdv_tc_kernel<HD, true><<<gkv, tcb::kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, P,
+                                                                                          (int)tkv, wait_ns, err);
+        else
+            tcb::bwd_dkdv_tc_kernel<HD, false><<<gkv, tcb::kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, P,
+                                                                                           (int)tkv, wait_ns, err);
+    }
     return cudaGetLastError();
 }
 

@@ -427,6 +427,42 @@ static bool fused_ring_segments(int64_t N, int R, int layout, int causal, std::v
     return !out.empty();
 }
 
+// The fused ring backward (tensor cores, contiguous or zigzag layout): kind 0, one dQ
+// segment per query chunk; kind 1, one dK/dV segment per key chunk; each tagged with its
+// rank, the kernels walk the partner ranges of steps 0..R-1 and keep the gradient on
+// chip, so each row is written once.  Heaviest first.  False when it does not apply.
+static bool fused_bwd_segments(int64_t N, int R, int layout, int causal, int kind, std::vector<BSeg> &out) {
+    out.clear();
+    if (layout == RA_LAYOUT_STRIPED) return false;
+    const int chunks = layout == RA_LAYOUT_ZIGZAG ? 2 * R : R;
+    if (chunks > kMaxBSeg || N > INT32_MAX) return false;
+    std::vector<std::pair<int64_t, BSeg>> work;
+    for (int r = 0; r < R; ++r)
+        for (const Range &f : rank_ranges(N, R, layout, r)) {
+            if (f.b <= f.a) continue;
+            BSeg g;
+            memset(&g, 0, sizeof g);
+            g.f0 = (int32_t)f.a;
+            g.f1 = (int32_t)f.b;
+            g.flags = SEG_FIRST | SEG_FINAL;
+            g.rank = r;
+            int64_t pairs = 0;
+            for (int s = 0; s < R; ++s) {
+                const int j = kind ? (r + s) % R : ((r - s) % R + R) % R;
+                for (const Range &p : rank_ranges(N, R, layout, j)) {
+                    if (p.b <= p.a) continue;
+                    if (causal && (kind ? f.a > p.b - 1 : p.a > f.b - 1)) continue;
+                    pairs += p.b - p.a;
+                }
+            }
+            work.push_back({pairs, g});
+        }
+    std::stable_sort(work.begin(), work.end(),
+                     [](const std::pair<int64_t, BSeg> &x, const std::pair<int64_t, BSeg> &y) { return x.first > y.first; });
+    for (const auto &w : work) out.push_back(w.second);
+    return !out.empty();
+}
+
 // ---------------------------------------------------------------- dispatch
 
 static void fill_common(StepParams &P, const ra_tensor *q, const ra_tensor *k, const ra_tensor *v,
@@ -781,8 +817,29 @@ ra_status ra_ring_sim_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tenso
     cudaError_t e = launch_bwd_rowdot(P, di.sms, st);
     if (e != cudaSuccess) result = cuda_fail(e, "backward D launch");
     else ++t_launches;
+    std::vector<BSeg> segs, kv_segs;
+    if (result == RA_OK && tc && ring_size > 1 && fused_bwd_segments(pb.N, ring_size, layout, causal, 0, segs) &&
+        fused_bwd_segments(pb.N, ring_size, layout, causal, 1, kv_segs)) {
+        // one dQ launch and one dK/dV launch walk every step; gradients stay on chip
+        P.ring_fused = 1;
+        P.ring_R = ring_size;
+        P.ring_layout = layout == RA_LAYOUT_ZIGZAG ? 1 : 0;
+        for (int kind = 0; kind < 2 && result == RA_OK; ++kind) {
+            const std::vector<BSeg> &g = kind == 0 ? segs : kv_segs;
+            P.nseg = (int32_t)g.size();
+            P.flen = 0;
+            for (size_t i = 0; i < g.size(); ++i) {
+                P.seg[i] = g[i];
+                P.flen = std::max<int32_t>(P.flen, g[i].f1 - g[i].f0);
+            }
+            e = launch_attn_bwd_tc(P, kind == 0 ? 1 : 2, di.sms, g_wait_limit_ns, di.err, st);
+            if (e != cudaSuccess) result = cuda_fail(e, "backward launch");
+            else ++t_launches;
+        }
+        delete Pp;
+        return result;
+    }
     const BwdPlan plan(pb.N, ring_size, layout, causal);
-    std::vector<BSeg> segs;
     for (int step = 0; step < ring_size && result == RA_OK; ++step) {
         for (int kind = 0; kind < 2 && result == RA_OK; ++kind) {
             plan.step(step, kind, segs);

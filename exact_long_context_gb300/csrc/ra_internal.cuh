@@ -87,6 +87,7 @@ struct BSeg {
     int32_t f_rank, s_rank;
     int32_t diag;
     int32_t flags;  // SEG_FIRST: no earlier step wrote the fixed range; SEG_FINAL: no later step will
+    int32_t rank;   // fused ring: the rank owning the fixed range (its partners follow from it)
 };
 constexpr int kMaxBSeg = 128;
 
@@ -105,6 +106,8 @@ struct BwdParams {
     int32_t rs;    // rank interleave of the striped layout (1 otherwise)
     int32_t flen;  // length of every segment's fixed range
     int32_t nseg;
+    int32_t ring_fused;           // one launch walks every ring step (contiguous / zigzag)
+    int32_t ring_R, ring_layout;  // fused ring: ring size, RA_LAYOUT_CONTIG (0) or ZIGZAG (1)
     BSeg seg[kMaxBSeg];
 };
 

@@ -52,6 +52,8 @@ CASES = [
     (1, 2, 2, 480, 64, 5, "striped", False, torch.bfloat16),
     (1, 2, 1, 96, 32, 2, "zigzag", True, torch.bfloat16),     # CUDA-core path (D = 32)
     (1, 2, 2, 2048, 128, 8, "zigzag", True, torch.bfloat16),
+    (1, 2, 1, 4096, 128, 2, "zigzag", True, torch.bfloat16),  # chunks of 8 tiles, 4 blocks
+    (1, 2, 2, 3072, 64, 3, "contig", True, torch.bfloat16),
 ]
 
 
