@@ -196,10 +196,13 @@ ra_status ra_attn_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v
  * D = rowsum(dout * O), adds dS K to its own dQ, and returns the block's dK = scale dS^T Q
  * and dV = P^T dout to the block's rank, which sums them over the steps.  Each step
  * applies the forward's causal rule (skipped, diagonal or full blocks; the striped
- * interleave's offset).  One launch of the dQ kernel and one of the dK/dV kernel per step
- * cover every rank; gradients that several steps write are carried between steps in fp32
- * in the workspace.  The sum over steps is the gradient of the whole sequence, so
- * ring_size = 1 (any layout) is ra_attn_bwd.
+ * interleave's offset).  bf16 with D in {64, 128} and a contiguous or zigzag layout of
+ * up to 128 chunks: one dQ launch walks each query chunk's partner blocks over all steps
+ * and one dK/dV launch walks each key chunk's partner ranks, (j + s) mod R at step s
+ * (the reverse ring), with both gradients kept in the kernels across steps.  Otherwise
+ * one launch of each kernel per step covers every rank, and gradients that several steps
+ * write are carried between steps in fp32 in the workspace.  The sum over steps is the
+ * gradient of the whole sequence, so ring_size = 1 (any layout) is ra_attn_bwd.
  *
  *   q, k, v, o, lse  the forward's inputs and outputs (natural sequence order)
  *   dout             [B, Hq, N, D] gradient of O (q's dtype)
