@@ -241,18 +241,22 @@ def run_ours(args, w, ws, rank, local):
         hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
         ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
         hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        if not varlen:
+            # the library's host-buffer call: it stages through device memory and overlaps
+            # the copies in and out with the kernels, head group by head group
+            hws = torch.empty(ra.ring_sim_fwd_host_workspace_bytes(hq, hk, w.ring_size), dtype=torch.uint8,
+                              device=dev)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
 
         def e2e_step():
+            if not varlen:
+                ra.ring_sim_fwd_host(hq, hk, hv, w.ring_size, w.layout, causal=w.causal, scale=w.scale,
+                                     o=ho, lse=hl, workspace=hws, stream=stream)
+                return
             dq.copy_(hq, non_blocking=True)
             dk.copy_(hk, non_blocking=True)
             dv.copy_(hv, non_blocking=True)
-            if varlen:
-                ra.attn_varlen_fwd(dq, dk, dv, cu, causal=w.causal, scale=w.scale, o=o, lse=lse,
-                                   stream=stream)
-            else:
-                ra.ring_sim_fwd(dq, dk, dv, w.ring_size, w.layout, causal=w.causal, scale=w.scale,
-                                o=o, lse=lse, workspace=wsbuf if need else None, stream=stream)
+            ra.attn_varlen_fwd(dq, dk, dv, cu, causal=w.causal, scale=w.scale, o=o, lse=lse, stream=stream)
             ho.copy_(o, non_blocking=True)
             hl.copy_(lse, non_blocking=True)
 

@@ -45,6 +45,7 @@ static ra_status cuda_fail(cudaError_t e, const char *what) {
 __device__ int g_device_error;
 
 static const int kMaxDev = 64;
+static const int kHostGroups = 8;  // head groups of the host-buffer pipeline
 static std::mutex g_mu;
 static int *g_err_ptr[kMaxDev];
 static int g_num_sms[kMaxDev];
@@ -868,6 +869,153 @@ ra_status ra_attn_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v
                       ra_tensor *dv, int causal, float scale, void *workspace, void *stream) {
     return ra_ring_sim_bwd(q, k, v, o, lse, dout, dq, dk, dv, 1, RA_LAYOUT_CONTIG, causal, scale, workspace,
                            stream);
+}
+
+// ---------------------------------------------------------------- host-buffer entry point
+
+// Streams and events of the host-buffer pipeline, created once per device (copies in on
+// one stream, copies out on another, so both directions of the link run at once).
+struct HostPipe {
+    cudaStream_t cin = nullptr, cout = nullptr;
+    cudaEvent_t ev[2 * kHostGroups + 2] = {};
+    bool ready = false;
+};
+static HostPipe g_pipe[kMaxDev];
+static std::mutex g_pipe_mu;
+
+static bool host_pipe(int dev, HostPipe *&hp, std::string &msg) {
+    if (dev < 0 || dev >= kMaxDev) {
+        msg = "device ordinal out of range";
+        return false;
+    }
+    hp = &g_pipe[dev];
+    if (hp->ready) return true;
+    cudaError_t e = cudaStreamCreateWithFlags(&hp->cin, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp->cout, cudaStreamNonBlocking);
+    for (int i = 0; e == cudaSuccess && i < 2 * kHostGroups + 2; ++i)
+        e = cudaEventCreateWithFlags(&hp->ev[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+        msg = std::string("host pipeline set-up: ") + cudaGetErrorString(e);
+        return false;
+    }
+    hp->ready = true;
+    return true;
+}
+
+static bool host_contiguous(const ra_tensor *t) {
+    return t->stride[3] == 1 && t->stride[2] == t->shape[3] && t->stride[1] == t->shape[2] * t->shape[3] &&
+           t->stride[0] == t->shape[1] * t->shape[2] * t->shape[3];
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t ra_ring_sim_fwd_host_workspace_bytes(const ra_tensor *q, const ra_tensor *k, int ring_size) {
+    if (!q || !k || ring_size < 1 || !is_dtype(q->dtype)) return 0;
+    for (int i = 0; i < 4; ++i)
+        if (q->shape[i] < 0 || k->shape[i] < 0) return 0;
+    const size_t es = (size_t)esize(q->dtype);
+    const size_t nq = (size_t)(q->shape[0] * q->shape[1] * q->shape[2] * q->shape[3]);
+    const size_t nk = (size_t)(k->shape[0] * k->shape[1] * k->shape[2] * k->shape[3]);
+    const size_t rows = (size_t)(q->shape[0] * q->shape[1] * q->shape[2]);
+    // device q, o, k, v, lse, and the ring's running result for one head group at most
+    // (every group runs on the caller's stream in turn)
+    return 2 * align256(nq * es) + 2 * align256(nk * es) + align256(rows * sizeof(float)) +
+           (ring_size > 1 ? align256(nq * sizeof(float)) : 0);
+}
+
+ra_status ra_ring_sim_fwd_host(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v, ra_tensor *o,
+                               float *lse, int ring_size, ra_layout layout, int causal, float scale,
+                               void *workspace, size_t workspace_bytes, void *stream) {
+    Problem pb;
+    ra_status s = check_qkvo(q, k, v, o, lse, pb);
+    if (s) return s;
+    if (isnan(scale)) return fail(RA_ERR_INVALID_ARG, "scale is NaN");
+    if ((s = check_ring(pb.N, ring_size, layout))) return s;
+    if (!host_contiguous(q) || !host_contiguous(k) || !host_contiguous(v) || !host_contiguous(o))
+        return fail(RA_ERR_INVALID_ARG, "host tensors must be contiguous [B, H, N, D]");
+    if (pb.B * pb.Hq * pb.N == 0) return RA_OK;
+    const size_t need = ra_ring_sim_fwd_host_workspace_bytes(q, k, ring_size);
+    if (!workspace || workspace_bytes < need)
+        return fail(RA_ERR_INVALID_ARG, "workspace is NULL or smaller than ra_ring_sim_fwd_host_workspace_bytes()");
+    if (reinterpret_cast<uintptr_t>(workspace) % 256)
+        return fail(RA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    DevInfo di;
+    std::string msg;
+    if (!device_info(di, msg)) return fail(RA_ERR_CUDA, msg);
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    HostPipe *hp = nullptr;
+    if (!host_pipe(di.dev, hp, msg)) return fail(RA_ERR_CUDA, msg);
+    const int64_t B = pb.B, Hq = pb.Hq, Hkv = pb.Hkv, N = pb.N, D = pb.D, G = Hq / Hkv;
+    const size_t es = (size_t)esize(pb.dtype);
+    const size_t nq = (size_t)(B * Hq * N * D), nk = (size_t)(B * Hkv * N * D);
+    char *w = static_cast<char *>(workspace);
+    char *dq = w, *dout = dq + align256(nq * es), *dk = dout + align256(nq * es), *dv = dk + align256(nk * es);
+    float *dl = reinterpret_cast<float *>(dv + align256(nk * es));
+    void *ring_ws = ring_size > 1 ? static_cast<void *>(reinterpret_cast<char *>(dl) + align256((size_t)(B * Hq * N) * 4))
+                                  : nullptr;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // head groups of whole KV heads (with their G query heads each)
+    const int ng = (int)std::min<int64_t>(Hkv, kHostGroups);
+    cudaError_t e = cudaEventRecord(hp->ev[2 * kHostGroups], st);  // prior work on the caller's stream
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->cin, hp->ev[2 * kHostGroups], 0);
+    const size_t qrow = (size_t)(N * D) * es;  // bytes of one head's rows
+    for (int g = 0; g < ng && e == cudaSuccess; ++g) {
+        const int64_t k0 = Hkv * g / ng, k1 = Hkv * (g + 1) / ng, q0 = k0 * G, q1 = k1 * G;
+        // in: q, k, v rows of the group, every batch (one 2-D copy each)
+        e = cudaMemcpy2DAsync(dq + q0 * qrow, (size_t)Hq * qrow, static_cast<const char *>(q->data) + q0 * qrow,
+                              (size_t)Hq * qrow, (size_t)(q1 - q0) * qrow, (size_t)B, cudaMemcpyHostToDevice, hp->cin);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(dk + k0 * qrow, (size_t)Hkv * qrow, static_cast<const char *>(k->data) + k0 * qrow,
+                                  (size_t)Hkv * qrow, (size_t)(k1 - k0) * qrow, (size_t)B, cudaMemcpyHostToDevice,
+                                  hp->cin);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(dv + k0 * qrow, (size_t)Hkv * qrow, static_cast<const char *>(v->data) + k0 * qrow,
+                                  (size_t)Hkv * qrow, (size_t)(k1 - k0) * qrow, (size_t)B, cudaMemcpyHostToDevice,
+                                  hp->cin);
+        if (e == cudaSuccess) e = cudaEventRecord(hp->ev[g], hp->cin);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(st, hp->ev[g], 0);
+        if (e != cudaSuccess) break;
+        // compute: the group's heads, viewed inside the full device tensors
+        ra_tensor tq = *q, tk = *k, tv = *v, to = *o;
+        const int64_t sq[4] = {Hq * N * D, N * D, D, 1}, sk[4] = {Hkv * N * D, N * D, D, 1};
+        for (int i = 0; i < 4; ++i) {
+            tq.stride[i] = to.stride[i] = sq[i];
+            tk.stride[i] = tv.stride[i] = sk[i];
+        }
+        tq.shape[1] = to.shape[1] = q1 - q0;
+        tk.shape[1] = tv.shape[1] = k1 - k0;
+        tq.data = dq + q0 * qrow;
+        to.data = dout + q0 * qrow;
+        tk.data = dk + k0 * qrow;
+        tv.data = dv + k0 * qrow;
+        // the group's LSE rows are strided by Hq * N across batches: compute into a
+        // packed [B, group heads, N] slice of the LSE buffer, one batch at a time
+        for (int64_t b = 0; b < B && s == RA_OK; ++b) {
+            ra_tensor bq = tq, bk = tk, bv = tv, bo = to;
+            bq.shape[0] = bk.shape[0] = bv.shape[0] = bo.shape[0] = 1;
+            bq.data = static_cast<char *>(tq.data) + (size_t)b * Hq * qrow;
+            bo.data = static_cast<char *>(to.data) + (size_t)b * Hq * qrow;
+            bk.data = static_cast<char *>(tk.data) + (size_t)b * Hkv * qrow;
+            bv.data = static_cast<char *>(tv.data) + (size_t)b * Hkv * qrow;
+            s = ra_ring_sim_fwd(&bq, &bk, &bv, &bo, dl + (b * Hq + q0) * N, ring_size, layout, causal, scale, ring_ws,
+                                stream);
+        }
+        if (s != RA_OK) return s;
+        e = cudaEventRecord(hp->ev[kHostGroups + g], st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->cout, hp->ev[kHostGroups + g], 0);
+        // out: o rows and LSE of the group
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(static_cast<char *>(o->data) + q0 * qrow, (size_t)Hq * qrow, dout + q0 * qrow,
+                                  (size_t)Hq * qrow, (size_t)(q1 - q0) * qrow, (size_t)B, cudaMemcpyDeviceToHost, hp->cout);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(lse + q0 * N, (size_t)(Hq * N) * 4, dl + q0 * N, (size_t)(Hq * N) * 4,
+                                  (size_t)((q1 - q0) * N) * 4, (size_t)B, cudaMemcpyDeviceToHost, hp->cout);
+    }
+    // the caller's stream sees every copy out complete
+    if (e == cudaSuccess) e = cudaEventRecord(hp->ev[2 * kHostGroups + 1], hp->cout);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, hp->ev[2 * kHostGroups + 1], 0);
+    if (e != cudaSuccess) return cuda_fail(e, "host-buffer pipeline");
+    return RA_OK;
 }
 
 ra_status ra_ulysses_all_to_all(const ra_tensor *in, ra_tensor *out, int sp, int to_heads,

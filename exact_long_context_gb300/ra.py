@@ -57,6 +57,10 @@ def lib() -> ctypes.CDLL:
             L.ra_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
             L.ra_attn_bwd.argtypes = [T, T, T, T, P, T, T, T, T, c_int, c_float, P, P]
             L.ra_attn_bwd.restype = c_int
+            L.ra_ring_sim_fwd_host_workspace_bytes.argtypes = [T, T, c_int]
+            L.ra_ring_sim_fwd_host_workspace_bytes.restype = ctypes.c_size_t
+            L.ra_ring_sim_fwd_host.argtypes = [T, T, T, T, P, c_int, c_int, c_int, c_float, P, ctypes.c_size_t, P]
+            L.ra_ring_sim_fwd_host.restype = c_int
             L.ra_ring_sim_bwd_workspace_bytes.argtypes = [T, T, c_int]
             L.ra_ring_sim_bwd_workspace_bytes.restype = ctypes.c_size_t
             L.ra_ring_sim_bwd.argtypes = [T, T, T, T, P, T, T, T, T, c_int, c_int, c_int, c_float, P, P]
@@ -86,7 +90,7 @@ def _check(status: int):
         raise RaError(status, lib().ra_last_error().decode())
 
 
-def _desc(t: torch.Tensor | None, name: str) -> RaTensor:
+def _desc(t: torch.Tensor | None, name: str, host: bool = False) -> RaTensor:
     d = RaTensor()
     if t is None:
         return d
@@ -98,8 +102,8 @@ def _desc(t: torch.Tensor | None, name: str) -> RaTensor:
         d.dtype = RA_BF16
     else:
         raise TypeError(f"{name}: dtype {t.dtype} (want float32 or bfloat16)")
-    if t.numel() and not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.numel() and t.is_cuda == host:
+        raise ValueError(f"{name} must be a {'host' if host else 'CUDA'} tensor")
     d.data = t.data_ptr() if t.numel() else None
     for i in range(4):
         d.shape[i] = t.shape[i]
@@ -259,6 +263,34 @@ def ring_sim_fwd(q, k, v, ring_size: int, layout="contig", causal=False, scale=N
                                  ctypes.byref(do), _ptr(lse), int(ring_size), LAYOUTS[layout],
                                  int(bool(causal)), float(scale or 0.0), _ptr(workspace),
                                  _stream(stream)))
+    return o, lse
+
+
+def ring_sim_fwd_host_workspace_bytes(q, k, ring_size: int) -> int:
+    """Device workspace bytes ring_sim_fwd_host needs (q, k: host tensors)."""
+    return int(lib().ra_ring_sim_fwd_host_workspace_bytes(ctypes.byref(_desc(q, "q", host=True)),
+                                                          ctypes.byref(_desc(k, "k", host=True)),
+                                                          int(ring_size)))
+
+
+def ring_sim_fwd_host(q, k, v, ring_size: int = 1, layout="contig", causal=False, scale=None, o=None,
+                      lse=None, workspace=None, stream=None):
+    """ring_sim_fwd on contiguous HOST tensors (pinned memory for asynchronous copies):
+    returns host (o, lse); the results are valid once `stream` has reached the call."""
+    B, Hq, N, _ = q.shape
+    if o is None:
+        o = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    if lse is None:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32).pin_memory()
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or lse.is_cuda:
+        raise ValueError("lse must be a contiguous float32 host tensor")
+    need = ring_sim_fwd_host_workspace_bytes(q, k, ring_size)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    d = [_desc(t, n, host=True) for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"))]
+    _check(lib().ra_ring_sim_fwd_host(*(ctypes.byref(x) for x in d), _ptr(lse), int(ring_size), LAYOUTS[layout],
+                                      int(bool(causal)), float(scale or 0.0), _ptr(workspace),
+                                      workspace.numel(), _stream(stream)))
     return o, lse
 
 

@@ -187,6 +187,31 @@ ra_status ra_attn_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v
                       ra_tensor *dv, int causal, float scale, void *workspace, void *stream);
 
 /*
+ * ra_ring_sim_fwd_host - ra_ring_sim_fwd on HOST buffers (no counterpart in the pages:
+ * the call a program makes when its tensors live in host memory).
+ *
+ * q, k, v, o and lse are host pointers (page-locked memory lets the copies run
+ * asynchronously; pageable memory works but each copy then waits).  The tensors must be
+ * contiguous [B, H, N, D]; lse is [B, Hq, N] float32.  The call stages through the
+ * caller's device workspace and pipelines by groups of whole KV heads (up to 8): the
+ * next group's q/k/v go in on one internal stream while the current group computes on
+ * `stream`, and finished groups' o/lse come out on another, so both directions of the
+ * host link overlap the kernels.  The call is ordered on `stream`: the host buffers may
+ * be read or reused once `stream` has reached this point (e.g. after
+ * cudaStreamSynchronize).  Calls for one device are serialised on the host while they
+ * enqueue.
+ *
+ *   workspace  device buffer of ra_ring_sim_fwd_host_workspace_bytes(q, k, ring_size)
+ *              bytes, 256-byte aligned, owned by the caller
+ * Errors: as ra_ring_sim_fwd, plus RA_ERR_INVALID_ARG for non-contiguous tensors or a
+ *   missing / small / misaligned workspace.
+ */
+size_t ra_ring_sim_fwd_host_workspace_bytes(const ra_tensor *q, const ra_tensor *k, int ring_size);
+ra_status ra_ring_sim_fwd_host(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v, ra_tensor *o,
+                               float *lse, int ring_size, ra_layout layout, int causal, float scale,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * ra_ring_sim_bwd - gradients of ra_ring_sim_fwd on the ring schedule of ring_size
  * simulated ranks, on one GPU.
  *
