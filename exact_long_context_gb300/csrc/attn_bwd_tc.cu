@@ -30,6 +30,7 @@
 // backward is one segment.  On a ring, the gradient of a range that earlier or later
 // steps also write is carried between steps in fp32 running buffers (store_grad_chunk).
 #include <climits>
+#include <cstring>
 
 #include "tc_common.cuh"
 
@@ -624,6 +625,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    // the dK/dV kernel reads only inputs ready before this launch: it may start on the
+    // SMs this grid frees
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0) {
         if (lane == 0) {
@@ -865,7 +869,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // per element-wise warp: the current query tile's LSE (log2 units) and D values of its columns
     float *s_stage = reinterpret_cast<float *>(base_ptr + C::BAR_OFF + 256);  // [8 warps][2][64]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if ((int)blockIdx.x >= total) return;
+    if ((int)blockIdx.x >= total) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        return;
+    }
     volatile int32_t *abort_flag = &bars->abort;
     const int G = P.Hq / P.Hkv;
     const int tps = (P.flen + kT - 1) / kT;
@@ -1125,13 +1132,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
+    // when launched to overlap the dQ kernel's tail, finish only after it has: work later
+    // in the stream then sees both kernels' writes (a no-op for a plain launch)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace tcb
 
 template <int HD>
 static cudaError_t launch_bwd_tc_hd(const BwdParams &P, int parts, int num_sms, int64_t wait_ns, int *err,
-                                    cudaStream_t stream) {
+                                    cudaStream_t stream, bool after_dq) {
     using C = tcb::BCfg<HD>;
     static int configured_mask = 0;
     int dev = 0;
@@ -1172,23 +1182,39 @@ static cudaError_t launch_bwd_tc_hd(const BwdParams &P, int parts, int num_sms, 
         if (e != cudaSuccess) return e;
     }
     if (parts & 2) {
-        if (P.ring_fused)
-            tcb::bwd_dkdv_tc_kernel<HD, true><<<gkv, tcb::kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, P,
-                                                                                          (int)tkv, wait_ns, err);
-        else
-            tcb::bwd_dkdv_tc_kernel<HD, false><<<gkv, tcb::kThreads, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, P,
-                                                                                           (int)tkv, wait_ns, err);
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof cfg);
+        cfg.gridDim = dim3(gkv);
+        cfg.blockDim = dim3(tcb::kThreads);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        if (after_dq || (parts & 1)) {  // overlaps the tail of the dQ kernel just launched (no data between them)
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+        }
+        const int itkv = (int)tkv;
+        cudaError_t e = P.ring_fused
+                            ? cudaLaunchKernelEx(&cfg, tcb::bwd_dkdv_tc_kernel<HD, true>, mq, mk, mv, mdo, P, itkv,
+                                                 wait_ns, err)
+                            : cudaLaunchKernelEx(&cfg, tcb::bwd_dkdv_tc_kernel<HD, false>, mq, mk, mv, mdo, P, itkv,
+                                                 wait_ns, err);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
 
 // The dQ kernel (parts & 1) and the dK/dV kernel (parts & 2) over the segments in P (the
 // D vector is computed before).
+// after_dq: the launch directly follows this call's dQ kernel on `stream`, so the dK/dV
+// kernel may start on the SMs the dQ grid frees (programmatic dependent launch).
 cudaError_t launch_attn_bwd_tc(const BwdParams &P, int parts, int num_sms, int64_t wait_ns, int *err,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, bool after_dq) {
     if (P.B <= 0 || P.Hq <= 0 || P.nseg <= 0 || P.flen <= 0) return cudaSuccess;
-    if (P.D == 128) return launch_bwd_tc_hd<128>(P, parts, num_sms, wait_ns, err, stream);
-    if (P.D == 64) return launch_bwd_tc_hd<64>(P, parts, num_sms, wait_ns, err, stream);
+    if (P.D == 128) return launch_bwd_tc_hd<128>(P, parts, num_sms, wait_ns, err, stream, after_dq);
+    if (P.D == 64) return launch_bwd_tc_hd<64>(P, parts, num_sms, wait_ns, err, stream, after_dq);
     return cudaErrorInvalidValue;
 }
 

@@ -21,7 +21,7 @@ cudaError_t launch_attn_bwd_simt(const BwdParams &P, int parts, cudaStream_t str
 cudaError_t launch_bwd_rowdot(const BwdParams &P, int num_sms, cudaStream_t stream);
 cudaError_t launch_ulysses(const UlyssesParams &P, int num_sms, cudaStream_t stream);
 cudaError_t launch_attn_bwd_tc(const BwdParams &P, int parts, int num_sms, int64_t wait_ns, int *err,
-                               cudaStream_t stream);
+                               cudaStream_t stream, bool after_dq);
 cudaError_t launch_fill_identity(void *o, int o_bf16, const int64_t *so, float *lse, int B, int H,
                                  int N, int D, int r0, int r1, int num_sms, cudaStream_t stream);
 }  // namespace ra
@@ -833,7 +833,7 @@ ra_status ra_ring_sim_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tenso
                 P.seg[i] = g[i];
                 P.flen = std::max<int32_t>(P.flen, g[i].f1 - g[i].f0);
             }
-            e = launch_attn_bwd_tc(P, kind == 0 ? 1 : 2, di.sms, g_wait_limit_ns, di.err, st);
+            e = launch_attn_bwd_tc(P, kind == 0 ? 1 : 2, di.sms, g_wait_limit_ns, di.err, st, kind == 1);
             if (e != cudaSuccess) result = cuda_fail(e, "backward launch");
             else ++t_launches;
         }
@@ -842,6 +842,7 @@ ra_status ra_ring_sim_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tenso
     }
     const BwdPlan plan(pb.N, ring_size, layout, causal);
     for (int step = 0; step < ring_size && result == RA_OK; ++step) {
+        int dq_launches_this_step = 0;
         for (int kind = 0; kind < 2 && result == RA_OK; ++kind) {
             plan.step(step, kind, segs);
             for (size_t f = 0; f < segs.size() && result == RA_OK; f += kMaxBSeg) {
@@ -853,8 +854,12 @@ ra_status ra_ring_sim_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tenso
                     P.flen = std::max<int32_t>(P.flen, segs[f + i].f1 - segs[f + i].f0);
                 }
                 const int parts = kind == 0 ? 1 : 2;
-                e = tc ? launch_attn_bwd_tc(P, parts, di.sms, g_wait_limit_ns, di.err, st)
+                // a step's dK/dV launch follows its dQ launch directly, unless the dQ
+                // segments took several launches
+                e = tc ? launch_attn_bwd_tc(P, parts, di.sms, g_wait_limit_ns, di.err, st,
+                                            kind == 1 && f == 0 && dq_launches_this_step == 1)
                        : launch_attn_bwd_simt(P, parts, st);
+                if (kind == 0) ++dq_launches_this_step;
                 if (e != cudaSuccess) result = cuda_fail(e, "backward launch");
                 else ++t_launches;
             }
