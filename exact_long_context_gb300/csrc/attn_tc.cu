@@ -36,6 +36,7 @@
 // DERR_TIMEOUT in the device error word, every role stops, waits (bounded) for its
 // own copies and MMAs in flight, and the tensor memory is released before exit.
 #include <cuda.h>
+#include <stddef.h>
 #include <string.h>
 
 #include <algorithm>
@@ -60,8 +61,9 @@ struct Cfg {
     static constexpr int NSTAGE = NSLOT / 2;            // a stage = (V_t, K_t+1) buffer pair
     static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + HD;
     static constexpr uint32_t TM_COLS = 512;
-    static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM_BYTES = 1024 + (2 + NSLOT) * TILE_BYTES + BAR_BYTES;
+    static constexpr int STAGE_BYTES = 2 * SLAB_BYTES;  // O staging: 128 rows x 64 columns per half
+    static constexpr int BAR_BYTES = 512;
+    static constexpr int SMEM_BYTES = 1024 + (2 + NSLOT) * TILE_BYTES + STAGE_BYTES + BAR_BYTES;
 };
 
 struct Bars {
@@ -70,14 +72,17 @@ struct Bars {
     uint64_t full[8];
     uint64_t empty[8];
     uint64_t s_full[2];
-    uint64_t p_full[2];
+    uint64_t it_full[4], it_empty[4];  // decoded-item ring: producer -> MMA issuer
+    int32_t it_info[4][4];             // nh[0], nh[1], nmax, skip0 (nmax < 0: no more items)
+    uint64_t st_full[2];  // O staging slab of half h written by its 4 warps
+    uint64_t st_free[2];  // ... and read by the bulk store issued from it
     uint64_t o_full[2];
     uint64_t drain;
     uint32_t tmem_base;
     int32_t abort;
     uint32_t p_count[2];  // P_h tiles published by the softmax warps (4 per tile)
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(sizeof(Bars) <= 512, "barrier block");
 
 // Register split between warpgroups (launch: 168 per thread x 384 threads = 64512).
 // Warpgroup 0 (TMA + MMA warps) gives back to 88, the two softmax warpgroups take 208:
@@ -136,6 +141,18 @@ struct Item {
     }
     __device__ __forceinline__ int last(int hh) const { return (!hh && skip0 == nmax - 1) ? nmax - 2 : nmax - 1; }
 };
+
+// What the MMA issuer needs of an item (handed over by the producer through shared memory).
+struct MItem {
+    int nh[2], nmax, skip0;
+    __device__ __forceinline__ bool part(int hh, int t) const {
+        return hh ? nh[1] > 0 : (nh[0] > 0 && t != skip0);
+    }
+    __device__ __forceinline__ int last(int hh) const { return (!hh && skip0 == nmax - 1) ? nmax - 2 : nmax - 1; }
+};
+constexpr int kItemRing = 4;  // decoded items in flight from the producer to the MMA issuer
+static_assert(sizeof(Bars::it_info) / sizeof(Bars::it_info[0]) == kItemRing, "item ring");
+static_assert(offsetof(Bars, it_info) % 16 == 0, "16-byte item records");
 
 // Fused ring (contiguous or zigzag layout): the key ranges rank r's query chunk ending at
 // q1 sees at step s, those of rank (r - s) mod R, with the forward's causal rule (a range
@@ -342,7 +359,8 @@ __device__ __forceinline__ bool decode_item(const StepParams &P, int L, int sub,
 template <int HD, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ StepParams P) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const __grid_constant__ StepParams P) {
     using C = Cfg<HD>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -350,7 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *base_ptr = smem_raw + (base - raw);
     const uint32_t sQ = base;
     const uint32_t sKV = base + 2 * C::TILE_BYTES;
-    Bars *bars = reinterpret_cast<Bars *>(base_ptr + (2 + C::NSLOT) * C::TILE_BYTES);
+    const uint32_t sStage = base + (2 + C::NSLOT) * C::TILE_BYTES;  // 1024-byte aligned
+    Bars *bars = reinterpret_cast<Bars *>(base_ptr + (2 + C::NSLOT) * C::TILE_BYTES + C::STAGE_BYTES);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int total = P.total_items;
@@ -372,10 +391,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&bars->q_full[hh]), 1);
             mbar_init(smem_u32(&bars->q_empty[hh]), 1);
             mbar_init(smem_u32(&bars->s_full[hh]), 1);
-            mbar_init(smem_u32(&bars->p_full[hh]), 4);  // one elected lane per softmax warp
+            mbar_init(smem_u32(&bars->st_full[hh]), 4);  // one elected lane per softmax warp
+            mbar_init(smem_u32(&bars->st_free[hh]), 1);
             mbar_init(smem_u32(&bars->o_full[hh]), 1);
         }
         mbar_init(b_drain, 1);
+#pragma unroll
+        for (int i = 0; i < kItemRing; ++i) {
+            mbar_init(smem_u32(&bars->it_full[i]), 1);
+            mbar_init(smem_u32(&bars->it_empty[i]), 1);
+        }
         bars->p_count[0] = bars->p_count[1] = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -400,6 +425,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             uint32_t issued = 0, last_ph = 0;  // per-slot bit sets
             uint32_t qcnt[2] = {0u, 0u};       // Q_h loads issued
+            uint32_t icnt = 0;                 // items handed to the MMA issuer
+            // hand item (nh0, nh1, nmax, skip0) to the MMA issuer once its ring slot is free
+            auto hand_over = [&](int a, int b, int c, int d) -> bool {
+                const int islot = icnt & (kItemRing - 1);
+                if (icnt >= (uint32_t)kItemRing &&
+                    !wait_phase(smem_u32(&bars->it_empty[islot]), (icnt / kItemRing - 1u) & 1u, abort_flag,
+                                P.wait_limit_ns, P.err))
+                    return false;
+                *reinterpret_cast<int4 *>(&bars->it_info[islot][0]) = make_int4(a, b, c, d);
+                mbar_arrive(smem_u32(&bars->it_full[islot]));  // release: the fields are visible
+                ++icnt;
+                return true;
+            };
             bool ok = true;
             for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, part)
                 const int L = snake_item(k2 >> 1);
@@ -407,6 +445,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 Item it;
                 if (!decode_item(P, L, k2 & 1, it)) continue;
                 if (it.nmax == 0) continue;
+                if (!hand_over(it.nh[0], it.nh[1], it.nmax, it.skip0)) {
+                    ok = false;
+                    break;
+                }
                 // Stages of an item: (K_0), then (V_t, K_t+1) for t = 0..n-1 (the last one
                 // V only).  Stage (K_0) first - it only needs a free buffer pair - then Q,
                 // which waits until the previous item has issued its last Q K^T.
@@ -469,6 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            if (ok) ok = hand_over(0, 0, -1, 0);  // no more items
             if (!ok) {  // wind down: let every copy this thread issued land
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh)
@@ -508,12 +551,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t qcnt[2] = {0u, 0u};  // Q_h loads consumed
             uint32_t pcnt[2] = {0u, 0u};  // P_h tiles consumed
             bool ok = true;
-            for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, part)
-                const int L = snake_item(k2 >> 1);
-                if (L >= total) continue;
-                Item it;
-                if (!decode_item(P, L, k2 & 1, it)) continue;
-                if (it.nmax == 0) continue;
+            // items come decoded from the producer (which runs ahead): the MMA thread's
+            // own decode would sit between an item's last P V and the next one's Q K^T
+            uint32_t icnt = 0;
+            for (;;) {
+                MItem it;
+                {
+                    const int islot = icnt & (kItemRing - 1);
+                    ok = wait_phase(smem_u32(&bars->it_full[islot]), (icnt / kItemRing) & 1u, abort_flag,
+                                    P.wait_limit_ns, P.err);
+                    if (!ok) break;
+                    const int4 v = *reinterpret_cast<const int4 *>(&bars->it_info[islot][0]);
+                    it.nh[0] = v.x;
+                    it.nh[1] = v.y;
+                    it.nmax = v.z;
+                    it.skip0 = v.w;
+                    mbar_arrive(smem_u32(&bars->it_empty[islot]));
+                    ++icnt;
+                }
+                if (it.nmax < 0) break;  // no more items
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     if (it.nh[hh] == 0 || !ok) continue;
@@ -575,6 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ph ^= 1u;
                     }
                 }
+                if (!ok) break;
             }
             // every MMA this thread issued completes before tensor memory is released
             mma_commit(b_drain);
@@ -593,6 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t b_o = smem_u32(&bars->o_full[hh]);
         const float sl2 = P.scale_log2;
         uint32_t scnt = 0, ocnt = 0;  // S_h tiles and O_h results seen
+        uint32_t spass = 0;           // O staging passes of this half
         bool ok = true;
         for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, part)
             const int L = snake_item(k2 >> 1);
@@ -742,6 +800,82 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (merge) w = merge_weights(lse_a, lse_b);
             const bool use_prev = merge && w.wa != 0.f;
             const float wb = w.wb * inv;
+            // Final rows of a half that lies wholly inside its segment (or is clipped by the
+            // end of the tensor) leave through shared memory and bulk tensor stores, 64
+            // columns at a time: row-per-thread global stores would issue 32 scattered
+            // 16-byte pieces per instruction and clog the SM's memory pipeline.
+            const bool tma_o = final_ && P.o_tma && (first_row + BM <= it.q1 || it.q1 == P.N / P.rs);
+            if (tma_o) {
+                const int srow = quarter * 32 + lane;
+                const uint32_t slab = sStage + hh * C::SLAB_BYTES;
+                const bool issuer = quarter == 0 && lane == 0;
+#pragma unroll 1
+                for (int c2 = 0; c2 < HD / 64 && ok; ++c2) {
+                    uint32_t pk[2][16];
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int c = c2 * 2 + cc;
+                        uint32_t o[32];
+                        tmem_ld32(tO + c * 32, o);
+                        float x[32];
+                        if (use_prev) {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4) {
+                                const float4 a = __ldcs(reinterpret_cast<const float4 *>(arow + c * 32 + i));
+                                x[i] = w.wa * a.x;
+                                x[i + 1] = w.wa * a.y;
+                                x[i + 2] = w.wa * a.z;
+                                x[i + 3] = w.wa * a.w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) x[i] = 0.f;
+                        }
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            pk[cc][i] = pack_bf16x2(fmaf(wb, __uint_as_float(o[2 * i]), x[2 * i]),
+                                                    fmaf(wb, __uint_as_float(o[2 * i + 1]), x[2 * i + 1]));
+                    }
+                    // the slab is free once the previous bulk store from it has read it
+                    if (spass > 0) {
+                        if (issuer) {
+                            bulk_wait_read0();
+                            mbar_arrive(smem_u32(&bars->st_free[hh]));
+                        }
+                        ok = __all_sync(0xffffffffu, wait_phase(smem_u32(&bars->st_free[hh]), (spass - 1u) & 1u,
+                                                                abort_flag, P.wait_limit_ns, P.err));
+                        if (!ok) break;
+                    }
+                    // 128-byte swizzle, as the tensor map expects: 16-byte piece j of row r
+                    // sits at piece j ^ (r mod 8)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t a = slab + srow * 128 + ((uint32_t)(j ^ (srow & 7)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                                     "r"(pk[j >> 2][(j & 3) * 4]), "r"(pk[j >> 2][(j & 3) * 4 + 1]),
+                                     "r"(pk[j >> 2][(j & 3) * 4 + 2]), "r"(pk[j >> 2][(j & 3) * 4 + 3])
+                                     : "memory");
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&bars->st_full[hh]));
+                    if (issuer) {
+                        ok = wait_phase(smem_u32(&bars->st_full[hh]), spass & 1u, abort_flag, P.wait_limit_ns,
+                                        P.err);
+                        if (ok) {
+                            tma_store_5d(&tm_o, slab, c2 * 64, it.q_rank, first_row, it.h, it.b);
+                            bulk_commit();
+                        }
+                    }
+                    // converged again (and agreed on ok) before the next warp-wide load
+                    ok = __all_sync(0xffffffffu, ok);
+                    ++spass;
+                }
+                if (!ok) break;
+                if (valid) P.lse[lrow] = first ? lse_b : w.L;
+                continue;
+            }
             __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(P.o) + (int64_t)it.b * P.so[0] +
                                   (int64_t)it.h * P.so[1] + (int64_t)pos * P.so[2];
 #pragma unroll 1
@@ -787,6 +921,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    // the bulk stores of O issued by a half's first thread are complete before exit
+    if (warp >= 4 && (warp & 3) == 0 && lane == 0) bulk_wait0();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -825,11 +961,14 @@ static cudaError_t launch_tc_hd(const StepParams &P, int blocks_y, int num_sms,
         if (e != cudaSuccess) return e;
         configured_mask |= 1 << (dev & 31);
     }
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!encode_map(&mq, P.q, P.B, P.Hq, P.N, P.D, P.sq, P.rs) ||
         !encode_map(&mk, P.k, P.B, P.Hkv, P.N, P.D, P.sk, P.rs) ||
         !encode_map(&mv, P.v, P.B, P.Hkv, P.N, P.D, P.sv, P.rs))
         return cudaErrorInvalidValue;
+    // O through bulk tensor stores when its layout allows a map (else row stores)
+    const bool o_map = encode_map(&mo, P.o, P.B, P.Hq, P.N, P.D, P.so, P.rs);
+    if (!o_map) memset(&mo, 0, sizeof mo);
     // Items: pairs of blocks for a ring step (its tail overlaps the next step's launch)
     // or when the pairs fill their rounds over the persistent grid to 93 %; single
     // blocks (heaviest first) otherwise, and for packed batches.
@@ -846,6 +985,7 @@ static cudaError_t launch_tc_hd(const StepParams &P, int blocks_y, int num_sms,
     StepParams Q = P;
     Q.total_items = (int32_t)total;
     Q.pair_items = use_pairs ? 1 : 0;
+    Q.o_tma = o_map ? 1 : 0;
     const int grid = (int)std::min<int64_t>(total, (int64_t)num_sms);
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
@@ -860,8 +1000,8 @@ static cudaError_t launch_tc_hd(const StepParams &P, int blocks_y, int num_sms,
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    if (P.ring_fused) return cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel<HD, true>, mq, mk, mv, Q);
-    return cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel<HD, false>, mq, mk, mv, Q);
+    if (P.ring_fused) return cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel<HD, true>, mq, mk, mv, mo, Q);
+    return cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel<HD, false>, mq, mk, mv, mo, Q);
 }
 
 cudaError_t launch_attn_tc(const StepParams &P, int blocks_y, int num_sms, cudaStream_t stream) {

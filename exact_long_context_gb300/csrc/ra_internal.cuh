@@ -55,6 +55,7 @@ struct StepParams {
     int32_t ring_fused;      // one launch walks every ring step: Seg = a query chunk of rank Seg::rank
     int32_t ring_R, ring_layout;  // fused ring: ring size, RA_LAYOUT_CONTIG (0) or ZIGZAG (1)
     int32_t rs;              // rank interleave stride of the sequence axis (1 unless striped)
+    int32_t o_tma;           // tensor-core kernel: final O rows leave through bulk tensor stores
     int64_t wait_limit_ns;
     int *err;  // device error word
     Seg seg[kMaxSeg];
