@@ -132,8 +132,11 @@ struct Item {
     int nh[2];  // key tiles each half takes part in
     int nmax;   // key tiles of the item (T)
     int T0;     // tiles of the first step (the only one with a diagonal range)
-    int skip0;  // the one tile half 0 sits out (the last of the first step), or -1
+    int skip0;  // the one tile half 0 sits out, or -1
+    int rev;    // the first `rev` tiles are walked last key tile first (0: in key order)
     KTiles kt;  // the first step's key ranges
+    // key tile of the item's t-th tile
+    __device__ __forceinline__ int tile(int t) const { return t < rev ? rev - 1 - t : t; }
     // Half 1 (the later rows) takes part in every tile; half 0 in every tile but the last
     // of the first step when that tile starts past its last row.
     __device__ __forceinline__ bool part(int hh, int t) const {
@@ -292,6 +295,7 @@ __device__ __forceinline__ bool decode_item(const StepParams &P, int L, int sub,
     it.nh[0] = it.nh[1] = 0;
     it.T0 = 0;
     it.skip0 = -1;
+    it.rev = 0;
     if (lb < 0) return true;
     const Seg &S = P.seg[si];
     it.rank = S.rank;
@@ -329,8 +333,19 @@ __device__ __forceinline__ bool decode_item(const StepParams &P, int L, int sub,
     // the first step: each half a prefix of its tiles; the later steps (fused ring): every
     // tile for both halves (their ranges lie wholly before or wholly after the chunk)
     it.T0 = max(it.nh[0], it.nh[1]);
-    // half 1 sees every first-step tile (its rows come later); half 0 at most one fewer
-    it.skip0 = (it.nh[0] > 0 && it.nh[0] < it.T0) ? it.T0 - 1 : -1;
+    // half 1 sees every first-step tile (its rows come later); half 0 at most one fewer:
+    // the last one.  Outside the fused ring the item walks its tiles last first, so that
+    // half 0 sits out the first tile: the halves start staggered (half 0's first S is
+    // computed before half 1's first P is in) and end together, and neither half's
+    // epilogue delays the other's start on the next item.
+    if (it.nh[0] > 0 && it.nh[0] < it.T0) {
+        if (P.ring_fused) {
+            it.skip0 = it.T0 - 1;
+        } else {
+            it.skip0 = 0;
+            it.rev = it.T0;
+        }
+    }
     int later = 0;
     if (P.ring_fused && it.T0 > 0)
         for (int s = 1; s < P.ring_R; ++s) {
@@ -468,14 +483,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t vbuf = sKV + (2 * slot) * C::TILE_BYTES;
                     const uint32_t kbuf = sKV + (2 * slot + 1) * C::TILE_BYTES;
                     if (has_v) {
-                        const int vs = FUSED ? vstart : it.kt.start(st);
+                        const int vs = FUSED ? vstart : it.kt.start(it.tile(st));
 #pragma unroll
                         for (int c = 0; c < C::SLABS; ++c)
                             tma_load_5d(vbuf + c * C::SLAB_BYTES, &tm_v, b_full, c * 64,
                                         it.kv_rank, vs, it.hk, it.b);
                     }
                     if (has_k) {
-                        const int ks = FUSED ? cur.start() : it.kt.start(st + 1);
+                        const int ks = FUSED ? cur.start() : it.kt.start(it.tile(st + 1));
                         if constexpr (FUSED) {
                             vstart = ks;
                             cursor_next(P, it, cur);
@@ -674,8 +689,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (FUSED) cursor_begin(P, it, cur);
             bool first_tile = true;
             for (int t = 0; t < it.nmax; ++t) {
-                const int ks = FUSED ? cur.start() : it.kt.start(t);
-                const int ke = FUSED ? cur.end() : it.kt.range_end(t);
+                const int ks = FUSED ? cur.start() : it.kt.start(it.tile(t));
+                const int ke = FUSED ? cur.end() : it.kt.range_end(it.tile(t));
                 if constexpr (FUSED) cursor_next(P, it, cur);
                 if (!it.part(hh, t)) continue;
                 ok = wait_phase(b_s, scnt & 1u, abort_flag, P.wait_limit_ns, P.err);
