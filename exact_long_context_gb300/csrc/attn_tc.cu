@@ -622,7 +622,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t vb = sKV + (2 * slot) * C::TILE_BYTES;
                     const uint32_t kb = sKV + (2 * slot + 1) * C::TILE_BYTES;
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        // outside the fused ring half 1 starts first (half 0 sits out the
+                        // item's first tile), and it is served first in every tile
+                        const int hh = FUSED ? h2 : 1 - h2;
                         if (it.part(hh, t)) {
                             ++pcnt[hh];
                             ok = wait_count(&bars->p_count[hh], 4u * pcnt[hh], abort_flag,
