@@ -61,7 +61,7 @@ struct Cfg {
     static constexpr int NSTAGE = NSLOT / 2;            // a stage = (V_t, K_t+1) buffer pair
     static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + HD;
     static constexpr uint32_t TM_COLS = 512;
-    static constexpr int STAGE_BYTES = 2 * SLAB_BYTES;  // O staging: 128 rows x 64 columns per half
+    static constexpr int STAGE_BYTES = 8 * 4096;  // O staging: 2 x (32 rows x 32 columns) per softmax warp
     static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM_BYTES = 1024 + (2 + NSLOT) * TILE_BYTES + STAGE_BYTES + BAR_BYTES;
 };
@@ -74,8 +74,6 @@ struct Bars {
     uint64_t s_full[2];
     uint64_t it_full[4], it_empty[4];  // decoded-item ring: producer -> MMA issuer
     int32_t it_info[4][4];             // nh[0], nh[1], nmax, skip0 (nmax < 0: no more items)
-    uint64_t st_full[2];  // O staging slab of half h written by its 4 warps
-    uint64_t st_free[2];  // ... and read by the bulk store issued from it
     uint64_t o_full[2];
     uint64_t drain;
     uint32_t tmem_base;
@@ -406,8 +404,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&bars->q_full[hh]), 1);
             mbar_init(smem_u32(&bars->q_empty[hh]), 1);
             mbar_init(smem_u32(&bars->s_full[hh]), 1);
-            mbar_init(smem_u32(&bars->st_full[hh]), 4);  // one elected lane per softmax warp
-            mbar_init(smem_u32(&bars->st_free[hh]), 1);
             mbar_init(smem_u32(&bars->o_full[hh]), 1);
         }
         mbar_init(b_drain, 1);
@@ -668,7 +664,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t b_o = smem_u32(&bars->o_full[hh]);
         const float sl2 = P.scale_log2;
         uint32_t scnt = 0, ocnt = 0;  // S_h tiles and O_h results seen
-        uint32_t spass = 0;           // O staging passes of this half
         bool ok = true;
         for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, part)
             const int L = snake_item(k2 >> 1);
@@ -819,78 +814,58 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool use_prev = merge && w.wa != 0.f;
             const float wb = w.wb * inv;
             // Final rows of a half that lies wholly inside its segment (or is clipped by the
-            // end of the tensor) leave through shared memory and bulk tensor stores, 64
-            // columns at a time: row-per-thread global stores would issue 32 scattered
+            // end of the tensor) leave through shared memory and bulk tensor stores: each warp
+            // stores its 32 rows 32 columns at a time from two 2 KiB buffers of its own, so no
+            // warp waits for another.  Row-per-thread global stores would issue 32 scattered
             // 16-byte pieces per instruction and clog the SM's memory pipeline.
             const bool tma_o = final_ && P.o_tma && (first_row + BM <= it.q1 || it.q1 == P.N / P.rs);
             if (tma_o) {
-                const int srow = quarter * 32 + lane;
-                const uint32_t slab = sStage + hh * C::SLAB_BYTES;
-                const bool issuer = quarter == 0 && lane == 0;
+                const uint32_t wbuf = sStage + (uint32_t)(hh * 4 + quarter) * 4096u;
 #pragma unroll 1
-                for (int c2 = 0; c2 < HD / 64 && ok; ++c2) {
-                    uint32_t pk[2][16];
+                for (int c = 0; c < HD / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c * 32, o);
+                    float x[32];
+                    if (use_prev) {
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int c = c2 * 2 + cc;
-                        uint32_t o[32];
-                        tmem_ld32(tO + c * 32, o);
-                        float x[32];
-                        if (use_prev) {
-#pragma unroll
-                            for (int i = 0; i < 32; i += 4) {
-                                const float4 a = __ldcs(reinterpret_cast<const float4 *>(arow + c * 32 + i));
-                                x[i] = w.wa * a.x;
-                                x[i + 1] = w.wa * a.y;
-                                x[i + 2] = w.wa * a.z;
-                                x[i + 3] = w.wa * a.w;
-                            }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) x[i] = 0.f;
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 a = __ldcs(reinterpret_cast<const float4 *>(arow + c * 32 + i));
+                            x[i] = w.wa * a.x;
+                            x[i + 1] = w.wa * a.y;
+                            x[i + 2] = w.wa * a.z;
+                            x[i + 3] = w.wa * a.w;
                         }
-                        tmem_ld_wait();
+                    } else {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            pk[cc][i] = pack_bf16x2(fmaf(wb, __uint_as_float(o[2 * i]), x[2 * i]),
-                                                    fmaf(wb, __uint_as_float(o[2 * i + 1]), x[2 * i + 1]));
+                        for (int i = 0; i < 32; ++i) x[i] = 0.f;
                     }
-                    // the slab is free once the previous bulk store from it has read it
-                    if (spass > 0) {
-                        if (issuer) {
-                            bulk_wait_read0();
-                            mbar_arrive(smem_u32(&bars->st_free[hh]));
-                        }
-                        ok = __all_sync(0xffffffffu, wait_phase(smem_u32(&bars->st_free[hh]), (spass - 1u) & 1u,
-                                                                abort_flag, P.wait_limit_ns, P.err));
-                        if (!ok) break;
-                    }
-                    // 128-byte swizzle, as the tensor map expects: 16-byte piece j of row r
-                    // sits at piece j ^ (r mod 8)
+                    tmem_ld_wait();
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t a = slab + srow * 128 + ((uint32_t)(j ^ (srow & 7)) << 4);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
-                                     "r"(pk[j >> 2][(j & 3) * 4]), "r"(pk[j >> 2][(j & 3) * 4 + 1]),
-                                     "r"(pk[j >> 2][(j & 3) * 4 + 2]), "r"(pk[j >> 2][(j & 3) * 4 + 3])
+                    for (int i = 0; i < 16; ++i)
+                        pk[i] = pack_bf16x2(fmaf(wb, __uint_as_float(o[2 * i]), x[2 * i]),
+                                            fmaf(wb, __uint_as_float(o[2 * i + 1]), x[2 * i + 1]));
+                    // this buffer's previous store (two stores ago) has read it
+                    const uint32_t buf = wbuf + (uint32_t)(c & 1) * 2048u;
+                    if (lane == 0) bulk_wait_read1();
+                    __syncwarp();
+                    // 64-byte swizzle, as the tensor map expects: 16-byte piece j of row r
+                    // sits at piece j ^ ((r / 2) mod 4)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t a = buf + lane * 64 + ((uint32_t)(j ^ ((lane >> 1) & 3)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pk[4 * j]),
+                                     "r"(pk[4 * j + 1]), "r"(pk[4 * j + 2]), "r"(pk[4 * j + 3])
                                      : "memory");
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&bars->st_full[hh]));
-                    if (issuer) {
-                        ok = wait_phase(smem_u32(&bars->st_full[hh]), spass & 1u, abort_flag, P.wait_limit_ns,
-                                        P.err);
-                        if (ok) {
-                            tma_store_5d(&tm_o, slab, c2 * 64, it.q_rank, first_row, it.h, it.b);
-                            bulk_commit();
-                        }
+                    if (lane == 0) {
+                        tma_store_5d(&tm_o, buf, c * 32, it.q_rank, first_row + quarter * 32, it.h, it.b);
+                        bulk_commit();
                     }
-                    // converged again (and agreed on ok) before the next warp-wide load
-                    ok = __all_sync(0xffffffffu, ok);
-                    ++spass;
+                    __syncwarp();
                 }
-                if (!ok) break;
                 if (valid) P.lse[lrow] = first ? lse_b : w.L;
                 continue;
             }
@@ -939,8 +914,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    // the bulk stores of O issued by a half's first thread are complete before exit
-    if (warp >= 4 && (warp & 3) == 0 && lane == 0) bulk_wait0();
+    // the bulk stores of O issued by each softmax warp are complete before exit
+    if (warp >= 4 && lane == 0) bulk_wait0();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -984,8 +959,9 @@ static cudaError_t launch_tc_hd(const StepParams &P, int blocks_y, int num_sms,
         !encode_map(&mk, P.k, P.B, P.Hkv, P.N, P.D, P.sk, P.rs) ||
         !encode_map(&mv, P.v, P.B, P.Hkv, P.N, P.D, P.sv, P.rs))
         return cudaErrorInvalidValue;
-    // O through bulk tensor stores when its layout allows a map (else row stores)
-    const bool o_map = encode_map(&mo, P.o, P.B, P.Hq, P.N, P.D, P.so, P.rs);
+    // O through bulk tensor stores (32 x 32 boxes, 64-byte swizzle) when its layout allows
+    // a map (else row stores)
+    const bool o_map = encode_map(&mo, P.o, P.B, P.Hq, P.N, P.D, P.so, P.rs, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     if (!o_map) memset(&mo, 0, sizeof mo);
     // Items: pairs of blocks for a ring step (its tail overlaps the next step's launch)
     // or when the pairs fill their rounds over the persistent grid to 93 %; single

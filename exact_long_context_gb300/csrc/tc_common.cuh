@@ -130,6 +130,8 @@ __device__ __forceinline__ void tma_store_5d(const CUtensorMap *map, uint32_t sr
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // the thread's bulk stores have read their shared-memory source
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// all but the most recent of the thread's bulk stores have read their source
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // the thread's bulk stores are complete
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // generic-proxy shared-memory writes become visible to the async proxy (bulk copies)
@@ -334,20 +336,21 @@ inline EncodeTiledFn get_encode_fn() {
 
 // [B, H, N, D] bf16 with element strides s[0..2] (D contiguous), the sequence axis
 // split as N = (N / rs) x rs (position = index * rs + rank), as a 5-D tiled map with
-// dims (D, rank, index, H, B); box 64 x 1 x 128 rows, 128-byte swizzle.  rs = 1 is the
-// plain layout.
+// dims (D, rank, index, H, B); box 64 x 1 x 128 rows, 128-byte swizzle unless given.  rs = 1
+// is the plain layout.
 inline bool encode_map(CUtensorMap *map, const void *ptr, int64_t B, int64_t H, int64_t N,
-                       int64_t D, const int64_t *s, int64_t rs) {
+                       int64_t D, const int64_t *s, int64_t rs, uint32_t box_cols = 64, uint32_t box_rows = 128,
+                       CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = get_encode_fn();
     if (!fn || rs < 1 || N % rs) return false;
     cuuint64_t dims[5] = {(cuuint64_t)D, (cuuint64_t)rs, (cuuint64_t)(N / rs), (cuuint64_t)H,
                           (cuuint64_t)B};
     cuuint64_t strides[4] = {(cuuint64_t)s[2] * 2, (cuuint64_t)(s[2] * rs) * 2,
                              (cuuint64_t)s[1] * 2, (cuuint64_t)s[0] * 2};
-    cuuint32_t box[5] = {64, 1, 128, 1, 1};
+    cuuint32_t box[5] = {box_cols, 1, box_rows, 1, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(ptr), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
