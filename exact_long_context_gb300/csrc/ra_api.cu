@@ -1099,6 +1099,10 @@ ra_status ra_lse_merge(ra_tensor *o_acc, float *lse_acc, const ra_tensor *o_blk,
             reinterpret_cast<uintptr_t>(P.oblk) % balign == 0 && P.sa[0] % 4 == 0 &&
             P.sa[1] % 4 == 0 && P.sa[2] % 4 == 0 && P.sb[0] % bvec == 0 && P.sb[1] % bvec == 0 &&
             P.sb[2] % bvec == 0;
+    // half a warp per row moves 8 values per lane: 16-byte block rows for bf16 too
+    P.half_warp = P.vec && P.D <= 128 &&
+                  (!P.blk_bf16 || (reinterpret_cast<uintptr_t>(P.oblk) % 16 == 0 && P.sb[0] % 8 == 0 &&
+                                   P.sb[1] % 8 == 0 && P.sb[2] % 8 == 0));
     cudaError_t e = launch_lse_merge(P, di.sms, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "lse_merge launch");
     ++t_launches;

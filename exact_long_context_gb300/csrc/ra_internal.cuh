@@ -72,6 +72,7 @@ struct MergeParams {
     int32_t blk_bf16;
     int32_t H, N, D;
     int32_t vec;  // rows are 16-byte aligned (8 for bf16) and D % 4 == 0
+    int32_t half_warp;  // vec, D <= 128 and bf16 rows 16-byte aligned: half a warp per row
     int64_t rows;
 };
 

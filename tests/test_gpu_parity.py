@@ -263,12 +263,19 @@ def test_workload_ring64_million(ra):
 # ---------------------------------------------------------------- LSE merge
 
 @pytest.mark.parametrize("blk_dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("D", [128, 64, 30])
-def test_lse_merge(ra, blk_dtype, D):
+@pytest.mark.parametrize("D,blk_offset", [(128, 0), (100, 0), (64, 0), (52, 0), (30, 0), (128, 4)])
+def test_lse_merge(ra, blk_dtype, D, blk_offset):
+    """D <= 128 with 16-byte rows takes the half-warp path (100 and 52: a lane with four
+    values at the row's end); a block tensor offset by four elements (8 bytes for bf16)
+    takes the one-warp-per-row path; D = 30 the scalar path."""
     B, H, N = 2, 3, 257
     g = torch.Generator(device="cuda").manual_seed(D)
     o_acc = torch.randn(B, H, N, D, generator=g, device="cuda")
     o_blk = torch.randn(B, H, N, D, generator=g, device="cuda").to(blk_dtype)
+    if blk_offset:
+        wide = torch.zeros(B, H, N, D + 2 * blk_offset, dtype=blk_dtype, device="cuda")
+        wide[..., blk_offset:blk_offset + D] = o_blk
+        o_blk = wide[..., blk_offset:blk_offset + D]
     lse_acc = torch.randn(B, H, N, generator=g, device="cuda") * 4
     lse_blk = torch.randn(B, H, N, generator=g, device="cuda") * 4
     lse_acc[0, 0, :10] = -math.inf
