@@ -10,8 +10,9 @@
 //   seq -> head:  out[r, s, j, :] = in[s / (S/sp), s % (S/sp), r * (H/sp) + j, :]
 //   head -> seq:  the inverse.
 //
-// HBM-bound: when rows are 16-byte aligned one thread moves one 16-byte piece, so the
-// grid-stride loop keeps every lane busy whatever D is; otherwise one warp per row.
+// HBM-bound: when rows are 16-byte aligned a thread moves four 16-byte pieces (rows of a
+// multiple of 64 bytes) or one, so the grid-stride loop keeps every lane busy whatever D
+// is; otherwise one warp per row.
 #include <algorithm>
 
 #include "ra_internal.cuh"
@@ -37,6 +38,27 @@ __device__ __forceinline__ void ulysses_offsets(const UlyssesParams &P, int64_t 
 // One thread per 16-byte piece of a row (aligned rows), else one warp per row.
 __global__ void __launch_bounds__(256) ulysses_kernel(const __grid_constant__ UlyssesParams P) {
     const int64_t rows = (int64_t)P.sp * P.S * (P.H / P.sp);
+    if (P.vec && (P.D * P.esize) % 64 == 0) {
+        // four 16-byte pieces per thread: one offset computation per 64 bytes, four loads
+        // in flight before the stores
+        const int per4 = P.D * P.esize / 64;
+        const int64_t total = rows * per4;
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+             i += (int64_t)gridDim.x * blockDim.x) {
+            const int64_t r = i / per4;
+            const int c = (int)(i - r * per4) * 4;
+            int64_t src, dst;
+            ulysses_offsets(P, r, src, dst);
+            const uint4 *ip = reinterpret_cast<const uint4 *>(static_cast<const char *>(P.in) + src * P.esize) + c;
+            uint4 *op = reinterpret_cast<uint4 *>(static_cast<char *>(P.out) + dst * P.esize) + c;
+            const uint4 v0 = __ldcs(ip), v1 = __ldcs(ip + 1), v2 = __ldcs(ip + 2), v3 = __ldcs(ip + 3);
+            __stcs(op, v0);
+            __stcs(op + 1, v1);
+            __stcs(op + 2, v2);
+            __stcs(op + 3, v3);
+        }
+        return;
+    }
     if (P.vec) {
         const int per = P.D * P.esize / 16;  // pieces per row
         const int64_t total = rows * per;
@@ -71,7 +93,8 @@ __global__ void __launch_bounds__(256) ulysses_kernel(const __grid_constant__ Ul
 cudaError_t launch_ulysses(const UlyssesParams &P, int num_sms, cudaStream_t stream) {
     const int64_t rows = (int64_t)P.sp * P.S * (P.H / P.sp);
     if (rows <= 0) return cudaSuccess;
-    const int64_t work = P.vec ? rows * (P.D * P.esize / 16) / 256 + 1 : (rows + 7) / 8;
+    const int64_t work = P.vec ? rows * (P.D * P.esize / ((P.D * P.esize) % 64 == 0 ? 64 : 16)) / 256 + 1
+                               : (rows + 7) / 8;
     const int grid = (int)std::min<int64_t>(work, (int64_t)num_sms * 16);
     ulysses_kernel<<<grid, 256, 0, stream>>>(P);
     return cudaGetLastError();
