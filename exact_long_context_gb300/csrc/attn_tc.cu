@@ -62,7 +62,7 @@ struct Cfg {
     static constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O0 = 256, TM_O1 = 256 + HD;
     static constexpr uint32_t TM_COLS = 512;
     static constexpr int STAGE_BYTES = 8 * 4096;  // O staging: 2 x (32 rows x 32 columns) per softmax warp
-    static constexpr int BAR_BYTES = 512;
+    static constexpr int BAR_BYTES = 1024;
     static constexpr int SMEM_BYTES = 1024 + (2 + NSLOT) * TILE_BYTES + STAGE_BYTES + BAR_BYTES;
 };
 
@@ -72,15 +72,15 @@ struct Bars {
     uint64_t full[8];
     uint64_t empty[8];
     uint64_t s_full[2];
-    uint64_t it_full[4], it_empty[4];  // decoded-item ring: producer -> MMA issuer
-    int32_t it_info[4][4];             // nh[0], nh[1], nmax, skip0 (nmax < 0: no more items)
+    uint64_t it_full[4], it_empty[4];  // decoded-item ring: producer -> MMA issuer, softmax warps
+    int32_t it_info[4][24];            // a decoded Item (nmax < 0: no more items)
     uint64_t o_full[2];
     uint64_t drain;
     uint32_t tmem_base;
     int32_t abort;
     uint32_t p_count[2];  // P_h tiles published by the softmax warps (4 per tile)
 };
-static_assert(sizeof(Bars) <= 512, "barrier block");
+static_assert(sizeof(Bars) <= 1024, "barrier block");
 
 // Register split between warpgroups (launch: 168 per thread x 384 threads = 64512).
 // Warpgroup 0 (TMA + MMA warps) gives back to 88, the two softmax warpgroups take 208:
@@ -121,7 +121,7 @@ struct KTiles {
 
 // One work item: 256 query rows (two 128-row halves) of one (batch, head) against the
 // key tiles of one segment.  Every role decodes the same items in the same order.
-struct Item {
+struct __align__(16) Item {
     int b, h, hk;
     int q_rank, kv_rank, diag;
     int qrow0, q1;
@@ -151,9 +151,22 @@ struct MItem {
     }
     __device__ __forceinline__ int last(int hh) const { return (!hh && skip0 == nmax - 1) ? nmax - 2 : nmax - 1; }
 };
-constexpr int kItemRing = 4;  // decoded items in flight from the producer to the MMA issuer
+constexpr int kItemRing = 4;  // decoded items in flight from the producer to the other roles
+constexpr uint32_t kItemReaders = 9;  // the MMA thread and one lane per softmax warp
 static_assert(sizeof(Bars::it_info) / sizeof(Bars::it_info[0]) == kItemRing, "item ring");
+static_assert(sizeof(Item) <= sizeof(Bars::it_info[0]) && sizeof(Item) % 16 == 0, "item record");
 static_assert(offsetof(Bars, it_info) % 16 == 0, "16-byte item records");
+
+__device__ __forceinline__ void item_store(int32_t *dst, const Item &it) {
+    const int4 *src = reinterpret_cast<const int4 *>(&it);
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(Item) / 16); ++i) reinterpret_cast<int4 *>(dst)[i] = src[i];
+}
+__device__ __forceinline__ void item_load(const int32_t *src, Item &it) {
+    int4 *dst = reinterpret_cast<int4 *>(&it);
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(Item) / 16); ++i) dst[i] = reinterpret_cast<const int4 *>(src)[i];
+}
 
 // Fused ring (contiguous or zigzag layout): the key ranges rank r's query chunk ending at
 // q1 sees at step s, those of rank (r - s) mod R, with the forward's causal rule (a range
@@ -416,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kItemRing; ++i) {
             mbar_init(smem_u32(&bars->it_full[i]), 1);
-            mbar_init(smem_u32(&bars->it_empty[i]), 1);
+            mbar_init(smem_u32(&bars->it_empty[i]), kItemReaders);
         }
         bars->p_count[0] = bars->p_count[1] = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -443,14 +456,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t issued = 0, last_ph = 0;  // per-slot bit sets
             uint32_t qcnt[2] = {0u, 0u};       // Q_h loads issued
             uint32_t icnt = 0;                 // items handed to the MMA issuer
-            // hand item (nh0, nh1, nmax, skip0) to the MMA issuer once its ring slot is free
-            auto hand_over = [&](int a, int b, int c, int d) -> bool {
+            // hand a decoded item to the MMA issuer and the softmax warps once its ring slot
+            // is free
+            auto hand_over = [&](const Item &x) -> bool {
                 const int islot = icnt & (kItemRing - 1);
                 if (icnt >= (uint32_t)kItemRing &&
                     !wait_phase(smem_u32(&bars->it_empty[islot]), (icnt / kItemRing - 1u) & 1u, abort_flag,
                                 P.wait_limit_ns, P.err))
                     return false;
-                *reinterpret_cast<int4 *>(&bars->it_info[islot][0]) = make_int4(a, b, c, d);
+                item_store(&bars->it_info[islot][0], x);
                 mbar_arrive(smem_u32(&bars->it_full[islot]));  // release: the fields are visible
                 ++icnt;
                 return true;
@@ -462,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 Item it;
                 if (!decode_item(P, L, k2 & 1, it)) continue;
                 if (it.nmax == 0) continue;
-                if (!hand_over(it.nh[0], it.nh[1], it.nmax, it.skip0)) {
+                if (!hand_over(it)) {
                     ok = false;
                     break;
                 }
@@ -528,7 +542,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (ok) ok = hand_over(0, 0, -1, 0);  // no more items
+            if (ok) {  // no more items
+                Item end;
+                memset(&end, 0, sizeof end);
+                end.nmax = -1;
+                ok = hand_over(end);
+            }
             if (!ok) {  // wind down: let every copy this thread issued land
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh)
@@ -578,11 +597,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = wait_phase(smem_u32(&bars->it_full[islot]), (icnt / kItemRing) & 1u, abort_flag,
                                     P.wait_limit_ns, P.err);
                     if (!ok) break;
-                    const int4 v = *reinterpret_cast<const int4 *>(&bars->it_info[islot][0]);
-                    it.nh[0] = v.x;
-                    it.nh[1] = v.y;
-                    it.nmax = v.z;
-                    it.skip0 = v.w;
+                    const Item &v = *reinterpret_cast<const Item *>(&bars->it_info[islot][0]);
+                    it.nh[0] = v.nh[0];
+                    it.nh[1] = v.nh[1];
+                    it.nmax = v.nmax;
+                    it.skip0 = v.skip0;
                     mbar_arrive(smem_u32(&bars->it_empty[islot]));
                     ++icnt;
                 }
@@ -672,13 +691,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t scnt = 0, ocnt = 0;  // S_h tiles and O_h results seen
         uint32_t gstage = 0;          // stages of the items so far: (K_0) and one per tile
         bool ok = true;
-        for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, part)
-            const int L = snake_item(k2 >> 1);
-            if (L >= total) continue;
+        uint32_t icnt = 0;
+        for (;;) {  // items, decoded by the producer
             Item it;
-            if (!decode_item(P, L, k2 & 1, it)) continue;
+            {
+                const int islot = icnt & (kItemRing - 1);
+                ok = wait_phase(smem_u32(&bars->it_full[islot]), (icnt / kItemRing) & 1u, abort_flag,
+                                P.wait_limit_ns, P.err);
+                if (!ok) break;
+                item_load(&bars->it_info[islot][0], it);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars->it_empty[islot]));
+                ++icnt;
+            }
+            if (it.nmax < 0) break;  // no more items
             const int n = hh ? it.nh[1] : it.nh[0];
-            if (it.nmax == 0) continue;
             const uint32_t sbase = gstage;  // tile t's S is computed in stage sbase + t
             gstage += 1u + (uint32_t)it.nmax;
             if (n == 0) continue;
