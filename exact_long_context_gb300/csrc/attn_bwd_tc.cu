@@ -31,6 +31,7 @@
 // steps also write is carried between steps in fp32 running buffers (store_grad_chunk).
 #include <climits>
 #include <cstring>
+#include <stddef.h>
 
 #include "tc_common.cuh"
 
@@ -53,6 +54,8 @@ constexpr uint32_t kNegInfBits = 0xff800000u;  // -inf as fp32 bits
 // [64g, 64g + 64) and writes its 32 packed columns at 32 + 32g, inside what it has read
 // and clear of the other group's columns (the order of its two 32-column chunks keeps a
 // chunk from being overwritten before it is read).
+constexpr int kBarBytes = 1024;  // barrier block and the decoded-item ring
+
 template <int HD>
 struct BCfg {
     static constexpr int SLABS = HD / 64;
@@ -67,9 +70,9 @@ struct BCfg {
     static constexpr uint32_t TM_DQ = 384;                    // dQ kernel: dQ
     static constexpr uint32_t TM_COLS = 512;
     static constexpr int BAR_OFF = (2 + 2 * NST) * TILE_BYTES;
-    static constexpr int SMEM_BYTES = 1024 + BAR_OFF + 256 + kEwWarps * 2 * 64 * 4;
+    static constexpr int SMEM_BYTES = 1024 + BAR_OFF + kBarBytes + kEwWarps * 2 * 64 * 4;
     static constexpr int BAR_OFF_DQ = (2 + KST + VST) * TILE_BYTES;
-    static constexpr int SMEM_BYTES_DQ = 1024 + BAR_OFF_DQ + 256;
+    static constexpr int SMEM_BYTES_DQ = 1024 + BAR_OFF_DQ + kBarBytes;
 };
 
 struct BBars {
@@ -80,8 +83,13 @@ struct BBars {
     uint32_t tmem_base;
     int32_t abort;
     uint32_t p_count[2];
+    uint64_t it_full[4], it_empty[4];  // decoded-item ring: producer -> MMA thread, element-wise warps
+    int32_t it_rec[4][32];             // a QRec or KRec
 };
-static_assert(sizeof(BBars) <= 256, "barrier block");
+static_assert(sizeof(BBars) <= kBarBytes, "barrier block");
+static_assert(offsetof(BBars, it_rec) % 16 == 0, "16-byte item records");
+constexpr int kItemRing = 4;
+constexpr uint32_t kItemReaders = 1 + kEwWarps;  // the MMA thread and one lane per element-wise warp
 
 // Work items are pairs of tiles of one segment and one head: tile p and tile tps-1-p of
 // the segment's fixed range.  Under causality the two costs add up to the same total,
@@ -386,7 +394,55 @@ __device__ __forceinline__ void bwd_init(BBars *bars, int nst) {
     mbar_init(smem_u32(&bars->s_full[1]), 1);
     mbar_init(smem_u32(&bars->o_full), 1);
     mbar_init(smem_u32(&bars->drain), 1);
+    for (int i = 0; i < kItemRing; ++i) {
+        mbar_init(smem_u32(&bars->it_full[i]), 1);
+        mbar_init(smem_u32(&bars->it_empty[i]), kItemReaders);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// The producer decodes each work item (item number, segment table) once and hands it,
+// with its segment, to the MMA thread and the element-wise warps through a ring in
+// shared memory; their own decode would sit between one item's last products and the
+// next item's first.  `end` marks the end of the launch's items.
+template <class ItemT>
+struct __align__(16) Rec {
+    ItemT it;
+    BSeg seg;
+    int end;
+};
+template <class R>
+__device__ __forceinline__ bool ring_put(BBars *bars, uint32_t &cnt, const R &r, volatile int32_t *abort_flag,
+                                         int64_t limit, int *err) {
+    static_assert(sizeof(R) <= sizeof(bars->it_rec[0]) && sizeof(R) % 16 == 0, "item record");
+    const int slot = cnt & (kItemRing - 1);
+    if (cnt >= (uint32_t)kItemRing &&
+        !wait_phase(smem_u32(&bars->it_empty[slot]), (cnt / kItemRing - 1u) & 1u, abort_flag, limit, err))
+        return false;
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(R) / 16); ++i)
+        reinterpret_cast<int4 *>(&bars->it_rec[slot][0])[i] = reinterpret_cast<const int4 *>(&r)[i];
+    mbar_arrive(smem_u32(&bars->it_full[slot]));  // release: the record is visible
+    ++cnt;
+    return true;
+}
+// every lane of the calling warp reads the record; `arrive`: this lane frees the slot
+template <class R>
+__device__ __forceinline__ bool ring_get(BBars *bars, uint32_t &cnt, R &r, bool warp_wide, volatile int32_t *abort_flag,
+                                         int64_t limit, int *err) {
+    const int slot = cnt & (kItemRing - 1);
+    if (!wait_phase(smem_u32(&bars->it_full[slot]), (cnt / kItemRing) & 1u, abort_flag, limit, err)) return false;
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(R) / 16); ++i)
+        reinterpret_cast<int4 *>(&r)[i] = reinterpret_cast<const int4 *>(&bars->it_rec[slot][0])[i];
+    if (warp_wide) {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&bars->it_empty[slot]));
+    } else {
+        mbar_arrive(smem_u32(&bars->it_empty[slot]));
+    }
+    ++cnt;
+    return true;
 }
 
 // 32 consecutive 32-bit columns of this thread's lane: 16 bf16 pairs.
@@ -636,15 +692,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_do);
             Ring kr = {0, 0u, 0u, 0u}, vr = {0, 0u, 0u, 0u};
-            uint32_t fcnt = 0;
+            uint32_t fcnt = 0, rcnt = 0;
             bool ok = true;
             for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, tile of the pair)
                 const int L = snake(k2 >> 1);
                 if (L >= total) continue;
-                QItem it;
-                if (!decode_q(P, tps, L, k2 & 1, it)) continue;
+                Rec<QItem> rec;
+                if (!decode_q(P, tps, L, k2 & 1, rec.it)) continue;
+                rec.seg = P.seg[rec.it.si];
+                rec.end = 0;
+                if (!(ok = ring_put(bars, rcnt, rec, abort_flag, limit, err))) break;
+                const QItem &it = rec.it;
                 if (it.n == 0) continue;
-                const BSeg &S = P.seg[it.si];
+                const BSeg &S = rec.seg;
                 const int hk = it.hk;
                 QWalk walk;
                 auto coords = [&](int t, int &row, int &head) {
@@ -655,6 +715,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 };
                 ok = produce_item_kv<HD>(bars, sQ, sK, sV, kr, vr, fcnt, &tm_q, &tm_do, it.r_lo, S.f_rank, it.h,
                                          &tm_k, &tm_v, S.s_rank, it.n, it.b, coords, abort_flag, limit, err);
+            }
+            if (ok) {  // no more items
+                Rec<QItem> rec;
+                memset(&rec, 0, sizeof rec);
+                rec.end = 1;
+                ok = ring_put(bars, rcnt, rec, abort_flag, limit, err);
             }
             if (!ok) {
                 if (fcnt) wait_phase_drain(smem_u32(&bars->fix_full), (fcnt - 1u) & 1u);
@@ -685,11 +751,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pend = false;
                 return true;
             };
-            for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {
-                const int L = snake(k2 >> 1);
-                if (L >= total) continue;
-                QItem it;
-                if (!decode_q(P, tps, L, k2 & 1, it)) continue;
+            uint32_t rcnt = 0;
+            while (ok) {
+                Rec<QItem> rec;
+                if (!(ok = ring_get(bars, rcnt, rec, false, abort_flag, limit, err))) break;
+                if (rec.end) break;
+                const QItem &it = rec.it;
                 const int n = it.n;
                 if (n == 0) continue;
                 ok = wait_phase(smem_u32(&bars->fix_full), fcnt & 1u, abort_flag, limit, err);
@@ -728,14 +795,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;
         const int grp = (warp - 4) >> 2;  // which 64 columns of a tile this warp owns
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        uint32_t g = 0, icnt = 0;
+        uint32_t g = 0, icnt = 0, rcnt = 0;
         bool ok = true;
-        for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, tile of the pair)
-            const int L = snake(k2 >> 1);
-            if (L >= total) continue;
-            QItem it;
-            if (!decode_q(P, tps, L, k2 & 1, it)) continue;
-            const BSeg &S = P.seg[it.si];
+        while (ok) {  // items, decoded by the producer
+            Rec<QItem> rec;
+            if (!(ok = ring_get(bars, rcnt, rec, true, abort_flag, limit, err))) break;
+            if (rec.end) break;
+            const QItem &it = rec.it;
+            const BSeg &S = rec.seg;
             const int n = it.n, diag = S.diag;
             const int row = it.r_lo + quarter * 32 + lane;  // index in the fixed range
             const bool valid = row < it.r_hi;
@@ -867,7 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sSt = base + 2 * C::TILE_BYTES;  // stages of (Q, dO)
     BBars *bars = reinterpret_cast<BBars *>(base_ptr + C::BAR_OFF);
     // per element-wise warp: the current query tile's LSE (log2 units) and D values of its columns
-    float *s_stage = reinterpret_cast<float *>(base_ptr + C::BAR_OFF + 256);  // [8 warps][2][64]
+    float *s_stage = reinterpret_cast<float *>(base_ptr + C::BAR_OFF + kBarBytes);  // [8 warps][2][64]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if ((int)blockIdx.x >= total) {
         asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -892,15 +959,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_do);
             int slot = 0;
-            uint32_t ph = 0, fcnt = 0, issued = 0, last_ph = 0;
+            uint32_t ph = 0, fcnt = 0, issued = 0, last_ph = 0, rcnt = 0;
             bool ok = true;
             for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, tile of the pair)
                 const int L = snake(k2 >> 1);
                 if (L >= total) continue;
-                KItem it;
-                if (!decode_kv(P, tps, L, k2 & 1, it)) continue;
+                Rec<KItem> rec;
+                if (!decode_kv(P, tps, L, k2 & 1, rec.it)) continue;
+                rec.seg = P.seg[rec.it.si];
+                rec.end = 0;
+                if (!(ok = ring_put(bars, rcnt, rec, abort_flag, limit, err))) break;
+                const KItem &it = rec.it;
                 if (it.n == 0) continue;
-                const BSeg &S = P.seg[it.si];
+                const BSeg &S = rec.seg;
                 const int hk = it.hk;
                 KWalk walk;
                 auto coords = [&](int t, int &row, int &head) {
@@ -913,6 +984,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       S.f_rank, hk, &tm_q, &tm_do, S.s_rank, it.n, it.b, coords, abort_flag,
                                       limit, err);
             }
+            if (ok) {  // no more items
+                Rec<KItem> rec;
+                memset(&rec, 0, sizeof rec);
+                rec.end = 1;
+                ok = ring_put(bars, rcnt, rec, abort_flag, limit, err);
+            }
             if (!ok) {
                 if (fcnt) wait_phase_drain(smem_u32(&bars->fix_full), (fcnt - 1u) & 1u);
                 for (int s2 = 0; s2 < C::NST; ++s2)
@@ -924,11 +1001,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             int slot = 0;
             uint32_t ph = 0, fcnt = 0, g = 0;
             bool ok = true;
-            for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {
-                const int L = snake(k2 >> 1);
-                if (L >= total) continue;
-                KItem it;
-                if (!decode_kv(P, tps, L, k2 & 1, it)) continue;
+            uint32_t rcnt = 0;
+            while (ok) {
+                Rec<KItem> rec;
+                if (!(ok = ring_get(bars, rcnt, rec, false, abort_flag, limit, err))) break;
+                if (rec.end) break;
+                const KItem &it = rec.it;
                 const int n = it.n;
                 if (n == 0) continue;
                 ok = wait_phase(smem_u32(&bars->fix_full), fcnt & 1u, abort_flag, limit, err);
@@ -1001,14 +1079,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         float *lb = s_stage + (warp - 4) * 2 * 64;  // this warp's columns only: no cross-warp barrier
         float *db = lb + 64;
-        uint32_t g = 0, icnt = 0;
+        uint32_t g = 0, icnt = 0, rcnt = 0;
         bool ok = true;
-        for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, tile of the pair)
-            const int L = snake(k2 >> 1);
-            if (L >= total) continue;
-            KItem it;
-            if (!decode_kv(P, tps, L, k2 & 1, it)) continue;
-            const BSeg &S = P.seg[it.si];
+        while (ok) {  // items, decoded by the producer
+            Rec<KItem> rec;
+            if (!(ok = ring_get(bars, rcnt, rec, true, abort_flag, limit, err))) break;
+            if (rec.end) break;
+            const KItem &it = rec.it;
+            const BSeg &S = P.seg[it.si];  // (read in place: a register copy would spill)
             const int n = it.n, diag = S.diag;
             const int key = it.c_lo + quarter * 32 + lane;  // index in the fixed range
             const bool kvalid = key < it.c_hi;
