@@ -3,12 +3,17 @@
 // One CTA owns a block of 256 query rows of one (batch, head) - two 128-row halves -
 // and streams the key/value tiles of its ring-step segment through shared memory.
 //
-//   warp 0        TMA producer: Q halves once, then K_t, V_t tiles into a ring of slots
+//   warp 0        TMA producer: decodes each work item once and hands it to the other
+//                 roles through a ring in shared memory; Q halves once per item, then
+//                 (V_t, K_t+1) stages into a ring of buffer pairs
 //   warp 1        MMA issuer (one lane) and tensor-memory owner:
 //                   S_h = Q_h K_t^T      (tcgen05.mma, A and B from shared memory)
 //                   O_h += P_h V_t       (tcgen05.mma, A = P from tensor memory)
-//   warps 4-7     softmax of half 0, one thread per query row
+//   warps 4-7     softmax of half 0, one thread per query row, and its epilogue
 //   warps 8-11    softmax of half 1
+//
+// Outside the fused ring a causal item walks its key tiles last first: half 0 sits out
+// the first tile, the halves start staggered and end on the same tile.
 //
 // Tensor memory (512 columns x 128 lanes x 32 bit): S_0 | S_1 | O_0 | O_1.  The bf16
 // P_h overwrites the first 64 columns of S_h once the softmax threads hold S_h in
@@ -31,6 +36,7 @@
 // Epilogue (per row): O / l and LSE = ln sum exp, then, by segment flags, a direct
 // write, or the log-sum-exp merge of the Twinkle page's `update_out_and_lse` into the
 // float32 running output - so a ring step's partial never goes to HBM unnormalised.
+// Final bf16 rows go out through per-warp shared-memory buffers and bulk tensor stores.
 //
 // Every mbarrier wait is bounded (globaltimer).  On a timeout the CTA records
 // DERR_TIMEOUT in the device error word, every role stops, waits (bounded) for its
