@@ -286,7 +286,8 @@ __device__ __forceinline__ int snake_item(int k) {
 // at the same time share the K/V tiles of a few heads in L2.  `sub` 0 is the later
 // block, 1 the earlier one (false when the pair has a single middle block).  Otherwise
 // an item is one block, as decode_work numbers them (heaviest first) with the heads
-// innermost, which balances best when there are few items per CTA; `sub` 1 is empty.
+// innermost, which balances best when there are few items per CTA (in the fused ring,
+// chunk by chunk); `sub` 1 is empty.
 __device__ __forceinline__ bool decode_item(const StepParams &P, int L, int sub, Item &it) {
     const int BH = P.B * P.Hq;
     int si, lb, bh;
@@ -294,7 +295,14 @@ __device__ __forceinline__ bool decode_item(const StepParams &P, int L, int sub,
         if (sub) return false;
         const int w = L / BH;
         bh = L - w * BH;
-        decode_work(P, w, si, lb);
+        if (P.ring_fused) {
+            // fused ring: a block's cost is mostly its chunk's later steps, so items go
+            // chunk by chunk (heaviest first, as the host orders them), last block first
+            si = w / P.blocks_per_seg;
+            lb = P.blocks_per_seg - 1 - (w - si * P.blocks_per_seg);
+        } else {
+            decode_work(P, w, si, lb);
+        }
     } else {
         const int np = (P.blocks_per_seg + 1) >> 1;
         const int per_seg = BH * np;
@@ -1012,16 +1020,20 @@ static cudaError_t launch_tc_hd(const StepParams &P, int blocks_y, int num_sms,
     // a map (else row stores)
     const bool o_map = encode_map(&mo, P.o, P.B, P.Hq, P.N, P.D, P.so, P.rs, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     if (!o_map) memset(&mo, 0, sizeof mo);
-    // Items: pairs of blocks for a ring step (its tail overlaps the next step's launch)
-    // or when the pairs fill their rounds over the persistent grid to 93 %; single
-    // blocks (heaviest first) otherwise, and for packed batches.
+    // Items: pairs of blocks for a ring step launched per step (its tail overlaps the
+    // next step's launch) or when the pairs fill their rounds over the persistent grid to
+    // 93 %; single blocks (heaviest first) otherwise, for the fused ring and for packed
+    // batches.
     const int64_t singles = (int64_t)P.B * P.Hq * blocks_y;
     const int64_t pairs = (int64_t)P.B * P.Hq * P.nseg * ((P.blocks_per_seg + 1) / 2);
     bool use_pairs = false;
     if (!P.var_blocks && pairs > 0) {
         const int64_t g = std::min<int64_t>(pairs, num_sms);
         const int64_t rounds = (pairs + g - 1) / g;
-        use_pairs = P.prefer_pairs || (double)pairs >= 0.93 * (double)(rounds * g);
+        // (a fused ring takes single blocks: its pairs differ in cost from chunk to chunk,
+        // and with a few rounds of them per CTA the grid ran unbalanced - ring8 zigzag
+        // 1245 TFLOP/s with pairs, 1563 with single blocks)
+        use_pairs = (P.prefer_pairs && !P.ring_fused) || (double)pairs >= 0.93 * (double)(rounds * g);
     }
     const int64_t total = use_pairs ? pairs : singles;
     if (total > 0x7fffffff) return cudaErrorInvalidValue;
