@@ -959,8 +959,21 @@ ra_status ra_ring_sim_fwd_host(const ra_tensor *q, const ra_tensor *k, const ra_
     void *ring_ws = ring_size > 1 ? static_cast<void *>(reinterpret_cast<char *>(dl) + align256((size_t)(B * Hq * N) * 4))
                                   : nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // head groups of whole KV heads (with their G query heads each)
-    const int ng = (int)std::min<int64_t>(Hkv, kHostGroups);
+    // Head groups of whole KV heads (with their G query heads each).  More groups overlap
+    // more of the copies with the kernels, but each group's launches must still fill the
+    // persistent grid: at least two rounds of 256-row blocks per launch where that
+    // leaves two or more groups (one KV head of the 8-rank N = 32K ring is a single round
+    // of 128 blocks, and eight such groups ran at a third of the grid's rate).
+    // When the copies take much longer than the kernels (the dense 4K workload moves
+    // 269 MB for 0.3 TFLOP), the kernels hide behind them whatever their grid fill, and
+    // the most groups overlap the most.  (Rates: ~1.2 PFLOP/s for the kernels, ~200 GB/s
+    // each way for pinned host copies, as measured on a GB300.)
+    const double flops = 4.0 * (double)(B * Hq) * (double)N * (double)N * (double)D * (causal ? 0.5 : 1.0);
+    const double bytes = (double)(2 * nq + 2 * nk) * (double)es;
+    const bool copy_bound = flops / 1.2e15 < 0.5 * bytes / 2.0e11;
+    const int64_t blocks = Hq * ((N + 255) / 256);  // work blocks of one batch
+    const int64_t most = std::min<int64_t>(Hkv, kHostGroups);
+    const int ng = (int)(copy_bound ? most : std::min<int64_t>(most, std::max<int64_t>(2, blocks / (2 * (int64_t)di.sms))));
     cudaError_t e = cudaEventRecord(hp->ev[2 * kHostGroups], st);  // prior work on the caller's stream
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->cin, hp->ev[2 * kHostGroups], 0);
     const size_t qrow = (size_t)(N * D) * es;  // bytes of one head's rows
