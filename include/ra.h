@@ -193,8 +193,9 @@ ra_status ra_attn_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v
  * q, k, v, o and lse are host pointers (page-locked memory lets the copies run
  * asynchronously; pageable memory works but each copy then waits).  The tensors must be
  * contiguous [B, H, N, D]; lse is [B, Hq, N] float32.  The call stages through the
- * caller's device workspace and pipelines by groups of whole KV heads (up to 8): the
- * next group's q/k/v go in on one internal stream while the current group computes on
+ * caller's device workspace and pipelines by groups of whole KV heads (up to 8; fewer
+ * when the kernels dominate and a group's launches would not fill the GPU): the next
+ * group's q/k/v go in on one internal stream while the current group computes on
  * `stream`, and finished groups' o/lse come out on another, so both directions of the
  * host link overlap the kernels.  The call is ordered on `stream`: the host buffers may
  * be read or reused once `stream` has reached this point (e.g. after
