@@ -136,7 +136,8 @@ struct __align__(16) Item {
     int nh[2];  // key tiles each half takes part in
     int nmax;   // key tiles of the item (T)
     int T0;     // tiles of the first step (the only one with a diagonal range)
-    int skip0;  // the one tile half 0 sits out, or -1
+    int skip0;  // the one tile half 0 sits out, or -1 (-2: the first tile of every step)
+    int tps;    // fused striped ring: tiles per step (every step the same), else 0
     int rev;    // the first `rev` tiles are walked last key tile first (0: in key order)
     KTiles kt;  // the first step's key ranges
     // key tile of the item's t-th tile
@@ -151,7 +152,7 @@ struct __align__(16) Item {
 
 // What the MMA issuer needs of an item (handed over by the producer through shared memory).
 struct MItem {
-    int nh[2], nmax, skip0;
+    int nh[2], nmax, skip0, tps;
     __device__ __forceinline__ bool part(int hh, int t) const {
         return hh ? nh[1] > 0 : (nh[0] > 0 && t != skip0);
     }
@@ -211,6 +212,53 @@ __device__ __forceinline__ int ring_ranges(const StepParams &P, int r, int q1, i
         ++n;
     }
     return n;
+}
+
+// Fused ring, striped layout: the keys of step s in the rank-local index space.  At step
+// s rank r holds rank j = (r - s) mod R's keys; under causality row i of rank r sees key
+// index k of rank j iff k + [j > r] <= i (the interleave puts rank j's k-th position
+// after rank r's k-th exactly when j > r), so rows ending before qend see [0, min(c,
+// qend - [j > r])).  Every step is a causal prefix with its own diagonal offset d.
+__device__ __forceinline__ void striped_range(const StepParams &P, int r, int qend, int s, int &end, int &j, int &d) {
+    const int R = P.ring_R, c = P.N / R;
+    j = ((r - s) % R + R) % R;
+    d = (P.causal && j > r) ? 1 : 0;
+    end = P.causal ? min(c, qend - d) : c;
+}
+
+// Walk of a fused striped item: step s, tile u of the step's tps tiles, each step's
+// tiles last key tile first (half 0 then sits out the first tile of each step, as an
+// item outside the fused ring sits out its first).
+struct StripeWalk {
+    int s, u, j, d, end;
+    __device__ __forceinline__ int start(int tps) const { return (tps - 1 - u) * BN; }
+};
+__device__ __forceinline__ void stripe_begin(const StepParams &P, const Item &it, StripeWalk &w) {
+    w.s = 0;
+    w.u = 0;
+    striped_range(P, it.rank, min(it.qrow0 + 2 * BM, it.q1), 0, w.end, w.j, w.d);
+}
+__device__ __forceinline__ void stripe_next(const StepParams &P, const Item &it, StripeWalk &w) {
+    if (++w.u < it.tps) return;
+    w.u = 0;
+    ++w.s;
+    striped_range(P, it.rank, min(it.qrow0 + 2 * BM, it.q1), w.s, w.end, w.j, w.d);
+}
+
+// Whether half hh takes part in tile t, and its last tile (MODE 2: the fused striped ring).
+template <int MODE, class I>
+__device__ __forceinline__ bool part_t(const I &it, int hh, int t) {
+    if constexpr (MODE == 2)
+        return hh ? it.nh[1] > 0 : (it.nh[0] > 0 && !(it.skip0 == -2 && t % it.tps == 0));
+    else
+        return it.part(hh, t);
+}
+template <int MODE, class I>
+__device__ __forceinline__ int last_t(const I &it, int hh) {
+    if constexpr (MODE == 2)
+        return it.nmax - 1;
+    else
+        return it.last(hh);
 }
 
 // Walks an item's key tiles in order: the first T0 tiles of step 0's ranges (the tiles
@@ -320,6 +368,7 @@ __device__ __forceinline__ bool decode_item(const StepParams &P, int L, int sub,
     it.nh[0] = it.nh[1] = 0;
     it.T0 = 0;
     it.skip0 = -1;
+    it.tps = 0;
     it.rev = 0;
     if (lb < 0) return true;
     const Seg &S = P.seg[si];
@@ -330,6 +379,24 @@ __device__ __forceinline__ bool decode_item(const StepParams &P, int L, int sub,
     it.kv_rank = S.kv_rank;
     it.diag = S.diag;
     it.flags = S.flags;
+    if (P.ring_fused && P.ring_layout == 2) {
+        // striped: every step is a causal prefix of the same tile count T (the chunk and
+        // the items' rows are whole 128-row tiles); half 0 sits out one tile per step when
+        // half 1 has rows
+        int end, j, d;
+        striped_range(P, S.rank, min(it.qrow0 + 2 * BM, S.q1), 0, end, j, d);
+        const int T = ntiles(0, end);
+        const bool two = it.qrow0 + BM < S.q1;
+        it.tps = T;
+        it.nmax = P.ring_R * T;
+        it.nh[1] = two ? it.nmax : 0;
+        it.nh[0] = (two && P.causal) ? P.ring_R * (T - 1) : it.nmax;
+        it.skip0 = (two && P.causal) ? -2 : -1;
+        it.T0 = T;
+        it.kt.k0[0] = it.kt.k1[0] = it.kt.k0[1] = it.kt.k1[1] = 0;
+        it.kt.nt0 = it.kt.ntot = 0;
+        return true;
+    }
     if (P.ring_fused) {  // step 0's ranges: the rank's own block
         int a0, b0, a1, b1;
         const int nr = ring_ranges(P, S.rank, S.q1, 0, a0, b0, a1, b1);
@@ -396,18 +463,22 @@ __device__ __forceinline__ bool decode_item(const StepParams &P, int L, int sub,
 
 // FUSED: the launch walks every step of a ring (P.ring_fused): key tiles come from a
 // cursor over the steps' ranges; otherwise from the item's segment ranges directly.
-template <int HD, bool FUSED>
+// MODE 0: one ring step (or the single pass); 1: a fused contiguous or zigzag ring; 2: a
+// fused striped ring.
+template <int HD, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                    const __grid_constant__ StepParams P) {
     using C = Cfg<HD>;
+    constexpr bool FUSED = MODE != 0;
+    constexpr bool STRIPED = MODE == 2;
     // Outside the fused ring, half 0 (the half the MMA thread serves last in each tile)
     // learns that its next S is ready from the stage's release (a commit after that S's
     // product, which is the stage's last), not from a commit of its own: two commits back
     // to back hold the MMA thread until the products before them complete.  (Measured:
     // +1.2 % on the dense pass; in the fused ring, with half 1 last, it cost 3-4 %.)
-    constexpr int kLastHalf = FUSED ? -1 : 0;
+    constexpr int kLastHalf = MODE == 1 ? -1 : 0;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -498,8 +569,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // V only).  Stage (K_0) first - it only needs a free buffer pair - then Q,
                 // which waits until the previous item has issued its last Q K^T.
                 TileCursor cur;
-                if constexpr (FUSED) cursor_begin(P, it, cur);
-                int vstart = 0;  // V_t is the tile K_t came from
+                StripeWalk sw;
+                if constexpr (STRIPED)
+                    stripe_begin(P, it, sw);
+                else if constexpr (FUSED)
+                    cursor_begin(P, it, cur);
+                int vstart = 0, vrank = it.kv_rank;  // V_t is the tile K_t came from
                 for (int st = -1; st < it.nmax && ok; ++st) {
                     const uint32_t b_empty = smem_u32(&bars->empty[slot]);
                     const uint32_t b_full = smem_u32(&bars->full[slot]);
@@ -516,19 +591,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int vs = FUSED ? vstart : it.kt.start(it.tile(st));
 #pragma unroll
                         for (int c = 0; c < C::SLABS; ++c)
-                            tma_load_5d(vbuf + c * C::SLAB_BYTES, &tm_v, b_full, c * 64,
-                                        it.kv_rank, vs, it.hk, it.b);
+                            tma_load_5d(vbuf + c * C::SLAB_BYTES, &tm_v, b_full, c * 64, vrank, vs, it.hk, it.b);
                     }
                     if (has_k) {
-                        const int ks = FUSED ? cur.start() : it.kt.start(it.tile(st + 1));
-                        if constexpr (FUSED) {
+                        int ks, kr = it.kv_rank;
+                        if constexpr (STRIPED) {
+                            ks = sw.start(it.tps);
+                            kr = sw.j;
+                            vstart = ks;
+                            vrank = kr;
+                            stripe_next(P, it, sw);
+                        } else if constexpr (FUSED) {
+                            ks = cur.start();
                             vstart = ks;
                             cursor_next(P, it, cur);
+                        } else {
+                            ks = it.kt.start(it.tile(st + 1));
                         }
 #pragma unroll
                         for (int c = 0; c < C::SLABS; ++c)
-                            tma_load_5d(kbuf + c * C::SLAB_BYTES, &tm_k, b_full, c * 64,
-                                        it.kv_rank, ks, it.hk, it.b);
+                            tma_load_5d(kbuf + c * C::SLAB_BYTES, &tm_k, b_full, c * 64, kr, ks, it.hk, it.b);
                     }
                     issued |= 1u << slot;
                     last_ph = (last_ph & ~(1u << slot)) | (ph << slot);
@@ -616,6 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     it.nh[1] = v.nh[1];
                     it.nmax = v.nmax;
                     it.skip0 = v.skip0;
+                    it.tps = v.tps;
                     mbar_arrive(smem_u32(&bars->it_empty[islot]));
                     ++icnt;
                 }
@@ -634,10 +717,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    if (it.part(hh, 0)) {
+                    if (part_t<MODE>(it, hh, 0)) {
                         issue_qk(hh, sKV + (2 * slot + 1) * C::TILE_BYTES);
                         if (hh != kLastHalf) mma_commit(smem_u32(&bars->s_full[hh]));
-                        if (it.last(hh) == 0) mma_commit(smem_u32(&bars->q_empty[hh]));
+                        if (last_t<MODE>(it, hh) == 0) mma_commit(smem_u32(&bars->q_empty[hh]));
                     }
                 }
                 mma_commit(smem_u32(&bars->empty[slot]));
@@ -660,8 +743,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int h2 = 0; h2 < 2; ++h2) {
                         // outside the fused ring half 1 starts first (half 0 sits out the
                         // item's first tile), and it is served first in every tile
-                        const int hh = FUSED ? h2 : 1 - h2;
-                        if (it.part(hh, t)) {
+                        const int hh = MODE == 1 ? h2 : 1 - h2;
+                        if (part_t<MODE>(it, hh, t)) {
                             ++pcnt[hh];
                             ok = wait_count(&bars->p_count[hh], 4u * pcnt[hh], abort_flag,
                                             P.wait_limit_ns, P.err);
@@ -669,12 +752,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tc_fence_after();
                             issue_pv(hh, vb, started[hh]);
                             started[hh] = true;
-                            if (t == it.last(hh)) mma_commit(smem_u32(&bars->o_full[hh]));
+                            if (t == last_t<MODE>(it, hh)) mma_commit(smem_u32(&bars->o_full[hh]));
                         }
-                        if (t + 1 < it.nmax && it.part(hh, t + 1)) {
+                        if (t + 1 < it.nmax && part_t<MODE>(it, hh, t + 1)) {
                             issue_qk(hh, kb);
                             if (hh != kLastHalf) mma_commit(smem_u32(&bars->s_full[hh]));
-                            if (t + 1 == it.last(hh)) mma_commit(smem_u32(&bars->q_empty[hh]));
+                            if (t + 1 == last_t<MODE>(it, hh)) mma_commit(smem_u32(&bars->q_empty[hh]));
                         }
                     }
                     if (!ok) break;
@@ -735,13 +818,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             float m_ref = -INFINITY, l = 0.f;
             TileCursor cur;
-            if constexpr (FUSED) cursor_begin(P, it, cur);
+            StripeWalk sw;
+            if constexpr (STRIPED)
+                stripe_begin(P, it, sw);
+            else if constexpr (FUSED)
+                cursor_begin(P, it, cur);
             bool first_tile = true;
             for (int t = 0; t < it.nmax; ++t) {
-                const int ks = FUSED ? cur.start() : it.kt.start(it.tile(t));
-                const int ke = FUSED ? cur.end() : it.kt.range_end(it.tile(t));
-                if constexpr (FUSED) cursor_next(P, it, cur);
-                if (!it.part(hh, t)) continue;
+                int ks, ke, dg = it.diag;  // the tile's keys and diagonal offset
+                if constexpr (STRIPED) {
+                    ks = sw.start(it.tps);
+                    ke = sw.end;
+                    dg = sw.d;
+                    stripe_next(P, it, sw);
+                } else if constexpr (FUSED) {
+                    ks = cur.start();
+                    ke = cur.end();
+                    cursor_next(P, it, cur);
+                } else {
+                    ks = it.kt.start(it.tile(t));
+                    ke = it.kt.range_end(it.tile(t));
+                }
+                if (!part_t<MODE>(it, hh, t)) continue;
                 if (hh == kLastHalf) {
                     const uint32_t gs = sbase + (uint32_t)t;
                     ok = wait_phase(smem_u32(&bars->empty[gs % C::NSTAGE]), (gs / C::NSTAGE) & 1u, abort_flag,
@@ -759,9 +857,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(tS + 96, r[3]);
                 tmem_ld_wait();
                 const bool need_mask =
-                    (ks + BN > ke) || (P.causal && (min(ks + BN, ke) - 1 + it.diag > first_row));
+                    (ks + BN > ke) || (P.causal && (min(ks + BN, ke) - 1 + dg > first_row));
                 if (need_mask) {
-                    const int lim = (P.causal ? min(ke, row_g + 1 - it.diag) : ke) - ks;
+                    const int lim = (P.causal ? min(ke, row_g + 1 - dg) : ke) - ks;
 #pragma unroll
                     for (int c = 0; c < 128; ++c)
                         if (c >= lim) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
@@ -1002,11 +1100,14 @@ static cudaError_t launch_tc_hd(const StepParams &P, int blocks_y, int num_sms,
     int dev = 0;
     cudaGetDevice(&dev);
     if (!(configured_mask & (1 << (dev & 31)))) {
-        cudaError_t e = cudaFuncSetAttribute(tc::attn_tc_kernel<HD, false>,
+        cudaError_t e = cudaFuncSetAttribute(tc::attn_tc_kernel<HD, 0>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(tc::attn_tc_kernel<HD, true>,
+            e = cudaFuncSetAttribute(tc::attn_tc_kernel<HD, 1>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(tc::attn_tc_kernel<HD, 2>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured_mask |= 1 << (dev & 31);
@@ -1055,8 +1156,9 @@ static cudaError_t launch_tc_hd(const StepParams &P, int blocks_y, int num_sms,
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    if (P.ring_fused) return cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel<HD, true>, mq, mk, mv, mo, Q);
-    return cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel<HD, false>, mq, mk, mv, mo, Q);
+    if (P.ring_fused && P.ring_layout == 2) return cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel<HD, 2>, mq, mk, mv, mo, Q);
+    if (P.ring_fused) return cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel<HD, 1>, mq, mk, mv, mo, Q);
+    return cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel<HD, 0>, mq, mk, mv, mo, Q);
 }
 
 cudaError_t launch_attn_tc(const StepParams &P, int blocks_y, int num_sms, cudaStream_t stream) {

@@ -399,7 +399,26 @@ struct BwdPlan {
 // launch holds).
 static bool fused_ring_segments(int64_t N, int R, int layout, int causal, std::vector<Seg> &out) {
     out.clear();
-    if (layout == RA_LAYOUT_STRIPED) return false;
+    if (layout == RA_LAYOUT_STRIPED) {
+        // one segment per rank, in the rank-local index space: the kernel walks each
+        // step's causal prefix with its diagonal offset.  Needs whole 128-row tiles per
+        // rank (every step of an item then has the same tile count); the ranks' work is
+        // the same, so their order does not matter.
+        const int64_t c = N / R;
+        if (R > kMaxSeg || c % 128 != 0 || c > INT32_MAX) return false;
+        for (int r = 0; r < R; ++r) {
+            Seg g;
+            memset(&g, 0, sizeof g);
+            g.q0 = 0;
+            g.q1 = (int32_t)c;
+            g.q_rank = r;
+            g.rank = r;
+            g.flags = SEG_FIRST | SEG_FINAL;
+            out.push_back(g);
+        }
+        (void)causal;
+        return true;
+    }
     const int chunks = layout == RA_LAYOUT_ZIGZAG ? 2 * R : R;
     if (chunks > kMaxSeg || N > INT32_MAX) return false;
     std::vector<std::pair<int64_t, Seg>> work;
@@ -574,7 +593,7 @@ ra_status ra_ring_sim_fwd(const ra_tensor *q, const ra_tensor *k, const ra_tenso
         // one launch walks every step: each query chunk's running result stays on chip
         P->ring_fused = 1;
         P->ring_R = ring_size;
-        P->ring_layout = layout == RA_LAYOUT_ZIGZAG ? 1 : 0;
+        P->ring_layout = layout == RA_LAYOUT_ZIGZAG ? 1 : (layout == RA_LAYOUT_STRIPED ? 2 : 0);
         P->prefer_pairs = 0;
         s = run_step(*P, segs, tc, di.sms, st);
     } else {

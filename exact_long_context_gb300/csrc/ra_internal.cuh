@@ -53,7 +53,7 @@ struct StepParams {
     int32_t pair_items;      // tensor-core kernel: items are pairs of blocks (set at launch)
     int32_t prefer_pairs;    // host: a ring step (tails overlap the next step's launch)
     int32_t ring_fused;      // one launch walks every ring step: Seg = a query chunk of rank Seg::rank
-    int32_t ring_R, ring_layout;  // fused ring: ring size, RA_LAYOUT_CONTIG (0) or ZIGZAG (1)
+    int32_t ring_R, ring_layout;  // fused ring: ring size, RA_LAYOUT_CONTIG (0), ZIGZAG (1) or STRIPED (2)
     int32_t rs;              // rank interleave stride of the sequence axis (1 unless striped)
     int32_t o_tma;           // tensor-core kernel: final O rows leave through bulk tensor stores
     int64_t wait_limit_ns;
