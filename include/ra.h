@@ -123,13 +123,14 @@ size_t ra_ring_sim_workspace_bytes(const ra_tensor *q, int ring_size);
  * partial for each rank's query rows (causality on global positions, so later
  * blocks are skipped and the diagonal block masked) is merged into the rank's running
  * result.  Two executions:
- *   - bf16, D in {64, 128}, contiguous or zigzag layout, up to 128 chunks: one launch
- *     walks every step; each query block's running (max, sum, O) stays in the kernel
- *     across the step boundaries (the LSE merge of consecutive steps' partials is the
- *     online-softmax rescale), and each row is written once.
- *   - otherwise (striped layout, float32, other D): one launch per step covering every
- *     simulated rank, merging into a float32 running result in the workspace by the LSE
- *     merge above, inside the attention kernel's epilogue.
+ *   - bf16, D in {64, 128}, contiguous or zigzag layout with up to 128 chunks, or the
+ *     striped layout with up to 128 ranks of whole 128-row tiles: one launch walks every
+ *     step; each query block's running (max, sum, O) stays in the kernel across the step
+ *     boundaries (the LSE merge of consecutive steps' partials is the online-softmax
+ *     rescale), and each row is written once.
+ *   - otherwise (float32, other D, other striped sizes): one launch per step covering
+ *     every simulated rank, merging into a float32 running result in the workspace by the
+ *     LSE merge above, inside the attention kernel's epilogue.
  * The result equals ra_attn_fwd on the whole sequence (up to rounding); inputs and
  * outputs are in natural sequence order; ring_size == 1 is ra_attn_fwd.
  *
