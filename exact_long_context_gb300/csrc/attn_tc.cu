@@ -461,10 +461,10 @@ __device__ __forceinline__ bool decode_item(const StepParams &P, int L, int sub,
 // warpgroup of half h finishes its epilogue (reads O_h) before it signals the next
 // item's first P_h, and only then is O_h overwritten.
 
-// FUSED: the launch walks every step of a ring (P.ring_fused): key tiles come from a
-// cursor over the steps' ranges; otherwise from the item's segment ranges directly.
-// MODE 0: one ring step (or the single pass); 1: a fused contiguous or zigzag ring; 2: a
-// fused striped ring.
+// MODE 0: one ring step (or the single pass): key tiles come from the item's segment
+// ranges.  MODE 1: a fused contiguous or zigzag ring (P.ring_fused): the launch walks
+// every step, key tiles from a cursor over the steps' ranges.  MODE 2: a fused striped
+// ring: every step a causal prefix, walked last tile first (StripeWalk).
 template <int HD, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
