@@ -5,6 +5,7 @@ import numpy as np
 import torch
 
 import oracle
+from exact_long_context_gb300 import synth
 
 # GPU-vs-oracle tolerances: bf16 inputs: max-abs on O <= 2e-2, LSE |d| <= 1e-3 max(1, |lse|);
 # float32 inputs (CUDA-core path): max-abs <= 1e-5 on both.
@@ -72,3 +73,23 @@ def assert_close(o_gpu, lse_gpu, o_ref, lse_ref, dtype, what=""):
         assert o_err <= F32_TOL, f"{what}: O max-abs {o_err:.3e} > {F32_TOL}"
         assert lse_abs <= F32_TOL, f"{what}: LSE abs {lse_abs:.3e} > {F32_TOL}"
     return o_err, lse_rel
+
+
+# softmax edge cases: kind -> scale (None = 1/sqrt(D))
+EDGE_SCALE = {"uniform": None, "flat": 0.01, "peaked": 4.0, "ramp_up": 1.0, "ramp_down": 1.0}
+
+
+def edge_inputs(kind, B, Hq, Hkv, N, D, seed, dtype=torch.bfloat16, device="cuda"):
+    """Seeded Q, K, V for a softmax edge case.  "uniform": Q = 0, every score 0, each row's
+    P uniform over its visible keys.  "ramp_up" / "ramp_down": key norms grow (shrink) by
+    0.25 -> 3 along the sequence, so the running maximum moves on most tiles of a walk.
+    "flat" / "peaked" are the plain draw under the small / large scale of EDGE_SCALE."""
+    q, k, v = synth.make_qkv(B, Hq, Hkv, N, D, dtype, seed=seed, device=device)
+    if kind == "uniform":
+        q = torch.zeros_like(q)
+    elif kind.startswith("ramp"):
+        f = torch.linspace(0.25, 3.0, N, device=device)
+        if kind == "ramp_down":
+            f = f.flip(0)
+        k = (k.float() * f.view(1, 1, N, 1)).to(dtype)
+    return q, k, v

@@ -4,7 +4,7 @@ import pytest
 import torch
 
 from exact_long_context_gb300 import synth
-from helpers import to_oracle
+from helpers import EDGE_SCALE, edge_inputs, to_oracle
 from oracle import backward as ob
 
 pytestmark = pytest.mark.gpu
@@ -92,3 +92,30 @@ def test_backward_empty_and_errors(ra):
     lse = torch.zeros(1, 2, 8, device="cuda")
     with pytest.raises(ra.RaError):
         ra.attn_bwd(q, q, q, q, lse, q.float(), causal=True)  # dtype mismatch
+
+
+@pytest.mark.parametrize("kind", ["uniform", "peaked", "ramp_up", "ramp_down"])
+def test_backward_edge_cases(ra, kind):
+    """Gradients on the softmax edge cases (scores all 0, very peaked, a running maximum
+    that moves along the walk) through the single pass and the zigzag and striped ring
+    schedules, with three query heads per KV head, against the fp64 gradients."""
+    B, Hq, Hkv, N, D = 1, 6, 2, 768, 128
+    scale = EDGE_SCALE[kind]
+    q, k, v = edge_inputs(kind, B, Hq, Hkv, N, D, seed=43)
+    g = torch.Generator(device="cuda").manual_seed(44)
+    dout = torch.randn(B, Hq, N, D, generator=g, device="cuda").to(torch.bfloat16)
+    o, lse = ra.attn_fwd(q, k, v, causal=True, scale=scale)
+    ref = ob.attention_bwd(to_oracle(q), to_oracle(k), to_oracle(v), to_oracle(dout), True, scale)[:3]
+    runs = [("single pass", lambda: ra.attn_bwd(q, k, v, o, lse, dout, causal=True, scale=scale))]
+    for R, layout in ((2, "zigzag"), (4, "striped")):
+        runs.append((f"{layout} R{R}", lambda R=R, layout=layout:
+                     ra.ring_sim_bwd(q, k, v, o, lse, dout, R, layout, True, scale=scale)))
+    for run, fn in runs:
+        grads = fn()
+        ra.check()
+        for name, got, r in zip(("dq", "dk", "dv"), grads, ref):
+            got = got.float().cpu().numpy().astype(np.float64)
+            assert np.all(np.isfinite(got)), (kind, run, name)
+            err = np.max(np.abs(got - r)) / max(1.0, np.max(np.abs(r)))
+            assert err <= TOL[torch.bfloat16], f"{kind} {run} {name}: scaled max-abs error {err:.3e}"
+            print(kind, run, name, f"{err:.2e}")

@@ -8,7 +8,8 @@ import torch
 import oracle
 from oracle import merge as om
 from exact_long_context_gb300 import synth
-from helpers import (assert_close, errors, gather_rows, oracle_full, sample_rows, to_oracle)
+from helpers import (EDGE_SCALE, assert_close, edge_inputs, errors, gather_rows, oracle_full,
+                     sample_rows, to_oracle)
 
 pytestmark = pytest.mark.gpu
 
@@ -213,24 +214,6 @@ def test_ring_invariants_gpu(ra):
 
 # ---------------------------------------------------------------- softmax edge cases
 
-EDGE_SCALE = {"uniform": None, "flat": 0.01, "peaked": 4.0, "ramp_up": 1.0, "ramp_down": 1.0}
-
-
-def _edge_inputs(kind, B, Hq, Hkv, N, D, seed):
-    q, k, v = synth.make_qkv(B, Hq, Hkv, N, D, torch.bfloat16, seed=seed, device="cuda")
-    if kind == "uniform":
-        # every score is 0: each row's P is uniform over its visible keys
-        q = torch.zeros_like(q)
-    elif kind.startswith("ramp"):
-        # key norms grow (or shrink) along the sequence, so the running maximum moves on
-        # most tiles of a walk and the lazy rescale of O runs
-        f = torch.linspace(0.25, 3.0, N, device="cuda")
-        if kind == "ramp_down":
-            f = f.flip(0)
-        k = (k.float() * f.view(1, 1, N, 1)).to(torch.bfloat16)
-    return q, k, v
-
-
 @pytest.mark.parametrize("kind", list(EDGE_SCALE))
 def test_softmax_edge_cases(ra, kind):
     """Scores all equal, nearly flat (scale 0.01), very peaked (scale 4: score spread ~45,
@@ -243,7 +226,7 @@ def test_softmax_edge_cases(ra, kind):
     bound (the kernel is deterministic, so the margin does not move between runs)."""
     B, Hq, Hkv, N, D = 2, 6, 2, 1024, 128
     scale = EDGE_SCALE[kind]
-    q, k, v = _edge_inputs(kind, B, Hq, Hkv, N, D, seed=41)
+    q, k, v = edge_inputs(kind, B, Hq, Hkv, N, D, seed=41)
     o_ref, l_ref = oracle_full(q, k, v, True, scale)
     runs = [("single pass", lambda: ra.attn_fwd(q, k, v, causal=True, scale=scale))]
     for R, layout in ((4, "zigzag"), (2, "contig"), (4, "striped")):
