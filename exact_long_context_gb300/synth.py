@@ -47,6 +47,9 @@ WORKLOADS = {
                                       torch.bfloat16, True, 1, "contig", 2),
     "ring8_zigzag_h8n32k": Workload("ring8_zigzag_h8n32k", 1, 8, 8, 32768, 128, torch.bfloat16,
                                     True, 8, "zigzag", 3),
+    # the same inputs as the zigzag ring: an A/B of the two partitions
+    "ring8_contig_h8n32k": Workload("ring8_contig_h8n32k", 1, 8, 8, 32768, 128, torch.bfloat16,
+                                    True, 8, "contig", 3),
     "ring8_striped_h8n32k": Workload("ring8_striped_h8n32k", 1, 8, 8, 32768, 128, torch.bfloat16,
                                      True, 8, "striped", 3),
     "gqa_ring16_zigzag_h32kv8n128k": Workload("gqa_ring16_zigzag_h32kv8n128k", 1, 32, 8, 131072,
