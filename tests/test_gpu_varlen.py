@@ -95,3 +95,25 @@ def test_varlen_many_sequences_span_launches(ra):
                                   kv_lo=cu[s], kv_hi=cu[s + 1], rows=[r])
         o_ref[n], l_ref[n] = oi[0], li[0]
     assert_close(og, lg, o_ref, l_ref, torch.bfloat16, "300 sequences")
+
+
+@pytest.mark.parametrize("cu", [[0], [3, 3, 3], [0, 0, 8]], ids=["no_sequences", "empty_sequences", "one_sequence_all_rows"])
+def test_varlen_degenerate_tables(ra, cu):
+    """No sequences, only empty ones (every row is padding: O = 0, LSE = -inf), and one
+    sequence over the whole packed length (the single pass, bit for bit)."""
+    T = 8
+    q, k, v = synth.make_qkv(1, 2, 1, T, 128, torch.bfloat16, seed=12, device="cuda")
+    o = torch.full_like(q, 7.0)
+    lse = torch.full((1, 2, T), 7.0, device="cuda")
+    o, lse = ra.attn_varlen_fwd(q, k, v, cu, causal=True, o=o, lse=lse)
+    ra.check()
+    covered = torch.zeros(T, dtype=torch.bool)
+    for a, b in zip(cu[:-1], cu[1:]):
+        covered[a:b] = True
+    pad = (~covered).nonzero().flatten().tolist()
+    assert torch.all(o[:, :, pad] == 0).item()
+    assert torch.all(torch.isneginf(lse[:, :, pad])).item()
+    if covered.all():
+        o1, l1 = ra.attn_fwd(q, k, v, causal=True)
+        ra.check()
+        assert torch.equal(o, o1) and torch.equal(lse, l1)
