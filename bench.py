@@ -356,6 +356,26 @@ def run_hbm_pass(args, w, ws, rank, local):
             "bytes_per_step": nbytes}
 
 
+def host_cpu_desc():
+    """The host CPU the oracle runs on: machine, model (or Arm part number) and the cores
+    this process may use."""
+    import platform
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                key, _, val = ln.partition(":")
+                key = key.strip().lower()
+                if key == "model name" or (key == "cpu part" and not model):
+                    model = (val.strip() if key == "model name" else f"CPU part {val.strip()}")
+                    if key == "model name":
+                        break
+    except OSError:
+        pass
+    avail = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return f"{platform.machine()}{', ' + model if model else ''}, {avail} cores available"
+
+
 def oracle_rate_sample(w, budget_s, seed=0):
     """Time the oracle on rows sampled from the workload; returns (flops, seconds, rows, threads)."""
     import oracle
@@ -433,7 +453,7 @@ def run_reference(args, w, ws, rank):
               f"(fp64 oracle, causal-adjusted FLOPs of the rows' visible keys)")
     return {"value": round(value, 6), "ms_per_step": round(tsec / args.steps * 1e3, 3),
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample, "cpu": host_cpu_desc()},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
@@ -510,7 +530,8 @@ def main():
             "value": round(f / sec / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
             "kind": "oracle",
             "sample": f"{nrows} uniformly random query rows of {w.name} (fp64 oracle, "
-                      f"{sec:.1f} s wall)"}
+                      f"{sec:.1f} s wall)",
+            "cpu": host_cpu_desc()}
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.barrier()
