@@ -69,6 +69,25 @@ def peaks():
     return 1900.0, 6800.0, "fallback"
 
 
+SPEC_DENSE_BF16_TFLOPS = 2250.0  # GB300 dense bf16 tensor rate, nominal (no sparsity)
+
+
+def peak_fractions(tflops: float) -> dict:
+    """Percent of the measured burst and sustained bf16 GEMM rates and of the nominal
+    dense bf16 rate, for a TFLOP/s figure."""
+    burst, _, kind = peaks()
+    sustained = None
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            sustained = json.load(f).get("bf16_tflops_sustained")
+    out = {f"of_{kind}_burst": round(100 * tflops / burst, 2),
+           "of_nominal_dense_bf16": round(100 * tflops / SPEC_DENSE_BF16_TFLOPS, 2)}
+    if sustained:
+        out["of_measured_sustained"] = round(100 * tflops / sustained, 2)
+    return out
+
+
 def kernel_hash():
     with open(KERNEL_SRC, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -518,6 +537,8 @@ def main():
     if rank == 0:
         line.update(res)
         line["pct_of_peak"] = round(100 * res["roofline"]["frac"], 2)
+        if line["unit"] == "TFLOP/s":
+            line["pct_of_peaks"] = peak_fractions(line["value"])
         if args.pass_ == "bwd":
             line["cpu_baseline"] = None  # the oracle's timed leg is the forward
             print(json.dumps(line), flush=True)

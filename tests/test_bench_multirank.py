@@ -50,3 +50,22 @@ def test_single_process_is_identity():
 
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.whole_job_rate(1.0, 4, 1, 2.0) == 2000.0
+
+
+def test_peak_fractions():
+    """A figure equal to a peak reads 100 % of it; the nominal dense bf16 rate is 2250."""
+    import json
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+
+    burst, _, kind = bench.peaks()
+    f = bench.peak_fractions(burst)
+    assert f[f"of_{kind}_burst"] == 100.0
+    assert f["of_nominal_dense_bf16"] == round(100 * burst / 2250.0, 2)
+    path = os.path.join(bench.ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            sus = json.load(fh).get("bf16_tflops_sustained")
+        if sus:
+            assert bench.peak_fractions(sus)["of_measured_sustained"] == 100.0
