@@ -18,13 +18,16 @@
 //
 // Warp roles: warp 0 TMA producer, warp 1 MMA issuer and tensor-memory owner, warps 4-11
 // the element-wise work and the epilogue: two warps per tensor-memory lane quarter, each
-// owning 32 of a sub-tile's 64 columns (one warp per scheduler left the exponentials and
-// the tensor-memory round trips exposed).  The streamed tile is handled as two 64-wide
-// halves with their own S / dP buffers, so the tensor core computes one half's S / dP
-// while the element-wise warps work on the other.  The bf16 P / dS overwrite the
-// columns of the fp32 S / dP they came from once those are in registers; the MMA
-// thread issues the next S / dP of a half after the products that read it (tcgen05 MMAs
-// of a thread run in order).  Every wait is bounded like the forward kernel's.
+// owning 64 of a tile's 128 columns (one warp per scheduler left the exponentials and
+// the tensor-memory round trips exposed).  Every S / dP product is a full 128 x 128 tile
+// (narrower products run the tensor core below its rate).  The dQ kernel rotates the S
+// and dP of consecutive tiles through three tensor-memory slots, so the next tile's S
+// is computed while the element-wise warps work on this one; the dK/dV kernel orders
+// its products so that the next tile's S^T and dP^T overlap the element-wise work.  The
+// bf16 P / dS overwrite the columns of the fp32 S / dP they came from once those are in
+// registers; the MMA thread issues a product that overwrites a slot after the products
+// that read it (tcgen05 MMAs of a thread run in order).  Every wait is bounded like the
+// forward kernel's.
 //
 // A launch covers the segments of one ring step (struct BSeg): the whole-sequence
 // backward is one segment.  On a ring, the gradient of a range that earlier or later
@@ -457,13 +460,15 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 
 // Producer: per item the fixed pair (fa, fb) at index f_row of rank f_rank of (fh, b), then
 // `n` streamed pairs (sa, sb) at the index and head coords(t) gives, of rank s_rank.
+// fix_in and coords' result: the coordinates lie inside their tensors (always true in
+// release builds; a debug build skips the loads of a tile outside, see in_bounds).
 // Shared by both kernels.
 template <int HD, typename StreamCoords>
 __device__ __forceinline__ bool produce_item(BBars *bars, uint32_t fix0, uint32_t st0, int &slot, uint32_t &ph,
                                              uint32_t &fcnt, uint32_t &issued, uint32_t &last_ph,
                                              const CUtensorMap *fa, const CUtensorMap *fb, int f_row, int f_rank,
                                              int fh, const CUtensorMap *sa, const CUtensorMap *sb, int s_rank,
-                                             int n, int b,
+                                             int n, int b, bool fix_in,
                                              StreamCoords coords, volatile int32_t *abort_flag,
                                              int64_t limit, int *err) {
     using C = BCfg<HD>;
@@ -471,7 +476,7 @@ __device__ __forceinline__ bool produce_item(BBars *bars, uint32_t fix0, uint32_
     {
         const uint32_t bf = smem_u32(&bars->fix_full);
         mbar_expect_tx(bf, 2 * C::TILE_BYTES);
-        for (int c = 0; c < C::SLABS; ++c) {
+        for (int c = 0; c < C::SLABS && fix_in; ++c) {
             tma_load_5d(fix0 + c * C::SLAB_BYTES, fa, bf, c * 64, f_rank, f_row, fh, b);
             tma_load_5d(fix0 + C::TILE_BYTES + c * C::SLAB_BYTES, fb, bf, c * 64, f_rank, f_row, fh, b);
         }
@@ -480,11 +485,11 @@ __device__ __forceinline__ bool produce_item(BBars *bars, uint32_t fix0, uint32_
     for (int t = 0; t < n; ++t) {
         if (!wait_phase(smem_u32(&bars->empty[slot]), ph ^ 1u, abort_flag, limit, err)) return false;
         int row, head;
-        coords(t, row, head);
+        const bool in = coords(t, row, head);
         const uint32_t bf = smem_u32(&bars->full[slot]);
         mbar_expect_tx(bf, 2 * C::TILE_BYTES);
         const uint32_t a0 = st0 + (2 * slot) * C::TILE_BYTES;
-        for (int c = 0; c < C::SLABS; ++c) {
+        for (int c = 0; c < C::SLABS && in; ++c) {
             tma_load_5d(a0 + c * C::SLAB_BYTES, sa, bf, c * 64, s_rank, row, head, b);
             tma_load_5d(a0 + C::TILE_BYTES + c * C::SLAB_BYTES, sb, bf, c * 64, s_rank, row, head, b);
         }
@@ -519,14 +524,14 @@ __device__ __forceinline__ bool produce_item_kv(BBars *bars, uint32_t fix0, uint
                                                 Ring &vr, uint32_t &fcnt, const CUtensorMap *fa,
                                                 const CUtensorMap *fb, int f_row, int f_rank, int fh,
                                                 const CUtensorMap *tk, const CUtensorMap *tv, int s_rank, int n,
-                                                int b, StreamCoords coords, volatile int32_t *abort_flag,
+                                                int b, bool fix_in, StreamCoords coords, volatile int32_t *abort_flag,
                                                 int64_t limit, int *err) {
     using C = BCfg<HD>;
     if (!wait_phase(smem_u32(&bars->fix_empty), (fcnt & 1u) ^ 1u, abort_flag, limit, err)) return false;
     {
         const uint32_t bf = smem_u32(&bars->fix_full);
         mbar_expect_tx(bf, 2 * C::TILE_BYTES);
-        for (int c = 0; c < C::SLABS; ++c) {
+        for (int c = 0; c < C::SLABS && fix_in; ++c) {
             tma_load_5d(fix0 + c * C::SLAB_BYTES, fa, bf, c * 64, f_rank, f_row, fh, b);
             tma_load_5d(fix0 + C::TILE_BYTES + c * C::SLAB_BYTES, fb, bf, c * 64, f_rank, f_row, fh, b);
         }
@@ -534,7 +539,7 @@ __device__ __forceinline__ bool produce_item_kv(BBars *bars, uint32_t fix0, uint
     }
     for (int t = 0; t < n; ++t) {
         int row, head;
-        coords(t, row, head);
+        const bool in = coords(t, row, head);
         for (int which = 0; which < 2; ++which) {
             Ring &r = which ? vr : kr;
             uint64_t *emp = which ? bars->emptyv : bars->empty;
@@ -543,7 +548,7 @@ __device__ __forceinline__ bool produce_item_kv(BBars *bars, uint32_t fix0, uint
             const uint32_t bf = smem_u32(&ful[r.slot]);
             mbar_expect_tx(bf, C::TILE_BYTES);
             const uint32_t dst = (which ? v0 : k0) + r.slot * C::TILE_BYTES;
-            for (int c = 0; c < C::SLABS; ++c)
+            for (int c = 0; c < C::SLABS && in; ++c)
                 tma_load_5d(dst + c * C::SLAB_BYTES, which ? tv : tk, bf, c * 64, s_rank, row, head, b);
             r.issued |= 1u << r.slot;
             r.last_ph = (r.last_ph & ~(1u << r.slot)) | (r.ph << r.slot);
@@ -691,6 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_do);
+            producer_delay(P.producer_delay_ns);
             Ring kr = {0, 0u, 0u, 0u}, vr = {0, 0u, 0u, 0u};
             uint32_t fcnt = 0, rcnt = 0;
             bool ok = true;
@@ -707,14 +713,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const BSeg &S = rec.seg;
                 const int hk = it.hk;
                 QWalk walk;
-                auto coords = [&](int t, int &row, int &head) {
+                auto coords = [&](int t, int &row, int &head) -> bool {
                     int klim;
                     walk.next<FUSED>(P, S, it, row, klim);
                     head = hk;
                     (void)t;
+                    return in_bounds(row >= 0 && row < P.N / P.rs && hk < P.Hkv && S.s_rank < P.rs, err);
                 };
+                const bool fix_in = in_bounds(it.r_lo >= 0 && it.r_lo < P.N / P.rs && it.h < P.Hq &&
+                                                  S.f_rank < P.rs && it.b < P.B,
+                                              err);
                 ok = produce_item_kv<HD>(bars, sQ, sK, sV, kr, vr, fcnt, &tm_q, &tm_do, it.r_lo, S.f_rank, it.h,
-                                         &tm_k, &tm_v, S.s_rank, it.n, it.b, coords, abort_flag, limit, err);
+                                         &tm_k, &tm_v, S.s_rank, it.n, it.b, fix_in, coords, abort_flag, limit, err);
             }
             if (ok) {  // no more items
                 Rec<QItem> rec;
@@ -805,9 +815,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const BSeg &S = rec.seg;
             const int n = it.n, diag = S.diag;
             const int row = it.r_lo + quarter * 32 + lane;  // index in the fixed range
-            const bool valid = row < it.r_hi;
             const int64_t pos = (int64_t)row * P.rs + S.f_rank;
             const int64_t lrow = ((int64_t)it.b * P.Hq + it.h) * P.N + pos;
+            const bool valid = row < it.r_hi && in_bounds(pos < P.N && lrow < (int64_t)P.B * P.Hq * P.N, err);
             const float lse_l2 = valid ? P.lse[lrow] * kLog2e : 0.f;
             const float d_r = valid ? P.dvec[lrow] : 0.f;
             float *accp = P.acc_q + lrow * HD;
@@ -958,6 +968,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_do);
+            producer_delay(P.producer_delay_ns);
             int slot = 0;
             uint32_t ph = 0, fcnt = 0, issued = 0, last_ph = 0, rcnt = 0;
             bool ok = true;
@@ -974,14 +985,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const BSeg &S = rec.seg;
                 const int hk = it.hk;
                 KWalk walk;
-                auto coords = [&](int t, int &row, int &head) {
+                auto coords = [&](int t, int &row, int &head) -> bool {
                     int qlim, g;
                     walk.next<FUSED>(P, S, it, row, qlim, g);
                     head = hk * G + g;
                     (void)t;
+                    return in_bounds(row >= 0 && row < P.N / P.rs && head < P.Hq && S.s_rank < P.rs, err);
                 };
+                const bool fix_in = in_bounds(it.c_lo >= 0 && it.c_lo < P.N / P.rs && hk < P.Hkv &&
+                                                  S.f_rank < P.rs && it.b < P.B,
+                                              err);
                 ok = produce_item<HD>(bars, sK, sSt, slot, ph, fcnt, issued, last_ph, &tm_k, &tm_v, it.c_lo,
-                                      S.f_rank, hk, &tm_q, &tm_do, S.s_rank, it.n, it.b, coords, abort_flag,
+                                      S.f_rank, hk, &tm_q, &tm_do, S.s_rank, it.n, it.b, fix_in, coords, abort_flag,
                                       limit, err);
             }
             if (ok) {  // no more items
@@ -1089,9 +1104,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const BSeg &S = P.seg[it.si];  // (read in place: a register copy would spill)
             const int n = it.n, diag = S.diag;
             const int key = it.c_lo + quarter * 32 + lane;  // index in the fixed range
-            const bool kvalid = key < it.c_hi;
             const int64_t kpos = (int64_t)key * P.rs + S.f_rank;
             const int64_t arow = (((int64_t)it.b * P.Hkv + it.hk) * P.N + kpos) * HD;
+            const bool kvalid = key < it.c_hi && in_bounds(kpos < P.N && it.hk < P.Hkv && it.b < P.B, err);
             if (kvalid && grp == 0 && !(S.flags & SEG_FIRST))
                 for (int i = 0; i < HD * 4; i += 128) {
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(P.acc_k + arow) + i));
@@ -1115,8 +1130,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int r = 0; r < 2; ++r) {
                     const int qme = q0 + grp * 64 + r * 32 + lane;
                     const int64_t li = ((int64_t)it.b * P.Hq + h) * P.N + (int64_t)qme * P.rs + S.s_rank;
-                    l[r] = qme < qlim ? P.lse[li] * kLog2e : 0.f;
-                    d[r] = qme < qlim ? P.dvec[li] : 0.f;
+                    const bool in = qme < qlim && in_bounds(li < (int64_t)P.B * P.Hq * P.N, err);
+                    l[r] = in ? P.lse[li] * kLog2e : 0.f;
+                    d[r] = in ? P.dvec[li] : 0.f;
                 }
             };
             float nl[2] = {0.f, 0.f}, nd[2] = {0.f, 0.f};

@@ -536,6 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
+            producer_delay(P.producer_delay_ns);
             int slot = 0;
             uint32_t ph = 0;
             uint32_t issued = 0, last_ph = 0;  // per-slot bit sets
@@ -589,9 +590,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t kbuf = sKV + (2 * slot + 1) * C::TILE_BYTES;
                     if (has_v) {
                         const int vs = FUSED ? vstart : it.kt.start(it.tile(st));
+                        if (in_bounds(vrank >= 0 && vrank < P.rs && vs >= 0 && vs < P.N / P.rs && it.hk >= 0 &&
+                                          it.hk < P.Hkv && it.b >= 0 && it.b < P.B,
+                                      P.err))
 #pragma unroll
-                        for (int c = 0; c < C::SLABS; ++c)
-                            tma_load_5d(vbuf + c * C::SLAB_BYTES, &tm_v, b_full, c * 64, vrank, vs, it.hk, it.b);
+                            for (int c = 0; c < C::SLABS; ++c)
+                                tma_load_5d(vbuf + c * C::SLAB_BYTES, &tm_v, b_full, c * 64, vrank, vs, it.hk, it.b);
                     }
                     if (has_k) {
                         int ks, kr = it.kv_rank;
@@ -608,9 +612,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         } else {
                             ks = it.kt.start(it.tile(st + 1));
                         }
+                        if (in_bounds(kr >= 0 && kr < P.rs && ks >= 0 && ks < P.N / P.rs && it.hk >= 0 &&
+                                          it.hk < P.Hkv && it.b >= 0 && it.b < P.B,
+                                      P.err))
 #pragma unroll
-                        for (int c = 0; c < C::SLABS; ++c)
-                            tma_load_5d(kbuf + c * C::SLAB_BYTES, &tm_k, b_full, c * 64, kr, ks, it.hk, it.b);
+                            for (int c = 0; c < C::SLABS; ++c)
+                                tma_load_5d(kbuf + c * C::SLAB_BYTES, &tm_k, b_full, c * 64, kr, ks, it.hk, it.b);
                     }
                     issued |= 1u << slot;
                     last_ph = (last_ph & ~(1u << slot)) | (ph << slot);
@@ -629,6 +636,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 break;
                             }
                             mbar_expect_tx(qf, C::TILE_BYTES);
+                            if (in_bounds(it.q_rank >= 0 && it.q_rank < P.rs && it.qrow0 + hh * BM >= 0 &&
+                                              it.qrow0 + hh * BM < P.N / P.rs && it.h >= 0 && it.h < P.Hq &&
+                                              it.b >= 0 && it.b < P.B,
+                                          P.err))
 #pragma unroll
                             for (int c = 0; c < C::SLABS; ++c)
                                 tma_load_5d(sQ + hh * C::TILE_BYTES + c * C::SLAB_BYTES, &tm_q, qf,
@@ -950,7 +961,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool first = (it.flags & SEG_FIRST) != 0;
             const bool final_ = (it.flags & SEG_FINAL) != 0;
             const int64_t lrow = ((int64_t)it.b * P.Hq + it.h) * P.N + pos;
-            const bool valid = row_g < it.q1;
+            const bool valid = row_g < it.q1 && in_bounds(pos >= 0 && pos < P.N && lrow < (int64_t)P.B * P.Hq * P.N, P.err);
             const bool merge = valid && !first;
             float *arow = P.oacc ? P.oacc + lrow * HD : nullptr;
             const float lse_a = merge ? P.lse[lrow] : -INFINITY;
@@ -1015,7 +1026,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) {
+                    // (debug builds: a box wholly past the end of the rows, of a half clipped
+                    // by the tensor's end, writes nothing and is skipped unchecked)
+                    if (lane == 0 && (!kDebugBounds || (first_row + quarter * 32 < P.N / P.rs &&
+                                                        in_bounds(first_row >= 0 && it.q_rank >= 0 &&
+                                                                      it.q_rank < P.rs && it.h >= 0 &&
+                                                                      it.h < P.Hq && it.b >= 0 && it.b < P.B,
+                                                                  P.err)))) {
                         tma_store_5d(&tm_o, buf, c * 32, it.q_rank, first_row + quarter * 32, it.h, it.b);
                         bulk_commit();
                     }
@@ -1086,6 +1103,12 @@ __global__ void wait_selftest_kernel(int64_t limit_ns, int *err) {
     mbar_init(smem_u32(&bar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     wait_phase(smem_u32(&bar), 0, &abort, limit_ns, err);
+}
+
+// One block, one thread: the device bounds check on an index outside its range (debug
+// builds record DERR_BOUNDS; nothing is accessed).
+__global__ void bounds_selftest_kernel(int n, int *err) {
+    if (threadIdx.x == 0) (void)bounds_check(n < 0, err);
 }
 
 }  // namespace tc
@@ -1169,6 +1192,17 @@ cudaError_t launch_attn_tc(const StepParams &P, int blocks_y, int num_sms, cudaS
 }
 
 int attn_tc_rows_per_block() { return 2 * tc::BM; }
+
+cudaError_t launch_bounds_selftest(int *err, cudaStream_t stream) {
+#ifdef RA_DEBUG_BOUNDS
+    tc::bounds_selftest_kernel<<<1, 32, 0, stream>>>(1, err);
+    return cudaGetLastError();
+#else
+    (void)err;
+    (void)stream;
+    return cudaErrorNotSupported;
+#endif
+}
 
 cudaError_t launch_wait_selftest(int64_t limit_ns, int *err, cudaStream_t stream) {
     tc::wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns, err);

@@ -15,6 +15,7 @@ cudaError_t launch_attn_simt(const StepParams &P, int blocks_y, cudaStream_t str
 cudaError_t launch_attn_tc(const StepParams &P, int blocks_y, int num_sms, cudaStream_t stream);
 int attn_tc_rows_per_block();
 cudaError_t launch_wait_selftest(int64_t limit_ns, int *err, cudaStream_t stream);
+cudaError_t launch_bounds_selftest(int *err, cudaStream_t stream);
 
 cudaError_t launch_lse_merge(const MergeParams &P, int num_sms, cudaStream_t stream);
 cudaError_t launch_attn_bwd_simt(const BwdParams &P, int parts, cudaStream_t stream);
@@ -38,8 +39,56 @@ static ra_status fail(ra_status s, const std::string &msg) {
     return s;
 }
 
+// Launch failures injected on the host (ra_debug_fail_next_launches): the next n kernel
+// launches of the calling thread report cudaErrorLaunchFailure without reaching the GPU.
+static thread_local int t_inject_launch_failures = 0;
+static thread_local bool t_injected = false;
+
+// Guard in front of every kernel launch: true when this launch is to fail (injected).
+static bool launch_injected() {
+    if (t_inject_launch_failures <= 0) return false;
+    --t_inject_launch_failures;
+    t_injected = true;
+    return true;
+}
+
+// Per-launch timing (ra_debug_time_launches): while on, each kernel launch of the calling
+// thread is bracketed by two CUDA events on its stream.
+struct TimedLaunch {
+    const char *name;
+    cudaEvent_t start, stop;
+};
+static thread_local bool t_time_launches = false;
+static thread_local std::vector<TimedLaunch> t_timed;
+
+// Every kernel launch goes through here: an injected failure, or the launch `f` (timed
+// when timing is on).
+template <class F>
+static cudaError_t guarded_launch(const char *name, cudaStream_t st, F &&f) {
+    if (launch_injected()) return cudaErrorLaunchFailure;
+    if (!t_time_launches) return f();
+    TimedLaunch t{name, nullptr, nullptr};
+    if (cudaEventCreate(&t.start) != cudaSuccess || cudaEventCreate(&t.stop) != cudaSuccess ||
+        cudaEventRecord(t.start, st) != cudaSuccess) {
+        if (t.start) cudaEventDestroy(t.start);
+        if (t.stop) cudaEventDestroy(t.stop);
+        return f();
+    }
+    const cudaError_t e = f();
+    if (cudaEventRecord(t.stop, st) == cudaSuccess) {
+        t_timed.push_back(t);
+    } else {
+        cudaEventDestroy(t.start);
+        cudaEventDestroy(t.stop);
+    }
+    return e;
+}
+
 static ra_status cuda_fail(cudaError_t e, const char *what) {
-    return fail(RA_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+    std::string msg = std::string(what) + ": " + cudaGetErrorString(e);
+    if (t_injected) msg += " (injected on the host by ra_debug_fail_next_launches)";
+    t_injected = false;
+    return fail(RA_ERR_CUDA, msg);
 }
 
 __device__ int g_device_error;
@@ -50,6 +99,7 @@ static std::mutex g_mu;
 static int *g_err_ptr[kMaxDev];
 static int g_num_sms[kMaxDev];
 static int64_t g_wait_limit_ns = 2000000000LL;
+static int64_t g_producer_delay_ns = 0;
 
 struct DevInfo {
     int dev;
@@ -122,7 +172,7 @@ struct Problem {
 };
 
 static ra_status check_qkvo(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v,
-                            const ra_tensor *o, const float *lse, Problem &pb) {
+                            const ra_tensor *o, const float *lse, Problem &pb, bool need_lse = true) {
     ra_status s;
     if ((s = check_tensor(q, "q")) || (s = check_tensor(k, "k")) || (s = check_tensor(v, "v")) ||
         (s = check_tensor(o, "o")))
@@ -146,7 +196,7 @@ static ra_status check_qkvo(const ra_tensor *q, const ra_tensor *k, const ra_ten
     if (pb.Hkv < 1 || pb.Hq % pb.Hkv != 0)
         return fail(RA_ERR_INVALID_ARG, "Hq must be a positive multiple of Hkv");
     if (pb.D < 1) return fail(RA_ERR_INVALID_ARG, "D must be >= 1");
-    if (!lse) return fail(RA_ERR_INVALID_ARG, "lse is NULL");
+    if (need_lse && !lse) return fail(RA_ERR_INVALID_ARG, "lse is NULL");
     if (pb.D > 128) return fail(RA_ERR_UNSUPPORTED, "head size D > 128 is not supported");
     if (pb.N > (int64_t)1 << 30 || pb.B * pb.Hq > 65535LL * 32768LL)
         return fail(RA_ERR_UNSUPPORTED, "problem too large for one launch grid");
@@ -159,100 +209,110 @@ struct Range {
     int64_t a, b;
 };
 
-static std::vector<Range> rank_ranges(int64_t N, int R, int layout, int r) {
+// Row ranges of rank r under the contiguous or zigzag layout, into out[0..2); returns how
+// many (1 or 2).  No allocation: the allocation-free entry point plans with it too.
+static int rank_ranges(int64_t N, int R, int layout, int r, Range out[2]) {
     if (layout == RA_LAYOUT_CONTIG) {
         const int64_t c = N / R;
-        return {{r * c, (r + 1) * c}};
+        out[0] = {r * c, (r + 1) * c};
+        return 1;
     }
     const int64_t h = N / (2 * (int64_t)R);
-    return {{r * h, (r + 1) * h}, {(2 * (int64_t)R - 1 - r) * h, (2 * (int64_t)R - r) * h}};
+    out[0] = {r * h, (r + 1) * h};
+    out[1] = {(2 * (int64_t)R - 1 - r) * h, (2 * (int64_t)R - r) * h};
+    return 2;
 }
 
-// Segments of one step before flags: for every rank r, each of its query chunks
-// against the chunks of rank (r - step) mod R that some row of the chunk can see.
-// Striped layout: rank r holds positions r, r + R, r + 2R, ...; its segment is indices
-// [0, N/R) of the interleave against the same indices of rank j, with key index j'
-// visible to row index i iff j' + [j > r] <= i under causality.
-static void step_segments(int64_t N, int R, int layout, int causal, int step,
-                          std::vector<Seg> &out) {
-    out.clear();
-    if (layout == RA_LAYOUT_STRIPED) {
-        const int64_t c = N / R;
-        for (int r = 0; r < R; ++r) {
-            const int j = ((r - step) % R + R) % R;
-            Seg s;
-            memset(&s, 0, sizeof s);
-            s.q0 = 0;
-            s.q1 = (int32_t)c;
-            s.k0[0] = 0;
-            s.k1[0] = (int32_t)c;
-            s.k0[1] = s.k1[1] = (int32_t)c;
-            s.rank = r;
-            s.q_rank = r;
-            s.kv_rank = j;
-            s.diag = (causal && j > r) ? 1 : 0;
-            if (c == 0 || (causal && s.diag > c - 1)) continue;  // no row sees a key
-            out.push_back(s);
-        }
-        return;
-    }
-    for (int r = 0; r < R; ++r) {
-        const int j = ((r - step) % R + R) % R;
-        const std::vector<Range> kv = rank_ranges(N, R, layout, j);
-        for (const Range &qr : rank_ranges(N, R, layout, r)) {
-            if (qr.b <= qr.a) continue;
-            Seg s;
-            memset(&s, 0, sizeof s);
-            s.q0 = (int32_t)qr.a;
-            s.q1 = (int32_t)qr.b;
-            int nk = 0;
-            for (const Range &kr : kv) {
-                if (kr.b <= kr.a) continue;
-                if (causal && kr.a > qr.b - 1) continue;  // every key after every row
-                s.k0[nk] = (int32_t)kr.a;
-                s.k1[nk] = (int32_t)kr.b;
-                ++nk;
-            }
-            if (nk == 0) continue;
-            if (nk == 1) s.k0[1] = s.k1[1] = s.k1[0];
-            s.rank = r;
-            out.push_back(s);
-        }
-    }
-}
-
-static bool chunk_touched(int64_t N, int R, int layout, int causal, int step, int r, int64_t q0,
-                          int64_t q1) {
+// Whether rank r's query chunk ending at row q1 - 1 sees any key of the block it holds at
+// `step` (that of rank (r - step) mod R).  Striped layout: every rank's rows are [0, N/R)
+// of its interleave, and under causality a later rank's block is seen from row index 1.
+static bool chunk_touched(int64_t N, int R, int layout, int causal, int step, int r, int64_t q1) {
     const int j = ((r - step) % R + R) % R;
     if (layout == RA_LAYOUT_STRIPED) {
         const int64_t c = N / R;
         return c > 0 && !(causal && j > r && c < 2);
     }
-    for (const Range &kr : rank_ranges(N, R, layout, j)) {
-        if (kr.b <= kr.a) continue;
-        if (causal && kr.a > q1 - 1) continue;
+    Range kv[2];
+    const int nk = rank_ranges(N, R, layout, j, kv);
+    for (int i = 0; i < nk; ++i) {
+        if (kv[i].b <= kv[i].a) continue;
+        if (causal && kv[i].a > q1 - 1) continue;  // every key after every row
         return true;
     }
-    (void)q0;
     return false;
 }
 
-static void plan_step(int64_t N, int R, int layout, int causal, int step, std::vector<Seg> &segs) {
-    step_segments(N, R, layout, causal, step, segs);
-    for (Seg &s : segs) {
-        bool earlier = false, later = false;
-        for (int t = 0; t < step && !earlier; ++t)
-            earlier = chunk_touched(N, R, layout, causal, t, s.rank, s.q0, s.q1);
-        for (int t = step + 1; t < R && !later; ++t)
-            later = chunk_touched(N, R, layout, causal, t, s.rank, s.q0, s.q1);
-        s.flags = (earlier ? 0 : SEG_FIRST) | (later ? 0 : SEG_FINAL);
+static int64_t seg_keys(const Seg &x) { return (int64_t)(x.k1[0] - x.k0[0]) + (x.k1[1] - x.k0[1]); }
+
+// The segments of one ring step into segs[0 .. 2R): for every rank r, each of its query
+// chunks against the chunks of rank (r - step) mod R that some row of the chunk can see,
+// flagged SEG_FIRST when no earlier step touches the chunk and SEG_FINAL when no later one
+// does, heaviest (most keys) first, equal ones in rank order.  Striped layout: rank r holds
+// positions r, r + R, r + 2R, ...; its segment is indices [0, N/R) of the interleave
+// against the same indices of rank j, with key index j' visible to row index i iff
+// j' + [j > r] <= i under causality.  Returns the number of segments.  No allocation
+// (a stable insertion sort), so the allocation-free entry point shares this schedule.
+static int plan_step(int64_t N, int R, int layout, int causal, int step, Seg *segs) {
+    int n = 0;
+    for (int r = 0; r < R; ++r) {
+        const int j = ((r - step) % R + R) % R;
+        Seg cand[2];
+        int nc = 0;
+        if (layout == RA_LAYOUT_STRIPED) {
+            const int64_t c = N / R;
+            Seg &g = cand[0];
+            memset(&g, 0, sizeof g);
+            g.q0 = 0;
+            g.q1 = (int32_t)c;
+            g.k0[0] = 0;
+            g.k1[0] = (int32_t)c;
+            g.k0[1] = g.k1[1] = (int32_t)c;
+            g.rank = r;
+            g.q_rank = r;
+            g.kv_rank = j;
+            g.diag = (causal && j > r) ? 1 : 0;
+            if (!(c == 0 || (causal && g.diag > c - 1))) nc = 1;  // else no row sees a key
+        } else {
+            Range qr[2], kv[2];
+            const int nq = rank_ranges(N, R, layout, r, qr);
+            const int nkv = rank_ranges(N, R, layout, j, kv);
+            for (int qi = 0; qi < nq; ++qi) {
+                if (qr[qi].b <= qr[qi].a) continue;
+                Seg &g = cand[nc];
+                memset(&g, 0, sizeof g);
+                g.q0 = (int32_t)qr[qi].a;
+                g.q1 = (int32_t)qr[qi].b;
+                int nk = 0;
+                for (int ki = 0; ki < nkv; ++ki) {
+                    if (kv[ki].b <= kv[ki].a) continue;
+                    if (causal && kv[ki].a > qr[qi].b - 1) continue;  // every key after every row
+                    g.k0[nk] = (int32_t)kv[ki].a;
+                    g.k1[nk] = (int32_t)kv[ki].b;
+                    ++nk;
+                }
+                if (nk == 0) continue;
+                if (nk == 1) g.k0[1] = g.k1[1] = g.k1[0];
+                g.rank = r;
+                ++nc;
+            }
+        }
+        for (int i = 0; i < nc; ++i) {
+            Seg g = cand[i];
+            bool earlier = false, later = false;
+            for (int t = 0; t < step && !earlier; ++t) earlier = chunk_touched(N, R, layout, causal, t, r, g.q1);
+            for (int t = step + 1; t < R && !later; ++t) later = chunk_touched(N, R, layout, causal, t, r, g.q1);
+            g.flags = (earlier ? 0 : SEG_FIRST) | (later ? 0 : SEG_FINAL);
+            // heaviest segments first (more keys), so they lead every dispatch round
+            int at = n;
+            while (at > 0 && seg_keys(segs[at - 1]) < seg_keys(g)) {
+                segs[at] = segs[at - 1];
+                --at;
+            }
+            segs[at] = g;
+            ++n;
+        }
     }
-    // heaviest segments first (more keys), so they lead every dispatch round
-    std::stable_sort(segs.begin(), segs.end(), [](const Seg &x, const Seg &y) {
-        const int64_t cx = (int64_t)(x.k1[0] - x.k0[0]) + (x.k1[1] - x.k0[1]);
-        const int64_t cy = (int64_t)(y.k1[0] - y.k0[0]) + (y.k1[1] - y.k0[1]);
-        return cx > cy;
-    });
+    return n;
 }
 
 static ra_status check_ring(int64_t N, int R, int layout) {
@@ -289,8 +349,11 @@ static void bwd_pairs(int64_t N, int R, int layout, int causal, int step, std::v
             out.push_back({r, j, {0, c}, {0, c}, diag});
             continue;
         }
-        for (const Range &qr : rank_ranges(N, R, layout, r))
-            for (const Range &kr : rank_ranges(N, R, layout, j)) {
+        Range qrs[2], krs[2];
+        const int nq = rank_ranges(N, R, layout, r, qrs), nk = rank_ranges(N, R, layout, j, krs);
+        for (int qi = 0; qi < nq; ++qi)
+            for (int ki = 0; ki < nk; ++ki) {
+                const Range &qr = qrs[qi], &kr = krs[ki];
                 if (qr.b <= qr.a || kr.b <= kr.a) continue;
                 if (causal && kr.a > qr.b - 1) continue;  // every key after every row
                 out.push_back({r, j, qr, kr, 0});
@@ -391,39 +454,42 @@ struct BwdPlan {
     }
 };
 
-// The fused ring launch (tensor cores, contiguous or zigzag layout): one segment per query
-// chunk, tagged with its rank; the kernel walks the chunk's key ranges of steps 0..R-1 in
-// ring order (those of rank (r - s) mod R) and keeps the running result on chip, so each
-// row is written once (SEG_FIRST | SEG_FINAL).  Heaviest chunks (most visible keys over
-// all steps) first.  False when it does not apply (striped layout, or more chunks than a
-// launch holds).
-static bool fused_ring_segments(int64_t N, int R, int layout, int causal, std::vector<Seg> &out) {
-    out.clear();
+// The fused ring launch (tensor cores): one segment per query chunk, tagged with its
+// rank; the kernel walks the chunk's key ranges of steps 0..R-1 in ring order (those of
+// rank (r - s) mod R) and keeps the running result on chip, so each row is written once
+// (SEG_FIRST | SEG_FINAL) and no float32 running output is needed.  Heaviest chunks (most
+// visible keys over all steps) first.  Fills out[0 .. kMaxSeg) and returns the segment
+// count, or 0 when the fused launch does not apply (more chunks than a launch holds; a
+// striped rank that is not whole 128-row tiles).  No allocation.
+static int fused_ring_segments(int64_t N, int R, int layout, int causal, Seg *out) {
     if (layout == RA_LAYOUT_STRIPED) {
         // one segment per rank, in the rank-local index space: the kernel walks each
         // step's causal prefix with its diagonal offset.  Needs whole 128-row tiles per
         // rank (every step of an item then has the same tile count); the ranks' work is
         // the same, so their order does not matter.
         const int64_t c = N / R;
-        if (R > kMaxSeg || c % 128 != 0 || c > INT32_MAX) return false;
+        if (R > kMaxSeg || c % 128 != 0 || c > INT32_MAX || c == 0) return 0;
         for (int r = 0; r < R; ++r) {
-            Seg g;
+            Seg &g = out[r];
             memset(&g, 0, sizeof g);
             g.q0 = 0;
             g.q1 = (int32_t)c;
             g.q_rank = r;
             g.rank = r;
             g.flags = SEG_FIRST | SEG_FINAL;
-            out.push_back(g);
         }
         (void)causal;
-        return true;
+        return R;
     }
     const int chunks = layout == RA_LAYOUT_ZIGZAG ? 2 * R : R;
-    if (chunks > kMaxSeg || N > INT32_MAX) return false;
-    std::vector<std::pair<int64_t, Seg>> work;
-    for (int r = 0; r < R; ++r)
-        for (const Range &qr : rank_ranges(N, R, layout, r)) {
+    if (chunks > kMaxSeg || N > INT32_MAX) return 0;
+    int64_t work[kMaxSeg];
+    int n = 0;
+    for (int r = 0; r < R; ++r) {
+        Range qrs[2];
+        const int nq = rank_ranges(N, R, layout, r, qrs);
+        for (int qi = 0; qi < nq; ++qi) {
+            const Range &qr = qrs[qi];
             if (qr.b <= qr.a) continue;
             Seg g;
             memset(&g, 0, sizeof g);
@@ -432,19 +498,28 @@ static bool fused_ring_segments(int64_t N, int R, int layout, int causal, std::v
             g.rank = r;
             g.flags = SEG_FIRST | SEG_FINAL;
             int64_t keys = 0;
-            for (int s = 0; s < R; ++s) {
-                const int j = ((r - s) % R + R) % R;
-                for (const Range &kr : rank_ranges(N, R, layout, j)) {
+            for (int st = 0; st < R; ++st) {
+                const int j = ((r - st) % R + R) % R;
+                Range krs[2];
+                const int nk = rank_ranges(N, R, layout, j, krs);
+                for (int ki = 0; ki < nk; ++ki) {
+                    const Range &kr = krs[ki];
                     if (kr.b <= kr.a || (causal && kr.a > qr.b - 1)) continue;
                     keys += kr.b - kr.a;
                 }
             }
-            work.push_back({keys, g});
+            int at = n;  // stable insertion, most keys first
+            while (at > 0 && work[at - 1] < keys) {
+                work[at] = work[at - 1];
+                out[at] = out[at - 1];
+                --at;
+            }
+            work[at] = keys;
+            out[at] = g;
+            ++n;
         }
-    std::stable_sort(work.begin(), work.end(),
-                     [](const std::pair<int64_t, Seg> &x, const std::pair<int64_t, Seg> &y) { return x.first > y.first; });
-    for (const auto &w : work) out.push_back(w.second);
-    return !out.empty();
+    }
+    return n;
 }
 
 // The fused ring backward (tensor cores, contiguous or zigzag layout): kind 0, one dQ
@@ -457,8 +532,11 @@ static bool fused_bwd_segments(int64_t N, int R, int layout, int causal, int kin
     const int chunks = layout == RA_LAYOUT_ZIGZAG ? 2 * R : R;
     if (chunks > kMaxBSeg || N > INT32_MAX) return false;
     std::vector<std::pair<int64_t, BSeg>> work;
-    for (int r = 0; r < R; ++r)
-        for (const Range &f : rank_ranges(N, R, layout, r)) {
+    for (int r = 0; r < R; ++r) {
+        Range frs[2];
+        const int nf = rank_ranges(N, R, layout, r, frs);
+        for (int fi = 0; fi < nf; ++fi) {
+            const Range &f = frs[fi];
             if (f.b <= f.a) continue;
             BSeg g;
             memset(&g, 0, sizeof g);
@@ -469,7 +547,10 @@ static bool fused_bwd_segments(int64_t N, int R, int layout, int causal, int kin
             int64_t pairs = 0;
             for (int s = 0; s < R; ++s) {
                 const int j = kind ? (r + s) % R : ((r - s) % R + R) % R;
-                for (const Range &p : rank_ranges(N, R, layout, j)) {
+                Range prs[2];
+                const int np = rank_ranges(N, R, layout, j, prs);
+                for (int pi = 0; pi < np; ++pi) {
+                    const Range &p = prs[pi];
                     if (p.b <= p.a) continue;
                     if (causal && (kind ? f.a > p.b - 1 : p.a > f.b - 1)) continue;
                     pairs += p.b - p.a;
@@ -477,6 +558,7 @@ static bool fused_bwd_segments(int64_t N, int R, int layout, int causal, int kin
             }
             work.push_back({pairs, g});
         }
+    }
     std::stable_sort(work.begin(), work.end(),
                      [](const std::pair<int64_t, BSeg> &x, const std::pair<int64_t, BSeg> &y) { return x.first > y.first; });
     for (const auto &w : work) out.push_back(w.second);
@@ -510,25 +592,33 @@ static void fill_common(StepParams &P, const ra_tensor *q, const ra_tensor *k, c
     const float sc = scale > 0.f ? scale : (float)(1.0 / sqrt((double)pb.D));
     P.scale_log2 = sc * kLog2e;
     P.wait_limit_ns = g_wait_limit_ns;
+    P.producer_delay_ns = g_producer_delay_ns;
     P.err = di.err;
     P.rs = 1;
 }
 
+// The arguments take the tensor-core kernels (bf16, D in {64, 128}, 16-byte aligned bases
+// and strides for the TMA maps) on an sm_103a device.
+static bool tc_args(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v, const ra_tensor *o,
+                    const Problem &pb) {
+    return pb.dtype == RA_BF16 && (pb.D == 64 || pb.D == 128) && aligned16(q) && aligned16(k) &&
+           aligned16(v) && aligned16(o);
+}
+
 static bool use_tensor_cores(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v,
                              const ra_tensor *o, const Problem &pb, const DevInfo &di) {
-    return di.tc_ok && pb.dtype == RA_BF16 && (pb.D == 64 || pb.D == 128) && aligned16(q) &&
-           aligned16(k) && aligned16(v) && aligned16(o);
+    return di.tc_ok && tc_args(q, k, v, o, pb);
 }
 
 // Launch the segments of one step (split into launches of <= kMaxSeg segments; all
 // segments of a step have equal query length).
-static ra_status run_step(StepParams &P, const std::vector<Seg> &segs, bool tc, int num_sms,
+static ra_status run_step(StepParams &P, const Seg *segs, int nsegs, bool tc, int num_sms,
                           cudaStream_t stream) {
     const int rows_per_block = tc ? attn_tc_rows_per_block() : 16;
-    for (size_t first = 0; first < segs.size(); first += kMaxSeg) {
-        const size_t n = std::min(segs.size() - first, (size_t)kMaxSeg);
+    for (int first = 0; first < nsegs; first += kMaxSeg) {
+        const int n = std::min(nsegs - first, kMaxSeg);
         int64_t qlen = 0;
-        for (size_t i = 0; i < n; ++i) {
+        for (int i = 0; i < n; ++i) {
             P.seg[i] = segs[first + i];
             qlen = std::max<int64_t>(qlen, segs[first + i].q1 - segs[first + i].q0);
         }
@@ -537,12 +627,37 @@ static ra_status run_step(StepParams &P, const std::vector<Seg> &segs, bool tc, 
         P.blocks_per_seg = (int32_t)((qlen + rows_per_block - 1) / rows_per_block);
         const int64_t blocks_y = (int64_t)P.nseg * P.blocks_per_seg;
         if (blocks_y > 65535) return fail(RA_ERR_UNSUPPORTED, "too many work blocks in one step");
-        cudaError_t e = tc ? launch_attn_tc(P, (int)blocks_y, num_sms, stream)
-                           : launch_attn_simt(P, (int)blocks_y, stream);
+        cudaError_t e = guarded_launch(tc ? "attn_tc" : "attn_simt", stream, [&] {
+            return tc ? launch_attn_tc(P, (int)blocks_y, num_sms, stream) : launch_attn_simt(P, (int)blocks_y, stream);
+        });
         P.chained = 1;  // later launches of this run may overlap this one's tail
         if (e != cudaSuccess) return cuda_fail(e, tc ? "attention (tensor-core) launch"
                                                      : "attention (CUDA-core) launch");
         ++t_launches;
+    }
+    return RA_OK;
+}
+
+// The launches of a ring run.  nfused > 0: segs holds the fused ring's segments, and one
+// launch walks every step with the running result on chip (P.oacc unused).  Otherwise one
+// launch per step merges into the float32 running output P.oacc (set by the caller when
+// ring_size > 1); segs must hold 2 * ring_size segments.  P.rs, P.prefer_pairs and the
+// common fields are the caller's.
+static ra_status ring_launches(StepParams &P, bool tc, int num_sms, int64_t N, int R, int layout, int causal,
+                               int nfused, Seg *segs, cudaStream_t st) {
+    if (nfused > 0) {
+        P.oacc = nullptr;
+        P.ring_fused = 1;
+        P.ring_R = R;
+        P.ring_layout = layout == RA_LAYOUT_ZIGZAG ? 1 : (layout == RA_LAYOUT_STRIPED ? 2 : 0);
+        P.prefer_pairs = 0;
+        return run_step(P, segs, nfused, tc, num_sms, st);
+    }
+    for (int step = 0; step < R; ++step) {
+        const int n = plan_step(N, R, layout, causal, step, segs);
+        if (n == 0) continue;
+        ra_status s = run_step(P, segs, n, tc, num_sms, st);
+        if (s) return s;
     }
     return RA_OK;
 }
@@ -562,6 +677,16 @@ size_t ra_ring_sim_workspace_bytes(const ra_tensor *q, int ring_size) {
     return (size_t)(q->shape[0] * q->shape[1] * q->shape[2] * q->shape[3]) * sizeof(float);
 }
 
+size_t ra_ring_sim_workspace_bytes_for(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v,
+                                       const ra_tensor *o, int ring_size, ra_layout layout, int causal) {
+    Problem pb;
+    if (check_qkvo(q, k, v, o, nullptr, pb, false) != RA_OK) return 0;
+    if (check_ring(pb.N, ring_size, layout) != RA_OK || ring_size == 1) return 0;
+    Seg segs[kMaxSeg];
+    if (tc_args(q, k, v, o, pb) && fused_ring_segments(pb.N, ring_size, layout, causal, segs) > 0) return 0;
+    return (size_t)(pb.B * pb.Hq * pb.N * pb.D) * sizeof(float);
+}
+
 ra_status ra_ring_sim_fwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v,
                           ra_tensor *o, float *lse, int ring_size, ra_layout layout, int causal,
                           float scale, void *workspace, void *stream) {
@@ -571,14 +696,21 @@ ra_status ra_ring_sim_fwd(const ra_tensor *q, const ra_tensor *k, const ra_tenso
     if (isnan(scale)) return fail(RA_ERR_INVALID_ARG, "scale is NaN");
     if ((s = check_ring(pb.N, ring_size, layout))) return s;
     if (pb.B * pb.Hq * pb.N == 0) return RA_OK;
-    if (ring_size > 1) {
-        if (!workspace) return fail(RA_ERR_INVALID_ARG, "workspace is NULL (ring_size > 1)");
-        if (reinterpret_cast<uintptr_t>(workspace) % 16)
-            return fail(RA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
-    }
+    if (workspace && reinterpret_cast<uintptr_t>(workspace) % 16)
+        return fail(RA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    static const char *kNeedWs =
+        "workspace is NULL, and this ring run keeps a float32 running output "
+        "(ra_ring_sim_workspace_bytes_for() bytes)";
+    std::vector<Seg> segs(std::max(2 * (size_t)ring_size, (size_t)kMaxSeg));
+    const int nfused_args =
+        (ring_size > 1 && tc_args(q, k, v, o, pb)) ? fused_ring_segments(pb.N, ring_size, layout, causal, segs.data()) : 0;
+    if (ring_size > 1 && nfused_args == 0 && !workspace) return fail(RA_ERR_INVALID_ARG, kNeedWs);
     DevInfo di;
     std::string msg;
     if (!device_info(di, msg)) return fail(RA_ERR_CUDA, msg);
+    const bool tc = use_tensor_cores(q, k, v, o, pb, di);
+    const int nfused = tc ? nfused_args : 0;
+    if (ring_size > 1 && nfused == 0 && !workspace) return fail(RA_ERR_INVALID_ARG, kNeedWs);
     StepParams *P = new StepParams;
     fill_common(*P, q, k, v, o, lse, pb, causal, scale, di);
     P->oacc = ring_size > 1 ? static_cast<float *>(workspace) : nullptr;
@@ -586,24 +718,8 @@ ra_status ra_ring_sim_fwd(const ra_tensor *q, const ra_tensor *k, const ra_tenso
     // per-step ring launches overlap their tails with the next step's launch, so they
     // take tile-pair items; striped rings measured better with single blocks
     P->prefer_pairs = (ring_size > 1 && layout != RA_LAYOUT_STRIPED) ? 1 : 0;
-    const bool tc = use_tensor_cores(q, k, v, o, pb, di);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    std::vector<Seg> segs;
-    if (tc && ring_size > 1 && fused_ring_segments(pb.N, ring_size, layout, causal, segs)) {
-        // one launch walks every step: each query chunk's running result stays on chip
-        P->ring_fused = 1;
-        P->ring_R = ring_size;
-        P->ring_layout = layout == RA_LAYOUT_ZIGZAG ? 1 : (layout == RA_LAYOUT_STRIPED ? 2 : 0);
-        P->prefer_pairs = 0;
-        s = run_step(*P, segs, tc, di.sms, st);
-    } else {
-        for (int step = 0; step < ring_size; ++step) {
-            plan_step(pb.N, ring_size, layout, causal, step, segs);
-            if (segs.empty()) continue;
-            s = run_step(*P, segs, tc, di.sms, st);
-            if (s) break;
-        }
-    }
+    s = ring_launches(*P, tc, di.sms, pb.N, ring_size, layout, causal, nfused, segs.data(),
+                      static_cast<cudaStream_t>(stream));
     delete P;
     return s;
 }
@@ -612,9 +728,9 @@ int64_t ra_ring_sim_plan(int64_t N, int ring_size, ra_layout layout, int causal,
                          int64_t *segments, int64_t cap) {
     if (N < 0 || N > ((int64_t)1 << 30) || step < 0 || step >= ring_size) return -1;
     if (check_ring(N, ring_size, layout) != RA_OK) return -1;
-    std::vector<Seg> segs;
-    plan_step(N, ring_size, layout, causal, step, segs);
-    for (int64_t i = 0; i < (int64_t)segs.size() && i < cap && segments; ++i) {
+    std::vector<Seg> segs(2 * (size_t)ring_size);
+    const int n = plan_step(N, ring_size, layout, causal, step, segs.data());
+    for (int64_t i = 0; i < (int64_t)n && i < cap && segments; ++i) {
         const Seg &x = segs[i];
         int64_t *o = segments + 12 * i;
         o[0] = x.q0;
@@ -630,7 +746,7 @@ int64_t ra_ring_sim_plan(int64_t N, int ring_size, ra_layout layout, int causal,
         o[10] = x.diag;
         o[11] = (layout == RA_LAYOUT_STRIPED) ? ring_size : 1;
     }
-    return (int64_t)segs.size();
+    return (int64_t)n;
 }
 
 int64_t ra_ring_sim_bwd_plan(int64_t N, int ring_size, ra_layout layout, int causal, int step, int kind,
@@ -708,8 +824,9 @@ ra_status ra_attn_varlen_fwd(const ra_tensor *q, const ra_tensor *k, const ra_te
             s = fail(RA_ERR_UNSUPPORTED, "too many work blocks in one launch");
             break;
         }
-        cudaError_t e = tc ? launch_attn_tc(*P, (int)blocks, di.sms, st)
-                           : launch_attn_simt(*P, (int)blocks, st);
+        cudaError_t e = guarded_launch(tc ? "attn_tc" : "attn_simt", st, [&] {
+            return tc ? launch_attn_tc(*P, (int)blocks, di.sms, st) : launch_attn_simt(*P, (int)blocks, st);
+        });
         if (e != cudaSuccess) {
             s = cuda_fail(e, "varlen attention launch");
             break;
@@ -731,9 +848,9 @@ ra_status ra_attn_varlen_fwd(const ra_tensor *q, const ra_tensor *k, const ra_te
         if (covered < pb.N) gaps.push_back({covered, pb.N});
     }
     for (size_t i = 0; i < gaps.size() && !s; ++i) {
-        cudaError_t e = launch_fill_identity(o->data, pb.dtype == RA_BF16, o->stride, lse, (int)pb.B,
+        cudaError_t e = guarded_launch("fill_identity", st, [&] { return launch_fill_identity(o->data, pb.dtype == RA_BF16, o->stride, lse, (int)pb.B,
                                              (int)pb.Hq, (int)pb.N, (int)pb.D, (int)gaps[i].first,
-                                             (int)gaps[i].second, di.sms, st);
+                                             (int)gaps[i].second, di.sms, st); });
         if (e != cudaSuccess) s = cuda_fail(e, "padding fill launch");
         else ++t_launches;
     }
@@ -829,12 +946,13 @@ ra_status ra_ring_sim_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tenso
     P.scale_log2 = P.scale * kLog2e;
     const bool striped = layout == RA_LAYOUT_STRIPED;
     P.rs = striped ? ring_size : 1;
+    P.producer_delay_ns = g_producer_delay_ns;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool tc = di.tc_ok && pb.dtype == RA_BF16 && (pb.D == 64 || pb.D == 128) && aligned16(q) &&
                     aligned16(k) && aligned16(v) && aligned16(dout) && aligned16(dq) &&
                     aligned16(dk) && aligned16(dv);
     ra_status result = RA_OK;
-    cudaError_t e = launch_bwd_rowdot(P, di.sms, st);
+    cudaError_t e = guarded_launch("bwd_rowdot", st, [&] { return launch_bwd_rowdot(P, di.sms, st); });
     if (e != cudaSuccess) result = cuda_fail(e, "backward D launch");
     else ++t_launches;
     std::vector<BSeg> segs, kv_segs;
@@ -852,7 +970,9 @@ ra_status ra_ring_sim_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tenso
                 P.seg[i] = g[i];
                 P.flen = std::max<int32_t>(P.flen, g[i].f1 - g[i].f0);
             }
-            e = launch_attn_bwd_tc(P, kind == 0 ? 1 : 2, di.sms, g_wait_limit_ns, di.err, st, kind == 1);
+            e = guarded_launch(kind == 0 ? "bwd_dq_tc" : "bwd_dkdv_tc", st, [&] {
+                return launch_attn_bwd_tc(P, kind == 0 ? 1 : 2, di.sms, g_wait_limit_ns, di.err, st, kind == 1);
+            });
             if (e != cudaSuccess) result = cuda_fail(e, "backward launch");
             else ++t_launches;
         }
@@ -875,9 +995,12 @@ ra_status ra_ring_sim_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tenso
                 const int parts = kind == 0 ? 1 : 2;
                 // a step's dK/dV launch follows its dQ launch directly, unless the dQ
                 // segments took several launches
-                e = tc ? launch_attn_bwd_tc(P, parts, di.sms, g_wait_limit_ns, di.err, st,
-                                            kind == 1 && f == 0 && dq_launches_this_step == 1)
-                       : launch_attn_bwd_simt(P, parts, st);
+                const bool after_dq = kind == 1 && f == 0 && dq_launches_this_step == 1;
+                e = guarded_launch(tc ? (kind == 0 ? "bwd_dq_tc" : "bwd_dkdv_tc") : (kind == 0 ? "bwd_dq_simt" : "bwd_dkdv_simt"),
+                                   st, [&] {
+                                       return tc ? launch_attn_bwd_tc(P, parts, di.sms, g_wait_limit_ns, di.err, st, after_dq)
+                                                 : launch_attn_bwd_simt(P, parts, st);
+                                   });
                 if (kind == 0) ++dq_launches_this_step;
                 if (e != cudaSuccess) result = cuda_fail(e, "backward launch");
                 else ++t_launches;
@@ -1090,7 +1213,8 @@ ra_status ra_ulysses_all_to_all(const ra_tensor *in, ra_tensor *out, int sp, int
     P.to_heads = to_heads ? 1 : 0;
     const int64_t per16 = 16 / P.esize;
     P.vec = (D % per16 == 0) && aligned16(in) && aligned16(out);
-    cudaError_t e = launch_ulysses(P, di.sms, static_cast<cudaStream_t>(stream));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = guarded_launch("ulysses", st, [&] { return launch_ulysses(P, di.sms, st); });
     if (e != cudaSuccess) return cuda_fail(e, "ulysses launch");
     ++t_launches;
     return RA_OK;
@@ -1135,7 +1259,8 @@ ra_status ra_lse_merge(ra_tensor *o_acc, float *lse_acc, const ra_tensor *o_blk,
     P.half_warp = P.vec && P.D <= 128 &&
                   (!P.blk_bf16 || (reinterpret_cast<uintptr_t>(P.oblk) % 16 == 0 && P.sb[0] % 8 == 0 &&
                                    P.sb[1] % 8 == 0 && P.sb[2] % 8 == 0));
-    cudaError_t e = launch_lse_merge(P, di.sms, static_cast<cudaStream_t>(stream));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = guarded_launch("lse_merge", st, [&] { return launch_lse_merge(P, di.sms, st); });
     if (e != cudaSuccess) return cuda_fail(e, "lse_merge launch");
     ++t_launches;
     return RA_OK;
@@ -1156,12 +1281,62 @@ ra_status ra_check_device_error(void *stream) {
         if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
         if (word == DERR_TIMEOUT)
             return fail(RA_ERR_TIMEOUT, "a device pipeline wait exceeded its time limit");
+        if (word == DERR_BOUNDS)
+            return fail(RA_ERR_BOUNDS, "a device-side bounds check failed (the access was skipped)");
         return fail(RA_ERR_CUDA, "device error word " + std::to_string(word));
     }
     return RA_OK;
 }
 
 void ra_debug_set_wait_limit_ns(int64_t ns) { g_wait_limit_ns = ns < 0 ? 2000000000LL : ns; }
+
+void ra_debug_set_producer_delay_ns(int64_t ns) { g_producer_delay_ns = ns < 0 ? 0 : std::min<int64_t>(ns, 100000000LL); }
+
+void ra_debug_fail_next_launches(int n) { t_inject_launch_failures = n > 0 ? n : 0; }
+
+void ra_debug_time_launches(int enable) { t_time_launches = enable != 0; }
+
+int ra_debug_launch_times(float *ms, int cap, char *names, int name_len) {
+    const int n = (int)t_timed.size();
+    for (int i = 0; i < n; ++i) {
+        TimedLaunch &t = t_timed[i];
+        float v = -1.f;
+        if (cudaEventSynchronize(t.stop) == cudaSuccess && cudaEventElapsedTime(&v, t.start, t.stop) != cudaSuccess)
+            v = -1.f;
+        if (i < cap) {
+            if (ms) ms[i] = v;
+            if (names && name_len > 0) {
+                strncpy(names + (size_t)i * name_len, t.name, (size_t)name_len - 1);
+                names[(size_t)i * name_len + name_len - 1] = 0;
+            }
+        }
+        cudaEventDestroy(t.start);
+        cudaEventDestroy(t.stop);
+    }
+    t_timed.clear();
+    cudaGetLastError();
+    return n;
+}
+
+int ra_debug_bounds_checked(void) {
+#ifdef RA_DEBUG_BOUNDS
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+ra_status ra_debug_bounds_selftest(void *stream) {
+    if (!ra_debug_bounds_checked())
+        return fail(RA_ERR_UNSUPPORTED, "this library was built without device bounds checks");
+    DevInfo di;
+    std::string msg;
+    if (!device_info(di, msg)) return fail(RA_ERR_CUDA, msg);
+    cudaError_t e = launch_bounds_selftest(di.err, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "bounds self-test launch");
+    ++t_launches;
+    return RA_OK;
+}
 
 ra_status ra_debug_wait_selftest(int64_t limit_ns, void *stream) {
     if (limit_ns < 0 || limit_ns > 10000000000LL)
@@ -1192,9 +1367,11 @@ int ra_version(void) { return 100; }
 // Some callers cannot let this library allocate device memory: a framework whose own
 // memory pool owns the device, a latency-critical loop where cudaMalloc/cudaFree would
 // synchronise the device, or a host application that hands a plugin only its input and
-// output buffers.  ra_ring_sim_fwd_noalloc serves them: the float32 running output that
-// ra_ring_sim_fwd keeps in a caller-provided workspace lives instead in the fixed array
-// below, and the call allocates nothing (no cudaMalloc/cudaFree, no host heap on success).
+// output buffers.  ra_ring_sim_fwd_noalloc serves them with the schedule of
+// ra_ring_sim_fwd: the fused ring keeps its running result on chip and needs no scratch;
+// the per-step launches keep the float32 running output, which ra_ring_sim_fwd holds in a
+// caller-provided workspace, in the fixed array below.  The call allocates nothing (no
+// cudaMalloc/cudaFree, no host heap on success).
 //
 // The array is part of this module: every GPU that loads the library holds it until the
 // process exits.  Host code must not pass the array's name to a kernel (in host code it
@@ -1227,80 +1404,6 @@ static bool noalloc_scratch(int dev, float **out, std::string &msg) {
     return true;
 }
 
-// Row ranges of rank r without a container: returns how many (1 or 2).
-static int noalloc_ranges(int64_t N, int R, int layout, int r, Range out[2]) {
-    if (layout == RA_LAYOUT_CONTIG) {
-        const int64_t c = N / R;
-        out[0] = {r * c, (r + 1) * c};
-        return 1;
-    }
-    const int64_t h = N / (2 * (int64_t)R);
-    out[0] = {r * h, (r + 1) * h};
-    out[1] = {(2 * (int64_t)R - 1 - r) * h, (2 * (int64_t)R - r) * h};
-    return 2;
-}
-
-static bool noalloc_touched(int64_t N, int R, int layout, int causal, int step, int r,
-                            int64_t q1) {
-    Range kv[2];
-    const int j = ((r - step) % R + R) % R;
-    const int nk = noalloc_ranges(N, R, layout, j, kv);
-    for (int i = 0; i < nk; ++i) {
-        if (kv[i].b <= kv[i].a) continue;
-        if (causal && kv[i].a > q1 - 1) continue;
-        return true;
-    }
-    return false;
-}
-
-// The same schedule as plan_step (same segments, flags and order) into a fixed array.
-static int noalloc_plan(int64_t N, int R, int layout, int causal, int step, Seg *segs) {
-    int n = 0;
-    for (int r = 0; r < R; ++r) {
-        Range qr[2], kv[2];
-        const int j = ((r - step) % R + R) % R;
-        const int nq = noalloc_ranges(N, R, layout, r, qr);
-        const int nkv = noalloc_ranges(N, R, layout, j, kv);
-        for (int qi = 0; qi < nq; ++qi) {
-            if (qr[qi].b <= qr[qi].a) continue;
-            Seg s;
-            memset(&s, 0, sizeof s);
-            s.q0 = (int32_t)qr[qi].a;
-            s.q1 = (int32_t)qr[qi].b;
-            int nk = 0;
-            for (int ki = 0; ki < nkv; ++ki) {
-                if (kv[ki].b <= kv[ki].a) continue;
-                if (causal && kv[ki].a > qr[qi].b - 1) continue;
-                s.k0[nk] = (int32_t)kv[ki].a;
-                s.k1[nk] = (int32_t)kv[ki].b;
-                ++nk;
-            }
-            if (nk == 0) continue;
-            if (nk == 1) s.k0[1] = s.k1[1] = s.k1[0];
-            s.rank = r;
-            bool earlier = false, later = false;
-            for (int t = 0; t < step && !earlier; ++t)
-                earlier = noalloc_touched(N, R, layout, causal, t, r, s.q1);
-            for (int t = step + 1; t < R && !later; ++t)
-                later = noalloc_touched(N, R, layout, causal, t, r, s.q1);
-            s.flags = (earlier ? 0 : SEG_FIRST) | (later ? 0 : SEG_FINAL);
-            // stable insertion by descending key count (the order plan_step produces)
-            const int64_t c = (int64_t)(s.k1[0] - s.k0[0]) + (s.k1[1] - s.k0[1]);
-            int at = n;
-            while (at > 0) {
-                const Seg &p = segs[at - 1];
-                const int64_t cp = (int64_t)(p.k1[0] - p.k0[0]) + (p.k1[1] - p.k0[1]);
-                if (cp >= c) break;
-                segs[at] = segs[at - 1];
-                --at;
-            }
-            segs[at] = s;
-            ++n;
-        }
-    }
-    return n;
-}
-
 }  // namespace
 
 extern "C" ra_status ra_ring_sim_fwd_noalloc(const ra_tensor *q, const ra_tensor *k,
@@ -1312,45 +1415,31 @@ extern "C" ra_status ra_ring_sim_fwd_noalloc(const ra_tensor *q, const ra_tensor
     if (s) return s;
     if (isnan(scale)) return fail(RA_ERR_INVALID_ARG, "scale is NaN");
     if ((s = check_ring(pb.N, ring_size, layout))) return s;
-    if (ring_size > kNoAllocMaxRing)
-        return fail(RA_ERR_UNSUPPORTED, "ra_ring_sim_fwd_noalloc: ring_size above 64");
-    if (layout == RA_LAYOUT_STRIPED)
-        return fail(RA_ERR_UNSUPPORTED, "ra_ring_sim_fwd_noalloc: contiguous or zigzag layout only");
     if (pb.B * pb.Hq * pb.N == 0) return RA_OK;
-    if (ring_size > 1 && pb.B * pb.Hq * pb.N * pb.D > kNoAllocScratchFloats)
-        return fail(RA_ERR_UNSUPPORTED,
-                    "ra_ring_sim_fwd_noalloc: B*Hq*N*D exceeds its fixed scratch of 8Mi floats "
-                    "(32 MiB); use ra_ring_sim_fwd with a caller-provided workspace");
     DevInfo di;
     std::string msg;
     if (!device_info(di, msg)) return fail(RA_ERR_CUDA, msg);
+    const bool tc = use_tensor_cores(q, k, v, o, pb, di);
+    // the schedule of ra_ring_sim_fwd, in a fixed array: the fused ring (running result on
+    // chip, no scratch) when it applies, else one launch per step over the scratch array
+    Seg segs[kNoAllocMaxSeg];
+    const int nfused = (tc && ring_size > 1) ? fused_ring_segments(pb.N, ring_size, layout, causal, segs) : 0;
     float *scratch = nullptr;
-    if (ring_size > 1 && !noalloc_scratch(di.dev, &scratch, msg)) return fail(RA_ERR_CUDA, msg);
+    if (ring_size > 1 && nfused == 0) {
+        if (ring_size > kNoAllocMaxRing)
+            return fail(RA_ERR_UNSUPPORTED,
+                        "ra_ring_sim_fwd_noalloc: ring_size above 64 outside the fused ring");
+        if (pb.B * pb.Hq * pb.N * pb.D > kNoAllocScratchFloats)
+            return fail(RA_ERR_UNSUPPORTED,
+                        "ra_ring_sim_fwd_noalloc: B*Hq*N*D exceeds its fixed scratch of 8Mi floats "
+                        "(32 MiB); use ra_ring_sim_fwd with a caller-provided workspace");
+        if (!noalloc_scratch(di.dev, &scratch, msg)) return fail(RA_ERR_CUDA, msg);
+    }
     StepParams P;
     fill_common(P, q, k, v, o, lse, pb, causal, scale, di);
     P.oacc = scratch;
-    P.prefer_pairs = ring_size > 1 ? 1 : 0;
-    const bool tc = use_tensor_cores(q, k, v, o, pb, di);
-    const int rows_per_block = tc ? attn_tc_rows_per_block() : 16;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    Seg segs[kNoAllocMaxSeg];
-    for (int step = 0; step < ring_size; ++step) {
-        const int n = noalloc_plan(pb.N, ring_size, layout, causal, step, segs);
-        if (n == 0) continue;
-        int64_t qlen = 0;
-        for (int i = 0; i < n; ++i) {
-            P.seg[i] = segs[i];
-            qlen = std::max<int64_t>(qlen, segs[i].q1 - segs[i].q0);
-        }
-        P.nseg = n;
-        P.rows_per_block = rows_per_block;
-        P.blocks_per_seg = (int32_t)((qlen + rows_per_block - 1) / rows_per_block);
-        const int64_t blocks_y = (int64_t)P.nseg * P.blocks_per_seg;
-        if (blocks_y > 65535) return fail(RA_ERR_UNSUPPORTED, "too many work blocks in one step");
-        cudaError_t e = tc ? launch_attn_tc(P, (int)blocks_y, di.sms, st)
-                           : launch_attn_simt(P, (int)blocks_y, st);
-        if (e != cudaSuccess) return cuda_fail(e, "attention launch (no-alloc)");
-        ++t_launches;
-    }
-    return RA_OK;
+    P.rs = (layout == RA_LAYOUT_STRIPED) ? ring_size : 1;
+    P.prefer_pairs = (ring_size > 1 && layout != RA_LAYOUT_STRIPED) ? 1 : 0;
+    return ring_launches(P, tc, di.sms, pb.N, ring_size, layout, causal, nfused, segs,
+                         static_cast<cudaStream_t>(stream));
 }

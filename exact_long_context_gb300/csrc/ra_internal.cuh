@@ -57,6 +57,7 @@ struct StepParams {
     int32_t rs;              // rank interleave stride of the sequence axis (1 unless striped)
     int32_t o_tma;           // tensor-core kernel: final O rows leave through bulk tensor stores
     int64_t wait_limit_ns;
+    int64_t producer_delay_ns;  // diagnostic: the TMA producer pauses this long before its first copy
     int *err;  // device error word
     Seg seg[kMaxSeg];
 };
@@ -110,6 +111,7 @@ struct BwdParams {
     int32_t nseg;
     int32_t ring_fused;           // one launch walks every ring step (contiguous / zigzag)
     int32_t ring_R, ring_layout;  // fused ring: ring size, RA_LAYOUT_CONTIG (0) or ZIGZAG (1)
+    int64_t producer_delay_ns;    // diagnostic: the TMA producer pauses this long before its first copy
     BSeg seg[kMaxBSeg];
 };
 
@@ -125,10 +127,41 @@ struct UlyssesParams {
 };
 
 // Device error codes (first one wins).
-enum : int { DERR_TIMEOUT = 1 };
+enum : int { DERR_TIMEOUT = 1, DERR_BOUNDS = 2 };
 
 __device__ __forceinline__ void record_error(int *err, int code) {
     if (err) atomicCAS(err, 0, code);
+}
+
+// Bounds check of a tile coordinate or row index before a global-memory access:
+// in_bounds(cond, err).  Debug builds (RA_DEBUG_BOUNDS defined, see build.py) record
+// DERR_BOUNDS in the device error word when cond is false and yield false, and the caller
+// skips the access (a skipped tile load then ends in a bounded wait that times out:
+// nothing traps or hangs).  Release builds yield true without evaluating cond.
+__device__ __forceinline__ bool bounds_check(bool ok, int *err) {
+    if (!ok) record_error(err, DERR_BOUNDS);
+    return ok;
+}
+#ifdef RA_DEBUG_BOUNDS
+#define in_bounds(cond, err) ::ra::bounds_check((cond), (err))
+constexpr bool kDebugBounds = true;
+#else
+#define in_bounds(cond, err) true
+constexpr bool kDebugBounds = false;
+#endif
+
+// Diagnostic pause of a pipeline's producer before its first copy (0: none), so that the
+// consumers' bounded waits run past a short limit and take the timeout path for real.
+__device__ __forceinline__ void producer_delay(int64_t ns) {
+    if (ns <= 0) return;
+    uint64_t t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    for (;;) {
+        uint64_t t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        if ((int64_t)(t - t0) >= ns) return;
+        __nanosleep(1000);
+    }
 }
 
 // Decode a work-block index into (segment, local block).

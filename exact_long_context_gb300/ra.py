@@ -14,9 +14,10 @@ import threading
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libra.so")
+# RA_LIBRARY=debug selects the bounds-checked debug build (build.py --debug-bounds)
+LIB_PATH = os.path.join(_HERE, "libra_debug.so" if os.environ.get("RA_LIBRARY") == "debug" else "libra.so")
 
-RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_TIMEOUT = range(5)
+RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_TIMEOUT, RA_ERR_BOUNDS = range(6)
 RA_F32, RA_BF16 = 0, 1
 LAYOUTS = {"contig": 0, "zigzag": 1, "striped": 2}
 SEG_FIRST, SEG_FINAL = 1, 2
@@ -50,6 +51,8 @@ def lib() -> ctypes.CDLL:
             L.ra_lse_merge.argtypes = [T, P, T, P, P]
             L.ra_ring_sim_workspace_bytes.argtypes = [T, c_int]
             L.ra_ring_sim_workspace_bytes.restype = ctypes.c_size_t
+            L.ra_ring_sim_workspace_bytes_for.argtypes = [T, T, T, T, c_int, c_int, c_int]
+            L.ra_ring_sim_workspace_bytes_for.restype = ctypes.c_size_t
             L.ra_ring_sim_fwd.argtypes = [T, T, T, T, P, c_int, c_int, c_int, c_float, P, P]
             L.ra_attn_varlen_fwd.argtypes = [T, T, T, T, P, P, c_int, c_int, c_float, P]
             L.ra_attn_varlen_fwd.restype = c_int
@@ -74,7 +77,18 @@ def lib() -> ctypes.CDLL:
             L.ra_check_device_error.argtypes = [P]
             L.ra_debug_set_wait_limit_ns.argtypes = [i64]
             L.ra_debug_set_wait_limit_ns.restype = None
+            L.ra_debug_set_producer_delay_ns.argtypes = [i64]
+            L.ra_debug_set_producer_delay_ns.restype = None
             L.ra_debug_wait_selftest.argtypes = [i64, P]
+            L.ra_debug_fail_next_launches.argtypes = [c_int]
+            L.ra_debug_fail_next_launches.restype = None
+            L.ra_debug_bounds_checked.restype = c_int
+            L.ra_debug_time_launches.argtypes = [c_int]
+            L.ra_debug_time_launches.restype = None
+            L.ra_debug_launch_times.argtypes = [P, c_int, P, c_int]
+            L.ra_debug_launch_times.restype = c_int
+            L.ra_debug_bounds_selftest.argtypes = [P]
+            L.ra_debug_bounds_selftest.restype = c_int
             L.ra_last_error.restype = ctypes.c_char_p
             L.ra_launch_count.argtypes = [c_int]
             L.ra_launch_count.restype = i64
@@ -245,15 +259,40 @@ def lse_merge(o_acc, lse_acc, o_blk, lse_blk, stream=None):
     return o_acc, lse_acc
 
 
-def ring_sim_workspace_bytes(q, ring_size: int) -> int:
-    return int(lib().ra_ring_sim_workspace_bytes(ctypes.byref(_desc(q, "q")), int(ring_size)))
+def ring_sim_workspace_bytes(q, ring_size: int, k=None, v=None, o=None, layout=None, causal=False) -> int:
+    """Device workspace bytes ring_sim_fwd needs: with k, v and layout, exactly that call's
+    need (0 for the single pass and the fused tensor-core ring; ``o`` defaults to a tensor
+    laid out like q); with q alone, the upper bound for any call with this q."""
+    if k is None:
+        return int(lib().ra_ring_sim_workspace_bytes(ctypes.byref(_desc(q, "q")), int(ring_size)))
+    d = [_desc(t, n) for t, n in ((q, "q"), (k, "k"), (v if v is not None else k, "v"),
+                                  (o if o is not None else q, "o"))]
+    return int(lib().ra_ring_sim_workspace_bytes_for(*(ctypes.byref(x) for x in d), int(ring_size),
+                                                     LAYOUTS[layout or "contig"], int(bool(causal))))
+
+
+_ws_need: dict = {}  # the exact workspace need of recent argument layouts
+
+
+def _ring_ws_need(q, k, v, o, ring_size, layout, causal) -> int:
+    if ring_size == 1:
+        return 0
+    key = (q.shape, q.stride(), q.dtype, k.shape, k.stride(), v.stride(), o.stride(),
+           q.data_ptr() % 16, k.data_ptr() % 16, v.data_ptr() % 16, o.data_ptr() % 16, ring_size, layout,
+           bool(causal))
+    need = _ws_need.get(key)
+    if need is None:
+        if len(_ws_need) > 256:
+            _ws_need.clear()
+        need = _ws_need[key] = ring_sim_workspace_bytes(q, ring_size, k, v, o, layout, causal)
+    return need
 
 
 def ring_sim_fwd(q, k, v, ring_size: int, layout="contig", causal=False, scale=None, o=None,
                  lse=None, workspace=None, stream=None):
     """Ring attention over ``ring_size`` simulated ranks on one GPU: returns (o, lse)."""
     o, lse = _outputs(q, o, lse)
-    need = ring_sim_workspace_bytes(q, ring_size)
+    need = _ring_ws_need(q, k, v, o, ring_size, layout, causal)
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     if workspace is not None and workspace.numel() < need:
@@ -320,6 +359,36 @@ def check(stream=None):
 
 def set_wait_limit_ns(ns: int):
     lib().ra_debug_set_wait_limit_ns(int(ns))
+
+
+def set_producer_delay_ns(ns: int):
+    """The tensor-core kernels' TMA producers pause ns before their first copy (0: none)."""
+    lib().ra_debug_set_producer_delay_ns(int(ns))
+
+
+def fail_next_launches(n: int):
+    """The calling thread's next n kernel launches fail on the host (RA_ERR_CUDA)."""
+    lib().ra_debug_fail_next_launches(int(n))
+
+
+def time_launches(enable: bool = True):
+    """Time each kernel launch of this thread on its own (two CUDA events per launch)."""
+    lib().ra_debug_time_launches(1 if enable else 0)
+
+
+def launch_times(cap: int = 4096) -> list[tuple[str, float]]:
+    """(kernel name, ms) of the launches timed since the previous read (up to cap)."""
+    L = lib()
+    ms = (ctypes.c_float * cap)()
+    names = ctypes.create_string_buffer(32 * cap)
+    n = L.ra_debug_launch_times(ctypes.cast(ms, ctypes.c_void_p), cap, ctypes.cast(names, ctypes.c_void_p), 32)
+    return [(names.raw[32 * i:32 * i + 32].split(b"\0", 1)[0].decode(), float(ms[i])) for i in range(min(n, cap))]
+
+
+def bounds_selftest(stream=None):
+    """Debug builds: a bounds check that fails on purpose (ra.check() then raises
+    RA_ERR_BOUNDS)."""
+    _check(lib().ra_debug_bounds_selftest(_stream(stream)))
 
 
 def wait_selftest(limit_ns: int, stream=None):

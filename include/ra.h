@@ -42,7 +42,8 @@ typedef enum {
     RA_ERR_INVALID_ARG = 1, /* null pointer, bad shape/stride/dtype/size rule */
     RA_ERR_UNSUPPORTED = 2, /* well-formed but outside what the library implements */
     RA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
-    RA_ERR_TIMEOUT = 4      /* a device-side pipeline wait exceeded its limit */
+    RA_ERR_TIMEOUT = 4,     /* a device-side pipeline wait exceeded its limit */
+    RA_ERR_BOUNDS = 5       /* debug builds only: a device-side bounds check failed */
 } ra_status;
 
 typedef enum { RA_F32 = 0, RA_BF16 = 1 } ra_dtype;
@@ -102,11 +103,25 @@ ra_status ra_lse_merge(ra_tensor *o_acc, float *lse_acc, const ra_tensor *o_blk,
                        const float *lse_blk, void *stream);
 
 /*
- * ra_ring_sim_workspace_bytes - device workspace that ra_ring_sim_fwd needs for the
- * float32 running output: B*Hq*N*D*4 bytes when ring_size > 1, else 0.  Returns 0 on
- * bad arguments.
+ * ra_ring_sim_workspace_bytes - an upper bound, valid for every call with this q, of the
+ * device workspace ra_ring_sim_fwd needs for its float32 running output: B*Hq*N*D*4 bytes
+ * when ring_size > 1, else 0.  Returns 0 on bad arguments.
+ * ra_ring_sim_workspace_bytes_for gives the exact need of one call.
  */
 size_t ra_ring_sim_workspace_bytes(const ra_tensor *q, int ring_size);
+
+/*
+ * ra_ring_sim_workspace_bytes_for - the device workspace ra_ring_sim_fwd needs for exactly
+ * these arguments: 0 when ring_size == 1, and 0 when the call runs the fused ring (bf16,
+ * D in {64, 128}, 16-byte aligned q, k, v, o; a contiguous or zigzag layout of at most
+ * 128 chunks, or the striped layout with at most 128 ranks of whole 128-row tiles), whose
+ * running result stays inside the kernel; otherwise B*Hq*N*D*4 bytes for the float32
+ * running output of the per-step launches.  ra_ring_sim_fwd accepts a NULL workspace
+ * exactly when this is 0.  Returns 0 on bad arguments (the call then reports them; the
+ * message is in ra_last_error()).
+ */
+size_t ra_ring_sim_workspace_bytes_for(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v,
+                                       const ra_tensor *o, int ring_size, ra_layout layout, int causal);
 
 /*
  * ra_ring_sim_fwd - ring attention over ring_size simulated ranks on one GPU.
@@ -137,8 +152,9 @@ size_t ra_ring_sim_workspace_bytes(const ra_tensor *q, int ring_size);
  *   ring_size  >= 1; contig and striped need N % ring_size == 0, zigzag
  *              N % (2 ring_size) == 0
  *   layout     ra_layout
- *   workspace  device buffer of ra_ring_sim_workspace_bytes() bytes (may be NULL when
- *              that is 0); contents on entry are ignored; owned by the caller
+ *   workspace  device buffer of ra_ring_sim_workspace_bytes_for() bytes, 16-byte
+ *              aligned (may be NULL when that is 0: the single pass and the fused ring
+ *              need none); contents on entry are ignored; owned by the caller
  * Errors: as ra_attn_fwd, plus RA_ERR_INVALID_ARG for a bad ring size / layout /
  *   divisibility or a missing workspace.
  */
@@ -306,18 +322,22 @@ int64_t ra_ring_sim_bwd_plan(int64_t N, int ring_size, ra_layout layout, int cau
  * host application that gives a plugin only its input and output buffers.  The pages
  * have no counterpart; this is a property of the library, not of the method.
  *
- * Same arguments, result and errors as ra_ring_sim_fwd, without the workspace: the
- * float32 running output lives in a fixed device array inside the library, 8 Mi floats
- * (32 MiB), which every GPU that loads the library holds until the process exits.
- *   - B*Hq*N*D must be <= 8388608 when ring_size > 1, and ring_size <= 64; larger
- *     problems get RA_ERR_UNSUPPORTED (use ra_ring_sim_fwd with a workspace).
+ * Same arguments, result and errors as ra_ring_sim_fwd, without the workspace, and the
+ * same schedule.  A call that runs the fused ring (ra_ring_sim_workspace_bytes_for() == 0:
+ * bf16, D in {64, 128}, aligned, a layout the fused kernel walks) needs no scratch at all.
+ * Otherwise the float32 running output lives in a fixed device array inside the library,
+ * 8 Mi floats (32 MiB), which every GPU that loads the library holds until the process
+ * exits.
+ *   - Calls that need the array: B*Hq*N*D must be <= 8388608 and ring_size <= 64;
+ *     larger ones get RA_ERR_UNSUPPORTED (use ra_ring_sim_fwd with a workspace).
  *   - The call allocates nothing: no cudaMalloc/cudaFree, no host heap on success.
- *   - The first call on a device looks up the array's device address (once per device,
- *     with that device current); make that first call before any stream capture.
- *   - Every call shares the array and it keeps the last call's contents.  Nothing in
- *     it needs clearing: each row's first partial is written, never merged.  Calls
- *     that overlap on the GPU (different streams, or different host threads) race on
- *     it: serialise them.
+ *   - The first call on a device that needs the array looks up its device address (once
+ *     per device, with that device current); make that first call before any stream
+ *     capture.
+ *   - Every such call shares the array and it keeps the last call's contents.  Nothing in
+ *     it needs clearing: each row's first partial is written, never merged.  Calls that
+ *     overlap on the GPU (different streams, or different host threads) race on it:
+ *     serialise them.
  */
 ra_status ra_ring_sim_fwd_noalloc(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v,
                                   ra_tensor *o, float *lse, int ring_size, ra_layout layout,
@@ -331,11 +351,58 @@ ra_status ra_ring_sim_fwd_noalloc(const ra_tensor *q, const ra_tensor *k, const 
 ra_status ra_check_device_error(void *stream);
 
 /*
- * ra_debug_set_wait_limit_ns - time limit of the kernels' pipeline waits on the
- * current device (default 2e9 ns).  A wait that exceeds it records RA_ERR_TIMEOUT and
- * the kernel winds down cleanly.  Values < 0 restore the default.  Diagnostic hook.
+ * ra_debug_set_wait_limit_ns - time limit of the kernels' pipeline waits (default 2e9 ns).
+ * A wait that exceeds it records RA_ERR_TIMEOUT and the kernel winds down cleanly (its
+ * copies and MMAs in flight complete, tensor memory is released) and returns.  The limit
+ * is read after a few dozen blocking probes of the barrier, each of which the hardware
+ * may suspend for a while, so it bounds long waits, not short ones.  Values < 0 restore
+ * the default.  Diagnostic hook.
+ *
+ * ra_debug_set_producer_delay_ns - the tensor-core kernels' TMA producers pause this long
+ * (at most 0.1 s; default 0) before their first copy.  With a short wait limit the
+ * consumers' waits then run out for real: the timeout path can be tested on any input
+ * without a fault or a hang.  Diagnostic hook.
+ * Both settings are process-wide and apply to the calls made after them.
  */
 void ra_debug_set_wait_limit_ns(int64_t ns);
+void ra_debug_set_producer_delay_ns(int64_t ns);
+
+/*
+ * ra_debug_fail_next_launches - make the calling thread's next n kernel launches fail on
+ * the host, before they reach the GPU: each reports RA_ERR_CUDA with a message that names
+ * this hook, as a real launch failure would.  n <= 0 clears it.  Diagnostic hook, for
+ * testing the callers' error paths without a GPU fault.
+ */
+void ra_debug_fail_next_launches(int n);
+
+/*
+ * ra_debug_time_launches - while enable != 0, each kernel launch of the calling thread is
+ * bracketed by two CUDA events recorded on its stream, so that every kernel of a call is
+ * timed on its own (the events also keep launches that would overlap - a ring step's tail
+ * and the next launch - apart).  For profiling; costs two event records per launch.
+ * ra_debug_launch_times - waits for the timed launches since the previous read, writes
+ * up to `cap` durations in milliseconds (-1 where an event failed) and kernel names (each
+ * NUL-terminated in a slot of name_len bytes; names may be NULL) in launch order, forgets
+ * them, and returns how many there were (which may exceed cap).
+ */
+void ra_debug_time_launches(int enable);
+int ra_debug_launch_times(float *ms, int cap, char *names, int name_len);
+
+/*
+ * Debug builds.  Built with RA_DEBUG_BOUNDS defined (libra_debug.so, build.py
+ * debug_bounds=True), the kernels check every tile coordinate and row index against its
+ * tensor before a global-memory access; a failed check records RA_ERR_BOUNDS in the device
+ * error word (read by ra_check_device_error) and skips the access instead of trapping (a
+ * skipped tile load then ends in a bounded wait that times out).  Release builds compile
+ * the checks away.
+ *
+ * ra_debug_bounds_checked - 1 in a debug build, else 0.
+ * ra_debug_bounds_selftest - launch one block whose bounds check fails on purpose (no
+ *   memory is accessed), so that ra_check_device_error returns RA_ERR_BOUNDS.
+ *   RA_ERR_UNSUPPORTED in release builds.
+ */
+int ra_debug_bounds_checked(void);
+ra_status ra_debug_bounds_selftest(void *stream);
 
 /*
  * ra_debug_wait_selftest - launch one block that waits, bounded by `limit_ns`, on a

@@ -53,7 +53,8 @@ def test_single_process_is_identity():
 
 
 def test_peak_fractions():
-    """A figure equal to a peak reads 100 % of it; the nominal dense bf16 rate is 2250."""
+    """A figure equal to a peak reads 100 % of it; the nominal dense bf16 rates are the
+    datasheet figures halved for 2:4 sparsity: 2250 (HGX B300) and 2500 (GB300 NVL72)."""
     import json
     import sys
     sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
@@ -62,7 +63,8 @@ def test_peak_fractions():
     burst, _, kind = bench.peaks()
     f = bench.peak_fractions(burst)
     assert f[f"of_{kind}_burst"] == 100.0
-    assert f["of_nominal_dense_bf16"] == round(100 * burst / 2250.0, 2)
+    assert f["of_nominal_dense_bf16_hgx_b300"] == round(100 * burst / 2250.0, 2)
+    assert f["of_nominal_dense_bf16_gb300_nvl72"] == round(100 * burst / 2500.0, 2)
     path = os.path.join(bench.ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as fh:

@@ -4,15 +4,16 @@ import pytest
 import torch
 
 from exact_long_context_gb300 import synth
-from helpers import EDGE_SCALE, edge_inputs, to_oracle
+from helpers import EDGE_SCALE, assert_grad_close, edge_inputs, to_oracle
 from oracle import backward as ob
 
 pytestmark = pytest.mark.gpu
 
-# max-abs error / max(1, max |reference|): float32 arithmetic with fp32 inputs, and with
-# bf16 inputs/outputs the rounding of O (inside D = rowsum(dO * O)) and of the stored
-# gradients (2^-9 relative), the same bound as the forward's bf16 output.
-TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
+# Tolerances (helpers.assert_grad_close): max-abs error / max(1, max |reference|) over the
+# tensor and, per row, against the row's own magnitude.  float32 arithmetic with fp32 inputs;
+# with bf16 inputs/outputs the rounding of O (inside D = rowsum(dO * O)), of P and dS before
+# the tensor-core products and of the stored gradients (2^-9 relative), the same bound as
+# the forward's bf16 output.
 
 
 @pytest.fixture(scope="module")
@@ -53,11 +54,8 @@ def test_backward_matches_oracle(ra, case):
     rq, rk, rv, _, _ = ob.attention_bwd(to_oracle(q), to_oracle(k), to_oracle(v), to_oracle(dout),
                                         causal)
     for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
-        got = got.float().cpu().numpy().astype(np.float64)
-        assert np.all(np.isfinite(got)), name
-        err = np.max(np.abs(got - ref)) / max(1.0, np.max(np.abs(ref)))
-        assert err <= TOL[dtype], f"{name}: scaled max-abs error {err:.3e}"
-        print(case, name, f"{err:.2e}")
+        scaled, row, p999 = assert_grad_close(got, ref, dtype, name)
+        print(case, name, f"scaled {scaled:.2e} row {row:.2e} p99.9 {p999:.2e}")
 
 
 def test_backward_tensor_cores_match_cuda_cores(ra):
@@ -114,8 +112,6 @@ def test_backward_edge_cases(ra, kind):
         grads = fn()
         ra.check()
         for name, got, r in zip(("dq", "dk", "dv"), grads, ref):
-            got = got.float().cpu().numpy().astype(np.float64)
-            assert np.all(np.isfinite(got)), (kind, run, name)
-            err = np.max(np.abs(got - r)) / max(1.0, np.max(np.abs(r)))
-            assert err <= TOL[torch.bfloat16], f"{kind} {run} {name}: scaled max-abs error {err:.3e}"
-            print(kind, run, name, f"{err:.2e}")
+            # nearly one-hot or uniform rows: per-row bound off (see helpers.assert_grad_close)
+            scaled, row, p999 = assert_grad_close(got, r, torch.bfloat16, f"{kind} {run} {name}", per_row=False)
+            print(kind, run, name, f"scaled {scaled:.2e} row {row:.2e} p99.9 {p999:.2e}")

@@ -77,7 +77,14 @@ def test_argument_errors_are_reported_without_touching_a_gpu(ra):
     assert _call(ra, _t(S), _t(KV), _t(KV), _t(S), R=3, layout=1) == IA
     assert _call(ra, _t(S), _t(KV), _t(KV), _t(S), R=256, layout=1) == IA  # 256 % 512
     assert _call(ra, _t(S), _t(KV), _t(KV), _t(S), R=4, layout=7) == IA
-    assert _call(ra, _t(S), _t(KV), _t(KV), _t(S), R=4, ws=None) == IA  # workspace missing
+    # workspace missing where the ring keeps a float32 running output: float32 inputs, a
+    # striped rank that is not whole 128-row tiles, more chunks than one fused launch holds
+    f32 = [_t(x, dtype=0) for x in (S, KV, KV, S)]
+    assert _call(ra, *f32, R=4, ws=None) == IA
+    assert _call(ra, _t(S), _t(KV), _t(KV), _t(S), R=4, layout=2, ws=None) == IA
+    long_q, long_kv = (1, 4, 256 * 128, 128), (1, 2, 256 * 128, 128)
+    assert _call(ra, _t(long_q), _t(long_kv), _t(long_kv), _t(long_q), R=128, layout=1, ws=None) == IA
+    assert "workspace" in ra.lib().ra_last_error().decode()
     big = (1, 4, 256, 192)
     assert _call(ra, _t(big), _t((1, 2, 256, 192)), _t((1, 2, 256, 192)), _t(big)) == UN
     assert "D > 128" in ra.lib().ra_last_error().decode()
@@ -92,6 +99,38 @@ def test_workspace_size(ra):
     assert L.ra_ring_sim_workspace_bytes(ctypes.byref(q), 1) == 0
     assert L.ra_ring_sim_workspace_bytes(ctypes.byref(q), 4) == 2 * 8 * 1024 * 128 * 4
     assert L.ra_ring_sim_workspace_bytes(ctypes.byref(q), 0) == 0
+
+
+def _ws_for(ra, q, kv, dtype=1, R=4, layout=0, causal=1, data=0x10000):
+    L = ra.lib()
+    P = ctypes.byref
+    return L.ra_ring_sim_workspace_bytes_for(P(_t(q, dtype, data)), P(_t(kv, dtype)), P(_t(kv, dtype)),
+                                             P(_t(q, dtype)), R, layout, causal)
+
+
+def test_workspace_size_for_the_call(ra):
+    """Zero exactly when the call runs the fused tensor-core ring (bf16, D 64 or 128, 16-byte
+    aligned, contiguous or zigzag with at most 128 chunks, or striped ranks of whole 128-row
+    tiles), whose running result stays in the kernel; the full float32 running output else."""
+    full = lambda q: q[0] * q[1] * q[2] * q[3] * 4  # noqa: E731
+    q, kv = (1, 8, 32768, 128), (1, 2, 32768, 128)
+    for layout in (0, 1, 2):
+        for causal in (0, 1):
+            assert _ws_for(ra, q, kv, layout=layout, causal=causal) == 0
+    assert _ws_for(ra, q, kv, R=64, layout=1) == 0  # 128 chunks: one launch
+    assert _ws_for(ra, q, kv, R=128, layout=1) == full(q)  # 256 chunks: per-step launches
+    assert _ws_for(ra, q, kv, R=128, layout=0) == 0  # 128 contiguous chunks
+    assert _ws_for(ra, q, kv, R=1) == 0  # the single pass
+    q64, kv64 = (1, 8, 4096, 64), (1, 8, 4096, 64)
+    assert _ws_for(ra, q64, kv64, R=8, layout=1) == 0
+    assert _ws_for(ra, q64, kv64, R=8, layout=1, dtype=0) == full(q64)  # float32: CUDA cores
+    q96, kv96 = (1, 8, 4096, 96), (1, 8, 4096, 96)
+    assert _ws_for(ra, q96, kv96, R=8, layout=1) == full(q96)  # D = 96: CUDA cores
+    assert _ws_for(ra, q, kv, R=8, layout=1, data=0x10008) == full(q)  # base not 16-byte aligned
+    qs, kvs = (1, 8, 8 * 192, 128), (1, 8, 8 * 192, 128)
+    assert _ws_for(ra, qs, kvs, R=8, layout=2) == full(qs)  # striped ranks of 192 rows
+    assert _ws_for(ra, qs, kvs, R=8, layout=1) == 0
+    assert _ws_for(ra, q, kv, R=3, layout=1) == 0 and "ring" in ra.lib().ra_last_error().decode()
 
 
 def test_merge_argument_errors(ra):
