@@ -424,6 +424,52 @@ def run_hbm_pass(args, w, ws, rank, local):
             "bytes_per_step": nbytes}
 
 
+def run_hostlink(args, ws, rank, local):
+    """Pinned host <-> device copy rates (one cudaMemcpyAsync per copy, through torch's
+    non-blocking copy_) at 8 MiB .. 1 GiB, each direction alone and both at once on two
+    streams: the bound of the end-to-end figure, whose step copies q, k, v in and o, lse out."""
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    out = {}
+    for mib in (8, 32, 128, 512, 1024):
+        n = mib << 20
+        h_in = torch.empty(n, dtype=torch.uint8).pin_memory()
+        h_out = torch.empty(n, dtype=torch.uint8).pin_memory()
+        d_a = torch.empty(n, dtype=torch.uint8, device=dev)
+        d_b = torch.empty(n, dtype=torch.uint8, device=dev)
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        reps = max(3, min(20, (2048 // mib)))
+
+        def timed(fn):
+            for _ in range(2):
+                fn()
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            for _ in range(reps):
+                fn()
+            torch.cuda.synchronize(dev)
+            return (time.perf_counter() - t0) / reps
+
+        def h2d():
+            with torch.cuda.stream(s_in):
+                d_a.copy_(h_in, non_blocking=True)
+
+        def d2h():
+            with torch.cuda.stream(s_out):
+                h_out.copy_(d_b, non_blocking=True)
+
+        def both():
+            h2d()
+            d2h()
+
+        t_in, t_out, t_both = timed(h2d), timed(d2h), timed(both)
+        out[f"{mib}MiB"] = {"h2d_gbs": round(n / t_in / 1e9, 1), "d2h_gbs": round(n / t_out / 1e9, 1),
+                            "both_gbs_each": round(n / t_both / 1e9, 1)}
+        del h_in, h_out, d_a, d_b
+    return {"value": max(v["h2d_gbs"] for v in out.values()), "unit": "GB/s", "sizes": out,
+            "how": "wall time of reps back-to-back cudaMemcpyAsync copies of pinned memory per size"}
+
+
 def host_cpu_desc():
     """The host CPU the oracle runs on: machine, model (or Arm part number) and the cores
     this process may use."""
@@ -536,9 +582,10 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
-    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "merge", "ulysses"], default="fwd",
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "merge", "ulysses", "hostlink"], default="fwd",
                     help="fwd (default): the hot path; bwd: its backward (ring schedule when ring_size > 1); "
-                         "merge / ulysses: the HBM-bound LSE merge / Ulysses exchange")
+                         "merge / ulysses: the HBM-bound LSE merge / Ulysses exchange; hostlink: pinned "
+                         "host <-> device copy rates (the end-to-end figure's bound)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -555,7 +602,8 @@ def main():
               "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{ws}"}
     metric = {"fwd": METRIC, "bwd": METRIC.replace("attention fwd", "attention bwd"),
               "merge": "lse_merge GB/s (algorithmic bytes) and % of measured HBM bandwidth",
-              "ulysses": "Ulysses all-to-all GB/s and % of measured HBM bandwidth"}[args.pass_]
+              "ulysses": "Ulysses all-to-all GB/s and % of measured HBM bandwidth",
+              "hostlink": "pinned host<->device copy GB/s"}[args.pass_]
     line = {"metric": metric, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
@@ -572,6 +620,12 @@ def main():
         print(json.dumps(line), flush=True)
         return
 
+    if args.pass_ == "hostlink":
+        if rank == 0:
+            line.update(run_hostlink(args, ws, rank, local))
+            line["config"] = {"workload": "pinned copies 8 MiB .. 1 GiB"}
+            print(json.dumps(line), flush=True)
+        return
     if args.pass_ in ("merge", "ulysses"):
         res = run_hbm_pass(args, w, ws, rank, local)
         if rank == 0:

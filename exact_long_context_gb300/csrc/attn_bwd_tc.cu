@@ -448,15 +448,6 @@ __device__ __forceinline__ bool ring_get(BBars *bars, uint32_t &cnt, R &r, bool 
     return true;
 }
 
-// 32 consecutive 32-bit columns of this thread's lane: 16 bf16 pairs.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-        : "memory");
-}
 
 // Producer: per item the fixed pair (fa, fb) at index f_row of rank f_rank of (fh, b), then
 // `n` streamed pairs (sa, sb) at the index and head coords(t) gives, of rank s_rank.
@@ -649,8 +640,7 @@ __device__ __forceinline__ void dq_tile_ew(uint32_t (&sv)[64], uint32_t tD, int 
     for (int cc = 0; cc < 2; ++cc) {
         const int c = cc == 0 ? FIRST : 1 - FIRST;
         uint32_t dp[32];
-        tmem_ld32(tD + grp * 64 + c * 32, dp);
-        tmem_ld_wait();
+        tmem_ld32_wait(tD + grp * 64 + c * 32, dp);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2)
@@ -833,9 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t tS = tmem + s_slot(g) + lane_off, tD = tmem + d_slot(g) + lane_off;
                 uint32_t sv[64];
-                tmem_ld32(tS + grp * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-                tmem_ld32(tS + grp * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-                tmem_ld_wait();
+                tmem_ld64_wait(tS + grp * 64, sv);
                 // S is in registers: its slot may take the next tile's dP
                 tc_fence_before();
                 __syncwarp();
@@ -876,8 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = grp * (HD / 64); c < (grp + 1) * (HD / 64); ++c) {  // this group's columns
                 uint32_t o[32];
                 if (n > 0) {
-                    tmem_ld32(tmem + C::TM_DQ + lane_off + c * 32, o);
-                    tmem_ld_wait();
+                    tmem_ld32_wait(tmem + C::TM_DQ + lane_off + c * 32, o);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = 0u;
@@ -918,8 +905,7 @@ __device__ __forceinline__ void ds_tile_ew(const uint32_t (&pv)[64], uint32_t tD
     for (int cc = 0; cc < 2; ++cc) {
         const int c = cc == 0 ? FIRST : 1 - FIRST;
         uint32_t dp[32];
-        tmem_ld32(tD + grp * 64 + c * 32, dp);
-        tmem_ld_wait();
+        tmem_ld32_wait(tD + grp * 64 + c * 32, dp);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2)
@@ -1152,9 +1138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 uint32_t pv[64];
-                tmem_ld32(tmem + lane_off + grp * 64, *reinterpret_cast<uint32_t(*)[32]>(&pv[0]));
-                tmem_ld32(tmem + lane_off + grp * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&pv[32]));
-                tmem_ld_wait();
+                tmem_ld64_wait(tmem + lane_off + grp * 64, pv);
                 if ((qa + 64 > qlim) || (P.causal && it.c_hi - 1 + diag > qa)) {
                     const int lo = P.causal ? key + diag - qa : 0;  // first visible column
                     const int hi = qlim - qa;
@@ -1210,8 +1194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = grp * (HD / 64); c < (grp + 1) * (HD / 64); ++c) {  // this group's columns
                     uint32_t o[32];
                     if (n > 0) {
-                        tmem_ld32(tmem + col + lane_off + c * 32, o);
-                        tmem_ld_wait();
+                        tmem_ld32_wait(tmem + col + lane_off + c * 32, o);
                     } else {
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] = 0u;

@@ -866,7 +866,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(tS + 32, r[1]);
                 tmem_ld32(tS + 64, r[2]);
                 tmem_ld32(tS + 96, r[3]);
-                tmem_ld_wait();
+                tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[128]>(&r[0][0]));
                 const bool need_mask =
                     (ks + BN > ke) || (P.causal && (min(ks + BN, ke) - 1 + dg > first_row));
                 if (need_mask) {
@@ -939,7 +939,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < HD / 32; ++c) {
                         uint32_t o[32];
                         tmem_ld32(tO + c * 32, o);
-                        tmem_ld_wait();
+                        tmem_ld_wait_regs(o);
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
                             o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
@@ -1005,7 +1005,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 32; ++i) x[i] = 0.f;
                     }
-                    tmem_ld_wait();
+                    tmem_ld_wait_regs(o);
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
@@ -1061,7 +1061,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) x[i] = 0.f;
                 }
-                tmem_ld_wait();
+                tmem_ld_wait_regs(o);
                 if (!valid) continue;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) x[i] = fmaf(wb, __uint_as_float(o[i]), x[i]);

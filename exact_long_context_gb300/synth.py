@@ -56,6 +56,11 @@ WORKLOADS = {
                                               128, torch.bfloat16, True, 16, "zigzag", 4),
     "ring64_zigzag_h8kv2n1m": Workload("ring64_zigzag_h8kv2n1m", 1, 8, 2, 1048576, 128,
                                        torch.bfloat16, True, 64, "zigzag", 5),
+    # head size 64 (the other tensor-core head size): the dense and ring shapes at D = 64
+    "dense_causal_b2h32n4k_d64": Workload("dense_causal_b2h32n4k_d64", 2, 32, 32, 4096, 64,
+                                          torch.bfloat16, True, 1, "contig", 6),
+    "ring8_zigzag_h16n32k_d64": Workload("ring8_zigzag_h16n32k_d64", 1, 16, 16, 32768, 64,
+                                         torch.bfloat16, True, 8, "zigzag", 7),
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 

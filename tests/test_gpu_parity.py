@@ -294,6 +294,19 @@ def test_workload_ring8_zigzag(ra):
         assert ((la - lse).abs() / lse.abs().clamp(min=1)).max().item() <= 1e-3, name
 
 
+@pytest.mark.parametrize("name", ["dense_causal_b2h32n4k_d64", "ring8_zigzag_h16n32k_d64"])
+def test_workload_head_size_64(ra, name):
+    """The dense and ring shapes at head size 64 (bench workloads): sampled rows against the
+    oracle, and the ring against the single pass."""
+    q, k, v, o, lse = _workload_case(ra, name, n_random=16, heads=[(0, 0), (0, 5), (0, 15)])
+    w = synth.WORKLOADS[name]
+    if w.ring_size > 1:
+        o1, l1 = ra.attn_fwd(q, k, v, causal=True, scale=w.scale)
+        ra.check()
+        assert (o1.float() - o.float()).abs().max().item() <= 2e-2
+        assert ((l1 - lse).abs() / lse.abs().clamp(min=1)).max().item() <= 1e-3
+
+
 def test_workload_gqa_ring16(ra):
     _workload_case(ra, "gqa_ring16_zigzag_h32kv8n128k", n_random=8)
 
