@@ -318,10 +318,11 @@ __device__ __forceinline__ void cursor_next(const StepParams &P, const Item &it,
     cursor_seek(P, it, c);
 }
 
-// Item L of a launch: L = w * (B*Hq) + bh, so the heaviest work blocks of every head
-// come first.  A persistent CTA takes one item per round of gridDim.x items, in snake
-// order (forward in even rounds, backward in odd ones) so that the heavy and light
-// ends of the cost-sorted list even out across CTAs.
+// Item L of a launch.  With a work counter (P.sched) each CTA's producer takes the next
+// item number when it needs one, so any order balances over the persistent grid.
+// Otherwise a CTA takes one item per round of gridDim.x items, in snake order (forward in
+// even rounds, backward in odd ones), so that the heavy and light ends of the cost-sorted
+// list even out across CTAs.
 __device__ __forceinline__ int snake_item(int k) {
     const int G = gridDim.x;
     return k * G + ((k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
@@ -341,8 +342,21 @@ __device__ __forceinline__ bool decode_item(const StepParams &P, int L, int sub,
     int si, lb, bh;
     if (!P.pair_items) {
         if (sub) return false;
-        const int w = L / BH;
-        bh = L - w * BH;
+        // single blocks: block rank w (heaviest first) outside, heads inside; with head groups,
+        // the heads of one group of P.head_group consecutive (batch, head) units go first, so
+        // the CTAs that run together read the K/V of those heads only (they stay in L2)
+        int w;
+        if (P.head_group > 0 && P.head_group < BH) {
+            const int per_group = P.head_group * P.blocks_y;
+            const int g = L / per_group;
+            const int r = L - g * per_group;
+            const int gsize = min(P.head_group, BH - g * P.head_group);
+            w = r / gsize;
+            bh = g * P.head_group + (r - w * gsize);
+        } else {
+            w = L / BH;
+            bh = L - w * BH;
+        }
         if (P.ring_fused) {
             // fused ring: a block's cost is mostly its chunk's later steps, so items go
             // chunk by chunk (heaviest first, as the host orders them), last block first
@@ -490,7 +504,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int total = P.total_items;
-    if ((int)blockIdx.x >= total) return;
+    if ((int)blockIdx.x >= total) {
+        if (P.sched && threadIdx.x == 0) sched_finish(P.sched);
+        return;
+    }
 
     const uint32_t b_drain = smem_u32(&bars->drain);
     volatile int32_t *abort_flag = &bars->abort;
@@ -556,9 +573,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             bool ok = true;
-            for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, part)
-                const int L = snake_item(k2 >> 1);
-                if (L >= total) continue;
+            int L = 0;
+            for (int k2 = 0; ok; ++k2) {  // (item, part)
+                if (P.sched) {
+                    if (!(k2 & 1)) L = atomicAdd(&P.sched[0], 1);
+                    if (L >= total) break;
+                } else {
+                    if ((k2 >> 1) * (int)gridDim.x >= total) break;
+                    L = snake_item(k2 >> 1);
+                    if (L >= total) continue;
+                }
                 Item it;
                 if (!decode_item(P, L, k2 & 1, it)) continue;
                 if (it.nmax == 0) continue;
@@ -1092,6 +1116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
+    if (P.sched && threadIdx.x == 0) sched_finish(P.sched);
 }
 
 // One block, one thread: a bounded wait on a barrier nothing completes.
@@ -1164,6 +1189,7 @@ static cudaError_t launch_tc_hd(const StepParams &P, int blocks_y, int num_sms,
     StepParams Q = P;
     Q.total_items = (int32_t)total;
     Q.pair_items = use_pairs ? 1 : 0;
+    Q.blocks_y = blocks_y;
     Q.o_tma = o_map ? 1 : 0;
     const int grid = (int)std::min<int64_t>(total, (int64_t)num_sms);
     cudaLaunchConfig_t cfg;

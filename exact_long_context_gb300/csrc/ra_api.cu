@@ -93,10 +93,18 @@ static ra_status cuda_fail(cudaError_t e, const char *what) {
 
 __device__ int g_device_error;
 
+// Work counter pairs of the tensor-core forward launches (next item, CTAs finished), used in
+// rotation: a launch takes the next pair, and its last CTA zeroes the pair again; a pair is
+// reused only kSchedSlots launches later, after that launch has long finished.
+constexpr int kSchedSlots = 1024;
+__device__ int g_sched[2 * kSchedSlots];
+
 static const int kMaxDev = 64;
 static const int kHostGroups = 8;  // head groups of the host-buffer pipeline
 static std::mutex g_mu;
 static int *g_err_ptr[kMaxDev];
+static int *g_sched_ptr[kMaxDev];
+static uint32_t g_sched_seq[kMaxDev];
 static int g_num_sms[kMaxDev];
 static int64_t g_wait_limit_ns = 2000000000LL;
 static int64_t g_producer_delay_ns = 0;
@@ -107,6 +115,13 @@ struct DevInfo {
     int sms;
     bool tc_ok;
 };
+
+// The work counter pair of the next tensor-core forward launch on `dev`.
+static int *next_sched(int dev) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_sched_ptr[dev]) return nullptr;
+    return g_sched_ptr[dev] + 2 * (g_sched_seq[dev]++ % kSchedSlots);
+}
 
 static bool device_info(DevInfo &d, std::string &msg) {
     if (cudaGetDevice(&d.dev) != cudaSuccess || d.dev < 0 || d.dev >= kMaxDev) {
@@ -122,6 +137,13 @@ static bool device_info(DevInfo &d, std::string &msg) {
             msg = std::string("cudaGetSymbolAddress(error word): ") + cudaGetErrorString(e);
             return false;
         }
+        void *ps = nullptr;
+        e = cudaGetSymbolAddress(&ps, g_sched);
+        if (e != cudaSuccess) {
+            msg = std::string("cudaGetSymbolAddress(work counters): ") + cudaGetErrorString(e);
+            return false;
+        }
+        g_sched_ptr[d.dev] = static_cast<int *>(ps);
         int sms = 0;
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d.dev);
         g_num_sms[d.dev] = sms > 0 ? sms : 1;
@@ -567,6 +589,21 @@ static bool fused_bwd_segments(int64_t N, int R, int layout, int causal, int kin
 
 // ---------------------------------------------------------------- dispatch
 
+// Query heads per group of consecutive single-block work items: a group's K and V (4 N D
+// bytes per KV head in bf16) within kGroupKvBytes, so that they stay in the 129 MB L2 while
+// the group's items run on the persistent grid; whole KV heads (G query heads) at least.
+// 0 (no grouping) when every head fits at once.
+constexpr double kGroupKvBytes = 48.0 * (1 << 20);
+static int32_t head_group(const Problem &pb) {
+    const int64_t G = pb.Hkv > 0 ? pb.Hq / pb.Hkv : 1;
+    const double per_kv = 4.0 * (double)pb.N * (double)pb.D;
+    const int64_t units = pb.B * pb.Hkv;  // (batch, KV head) units
+    int64_t kv = (int64_t)(kGroupKvBytes / std::max(per_kv, 1.0));
+    kv = std::max<int64_t>(kv, 1);
+    if (kv >= units) return 0;
+    return (int32_t)std::min<int64_t>(kv * G, 1 << 30);
+}
+
 static void fill_common(StepParams &P, const ra_tensor *q, const ra_tensor *k, const ra_tensor *v,
                         const ra_tensor *o, float *lse, const Problem &pb, int causal,
                         float scale, const DevInfo &di) {
@@ -593,6 +630,7 @@ static void fill_common(StepParams &P, const ra_tensor *q, const ra_tensor *k, c
     P.scale_log2 = sc * kLog2e;
     P.wait_limit_ns = g_wait_limit_ns;
     P.producer_delay_ns = g_producer_delay_ns;
+    P.head_group = head_group(pb);
     P.err = di.err;
     P.rs = 1;
 }
@@ -612,7 +650,7 @@ static bool use_tensor_cores(const ra_tensor *q, const ra_tensor *k, const ra_te
 
 // Launch the segments of one step (split into launches of <= kMaxSeg segments; all
 // segments of a step have equal query length).
-static ra_status run_step(StepParams &P, const Seg *segs, int nsegs, bool tc, int num_sms,
+static ra_status run_step(StepParams &P, const Seg *segs, int nsegs, bool tc, int num_sms, int dev,
                           cudaStream_t stream) {
     const int rows_per_block = tc ? attn_tc_rows_per_block() : 16;
     for (int first = 0; first < nsegs; first += kMaxSeg) {
@@ -627,6 +665,7 @@ static ra_status run_step(StepParams &P, const Seg *segs, int nsegs, bool tc, in
         P.blocks_per_seg = (int32_t)((qlen + rows_per_block - 1) / rows_per_block);
         const int64_t blocks_y = (int64_t)P.nseg * P.blocks_per_seg;
         if (blocks_y > 65535) return fail(RA_ERR_UNSUPPORTED, "too many work blocks in one step");
+        P.sched = tc ? next_sched(dev) : nullptr;
         cudaError_t e = guarded_launch(tc ? "attn_tc" : "attn_simt", stream, [&] {
             return tc ? launch_attn_tc(P, (int)blocks_y, num_sms, stream) : launch_attn_simt(P, (int)blocks_y, stream);
         });
@@ -643,20 +682,20 @@ static ra_status run_step(StepParams &P, const Seg *segs, int nsegs, bool tc, in
 // launch per step merges into the float32 running output P.oacc (set by the caller when
 // ring_size > 1); segs must hold 2 * ring_size segments.  P.rs, P.prefer_pairs and the
 // common fields are the caller's.
-static ra_status ring_launches(StepParams &P, bool tc, int num_sms, int64_t N, int R, int layout, int causal,
-                               int nfused, Seg *segs, cudaStream_t st) {
+static ra_status ring_launches(StepParams &P, bool tc, int num_sms, int dev, int64_t N, int R, int layout,
+                               int causal, int nfused, Seg *segs, cudaStream_t st) {
     if (nfused > 0) {
         P.oacc = nullptr;
         P.ring_fused = 1;
         P.ring_R = R;
         P.ring_layout = layout == RA_LAYOUT_ZIGZAG ? 1 : (layout == RA_LAYOUT_STRIPED ? 2 : 0);
         P.prefer_pairs = 0;
-        return run_step(P, segs, nfused, tc, num_sms, st);
+        return run_step(P, segs, nfused, tc, num_sms, dev, st);
     }
     for (int step = 0; step < R; ++step) {
         const int n = plan_step(N, R, layout, causal, step, segs);
         if (n == 0) continue;
-        ra_status s = run_step(P, segs, n, tc, num_sms, st);
+        ra_status s = run_step(P, segs, n, tc, num_sms, dev, st);
         if (s) return s;
     }
     return RA_OK;
@@ -718,7 +757,7 @@ ra_status ra_ring_sim_fwd(const ra_tensor *q, const ra_tensor *k, const ra_tenso
     // per-step ring launches overlap their tails with the next step's launch, so they
     // take tile-pair items; striped rings measured better with single blocks
     P->prefer_pairs = (ring_size > 1 && layout != RA_LAYOUT_STRIPED) ? 1 : 0;
-    s = ring_launches(*P, tc, di.sms, pb.N, ring_size, layout, causal, nfused, segs.data(),
+    s = ring_launches(*P, tc, di.sms, di.dev, pb.N, ring_size, layout, causal, nfused, segs.data(),
                       static_cast<cudaStream_t>(stream));
     delete P;
     return s;
@@ -824,6 +863,7 @@ ra_status ra_attn_varlen_fwd(const ra_tensor *q, const ra_tensor *k, const ra_te
             s = fail(RA_ERR_UNSUPPORTED, "too many work blocks in one launch");
             break;
         }
+        P->sched = tc ? next_sched(di.dev) : nullptr;
         cudaError_t e = guarded_launch(tc ? "attn_tc" : "attn_simt", st, [&] {
             return tc ? launch_attn_tc(*P, (int)blocks, di.sms, st) : launch_attn_simt(*P, (int)blocks, st);
         });
@@ -1350,6 +1390,19 @@ ra_status ra_debug_wait_selftest(int64_t limit_ns, void *stream) {
     return RA_OK;
 }
 
+int ra_debug_work_counters_in_use(void *stream) {
+    DevInfo di;
+    std::string msg;
+    if (!device_info(di, msg)) return -1;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return -1;
+    static int host[2 * kSchedSlots];
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (cudaMemcpyFromSymbol(host, g_sched, sizeof(host)) != cudaSuccess) return -1;
+    int n = 0;
+    for (int i = 0; i < kSchedSlots; ++i) n += (host[2 * i] != 0 || host[2 * i + 1] != 0);
+    return n;
+}
+
 const char *ra_last_error(void) { return t_last_error.c_str(); }
 
 int64_t ra_launch_count(int reset) {
@@ -1440,6 +1493,6 @@ extern "C" ra_status ra_ring_sim_fwd_noalloc(const ra_tensor *q, const ra_tensor
     P.oacc = scratch;
     P.rs = (layout == RA_LAYOUT_STRIPED) ? ring_size : 1;
     P.prefer_pairs = (ring_size > 1 && layout != RA_LAYOUT_STRIPED) ? 1 : 0;
-    return ring_launches(P, tc, di.sms, pb.N, ring_size, layout, causal, nfused, segs,
+    return ring_launches(P, tc, di.sms, di.dev, pb.N, ring_size, layout, causal, nfused, segs,
                          static_cast<cudaStream_t>(stream));
 }

@@ -59,6 +59,11 @@ struct StepParams {
     int64_t wait_limit_ns;
     int64_t producer_delay_ns;  // diagnostic: the TMA producer pauses this long before its first copy
     int *err;  // device error word
+    // tensor-core kernel: this launch's work counter pair (next item, CTAs finished), zero on
+    // entry and reset to zero by the last CTA; NULL: a static assignment of items to CTAs
+    int *sched;
+    int32_t blocks_y;    // work blocks per head (set at launch)
+    int32_t head_group;  // single-block items: query heads per group of consecutive items (0: all)
     Seg seg[kMaxSeg];
 };
 
@@ -149,6 +154,17 @@ constexpr bool kDebugBounds = true;
 #define in_bounds(cond, err) true
 constexpr bool kDebugBounds = false;
 #endif
+
+// End of a CTA of a launch with a work counter pair: the last CTA to finish zeroes the pair
+// for the launch that next uses it (every CTA has taken its last item number by then).
+__device__ __forceinline__ void sched_finish(int *sched) {
+    __threadfence();
+    if (atomicAdd(&sched[1], 1) == (int)(gridDim.x * gridDim.y * gridDim.z) - 1) {
+        atomicExch(&sched[0], 0);
+        atomicExch(&sched[1], 0);
+        __threadfence();
+    }
+}
 
 // Diagnostic pause of a pipeline's producer before its first copy (0: none), so that the
 // consumers' bounded waits run past a short limit and take the timeout path for real.

@@ -89,6 +89,8 @@ def lib() -> ctypes.CDLL:
             L.ra_debug_launch_times.restype = c_int
             L.ra_debug_bounds_selftest.argtypes = [P]
             L.ra_debug_bounds_selftest.restype = c_int
+            L.ra_debug_work_counters_in_use.argtypes = [P]
+            L.ra_debug_work_counters_in_use.restype = c_int
             L.ra_last_error.restype = ctypes.c_char_p
             L.ra_launch_count.argtypes = [c_int]
             L.ra_launch_count.restype = i64
@@ -389,6 +391,12 @@ def bounds_selftest(stream=None):
     """Debug builds: a bounds check that fails on purpose (ra.check() then raises
     RA_ERR_BOUNDS)."""
     _check(lib().ra_debug_bounds_selftest(_stream(stream)))
+
+
+def work_counters_in_use(stream=None) -> int:
+    """Synchronise the stream, then count the forward kernels' work-counter pairs that are
+    not zero (0 whenever no launch is in flight; -1 on a CUDA failure)."""
+    return int(lib().ra_debug_work_counters_in_use(_stream(stream)))
 
 
 def wait_selftest(limit_ns: int, stream=None):

@@ -389,6 +389,15 @@ void ra_debug_time_launches(int enable);
 int ra_debug_launch_times(float *ms, int cap, char *names, int name_len);
 
 /*
+ * ra_debug_work_counters_in_use - synchronise `stream`, then count the work-counter pairs
+ * of the current device that are not zero.  Each tensor-core forward launch takes its work
+ * items from one of 1024 counter pairs (in rotation) and its last block to finish zeroes
+ * the pair again, also when the launch ends early on a wait timeout; so with no launch in
+ * flight on the device this is 0.  -1 if the device or the copy fails.  Diagnostic hook.
+ */
+int ra_debug_work_counters_in_use(void *stream);
+
+/*
  * Debug builds.  Built with RA_DEBUG_BOUNDS defined (libra_debug.so, build.py
  * debug_bounds=True), the kernels check every tile coordinate and row index against its
  * tensor before a global-memory access; a failed check records RA_ERR_BOUNDS in the device

@@ -64,6 +64,7 @@ def test_injected_launch_failure_is_reported_and_the_next_call_runs(ra):
         assert "injected" in str(ei.value), (name, str(ei.value))
         assert _status(ra) == ra.RA_OK, name  # nothing reached the GPU
     ra.fail_next_launches(0)
+    assert ra.work_counters_in_use() == 0
     o2, lse2 = ra.attn_fwd(q, k, v, causal=True)
     ra.check()
     ro, rl = oracle_full(q, k, v, True)
@@ -108,6 +109,8 @@ def test_kernel_waits_time_out_cleanly_and_the_context_survives(ra):
             for a, b in zip(out, want[name]):
                 assert torch.equal(a, b), name
     assert timeouts, "no wait ran out behind a paused producer"
+    # launches that ended on a timeout still released their work counters
+    assert ra.work_counters_in_use() == 0
     # the context is usable and the default limit is back
     o, lse = ra.attn_fwd(q, k, v, causal=True)
     assert _status(ra) == ra.RA_OK

@@ -317,6 +317,44 @@ def test_workload_ring64_million(ra):
     _workload_case(ra, "ring64_zigzag_h8kv2n1m", n_random=4, heads=heads)
 
 
+WORK_ORDER_CASES = {
+    # (B, Hq, Hkv, N, D, ring_size, layout): heads per group of consecutive work items
+    # (K/V of a group within 48 MiB) and the groups' shapes
+    "dense b2h32n4k: groups of 24, 24, 16 heads": (2, 32, 32, 4096, 128, 1, "contig"),
+    "gqa b2 hq8 hkv4 n16k: groups of 12 and 4, across the batch": (2, 8, 4, 16384, 128, 1, "contig"),
+    "fused ring8 zigzag h8n32k: groups of 3, 3, 2": (1, 8, 8, 32768, 128, 8, "zigzag"),
+    "fused ring8 zigzag h16n32k d64: groups of 6, 6, 4": (1, 16, 16, 32768, 64, 8, "zigzag"),
+    "fused ring4 striped h8n32k: groups of 3, 3, 2": (1, 8, 8, 32768, 128, 4, "striped"),
+    # 160 zigzag chunks are more than one launch takes: one launch per step, tile-pair items
+    "per-step ring80 zigzag h8n20k: tile pairs": (1, 8, 8, 20480, 128, 80, "zigzag"),
+    # 10920-row ranks are not whole tiles: per-step launches of single blocks
+    "per-step ring3 striped h8n32760: single blocks": (1, 8, 8, 32760, 128, 3, "striped"),
+}
+
+
+@pytest.mark.parametrize("name", list(WORK_ORDER_CASES))
+def test_every_work_item_runs_once(ra, name):
+    """O and the LSE start as NaN; every row must be written (each work item taken exactly
+    once from the launch's work counter, in head groups), sampled rows match the oracle, and
+    every counter pair is back to zero after the launch."""
+    B, Hq, Hkv, N, D, R, layout = WORK_ORDER_CASES[name]
+    q, k, v = synth.make_qkv(B, Hq, Hkv, N, D, torch.bfloat16, seed=41, device="cuda")
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full(q.shape[:3], float("nan"), device="cuda")
+    if R > 1:
+        ra.ring_sim_fwd(q, k, v, R, layout, causal=True, o=o, lse=lse)
+    else:
+        ra.attn_fwd(q, k, v, causal=True, o=o, lse=lse)
+    ra.check()
+    assert ra.work_counters_in_use() == 0
+    assert not torch.isnan(o).any().item() and not torch.isnan(lse).any().item()
+    chunk = N // (2 * R) if layout == "zigzag" else N // R
+    rows = sample_rows(B, Hq, N, chunk=chunk, n_random=2, seed=41, heads=[(0, 0), (B - 1, Hq - 1)])
+    o_ref, l_ref = oracle.attention(to_oracle(q), to_oracle(k), to_oracle(v), True, rows=rows)
+    og, lg = gather_rows(o, lse, rows)
+    assert_close(og, lg, o_ref, l_ref, torch.bfloat16, name)
+
+
 # ---------------------------------------------------------------- LSE merge
 
 @pytest.mark.parametrize("blk_dtype", [torch.float32, torch.bfloat16])

@@ -99,6 +99,7 @@ def test_noalloc_matches_oracle_and_workspace_entry_point_twice(ra, name):
             ro, rl = oracle.attention(to_oracle(q), to_oracle(k), to_oracle(v), causal, rows=rows)
             og, lg = gather_rows(o, lse, rows)
             assert_close(og, lg, ro, rl, dtype, f"{name} call {call}")
+    assert ra.work_counters_in_use() == 0
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(ra):
