@@ -61,35 +61,63 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const __grid_constant__
 // The same for bf16 rows of 16-byte multiples with 16-byte aligned starts: each lane
 // reads 8 elements of O and of dO per load; a warp covers 256 elements of a row per
 // pass (two rows of D = 128, four of D = 64), so every lane has work and the loads stay
-// coalesced.  HBM-bound: 4 D bytes read per row.
+// coalesced.  A warp takes kRowdotPasses passes at a time and issues all their loads
+// before the first product, so each lane has 2 * kRowdotPasses 16-byte loads in flight.
+// HBM-bound: 4 D bytes read per row.
+constexpr int kRowdotPasses = 4;
 __global__ void __launch_bounds__(256) bwd_rowdot_vec_kernel(const __grid_constant__ BwdParams P) {
     const int lane = threadIdx.x & 31;
     const int per_row = P.D / 8;                 // lanes per row (8 or 16)
     const int rows_per_warp = 32 / per_row;      // 4 or 2
     const int sub = lane / per_row, l = lane - sub * per_row;
     const int64_t rows = (int64_t)P.B * P.Hq * P.N;
-    const int64_t wstride = (int64_t)gridDim.x * 8 * rows_per_warp;
-    for (int64_t row0 = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * rows_per_warp; row0 < rows;
-         row0 += wstride) {
-        const int64_t row = row0 + sub;
-        float acc = 0.f;
-        if (row < rows) {
-            const int64_t n = row % P.N, bh = row / P.N;
-            const int64_t h = bh % P.Hq, b = bh / P.Hq;
-            const uint4 x = __ldcs(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(P.o) + b * P.so[0] +
-                                                                 h * P.so[1] + n * P.so[2]) + l);
-            const uint4 y = __ldcs(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(P.dout) +
-                                                                 b * P.sdo[0] + h * P.sdo[1] + n * P.sdo[2]) + l);
-            const uint32_t xa[4] = {x.x, x.y, x.z, x.w}, ya[4] = {y.x, y.y, y.z, y.w};
+    const int64_t span = (int64_t)rows_per_warp * kRowdotPasses;  // rows of one warp iteration
+    const int64_t wstride = (int64_t)gridDim.x * 8 * span;
+    for (int64_t row0 = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * span; row0 < rows; row0 += wstride) {
+        // (batch, head, position) of this lane's first row, then stepped: two divisions per
+        // warp iteration instead of two 64-bit divisions per row (they made the pass
+        // issue-bound)
+        const int64_t first = row0 + sub;
+        const int64_t bh0 = first / P.N;
+        int n = (int)(first - bh0 * P.N);
+        int64_t b = bh0 / P.Hq;
+        int h = (int)(bh0 - b * P.Hq);
+        uint4 x[kRowdotPasses], y[kRowdotPasses];
+#pragma unroll
+        for (int p = 0; p < kRowdotPasses; ++p) {
+            if (p > 0) {
+                n += rows_per_warp;
+                while (n >= P.N) {
+                    n -= P.N;
+                    if (++h == P.Hq) {
+                        h = 0;
+                        ++b;
+                    }
+                }
+            }
+            const int64_t row = row0 + p * rows_per_warp + sub;
+            x[p] = y[p] = make_uint4(0u, 0u, 0u, 0u);
+            if (row < rows) {
+                x[p] = __ldcs(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(P.o) + b * P.so[0] +
+                                                              (int64_t)h * P.so[1] + (int64_t)n * P.so[2]) + l);
+                y[p] = __ldcs(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(P.dout) + b * P.sdo[0] +
+                                                              (int64_t)h * P.sdo[1] + (int64_t)n * P.sdo[2]) + l);
+            }
+        }
+#pragma unroll
+        for (int p = 0; p < kRowdotPasses; ++p) {
+            const uint32_t xa[4] = {x[p].x, x[p].y, x[p].z, x[p].w}, ya[4] = {y[p].x, y[p].y, y[p].z, y[p].w};
+            float acc = 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 acc = fmaf(__uint_as_float(xa[i] << 16), __uint_as_float(ya[i] << 16), acc);
                 acc = fmaf(__uint_as_float(xa[i] & 0xffff0000u), __uint_as_float(ya[i] & 0xffff0000u), acc);
             }
+            // reduce within each row's group of lanes
+            for (int o = per_row >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            const int64_t row = row0 + p * rows_per_warp + sub;
+            if (l == 0 && row < rows) P.dvec[row] = acc;
         }
-        // reduce within each row's group of lanes
-        for (int o = per_row >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (l == 0 && row < rows) P.dvec[row] = acc;
     }
 }
 
@@ -305,8 +333,9 @@ cudaError_t launch_bwd_rowdot(const BwdParams &P, int num_sms, cudaStream_t stre
                      P.so[2] % 8 == 0 && P.sdo[0] % 8 == 0 && P.sdo[1] % 8 == 0 && P.sdo[2] % 8 == 0 &&
                      reinterpret_cast<uintptr_t>(P.o) % 16 == 0 && reinterpret_cast<uintptr_t>(P.dout) % 16 == 0;
     if (vec) {
-        const int64_t warps = (rows + (256 / P.D) * 8 - 1) / ((256 / P.D) * 8) * 8;  // warps needed
-        const int g = (int)std::min<int64_t>((warps + 7) / 8, (int64_t)num_sms * 16);
+        const int64_t span = (int64_t)(256 / P.D) * kRowdotPasses;  // rows of one warp iteration
+        const int64_t warps = (rows + span - 1) / span;                  // warps needed
+        const int g = (int)std::min<int64_t>((warps + 7) / 8, (int64_t)num_sms * 8);
         bwd_rowdot_vec_kernel<<<g, 256, 0, stream>>>(P);
         return cudaGetLastError();
     }

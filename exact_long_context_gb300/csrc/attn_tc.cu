@@ -357,7 +357,14 @@ __device__ __forceinline__ bool decode_item(const StepParams &P, int L, int sub,
             w = L / BH;
             bh = L - w * BH;
         }
-        if (P.ring_fused) {
+        if (P.ring_fused && P.ring_layout == 2) {
+            // fused striped ring: every rank's chunk costs the same block by block (block lb
+            // walks R steps of 2 lb + 2 tiles), so items go block by block across the ranks,
+            // the last (heaviest) block first: longest first over the whole launch
+            const int wb = w / P.nseg;
+            si = w - wb * P.nseg;
+            lb = P.blocks_per_seg - 1 - wb;
+        } else if (P.ring_fused) {
             // fused ring: a block's cost is mostly its chunk's later steps, so items go
             // chunk by chunk (heaviest first, as the host orders them), last block first
             si = w / P.blocks_per_seg;

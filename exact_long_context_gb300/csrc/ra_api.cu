@@ -100,7 +100,7 @@ constexpr int kSchedSlots = 1024;
 __device__ int g_sched[2 * kSchedSlots];
 
 static const int kMaxDev = 64;
-static const int kHostGroups = 8;  // head groups of the host-buffer pipeline
+static const int kHostGroups = 8;  // head groups of the host-buffer pipeline (at most)
 static std::mutex g_mu;
 static int *g_err_ptr[kMaxDev];
 static int *g_sched_ptr[kMaxDev];
@@ -1141,19 +1141,21 @@ ra_status ra_ring_sim_fwd_host(const ra_tensor *q, const ra_tensor *k, const ra_
     void *ring_ws = ring_size > 1 ? static_cast<void *>(reinterpret_cast<char *>(dl) + align256((size_t)(B * Hq * N) * 4))
                                   : nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // Head groups of whole KV heads (with their G query heads each).  More groups overlap
-    // more of the copies with the kernels, but each group's launches must still fill the
-    // persistent grid: at least two rounds of 256-row blocks per launch where that
-    // leaves two or more groups (one KV head of the 8-rank N = 32K ring is a single round
-    // of 128 blocks, and eight such groups ran at a third of the grid's rate).
-    // When the copies take much longer than the kernels (the dense 4K workload moves
-    // 269 MB for 0.3 TFLOP), the kernels hide behind them whatever their grid fill, and
-    // the most groups overlap the most.  (Rates: ~1.2 PFLOP/s for the kernels, ~200 GB/s
-    // each way for pinned host copies, as measured on a GB300.)
+    // Head groups of whole KV heads (with their G query heads each), every batch in one
+    // launch.  More groups overlap more of the copies with the kernels, and the last
+    // group's kernel and copy out, which nothing overlaps, get shorter; but each group's
+    // launch must still fill the persistent grid: at least two rounds of 256-row blocks
+    // where that leaves two or more groups (one KV head of the 8-rank N = 32K ring is a
+    // single round of 128 blocks, and eight such groups ran at a third of the grid's
+    // rate).  When the copies take much longer than the kernels (the dense 4K workload
+    // moves 269 MB for 0.3 TFLOP), the kernels hide behind them whatever their grid fill;
+    // eight groups then beat sixteen (the copies alone, measured on a GB300: 1.16 ms
+    // against 1.22 ms for that workload's 269 MB).  (Rates: ~1.2 PFLOP/s for the kernels,
+    // ~200 GB/s each way for pinned host copies.)
     const double flops = 4.0 * (double)(B * Hq) * (double)N * (double)N * (double)D * (causal ? 0.5 : 1.0);
     const double bytes = (double)(2 * nq + 2 * nk) * (double)es;
     const bool copy_bound = flops / 1.2e15 < 0.5 * bytes / 2.0e11;
-    const int64_t blocks = Hq * ((N + 255) / 256);  // work blocks of one batch
+    const int64_t blocks = B * Hq * ((N + 255) / 256);  // work blocks of the whole problem
     const int64_t most = std::min<int64_t>(Hkv, kHostGroups);
     const int ng = (int)(copy_bound ? most : std::min<int64_t>(most, std::max<int64_t>(2, blocks / (2 * (int64_t)di.sms))));
     cudaError_t e = cudaEventRecord(hp->ev[2 * kHostGroups], st);  // prior work on the caller's stream
@@ -1175,7 +1177,9 @@ ra_status ra_ring_sim_fwd_host(const ra_tensor *q, const ra_tensor *k, const ra_
         if (e == cudaSuccess) e = cudaEventRecord(hp->ev[g], hp->cin);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(st, hp->ev[g], 0);
         if (e != cudaSuccess) break;
-        // compute: the group's heads, viewed inside the full device tensors
+        // compute: the group's heads of every batch, viewed inside the full device tensors;
+        // their LSE goes to a packed [B, group heads, N] slice of the LSE buffer (the
+        // group's rows of the full [B, Hq, N] layout are strided across batches)
         ra_tensor tq = *q, tk = *k, tv = *v, to = *o;
         const int64_t sq[4] = {Hq * N * D, N * D, D, 1}, sk[4] = {Hkv * N * D, N * D, D, 1};
         for (int i = 0; i < 4; ++i) {
@@ -1188,18 +1192,8 @@ ra_status ra_ring_sim_fwd_host(const ra_tensor *q, const ra_tensor *k, const ra_
         to.data = dout + q0 * qrow;
         tk.data = dk + k0 * qrow;
         tv.data = dv + k0 * qrow;
-        // the group's LSE rows are strided by Hq * N across batches: compute into a
-        // packed [B, group heads, N] slice of the LSE buffer, one batch at a time
-        for (int64_t b = 0; b < B && s == RA_OK; ++b) {
-            ra_tensor bq = tq, bk = tk, bv = tv, bo = to;
-            bq.shape[0] = bk.shape[0] = bv.shape[0] = bo.shape[0] = 1;
-            bq.data = static_cast<char *>(tq.data) + (size_t)b * Hq * qrow;
-            bo.data = static_cast<char *>(to.data) + (size_t)b * Hq * qrow;
-            bk.data = static_cast<char *>(tk.data) + (size_t)b * Hkv * qrow;
-            bv.data = static_cast<char *>(tv.data) + (size_t)b * Hkv * qrow;
-            s = ra_ring_sim_fwd(&bq, &bk, &bv, &bo, dl + (b * Hq + q0) * N, ring_size, layout, causal, scale, ring_ws,
-                                stream);
-        }
+        float *glse = dl + B * q0 * N;
+        s = ra_ring_sim_fwd(&tq, &tk, &tv, &to, glse, ring_size, layout, causal, scale, ring_ws, stream);
         if (s != RA_OK) return s;
         e = cudaEventRecord(hp->ev[kHostGroups + g], st);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->cout, hp->ev[kHostGroups + g], 0);
@@ -1208,7 +1202,7 @@ ra_status ra_ring_sim_fwd_host(const ra_tensor *q, const ra_tensor *k, const ra_
             e = cudaMemcpy2DAsync(static_cast<char *>(o->data) + q0 * qrow, (size_t)Hq * qrow, dout + q0 * qrow,
                                   (size_t)Hq * qrow, (size_t)(q1 - q0) * qrow, (size_t)B, cudaMemcpyDeviceToHost, hp->cout);
         if (e == cudaSuccess)
-            e = cudaMemcpy2DAsync(lse + q0 * N, (size_t)(Hq * N) * 4, dl + q0 * N, (size_t)(Hq * N) * 4,
+            e = cudaMemcpy2DAsync(lse + q0 * N, (size_t)(Hq * N) * 4, dl + B * q0 * N, (size_t)((q1 - q0) * N) * 4,
                                   (size_t)((q1 - q0) * N) * 4, (size_t)B, cudaMemcpyDeviceToHost, hp->cout);
     }
     // the caller's stream sees every copy out complete

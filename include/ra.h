@@ -332,8 +332,7 @@ int64_t ra_ring_sim_bwd_plan(int64_t N, int ring_size, ra_layout layout, int cau
  *     larger ones get RA_ERR_UNSUPPORTED (use ra_ring_sim_fwd with a workspace).
  *   - The call allocates nothing: no cudaMalloc/cudaFree, no host heap on success.
  *   - The first call on a device that needs the array looks up its device address (once
- *     per device, with that device current); make that first call before any stream
- *     capture.
+ *     per device, with that device current).
  *   - Every such call shares the array and it keeps the last call's contents.  Nothing in
  *     it needs clearing: each row's first partial is written, never merged.  Calls that
  *     overlap on the GPU (different streams, or different host threads) race on it:

@@ -27,7 +27,8 @@ CASES = [
     (2, 6, 3, 768, 64, 3, "striped", True, torch.bfloat16),
     (1, 4, 1, 512, 128, 2, "contig", False, torch.bfloat16),
     (2, 2, 2, 96, 16, 4, "zigzag", True, torch.float32),
-    (1, 16, 16, 256, 128, 1, "contig", True, torch.bfloat16),  # more KV heads than groups
+    (1, 24, 24, 256, 128, 1, "contig", True, torch.bfloat16),  # more KV heads than groups
+    (2, 12, 6, 512, 128, 2, "zigzag", True, torch.bfloat16),  # one KV head per group, two batches
 ]
 
 
