@@ -102,6 +102,26 @@ constexpr uint32_t kItemReaders = 1 + kEwWarps;  // the MMA thread and one lane 
 // first (0) or second (1) tile; false when the pair has a single (middle) tile.
 __device__ __forceinline__ int tile_pairs(int tps) { return (tps + 1) >> 1; }
 
+// A launch over one segment whose CTAs take items from a work counter (P.single) uses
+// single tiles instead, longest first: equal-cost pairs leave the last round of the
+// persistent grid part empty (1024 pairs on 152 SMs is 6.7 rounds), single tiles taken
+// heaviest first fill it.  Item L is tile rank w of unit u (a head, or a (batch, KV head)),
+// the units innermost within groups of hg consecutive units (hg 0: one group), so the CTAs
+// that run together stream the tiles of a few heads only (they stay in L2).
+__device__ __forceinline__ void group_decode(int L, int hg, int units, int tiles, int &w, int &u) {
+    if (hg > 0 && hg < units) {
+        const int per = hg * tiles;
+        const int g = L / per;
+        const int r = L - g * per;
+        const int gs = min(hg, units - g * hg);
+        w = r / gs;
+        u = g * hg + (r - w * gs);
+    } else {
+        w = L / units;
+        u = L - w * units;
+    }
+}
+
 // Fused ring (contiguous or zigzag layout): the streamed ranges of step s for a fixed
 // range [f0, f1) of rank `rank`.  dQ (kind 0): the key chunks of rank (rank - s) mod R
 // that some row of the range sees; dK/dV (kind 1): the query chunks of rank
@@ -224,14 +244,23 @@ struct QItem {
 };
 __device__ __forceinline__ bool decode_q(const BwdParams &P, int tps, int L, int sub, QItem &it) {
     const int BH = P.B * P.Hq;
-    const int np = tile_pairs(tps);
-    const int per_seg = BH * np;
-    it.si = L / per_seg;
-    const int rem = L - it.si * per_seg;
-    const int bh = rem / np;
-    const int pp = rem - bh * np;
-    const int qi = sub ? pp : tps - 1 - pp;  // the later (heavier) query tile first
-    if (sub && qi == tps - 1 - pp) return false;
+    int bh, qi;
+    if (P.single) {  // one segment, single tiles: under causality the last query tile is the heaviest
+        if (sub) return false;
+        int w;
+        group_decode(L, P.head_group, BH, tps, w, bh);
+        it.si = 0;
+        qi = P.causal ? tps - 1 - w : w;
+    } else {
+        const int np = tile_pairs(tps);
+        const int per_seg = BH * np;
+        it.si = L / per_seg;
+        const int rem = L - it.si * per_seg;
+        bh = rem / np;
+        const int pp = rem - bh * np;
+        qi = sub ? pp : tps - 1 - pp;  // the later (heavier) query tile first
+        if (sub && qi == tps - 1 - pp) return false;
+    }
     it.b = bh / P.Hq;
     it.h = bh - it.b * P.Hq;
     it.hk = it.h / (P.Hq / P.Hkv);
@@ -280,14 +309,21 @@ struct KItem {
 };
 __device__ __forceinline__ bool decode_kv(const BwdParams &P, int tps, int L, int sub, KItem &it) {
     const int BHk = P.B * P.Hkv;
-    const int np = tile_pairs(tps);
-    const int per_seg = BHk * np;
-    it.si = L / per_seg;
-    const int rem = L - it.si * per_seg;
-    const int bhk = rem / np;
-    const int pp = rem - bhk * np;
-    const int kj = sub ? tps - 1 - pp : pp;
-    if (sub && kj == pp) return false;
+    int bhk, kj;
+    if (P.single) {  // one segment, single tiles: under causality the first key tile is the heaviest
+        if (sub) return false;
+        group_decode(L, P.head_group, BHk, tps, kj, bhk);
+        it.si = 0;
+    } else {
+        const int np = tile_pairs(tps);
+        const int per_seg = BHk * np;
+        it.si = L / per_seg;
+        const int rem = L - it.si * per_seg;
+        bhk = rem / np;
+        const int pp = rem - bhk * np;
+        kj = sub ? tps - 1 - pp : pp;
+        if (sub && kj == pp) return false;
+    }
     it.b = bhk / P.Hkv;
     it.hk = bhk - it.b * P.Hkv;
     const BSeg &S = P.seg[it.si];
@@ -665,7 +701,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sV = base + (2 + C::KST) * C::TILE_BYTES;    // ring of V tiles
     BBars *bars = reinterpret_cast<BBars *>(base_ptr + C::BAR_OFF_DQ);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if ((int)blockIdx.x >= total) return;
+    if ((int)blockIdx.x >= total) {
+        if (P.sched && threadIdx.x == 0) sched_finish(P.sched);
+        return;
+    }
     volatile int32_t *abort_flag = &bars->abort;
     const int tps = (P.flen + kT - 1) / kT;
     const float sl2 = P.scale_log2;
@@ -690,9 +729,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             Ring kr = {0, 0u, 0u, 0u}, vr = {0, 0u, 0u, 0u};
             uint32_t fcnt = 0, rcnt = 0;
             bool ok = true;
-            for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, tile of the pair)
-                const int L = snake(k2 >> 1);
-                if (L >= total) continue;
+            int L = 0;
+            for (int k2 = 0; ok; ++k2) {  // (item, tile of the pair)
+                if (P.sched) {  // the next item number from the launch's work counter
+                    if (!(k2 & 1)) L = atomicAdd(&P.sched[0], 1);
+                    if (L >= total) break;
+                } else {
+                    if ((k2 >> 1) * (int)gridDim.x >= total) break;
+                    L = snake(k2 >> 1);
+                    if (L >= total) continue;
+                }
                 Rec<QItem> rec;
                 if (!decode_q(P, tps, L, k2 & 1, rec.it)) continue;
                 rec.seg = P.seg[rec.it.si];
@@ -878,6 +924,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
+    if (P.sched && threadIdx.x == 0) sched_finish(P.sched);
 }
 
 // ---------------------------------------------------------------- dK / dV kernel
@@ -933,6 +980,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *s_stage = reinterpret_cast<float *>(base_ptr + C::BAR_OFF + kBarBytes);  // [8 warps][2][64]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if ((int)blockIdx.x >= total) {
+        if (P.sched && threadIdx.x == 0) sched_finish(P.sched);
         asm volatile("griddepcontrol.wait;" ::: "memory");
         return;
     }
@@ -958,9 +1006,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             int slot = 0;
             uint32_t ph = 0, fcnt = 0, issued = 0, last_ph = 0, rcnt = 0;
             bool ok = true;
-            for (int k2 = 0; (k2 >> 1) * (int)gridDim.x < total && ok; ++k2) {  // (item, tile of the pair)
-                const int L = snake(k2 >> 1);
-                if (L >= total) continue;
+            int L = 0;
+            for (int k2 = 0; ok; ++k2) {  // (item, tile of the pair)
+                if (P.sched) {  // the next item number from the launch's work counter
+                    if (!(k2 & 1)) L = atomicAdd(&P.sched[0], 1);
+                    if (L >= total) break;
+                } else {
+                    if ((k2 >> 1) * (int)gridDim.x >= total) break;
+                    L = snake(k2 >> 1);
+                    if (L >= total) continue;
+                }
                 Rec<KItem> rec;
                 if (!decode_kv(P, tps, L, k2 & 1, rec.it)) continue;
                 rec.seg = P.seg[rec.it.si];
@@ -1209,12 +1264,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
+    if (P.sched && threadIdx.x == 0) sched_finish(P.sched);
     // when launched to overlap the dQ kernel's tail, finish only after it has: work later
     // in the stream then sees both kernels' writes (a no-op for a plain launch)
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace tcb
+
+// Units per head group of single-tile backward items: whole KV heads whose streamed
+// tiles (dQ kernel: K and V, 4 N D bytes per KV head; dK/dV kernel: Q and dO of its G query
+// heads) fit in 48 MiB, so they stay in the 129 MB L2 while the group runs; counted in
+// query heads for the dQ kernel, in (batch, KV head) units for the dK/dV kernel.  0: one
+// group (everything fits).
+static int32_t bwd_head_group(const BwdParams &P, int kind) {
+    const int64_t G = P.Hkv > 0 ? P.Hq / P.Hkv : 1;
+    const double per_kv = 4.0 * (double)P.N * (double)P.D * (kind ? (double)G : 1.0);
+    const int64_t units = (int64_t)P.B * P.Hkv;
+    const int64_t kv = std::max<int64_t>((int64_t)(48.0 * (1 << 20) / std::max(per_kv, 1.0)), 1);
+    if (kv >= units) return 0;
+    return (int32_t)std::min<int64_t>(kind ? kv : kv * G, 1 << 30);
+}
 
 template <int HD>
 static cudaError_t launch_bwd_tc_hd(const BwdParams &P, int parts, int num_sms, int64_t wait_ns, int *err,
@@ -1244,16 +1314,35 @@ static cudaError_t launch_bwd_tc_hd(const BwdParams &P, int parts, int num_sms, 
         !encode_map(&mv, P.v, P.B, P.Hkv, P.N, P.D, P.sv, P.rs) ||
         !encode_map(&mdo, P.dout, P.B, P.Hq, P.N, P.D, P.sdo, P.rs))
         return cudaErrorInvalidValue;
-    const int np = ((P.flen + tcb::kT - 1) / tcb::kT + 1) / 2;  // tile pairs per segment and head
-    const int64_t tq = (int64_t)P.B * P.Hq * P.nseg * np, tkv = (int64_t)P.B * P.Hkv * P.nseg * np;
+    const int tps = (P.flen + tcb::kT - 1) / tcb::kT;
+    const int np = (tps + 1) / 2;  // tile pairs per segment and head
+    // a one-segment launch with a work counter takes single tiles, longest first, in head
+    // groups; otherwise equal-cost tile pairs in static snake order (a fused ring's items,
+    // whose cost is mostly their later steps, keep pairs)
+    BwdParams Pq = P, Pk = P;
+    Pq.single = Pk.single = 0;
+    Pq.head_group = Pk.head_group = 0;
+    if (parts == 3) Pk.sched = nullptr;  // one counter pair per launch
+    if (P.nseg == 1 && !P.ring_fused) {
+        if (Pq.sched) {
+            Pq.single = 1;
+            Pq.head_group = bwd_head_group(P, 0);
+        }
+        if (Pk.sched) {
+            Pk.single = 1;
+            Pk.head_group = bwd_head_group(P, 1);
+        }
+    }
+    const int64_t tq = Pq.single ? (int64_t)P.B * P.Hq * tps : (int64_t)P.B * P.Hq * P.nseg * np;
+    const int64_t tkv = Pk.single ? (int64_t)P.B * P.Hkv * tps : (int64_t)P.B * P.Hkv * P.nseg * np;
     if (tq > 0x7fffffff || tkv > 0x7fffffff) return cudaErrorInvalidValue;
     const int gq = (int)std::min<int64_t>(tq, num_sms), gkv = (int)std::min<int64_t>(tkv, num_sms);
     if (parts & 1) {
         if (P.ring_fused)
-            tcb::bwd_dq_tc_kernel<HD, true><<<gq, tcb::kThreads, C::SMEM_BYTES_DQ, stream>>>(mq, mk, mv, mdo, P, (int)tq,
+            tcb::bwd_dq_tc_kernel<HD, true><<<gq, tcb::kThreads, C::SMEM_BYTES_DQ, stream>>>(mq, mk, mv, mdo, Pq, (int)tq,
                                                                                           wait_ns, err);
         else
-            tcb::bwd_dq_tc_kernel<HD, false><<<gq, tcb::kThreads, C::SMEM_BYTES_DQ, stream>>>(mq, mk, mv, mdo, P,
+            tcb::bwd_dq_tc_kernel<HD, false><<<gq, tcb::kThreads, C::SMEM_BYTES_DQ, stream>>>(mq, mk, mv, mdo, Pq,
                                                                                            (int)tq, wait_ns, err);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -1274,9 +1363,9 @@ static cudaError_t launch_bwd_tc_hd(const BwdParams &P, int parts, int num_sms, 
         }
         const int itkv = (int)tkv;
         cudaError_t e = P.ring_fused
-                            ? cudaLaunchKernelEx(&cfg, tcb::bwd_dkdv_tc_kernel<HD, true>, mq, mk, mv, mdo, P, itkv,
+                            ? cudaLaunchKernelEx(&cfg, tcb::bwd_dkdv_tc_kernel<HD, true>, mq, mk, mv, mdo, Pk, itkv,
                                                  wait_ns, err)
-                            : cudaLaunchKernelEx(&cfg, tcb::bwd_dkdv_tc_kernel<HD, false>, mq, mk, mv, mdo, P, itkv,
+                            : cudaLaunchKernelEx(&cfg, tcb::bwd_dkdv_tc_kernel<HD, false>, mq, mk, mv, mdo, Pk, itkv,
                                                  wait_ns, err);
         if (e != cudaSuccess) return e;
     }

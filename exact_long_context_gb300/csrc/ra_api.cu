@@ -1010,6 +1010,7 @@ ra_status ra_ring_sim_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tenso
                 P.seg[i] = g[i];
                 P.flen = std::max<int32_t>(P.flen, g[i].f1 - g[i].f0);
             }
+            P.sched = next_sched(di.dev);
             e = guarded_launch(kind == 0 ? "bwd_dq_tc" : "bwd_dkdv_tc", st, [&] {
                 return launch_attn_bwd_tc(P, kind == 0 ? 1 : 2, di.sms, g_wait_limit_ns, di.err, st, kind == 1);
             });
@@ -1036,6 +1037,7 @@ ra_status ra_ring_sim_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tenso
                 // a step's dK/dV launch follows its dQ launch directly, unless the dQ
                 // segments took several launches
                 const bool after_dq = kind == 1 && f == 0 && dq_launches_this_step == 1;
+                P.sched = tc ? next_sched(di.dev) : nullptr;
                 e = guarded_launch(tc ? (kind == 0 ? "bwd_dq_tc" : "bwd_dkdv_tc") : (kind == 0 ? "bwd_dq_simt" : "bwd_dkdv_simt"),
                                    st, [&] {
                                        return tc ? launch_attn_bwd_tc(P, parts, di.sms, g_wait_limit_ns, di.err, st, after_dq)

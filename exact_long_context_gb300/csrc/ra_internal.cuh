@@ -117,6 +117,9 @@ struct BwdParams {
     int32_t ring_fused;           // one launch walks every ring step (contiguous / zigzag)
     int32_t ring_R, ring_layout;  // fused ring: ring size, RA_LAYOUT_CONTIG (0) or ZIGZAG (1)
     int64_t producer_delay_ns;    // diagnostic: the TMA producer pauses this long before its first copy
+    int *sched;                   // work counter pair of this launch (nullptr: static snake order)
+    int32_t single;               // one-segment launch: single-tile items, longest first
+    int32_t head_group;           // single-tile items: units (heads) per group of consecutive items (0: one group)
     BSeg seg[kMaxBSeg];
 };
 

@@ -81,6 +81,39 @@ def test_backward_tensor_cores_match_cuda_cores(ra):
         assert err <= 2e-2, (name, err)
 
 
+def test_backward_every_tile_runs_once_in_head_groups(ra):
+    """A whole-sequence backward whose tiles go in head groups of single tiles from the
+    kernels' work counters (dQ: groups of 12 and 4 query heads across the two batches;
+    dK/dV: groups of 3, 3 and 2 (batch, KV head) units): gradients start as NaN and must all
+    be written, sampled rows match the oracle, and every counter pair is back to zero."""
+    B, Hq, Hkv, N, D = 2, 8, 4, 16384, 128
+    dtype = torch.bfloat16
+    q, k, v = synth.make_qkv(B, Hq, Hkv, N, D, dtype, seed=61, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(62)
+    dout = torch.randn(B, Hq, N, D, generator=g, device="cuda").to(dtype)
+    o, lse = ra.attn_fwd(q, k, v, causal=True)
+    dq = torch.full_like(q, float("nan"))
+    dk = torch.full_like(k, float("nan"))
+    dv = torch.full_like(v, float("nan"))
+    ra.attn_bwd(q, k, v, o, lse, dout, causal=True, dq=dq, dk=dk, dv=dv)
+    ra.check()
+    assert ra.work_counters_in_use() == 0
+    for t in (dq, dk, dv):
+        assert not torch.isnan(t).any().item()
+    rng = np.random.default_rng(63)
+    q_rows = np.array([(int(b), int(h), int(i)) for b, h, i in
+                       zip(rng.integers(0, B, 6), rng.integers(0, Hq, 6), rng.integers(0, N, 6))]
+                      + [(0, 0, 0), (1, Hq - 1, N - 1), (1, 4, 127), (0, 7, 128)])
+    # keys near the end (few rows see them, so the oracle stays quick) in every group
+    kv_rows = np.array([(b, hk, j) for b in range(B) for hk in range(Hkv) for j in (N - 1, N - 129 - hk)])
+    args = [to_oracle(t) for t in (q, k, v, dout)]
+    rq, rk, rv = ob.gradient_rows(*args, True, None, q_rows, kv_rows)
+    for name, got, rows, ref in (("dq", dq, q_rows, rq), ("dk", dk, kv_rows, rk), ("dv", dv, kv_rows, rv)):
+        sel = got[rows[:, 0], rows[:, 1], rows[:, 2]].float().cpu().numpy().astype(np.float64)
+        scaled, row, p999 = assert_grad_close(sel, ref, dtype, f"{name} sampled")
+        print(name, f"sampled: scaled {scaled:.2e} row {row:.2e} p99.9 {p999:.2e}")
+
+
 def test_backward_empty_and_errors(ra):
     q = torch.empty(1, 2, 0, 64, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(1, 2, 0, device="cuda")
