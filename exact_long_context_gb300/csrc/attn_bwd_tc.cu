@@ -127,9 +127,22 @@ __device__ __forceinline__ void group_decode(int L, int hg, int units, int tiles
 // that some row of the range sees; dK/dV (kind 1): the query chunks of rank
 // (rank + s) mod R that see some key of the range (the rank holding this block at step s).
 // Ranges are in increasing position; returns their number (0..2).
+// Striped layout (P.ring_layout 2): ranges are in the partner rank's own index space, and
+// the fixed range of a dQ item is its query tile [f0, f1): at step s the keys of rank
+// j = (rank - s) mod R that a row of the tile can see are [0, min(c, f1)) (the diagonal
+// offset of striped_step masks key f1 - 1 when j > rank); the queries of rank
+// (rank + s) mod R are [0, c), of which a dK/dV item walks those from its first key on.
 __device__ __forceinline__ int ring_ranges_bwd(const BwdParams &P, int kind, int rank, int f0, int f1, int s,
                                                int &a0, int &b0, int &a1, int &b1) {
     const int R = P.ring_R;
+    if (P.ring_layout == 2) {
+        const int c = P.N / R;
+        a0 = a1 = b1 = 0;
+        b0 = (kind || !P.causal) ? c : min(c, f1);
+        (void)f0;
+        (void)s;
+        return b0 > 0 ? 1 : 0;
+    }
     const int j = kind ? (rank + s) % R : ((rank - s) % R + R) % R;
     int ca0, cb0, ca1 = 0, cb1 = 0, nc;
     if (P.ring_layout == 0) {
@@ -161,6 +174,17 @@ __device__ __forceinline__ int ring_ranges_bwd(const BwdParams &P, int kind, int
         ++n;
     }
     return n;
+}
+
+// Striped layout: the rank holding the streamed tiles of step s and their diagonal offset.
+// Rank j's k-th position follows rank r's k-th exactly when j > r, so key k of rank j is
+// visible to row i of rank r iff k + [j > r] <= i (dQ: j = (r - s) mod R; dK/dV: the
+// queries of rank j = (r + s) mod R see key k of rank r iff k + [r > j] <= i).
+__device__ __forceinline__ void striped_step(const BwdParams &P, int kind, int rank, int s, int &srank, int &dg) {
+    const int R = P.ring_R;
+    const int j = kind ? (rank + s) % R : ((rank - s) % R + R) % R;
+    srank = j;
+    dg = P.causal ? (kind ? (rank > j ? 1 : 0) : (j > rank ? 1 : 0)) : 0;
 }
 
 // Walks the streamed tiles of the later steps (s = 1 .. R-1) of a fused ring item: every
@@ -242,6 +266,14 @@ struct QItem {
     int b, h, hk, si, r_lo, r_hi, n0, n1, n;
     int sa0, sb0, sa1, sb1;
 };
+// The fixed range whose streamed ranges a dQ item walks: its segment's, or under the
+// striped layout its own query tile (every step is then a causal prefix of the tile).
+__device__ __forceinline__ int q_fix0(const BwdParams &P, const BSeg &S, const QItem &it) {
+    return P.ring_layout == 2 ? it.r_lo : S.f0;
+}
+__device__ __forceinline__ int q_fix1(const BwdParams &P, const BSeg &S, const QItem &it) {
+    return P.ring_layout == 2 ? it.r_hi : S.f1;
+}
 __device__ __forceinline__ bool decode_q(const BwdParams &P, int tps, int L, int sub, QItem &it) {
     const int BH = P.B * P.Hq;
     int bh, qi;
@@ -268,7 +300,8 @@ __device__ __forceinline__ bool decode_q(const BwdParams &P, int tps, int L, int
     it.r_lo = S.f0 + qi * kT;
     it.r_hi = min(it.r_lo + kT, S.f1);
     if (P.ring_fused) {
-        const int nr = ring_ranges_bwd(P, 0, S.rank, S.f0, S.f1, 0, it.sa0, it.sb0, it.sa1, it.sb1);
+        const int nr = ring_ranges_bwd(P, 0, S.rank, q_fix0(P, S, it), q_fix1(P, S, it), 0, it.sa0, it.sb0, it.sa1,
+                                       it.sb1);
         if (nr < 2) it.sa1 = it.sb1 = it.sb0;
     } else {
         it.sa0 = S.s0[0];
@@ -287,7 +320,7 @@ __device__ __forceinline__ bool decode_q(const BwdParams &P, int tps, int L, int
         it.n1 += np_;
     }
     it.n = it.n1;
-    if (P.ring_fused && it.n1 > 0) it.n += later_tiles(P, 0, S.rank, S.f0, S.f1, 0);
+    if (P.ring_fused && it.n1 > 0) it.n += later_tiles(P, 0, S.rank, q_fix0(P, S, it), q_fix1(P, S, it), 0);
     return true;
 }
 
@@ -377,15 +410,22 @@ __device__ __forceinline__ void kv_tile0(const KItem &it, int tt, int &q0, int &
 struct QWalk {
     BCursor c;
     int t = 0;
+    // k0, klim: the key tile's first index and its range's end; srank, dg: the rank holding
+    // those keys and the tile's diagonal offset (key k visible to row i iff k + dg <= i)
     template <bool FUSED>
-    __device__ __forceinline__ void next(const BwdParams &P, const BSeg &S, const QItem &it, int &k0, int &klim) {
+    __device__ __forceinline__ void next(const BwdParams &P, const BSeg &S, const QItem &it, int &k0, int &klim,
+                                         int &srank, int &dg) {
+        srank = S.s_rank;
+        dg = S.diag;
         if (!FUSED || t < it.n1) {
             q_tile(S, it, t, k0, klim);
         } else {
-            if (t == it.n1) bcur_begin(P, 0, S.rank, S.f0, S.f1, 0, c);
+            const int f0 = q_fix0(P, S, it), f1 = q_fix1(P, S, it);
+            if (t == it.n1) bcur_begin(P, 0, S.rank, f0, f1, 0, c);
             k0 = c.start();
             klim = c.end();
-            bcur_next(P, 0, S.rank, S.f0, S.f1, 0, c);
+            if (P.ring_layout == 2) striped_step(P, 0, S.rank, c.s, srank, dg);
+            bcur_next(P, 0, S.rank, f0, f1, 0, c);
         }
         ++t;
     }
@@ -393,11 +433,15 @@ struct QWalk {
 struct KWalk {
     BCursor c;
     int t = 0;
+    // q0, qlim: the query tile's first index and its range's end; g: its query head in the
+    // KV head's group; srank, dg: the rank holding those queries and the diagonal offset
     template <bool FUSED>
     __device__ __forceinline__ void next(const BwdParams &P, const BSeg &S, const KItem &it, int &q0, int &qlim,
-                                         int &g) {
+                                         int &g, int &srank, int &dg) {
         g = t / it.per;
         const int tt = t - g * it.per;
+        srank = S.s_rank;
+        dg = S.diag;
         if (!FUSED || tt < it.per0) {
             kv_tile0(it, tt, q0, qlim);
         } else {
@@ -405,6 +449,7 @@ struct KWalk {
             if (tt == it.per0) bcur_begin(P, 1, S.rank, S.f0, S.f1, vis0, c);
             q0 = c.start();
             qlim = c.end();
+            if (P.ring_layout == 2) striped_step(P, 1, S.rank, c.s, srank, dg);
             bcur_next(P, 1, S.rank, S.f0, S.f1, vis0, c);
         }
         ++t;
@@ -494,7 +539,7 @@ template <int HD, typename StreamCoords>
 __device__ __forceinline__ bool produce_item(BBars *bars, uint32_t fix0, uint32_t st0, int &slot, uint32_t &ph,
                                              uint32_t &fcnt, uint32_t &issued, uint32_t &last_ph,
                                              const CUtensorMap *fa, const CUtensorMap *fb, int f_row, int f_rank,
-                                             int fh, const CUtensorMap *sa, const CUtensorMap *sb, int s_rank,
+                                             int fh, const CUtensorMap *sa, const CUtensorMap *sb,
                                              int n, int b, bool fix_in,
                                              StreamCoords coords, volatile int32_t *abort_flag,
                                              int64_t limit, int *err) {
@@ -511,8 +556,8 @@ __device__ __forceinline__ bool produce_item(BBars *bars, uint32_t fix0, uint32_
     }
     for (int t = 0; t < n; ++t) {
         if (!wait_phase(smem_u32(&bars->empty[slot]), ph ^ 1u, abort_flag, limit, err)) return false;
-        int row, head;
-        const bool in = coords(t, row, head);
+        int row, head, s_rank;
+        const bool in = coords(t, row, head, s_rank);
         const uint32_t bf = smem_u32(&bars->full[slot]);
         mbar_expect_tx(bf, 2 * C::TILE_BYTES);
         const uint32_t a0 = st0 + (2 * slot) * C::TILE_BYTES;
@@ -550,7 +595,7 @@ template <int HD, typename StreamCoords>
 __device__ __forceinline__ bool produce_item_kv(BBars *bars, uint32_t fix0, uint32_t k0, uint32_t v0, Ring &kr,
                                                 Ring &vr, uint32_t &fcnt, const CUtensorMap *fa,
                                                 const CUtensorMap *fb, int f_row, int f_rank, int fh,
-                                                const CUtensorMap *tk, const CUtensorMap *tv, int s_rank, int n,
+                                                const CUtensorMap *tk, const CUtensorMap *tv, int n,
                                                 int b, bool fix_in, StreamCoords coords, volatile int32_t *abort_flag,
                                                 int64_t limit, int *err) {
     using C = BCfg<HD>;
@@ -565,8 +610,8 @@ __device__ __forceinline__ bool produce_item_kv(BBars *bars, uint32_t fix0, uint
         ++fcnt;
     }
     for (int t = 0; t < n; ++t) {
-        int row, head;
-        const bool in = coords(t, row, head);
+        int row, head, s_rank;
+        const bool in = coords(t, row, head, s_rank);
         for (int which = 0; which < 2; ++which) {
             Ring &r = which ? vr : kr;
             uint64_t *emp = which ? bars->emptyv : bars->empty;
@@ -749,18 +794,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const BSeg &S = rec.seg;
                 const int hk = it.hk;
                 QWalk walk;
-                auto coords = [&](int t, int &row, int &head) -> bool {
-                    int klim;
-                    walk.next<FUSED>(P, S, it, row, klim);
+                auto coords = [&](int t, int &row, int &head, int &srank) -> bool {
+                    int klim, dg;
+                    walk.next<FUSED>(P, S, it, row, klim, srank, dg);
                     head = hk;
                     (void)t;
-                    return in_bounds(row >= 0 && row < P.N / P.rs && hk < P.Hkv && S.s_rank < P.rs, err);
+                    return in_bounds(row >= 0 && row < P.N / P.rs && hk < P.Hkv && srank >= 0 && srank < P.rs, err);
                 };
                 const bool fix_in = in_bounds(it.r_lo >= 0 && it.r_lo < P.N / P.rs && it.h < P.Hq &&
                                                   S.f_rank < P.rs && it.b < P.B,
                                               err);
                 ok = produce_item_kv<HD>(bars, sQ, sK, sV, kr, vr, fcnt, &tm_q, &tm_do, it.r_lo, S.f_rank, it.h,
-                                         &tm_k, &tm_v, S.s_rank, it.n, it.b, fix_in, coords, abort_flag, limit, err);
+                                         &tm_k, &tm_v, it.n, it.b, fix_in, coords, abort_flag, limit, err);
             }
             if (ok) {  // no more items
                 Rec<QItem> rec;
@@ -849,7 +894,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (rec.end) break;
             const QItem &it = rec.it;
             const BSeg &S = rec.seg;
-            const int n = it.n, diag = S.diag;
+            const int n = it.n;
             const int row = it.r_lo + quarter * 32 + lane;  // index in the fixed range
             const int64_t pos = (int64_t)row * P.rs + S.f_rank;
             const int64_t lrow = ((int64_t)it.b * P.Hq + it.h) * P.N + pos;
@@ -863,7 +908,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             QWalk walk;
             for (int t = 0; t < n && ok; ++t, ++g) {
                 int kt0, klim;
-                walk.next<FUSED>(P, S, it, kt0, klim);
+                int srank_t, diag;  // (the keys' rank: the producer's concern here)
+                walk.next<FUSED>(P, S, it, kt0, klim, srank_t, diag);
+                (void)srank_t;
                 ok = wait_phase(smem_u32(&bars->s_full[0]), g & 1u, abort_flag, limit, err);
                 if (!ok) break;
                 tc_fence_after();
@@ -1026,18 +1073,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const BSeg &S = rec.seg;
                 const int hk = it.hk;
                 KWalk walk;
-                auto coords = [&](int t, int &row, int &head) -> bool {
-                    int qlim, g;
-                    walk.next<FUSED>(P, S, it, row, qlim, g);
+                auto coords = [&](int t, int &row, int &head, int &srank) -> bool {
+                    int qlim, g, dg;
+                    walk.next<FUSED>(P, S, it, row, qlim, g, srank, dg);
                     head = hk * G + g;
                     (void)t;
-                    return in_bounds(row >= 0 && row < P.N / P.rs && head < P.Hq && S.s_rank < P.rs, err);
+                    return in_bounds(row >= 0 && row < P.N / P.rs && head < P.Hq && srank >= 0 && srank < P.rs, err);
                 };
                 const bool fix_in = in_bounds(it.c_lo >= 0 && it.c_lo < P.N / P.rs && hk < P.Hkv &&
                                                   S.f_rank < P.rs && it.b < P.B,
                                               err);
                 ok = produce_item<HD>(bars, sK, sSt, slot, ph, fcnt, issued, last_ph, &tm_k, &tm_v, it.c_lo,
-                                      S.f_rank, hk, &tm_q, &tm_do, S.s_rank, it.n, it.b, fix_in, coords, abort_flag,
+                                      S.f_rank, hk, &tm_q, &tm_do, it.n, it.b, fix_in, coords, abort_flag,
                                       limit, err);
             }
             if (ok) {  // no more items
@@ -1143,7 +1190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (rec.end) break;
             const KItem &it = rec.it;
             const BSeg &S = P.seg[it.si];  // (read in place: a register copy would spill)
-            const int n = it.n, diag = S.diag;
+            const int n = it.n;
             const int key = it.c_lo + quarter * 32 + lane;  // index in the fixed range
             const int64_t kpos = (int64_t)key * P.rs + S.f_rank;
             const int64_t arow = (((int64_t)it.b * P.Hkv + it.hk) * P.N + kpos) * HD;
@@ -1158,19 +1205,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the walk runs one tile ahead: fetch() takes tile t+1's coordinates and values
             // while tile t is processed, and hands the coordinates on
             KWalk walk;
-            int nq0 = 0, nqlim = 0, ngh = 0;
+            int nq0 = 0, nqlim = 0, ngh = 0, ndiag = 0;
             auto fetch = [&](int t, float (&l)[2], float (&d)[2]) {
-                int q0, qlim, gh;
-                walk.next<FUSED>(P, S, it, q0, qlim, gh);
+                int q0, qlim, gh, srank, dg;
+                walk.next<FUSED>(P, S, it, q0, qlim, gh, srank, dg);
                 nq0 = q0;
                 nqlim = qlim;
                 ngh = gh;
+                ndiag = dg;
                 (void)t;
                 const int h = it.hk * G + gh;
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const int qme = q0 + grp * 64 + r * 32 + lane;
-                    const int64_t li = ((int64_t)it.b * P.Hq + h) * P.N + (int64_t)qme * P.rs + S.s_rank;
+                    const int64_t li = ((int64_t)it.b * P.Hq + h) * P.N + (int64_t)qme * P.rs + srank;
                     const bool in = qme < qlim && in_bounds(li < (int64_t)P.B * P.Hq * P.N, err);
                     l[r] = in ? P.lse[li] * kLog2e : 0.f;
                     d[r] = in ? P.dvec[li] : 0.f;
@@ -1179,7 +1227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float nl[2] = {0.f, 0.f}, nd[2] = {0.f, 0.f};
             if (n > 0) fetch(0, nl, nd);
             for (int t = 0; t < n && ok; ++t, ++g) {
-                const int q0 = nq0, qlim = nqlim;
+                const int q0 = nq0, qlim = nqlim, diag = ndiag;
                 (void)ngh;
                 const int qa = q0 + grp * 64;  // first query of this warp's columns
                 __syncwarp();  // every lane is done with the previous tile's values

@@ -550,7 +550,26 @@ static int fused_ring_segments(int64_t N, int R, int layout, int causal, Seg *ou
 // chip, so each row is written once.  Heaviest first.  False when it does not apply.
 static bool fused_bwd_segments(int64_t N, int R, int layout, int causal, int kind, std::vector<BSeg> &out) {
     out.clear();
-    if (layout == RA_LAYOUT_STRIPED) return false;
+    if (layout == RA_LAYOUT_STRIPED) {
+        // one segment per rank in the rank-local index space; every step's partner tiles
+        // follow from the rank and the step (the kernels' striped walk).  Needs whole
+        // 128-row tiles per rank; the ranks' work is the same, so their order does not matter.
+        const int64_t c = N / R;
+        if (R > kMaxBSeg || c % 128 != 0 || c > INT32_MAX || c == 0) return false;
+        for (int r = 0; r < R; ++r) {
+            BSeg g;
+            memset(&g, 0, sizeof g);
+            g.f0 = 0;
+            g.f1 = (int32_t)c;
+            g.f_rank = g.s_rank = r;  // step 0: the rank's own keys and queries
+            g.flags = SEG_FIRST | SEG_FINAL;
+            g.rank = r;
+            out.push_back(g);
+        }
+        (void)causal;
+        (void)kind;
+        return true;
+    }
     const int chunks = layout == RA_LAYOUT_ZIGZAG ? 2 * R : R;
     if (chunks > kMaxBSeg || N > INT32_MAX) return false;
     std::vector<std::pair<int64_t, BSeg>> work;
@@ -1001,7 +1020,7 @@ ra_status ra_ring_sim_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tenso
         // one dQ launch and one dK/dV launch walk every step; gradients stay on chip
         P.ring_fused = 1;
         P.ring_R = ring_size;
-        P.ring_layout = layout == RA_LAYOUT_ZIGZAG ? 1 : 0;
+        P.ring_layout = layout == RA_LAYOUT_ZIGZAG ? 1 : (layout == RA_LAYOUT_STRIPED ? 2 : 0);
         for (int kind = 0; kind < 2 && result == RA_OK; ++kind) {
             const std::vector<BSeg> &g = kind == 0 ? segs : kv_segs;
             P.nseg = (int32_t)g.size();

@@ -114,8 +114,8 @@ struct BwdParams {
     int32_t rs;    // rank interleave of the striped layout (1 otherwise)
     int32_t flen;  // length of every segment's fixed range
     int32_t nseg;
-    int32_t ring_fused;           // one launch walks every ring step (contiguous / zigzag)
-    int32_t ring_R, ring_layout;  // fused ring: ring size, RA_LAYOUT_CONTIG (0) or ZIGZAG (1)
+    int32_t ring_fused;           // one launch walks every ring step (striped: ranks of whole tiles)
+    int32_t ring_R, ring_layout;  // fused ring: ring size, RA_LAYOUT_CONTIG (0), ZIGZAG (1) or STRIPED (2)
     int64_t producer_delay_ns;    // diagnostic: the TMA producer pauses this long before its first copy
     int *sched;                   // work counter pair of this launch (nullptr: static snake order)
     int32_t single;               // one-segment launch: single-tile items, longest first

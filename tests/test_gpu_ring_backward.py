@@ -46,6 +46,11 @@ CASES = [
     (1, 2, 2, 2048, 128, 8, "zigzag", True, torch.bfloat16),
     (1, 2, 1, 4096, 128, 2, "zigzag", True, torch.bfloat16),  # chunks of 8 tiles, 4 blocks
     (1, 2, 2, 3072, 64, 3, "contig", True, torch.bfloat16),
+    # striped ranks of whole tiles: one fused launch per kernel walks every step
+    (1, 4, 2, 1536, 128, 3, "striped", True, torch.bfloat16),   # 512 per rank, GQA
+    (1, 2, 2, 1024, 64, 4, "striped", True, torch.bfloat16),    # 256 per rank, D = 64
+    (2, 2, 1, 768, 128, 3, "striped", False, torch.bfloat16),   # non-causal, batch 2
+    (1, 2, 2, 1024, 128, 8, "striped", True, torch.bfloat16),   # one tile per rank
 ]
 
 
@@ -106,11 +111,12 @@ def test_ring_backward_tensor_cores_match_cuda_cores(ra):
         assert err <= 1e-2
 
 
-def test_ring_backward_full_size_sampled(ra):
-    """The 8-rank zigzag ring over 32768 positions (8 heads, head_dim 128, bf16):
-    sampled dQ rows and dK/dV rows against the oracle one by one, the ring against the
-    single pass, and sum_j dV_j = sum_i dO_i (each row of P sums to one)."""
-    w = synth.WORKLOADS["ring8_zigzag_h8n32k"]
+@pytest.mark.parametrize("name", ["ring8_zigzag_h8n32k", "ring8_striped_h8n32k"])
+def test_ring_backward_full_size_sampled(ra, name):
+    """The 8-rank zigzag and striped rings over 32768 positions (8 heads, head_dim 128,
+    bf16): sampled dQ rows and dK/dV rows against the oracle one by one, the ring against
+    the single pass, and sum_j dV_j = sum_i dO_i (each row of P sums to one)."""
+    w = synth.WORKLOADS[name]
     q, k, v = synth.workload_inputs(w, device="cuda")
     B, Hq, N, D = q.shape
     Hkv = k.shape[1]
@@ -122,9 +128,10 @@ def test_ring_backward_full_size_sampled(ra):
     ra.check()
     rng = np.random.default_rng(8)
     # query rows anywhere; key rows of every KV head in the last chunk and at the start of
-    # the second-to-last (keys whose gradients two ring steps write: the back chunk of rank 0
-    # and the front of rank 1's), and one key of an early chunk (chunk 2, rank 2's front
-    # chunk, seen by nearly every row and written on every step that reaches it)
+    # the second-to-last (zigzag: keys whose gradients two ring steps write, the back chunk
+    # of rank 0 and the front of rank 1's), and one key of an early chunk (zigzag: chunk 2,
+    # rank 2's front chunk, seen by nearly every row and written on every step that reaches
+    # it); under the striped layout the same positions fall on every rank
     chunk = N // (2 * R)
     q_rows = np.array([(0, int(h), int(i)) for h, i in zip(rng.integers(0, Hq, 12), rng.integers(0, N, 12))]
                       + [(0, 0, 0), (0, Hq - 1, N - 1), (0, 3, chunk), (0, 5, chunk - 1)])
@@ -133,10 +140,10 @@ def test_ring_backward_full_size_sampled(ra):
     kv_rows = np.array(kv_rows)
     args = [to_oracle(t) for t in (q, k, v, dout)]
     rq, rk, rv = ob.gradient_rows(*args, True, None, q_rows, kv_rows)
-    for name, got, rows, ref in (("dq", dq, q_rows, rq), ("dk", dk, kv_rows, rk), ("dv", dv, kv_rows, rv)):
+    for gname, got, rows, ref in (("dq", dq, q_rows, rq), ("dk", dk, kv_rows, rk), ("dv", dv, kv_rows, rv)):
         sel = got[rows[:, 0], rows[:, 1], rows[:, 2]].float().cpu().numpy().astype(np.float64)
-        scaled, row, p999 = assert_grad_close(sel, ref, torch.bfloat16, f"{name} sampled")
-        print(name, f"sampled: scaled {scaled:.2e} row {row:.2e} p99.9 {p999:.2e}")
+        scaled, row, p999 = assert_grad_close(sel, ref, torch.bfloat16, f"{name} {gname} sampled")
+        print(name, gname, f"sampled: scaled {scaled:.2e} row {row:.2e} p99.9 {p999:.2e}")
     # the ring against the single pass on the same forward outputs
     sq, sk, sv = ra.attn_bwd(q, k, v, o, lse, dout, causal=True)
     for x, y in ((dq, sq), (dk, sk), (dv, sv)):
