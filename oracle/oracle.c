@@ -229,5 +229,5 @@ int oracle_attention_rows(const void *q, const void *k, const void *v, int dtype
     return 0;
 }
 
-/* Which planted variant this build is (0 = the real oracle). */
+/* Which planted variant this compiled library is (0 = the real oracle). */
 int oracle_plant(void) { return ORACLE_PLANT; }
