@@ -211,7 +211,8 @@ ra_status ra_attn_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v
  * asynchronously; pageable memory works but each copy then waits).  The tensors must be
  * contiguous [B, H, N, D]; lse is [B, Hq, N] float32.  The call stages through the
  * caller's device workspace and pipelines by groups of whole KV heads (up to 8; fewer
- * when the kernels dominate and a group's launches would not fill the GPU): the next
+ * when the kernels dominate and a group's launch would not fill the GPU), one launch per
+ * group over every batch: the next
  * group's q/k/v go in on one internal stream while the current group computes on
  * `stream`, and finished groups' o/lse come out on another, so both directions of the
  * host link overlap the kernels.  The call is ordered on `stream`: the host buffers may
@@ -240,9 +241,10 @@ ra_status ra_ring_sim_fwd_host(const ra_tensor *q, const ra_tensor *k, const ra_
  * and dV = P^T dout to the block's rank, which sums them over the steps.  Each step
  * applies the forward's causal rule (skipped, diagonal or full blocks; the striped
  * interleave's offset).  bf16 with D in {64, 128} and a contiguous or zigzag layout of
- * up to 128 chunks: one dQ launch walks each query chunk's partner blocks over all steps
- * and one dK/dV launch walks each key chunk's partner ranks, (j + s) mod R at step s
- * (the reverse ring), with both gradients kept in the kernels across steps.  Otherwise
+ * up to 128 chunks, or the striped layout with up to 128 ranks of whole 128-row tiles:
+ * one dQ launch walks each query chunk's partner blocks over all steps and one dK/dV
+ * launch walks each key chunk's partner ranks, (j + s) mod R at step s (the reverse
+ * ring), with both gradients kept in the kernels across steps.  Otherwise
  * one launch of each kernel per step covers every rank, and gradients that several steps
  * write are carried between steps in fp32 in the workspace.  The sum over steps is the
  * gradient of the whole sequence, so ring_size = 1 (any layout) is ra_attn_bwd.
