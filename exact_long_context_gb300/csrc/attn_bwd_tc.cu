@@ -456,11 +456,6 @@ struct KWalk {
     }
 };
 
-__device__ __forceinline__ int snake(int k) {
-    const int G = gridDim.x;
-    return k * G + ((k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
-}
-
 // ---------------------------------------------------------------- shared pieces
 
 __device__ __forceinline__ void bwd_init(BBars *bars, int nst) {
@@ -747,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     BBars *bars = reinterpret_cast<BBars *>(base_ptr + C::BAR_OFF_DQ);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if ((int)blockIdx.x >= total) {
-        if (P.sched && threadIdx.x == 0) sched_finish(P.sched);
+        if (threadIdx.x == 0) sched_finish(P.sched);
         return;
     }
     volatile int32_t *abort_flag = &bars->abort;
@@ -776,14 +771,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             int L = 0;
             for (int k2 = 0; ok; ++k2) {  // (item, tile of the pair)
-                if (P.sched) {  // the next item number from the launch's work counter
-                    if (!(k2 & 1)) L = atomicAdd(&P.sched[0], 1);
-                    if (L >= total) break;
-                } else {
-                    if ((k2 >> 1) * (int)gridDim.x >= total) break;
-                    L = snake(k2 >> 1);
-                    if (L >= total) continue;
-                }
+                if (!(k2 & 1)) L = atomicAdd(&P.sched[0], 1);  // the next item number
+                if (L >= total) break;
                 Rec<QItem> rec;
                 if (!decode_q(P, tps, L, k2 & 1, rec.it)) continue;
                 rec.seg = P.seg[rec.it.si];
@@ -971,7 +960,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
-    if (P.sched && threadIdx.x == 0) sched_finish(P.sched);
+    if (threadIdx.x == 0) sched_finish(P.sched);
 }
 
 // ---------------------------------------------------------------- dK / dV kernel
@@ -1027,7 +1016,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *s_stage = reinterpret_cast<float *>(base_ptr + C::BAR_OFF + kBarBytes);  // [8 warps][2][64]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if ((int)blockIdx.x >= total) {
-        if (P.sched && threadIdx.x == 0) sched_finish(P.sched);
+        if (threadIdx.x == 0) sched_finish(P.sched);
         asm volatile("griddepcontrol.wait;" ::: "memory");
         return;
     }
@@ -1055,14 +1044,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             int L = 0;
             for (int k2 = 0; ok; ++k2) {  // (item, tile of the pair)
-                if (P.sched) {  // the next item number from the launch's work counter
-                    if (!(k2 & 1)) L = atomicAdd(&P.sched[0], 1);
-                    if (L >= total) break;
-                } else {
-                    if ((k2 >> 1) * (int)gridDim.x >= total) break;
-                    L = snake(k2 >> 1);
-                    if (L >= total) continue;
-                }
+                if (!(k2 & 1)) L = atomicAdd(&P.sched[0], 1);  // the next item number
+                if (L >= total) break;
                 Rec<KItem> rec;
                 if (!decode_kv(P, tps, L, k2 & 1, rec.it)) continue;
                 rec.seg = P.seg[rec.it.si];
@@ -1312,7 +1295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
-    if (P.sched && threadIdx.x == 0) sched_finish(P.sched);
+    if (threadIdx.x == 0) sched_finish(P.sched);
     // when launched to overlap the dQ kernel's tail, finish only after it has: work later
     // in the stream then sees both kernels' writes (a no-op for a plain launch)
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -1364,23 +1347,14 @@ static cudaError_t launch_bwd_tc_hd(const BwdParams &P, int parts, int num_sms, 
         return cudaErrorInvalidValue;
     const int tps = (P.flen + tcb::kT - 1) / tcb::kT;
     const int np = (tps + 1) / 2;  // tile pairs per segment and head
-    // a one-segment launch with a work counter takes single tiles, longest first, in head
-    // groups; otherwise equal-cost tile pairs in static snake order (a fused ring's items,
-    // whose cost is mostly their later steps, keep pairs)
+    // a one-segment launch takes single tiles, longest first, in head groups; otherwise
+    // equal-cost tile pairs, segment by segment (a fused ring's items, whose cost is mostly
+    // their later steps, keep pairs)
+    if (!P.sched || parts == 3) return cudaErrorInvalidValue;  // one work counter pair per launch
     BwdParams Pq = P, Pk = P;
-    Pq.single = Pk.single = 0;
-    Pq.head_group = Pk.head_group = 0;
-    if (parts == 3) Pk.sched = nullptr;  // one counter pair per launch
-    if (P.nseg == 1 && !P.ring_fused) {
-        if (Pq.sched) {
-            Pq.single = 1;
-            Pq.head_group = bwd_head_group(P, 0);
-        }
-        if (Pk.sched) {
-            Pk.single = 1;
-            Pk.head_group = bwd_head_group(P, 1);
-        }
-    }
+    Pq.single = Pk.single = (P.nseg == 1 && !P.ring_fused) ? 1 : 0;
+    Pq.head_group = Pq.single ? bwd_head_group(P, 0) : 0;
+    Pk.head_group = Pk.single ? bwd_head_group(P, 1) : 0;
     const int64_t tq = Pq.single ? (int64_t)P.B * P.Hq * tps : (int64_t)P.B * P.Hq * P.nseg * np;
     const int64_t tkv = Pk.single ? (int64_t)P.B * P.Hkv * tps : (int64_t)P.B * P.Hkv * P.nseg * np;
     if (tq > 0x7fffffff || tkv > 0x7fffffff) return cudaErrorInvalidValue;
@@ -1420,10 +1394,11 @@ static cudaError_t launch_bwd_tc_hd(const BwdParams &P, int parts, int num_sms, 
     return cudaGetLastError();
 }
 
-// The dQ kernel (parts & 1) and the dK/dV kernel (parts & 2) over the segments in P (the
-// D vector is computed before).
-// after_dq: the launch directly follows this call's dQ kernel on `stream`, so the dK/dV
-// kernel may start on the SMs the dQ grid frees (programmatic dependent launch).
+// The dQ kernel (parts 1) or the dK/dV kernel (parts 2) over the segments in P (the D
+// vector is computed before), taking its items from the work counter pair P.sched: one
+// kernel per call, since each launch needs its own pair.
+// after_dq: the launch directly follows a dQ kernel on `stream`, so the dK/dV kernel may
+// start on the SMs the dQ grid frees (programmatic dependent launch).
 cudaError_t launch_attn_bwd_tc(const BwdParams &P, int parts, int num_sms, int64_t wait_ns, int *err,
                                cudaStream_t stream, bool after_dq) {
     if (P.B <= 0 || P.Hq <= 0 || P.nseg <= 0 || P.flen <= 0) return cudaSuccess;

@@ -318,15 +318,9 @@ __device__ __forceinline__ void cursor_next(const StepParams &P, const Item &it,
     cursor_seek(P, it, c);
 }
 
-// Item L of a launch.  With a work counter (P.sched) each CTA's producer takes the next
-// item number when it needs one, so any order balances over the persistent grid.
-// Otherwise a CTA takes one item per round of gridDim.x items, in snake order (forward in
-// even rounds, backward in odd ones), so that the heavy and light ends of the cost-sorted
-// list even out across CTAs.
-__device__ __forceinline__ int snake_item(int k) {
-    const int G = gridDim.x;
-    return k * G + ((k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
-}
+// Items of a launch are numbered heaviest first (decode_item); each CTA's producer takes
+// the next item number from the launch's work counter (P.sched) when it needs one, so the
+// persistent grid balances whatever the items' costs.
 
 // Work item L, part `sub`.  With P.pair_items (segments of equal length): an item is a
 // pair of 256-row blocks of one segment and one head, block p and block nb-1-p, so under
@@ -512,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int total = P.total_items;
     if ((int)blockIdx.x >= total) {
-        if (P.sched && threadIdx.x == 0) sched_finish(P.sched);
+        if (threadIdx.x == 0) sched_finish(P.sched);
         return;
     }
 
@@ -582,14 +576,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             int L = 0;
             for (int k2 = 0; ok; ++k2) {  // (item, part)
-                if (P.sched) {
-                    if (!(k2 & 1)) L = atomicAdd(&P.sched[0], 1);
-                    if (L >= total) break;
-                } else {
-                    if ((k2 >> 1) * (int)gridDim.x >= total) break;
-                    L = snake_item(k2 >> 1);
-                    if (L >= total) continue;
-                }
+                if (!(k2 & 1)) L = atomicAdd(&P.sched[0], 1);  // the next item number
+                if (L >= total) break;
                 Item it;
                 if (!decode_item(P, L, k2 & 1, it)) continue;
                 if (it.nmax == 0) continue;
@@ -1123,7 +1111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
-    if (P.sched && threadIdx.x == 0) sched_finish(P.sched);
+    if (threadIdx.x == 0) sched_finish(P.sched);
 }
 
 // One block, one thread: a bounded wait on a barrier nothing completes.
@@ -1151,6 +1139,7 @@ template <int HD>
 static cudaError_t launch_tc_hd(const StepParams &P, int blocks_y, int num_sms,
                                 cudaStream_t stream) {
     using C = tc::Cfg<HD>;
+    if (!P.sched) return cudaErrorInvalidValue;  // items come from a work counter pair
     static int configured_mask = 0;  // per device ordinal bit (devices < 32)
     int dev = 0;
     cudaGetDevice(&dev);

@@ -60,7 +60,7 @@ struct StepParams {
     int64_t producer_delay_ns;  // diagnostic: the TMA producer pauses this long before its first copy
     int *err;  // device error word
     // tensor-core kernel: this launch's work counter pair (next item, CTAs finished), zero on
-    // entry and reset to zero by the last CTA; NULL: a static assignment of items to CTAs
+    // entry and reset to zero by the last CTA (required)
     int *sched;
     int32_t blocks_y;    // work blocks per head (set at launch)
     int32_t head_group;  // single-block items: query heads per group of consecutive items (0: all)
@@ -117,7 +117,7 @@ struct BwdParams {
     int32_t ring_fused;           // one launch walks every ring step (striped: ranks of whole tiles)
     int32_t ring_R, ring_layout;  // fused ring: ring size, RA_LAYOUT_CONTIG (0), ZIGZAG (1) or STRIPED (2)
     int64_t producer_delay_ns;    // diagnostic: the TMA producer pauses this long before its first copy
-    int *sched;                   // work counter pair of this launch (nullptr: static snake order)
+    int *sched;                   // tensor-core kernels: work counter pair of this launch (required)
     int32_t single;               // one-segment launch: single-tile items, longest first
     int32_t head_group;           // single-tile items: units (heads) per group of consecutive items (0: one group)
     BSeg seg[kMaxBSeg];
