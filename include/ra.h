@@ -23,6 +23,11 @@
  * Paths (all on the GPU; there is no CPU path):
  *   bf16, D in {64, 128}, 16-byte aligned base and row strides: tcgen05 tensor-core
  *     kernel (TMA-fed shared-memory pipeline, S and O accumulated in tensor memory).
+ *     Its persistent launches take their work items from one of 1024 work-counter pairs
+ *     per device, in rotation, and each launch zeroes its pair again when it ends; so at
+ *     most 1024 tensor-core launches of the library may be in flight on one device at a
+ *     time (launches on one stream run in order; only launches on many streams at once
+ *     could reach that).
  *   anything else with D <= 128 (float32 inputs, other head sizes, unaligned strides):
  *     a CUDA-core kernel computing in float32.
  *   D > 128: RA_ERR_UNSUPPORTED.
