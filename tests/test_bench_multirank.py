@@ -43,6 +43,41 @@ def test_two_gloo_ranks_take_the_slowest_rank():
         assert abs(res[rank][4] - 2.0e12 * 10 * 2 / 0.150) < 1e-3 * res[rank][4]
 
 
+def _rank_with_dead_peer(rank, world, port, out):
+    import datetime
+    import sys
+    import time
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=10))
+    if rank == 1:
+        os._exit(0)  # the peer dies between steps, with nothing of its own in flight
+    t0 = time.time()
+    try:
+        bench.max_over_ranks(1.0)
+        out[rank] = ("returned", time.time() - t0)
+    except Exception as e:  # the collective reports the missing peer instead of waiting forever
+        out[rank] = (type(e).__name__, time.time() - t0)
+
+
+def test_a_dead_peer_is_reported_not_waited_for():
+    """Failure detection on the host: one of two gloo ranks exits after joining the group;
+    the survivor's max-over-ranks reduction raises within the group's timeout instead of
+    hanging (no GPU is involved)."""
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_rank_with_dead_peer, args=(2, port, out), nprocs=2, join=True)
+        res = dict(out)
+    assert 0 in res and 1 not in res
+    kind, elapsed = res[0]
+    assert kind != "returned", "the reduction returned without its peer"
+    assert elapsed < 60.0
+
+
 def test_single_process_is_identity():
     import sys
     sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
