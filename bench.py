@@ -55,6 +55,16 @@ def max_over_ranks(x: float) -> float:
     return float(t.item())
 
 
+def emit(args, line: dict):
+    """The run's one JSON line on stdout, and appended to the --results JSON-lines file when
+    one is given (one record per run: config, rates, roofline, baselines, clocks)."""
+    text = json.dumps(line)
+    print(text, flush=True)
+    if getattr(args, "results", None):
+        with open(args.results, "a") as f:
+            f.write(text + "\n")
+
+
 def whole_job_rate(units_per_rank_step: float, steps: int, world: int, max_ms: float) -> float:
     """Units processed by all ranks per second of the slowest rank's timed region."""
     return units_per_rank_step * steps * world / (max_ms * 1e-3)
@@ -586,6 +596,8 @@ def main():
                     help="fwd (default): the hot path; bwd: its backward (ring schedule when ring_size > 1); "
                          "merge / ulysses: the HBM-bound LSE merge / Ulysses exchange; hostlink: pinned "
                          "host <-> device copy rates (the end-to-end figure's bound)")
+    ap.add_argument("--results", default=None,
+                    help="also append the JSON line to this JSON-lines file (rank 0)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -617,14 +629,14 @@ def main():
             return
         line.update(res)
         line["impl"] = "reference"
-        print(json.dumps(line), flush=True)
+        emit(args, line)
         return
 
     if args.pass_ == "hostlink":
         if rank == 0:
             line.update(run_hostlink(args, ws, rank, local))
             line["config"] = {"workload": "pinned copies 8 MiB .. 1 GiB"}
-            print(json.dumps(line), flush=True)
+            emit(args, line)
         return
     if args.pass_ in ("merge", "ulysses"):
         res = run_hbm_pass(args, w, ws, rank, local)
@@ -632,7 +644,7 @@ def main():
             line.update(res)
             line["unit"] = "GB/s"
             line["dtype"] = "f32+bf16" if args.pass_ == "merge" else line["dtype"]
-            print(json.dumps(line), flush=True)
+            emit(args, line)
         if ws > 1:
             torch.distributed.barrier()
             torch.distributed.destroy_process_group()
@@ -645,7 +657,7 @@ def main():
             line["pct_of_peaks"] = peak_fractions(line["value"])
         if args.pass_ == "bwd":
             line["cpu_baseline"] = None  # the oracle's timed leg is the forward
-            print(json.dumps(line), flush=True)
+            emit(args, line)
             if ws > 1:
                 torch.distributed.barrier()
                 torch.distributed.destroy_process_group()
@@ -663,7 +675,7 @@ def main():
                 "value": round(f1 / sec1 / 1e12, 7), "unit": "TFLOP/s", "cores": 1,
                 "sample": f"{nrows1} uniformly random query rows of {w.name} (fp64 oracle, one thread, "
                           f"{sec1:.1f} s wall)"}
-        print(json.dumps(line), flush=True)
+        emit(args, line)
     if ws > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()

@@ -106,3 +106,22 @@ def test_peak_fractions():
             sus = json.load(fh).get("bf16_tflops_sustained")
         if sus:
             assert bench.peak_fractions(sus)["of_measured_sustained"] == 100.0
+
+
+def test_results_file_gets_one_record_per_run(tmp_path, capsys):
+    """--results appends each run's JSON line to a JSON-lines file, as printed."""
+    import json
+    import sys
+    import types
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+
+    path = tmp_path / "runs.jsonl"
+    args = types.SimpleNamespace(results=str(path))
+    bench.emit(args, {"metric": "m", "value": 1.0})
+    bench.emit(args, {"metric": "m", "value": 2.0})
+    printed = [json.loads(x) for x in capsys.readouterr().out.strip().splitlines()]
+    stored = [json.loads(x) for x in path.read_text().strip().splitlines()]
+    assert printed == stored == [{"metric": "m", "value": 1.0}, {"metric": "m", "value": 2.0}]
+    bench.emit(types.SimpleNamespace(results=None), {"value": 3.0})  # stdout only
+    assert len(path.read_text().strip().splitlines()) == 2
