@@ -73,7 +73,10 @@ struct BCfg {
     static constexpr uint32_t TM_DQ = 384;                    // dQ kernel: dQ
     static constexpr uint32_t TM_COLS = 512;
     static constexpr int BAR_OFF = (2 + 2 * NST) * TILE_BYTES;
-    static constexpr int SMEM_BYTES = 1024 + BAR_OFF + kBarBytes + kEwWarps * 2 * 64 * 4;
+    // dK/dV kernel: per element-wise warp, its LSE/D values, then a 2 KiB staging buffer
+    // for the bulk tensor stores of final dK/dV rows (32 rows x 32 columns)
+    static constexpr int STG_OFF = BAR_OFF + kBarBytes + kEwWarps * 2 * 64 * 4;
+    static constexpr int SMEM_BYTES = 1024 + STG_OFF + kEwWarps * 2048;
     static constexpr int BAR_OFF_DQ = (2 + KST + VST) * TILE_BYTES;
     static constexpr int SMEM_BYTES_DQ = 1024 + BAR_OFF_DQ + kBarBytes;
 };
@@ -1003,6 +1006,7 @@ template <int HD, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                        const __grid_constant__ BwdParams P, int total, int64_t limit, int *err) {
     using C = BCfg<HD>;
     extern __shared__ uint8_t smem_raw[];
@@ -1272,6 +1276,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   (int64_t)it.hk * P.sdv[1] + kpos * P.sdv[2];
             __nv_bfloat16 *krow = static_cast<__nv_bfloat16 *>(P.dk) + (int64_t)it.b * P.sdk[0] +
                                   (int64_t)it.hk * P.sdk[1] + kpos * P.sdk[2];
+            // Final rows of a key tile that lies wholly inside its range (or is clipped by the
+            // end of the tensor) leave through shared memory and bulk tensor stores, 32 rows x
+            // 32 columns per warp at a time: row-per-thread stores would issue 32 scattered
+            // 16-byte pieces per instruction (measured: the stores cost 6 % of the dense
+            // backward).  The rest are written row by row (store_grad_chunk).
+            const int row0 = it.c_lo + quarter * 32;
+            // (only rows that no other step adds to: first and final, with no running value)
+            const bool tma = n > 0 && (S.flags & SEG_FIRST) && (S.flags & SEG_FINAL) && P.dkv_tma &&
+                             (it.c_hi - it.c_lo == kT || it.c_hi == P.N / P.rs);
+            const uint32_t stg = smem_u32(base_ptr + C::STG_OFF) + (uint32_t)(warp - 4) * 2048u;
             for (int which = 0; which < 2; ++which) {
                 const float mul = which ? P.scale : 1.f;
                 __nv_bfloat16 *dst = which ? krow : vrow;
@@ -1285,12 +1299,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] = 0u;
                     }
+                    if (tma) {
+                        if (row0 >= P.N / P.rs) continue;  // a box wholly past the rows writes nothing
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            pk[i] = pack_bf16x2(mul * __uint_as_float(o[2 * i]), mul * __uint_as_float(o[2 * i + 1]));
+                        if (lane == 0) bulk_wait_read0();  // this warp's previous store has read the buffer
+                        __syncwarp();
+                        // 64-byte swizzle, as the tensor map expects: 16-byte piece j of row r
+                        // sits at piece j ^ ((r / 2) mod 4)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t a = stg + lane * 64 + ((uint32_t)(j ^ ((lane >> 1) & 3)) << 4);
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pk[4 * j]),
+                                         "r"(pk[4 * j + 1]), "r"(pk[4 * j + 2]), "r"(pk[4 * j + 3])
+                                         : "memory");
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0 && in_bounds(row0 >= 0 && S.f_rank < P.rs && it.hk < P.Hkv && it.b < P.B, err)) {
+                            tma_store_5d(which ? &tm_dk : &tm_dv, stg, c * 32, S.f_rank, row0, it.hk, it.b);
+                            bulk_commit();
+                        }
+                        __syncwarp();
+                        continue;
+                    }
                     if (!kvalid) continue;
                     store_grad_chunk(dst + c * 32, acc + c * 32, o, mul, S.flags);
                 }
             }
         }
     }
+    // the bulk stores of dK/dV issued by each element-wise warp are complete before exit
+    if (warp >= 4 && lane == 0) bulk_wait0();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1351,10 +1393,20 @@ static cudaError_t launch_bwd_tc_hd(const BwdParams &P, int parts, int num_sms, 
     // equal-cost tile pairs, segment by segment (a fused ring's items, whose cost is mostly
     // their later steps, keep pairs)
     if (!P.sched || parts == 3) return cudaErrorInvalidValue;  // one work counter pair per launch
+    // dK and dV through bulk tensor stores (32 x 32 boxes, 64-byte swizzle) when their
+    // layouts allow a map (else row stores)
+    CUtensorMap mdk, mdv;
+    const bool dkv_map = encode_map(&mdk, P.dk, P.B, P.Hkv, P.N, P.D, P.sdk, P.rs, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) &&
+                         encode_map(&mdv, P.dv, P.B, P.Hkv, P.N, P.D, P.sdv, P.rs, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!dkv_map) {
+        memset(&mdk, 0, sizeof mdk);
+        memset(&mdv, 0, sizeof mdv);
+    }
     BwdParams Pq = P, Pk = P;
     Pq.single = Pk.single = (P.nseg == 1 && !P.ring_fused) ? 1 : 0;
     Pq.head_group = Pq.single ? bwd_head_group(P, 0) : 0;
     Pk.head_group = Pk.single ? bwd_head_group(P, 1) : 0;
+    Pk.dkv_tma = dkv_map ? 1 : 0;
     const int64_t tq = Pq.single ? (int64_t)P.B * P.Hq * tps : (int64_t)P.B * P.Hq * P.nseg * np;
     const int64_t tkv = Pk.single ? (int64_t)P.B * P.Hkv * tps : (int64_t)P.B * P.Hkv * P.nseg * np;
     if (tq > 0x7fffffff || tkv > 0x7fffffff) return cudaErrorInvalidValue;
@@ -1385,9 +1437,9 @@ static cudaError_t launch_bwd_tc_hd(const BwdParams &P, int parts, int num_sms, 
         }
         const int itkv = (int)tkv;
         cudaError_t e = P.ring_fused
-                            ? cudaLaunchKernelEx(&cfg, tcb::bwd_dkdv_tc_kernel<HD, true>, mq, mk, mv, mdo, Pk, itkv,
+                            ? cudaLaunchKernelEx(&cfg, tcb::bwd_dkdv_tc_kernel<HD, true>, mq, mk, mv, mdo, mdk, mdv, Pk, itkv,
                                                  wait_ns, err)
-                            : cudaLaunchKernelEx(&cfg, tcb::bwd_dkdv_tc_kernel<HD, false>, mq, mk, mv, mdo, Pk, itkv,
+                            : cudaLaunchKernelEx(&cfg, tcb::bwd_dkdv_tc_kernel<HD, false>, mq, mk, mv, mdo, mdk, mdv, Pk, itkv,
                                                  wait_ns, err);
         if (e != cudaSuccess) return e;
     }

@@ -120,6 +120,7 @@ struct BwdParams {
     int *sched;                   // tensor-core kernels: work counter pair of this launch (required)
     int32_t single;               // one-segment launch: single-tile items, longest first
     int32_t head_group;           // single-tile items: units (heads) per group of consecutive items (0: one group)
+    int32_t dkv_tma;              // dK/dV kernel: final rows leave through bulk tensor stores
     BSeg seg[kMaxBSeg];
 };
 
