@@ -73,10 +73,14 @@ struct BCfg {
     static constexpr uint32_t TM_DQ = 384;                    // dQ kernel: dQ
     static constexpr uint32_t TM_COLS = 512;
     static constexpr int BAR_OFF = (2 + 2 * NST) * TILE_BYTES;
-    // dK/dV kernel: per element-wise warp, its LSE/D values, then a 2 KiB staging buffer
-    // for the bulk tensor stores of final dK/dV rows (32 rows x 32 columns)
+    // dK/dV kernel: per element-wise warp, its LSE/D values, then (outside the fused ring) a
+    // 2 KiB staging buffer for the bulk tensor stores of final dK/dV rows (32 rows x 32
+    // columns).  The fused ring writes its rows once per long item: there the buffer's
+    // shared memory (taken from L1) cost more than the stores gained (ring8 -0.4 % zigzag,
+    // -1.6 % striped), so it keeps row stores.
     static constexpr int STG_OFF = BAR_OFF + kBarBytes + kEwWarps * 2 * 64 * 4;
-    static constexpr int SMEM_BYTES = 1024 + STG_OFF + kEwWarps * 2048;
+    static constexpr int SMEM_BYTES_FUSED = 1024 + STG_OFF;
+    static constexpr int SMEM_BYTES = SMEM_BYTES_FUSED + kEwWarps * 2048;
     static constexpr int BAR_OFF_DQ = (2 + KST + VST) * TILE_BYTES;
     static constexpr int SMEM_BYTES_DQ = 1024 + BAR_OFF_DQ + kBarBytes;
 };
@@ -1283,7 +1287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // backward).  The rest are written row by row (store_grad_chunk).
             const int row0 = it.c_lo + quarter * 32;
             // (only rows that no other step adds to: first and final, with no running value)
-            const bool tma = n > 0 && (S.flags & SEG_FIRST) && (S.flags & SEG_FINAL) && P.dkv_tma &&
+            const bool tma = !FUSED && n > 0 && (S.flags & SEG_FIRST) && (S.flags & SEG_FINAL) && P.dkv_tma &&
                              (it.c_hi - it.c_lo == kT || it.c_hi == P.N / P.rs);
             const uint32_t stg = smem_u32(base_ptr + C::STG_OFF) + (uint32_t)(warp - 4) * 2048u;
             for (int which = 0; which < 2; ++which) {
@@ -1377,7 +1381,7 @@ static cudaError_t launch_bwd_tc_hd(const BwdParams &P, int parts, int num_sms, 
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(tcb::bwd_dkdv_tc_kernel<HD, true>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES_FUSED);
         if (e != cudaSuccess) return e;
         configured_mask |= 1 << (dev & 31);
     }
@@ -1426,7 +1430,7 @@ static cudaError_t launch_bwd_tc_hd(const BwdParams &P, int parts, int num_sms, 
         memset(&cfg, 0, sizeof cfg);
         cfg.gridDim = dim3(gkv);
         cfg.blockDim = dim3(tcb::kThreads);
-        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.dynamicSmemBytes = P.ring_fused ? C::SMEM_BYTES_FUSED : C::SMEM_BYTES;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
