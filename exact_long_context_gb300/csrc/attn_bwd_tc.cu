@@ -532,6 +532,17 @@ __device__ __forceinline__ bool ring_get(BBars *bars, uint32_t &cnt, R &r, bool 
 }
 
 
+// The fixed pair of an item is read once, from DRAM, and its loads wait until the previous
+// item's last product on the pair is done: start it towards L2 as soon as the item is known.
+template <int HD>
+__device__ __forceinline__ void prefetch_fixed(const CUtensorMap *fa, const CUtensorMap *fb, int f_row, int f_rank,
+                                               int fh, int b, bool fix_in) {
+    for (int c = 0; c < BCfg<HD>::SLABS && fix_in; ++c) {
+        tma_prefetch_5d(fa, c * 64, f_rank, f_row, fh, b);
+        tma_prefetch_5d(fb, c * 64, f_rank, f_row, fh, b);
+    }
+}
+
 // Producer: per item the fixed pair (fa, fb) at index f_row of rank f_rank of (fh, b), then
 // `n` streamed pairs (sa, sb) at the index and head coords(t) gives, of rank s_rank.
 // fix_in and coords' result: the coordinates lie inside their tensors (always true in
@@ -546,6 +557,7 @@ __device__ __forceinline__ bool produce_item(BBars *bars, uint32_t fix0, uint32_
                                              StreamCoords coords, volatile int32_t *abort_flag,
                                              int64_t limit, int *err) {
     using C = BCfg<HD>;
+    prefetch_fixed<HD>(fa, fb, f_row, f_rank, fh, b, fix_in);
     if (!wait_phase(smem_u32(&bars->fix_empty), (fcnt & 1u) ^ 1u, abort_flag, limit, err)) return false;
     {
         const uint32_t bf = smem_u32(&bars->fix_full);
@@ -601,6 +613,7 @@ __device__ __forceinline__ bool produce_item_kv(BBars *bars, uint32_t fix0, uint
                                                 int b, bool fix_in, StreamCoords coords, volatile int32_t *abort_flag,
                                                 int64_t limit, int *err) {
     using C = BCfg<HD>;
+    prefetch_fixed<HD>(fa, fb, f_row, f_rank, fh, b, fix_in);
     if (!wait_phase(smem_u32(&bars->fix_empty), (fcnt & 1u) ^ 1u, abort_flag, limit, err)) return false;
     {
         const uint32_t bf = smem_u32(&bars->fix_full);

@@ -118,6 +118,16 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// L2 prefetch of a tile (5-D map): a hint that starts the tile on its way from DRAM; it
+// writes no shared memory and signals nothing.  Same coordinate rule as a load.
+__device__ __forceinline__ void tma_prefetch_5d(const CUtensorMap *map, int c0, int c1, int c2, int c3,
+                                                int c4) {
+    asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+                 : "memory");
+}
+
 // Tiled bulk store smem -> global (5-D map), tracked by the thread's bulk groups.
 __device__ __forceinline__ void tma_store_5d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2,
                                              int c3, int c4) {
