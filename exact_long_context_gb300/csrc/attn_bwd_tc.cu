@@ -840,8 +840,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool pend = false, pend_acc = false, pend_last = false;
             int pend_slot = 0;
             uint32_t pend_g = 0;
-            auto flush = [&]() -> bool {
-                if (!wait_count(&bars->p_count[1], (uint32_t)kEwWarps * (pend_g + 1u), abort_flag, limit, err))
+            // done: the element-wise warps' completion count, read earlier, already shows the
+            // pending tile's dS stored (then no wait here)
+            auto flush = [&](bool done) -> bool {
+                if (!done &&
+                    !wait_count(&bars->p_count[1], (uint32_t)kEwWarps * (pend_g + 1u), abort_flag, limit, err))
                     return false;
                 tc_fence_after();
                 issue_tn<HD>(tmem + C::TM_DQ, tmem + d_slot(pend_g) + 32, sK + pend_slot * C::TILE_BYTES,
@@ -866,7 +869,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     tc_fence_after();
                     issue_nt<HD>(tmem + s_slot(g), sQ, sK + kr.slot * C::TILE_BYTES);  // S = Q K^T
-                    if (g > 0) {  // this tile's dP goes where the previous tile's S was read from
+                    // Every wait of this thread leaves the tensor pipe without queued work, so
+                    // the completion count of the element-wise warps is read here, once, and
+                    // looked at only after this tile's dP is issued.  The warps finish a tile
+                    // while the next one's S is computed, so it usually shows the previous
+                    // tile done: then neither the wait for its S to be read (implied: each
+                    // warp counts a tile read before it counts it done) nor the one for its
+                    // dS is needed.
+                    const uint32_t done_cnt = count_peek(&bars->p_count[1]);
+                    const bool prev_done = g > 0 && (int32_t)(done_cnt - (uint32_t)kEwWarps * g) >= 0;
+                    if (g > 0 && !prev_done) {  // this tile's dP goes where the previous tile's S was read from
                         ok = wait_count(&bars->p_count[0], (uint32_t)kEwWarps * g, abort_flag, limit, err);
                         if (!ok) break;
                     }
@@ -878,7 +890,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(smem_u32(&bars->emptyv[vr.slot]));  // the V tile is free
                     vr.advance<C::VST>();
                     if (t == n - 1) mma_commit(smem_u32(&bars->fix_empty));
-                    if (pend && !(ok = flush())) break;
+                    if (pend && !(ok = flush(prev_done))) break;
                     pend = true;
                     pend_acc = t > 0;
                     pend_last = t == n - 1;
@@ -887,7 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     kr.advance<C::KST>();
                 }
             }
-            if (ok && pend) ok = flush();
+            if (ok && pend) ok = flush(false);
             mma_commit(smem_u32(&bars->drain));
             wait_phase_drain(smem_u32(&bars->drain), 0);
         }
