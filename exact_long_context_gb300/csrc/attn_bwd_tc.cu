@@ -90,6 +90,7 @@ struct BBars {
     uint64_t full[4], empty[4];    // streamed pairs (dK/dV kernel) or K tiles (dQ kernel)
     uint64_t fullv[4], emptyv[4];  // V tiles (dQ kernel)
     uint64_t s_full[2], o_full, drain;
+    uint64_t dq_done[2], drain2, pad_;  // dQ kernel: the dQ issuer's products (alternating), its drain
     uint32_t tmem_base;
     int32_t abort;
     uint32_t p_count[2];
@@ -100,6 +101,7 @@ static_assert(sizeof(BBars) <= kBarBytes, "barrier block");
 static_assert(offsetof(BBars, it_rec) % 16 == 0, "16-byte item records");
 constexpr int kItemRing = 4;
 constexpr uint32_t kItemReaders = 1 + kEwWarps;  // the MMA thread and one lane per element-wise warp
+constexpr uint32_t kItemReadersDq = 2 + kEwWarps;  // dQ kernel: its two MMA issuers and the element-wise warps
 
 // Work items are pairs of tiles of one segment and one head: tile p and tile tps-1-p of
 // the segment's fixed range.  Under causality the two costs add up to the same total,
@@ -465,7 +467,7 @@ struct KWalk {
 
 // ---------------------------------------------------------------- shared pieces
 
-__device__ __forceinline__ void bwd_init(BBars *bars, int nst) {
+__device__ __forceinline__ void bwd_init(BBars *bars, int nst, uint32_t readers) {
     bars->abort = 0;
     bars->p_count[0] = bars->p_count[1] = 0;
     mbar_init(smem_u32(&bars->fix_full), 1);
@@ -480,9 +482,12 @@ __device__ __forceinline__ void bwd_init(BBars *bars, int nst) {
     mbar_init(smem_u32(&bars->s_full[1]), 1);
     mbar_init(smem_u32(&bars->o_full), 1);
     mbar_init(smem_u32(&bars->drain), 1);
+    mbar_init(smem_u32(&bars->dq_done[0]), 1);
+    mbar_init(smem_u32(&bars->dq_done[1]), 1);
+    mbar_init(smem_u32(&bars->drain2), 1);
     for (int i = 0; i < kItemRing; ++i) {
         mbar_init(smem_u32(&bars->it_full[i]), 1);
-        mbar_init(smem_u32(&bars->it_empty[i]), kItemReaders);
+        mbar_init(smem_u32(&bars->it_empty[i]), readers);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -769,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tps = (P.flen + kT - 1) / kT;
     const float sl2 = P.scale_log2;
 
-    if (threadIdx.x == 0) bwd_init(bars, 4);
+    if (threadIdx.x == 0) bwd_init(bars, 4, kItemReadersDq);
     if (warp == 1) tmem_alloc(smem_u32(&bars->tmem_base), C::TM_COLS);
     tc_fence_before();
     __syncthreads();
@@ -833,27 +838,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
+            // S / dP issuer.  Tile g's S goes to the slot that held dS of tile g - 2, so it
+            // waits for that tile's dQ product (the other issuer's) to complete; its dP goes
+            // to the slot of tile g - 1's S once the element-wise warps have read that.
             Ring kr = {0, 0u, 0u, 0u}, vr = {0, 0u, 0u, 0u};
             uint32_t fcnt = 0, g = 0;
             bool ok = true;
-            // the dQ product of the previous tile, issued once its dS is in tensor memory
-            bool pend = false, pend_acc = false, pend_last = false;
-            int pend_slot = 0;
-            uint32_t pend_g = 0;
-            // done: the element-wise warps' completion count, read earlier, already shows the
-            // pending tile's dS stored (then no wait here)
-            auto flush = [&](bool done) -> bool {
-                if (!done &&
-                    !wait_count(&bars->p_count[1], (uint32_t)kEwWarps * (pend_g + 1u), abort_flag, limit, err))
-                    return false;
-                tc_fence_after();
-                issue_tn<HD>(tmem + C::TM_DQ, tmem + d_slot(pend_g) + 32, sK + pend_slot * C::TILE_BYTES,
-                             pend_acc);  // dQ += dS K
-                mma_commit(smem_u32(&bars->empty[pend_slot]));  // the K tile is free
-                if (pend_last) mma_commit(smem_u32(&bars->o_full));
-                pend = false;
-                return true;
-            };
             uint32_t rcnt = 0;
             while (ok) {
                 Rec<QItem> rec;
@@ -865,20 +855,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = wait_phase(smem_u32(&bars->fix_full), fcnt & 1u, abort_flag, limit, err);
                 ++fcnt;
                 for (int t = 0; ok && t < n; ++t, ++g) {
+                    // dq_done[g & 1] completes once per tile of that parity: tile g - 2's is
+                    // its completion number (g - 2) / 2
+                    if (g >= 2) {
+                        ok = wait_phase(smem_u32(&bars->dq_done[g & 1u]), ((g - 2u) >> 1) & 1u, abort_flag, limit, err);
+                        if (!ok) break;
+                    }
                     ok = wait_phase(smem_u32(&bars->full[kr.slot]), kr.ph, abort_flag, limit, err);
                     if (!ok) break;
                     tc_fence_after();
                     issue_nt<HD>(tmem + s_slot(g), sQ, sK + kr.slot * C::TILE_BYTES);  // S = Q K^T
-                    // Every wait of this thread leaves the tensor pipe without queued work, so
-                    // the completion count of the element-wise warps is read here, once, and
-                    // looked at only after this tile's dP is issued.  The warps finish a tile
-                    // while the next one's S is computed, so it usually shows the previous
-                    // tile done: then neither the wait for its S to be read (implied: each
-                    // warp counts a tile read before it counts it done) nor the one for its
-                    // dS is needed.
-                    const uint32_t done_cnt = count_peek(&bars->p_count[1]);
-                    const bool prev_done = g > 0 && (int32_t)(done_cnt - (uint32_t)kEwWarps * g) >= 0;
-                    if (g > 0 && !prev_done) {  // this tile's dP goes where the previous tile's S was read from
+                    if (g > 0) {  // this tile's dP goes where the previous tile's S was read from
                         ok = wait_count(&bars->p_count[0], (uint32_t)kEwWarps * g, abort_flag, limit, err);
                         if (!ok) break;
                     }
@@ -890,18 +877,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(smem_u32(&bars->emptyv[vr.slot]));  // the V tile is free
                     vr.advance<C::VST>();
                     if (t == n - 1) mma_commit(smem_u32(&bars->fix_empty));
-                    if (pend && !(ok = flush(prev_done))) break;
-                    pend = true;
-                    pend_acc = t > 0;
-                    pend_last = t == n - 1;
-                    pend_slot = kr.slot;
-                    pend_g = g;
-                    kr.advance<C::KST>();
+                    kr.advance<C::KST>();  // (the dQ issuer frees the K tile)
                 }
             }
-            if (ok && pend) ok = flush(false);
             mma_commit(smem_u32(&bars->drain));
             wait_phase_drain(smem_u32(&bars->drain), 0);
+        }
+    } else if (warp == 2) {
+        if (lane == 0) {
+            // dQ issuer: dQ += dS K for each tile once the element-wise warps have stored its
+            // dS.  A thread that issues tcgen05 MMAs stalls on each until the tensor pipe
+            // takes it, and the pipe runs dry while that thread waits on anything; with the
+            // dQ products on their own thread, the waits of each issuer are covered by the
+            // other's products.  Tile g's K tile sits in slot g mod KST of the K ring.
+            uint32_t g = 0, rcnt = 0;
+            bool ok = true;
+            while (ok) {
+                Rec<QItem> rec;
+                if (!(ok = ring_get(bars, rcnt, rec, false, abort_flag, limit, err))) break;
+                if (rec.end) break;
+                const int n = rec.it.n;
+                for (int t = 0; ok && t < n; ++t, ++g) {
+                    ok = wait_count(&bars->p_count[1], (uint32_t)kEwWarps * (g + 1u), abort_flag, limit, err);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t ks = g % (uint32_t)C::KST;
+                    issue_tn<HD>(tmem + C::TM_DQ, tmem + d_slot(g) + 32, sK + ks * C::TILE_BYTES,
+                                 t > 0);  // dQ += dS K
+                    mma_commit(smem_u32(&bars->dq_done[g & 1u]));
+                    mma_commit(smem_u32(&bars->empty[ks]));  // the K tile is free
+                    if (t == n - 1) mma_commit(smem_u32(&bars->o_full));
+                }
+            }
+            mma_commit(smem_u32(&bars->drain2));
+            wait_phase_drain(smem_u32(&bars->drain2), 0);
         }
     } else if (warp >= 4) {
         const int quarter = warp & 3;
@@ -1058,7 +1067,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tps = (P.flen + kT - 1) / kT;
     const float sl2 = P.scale_log2;
 
-    if (threadIdx.x == 0) bwd_init(bars, C::NST);
+    if (threadIdx.x == 0) bwd_init(bars, C::NST, kItemReaders);
     if (warp == 1) tmem_alloc(smem_u32(&bars->tmem_base), C::TM_COLS);
     tc_fence_before();
     __syncthreads();
