@@ -743,10 +743,15 @@ __device__ __forceinline__ void dq_tile_ew(uint32_t (&sv)[64], uint32_t tD, int 
         uint32_t dp[32];
         tmem_ld32_wait(tD + grp * 64 + c * 32, dp);
         uint32_t pk[16];
+        const uint64_t d2 = pack_f32x2(d_r, d_r);
 #pragma unroll
-        for (int e = 0; e < 32; e += 2)
-            pk[e / 2] = pack_bf16x2(__uint_as_float(sv[c * 32 + e]) * (__uint_as_float(dp[e]) - d_r),
-                                    __uint_as_float(sv[c * 32 + e + 1]) * (__uint_as_float(dp[e + 1]) - d_r));
+        for (int e = 0; e < 32; e += 2) {  // dS = P (dP - D), two columns per paired op
+            const uint64_t ds = fmul2(pack_f32x2(__uint_as_float(sv[c * 32 + e]), __uint_as_float(sv[c * 32 + e + 1])),
+                                      fsub2(pack_f32x2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), d2));
+            float d0, d1;
+            unpack_f32x2(ds, d0, d1);
+            pk[e / 2] = pack_bf16x2(d0, d1);
+        }
         tmem_st16(tD + 32 + 32 * grp + 16 * c, pk);
     }
 }
@@ -1032,10 +1037,14 @@ __device__ __forceinline__ void ds_tile_ew(const uint32_t (&pv)[64], uint32_t tD
         tmem_ld32_wait(tD + grp * 64 + c * 32, dp);
         uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2)
-            pk[e / 2] = pack_bf16x2(__uint_as_float(pv[c * 32 + e]) * (__uint_as_float(dp[e]) - du[c * 32 + e]),
-                                    __uint_as_float(pv[c * 32 + e + 1]) *
-                                        (__uint_as_float(dp[e + 1]) - du[c * 32 + e + 1]));
+        for (int e = 0; e < 32; e += 2) {  // two columns per paired op
+            const uint64_t ds = fmul2(pack_f32x2(__uint_as_float(pv[c * 32 + e]), __uint_as_float(pv[c * 32 + e + 1])),
+                                      fsub2(pack_f32x2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
+                                            pack_f32x2(du[c * 32 + e], du[c * 32 + e + 1])));
+            float d0, d1;
+            unpack_f32x2(ds, d0, d1);
+            pk[e / 2] = pack_bf16x2(d0, d1);
+        }
         tmem_st16(tD + 32 + 32 * grp + 16 * c, pk);
     }
 }
@@ -1256,8 +1265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 (void)ngh;
                 const int qa = q0 + grp * 64;  // first query of this warp's columns
                 __syncwarp();  // every lane is done with the previous tile's values
-                lb[lane] = nl[0];
-                lb[32 + lane] = nl[1];
+                lb[lane] = -nl[0];  // negated: the exponent's FFMA adds it
+                lb[32 + lane] = -nl[1];
                 db[lane] = nd[0];
                 db[32 + lane] = nd[1];
                 __syncwarp();
@@ -1276,7 +1285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 64; e += 2) {
                     const uint64_t x = ffma2(pack_f32x2(__uint_as_float(pv[e]), __uint_as_float(pv[e + 1])),
-                                             pack_f32x2(sl2, sl2), pack_f32x2(-lb[e], -lb[e + 1]));
+                                             pack_f32x2(sl2, sl2), pack_f32x2(lb[e], lb[e + 1]));
                     float x0, x1;
                     unpack_f32x2(x, x0, x1);
                     pv[e] = __float_as_uint(ex2(x0));
