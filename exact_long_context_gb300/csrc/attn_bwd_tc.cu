@@ -934,8 +934,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t pos = (int64_t)row * P.rs + S.f_rank;
             const int64_t lrow = ((int64_t)it.b * P.Hq + it.h) * P.N + pos;
             const bool valid = row < it.r_hi && in_bounds(pos < P.N && lrow < (int64_t)P.B * P.Hq * P.N, err);
-            const float lse_l2 = valid ? P.lse[lrow] * kLog2e : 0.f;
-            const float d_r = valid ? P.dvec[lrow] : 0.f;
+            // the row's LSE and D, kept as loaded until the first tile's S is in: arithmetic
+            // on them here would stall the warp until the loads return
+            float lse_raw = 0.f, d_r = 0.f;
+            if (valid) {
+                lse_raw = P.lse[lrow];
+                d_r = P.dvec[lrow];
+            }
             float *accp = P.acc_q + lrow * HD;
             if (valid && grp == 0 && !(S.flags & SEG_FIRST))
                 for (int i = 0; i < HD * 4; i += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(
@@ -956,6 +961,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) count_release_add(&bars->p_count[0]);
+                // (opaque per tile, so the scaling below stays here and is not hoisted to the load)
+                asm volatile("" : "+f"(lse_raw), "+f"(d_r));
+                const float nl2 = lse_raw * -kLog2e;  // -LSE in log2 units
                 const int k0 = kt0 + grp * 64;  // first key of this warp's columns
                 if ((k0 + 64 > klim) || (P.causal && k0 + 63 + diag > row) || !valid) {
                     const int hi = !valid ? 0 : (P.causal ? min(klim, row + 1 - diag) : klim) - k0;
@@ -965,7 +973,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 64; e += 2) {
                     const uint64_t x = ffma2(pack_f32x2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
-                                             pack_f32x2(sl2, sl2), pack_f32x2(-lse_l2, -lse_l2));
+                                             pack_f32x2(sl2, sl2), pack_f32x2(nl2, nl2));
                     float x0, x1;
                     unpack_f32x2(x, x0, x1);
                     sv[e] = __float_as_uint(ex2(x0));
@@ -1234,8 +1242,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(P.acc_k + arow) + i));
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(P.acc_v + arow) + i));
                 }
-            // LSE (log2 units) and D of this lane's two queries of tile t; the next tile's
-            // are loaded while this one is processed, so their latency is hidden
+            // LSE and D of this lane's two queries of tile t; the next tile's are loaded while
+            // this one is processed.  fetch() keeps them as loaded: any arithmetic on them
+            // here would stall the warp until the load returns (it did: ~750 cycles a tile).
+            // They are scaled to log2 units when staged, a tile later.
             // the walk runs one tile ahead: fetch() takes tile t+1's coordinates and values
             // while tile t is processed, and hands the coordinates on
             KWalk walk;
@@ -1254,8 +1264,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int qme = q0 + grp * 64 + r * 32 + lane;
                     const int64_t li = ((int64_t)it.b * P.Hq + h) * P.N + (int64_t)qme * P.rs + srank;
                     const bool in = qme < qlim && in_bounds(li < (int64_t)P.B * P.Hq * P.N, err);
-                    l[r] = in ? P.lse[li] * kLog2e : 0.f;
-                    d[r] = in ? P.dvec[li] : 0.f;
+                    float lv = 0.f, dv = 0.f;
+                    if (in) {
+                        lv = P.lse[li];
+                        dv = P.dvec[li];
+                    }
+                    l[r] = lv;
+                    d[r] = dv;
                 }
             };
             float nl[2] = {0.f, 0.f}, nd[2] = {0.f, 0.f};
@@ -1265,8 +1280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 (void)ngh;
                 const int qa = q0 + grp * 64;  // first query of this warp's columns
                 __syncwarp();  // every lane is done with the previous tile's values
-                lb[lane] = -nl[0];  // negated: the exponent's FFMA adds it
-                lb[32 + lane] = -nl[1];
+                lb[lane] = nl[0] * -kLog2e;  // -LSE in log2 units: the exponent's FFMA adds it
+                lb[32 + lane] = nl[1] * -kLog2e;
                 db[lane] = nd[0];
                 db[32 + lane] = nd[1];
                 __syncwarp();
