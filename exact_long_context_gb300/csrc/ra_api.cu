@@ -1182,8 +1182,22 @@ ra_status ra_ring_sim_fwd_host(const ra_tensor *q, const ra_tensor *k, const ra_
     cudaError_t e = cudaEventRecord(hp->ev[2 * kHostGroups], st);  // prior work on the caller's stream
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->cin, hp->ev[2 * kHostGroups], 0);
     const size_t qrow = (size_t)(N * D) * es;  // bytes of one head's rows
+    // Group boundaries in KV heads.  Copy-bound with heads to spare (Hkv >= 3 ng): sizes
+    // falling linearly to one head, so that what nothing overlaps at the end - the last
+    // groups' kernels and copies out, after the last copy in - is small; else equal groups.
+    int64_t kb[kHostGroups + 1];
+    const bool falling = copy_bound && ng >= 4 && Hkv >= 3 * (int64_t)ng;
+    const int64_t wsum = (int64_t)ng * (ng + 1) / 2;
+    kb[0] = 0;
+    for (int g = 1; g <= ng; ++g) {
+        const int64_t w = (int64_t)g * ng - (int64_t)g * (g - 1) / 2;  // weights ng, ng-1, ... of groups < g
+        int64_t b = falling ? (Hkv * w + wsum / 2) / wsum : Hkv * g / ng;
+        b = std::max<int64_t>(b, kb[g - 1] + 1);
+        b = std::min<int64_t>(b, Hkv - (ng - g));
+        kb[g] = b;
+    }
     for (int g = 0; g < ng && e == cudaSuccess; ++g) {
-        const int64_t k0 = Hkv * g / ng, k1 = Hkv * (g + 1) / ng, q0 = k0 * G, q1 = k1 * G;
+        const int64_t k0 = kb[g], k1 = kb[g + 1], q0 = k0 * G, q1 = k1 * G;
         // in: q, k, v rows of the group, every batch (one 2-D copy each)
         e = cudaMemcpy2DAsync(dq + q0 * qrow, (size_t)Hq * qrow, static_cast<const char *>(q->data) + q0 * qrow,
                               (size_t)Hq * qrow, (size_t)(q1 - q0) * qrow, (size_t)B, cudaMemcpyHostToDevice, hp->cin);
