@@ -17,7 +17,7 @@
 //                 dV += P^T dO,  dK += dS^T Q       (A from tensor memory)
 //
 // Warp roles: warp 0 TMA producer, warp 1 MMA issuer and tensor-memory owner (the dQ
-// kernel: S and dP; warp 2 issues its dQ products), warps 4-11 the element-wise work and
+// kernel: S and dQ; warp 2 issues its dP products), warps 4-11 the element-wise work and
 // the epilogue: two warps per tensor-memory lane quarter, each owning 64 of a tile's 128
 // columns (one warp per scheduler left the exponentials and the tensor-memory round trips
 // exposed).  Every S / dP product is a full 128 x 128 tile (narrower products run the
@@ -27,8 +27,8 @@
 // next tile's S^T and dP^T overlap the element-wise work.  The bf16 P / dS overwrite the
 // columns of the fp32 S / dP they came from once those are in registers; an issuer puts a
 // product that overwrites a slot after the products that read it (tcgen05 MMAs of a
-// thread run in order), or, across the dQ kernel's two issuers, waits for their
-// completion.  Every wait is bounded like the forward kernel's.
+// thread run in order), or, for a slot the other issuer reads, waits for the element-wise
+// warps to be past that read.  Every wait is bounded like the forward kernel's.
 //
 // A launch covers the segments of one ring step (struct BSeg): the whole-sequence
 // backward is one segment.  On a ring, the gradient of a range that earlier or later
