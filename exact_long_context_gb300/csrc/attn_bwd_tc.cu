@@ -17,7 +17,7 @@
 //                 dV += P^T dO,  dK += dS^T Q       (A from tensor memory)
 //
 // Warp roles: warp 0 TMA producer, warp 1 MMA issuer and tensor-memory owner (the dQ
-// kernel: S and dQ; warp 2 issues its dP products), warps 4-11 the element-wise work and
+// kernel: S and dP; warp 2 issues its dQ products), warps 4-11 the element-wise work and
 // the epilogue: two warps per tensor-memory lane quarter, each owning 64 of a tile's 128
 // columns (one warp per scheduler left the exponentials and the tensor-memory round trips
 // exposed).  Every S / dP product is a full 128 x 128 tile (narrower products run the
@@ -27,8 +27,8 @@
 // next tile's S^T and dP^T overlap the element-wise work.  The bf16 P / dS overwrite the
 // columns of the fp32 S / dP they came from once those are in registers; an issuer puts a
 // product that overwrites a slot after the products that read it (tcgen05 MMAs of a
-// thread run in order), or, for a slot the other issuer reads, waits for the element-wise
-// warps to be past that read.  Every wait is bounded like the forward kernel's.
+// thread run in order), or, across the dQ kernel's two issuers, waits for their
+// completion.  Every wait is bounded like the forward kernel's.
 //
 // A launch covers the segments of one ring step (struct BSeg): the whole-sequence
 // backward is one segment.  On a ring, the gradient of a range that earlier or later
@@ -91,8 +91,7 @@ struct BBars {
     uint64_t full[4], empty[4];    // streamed pairs (dK/dV kernel) or K tiles (dQ kernel)
     uint64_t fullv[4], emptyv[4];  // V tiles (dQ kernel)
     uint64_t s_full[2], o_full, drain;
-    uint64_t d_full[2], drain2;    // dQ kernel: dP of tiles of each parity; the dP issuer's drain
-    uint32_t s_issued, pad_;       // dQ kernel: S products issued (S / dQ issuer -> dP issuer)
+    uint64_t dq_done[2], drain2, pad_;  // dQ kernel: the dQ issuer's products (alternating), its drain
     uint32_t tmem_base;
     int32_t abort;
     uint32_t p_count[2];
@@ -469,14 +468,11 @@ struct KWalk {
 
 // ---------------------------------------------------------------- shared pieces
 
-// fix_releases: arrivals that free the fixed pair (the dQ kernel's two issuers each
-// release the tile their products read)
-__device__ __forceinline__ void bwd_init(BBars *bars, int nst, uint32_t readers, uint32_t fix_releases) {
+__device__ __forceinline__ void bwd_init(BBars *bars, int nst, uint32_t readers) {
     bars->abort = 0;
     bars->p_count[0] = bars->p_count[1] = 0;
-    bars->s_issued = 0;
     mbar_init(smem_u32(&bars->fix_full), 1);
-    mbar_init(smem_u32(&bars->fix_empty), fix_releases);
+    mbar_init(smem_u32(&bars->fix_empty), 1);
     for (int s = 0; s < nst; ++s) {
         mbar_init(smem_u32(&bars->full[s]), 1);
         mbar_init(smem_u32(&bars->empty[s]), 1);
@@ -487,8 +483,8 @@ __device__ __forceinline__ void bwd_init(BBars *bars, int nst, uint32_t readers,
     mbar_init(smem_u32(&bars->s_full[1]), 1);
     mbar_init(smem_u32(&bars->o_full), 1);
     mbar_init(smem_u32(&bars->drain), 1);
-    mbar_init(smem_u32(&bars->d_full[0]), 1);
-    mbar_init(smem_u32(&bars->d_full[1]), 1);
+    mbar_init(smem_u32(&bars->dq_done[0]), 1);
+    mbar_init(smem_u32(&bars->dq_done[1]), 1);
     mbar_init(smem_u32(&bars->drain2), 1);
     for (int i = 0; i < kItemRing; ++i) {
         mbar_init(smem_u32(&bars->it_full[i]), 1);
@@ -784,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tps = (P.flen + kT - 1) / kT;
     const float sl2 = P.scale_log2;
 
-    if (threadIdx.x == 0) bwd_init(bars, 4, kItemReadersDq, 2);
+    if (threadIdx.x == 0) bwd_init(bars, 4, kItemReadersDq);
     if (warp == 1) tmem_alloc(smem_u32(&bars->tmem_base), C::TM_COLS);
     tc_fence_before();
     __syncthreads();
@@ -848,30 +844,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // S / dQ issuer: S(g), then dQ(g - 1) += dS K once the element-wise warps have
-            // stored that tile's dS.  Tile g's S reuses the slot of tile g - 2's dS, which
-            // dQ(g - 2) - issued before it by this thread, so run before it - has read.
-            // A thread that issues tcgen05 MMAs stalls on each until the tensor pipe takes
-            // it, so the pipe runs dry while its one issuer waits; the dP products, which
-            // only wait for the element-wise warps to have read the previous S, go on a
-            // thread of their own (warp 2).  Tile g's K sits in slot g mod KST of the K ring.
-            Ring kr = {0, 0u, 0u, 0u};
+            // S / dP issuer.  Tile g's S goes to the slot that held dS of tile g - 2, so it
+            // waits for that tile's dQ product (the other issuer's) to complete; its dP goes
+            // to the slot of tile g - 1's S once the element-wise warps have read that.
+            Ring kr = {0, 0u, 0u, 0u}, vr = {0, 0u, 0u, 0u};
             uint32_t fcnt = 0, g = 0;
             bool ok = true;
-            bool pend = false, pend_acc = false, pend_last = false;  // the previous tile's dQ
-            uint32_t pend_g = 0;
-            int pend_slot = 0;
-            auto flush = [&]() -> bool {
-                if (!wait_count(&bars->p_count[1], (uint32_t)kEwWarps * (pend_g + 1u), abort_flag, limit, err))
-                    return false;
-                tc_fence_after();
-                issue_tn<HD>(tmem + C::TM_DQ, tmem + d_slot(pend_g) + 32, sK + pend_slot * C::TILE_BYTES,
-                             pend_acc);  // dQ += dS K
-                mma_commit(smem_u32(&bars->empty[pend_slot]));  // the K tile is free
-                if (pend_last) mma_commit(smem_u32(&bars->o_full));
-                pend = false;
-                return true;
-            };
             uint32_t rcnt = 0;
             while (ok) {
                 Rec<QItem> rec;
@@ -883,62 +861,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = wait_phase(smem_u32(&bars->fix_full), fcnt & 1u, abort_flag, limit, err);
                 ++fcnt;
                 for (int t = 0; ok && t < n; ++t, ++g) {
+                    // dq_done[g & 1] completes once per tile of that parity: tile g - 2's is
+                    // its completion number (g - 2) / 2
+                    if (g >= 2) {
+                        ok = wait_phase(smem_u32(&bars->dq_done[g & 1u]), ((g - 2u) >> 1) & 1u, abort_flag, limit, err);
+                        if (!ok) break;
+                    }
                     ok = wait_phase(smem_u32(&bars->full[kr.slot]), kr.ph, abort_flag, limit, err);
                     if (!ok) break;
                     tc_fence_after();
                     issue_nt<HD>(tmem + s_slot(g), sQ, sK + kr.slot * C::TILE_BYTES);  // S = Q K^T
-                    // s_full[g & 1] completes once per tile of that parity: the next completion,
-                    // S(g + 2), follows dQ(g), which waits for the element-wise warps to finish
-                    // tile g, so their wait for this one cannot miss it
-                    mma_commit(smem_u32(&bars->s_full[g & 1u]));
-                    count_release_add(&bars->s_issued);  // the dP issuer queues dP(g) after it
-                    if (t == n - 1) mma_commit(smem_u32(&bars->fix_empty));  // Q is free
-                    if (pend && !(ok = flush())) break;
-                    pend = true;
-                    pend_acc = t > 0;
-                    pend_last = t == n - 1;
-                    pend_slot = kr.slot;
-                    pend_g = g;
-                    kr.advance<C::KST>();
+                    if (g > 0) {  // this tile's dP goes where the previous tile's S was read from
+                        ok = wait_count(&bars->p_count[0], (uint32_t)kEwWarps * g, abort_flag, limit, err);
+                        if (!ok) break;
+                    }
+                    ok = wait_phase(smem_u32(&bars->fullv[vr.slot]), vr.ph, abort_flag, limit, err);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_nt<HD>(tmem + d_slot(g), sDo, sV + vr.slot * C::TILE_BYTES);  // dP = dO V^T
+                    mma_commit(smem_u32(&bars->s_full[0]));
+                    mma_commit(smem_u32(&bars->emptyv[vr.slot]));  // the V tile is free
+                    vr.advance<C::VST>();
+                    if (t == n - 1) mma_commit(smem_u32(&bars->fix_empty));
+                    kr.advance<C::KST>();  // (the dQ issuer frees the K tile)
                 }
             }
-            if (ok && pend) ok = flush();
             mma_commit(smem_u32(&bars->drain));
             wait_phase_drain(smem_u32(&bars->drain), 0);
         }
     } else if (warp == 2) {
         if (lane == 0) {
-            // dP issuer: dP(g) = dO V^T into the slot of tile g - 1's S once the element-wise
-            // warps have read that S, and after S(g) is queued (so that dP(g), needed later,
-            // does not go ahead of it).
-            Ring vr = {0, 0u, 0u, 0u};
-            uint32_t fcnt = 0, g = 0, rcnt = 0;
+            // dQ issuer: dQ += dS K for each tile once the element-wise warps have stored its
+            // dS.  A thread that issues tcgen05 MMAs stalls on each until the tensor pipe
+            // takes it, and the pipe runs dry while that thread waits on anything; with the
+            // dQ products on their own thread, the waits of each issuer are covered by the
+            // other's products.  Tile g's K tile sits in slot g mod KST of the K ring.
+            uint32_t g = 0, rcnt = 0;
             bool ok = true;
             while (ok) {
                 Rec<QItem> rec;
                 if (!(ok = ring_get(bars, rcnt, rec, false, abort_flag, limit, err))) break;
                 if (rec.end) break;
                 const int n = rec.it.n;
-                if (n == 0) continue;
-                ok = wait_phase(smem_u32(&bars->fix_full), fcnt & 1u, abort_flag, limit, err);
-                ++fcnt;
                 for (int t = 0; ok && t < n; ++t, ++g) {
-                    if (g > 0) {
-                        ok = wait_count(&bars->p_count[0], (uint32_t)kEwWarps * g, abort_flag, limit, err);
-                        if (!ok) break;
-                    }
-                    ok = wait_count(&bars->s_issued, g + 1u, abort_flag, limit, err);
-                    if (!ok) break;
-                    ok = wait_phase(smem_u32(&bars->fullv[vr.slot]), vr.ph, abort_flag, limit, err);
+                    ok = wait_count(&bars->p_count[1], (uint32_t)kEwWarps * (g + 1u), abort_flag, limit, err);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_nt<HD>(tmem + d_slot(g), sDo, sV + vr.slot * C::TILE_BYTES);  // dP = dO V^T
-                    // d_full[g & 1]: the next completion, dP(g + 2), waits for the warps to have
-                    // read S(g + 1), after they finished tile g
-                    mma_commit(smem_u32(&bars->d_full[g & 1u]));
-                    mma_commit(smem_u32(&bars->emptyv[vr.slot]));  // the V tile is free
-                    vr.advance<C::VST>();
-                    if (t == n - 1) mma_commit(smem_u32(&bars->fix_empty));  // dO is free
+                    const uint32_t ks = g % (uint32_t)C::KST;
+                    issue_tn<HD>(tmem + C::TM_DQ, tmem + d_slot(g) + 32, sK + ks * C::TILE_BYTES,
+                                 t > 0);  // dQ += dS K
+                    mma_commit(smem_u32(&bars->dq_done[g & 1u]));
+                    mma_commit(smem_u32(&bars->empty[ks]));  // the K tile is free
+                    if (t == n - 1) mma_commit(smem_u32(&bars->o_full));
                 }
             }
             mma_commit(smem_u32(&bars->drain2));
@@ -978,7 +952,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int srank_t, diag;  // (the keys' rank: the producer's concern here)
                 walk.next<FUSED>(P, S, it, kt0, klim, srank_t, diag);
                 (void)srank_t;
-                ok = wait_phase(smem_u32(&bars->s_full[g & 1u]), (g >> 1) & 1u, abort_flag, limit, err);  // S(g)
+                ok = wait_phase(smem_u32(&bars->s_full[0]), g & 1u, abort_flag, limit, err);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t tS = tmem + s_slot(g) + lane_off, tD = tmem + d_slot(g) + lane_off;
@@ -1006,9 +980,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sv[e] = __float_as_uint(ex2(x0));
                     sv[e + 1] = __float_as_uint(ex2(x1));
                 }
-                ok = wait_phase(smem_u32(&bars->d_full[g & 1u]), (g >> 1) & 1u, abort_flag, limit, err);  // dP(g)
-                if (!ok) break;
-                tc_fence_after();
                 if (grp == 0)
                     dq_tile_ew<1>(sv, tD, 0, d_r);
                 else
@@ -1114,7 +1085,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tps = (P.flen + kT - 1) / kT;
     const float sl2 = P.scale_log2;
 
-    if (threadIdx.x == 0) bwd_init(bars, C::NST, kItemReaders, 1);
+    if (threadIdx.x == 0) bwd_init(bars, C::NST, kItemReaders);
     if (warp == 1) tmem_alloc(smem_u32(&bars->tmem_base), C::TM_COLS);
     tc_fence_before();
     __syncthreads();

@@ -155,3 +155,34 @@ def test_ring_backward_full_size_sampled(ra, name):
     rhs = dout.double().view(B, Hkv, G, N, D).sum(dim=(2, 3))
     bound = 2.0 ** -8 * (dv.double().abs().sum(dim=2) + dout.double().abs().view(B, Hkv, G, N, D).sum(dim=(2, 3)))
     assert torch.all((lhs - rhs).abs() <= bound)
+
+
+REPEAT_CASES = [
+    # B, Hq, Hkv, N, D, R, layout: fused rings whose kernels hand tensor-memory slots between
+    # several threads; a race there shows as a run that differs from the others
+    (1, 2, 2, 1024, 64, 4, "striped"),
+    (1, 2, 2, 1024, 128, 4, "striped"),
+    (1, 4, 2, 2048, 64, 4, "zigzag"),
+    (1, 2, 2, 1024, 64, 1, "contig"),
+]
+
+
+@pytest.mark.parametrize("case", REPEAT_CASES, ids=lambda c: f"N{c[3]}D{c[4]}R{c[5]}{c[6]}")
+def test_ring_backward_is_repeatable(ra, case):
+    """The same causal backward 60 times: every run finite and bit-identical to the first
+    (each output element has one writer and a fixed order of additions, so any difference
+    is a race)."""
+    B, Hq, Hkv, N, D, R, layout = case
+    q, k, v, dout = _inputs(B, Hq, Hkv, N, D, torch.bfloat16, seed=N * 3 + R)
+    o, lse = ra.ring_sim_fwd(q, k, v, R, layout, True)
+    first = None
+    for i in range(60):
+        grads = ra.ring_sim_bwd(q, k, v, o, lse, dout, R, layout, True)
+        ra.check()
+        for name, t in zip(("dq", "dk", "dv"), grads):
+            assert torch.isfinite(t.float()).all().item(), f"run {i}: non-finite {name}"
+        if first is None:
+            first = [t.clone() for t in grads]
+        else:
+            for name, a, b in zip(("dq", "dk", "dv"), first, grads):
+                assert torch.equal(a, b), f"run {i}: {name} differs from the first run"
