@@ -199,6 +199,33 @@ def test_ring_sim_small(ra, case):
     print(case, "errors", err)
 
 
+FWD_REPEAT_CASES = [
+    # B, Hq, Hkv, N, D, R, layout, causal: the single pass and fused rings, both head sizes
+    (1, 4, 2, 2048, 128, 1, "contig", True),
+    (1, 4, 2, 2048, 64, 4, "zigzag", True),
+    (1, 2, 2, 1024, 128, 4, "striped", True),
+    (1, 2, 2, 1024, 64, 4, "striped", True),
+    (2, 6, 2, 1024, 128, 4, "zigzag", False),
+]
+
+
+@pytest.mark.parametrize("case", FWD_REPEAT_CASES, ids=lambda c: f"{c[6]}R{c[5]}N{c[3]}D{c[4]}{'c' if c[7] else 'n'}")
+def test_forward_is_repeatable(ra, case):
+    """The same forward 60 times: every run bit-identical to the first (the producer, the
+    MMA thread and the softmax warps hand tensor-memory and shared-memory buffers to one
+    another; each output row is written once from a fixed order of additions, so any
+    difference is a race)."""
+    B, Hq, Hkv, N, D, R, layout, causal = case
+    q, k, v = synth.make_qkv(B, Hq, Hkv, N, D, torch.bfloat16, seed=R * 10 + N, device="cuda")
+    o0, l0 = ra.ring_sim_fwd(q, k, v, R, layout, causal=causal)
+    ra.check()
+    assert torch.isfinite(o0.float()).all().item()
+    for i in range(59):
+        o, lse = ra.ring_sim_fwd(q, k, v, R, layout, causal=causal)
+        ra.check()
+        assert torch.equal(o, o0) and torch.equal(lse, l0), f"run {i + 1} differs from the first"
+
+
 def test_ring_invariants_gpu(ra):
     """R = 1 vs R = 4 contig / zigzag / striped on the GPU: same result within rounding."""
     q, k, v = synth.make_qkv(1, 4, 2, 4096, 128, torch.bfloat16, seed=9, device="cuda")
