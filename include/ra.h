@@ -216,8 +216,9 @@ ra_status ra_attn_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v
  * asynchronously; pageable memory works but each copy then waits).  The tensors must be
  * contiguous [B, H, N, D]; lse is [B, Hq, N] float32.  The call stages through the
  * caller's device workspace and pipelines by groups of whole KV heads (up to 8; fewer
- * when the kernels dominate and a group's launch would not fill the GPU), one launch per
- * group over every batch: the next
+ * when the kernels dominate and a group's launch would not fill the GPU; when the copies
+ * dominate and there are at least three KV heads per group, group sizes fall to one head
+ * at the end), one launch per group over every batch: the next
  * group's q/k/v go in on one internal stream while the current group computes on
  * `stream`, and finished groups' o/lse come out on another, so both directions of the
  * host link overlap the kernels.  The call is ordered on `stream`: the host buffers may
