@@ -253,6 +253,15 @@ __device__ __forceinline__ bool part_t(const I &it, int hh, int t) {
     else
         return it.part(hh, t);
 }
+// The same with tile t's position in its step given (MODE 2; the callers count it, since a
+// division per test would sit between the MMA thread's products).
+template <int MODE, class I>
+__device__ __forceinline__ bool part_pos(const I &it, int hh, int t, int pos) {
+    if constexpr (MODE == 2)
+        return hh ? it.nh[1] > 0 : (it.nh[0] > 0 && !(it.skip0 == -2 && pos == 0));
+    else
+        return it.part(hh, t);
+}
 template <int MODE, class I>
 __device__ __forceinline__ int last_t(const I &it, int hh) {
     if constexpr (MODE == 2)
@@ -747,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    if (part_t<MODE>(it, hh, 0)) {
+                    if (part_pos<MODE>(it, hh, 0, 0)) {
                         issue_qk(hh, sKV + (2 * slot + 1) * C::TILE_BYTES);
                         if (hh != kLastHalf) mma_commit(smem_u32(&bars->s_full[hh]));
                         if (last_t<MODE>(it, hh) == 0) mma_commit(smem_u32(&bars->q_empty[hh]));
@@ -762,7 +771,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // issues the next Q K^T of a tile it takes part in even when it sat this
                 // tile out: its last P was read by the P V issued before)
                 bool started[2] = {false, false};
+                int upos = 0;  // MODE 2: tile t's position in its step
                 for (int t = 0; ok && t < it.nmax; ++t) {
+                    const int unext = (upos + 1 == it.tps) ? 0 : upos + 1;
                     ok = wait_phase(smem_u32(&bars->full[slot]), ph, abort_flag, P.wait_limit_ns,
                                     P.err);
                     if (!ok) break;
@@ -774,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // outside the fused ring half 1 starts first (half 0 sits out the
                         // item's first tile), and it is served first in every tile
                         const int hh = MODE == 1 ? h2 : 1 - h2;
-                        if (part_t<MODE>(it, hh, t)) {
+                        if (part_pos<MODE>(it, hh, t, upos)) {
                             ++pcnt[hh];
                             ok = wait_count(&bars->p_count[hh], 4u * pcnt[hh], abort_flag,
                                             P.wait_limit_ns, P.err);
@@ -784,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             started[hh] = true;
                             if (t == last_t<MODE>(it, hh)) mma_commit(smem_u32(&bars->o_full[hh]));
                         }
-                        if (t + 1 < it.nmax && part_t<MODE>(it, hh, t + 1)) {
+                        if (t + 1 < it.nmax && part_pos<MODE>(it, hh, t + 1, unext)) {
                             issue_qk(hh, kb);
                             if (hh != kLastHalf) mma_commit(smem_u32(&bars->s_full[hh]));
                             if (t + 1 == last_t<MODE>(it, hh)) mma_commit(smem_u32(&bars->q_empty[hh]));
@@ -796,6 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         slot = 0;
                         ph ^= 1u;
                     }
+                    upos = unext;
                 }
                 if (!ok) break;
             }
@@ -856,7 +868,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool first_tile = true;
             for (int t = 0; t < it.nmax; ++t) {
                 int ks, ke, dg = it.diag;  // the tile's keys and diagonal offset
+                int upos = 0;              // (striped) the tile's position in its step
                 if constexpr (STRIPED) {
+                    upos = sw.u;
                     ks = sw.start(it.tps);
                     ke = sw.end;
                     dg = sw.d;
@@ -869,7 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ks = it.kt.start(it.tile(t));
                     ke = it.kt.range_end(it.tile(t));
                 }
-                if (!part_t<MODE>(it, hh, t)) continue;
+                if (!part_pos<MODE>(it, hh, t, upos)) continue;
                 if (hh == kLastHalf) {
                     const uint32_t gs = sbase + (uint32_t)t;
                     ok = wait_phase(smem_u32(&bars->empty[gs % C::NSTAGE]), (gs / C::NSTAGE) & 1u, abort_flag,
