@@ -417,9 +417,13 @@ __device__ __forceinline__ void kv_tile0(const KItem &it, int tt, int &q0, int &
 // Sequential walks over an item's streamed tiles (the producer and the element-wise warps
 // take them in order): the first step's from the item's ranges, a fused ring's later
 // steps from a cursor.
+// (The walks avoid runtime divisions per tile where they can: the element-wise warps take a
+// tile's walk on their path between tiles, and a division there costs more than the rest of
+// the step.)
 struct QWalk {
     BCursor c;
     int t = 0;
+    int cs = -1, csr = 0, cdg = 0;  // striped: the step whose rank and offset are cached
     // k0, klim: the key tile's first index and its range's end; srank, dg: the rank holding
     // those keys and the tile's diagonal offset (key k visible to row i iff k + dg <= i)
     template <bool FUSED>
@@ -434,7 +438,14 @@ struct QWalk {
             if (t == it.n1) bcur_begin(P, 0, S.rank, f0, f1, 0, c);
             k0 = c.start();
             klim = c.end();
-            if (P.ring_layout == 2) striped_step(P, 0, S.rank, c.s, srank, dg);
+            if (P.ring_layout == 2) {
+                if (c.s != cs) {
+                    striped_step(P, 0, S.rank, c.s, csr, cdg);
+                    cs = c.s;
+                }
+                srank = csr;
+                dg = cdg;
+            }
             bcur_next(P, 0, S.rank, f0, f1, 0, c);
         }
         ++t;
@@ -448,7 +459,9 @@ struct KWalk {
     template <bool FUSED>
     __device__ __forceinline__ void next(const BwdParams &P, const BSeg &S, const KItem &it, int &q0, int &qlim,
                                          int &g, int &srank, int &dg) {
-        g = t / it.per;
+        // tile t's query head in the group and its index in that head's walk (one head per
+        // KV head: no division)
+        g = P.Hq == P.Hkv ? 0 : t / it.per;
         const int tt = t - g * it.per;
         srank = S.s_rank;
         dg = S.diag;
