@@ -245,16 +245,10 @@ __device__ __forceinline__ void stripe_next(const StepParams &P, const Item &it,
     striped_range(P, it.rank, min(it.qrow0 + 2 * BM, it.q1), w.s, w.end, w.j, w.d);
 }
 
-// Whether half hh takes part in tile t, and its last tile (MODE 2: the fused striped ring).
-template <int MODE, class I>
-__device__ __forceinline__ bool part_t(const I &it, int hh, int t) {
-    if constexpr (MODE == 2)
-        return hh ? it.nh[1] > 0 : (it.nh[0] > 0 && !(it.skip0 == -2 && t % it.tps == 0));
-    else
-        return it.part(hh, t);
-}
-// The same with tile t's position in its step given (MODE 2; the callers count it, since a
-// division per test would sit between the MMA thread's products).
+// Whether half hh takes part in tile t, given the tile's position in its step (MODE 2, the
+// fused striped ring: half 0 sits out each step's first tile; the callers count the
+// position, since a division per test would sit between the MMA thread's products), and
+// its last tile.
 template <int MODE, class I>
 __device__ __forceinline__ bool part_pos(const I &it, int hh, int t, int pos) {
     if constexpr (MODE == 2)
