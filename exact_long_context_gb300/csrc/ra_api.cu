@@ -1083,6 +1083,30 @@ ra_status ra_attn_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v
 
 // Streams and events of the host-buffer pipeline, created once per device (copies in on
 // one stream, copies out on another, so both directions of the link run at once).
+// Boundaries (in KV heads) of the host-buffer call's ng head groups: kb[0] = 0 < kb[1] < ...
+// < kb[ng] = hkv.  Copy-bound with heads to spare (hkv >= 3 ng, ng >= 4): sizes falling in
+// proportion to ng, ng - 1, ..., 1 (to one head for 32 heads in 8 groups), so that what
+// nothing overlaps at the end - the last groups' kernels and copies out, after the last copy
+// in - is small; else equal groups.
+static void host_group_bounds(int64_t hkv, int ng, bool copy_bound, int64_t *kb) {
+    const bool falling = copy_bound && ng >= 4 && hkv >= 3 * (int64_t)ng;
+    const int64_t wsum = (int64_t)ng * (ng + 1) / 2;
+    kb[0] = 0;
+    for (int g = 1; g <= ng; ++g) {
+        const int64_t w = (int64_t)g * ng - (int64_t)g * (g - 1) / 2;  // weights ng, ng-1, ... of groups < g
+        int64_t b = falling ? (hkv * w + wsum / 2) / wsum : hkv * g / ng;
+        b = std::max<int64_t>(b, kb[g - 1] + 1);
+        b = std::min<int64_t>(b, hkv - (ng - g));
+        kb[g] = b;
+    }
+}
+
+extern "C" int ra_debug_host_group_bounds(int64_t hkv, int ng, int copy_bound, int64_t *out) {
+    if (hkv < 1 || ng < 1 || ng > kHostGroups || ng > hkv || !out) return -1;
+    host_group_bounds(hkv, ng, copy_bound != 0, out);
+    return ng;
+}
+
 struct HostPipe {
     cudaStream_t cin = nullptr, cout = nullptr;
     cudaEvent_t ev[2 * kHostGroups + 2] = {};
@@ -1182,20 +1206,8 @@ ra_status ra_ring_sim_fwd_host(const ra_tensor *q, const ra_tensor *k, const ra_
     cudaError_t e = cudaEventRecord(hp->ev[2 * kHostGroups], st);  // prior work on the caller's stream
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->cin, hp->ev[2 * kHostGroups], 0);
     const size_t qrow = (size_t)(N * D) * es;  // bytes of one head's rows
-    // Group boundaries in KV heads.  Copy-bound with heads to spare (Hkv >= 3 ng): sizes
-    // falling linearly to one head, so that what nothing overlaps at the end - the last
-    // groups' kernels and copies out, after the last copy in - is small; else equal groups.
     int64_t kb[kHostGroups + 1];
-    const bool falling = copy_bound && ng >= 4 && Hkv >= 3 * (int64_t)ng;
-    const int64_t wsum = (int64_t)ng * (ng + 1) / 2;
-    kb[0] = 0;
-    for (int g = 1; g <= ng; ++g) {
-        const int64_t w = (int64_t)g * ng - (int64_t)g * (g - 1) / 2;  // weights ng, ng-1, ... of groups < g
-        int64_t b = falling ? (Hkv * w + wsum / 2) / wsum : Hkv * g / ng;
-        b = std::max<int64_t>(b, kb[g - 1] + 1);
-        b = std::min<int64_t>(b, Hkv - (ng - g));
-        kb[g] = b;
-    }
+    host_group_bounds(Hkv, ng, copy_bound, kb);
     for (int g = 0; g < ng && e == cudaSuccess; ++g) {
         const int64_t k0 = kb[g], k1 = kb[g + 1], q0 = k0 * G, q1 = k1 * G;
         // in: q, k, v rows of the group, every batch (one 2-D copy each)

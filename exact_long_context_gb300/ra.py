@@ -91,6 +91,8 @@ def lib() -> ctypes.CDLL:
             L.ra_debug_bounds_selftest.restype = c_int
             L.ra_debug_work_counters_in_use.argtypes = [P]
             L.ra_debug_work_counters_in_use.restype = c_int
+            L.ra_debug_host_group_bounds.argtypes = [ctypes.c_int64, c_int, c_int, P]
+            L.ra_debug_host_group_bounds.restype = c_int
             L.ra_last_error.restype = ctypes.c_char_p
             L.ra_launch_count.argtypes = [c_int]
             L.ra_launch_count.restype = i64
@@ -409,3 +411,12 @@ def launch_count(reset=False) -> int:
 
 def version() -> int:
     return int(lib().ra_version())
+
+
+def host_group_bounds(hkv: int, ng: int, copy_bound: bool) -> list[int]:
+    """Boundaries (in KV heads) of the host-buffer call's head groups (diagnostic)."""
+    out = (ctypes.c_int64 * (ng + 1))()
+    n = lib().ra_debug_host_group_bounds(int(hkv), int(ng), 1 if copy_bound else 0, ctypes.cast(out, ctypes.c_void_p))
+    if n < 0:
+        raise ValueError("host_group_bounds: arguments out of range")
+    return [int(x) for x in out]

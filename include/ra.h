@@ -217,8 +217,8 @@ ra_status ra_attn_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v
  * contiguous [B, H, N, D]; lse is [B, Hq, N] float32.  The call stages through the
  * caller's device workspace and pipelines by groups of whole KV heads (up to 8; fewer
  * when the kernels dominate and a group's launch would not fill the GPU; when the copies
- * dominate and there are at least three KV heads per group, group sizes fall to one head
- * at the end), one launch per group over every batch: the next
+ * dominate and there are at least three KV heads per group, group sizes fall along the
+ * pipeline), one launch per group over every batch: the next
  * group's q/k/v go in on one internal stream while the current group computes on
  * `stream`, and finished groups' o/lse come out on another, so both directions of the
  * host link overlap the kernels.  The call is ordered on `stream`: the host buffers may
@@ -403,6 +403,16 @@ int ra_debug_launch_times(float *ms, int cap, char *names, int name_len);
  * flight on the device this is 0.  -1 if the device or the copy fails.  Diagnostic hook.
  */
 int ra_debug_work_counters_in_use(void *stream);
+
+/*
+ * ra_debug_host_group_bounds - the head groups ra_ring_sim_fwd_host would use for `hkv` KV
+ * heads in `ng` groups (1 <= ng <= min(8, hkv)): writes ng + 1 boundaries (in KV heads,
+ * 0 = out[0] < out[1] < ... < out[ng] = hkv) to `out` and returns ng, or -1 for arguments
+ * out of range.  copy_bound != 0: the schedule used when the copies dominate (once
+ * hkv >= 3 ng and ng >= 4, sizes in proportion to ng, ng - 1, ..., 1).  Host only;
+ * diagnostic hook.
+ */
+int ra_debug_host_group_bounds(int64_t hkv, int ng, int copy_bound, int64_t *out);
 
 /*
  * Debug builds.  Built with RA_DEBUG_BOUNDS defined (libra_debug.so, build.py

@@ -317,3 +317,29 @@ def test_backward_plan_covers_every_visible_pair_once(ra, layout, causal, R):
             for g in ra.ring_sim_bwd_plan(N, R, layout, causal, s, kind):
                 rid = ({rank_of[p] for p in positions(g["f0"], g["f1"], g["f_rank"])}.pop(), g["f0"])
                 assert bool(g["flags"] & 2) == (last[rid] == s)
+
+
+def test_host_call_head_groups(ra):
+    """The host-buffer call's head groups: every KV head in exactly one non-empty group, in
+    order; equal sizes (within one head) unless the call is copy-bound with at least three
+    heads per group, where sizes fall in proportion to ng, ng - 1, ..., 1 and the last group
+    is the smallest (the dense workload's 32 heads in 8 groups: 7, 6, 6, 4, 4, 2, 2, 1)."""
+    assert ra.host_group_bounds(32, 8, True) == [0, 7, 13, 19, 23, 27, 29, 31, 32]
+    for hkv in range(1, 130):
+        for ng in range(1, min(8, hkv) + 1):
+            for copy_bound in (False, True):
+                kb = ra.host_group_bounds(hkv, ng, copy_bound)
+                assert kb[0] == 0 and kb[-1] == hkv and len(kb) == ng + 1
+                sizes = [b - a for a, b in zip(kb, kb[1:])]
+                assert min(sizes) >= 1, (hkv, ng, copy_bound, sizes)
+                if copy_bound and ng >= 4 and hkv >= 3 * ng:
+                    assert sizes[-1] == min(sizes) and sizes[0] == max(sizes), (hkv, ng, sizes)
+                    assert all(a + 1 >= b for a, b in zip(sizes, sizes[1:])), (hkv, ng, sizes)
+                    share = [hkv * (ng - g) / (ng * (ng + 1) / 2) for g in range(ng)]
+                    assert all(abs(z - w) <= 1.0 for z, w in zip(sizes, share)), (hkv, ng, sizes)
+                else:
+                    assert max(sizes) - min(sizes) <= 1, (hkv, ng, copy_bound, sizes)
+    with pytest.raises(ValueError):
+        ra.host_group_bounds(4, 5, True)  # more groups than heads
+    with pytest.raises(ValueError):
+        ra.host_group_bounds(64, 9, True)  # more than the call's 8 groups
