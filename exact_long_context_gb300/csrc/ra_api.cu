@@ -1081,8 +1081,6 @@ ra_status ra_attn_bwd(const ra_tensor *q, const ra_tensor *k, const ra_tensor *v
 
 // ---------------------------------------------------------------- host-buffer entry point
 
-// Streams and events of the host-buffer pipeline, created once per device (copies in on
-// one stream, copies out on another, so both directions of the link run at once).
 // Boundaries (in KV heads) of the host-buffer call's ng head groups: kb[0] = 0 < kb[1] < ...
 // < kb[ng] = hkv.  Copy-bound with heads to spare (hkv >= 3 ng, ng >= 4): sizes falling in
 // proportion to ng, ng - 1, ..., 1 (to one head for 32 heads in 8 groups), so that what
@@ -1107,6 +1105,8 @@ extern "C" int ra_debug_host_group_bounds(int64_t hkv, int ng, int copy_bound, i
     return ng;
 }
 
+// Streams and events of the host-buffer pipeline, created once per device (copies in on
+// one stream, copies out on another, so both directions of the link run at once).
 struct HostPipe {
     cudaStream_t cin = nullptr, cout = nullptr;
     cudaEvent_t ev[2 * kHostGroups + 2] = {};

@@ -94,14 +94,6 @@ __device__ __forceinline__ bool wait_count(const uint32_t *ctr, uint32_t target,
     }
 }
 
-// Read the shared counter now (acquire) without waiting: the caller compares the value
-// later, so the load's latency passes while it issues other work.
-__device__ __forceinline__ uint32_t count_peek(const uint32_t *ctr) {
-    uint32_t v;
-    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(ctr)) : "memory");
-    return v;
-}
-
 __device__ __forceinline__ void count_release_add(uint32_t *ctr) {
     asm volatile("red.release.cta.shared::cta.add.u32 [%0], 1;" ::"r"(smem_u32(ctr)) : "memory");
 }
