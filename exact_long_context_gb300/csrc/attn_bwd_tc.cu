@@ -91,7 +91,8 @@ struct BBars {
     uint64_t full[4], empty[4];    // streamed pairs (dK/dV kernel) or K tiles (dQ kernel)
     uint64_t fullv[4], emptyv[4];  // V tiles (dQ kernel)
     uint64_t s_full[2], o_full, drain;
-    uint64_t dq_done[2], drain2, pad_;  // dQ kernel: the dQ issuer's products (alternating), its drain
+    uint64_t dq_done[2], drain2;  // dQ kernel: the dQ issuer's products (alternating), its drain
+    uint32_t ds_count[2];         // dQ kernel: dS tiles stored, counted apart by tile parity
     uint32_t tmem_base;
     int32_t abort;
     uint32_t p_count[2];
@@ -484,6 +485,7 @@ struct KWalk {
 __device__ __forceinline__ void bwd_init(BBars *bars, int nst, uint32_t readers) {
     bars->abort = 0;
     bars->p_count[0] = bars->p_count[1] = 0;
+    bars->ds_count[0] = bars->ds_count[1] = 0;
     mbar_init(smem_u32(&bars->fix_full), 1);
     mbar_init(smem_u32(&bars->fix_empty), 1);
     for (int s = 0; s < nst; ++s) {
@@ -917,7 +919,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (rec.end) break;
                 const int n = rec.it.n;
                 for (int t = 0; ok && t < n; ++t, ++g) {
-                    ok = wait_count(&bars->p_count[1], (uint32_t)kEwWarps * (g + 1u), abort_flag, limit, err);
+                    // every element-wise warp has stored tile g's dS.  A count summed over the
+                    // warps can reach 8 (g + 1) early: the warps that are done may already
+                    // store tile g + 1's dS (its dP does not wait for this product) while one
+                    // still works on tile g.  No warp gets two tiles ahead of another (tile
+                    // g + 2's S needs every warp to have read tile g + 1's), so counting the
+                    // tiles of each parity apart makes the count exact.
+                    ok = wait_count(&bars->ds_count[g & 1u], (uint32_t)kEwWarps * ((g >> 1) + 1u), abort_flag, limit,
+                                    err);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t ks = g % (uint32_t)C::KST;
@@ -1000,7 +1009,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) count_release_add(&bars->p_count[1]);
+                if (lane == 0) count_release_add(&bars->ds_count[g & 1u]);
             }
             if (!ok) break;
             if (n > 0) {
