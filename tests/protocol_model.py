@@ -1,0 +1,196 @@
+"""A model of the dQ kernel's hand-off protocol between its MMA issuers and its element-wise
+warps, run under random schedules to look for races.
+
+Test infrastructure: it restates, in Python, the order of waits, products, commits and counter
+updates of the tensor-core dQ kernel (csrc/attn_bwd_tc.cu) and checks the data those steps
+hand over.  Nothing here runs the kernel.
+
+What is modelled:
+- three 128-column tensor-memory slots in rotation (tile g: S in slot s(g), dP in slot d(g) =
+  s(g - 1), S(g) overwriting the slot of dS(g - 2));
+- each element-wise warp owns its own lanes of every slot: a product writes all lanes, a warp
+  reads and writes its own, the dQ product reads all;
+- an issuer's products run in its own order; products of two issuers interleave freely;
+- `tcgen05.commit`: an arrival once every earlier product of that issuer has run;
+- mbarrier waits with the hardware's parity test (a wait for completion k passes when the
+  number of completed phases differs from k in parity - so it also passes two phases late);
+- counters the warps add to (release) and issuers wait on (acquire).
+A check fails when a warp or a product reads a slot whose lanes do not hold what it expects
+(overwritten early or not yet written), or when the schedule deadlocks.
+"""
+import random
+
+
+class Barrier:
+    def __init__(self):
+        self.done = 0  # completed phases
+
+    def passes(self, k):
+        """A parity wait for completion number k (0-based)."""
+        return (self.done & 1) != (k & 1)
+
+
+class Violation(Exception):
+    pass
+
+
+def s_slot(g):
+    return (0, 2, 1)[g % 3]
+
+
+def d_slot(g):
+    return (1, 0, 2)[g % 3]
+
+
+class Model:
+    """variant: 'split' (warp 1: S and dP; warp 2: dQ) or 'rearranged' (warp 1: S and dQ;
+    warp 2: dP); ds_by_parity / read_by_parity: the dS-stored (S-read) counts kept apart by
+    tile parity instead of summed."""
+
+    def __init__(self, variant, ds_by_parity, read_by_parity=False, warps=4, tiles=10, seed=0, slow=None):
+        self.variant, self.nw, self.T = variant, warps, tiles
+        self.ds_by_parity, self.read_by_parity = ds_by_parity, read_by_parity
+        self.rng = random.Random(seed)
+        self.slow = slow  # actor name scheduled rarely, to open lags
+        self.tags = [[None] * warps for _ in range(3)]
+        self.p0 = [0, 0]   # S read (by parity, or summed in [0])
+        self.p1 = [0, 0]   # dS stored
+        self.s_issued = 0
+        self.bar = {n: Barrier() for n in ("s0", "s1", "d0", "d1", "q0", "q1")}
+        self.fifo = {"w1": [], "w2": []}
+        self.actors = {}
+
+    # ---- counters
+    def _add(self, ctr, by_parity, g):
+        ctr[(g & 1) if by_parity else 0] += 1
+
+    def _reached(self, ctr, by_parity, g):
+        """Every warp has counted tile g (as far as the count can tell)."""
+        if by_parity:
+            return ctr[g & 1] >= self.nw * ((g >> 1) + 1)
+        return ctr[0] >= self.nw * (g + 1)
+
+    # ---- products
+    def _write(self, slot, tag):
+        self.tags[slot] = [tag] * self.nw
+
+    def _read_all(self, slot, tag, what):
+        if any(t != tag for t in self.tags[slot]):
+            raise Violation(f"{what}: slot {slot} holds {self.tags[slot]}, expected {tag}")
+
+    def _read_own(self, slot, w, tag, what):
+        if self.tags[slot][w] != tag:
+            raise Violation(f"{what}: warp {w} finds {self.tags[slot][w]} in slot {slot}, expected {tag}")
+
+    # ---- programs (generators yielding a wait predicate, or None for one step)
+    def w1_split(self):
+        for g in range(self.T):
+            if g >= 2:
+                k = (g - 2) >> 1
+                yield lambda g=g, k=k: self.bar[f"q{g & 1}"].passes(k)
+            self.fifo["w1"].append(("mma", lambda g=g: self._write(s_slot(g), ("S", g))))
+            yield None
+            if g > 0:
+                yield lambda g=g: self._reached(self.p0, self.read_by_parity, g - 1)
+            self.fifo["w1"].append(("mma", lambda g=g: self._write(d_slot(g), ("dP", g))))
+            self.fifo["w1"].append(("commit", "s0"))
+            yield None
+
+    def w2_split(self):
+        for g in range(self.T):
+            yield lambda g=g: self._reached(self.p1, self.ds_by_parity, g)
+            self.fifo["w2"].append(("mma", lambda g=g: self._read_all(d_slot(g), ("dS", g), f"dQ({g})")))
+            self.fifo["w2"].append(("commit", f"q{g & 1}"))
+            yield None
+
+    def w1_rearranged(self):
+        for g in range(self.T + 1):
+            if g < self.T:
+                self.fifo["w1"].append(("mma", lambda g=g: self._write(s_slot(g), ("S", g))))
+                self.fifo["w1"].append(("commit", f"s{g & 1}"))
+                yield None
+                self.s_issued += 1
+                yield None
+            if g >= 1:  # dQ(g - 1) once every warp stored its dS
+                yield lambda g=g: self._reached(self.p1, self.ds_by_parity, g - 1)
+                self.fifo["w1"].append(("mma", lambda g=g: self._read_all(d_slot(g - 1), ("dS", g - 1),
+                                                                           f"dQ({g - 1})")))
+                yield None
+
+    def w2_rearranged(self):
+        for g in range(self.T):
+            if g > 0:
+                yield lambda g=g: self._reached(self.p0, self.read_by_parity, g - 1)
+            yield lambda g=g: self.s_issued >= g + 1
+            self.fifo["w2"].append(("mma", lambda g=g: self._write(d_slot(g), ("dP", g))))
+            self.fifo["w2"].append(("commit", f"d{g & 1}"))
+            yield None
+
+    def ew(self, w):
+        for g in range(self.T):
+            if self.variant == "split":
+                yield lambda g=g: self.bar["s0"].passes(g)  # S(g) and dP(g)
+            else:
+                yield lambda g=g: self.bar[f"s{g & 1}"].passes(g >> 1)
+            self._read_own(s_slot(g), w, ("S", g), f"warp {w} S({g})")
+            yield None
+            self._add(self.p0, self.read_by_parity, g)
+            yield None
+            if self.variant != "split":
+                yield lambda g=g: self.bar[f"d{g & 1}"].passes(g >> 1)
+            self._read_own(d_slot(g), w, ("dP", g), f"warp {w} dP({g})")
+            yield None
+            self.tags[d_slot(g)][w] = ("dS", g)
+            yield None
+            self._add(self.p1, self.ds_by_parity, g)
+            yield None
+
+    def pipe(self, who):
+        while True:
+            if not self.fifo[who]:
+                yield lambda: bool(self.fifo[who]) or self._issuer_done(who)
+                if not self.fifo[who]:
+                    return
+            kind, x = self.fifo[who].pop(0)
+            if kind == "mma":
+                x()
+            else:
+                self.bar[x].done += 1
+            yield None
+
+    def _issuer_done(self, who):
+        return self.actors.get(who) is None
+
+    def run(self):
+        if self.variant == "split":
+            self.actors["w1"], self.actors["w2"] = self.w1_split(), self.w2_split()
+        else:
+            self.actors["w1"], self.actors["w2"] = self.w1_rearranged(), self.w2_rearranged()
+        for w in range(self.nw):
+            self.actors[f"ew{w}"] = self.ew(w)
+        self.actors["pipe1"], self.actors["pipe2"] = self.pipe("w1"), self.pipe("w2")
+        waiting = {n: None for n in self.actors}
+        while any(a is not None for a in self.actors.values()):
+            ready = [n for n, a in self.actors.items() if a is not None and (waiting[n] is None or waiting[n]())]
+            if not ready:
+                raise Violation("deadlock: " + ", ".join(n for n, a in self.actors.items() if a is not None))
+            if self.slow in ready and len(ready) > 1 and self.rng.random() < 0.9:
+                ready.remove(self.slow)
+            name = self.rng.choice(ready)
+            try:
+                waiting[name] = next(self.actors[name])
+            except StopIteration:
+                self.actors[name] = None
+                waiting[name] = None
+        return True
+
+
+def find_violation(variant, ds_by_parity, read_by_parity=False, runs=300, tiles=10, warps=4):
+    """The first violation over `runs` random schedules (half of them with one slow warp), or None."""
+    for seed in range(runs):
+        slow = "ew0" if seed % 2 else None
+        try:
+            Model(variant, ds_by_parity, read_by_parity, warps=warps, tiles=tiles, seed=seed, slow=slow).run()
+        except Violation as e:
+            return f"seed {seed}: {e}"
+    return None

@@ -1,0 +1,30 @@
+"""The dQ kernel's hand-off protocol under random schedules (tests/protocol_model.py): the
+protocol the kernel uses has no race; the two variants that raced on the GPU are caught."""
+from protocol_model import find_violation
+
+
+def test_kernel_protocol_has_no_race():
+    """Warp 1 issues S and dP, warp 2 dQ; stored dS tiles counted by parity (the kernel)."""
+    assert find_violation("split", ds_by_parity=True, runs=1500, tiles=12) is None
+
+
+def test_summed_ds_count_races():
+    """One count of stored dS tiles summed over the warps (the kernel before the fix): the dQ
+    product can read a lagging warp's lanes before its dS is written."""
+    v = find_violation("split", ds_by_parity=False, runs=400)
+    assert v is not None and "dQ(" in v, v
+
+
+def test_rearranged_split_races_with_summed_counts():
+    """Warp 1 issuing S and dQ, warp 2 dP, with summed counts (the rearrangement that gave
+    non-finite dQ on the GPU)."""
+    assert find_violation("rearranged", ds_by_parity=False, runs=400) is not None
+    # counting dS by parity alone leaves the S-read count summed: dP(g) can overwrite a
+    # lagging warp's S(g - 1)
+    v = find_violation("rearranged", ds_by_parity=True, read_by_parity=False, runs=400)
+    assert v is not None and " S(" in v, v
+
+
+def test_rearranged_split_with_both_counts_by_parity():
+    """With both counts kept by parity the rearrangement passes the model too."""
+    assert find_violation("rearranged", ds_by_parity=True, read_by_parity=True, runs=1500, tiles=12) is None
