@@ -1,9 +1,10 @@
-"""A model of the dQ kernel's hand-off protocol between its MMA issuers and its element-wise
-warps, run under random schedules to look for races.
+"""Models of the backward kernels' hand-off protocols between their MMA issuers and their
+element-wise warps, run under random schedules to look for races.
 
 Test infrastructure: it restates, in Python, the order of waits, products, commits and counter
-updates of the tensor-core dQ kernel (csrc/attn_bwd_tc.cu) and checks the data those steps
-hand over.  Nothing here runs the kernel.
+updates of the tensor-core dQ and dK/dV kernels (csrc/attn_bwd_tc.cu) and checks the data those
+steps hand over.  Nothing here runs the kernels; item boundaries, epilogues and the K/V rings
+are left out.
 
 What is modelled:
 - three 128-column tensor-memory slots in rotation (tile g: S in slot s(g), dP in slot d(g) =
@@ -169,6 +170,10 @@ class Model:
         for w in range(self.nw):
             self.actors[f"ew{w}"] = self.ew(w)
         self.actors["pipe1"], self.actors["pipe2"] = self.pipe("w1"), self.pipe("w2")
+        return self._schedule()
+
+    def _schedule(self):
+        """Runs the actors to the end, one step of a random ready actor at a time."""
         waiting = {n: None for n in self.actors}
         while any(a is not None for a in self.actors.values()):
             ready = [n for n, a in self.actors.items() if a is not None and (waiting[n] is None or waiting[n]())]
@@ -191,6 +196,76 @@ def find_violation(variant, ds_by_parity, read_by_parity=False, runs=300, tiles=
         slow = "ew0" if seed % 2 else None
         try:
             Model(variant, ds_by_parity, read_by_parity, warps=warps, tiles=tiles, seed=seed, slow=slow).run()
+        except Violation as e:
+            return f"seed {seed}: {e}"
+    return None
+
+
+class DkdvModel(Model):
+    """The dK/dV kernel's protocol: one issuer; slot 0 holds S^T(t) and then the P^T(t) the
+    warps write over it (read by dV(t)), slot 1 dP^T(t) and then dS^T(t) (read by dK(t)).
+    Product order dV(t), S^T(t + 1), dK(t), dP^T(t + 1); swap_order=True puts S^T(t + 1)
+    before dV(t) (a planted mistake: it overwrites P^T(t) before dV(t) reads it)."""
+
+    def __init__(self, swap_order=False, warps=4, tiles=10, seed=0, slow=None):
+        super().__init__("dkdv", ds_by_parity=False, warps=warps, tiles=tiles, seed=seed, slow=slow)
+        self.tags = [[None] * warps for _ in range(2)]
+        self.swap = swap_order
+
+    def issuer(self):
+        f = self.fifo["w1"]
+        f.append(("mma", lambda: self._write(0, ("S", 0))))
+        f.append(("commit", "s0"))
+        f.append(("mma", lambda: self._write(1, ("dP", 0))))
+        f.append(("commit", "s1"))
+        yield None
+        for t in range(self.T):
+            nxt = t + 1 < self.T
+            if self.swap and nxt:
+                f.append(("mma", lambda t=t: self._write(0, ("S", t + 1))))
+                f.append(("commit", "s0"))
+            yield lambda t=t: self._reached(self.p0, False, t)
+            f.append(("mma", lambda t=t: self._read_all(0, ("P", t), f"dV({t})")))
+            if nxt and not self.swap:
+                f.append(("mma", lambda t=t: self._write(0, ("S", t + 1))))
+                f.append(("commit", "s0"))
+            yield None
+            yield lambda t=t: self._reached(self.p1, False, t)
+            f.append(("mma", lambda t=t: self._read_all(1, ("dS", t), f"dK({t})")))
+            if nxt:
+                f.append(("mma", lambda t=t: self._write(1, ("dP", t + 1))))
+                f.append(("commit", "s1"))
+            yield None
+
+    def ew(self, w):
+        for t in range(self.T):
+            yield lambda t=t: self.bar["s0"].passes(t)
+            self._read_own(0, w, ("S", t), f"warp {w} S^T({t})")
+            yield None
+            self.tags[0][w] = ("P", t)
+            yield None
+            self._add(self.p0, False, t)
+            yield lambda t=t: self.bar["s1"].passes(t)
+            self._read_own(1, w, ("dP", t), f"warp {w} dP^T({t})")
+            yield None
+            self.tags[1][w] = ("dS", t)
+            yield None
+            self._add(self.p1, False, t)
+            yield None
+
+    def run(self):
+        self.actors["w1"] = self.issuer()
+        for w in range(self.nw):
+            self.actors[f"ew{w}"] = self.ew(w)
+        self.actors["pipe1"] = self.pipe("w1")
+        return self._schedule()
+
+
+def find_violation_dkdv(swap_order=False, runs=300, tiles=10, warps=4):
+    """As find_violation, for the dK/dV kernel's protocol."""
+    for seed in range(runs):
+        try:
+            DkdvModel(swap_order, warps=warps, tiles=tiles, seed=seed, slow="ew0" if seed % 2 else None).run()
         except Violation as e:
             return f"seed {seed}: {e}"
     return None

@@ -1,5 +1,6 @@
-"""The dQ kernel's hand-off protocol under random schedules (tests/protocol_model.py): the
-protocol the kernel uses has no race; the two variants that raced on the GPU are caught."""
+"""The backward kernels' hand-off protocols under random schedules (tests/protocol_model.py):
+the protocols the kernels use have no race; the two dQ variants that raced on the GPU, and a
+planted mistake in the dK/dV order, are caught."""
 from protocol_model import find_violation
 
 
@@ -28,3 +29,12 @@ def test_rearranged_split_races_with_summed_counts():
 def test_rearranged_split_with_both_counts_by_parity():
     """With both counts kept by parity the rearrangement passes the model too."""
     assert find_violation("rearranged", ds_by_parity=True, read_by_parity=True, runs=1500, tiles=12) is None
+
+
+def test_dkdv_protocol_has_no_race():
+    """The dK/dV kernel: one issuer, products dV(t), S^T(t + 1), dK(t), dP^T(t + 1)."""
+    from protocol_model import find_violation_dkdv
+    assert find_violation_dkdv(runs=1500, tiles=12) is None
+    # a planted mistake: S^T(t + 1) before dV(t) overwrites P^T(t) before it is read
+    v = find_violation_dkdv(swap_order=True, runs=100)
+    assert v is not None and "dV(" in v, v
