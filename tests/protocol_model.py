@@ -1,9 +1,9 @@
-"""Models of the backward kernels' hand-off protocols between their MMA issuers and their
-element-wise warps, run under random schedules to look for races.
+"""Models of the attention kernels' hand-off protocols between their MMA issuers and their
+element-wise (softmax) warps, run under random schedules to look for races.
 
 Test infrastructure: it restates, in Python, the order of waits, products, commits and counter
-updates of the tensor-core dQ and dK/dV kernels (csrc/attn_bwd_tc.cu) and checks the data those
-steps hand over.  Nothing here runs the kernels; item boundaries, epilogues and the K/V rings
+updates of the tensor-core dQ and dK/dV kernels (csrc/attn_bwd_tc.cu) and of the forward
+kernel (csrc/attn_tc.cu, one ring step) and checks the data those steps hand over.  Nothing here runs the kernels; item boundaries, epilogues and the K/V rings
 are left out.
 
 What is modelled:
@@ -266,6 +266,132 @@ def find_violation_dkdv(swap_order=False, runs=300, tiles=10, warps=4):
     for seed in range(runs):
         try:
             DkdvModel(swap_order, warps=warps, tiles=tiles, seed=seed, slow="ew0" if seed % 2 else None).run()
+        except Violation as e:
+            return f"seed {seed}: {e}"
+    return None
+
+
+class ForwardModel(Model):
+    """The forward kernel's protocol for one item (kernel mode 0): two halves of query rows,
+    each with an S slot (P written over it) and an O accumulator in tensor memory; a ring of
+    two shared-memory stages, stage 0 = K_0 and stage s + 1 = (V_s, K_s+1), refilled by the
+    producer once the MMA thread releases them; half 0 sits out tile 0 and takes its S signal
+    from the stage release, half 1 from its own barrier; the softmax warps count P stored per
+    half and may rescale O (read and write it) before they do.  pv_late=True issues each
+    half's next QK^T before its P V (a planted mistake: it overwrites P before P V reads it)."""
+
+    def __init__(self, pv_late=False, warps=2, tiles=10, seed=0, slow=None):
+        super().__init__("fwd", ds_by_parity=False, warps=warps, tiles=tiles, seed=seed, slow=slow)
+        self.S = [[None] * warps for _ in range(2)]   # per half, per warp's lanes
+        self.O = [[None] * warps for _ in range(2)]
+        self.stage = [None, None]                     # shared-memory slot -> stage it holds
+        self.pc = [0, 0]
+        self.bar = {n: Barrier() for n in ("full0", "full1", "empty0", "empty1", "s1", "o0", "o1")}
+        self.pv_late = pv_late
+
+    def part(self, h, t):
+        return h == 1 or t >= 1
+
+    def producer(self):
+        for s in range(self.T + 1):
+            if s >= 2:
+                yield lambda s=s: self.bar[f"empty{s % 2}"].passes((s - 2) // 2)
+            self.stage[s % 2] = s
+            yield None
+            self.bar[f"full{s % 2}"].done += 1
+            yield None
+
+    def _stage_holds(self, s, what):
+        if self.stage[s % 2] != s:
+            raise Violation(f"{what}: stage slot {s % 2} holds stage {self.stage[s % 2]}, expected {s}")
+
+    def _qk(self, h, t, s):
+        def run():
+            self._stage_holds(s, f"QK_{h}({t})")
+            self.S[h] = [("S", t)] * self.nw
+        return run
+
+    def _pv(self, h, t, s):
+        def run():
+            self._stage_holds(s, f"PV_{h}({t})")
+            if any(x != ("P", t) for x in self.S[h]):
+                raise Violation(f"PV_{h}({t}): S slot of half {h} holds {self.S[h]}")
+            prev = ("O", t - 1) if t > (0 if h == 1 else 1) else None
+            if any(x != prev for x in self.O[h]):
+                raise Violation(f"PV_{h}({t}): O of half {h} holds {self.O[h]}, expected {prev}")
+            self.O[h] = [("O", t)] * self.nw
+        return run
+
+    def mma(self):
+        f = self.fifo["w1"]
+        yield lambda: self.bar["full0"].passes(0)
+        f.append(("mma", self._qk(1, 0, 0)))     # half 0 sits out tile 0
+        f.append(("commit", "s1"))
+        f.append(("commit", "empty0"))
+        yield None
+        for t in range(self.T):
+            s = t + 1  # stage (V_t, K_t+1)
+            yield lambda s=s: self.bar[f"full{s % 2}"].passes(s // 2)
+            for h in (1, 0):
+                nxt = t + 1 < self.T
+                if self.pv_late and nxt:
+                    f.append(("mma", self._qk(h, t + 1, s)))
+                if self.part(h, t):
+                    self.pc[h] += 1
+                    yield lambda h=h, k=self.pc[h]: self.p1[h] >= self.nw * k
+                    f.append(("mma", self._pv(h, t, s)))
+                    if t == self.T - 1:
+                        f.append(("commit", f"o{h}"))
+                if nxt and not self.pv_late:
+                    f.append(("mma", self._qk(h, t + 1, s)))
+                if nxt and h == 1:
+                    f.append(("commit", "s1"))
+                yield None
+            f.append(("commit", f"empty{s % 2}"))
+            yield None
+
+    def softmax(self, h, w):
+        scnt = 0
+        for t in range(self.T):
+            if not self.part(h, t):
+                continue
+            if h == 0:
+                yield lambda t=t: self.bar[f"empty{t % 2}"].passes(t // 2)  # release of the stage of QK_0(t)
+            else:
+                yield lambda k=scnt: self.bar["s1"].passes(k)
+                scnt += 1
+            if self.S[h][w] != ("S", t):
+                raise Violation(f"half {h} warp {w} S({t}): finds {self.S[h][w]}")
+            yield None
+            first = t == (0 if h == 1 else 1)
+            if not first:  # an O rescale reads and writes the accumulator
+                if self.O[h][w] != ("O", t - 1):
+                    raise Violation(f"half {h} warp {w} rescale at tile {t}: O holds {self.O[h][w]}")
+                yield None
+            self.S[h][w] = ("P", t)
+            yield None
+            self.p1[h] += 1
+            yield None
+        yield lambda: self.bar[f"o{h}"].passes(0)
+        if self.O[h][w] != ("O", self.T - 1):
+            raise Violation(f"half {h} warp {w} epilogue: O holds {self.O[h][w]}")
+        yield None
+
+    def run(self):
+        self.actors["prod"] = self.producer()
+        self.actors["w1"] = self.mma()
+        for h in (0, 1):
+            for w in range(self.nw):
+                self.actors[f"sm{h}{w}"] = self.softmax(h, w)
+        self.actors["pipe1"] = self.pipe("w1")
+        return self._schedule()
+
+
+def find_violation_fwd(pv_late=False, runs=300, tiles=10, warps=2):
+    """As find_violation, for the forward kernel's protocol (one item)."""
+    for seed in range(runs):
+        try:
+            ForwardModel(pv_late, warps=warps, tiles=tiles, seed=seed, slow="sm00" if seed % 2 else None).run()
         except Violation as e:
             return f"seed {seed}: {e}"
     return None

@@ -1,6 +1,6 @@
-"""The backward kernels' hand-off protocols under random schedules (tests/protocol_model.py):
-the protocols the kernels use have no race; the two dQ variants that raced on the GPU, and a
-planted mistake in the dK/dV order, are caught."""
+"""The attention kernels' hand-off protocols under random schedules (tests/protocol_model.py):
+the protocols the kernels use have no race; the two dQ variants that raced on the GPU, and
+planted mistakes in the dK/dV and forward orders, are caught."""
 from protocol_model import find_violation
 
 
@@ -38,3 +38,13 @@ def test_dkdv_protocol_has_no_race():
     # a planted mistake: S^T(t + 1) before dV(t) overwrites P^T(t) before it is read
     v = find_violation_dkdv(swap_order=True, runs=100)
     assert v is not None and "dV(" in v, v
+
+
+def test_forward_protocol_has_no_race():
+    """The forward kernel: half 1 served first in each tile, half 0 signalled by the stage
+    release, P V before the next Q K^T of the same half."""
+    from protocol_model import find_violation_fwd
+    assert find_violation_fwd(runs=1500, tiles=10) is None
+    # a planted mistake: the next Q K^T before P V overwrites P before it is read
+    v = find_violation_fwd(pv_late=True, runs=100)
+    assert v is not None and "PV_" in v, v
