@@ -768,6 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int upos = 0;  // MODE 2: tile t's position in its step
                 for (int t = 0; ok && t < it.nmax; ++t) {
                     const int unext = (upos + 1 == it.tps) ? 0 : upos + 1;
+                    bool o_due = false;  // the half signalled by stage releases finished its O
                     ok = wait_phase(smem_u32(&bars->full[slot]), ph, abort_flag, P.wait_limit_ns,
                                     P.err);
                     if (!ok) break;
@@ -787,7 +788,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tc_fence_after();
                             issue_pv(hh, vb, started[hh]);
                             started[hh] = true;
-                            if (t == last_t<MODE>(it, hh)) mma_commit(smem_u32(&bars->o_full[hh]));
+                            if (t == last_t<MODE>(it, hh)) {
+                                if (hh == kLastHalf)
+                                    o_due = true;
+                                else
+                                    mma_commit(smem_u32(&bars->o_full[hh]));
+                            }
                         }
                         if (t + 1 < it.nmax && part_pos<MODE>(it, hh, t + 1, unext)) {
                             issue_qk(hh, kb);
@@ -797,6 +803,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (!ok) break;
                     mma_commit(smem_u32(&bars->empty[slot]));
+                    // The O-ready commit of the half signalled by stage releases comes after
+                    // the release of the item's last stage.  That half's softmax warps wait
+                    // for each S on the release of the stage that computed it, by parity, and
+                    // their first such wait in the next item can fall on this stage's buffer:
+                    // once they have seen O ready, this release has arrived too, so that wait
+                    // cannot pass a phase early.
+                    if constexpr (kLastHalf >= 0)
+                        if (o_due) mma_commit(smem_u32(&bars->o_full[kLastHalf]));
                     if (++slot == C::NSTAGE) {
                         slot = 0;
                         ph ^= 1u;

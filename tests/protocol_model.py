@@ -272,110 +272,185 @@ def find_violation_dkdv(swap_order=False, runs=300, tiles=10, warps=4):
 
 
 class ForwardModel(Model):
-    """The forward kernel's protocol for one item (kernel mode 0): two halves of query rows,
-    each with an S slot (P written over it) and an O accumulator in tensor memory; a ring of
-    two shared-memory stages, stage 0 = K_0 and stage s + 1 = (V_s, K_s+1), refilled by the
-    producer once the MMA thread releases them; half 0 sits out tile 0 and takes its S signal
-    from the stage release, half 1 from its own barrier; the softmax warps count P stored per
-    half and may rescale O (read and write it) before they do.  pv_late=True issues each
-    half's next QK^T before its P V (a planted mistake: it overwrites P before P V reads it)."""
+    """The forward kernel's protocol over a run of items (tests/protocol_model.py's forward
+    part; csrc/attn_tc.cu).  Each item has two halves of query rows; half h has an S slot
+    (P written over it), an O accumulator and a Q buffer.  Stages run on across items: an
+    item's stage 0 holds K_0, stage t + 1 holds (V_t, K_t+1); a ring of `nstage` stage
+    buffers is refilled by the producer once the MMA thread releases a stage, and the
+    producer reloads Q_h once the MMA thread has issued the item's last Q_h K^T.
 
-    def __init__(self, pv_late=False, warps=2, tiles=10, seed=0, slow=None):
-        super().__init__("fwd", ds_by_parity=False, warps=warps, tiles=tiles, seed=seed, slow=slow)
-        self.S = [[None] * warps for _ in range(2)]   # per half, per warp's lanes
-        self.O = [[None] * warps for _ in range(2)]
-        self.stage = [None, None]                     # shared-memory slot -> stage it holds
-        self.pc = [0, 0]
-        self.bar = {n: Barrier() for n in ("full0", "full1", "empty0", "empty1", "s1", "o0", "o1")}
+    items: (nmax, skips, has1) per item: its tile count, the tiles half 0 sits out, whether
+    half 1 has rows.  last_half: the half (0) whose softmax learns of its next S from the
+    release of the stage that computed it, or None (both halves signalled by their own
+    barrier, the fused contiguous / zigzag ring).  o_after_release: the last half's O-ready
+    commit goes after the release of the item's last stage (else before it, at its P V).
+    pv_late: the next Q K^T before P V (a planted mistake: it overwrites P before it is read)."""
+
+    def __init__(self, items, last_half=0, o_after_release=True, pv_late=False, nstage=2, warps=2,
+                 seed=0, slow=None):
+        super().__init__("fwd", ds_by_parity=False, warps=warps, tiles=0, seed=seed, slow=slow)
+        self.items = items
+        self.lh = last_half
+        self.o_after = o_after_release
         self.pv_late = pv_late
+        self.ns = nstage
+        self.S = [[None] * warps for _ in range(2)]  # per half, per warp's lanes
+        self.O = [[None] * warps for _ in range(2)]
+        self.Q = [None, None]
+        self.buf = [None] * nstage                   # stage buffer -> the stage it holds
+        self.pcount = [0, 0]                         # P tiles published, summed over the warps
+        names = ["s0", "s1", "o0", "o1", "q_full0", "q_full1", "q_empty0", "q_empty1"]
+        names += [f"full{i}" for i in range(nstage)] + [f"empty{i}" for i in range(nstage)]
+        self.bar = {n: Barrier() for n in names}
+        self.fifo = {"w1": []}
+        order = (1, 0) if last_half == 0 else (0, 1)
+        self.order = order
 
-    def part(self, h, t):
-        return h == 1 or t >= 1
+    # ---- item shape
+    def part(self, i, h, t):
+        nmax, skips, has1 = self.items[i]
+        return has1 if h else t not in skips
 
+    def last(self, i, h):
+        nmax = self.items[i][0]
+        return max(t for t in range(nmax) if self.part(i, h, t))
+
+    def has(self, i, h):
+        return any(self.part(i, h, t) for t in range(self.items[i][0]))
+
+    def sbase(self, i):
+        return sum(1 + n for n, _, _ in self.items[:i])
+
+    # ---- products
+    def _qk(self, i, h, t, gs):
+        def run():
+            if self.buf[gs % self.ns] != gs:
+                raise Violation(f"QK_{h}({i},{t}): buffer {gs % self.ns} holds stage {self.buf[gs % self.ns]}, not {gs}")
+            if self.Q[h] != i:
+                raise Violation(f"QK_{h}({i},{t}): Q_{h} holds item {self.Q[h]}")
+            self.S[h] = [("S", i, t)] * self.nw
+        return run
+
+    def _pv(self, i, h, t, gs, prev):
+        def run():
+            if self.buf[gs % self.ns] != gs:
+                raise Violation(f"PV_{h}({i},{t}): buffer {gs % self.ns} holds stage {self.buf[gs % self.ns]}, not {gs}")
+            if any(x != ("P", i, t) for x in self.S[h]):
+                raise Violation(f"PV_{h}({i},{t}): S slot of half {h} holds {self.S[h]}")
+            want = None if prev is None else ("O", i, prev)
+            if prev is not None and any(x != want for x in self.O[h]):
+                raise Violation(f"PV_{h}({i},{t}): O of half {h} holds {self.O[h]}, expected {want}")
+            self.O[h] = [("O", i, t)] * self.nw
+        return run
+
+    # ---- programs
     def producer(self):
-        for s in range(self.T + 1):
-            if s >= 2:
-                yield lambda s=s: self.bar[f"empty{s % 2}"].passes((s - 2) // 2)
-            self.stage[s % 2] = s
-            yield None
-            self.bar[f"full{s % 2}"].done += 1
-            yield None
-
-    def _stage_holds(self, s, what):
-        if self.stage[s % 2] != s:
-            raise Violation(f"{what}: stage slot {s % 2} holds stage {self.stage[s % 2]}, expected {s}")
-
-    def _qk(self, h, t, s):
-        def run():
-            self._stage_holds(s, f"QK_{h}({t})")
-            self.S[h] = [("S", t)] * self.nw
-        return run
-
-    def _pv(self, h, t, s):
-        def run():
-            self._stage_holds(s, f"PV_{h}({t})")
-            if any(x != ("P", t) for x in self.S[h]):
-                raise Violation(f"PV_{h}({t}): S slot of half {h} holds {self.S[h]}")
-            prev = ("O", t - 1) if t > (0 if h == 1 else 1) else None
-            if any(x != prev for x in self.O[h]):
-                raise Violation(f"PV_{h}({t}): O of half {h} holds {self.O[h]}, expected {prev}")
-            self.O[h] = [("O", t)] * self.nw
-        return run
+        gs, qn = 0, [0, 0]
+        for i, (nmax, _, _) in enumerate(self.items):
+            for st in range(-1, nmax):
+                if gs >= self.ns:
+                    yield lambda gs=gs: self.bar[f"empty{gs % self.ns}"].passes(gs // self.ns - 1)
+                self.buf[gs % self.ns] = gs
+                yield None
+                self.bar[f"full{gs % self.ns}"].done += 1
+                yield None
+                if st == -1:  # Q of the item, once its previous user has issued its last Q K^T
+                    for h in (0, 1):
+                        if not self.has(i, h):
+                            continue
+                        if qn[h] >= 1:
+                            yield lambda h=h, k=qn[h] - 1: self.bar[f"q_empty{h}"].passes(k)
+                        self.Q[h] = i
+                        yield None
+                        self.bar[f"q_full{h}"].done += 1
+                        qn[h] += 1
+                        yield None
+                gs += 1
 
     def mma(self):
         f = self.fifo["w1"]
-        yield lambda: self.bar["full0"].passes(0)
-        f.append(("mma", self._qk(1, 0, 0)))     # half 0 sits out tile 0
-        f.append(("commit", "s1"))
-        f.append(("commit", "empty0"))
-        yield None
-        for t in range(self.T):
-            s = t + 1  # stage (V_t, K_t+1)
-            yield lambda s=s: self.bar[f"full{s % 2}"].passes(s // 2)
-            for h in (1, 0):
-                nxt = t + 1 < self.T
-                if self.pv_late and nxt:
-                    f.append(("mma", self._qk(h, t + 1, s)))
-                if self.part(h, t):
-                    self.pc[h] += 1
-                    yield lambda h=h, k=self.pc[h]: self.p1[h] >= self.nw * k
-                    f.append(("mma", self._pv(h, t, s)))
-                    if t == self.T - 1:
-                        f.append(("commit", f"o{h}"))
-                if nxt and not self.pv_late:
-                    f.append(("mma", self._qk(h, t + 1, s)))
-                if nxt and h == 1:
-                    f.append(("commit", "s1"))
-                yield None
-            f.append(("commit", f"empty{s % 2}"))
+        gs, qn, pc = 0, [0, 0], [0, 0]
+        for i, (nmax, _, _) in enumerate(self.items):
+            for h in (0, 1):
+                if self.has(i, h):
+                    yield lambda h=h, k=qn[h]: self.bar[f"q_full{h}"].passes(k)
+                    qn[h] += 1
+            yield lambda gs=gs: self.bar[f"full{gs % self.ns}"].passes(gs // self.ns)
+            for h in (0, 1):
+                if self.part(i, h, 0):
+                    f.append(("mma", self._qk(i, h, 0, gs)))
+                    if h != self.lh:
+                        f.append(("commit", f"s{h}"))
+                    if self.last(i, h) == 0:
+                        f.append(("commit", f"q_empty{h}"))
+            f.append(("commit", f"empty{gs % self.ns}"))
+            gs += 1
             yield None
+            prev = [None, None]
+            for t in range(nmax):
+                yield lambda gs=gs: self.bar[f"full{gs % self.ns}"].passes(gs // self.ns)
+                o_due = False
+                for h in self.order:
+                    nxt = t + 1 < nmax and self.part(i, h, t + 1)
+                    if self.pv_late and nxt:
+                        f.append(("mma", self._qk(i, h, t + 1, gs)))
+                    if self.part(i, h, t):
+                        pc[h] += 1
+                        yield lambda h=h, k=pc[h]: self.pcount[h] >= self.nw * k
+                        f.append(("mma", self._pv(i, h, t, gs, prev[h])))
+                        prev[h] = t
+                        if t == self.last(i, h):
+                            if h == self.lh and self.o_after:
+                                o_due = True
+                            else:
+                                f.append(("commit", f"o{h}"))
+                    if nxt and not self.pv_late:
+                        f.append(("mma", self._qk(i, h, t + 1, gs)))
+                    if nxt:
+                        if h != self.lh:
+                            f.append(("commit", f"s{h}"))
+                        if t + 1 == self.last(i, h):
+                            f.append(("commit", f"q_empty{h}"))
+                    yield None
+                f.append(("commit", f"empty{gs % self.ns}"))
+                if o_due:
+                    f.append(("commit", f"o{self.lh}"))
+                gs += 1
+                yield None
 
     def softmax(self, h, w):
-        scnt = 0
-        for t in range(self.T):
-            if not self.part(h, t):
+        scnt = ocnt = 0
+        for i, (nmax, _, _) in enumerate(self.items):
+            sb = self.sbase(i)
+            if not self.has(i, h):
                 continue
-            if h == 0:
-                yield lambda t=t: self.bar[f"empty{t % 2}"].passes(t // 2)  # release of the stage of QK_0(t)
-            else:
-                yield lambda k=scnt: self.bar["s1"].passes(k)
-                scnt += 1
-            if self.S[h][w] != ("S", t):
-                raise Violation(f"half {h} warp {w} S({t}): finds {self.S[h][w]}")
-            yield None
-            first = t == (0 if h == 1 else 1)
-            if not first:  # an O rescale reads and writes the accumulator
-                if self.O[h][w] != ("O", t - 1):
-                    raise Violation(f"half {h} warp {w} rescale at tile {t}: O holds {self.O[h][w]}")
+            prev = None
+            for t in range(nmax):
+                if not self.part(i, h, t):
+                    continue
+                if h == self.lh:
+                    gs = sb + t
+                    yield lambda gs=gs: self.bar[f"empty{gs % self.ns}"].passes(gs // self.ns)
+                else:
+                    yield lambda k=scnt: self.bar[f"s{h}"].passes(k)
+                    scnt += 1
+                if self.S[h][w] != ("S", i, t):
+                    raise Violation(f"half {h} warp {w} S({i},{t}): finds {self.S[h][w]}")
                 yield None
-            self.S[h][w] = ("P", t)
+                if prev is not None:  # a rescale reads and writes the accumulator
+                    if self.O[h][w] != ("O", i, prev):
+                        raise Violation(f"half {h} warp {w} rescale at ({i},{t}): O holds {self.O[h][w]}")
+                    yield None
+                self.S[h][w] = ("P", i, t)
+                yield None
+                self.pcount[h] += 1
+                prev = t
+                yield None
+            yield lambda k=ocnt: self.bar[f"o{h}"].passes(k)
+            ocnt += 1
+            if self.O[h][w] != ("O", i, prev):
+                raise Violation(f"half {h} warp {w} epilogue of item {i}: O holds {self.O[h][w]}")
             yield None
-            self.p1[h] += 1
-            yield None
-        yield lambda: self.bar[f"o{h}"].passes(0)
-        if self.O[h][w] != ("O", self.T - 1):
-            raise Violation(f"half {h} warp {w} epilogue: O holds {self.O[h][w]}")
-        yield None
 
     def run(self):
         self.actors["prod"] = self.producer()
@@ -387,11 +462,35 @@ class ForwardModel(Model):
         return self._schedule()
 
 
-def find_violation_fwd(pv_late=False, runs=300, tiles=10, warps=2):
-    """As find_violation, for the forward kernel's protocol (one item)."""
+def random_items(rng, mode, n=4):
+    """Item shapes of a kernel mode: 'single' (one ring step or the single pass: half 0 may
+    sit out the first tile), 'fused' (contiguous / zigzag ring: half 0 may sit out the last
+    tile of the first step) or 'striped' (half 0 sits out the first tile of every step)."""
+    items = []
+    for _ in range(n):
+        has1 = rng.random() < 0.8
+        if mode == "striped":
+            T, R = rng.randint(2, 3), rng.randint(1, 3)
+            items.append((R * T, set(range(0, R * T, T)) if has1 else set(), has1))
+            continue
+        t0 = rng.randint(1, 4)
+        nmax = t0 + (rng.randint(0, 3) if mode == "fused" else 0)
+        skip = set()
+        if has1 and t0 >= 2 and rng.random() < 0.7:
+            skip = {0} if mode == "single" else {t0 - 1}
+        items.append((nmax, skip, has1))
+    return items
+
+
+def find_violation_fwd(mode="single", o_after_release=True, pv_late=False, runs=300, nstage=2, warps=2):
+    """As find_violation, for the forward kernel's protocol over random runs of items."""
     for seed in range(runs):
+        rng = random.Random(1000 + seed)
+        items = random_items(rng, mode)
+        slow = ("pipe1", "sm00", None)[seed % 3]
         try:
-            ForwardModel(pv_late, warps=warps, tiles=tiles, seed=seed, slow="sm00" if seed % 2 else None).run()
+            ForwardModel(items, last_half=None if mode == "fused" else 0, o_after_release=o_after_release,
+                         pv_late=pv_late, nstage=nstage, warps=warps, seed=seed, slow=slow).run()
         except Violation as e:
-            return f"seed {seed}: {e}"
+            return f"seed {seed} items {items}: {e}"
     return None

@@ -41,10 +41,27 @@ def test_dkdv_protocol_has_no_race():
 
 
 def test_forward_protocol_has_no_race():
-    """The forward kernel: half 1 served first in each tile, half 0 signalled by the stage
-    release, P V before the next Q K^T of the same half."""
+    """The forward kernel over runs of items, in each of its modes and both stage-ring depths:
+    half 0 signalled by stage releases outside the fused contiguous / zigzag ring, its
+    O-ready commit after the release of the item's last stage."""
     from protocol_model import find_violation_fwd
-    assert find_violation_fwd(runs=1500, tiles=10) is None
-    # a planted mistake: the next Q K^T before P V overwrites P before it is read
-    v = find_violation_fwd(pv_late=True, runs=100)
+    for mode in ("single", "fused", "striped"):
+        for nstage in (2, 4):
+            assert find_violation_fwd(mode, runs=300, nstage=nstage) is None, (mode, nstage)
+
+
+def test_forward_o_ready_before_release_races():
+    """With half 0's O-ready commit before the release of the item's last stage (the kernel's
+    earlier order), half 0 can finish its epilogue and take the next item's first stage-release
+    wait on that stage's buffer a phase early (two stage buffers), and read a stale S."""
+    from protocol_model import find_violation_fwd
+    for mode in ("single", "striped"):
+        v = find_violation_fwd(mode, o_after_release=False, runs=300, nstage=2)
+        assert v is not None and "half 0" in v and " S(" in v, v
+
+
+def test_forward_planted_early_qk_is_caught():
+    """A planted mistake: the next Q K^T before the P V that reads P."""
+    from protocol_model import find_violation_fwd
+    v = find_violation_fwd("single", pv_late=True, runs=100)
     assert v is not None and "PV_" in v, v
