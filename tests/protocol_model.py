@@ -3,18 +3,22 @@ element-wise (softmax) warps, run under random schedules to look for races.
 
 Test infrastructure: it restates, in Python, the order of waits, products, commits and counter
 updates of the tensor-core dQ and dK/dV kernels (csrc/attn_bwd_tc.cu) and of the forward
-kernel (csrc/attn_tc.cu, one ring step) and checks the data those steps hand over.  Nothing here runs the kernels; item boundaries, epilogues and the K/V rings
-are left out.
+kernel (csrc/attn_tc.cu) and checks the data those steps hand over.  Nothing here runs the
+kernels.  The backward models cover one item's tiles (their waits are all taken in sequence,
+one per completion, across items too); the forward model covers runs of items with its
+producer, its stage ring and the Q reloads, since one of its waits skips phases.
 
 What is modelled:
-- three 128-column tensor-memory slots in rotation (tile g: S in slot s(g), dP in slot d(g) =
-  s(g - 1), S(g) overwriting the slot of dS(g - 2));
+- the backward kernels' three 128-column tensor-memory slots in rotation (tile g: S in slot
+  s(g), dP in slot d(g) = s(g - 1), S(g) overwriting the slot of dS(g - 2)); the forward
+  kernel's S/P slot and O accumulator per half of the item's rows;
 - each element-wise warp owns its own lanes of every slot: a product writes all lanes, a warp
   reads and writes its own, the dQ product reads all;
 - an issuer's products run in its own order; products of two issuers interleave freely;
 - `tcgen05.commit`: an arrival once every earlier product of that issuer has run;
-- mbarrier waits with the hardware's parity test (a wait for completion k passes when the
-  number of completed phases differs from k in parity - so it also passes two phases late);
+- mbarrier waits with the hardware's parity test: a wait for completion k (0-based) passes
+  when the number of completed phases differs from k in parity, so it passes one phase early
+  (k - 1 completed) and not at all two phases late (k + 2 completed);
 - counters the warps add to (release) and issuers wait on (acquire).
 A check fails when a warp or a product reads a slot whose lanes do not hold what it expects
 (overwritten early or not yet written), or when the schedule deadlocks.
