@@ -4,9 +4,11 @@ element-wise (softmax) warps, run under random schedules to look for races.
 Test infrastructure: it restates, in Python, the order of waits, products, commits and counter
 updates of the tensor-core dQ and dK/dV kernels (csrc/attn_bwd_tc.cu) and of the forward
 kernel (csrc/attn_tc.cu) and checks the data those steps hand over.  Nothing here runs the
-kernels.  The backward models cover one item's tiles (their waits are all taken in sequence,
-one per completion, across items too); the forward model covers runs of items with its
-producer, its stage ring and the Q reloads, since one of its waits skips phases.
+kernels.  The dQ model runs one item or a run of items (each item's dQ accumulator is read by
+the warps' epilogue before the next item's first dQ product overwrites it); the dK/dV model
+runs one item (its waits are all taken in sequence, one per completion, across items too);
+the forward model runs sequences of items with its producer, its stage ring and the Q
+reloads, since one of its waits skips phases.
 
 What is modelled:
 - the backward kernels' three 128-column tensor-memory slots in rotation (tile g: S in slot
@@ -52,8 +54,19 @@ class Model:
     warp 2: dP); ds_by_parity / read_by_parity: the dS-stored (S-read) counts kept apart by
     tile parity instead of summed."""
 
-    def __init__(self, variant, ds_by_parity, read_by_parity=False, warps=4, tiles=10, seed=0, slow=None):
-        self.variant, self.nw, self.T = variant, warps, tiles
+    def __init__(self, variant, ds_by_parity, read_by_parity=False, warps=4, tiles=10, seed=0, slow=None,
+                 items=None, late_epilogue=False):
+        items = items if items is not None else [tiles]
+        self.variant, self.nw, self.T = variant, warps, sum(items)
+        # the dQ kernel's items: tile g belongs to item item_of[g] as its t_of[g]-th tile; each
+        # item's dQ products accumulate into one tensor-memory accumulator (the first of an
+        # item overwrites it), read by the warps' epilogue once the item's last dQ completes
+        self.items = items
+        self.item_of = [i for i, n in enumerate(items) for _ in range(n)]
+        self.t_of = [t for n in items for t in range(n)]
+        self.DQ = [None] * warps
+        # planted mistake: a warp reads an item's dQ only after storing the next item's first dS
+        self.late_epilogue = late_epilogue
         self.ds_by_parity, self.read_by_parity = ds_by_parity, read_by_parity
         self.rng = random.Random(seed)
         self.slow = slow  # actor name scheduled rarely, to open lags
@@ -61,7 +74,7 @@ class Model:
         self.p0 = [0, 0]   # S read (by parity, or summed in [0])
         self.p1 = [0, 0]   # dS stored
         self.s_issued = 0
-        self.bar = {n: Barrier() for n in ("s0", "s1", "d0", "d1", "q0", "q1")}
+        self.bar = {n: Barrier() for n in ("s0", "s1", "d0", "d1", "q0", "q1", "o")}
         self.fifo = {"w1": [], "w2": []}
         self.actors = {}
 
@@ -87,6 +100,23 @@ class Model:
         if self.tags[slot][w] != tag:
             raise Violation(f"{what}: warp {w} finds {self.tags[slot][w]} in slot {slot}, expected {tag}")
 
+    def _dq(self, g):
+        """dQ(g): reads every warp's dS(g); accumulates into the item's dQ (the first
+        product of an item overwrites the accumulator)."""
+        def run():
+            self._read_all(d_slot(g), ("dS", g), f"dQ({g})")
+            i, t = self.item_of[g], self.t_of[g]
+            if t > 0 and any(x != ("dQ", i, g - 1) for x in self.DQ):
+                raise Violation(f"dQ({g}): accumulator holds {self.DQ}, expected {('dQ', i, g - 1)}")
+            self.DQ = [("dQ", i, g)] * self.nw
+        return run
+
+    def _dq_ready(self, g):
+        return self._reached(self.p1, self.ds_by_parity, g)
+
+    def _item_last(self, g):
+        return self.t_of[g] == self.items[self.item_of[g]] - 1
+
     # ---- programs (generators yielding a wait predicate, or None for one step)
     def w1_split(self):
         for g in range(self.T):
@@ -103,9 +133,11 @@ class Model:
 
     def w2_split(self):
         for g in range(self.T):
-            yield lambda g=g: self._reached(self.p1, self.ds_by_parity, g)
-            self.fifo["w2"].append(("mma", lambda g=g: self._read_all(d_slot(g), ("dS", g), f"dQ({g})")))
+            yield lambda g=g: self._dq_ready(g)
+            self.fifo["w2"].append(("mma", self._dq(g)))
             self.fifo["w2"].append(("commit", f"q{g & 1}"))
+            if self._item_last(g):
+                self.fifo["w2"].append(("commit", "o"))
             yield None
 
     def w1_rearranged(self):
@@ -117,9 +149,10 @@ class Model:
                 self.s_issued += 1
                 yield None
             if g >= 1:  # dQ(g - 1) once every warp stored its dS
-                yield lambda g=g: self._reached(self.p1, self.ds_by_parity, g - 1)
-                self.fifo["w1"].append(("mma", lambda g=g: self._read_all(d_slot(g - 1), ("dS", g - 1),
-                                                                           f"dQ({g - 1})")))
+                yield lambda g=g: self._dq_ready(g - 1)
+                self.fifo["w1"].append(("mma", self._dq(g - 1)))
+                if self._item_last(g - 1):
+                    self.fifo["w1"].append(("commit", "o"))
                 yield None
 
     def w2_rearranged(self):
@@ -149,6 +182,21 @@ class Model:
             yield None
             self._add(self.p1, self.ds_by_parity, g)
             yield None
+            # epilogue: the item's dQ, once its last product completed
+            if self.late_epilogue:
+                if self.t_of[g] == 0 and g > 0:
+                    yield from self._epilogue(w, g - 1)
+                if g == self.T - 1:
+                    yield from self._epilogue(w, g)
+            elif self._item_last(g):
+                yield from self._epilogue(w, g)
+
+    def _epilogue(self, w, g):
+        i = self.item_of[g]
+        yield lambda i=i: self.bar["o"].passes(i)
+        if self.DQ[w] != ("dQ", i, g):
+            raise Violation(f"warp {w} epilogue of item {i}: dQ accumulator holds {self.DQ[w]}")
+        yield None
 
     def pipe(self, who):
         while True:
@@ -194,12 +242,19 @@ class Model:
         return True
 
 
-def find_violation(variant, ds_by_parity, read_by_parity=False, runs=300, tiles=10, warps=4):
-    """The first violation over `runs` random schedules (half of them with one slow warp), or None."""
+def find_violation(variant, ds_by_parity, read_by_parity=False, runs=300, tiles=10, warps=4, items=False,
+                   late_epilogue=False):
+    """The first violation over `runs` random schedules (half of them with one slow warp), or None.
+    items=True: each schedule runs a random sequence of items of 1 to 4 tiles (else one item)."""
     for seed in range(runs):
         slow = "ew0" if seed % 2 else None
+        its = None
+        if items:
+            rng = random.Random(2000 + seed)
+            its = [rng.randint(1, 4) for _ in range(rng.randint(2, 4))]
         try:
-            Model(variant, ds_by_parity, read_by_parity, warps=warps, tiles=tiles, seed=seed, slow=slow).run()
+            Model(variant, ds_by_parity, read_by_parity, warps=warps, tiles=tiles, seed=seed, slow=slow,
+                  items=its, late_epilogue=late_epilogue).run()
         except Violation as e:
             return f"seed {seed}: {e}"
     return None

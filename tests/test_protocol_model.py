@@ -7,6 +7,16 @@ from protocol_model import find_violation
 def test_kernel_protocol_has_no_race():
     """Warp 1 issues S and dP, warp 2 dQ; stored dS tiles counted by parity (the kernel)."""
     assert find_violation("split", ds_by_parity=True, runs=1500, tiles=12) is None
+    # runs of items: each item's first dQ product overwrites the accumulator that the
+    # warps' epilogue of the item before reads
+    assert find_violation("split", ds_by_parity=True, runs=600, items=True) is None
+
+
+def test_dq_epilogue_after_next_dS_is_caught():
+    """A planted mistake: a warp reading an item's dQ only after storing the next item's first
+    dS lets that item's first dQ product overwrite the accumulator before the read."""
+    v = find_violation("split", ds_by_parity=True, runs=200, items=True, late_epilogue=True)
+    assert v is not None and "epilogue of item" in v, v
 
 
 def test_summed_ds_count_races():
@@ -29,6 +39,7 @@ def test_rearranged_split_races_with_summed_counts():
 def test_rearranged_split_with_both_counts_by_parity():
     """With both counts kept by parity the rearrangement passes the model too."""
     assert find_violation("rearranged", ds_by_parity=True, read_by_parity=True, runs=1500, tiles=12) is None
+    assert find_violation("rearranged", ds_by_parity=True, read_by_parity=True, runs=600, items=True) is None
 
 
 def test_dkdv_protocol_has_no_race():
