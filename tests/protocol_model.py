@@ -4,11 +4,11 @@ element-wise (softmax) warps, run under random schedules to look for races.
 Test infrastructure: it restates, in Python, the order of waits, products, commits and counter
 updates of the tensor-core dQ and dK/dV kernels (csrc/attn_bwd_tc.cu) and of the forward
 kernel (csrc/attn_tc.cu) and checks the data those steps hand over.  Nothing here runs the
-kernels.  The dQ model runs one item or a run of items (each item's dQ accumulator is read by
-the warps' epilogue before the next item's first dQ product overwrites it); the dK/dV model
-runs one item (its waits are all taken in sequence, one per completion, across items too);
-the forward model runs sequences of items with its producer, its stage ring and the Q
-reloads, since one of its waits skips phases.
+kernels.  The dQ and dK/dV models run one item or a sequence of items (each item's
+accumulators are read by the warps' epilogue before the next item's first products overwrite
+them; the shared-memory rings are left out, their waits being taken one per completion); the
+forward model runs sequences of items with its producer, its stage ring and the Q reloads,
+since one of its waits skips phases.
 
 What is modelled:
 - the backward kernels' three 128-column tensor-memory slots in rotation (tile g: S in slot
@@ -264,53 +264,85 @@ class DkdvModel(Model):
     """The dK/dV kernel's protocol: one issuer; slot 0 holds S^T(t) and then the P^T(t) the
     warps write over it (read by dV(t)), slot 1 dP^T(t) and then dS^T(t) (read by dK(t)).
     Product order dV(t), S^T(t + 1), dK(t), dP^T(t + 1); swap_order=True puts S^T(t + 1)
-    before dV(t) (a planted mistake: it overwrites P^T(t) before dV(t) reads it)."""
+    before dV(t) (a planted mistake: it overwrites P^T(t) before dV(t) reads it).  Over a
+    run of items, an item starts with S^T and dP^T of its first tile, its first dV and dK
+    overwrite the accumulators and the warps read them in their epilogue once the item's
+    last dK completed; late_epilogue=True moves that read after the next item's first P^T
+    (a planted mistake)."""
 
-    def __init__(self, swap_order=False, warps=4, tiles=10, seed=0, slow=None):
-        super().__init__("dkdv", ds_by_parity=False, warps=warps, tiles=tiles, seed=seed, slow=slow)
+    def __init__(self, swap_order=False, warps=4, tiles=10, seed=0, slow=None, items=None, late_epilogue=False):
+        super().__init__("dkdv", ds_by_parity=False, warps=warps, tiles=tiles, seed=seed, slow=slow,
+                         items=items, late_epilogue=late_epilogue)
         self.tags = [[None] * warps for _ in range(2)]
         self.swap = swap_order
+        self.acc = {"dV": [None] * warps, "dK": [None] * warps}
+
+    def _acc(self, name, slot, want, g):
+        """dV(g) or dK(g): reads every warp's lanes of the slot, accumulates into the item's
+        accumulator (the item's first product overwrites it)."""
+        def run():
+            self._read_all(slot, (want, g), f"{name}({g})")
+            i, t = self.item_of[g], self.t_of[g]
+            if t > 0 and any(x != (name, i, g - 1) for x in self.acc[name]):
+                raise Violation(f"{name}({g}): accumulator holds {self.acc[name]}, expected {(name, i, g - 1)}")
+            self.acc[name] = [(name, i, g)] * self.nw
+        return run
 
     def issuer(self):
         f = self.fifo["w1"]
-        f.append(("mma", lambda: self._write(0, ("S", 0))))
-        f.append(("commit", "s0"))
-        f.append(("mma", lambda: self._write(1, ("dP", 0))))
-        f.append(("commit", "s1"))
-        yield None
-        for t in range(self.T):
-            nxt = t + 1 < self.T
-            if self.swap and nxt:
-                f.append(("mma", lambda t=t: self._write(0, ("S", t + 1))))
+        for g in range(self.T):
+            if self.t_of[g] == 0:  # the item's first tile
+                f.append(("mma", lambda g=g: self._write(0, ("S", g))))
                 f.append(("commit", "s0"))
-            yield lambda t=t: self._reached(self.p0, False, t)
-            f.append(("mma", lambda t=t: self._read_all(0, ("P", t), f"dV({t})")))
+                f.append(("mma", lambda g=g: self._write(1, ("dP", g))))
+                f.append(("commit", "s1"))
+                yield None
+            nxt = not self._item_last(g)
+            if self.swap and nxt:
+                f.append(("mma", lambda g=g: self._write(0, ("S", g + 1))))
+                f.append(("commit", "s0"))
+            yield lambda g=g: self._reached(self.p0, False, g)
+            f.append(("mma", self._acc("dV", 0, "P", g)))
             if nxt and not self.swap:
-                f.append(("mma", lambda t=t: self._write(0, ("S", t + 1))))
+                f.append(("mma", lambda g=g: self._write(0, ("S", g + 1))))
                 f.append(("commit", "s0"))
             yield None
-            yield lambda t=t: self._reached(self.p1, False, t)
-            f.append(("mma", lambda t=t: self._read_all(1, ("dS", t), f"dK({t})")))
+            yield lambda g=g: self._reached(self.p1, False, g)
+            f.append(("mma", self._acc("dK", 1, "dS", g)))
+            if not nxt:
+                f.append(("commit", "o"))
             if nxt:
-                f.append(("mma", lambda t=t: self._write(1, ("dP", t + 1))))
+                f.append(("mma", lambda g=g: self._write(1, ("dP", g + 1))))
                 f.append(("commit", "s1"))
             yield None
 
     def ew(self, w):
-        for t in range(self.T):
-            yield lambda t=t: self.bar["s0"].passes(t)
-            self._read_own(0, w, ("S", t), f"warp {w} S^T({t})")
+        for g in range(self.T):
+            yield lambda g=g: self.bar["s0"].passes(g)
+            self._read_own(0, w, ("S", g), f"warp {w} S^T({g})")
             yield None
-            self.tags[0][w] = ("P", t)
+            self.tags[0][w] = ("P", g)
             yield None
-            self._add(self.p0, False, t)
-            yield lambda t=t: self.bar["s1"].passes(t)
-            self._read_own(1, w, ("dP", t), f"warp {w} dP^T({t})")
+            self._add(self.p0, False, g)
+            if self.late_epilogue and self.t_of[g] == 0 and g > 0:
+                yield from self._epilogue_kv(w, g - 1)
+            yield lambda g=g: self.bar["s1"].passes(g)
+            self._read_own(1, w, ("dP", g), f"warp {w} dP^T({g})")
             yield None
-            self.tags[1][w] = ("dS", t)
+            self.tags[1][w] = ("dS", g)
             yield None
-            self._add(self.p1, False, t)
+            self._add(self.p1, False, g)
             yield None
+            if self._item_last(g) and (not self.late_epilogue or g == self.T - 1):
+                yield from self._epilogue_kv(w, g)
+
+    def _epilogue_kv(self, w, g):
+        i = self.item_of[g]
+        yield lambda i=i: self.bar["o"].passes(i)
+        for name in ("dV", "dK"):
+            if self.acc[name][w] != (name, i, g):
+                raise Violation(f"warp {w} epilogue of item {i}: {name} accumulator holds {self.acc[name][w]}")
+        yield None
 
     def run(self):
         self.actors["w1"] = self.issuer()
@@ -320,11 +352,16 @@ class DkdvModel(Model):
         return self._schedule()
 
 
-def find_violation_dkdv(swap_order=False, runs=300, tiles=10, warps=4):
+def find_violation_dkdv(swap_order=False, runs=300, tiles=10, warps=4, items=False, late_epilogue=False):
     """As find_violation, for the dK/dV kernel's protocol."""
     for seed in range(runs):
+        its = None
+        if items:
+            rng = random.Random(3000 + seed)
+            its = [rng.randint(1, 4) for _ in range(rng.randint(2, 4))]
         try:
-            DkdvModel(swap_order, warps=warps, tiles=tiles, seed=seed, slow="ew0" if seed % 2 else None).run()
+            DkdvModel(swap_order, warps=warps, tiles=tiles, seed=seed, slow="ew0" if seed % 2 else None,
+                      items=its, late_epilogue=late_epilogue).run()
         except Violation as e:
             return f"seed {seed}: {e}"
     return None

@@ -46,6 +46,7 @@ def test_dkdv_protocol_has_no_race():
     """The dK/dV kernel: one issuer, products dV(t), S^T(t + 1), dK(t), dP^T(t + 1)."""
     from protocol_model import find_violation_dkdv
     assert find_violation_dkdv(runs=1500, tiles=12) is None
+    assert find_violation_dkdv(runs=600, items=True) is None
     # a planted mistake: S^T(t + 1) before dV(t) overwrites P^T(t) before it is read
     v = find_violation_dkdv(swap_order=True, runs=100)
     assert v is not None and "dV(" in v, v
@@ -76,3 +77,11 @@ def test_forward_planted_early_qk_is_caught():
     from protocol_model import find_violation_fwd
     v = find_violation_fwd("single", pv_late=True, runs=100)
     assert v is not None and "PV_" in v, v
+
+
+def test_dkdv_epilogue_after_next_p_is_caught():
+    """A planted mistake: a warp reading an item's dK/dV only after writing the next item's
+    first P^T lets that item's first dV product overwrite the accumulator before the read."""
+    from protocol_model import find_violation_dkdv
+    v = find_violation_dkdv(runs=200, items=True, late_epilogue=True)
+    assert v is not None and "epilogue of item" in v, v
